@@ -1,0 +1,152 @@
+/*
+ * drs.h -- C ABI of libdrs, the GB300 (sm_103a) implementation of the
+ * DiffusionGemma per-row sampler statistics.
+ *
+ * The operations follow the page "vllm.model_executor.models.
+ * diffusion_gemma_sampler": the module docstring (argmax, Gumbel-max sample,
+ * softmax entropy and the softmax in the model dtype, one read of each row),
+ * sample_row_stats and its PyTorch definition sample_row_stats_reference,
+ * and stash_converged_logprobs / _lp_topk_kernel (top-k logprobs of the rows
+ * of converged slots, keys ordered by value then by lower index).
+ *
+ * Conventions for every entry point:
+ *   - Array arguments are DEVICE pointers owned by the caller, unless stated
+ *     otherwise. The library allocates no device memory in any call.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream). Results are ready when the
+ *     stream is.
+ *   - Host-side argument checks return DRS_ERR_INVALID_ARG without
+ *     launching anything. Launch failures return DRS_ERR_CUDA. A device-side
+ *     wait that runs out of time makes the kernel skip its remaining writes
+ *     and raise a device flag, read with drs_get_device_error().
+ *   - The library cannot check the length of device arrays; the caller
+ *     guarantees the sizes stated below.
+ *   - Not thread-safe for concurrent calls that share one workspace.
+ */
+#ifndef DRS_H_
+#define DRS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum drs_status {
+    DRS_OK = 0,
+    DRS_ERR_INVALID_ARG = -1,
+    DRS_ERR_UNSUPPORTED = -2,
+    DRS_ERR_CUDA = -3,
+    DRS_ERR_DEVICE_TIMEOUT = -4
+} drs_status;
+
+typedef enum drs_probs_dtype {
+    DRS_PROBS_NONE = 0,
+    DRS_PROBS_BF16 = 1,
+    DRS_PROBS_FP16 = 2
+} drs_probs_dtype;
+
+/* Largest vocabulary (row length) the kernels accept. */
+#define DRS_MAX_VOCAB 1048576
+
+/*
+ * Bytes of device workspace drs_row_stats needs (at least 256-byte aligned,
+ * contents arbitrary, no initialisation needed). The workspace carries the
+ * per-row partial results that the CTAs sharing one row exchange. One
+ * workspace must not be used by two calls that can run at the same time.
+ */
+size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab);
+
+/*
+ * Per-row statistics of temperature-scaled logits (sample_row_stats and
+ * sample_row_stats_reference on the page above).
+ *
+ *   logits      fp32 [rows, vocab], row i at logits + i * row_stride, unit
+ *               column stride. row_stride >= vocab; the columns between
+ *               vocab and row_stride are never read.
+ *   temps       fp32 [ceil(rows / canvas_len)]; row i uses
+ *               T = temps[i / canvas_len]. The scaled logit is the IEEE fp32
+ *               quotient x / max(T, 1e-10f). T > 0 draws Gumbel noise; T <= 0
+ *               is greedy (sample = argmax). NaN temperatures, NaN or +inf
+ *               logits are not supported; -inf logits are.
+ *   seed        noise key. The noise of (row, col) is Philox4x32-10 with key
+ *               (lo32(seed), hi32(seed)) and counter (lo32(col/4),
+ *               hi32(col/4), lo32(row), hi32(row)), word col % 4, mapped to
+ *               u = max((word >> 8) * 2^-24, 1e-20f); g = -log(-log u). The
+ *               same function is exposed by drs_philox_gumbel.
+ *   argmax      int64 [rows]: lowest column of the largest scaled logit.
+ *   sample      int64 [rows]: lowest column of the largest scaled logit + g.
+ *   entropy     fp32 [rows]: entropy of softmax(scaled); -inf columns drop
+ *               out; a row that is -inf everywhere has entropy 0.
+ *   probs       probs_dtype NONE: must be NULL. BF16/FP16: 16-bit
+ *               [rows, vocab] with row stride probs_row_stride >= vocab
+ *               (elements), softmax(scaled) rounded to nearest even.
+ *   workspace   device scratch of drs_row_stats_workspace_bytes(rows, vocab)
+ *               bytes; may be NULL only when that function returns 0.
+ *
+ * rows == 0 returns DRS_OK without launching. vocab must be in
+ * [1, DRS_MAX_VOCAB]; canvas_len >= 1.
+ */
+drs_status drs_row_stats(const float *logits, int64_t rows, int64_t vocab,
+                         int64_t row_stride, const float *temps,
+                         int64_t canvas_len, uint64_t seed, int64_t *argmax,
+                         int64_t *sample, float *entropy,
+                         drs_probs_dtype probs_dtype, void *probs,
+                         int64_t probs_row_stride, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of device workspace drs_topk_logprobs needs (256-byte aligned,
+ * contents arbitrary). Same sharing rule as the row-stats workspace.
+ */
+size_t drs_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k);
+
+/*
+ * Top-k logprobs of the rows of converged slots (stash_converged_logprobs
+ * and _lp_topk_kernel on the page above).
+ *
+ *   logits, rows, vocab, row_stride, temps, canvas_len: as drs_row_stats;
+ *               rows must be a multiple of canvas_len.
+ *   keep        uint8 [rows / canvas_len]: slot n is converged when
+ *               keep[n] != 0. Rows of other slots are skipped and their
+ *               outputs are not written.
+ *   k           0 <= k <= min(vocab, 1024); k == 0 does nothing.
+ *   out_ids     int32 [rows, k]: for a kept row, the columns of the k
+ *               largest scaled logits, ordered by value and then by lower
+ *               column (-0.0 equals +0.0).
+ *   out_logprobs fp32 [rows, k]: scaled - max - log(sum exp(scaled - max))
+ *               of those columns (NaN for a row that is -inf everywhere).
+ */
+drs_status drs_topk_logprobs(const float *logits, int64_t rows, int64_t vocab,
+                             int64_t row_stride, const float *temps,
+                             int64_t canvas_len, const uint8_t *keep,
+                             int32_t k, int32_t *out_ids, float *out_logprobs,
+                             void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
+ * The sampler's noise, materialised (the generator of drs_row_stats).
+ * For r in [0, rows), c in [0, vocab): out_bits[r * vocab + c] is the
+ * Philox word of (row0 + r, c) and out_gumbel[r * vocab + c] the fp32
+ * -log(-log u) of it. Either output may be NULL; rows == 0 is a no-op.
+ */
+drs_status drs_philox_gumbel(uint64_t seed, int64_t row0, int64_t rows,
+                             int64_t vocab, uint32_t *out_bits,
+                             float *out_gumbel, void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *drs_status_string(drs_status s);
+
+/*
+ * Synchronise `stream`, then read and clear the device flag raised by a
+ * kernel whose bounded wait ran out of time on the current device.
+ * Returns DRS_OK, DRS_ERR_DEVICE_TIMEOUT or DRS_ERR_CUDA.
+ */
+drs_status drs_get_device_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DRS_H_ */

@@ -1,0 +1,328 @@
+/*
+ * drs_oracle.c -- TEST INFRASTRUCTURE, not part of the product path.
+ *
+ * A plain, slow, single-threaded CPU restatement of what the DiffusionGemma
+ * per-row sampler statistics compute, used only to check the CUDA library.
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load this code. It shares nothing with the CUDA sources: no header, no
+ * helper, no table.
+ *
+ * Sources (page "vllm.model_executor.models.diffusion_gemma_sampler"):
+ *   - module docstring: per canvas position, the argmax of the temperature-
+ *     scaled logits, a Gumbel-max sample, the softmax entropy and the softmax
+ *     in the model dtype;
+ *   - sample_row_stats docstring: row i uses temps[i // canvas_len]; a zero
+ *     temperature is greedy, and the entropy clamps T at 1e-10;
+ *   - sample_row_stats_reference: the PyTorch definition followed step by
+ *     step below (divide by clamp(T, 1e-10), uniform noise clamped at 1e-20,
+ *     noisy = scaled + (-log(-log u)) * (T > 0), log_softmax, exp,
+ *     entropy = -sum over p > 0 of p log p, argmax of scaled and of noisy);
+ *   - stash_converged_logprobs docstring and _lp_topk_kernel docstring: the
+ *     num_topk largest scaled logits of kept rows, ordered by value and then
+ *     by lower index, and their logprobs.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - the noise: the reference draws it with an unseeded rand_like; the
+ *     kernel takes a seed. Here u comes from Philox4x32-10 (Salmon, Moraes,
+ *     Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11) with
+ *     key (lo32(seed), hi32(seed)) and counter
+ *     (lo32(col/4), hi32(col/4), lo32(row), hi32(row)), word col%4, mapped to
+ *     u = (word >> 8) * 2^-24 and clamped below at 1e-20f;
+ *   - ties: lowest index for argmax, sample and top-k;
+ *   - -0.0 and +0.0 are the same value for the top-k order;
+ *   - the top-k logprob clamps T at 1e-10 like the row statistics;
+ *   - a row that is -inf everywhere: argmax = sample = 0, entropy = 0,
+ *     probs = NaN, top-k logprobs = NaN (what the PyTorch definition gives).
+ *
+ * Floating point: the scaled logit is one IEEE fp32 division; everything
+ * after it is in double. Build with -ffp-contract=off and without fast-math.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- Philox */
+
+/* Philox4x32 round constants from the SC'11 paper: the two multipliers and
+ * the two Weyl-sequence key increments. */
+#define ORACLE_PHILOX_M0 0xD2511F53u
+#define ORACLE_PHILOX_M1 0xCD9E8D57u
+#define ORACLE_PHILOX_W0 0x9E3779B9u
+#define ORACLE_PHILOX_W1 0xBB67AE85u
+
+/* Ten rounds of the Philox4x32 bijection. Each round multiplies words 0 and
+ * 2 by the two constants, takes the high halves xor the other two words xor
+ * the round key as the new words 0 and 2, and the low halves as the new
+ * words 1 and 3 (crossed). The key advances by the Weyl increments between
+ * rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2],
+                          uint32_t out[4]) {
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t prod_a = (uint64_t)ORACLE_PHILOX_M0 * (uint64_t)x0;
+        uint64_t prod_b = (uint64_t)ORACLE_PHILOX_M1 * (uint64_t)x2;
+        uint32_t hi_a = (uint32_t)(prod_a >> 32), lo_a = (uint32_t)prod_a;
+        uint32_t hi_b = (uint32_t)(prod_b >> 32), lo_b = (uint32_t)prod_b;
+        uint32_t y0 = hi_b ^ x1 ^ k0;
+        uint32_t y1 = lo_b;
+        uint32_t y2 = hi_a ^ x3 ^ k1;
+        uint32_t y3 = lo_a;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+        k0 += ORACLE_PHILOX_W0;
+        k1 += ORACLE_PHILOX_W1;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* The 32 random bits that drive the noise of (row, col). */
+uint32_t oracle_noise_bits(uint64_t seed, int64_t row, int64_t col) {
+    uint64_t group = (uint64_t)col >> 2;
+    uint32_t ctr[4] = {(uint32_t)group, (uint32_t)(group >> 32),
+                       (uint32_t)(uint64_t)row, (uint32_t)((uint64_t)row >> 32)};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    return out[(uint64_t)col & 3u];
+}
+
+/* u in [0, 1 - 2^-24] on a 2^-24 grid, then clamp(min=1e-20) in fp32. */
+float oracle_uniform(uint32_t bits) {
+    float u = (float)(bits >> 8) * 0x1p-24f; /* exact: 24-bit integer */
+    const float lo = 1e-20f;
+    return u < lo ? lo : u;
+}
+
+/* The Gumbel noise -log(-log u), in double. */
+double oracle_gumbel_of_bits(uint32_t bits) {
+    double u = (double)oracle_uniform(bits);
+    return -log(-log(u));
+}
+
+/* Fill bits[r, c] and gumbel[r, c] (either may be NULL) for rows
+ * row0 .. row0 + rows - 1 and columns 0 .. vocab - 1, row-major. */
+void oracle_philox_gumbel(uint64_t seed, int64_t row0, int64_t rows,
+                          int64_t vocab, uint32_t *bits, double *gumbel) {
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < vocab; ++c) {
+            uint32_t b = oracle_noise_bits(seed, row0 + r, c);
+            if (bits) bits[r * vocab + c] = b;
+            if (gumbel) gumbel[r * vocab + c] = oracle_gumbel_of_bits(b);
+        }
+    }
+}
+
+/* ------------------------------------------------- narrowing conversions */
+
+/* fp32 -> bfloat16 bits, round to nearest even (the top 16 bits of the
+ * fp32 encoding after adding half an ulp of bf16 plus the tie bit). */
+uint16_t oracle_f32_to_bf16_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u); /* quiet NaN */
+    uint32_t tie = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7FFFu + tie) >> 16);
+}
+
+/* fp32 -> IEEE binary16 bits, round to nearest even, through the compiler's
+ * _Float16 conversion. */
+uint16_t oracle_f32_to_f16_bits(float f) {
+    _Float16 h = (_Float16)f;
+    uint16_t b;
+    memcpy(&b, &h, 2);
+    return b;
+}
+
+/* ------------------------------------------------------------ row stats */
+
+enum { ORACLE_PROBS_NONE = 0, ORACLE_PROBS_BF16 = 1, ORACLE_PROBS_FP16 = 2 };
+
+/* The clamp(min=1e-10) of the temperature, in fp32 like the tensor it
+ * applies to. */
+static float oracle_clamped_temp(float t) {
+    const float lo = 1e-10f;
+    return t > lo ? t : lo;
+}
+
+/*
+ * Row statistics for rows [row_begin, row_end) of a [rows, row_stride]
+ * fp32 buffer whose first `vocab` columns are the logits.
+ *
+ * Outputs are indexed by the global row and only that range is written:
+ *   argmax[i], sample[i]  lowest index of the max of scaled / noisy;
+ *   entropy[i]            log S - W / S (S, W over the finite columns);
+ *   entropy_check[i]      -sum_{p>0} p log p, the PyTorch form (may be NULL);
+ *   probs                 16-bit codes, row i at probs + i * probs_row_stride
+ *                         (probs_dtype NONE: not touched, may be NULL);
+ *   sample_gap[i]         best minus second-best noisy score (double), or
+ *                         +inf when the sample is not drawn by noise
+ *                         (may be NULL).
+ * Returns 0, or -1 if scratch memory could not be allocated.
+ */
+int oracle_row_stats(const float *logits, int64_t rows, int64_t vocab,
+                     int64_t row_stride, const float *temps, int64_t canvas_len,
+                     uint64_t seed, int64_t row_begin, int64_t row_end,
+                     int64_t *argmax, int64_t *sample, double *entropy,
+                     double *entropy_check, int probs_dtype, uint16_t *probs,
+                     int64_t probs_row_stride, double *sample_gap) {
+    (void)rows;
+    float *scaled = (float *)malloc((size_t)vocab * sizeof(float));
+    if (!scaled) return -1;
+    for (int64_t i = row_begin; i < row_end; ++i) {
+        const float *x = logits + i * row_stride;
+        float temp = temps[i / canvas_len];
+        float te = oracle_clamped_temp(temp);
+
+        /* scaled = logits / clamp(temp, 1e-10): one fp32 division each. */
+        for (int64_t j = 0; j < vocab; ++j) scaled[j] = x[j] / te;
+
+        /* argmax of scaled: first index attaining the maximum. */
+        int64_t arg = 0;
+        float mx = scaled[0];
+        for (int64_t j = 1; j < vocab; ++j) {
+            if (scaled[j] > mx) { mx = scaled[j]; arg = j; }
+        }
+        argmax[i] = arg;
+
+        /* softmax statistics in double. */
+        double m = (double)mx;
+        double h = 0.0, h_check = 0.0;
+        double s_sum = 0.0;
+        if (m == -INFINITY) {
+            /* log_softmax is NaN everywhere; where(p > 0) drops all. */
+            h = 0.0;
+            h_check = 0.0;
+        } else {
+            double w_sum = 0.0;
+            for (int64_t j = 0; j < vocab; ++j) {
+                if (scaled[j] == -INFINITY) continue; /* 0 * -inf dropped */
+                double d = (double)scaled[j] - m;
+                double e = exp(d);
+                s_sum += e;
+                w_sum += e * d;
+            }
+            double log_s = log(s_sum);
+            h = log_s - w_sum / s_sum;
+            for (int64_t j = 0; j < vocab; ++j) {
+                double d = (double)scaled[j] - m;
+                double p = exp(d) / s_sum;
+                if (p > 0.0) h_check -= p * (d - log_s);
+            }
+        }
+        entropy[i] = h;
+        if (entropy_check) entropy_check[i] = h_check;
+
+        /* probs = exp(log_softmax) -> fp32 -> model dtype. */
+        if (probs_dtype != ORACLE_PROBS_NONE && probs) {
+            uint16_t *out = probs + i * probs_row_stride;
+            for (int64_t j = 0; j < vocab; ++j) {
+                float pf;
+                if (m == -INFINITY) {
+                    pf = NAN;
+                } else {
+                    double p = exp((double)scaled[j] - m) / s_sum;
+                    pf = (float)p;
+                }
+                out[j] = probs_dtype == ORACLE_PROBS_BF16
+                             ? oracle_f32_to_bf16_bits(pf)
+                             : oracle_f32_to_f16_bits(pf);
+            }
+        }
+
+        /* Gumbel-max sample: noise only where temp > 0. */
+        if (temp > 0.0f) {
+            double best = -INFINITY, second = -INFINITY;
+            int64_t best_j = 0;
+            int have = 0;
+            for (int64_t j = 0; j < vocab; ++j) {
+                double score = (double)scaled[j] +
+                               oracle_gumbel_of_bits(oracle_noise_bits(seed, i, j));
+                if (!have || score > best) {
+                    if (have) second = best > second ? best : second;
+                    best = score;
+                    best_j = j;
+                    have = 1;
+                } else if (score > second) {
+                    second = score;
+                }
+            }
+            sample[i] = best_j;
+            if (sample_gap)
+                sample_gap[i] = (best == -INFINITY) ? INFINITY : best - second;
+        } else {
+            sample[i] = arg;
+            if (sample_gap) sample_gap[i] = INFINITY;
+        }
+    }
+    free(scaled);
+    return 0;
+}
+
+/* --------------------------------------------------------------- top-k */
+
+typedef struct {
+    float value;
+    int64_t index;
+} oracle_ranked;
+
+/* Descending value, then ascending index: a total order, so the first k
+ * after sorting are unique. */
+static int oracle_rank_cmp(const void *pa, const void *pb) {
+    const oracle_ranked *a = (const oracle_ranked *)pa;
+    const oracle_ranked *b = (const oracle_ranked *)pb;
+    if (a->value > b->value) return -1;
+    if (a->value < b->value) return 1;
+    if (a->index < b->index) return -1;
+    if (a->index > b->index) return 1;
+    return 0;
+}
+
+/*
+ * Top-k logprobs of the rows of kept slots in [row_begin, row_end): row i is
+ * kept when keep[i / canvas_len] != 0. out_ids[i * k + r] and
+ * out_logprobs[i * k + r] receive the r-th largest scaled logit's column and
+ * its logprob scaled - max - log(sum exp(scaled - max)). Rows of slots that
+ * are not kept are not touched. Returns 0, or -1 on allocation failure.
+ */
+int oracle_topk_logprobs(const float *logits, int64_t rows, int64_t vocab,
+                         int64_t row_stride, const float *temps,
+                         int64_t canvas_len, const uint8_t *keep, int32_t k,
+                         int64_t row_begin, int64_t row_end, int32_t *out_ids,
+                         double *out_logprobs) {
+    (void)rows;
+    if (k <= 0) return 0;
+    oracle_ranked *items = (oracle_ranked *)malloc((size_t)vocab * sizeof(oracle_ranked));
+    if (!items) return -1;
+    for (int64_t i = row_begin; i < row_end; ++i) {
+        int64_t slot = i / canvas_len;
+        if (!keep[slot]) continue;
+        const float *x = logits + i * row_stride;
+        float te = oracle_clamped_temp(temps[slot]);
+        float mx = -INFINITY;
+        for (int64_t j = 0; j < vocab; ++j) {
+            float s = x[j] / te;
+            s = s + 0.0f; /* -0.0 and +0.0 are one value */
+            items[j].value = s;
+            items[j].index = j;
+            if (s > mx) mx = s;
+        }
+        double m = (double)mx;
+        double log_s = NAN;
+        if (m != -INFINITY) {
+            double s_sum = 0.0;
+            for (int64_t j = 0; j < vocab; ++j)
+                if (items[j].value != -INFINITY) s_sum += exp((double)items[j].value - m);
+            log_s = log(s_sum);
+        }
+        qsort(items, (size_t)vocab, sizeof(oracle_ranked), oracle_rank_cmp);
+        for (int32_t r = 0; r < k; ++r) {
+            out_ids[i * k + r] = (int32_t)items[r].index;
+            out_logprobs[i * k + r] =
+                (m == -INFINITY) ? NAN : (double)items[r].value - m - log_s;
+        }
+    }
+    free(items);
+    return 0;
+}
