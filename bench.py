@@ -1,0 +1,446 @@
+"""Benchmark of the DiffusionGemma row-statistics hot path on GB300.
+
+One step = one pass of the whole path over one batch: drs_row_stats (argmax,
+Gumbel-max sample, entropy, bf16 softmax) over 2048 x 262144 fp32 logits,
+then drs_topk_logprobs (k = 20) over the rows of the converged (even)
+slots. Inputs are synthetic (workloads.py, "step") and resident in HBM when
+the timed region starts; at 2.1 GB they are larger than L2, so no flush is
+needed between steps.
+
+Prints ONE JSON line (rank 0). `value` is rows/s over all GPUs; `roofline`
+describes the row-statistics kernel (algorithmic bytes rows*stride*4 read +
+rows*V*2 written per launch over its CUDA-event time); `e2e` repeats the step
+through the public API from pinned host buffers, copies included;
+`cpu_baseline` times the CPU oracle on a bounded sample of the same rows.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own batch (weak scaling, rows keyed by
+global row index so results equal one big batch); no collective touches
+the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "rows/s and achieved HBM GB/s (% of roofline) for row_stats at 2048x262144 fp32"
+WORKLOAD = "step"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxs.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def _clocks_rejected(c):
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if bad & set(c.get("reasons", [])):
+        return True
+    if c.get("sm_mhz") and c.get("sm_max_mhz") and c["sm_mhz"] < 0.6 * c["sm_max_mhz"]:
+        return True
+    return False
+
+
+# ---------------------------------------------------------------- our arm
+
+def _make_batch(rank: int):
+    w = workloads.make(WORKLOAD, device="cuda", data_seed=rank)
+    return w
+
+
+def _run_ours(args, world, rank, local):
+    import vocab_row_sampling_gb300 as drs
+    drs.load(build_if_missing=True)
+    torch.cuda.set_device(local)
+    w = _make_batch(rank)
+    rows, V, stride = w["rows"], w["vocab"], w["row_stride"]
+    logits = w["logits"][:, :V]
+    temps, keep = w["temps"].cuda(), w["keep"].cuda()
+    k = w["k"]
+    row0 = rank * rows
+    dev = logits.device
+    stream = torch.cuda.current_stream()
+    # temps of the whole (multi-rank) batch: this rank's slots sit at the
+    # offset of its first global row
+    slots = rows // w["canvas_len"]
+    temps_all = torch.zeros((rank + 1) * slots, dtype=torch.float32, device=dev)
+    temps_all[rank * slots:] = temps
+
+    argmax = torch.empty(rows, dtype=torch.int64, device=dev)
+    sample = torch.empty(rows, dtype=torch.int64, device=dev)
+    entropy = torch.empty(rows, dtype=torch.float32, device=dev)
+    probs = torch.empty(rows, V, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(rows, k, dtype=torch.int32, device=dev)
+    lps = torch.empty(rows, k, dtype=torch.float32, device=dev)
+    ws_rs = drs.workspace(drs.drs_row_stats_workspace_bytes(rows, V), dev)
+    ws_tk = drs.workspace(drs.drs_topk_workspace_bytes(rows, V, k), dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        drs.drs_row_stats(logits, temps_all, w["canvas_len"], 0, argmax, sample, entropy,
+                          drs.DRS_PROBS_BF16, probs, ws_rs, stream, row0=row0)
+        if ev is not None:
+            ev[1].record(stream)
+        drs.drs_topk_logprobs(logits, temps, w["canvas_len"], keep, k, ids, lps, ws_tk, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if drs.drs_get_device_error() != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    def timed():
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(world)
+        torch.cuda.synchronize()
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            start.record(stream)
+            for i in range(args.steps):
+                step(evs[i])
+            stop.record(stream)
+            torch.cuda.synchronize()
+        _barrier(world)
+        total_ms = start.elapsed_time(stop)
+        rs_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        tk_ms = [e[1].elapsed_time(e[2]) for e in evs]
+        return total_ms, rs_ms, tk_ms, clk.summary()
+
+    total_ms, rs_ms, tk_ms, clocks = timed()
+    if _clocks_rejected(clocks):
+        total_ms, rs_ms, tk_ms, clocks = timed()
+        clocks["remeasured"] = True
+    if drs.drs_get_device_error() != 0:
+        raise RuntimeError("device-side wait timed out during the timed region")
+    total_ms = _max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * rows * args.steps / (total_ms / 1e3)
+
+    rs_avg_ms = sum(rs_ms) / len(rs_ms)
+    tk_avg_ms = sum(tk_ms) / len(tk_ms)
+    bytes_rs = rows * stride * 4 + rows * V * 2
+    kept_rows = int(keep.sum().item()) * w["canvas_len"]
+    bytes_tk = kept_rows * V * 4
+    peak, peak_kind = _peak_hbm()
+    achieved = bytes_rs / (rs_avg_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(),
+                "kernel": "row_stats_kernel", "peak_kind": f"{peak_kind} copy bandwidth",
+                "bytes_per_launch": bytes_rs, "avg_launch_ms": round(rs_avg_ms, 4)}
+
+    out = {"metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic (seeded N(0,3^2) + one +8 spike per row, temps U[0.5,1.5])",
+           "config": {"workload": "step: 2048 x 262144 fp32 logits, bf16 probs, top-k 20 on "
+                                  "the even (converged) slots",
+                      "rows": rows, "vocab": V, "row_stride": stride, "k": k,
+                      "kept_rows": kept_rows,
+                      "l2": "inputs (2.1 GB) larger than L2 (126 MB); no flush"},
+           "roofline": roofline,
+           "kernels": {"row_stats": {"avg_ms": round(rs_avg_ms, 4),
+                                     "rows_per_s": round(rows / (rs_avg_ms / 1e3), 1),
+                                     "gbs": round(achieved, 1),
+                                     "frac_of_peak": round(achieved / peak, 4)},
+                       "topk_logprobs": {"avg_ms": round(tk_avg_ms, 4),
+                                         "gbs_read": round(bytes_tk / (tk_avg_ms / 1e3) / 1e9, 1),
+                                         "frac_of_peak": round(bytes_tk / (tk_avg_ms / 1e3) / 1e9
+                                                               / peak, 4)}},
+           "gpu_launches": 2 * args.steps,
+           "clocks": clocks}
+
+    # end to end through the public API from pinned host memory
+    out["e2e"] = _e2e(args, drs, w, rank, world, row0, temps_all, keep, k)
+    if rank == 0 and world == 1:
+        out["cpu_baseline"] = _cpu_baseline(logits, w, seconds=args.cpu_seconds)
+    del logits, probs
+    return out
+
+
+def _traffic_from_profile():
+    """DRAM bytes per launch of the row-stats kernel from the committed ncu
+    summary, if one matches the current kernel (else null)."""
+    path = os.path.join(ROOT, "profiles", "row_stats_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def _e2e(args, drs, w, rank, world, row0, temps_all, keep, k):
+    rows, V = w["rows"], w["vocab"]
+    host = torch.empty(rows, V, dtype=torch.float32, pin_memory=True)
+    host.copy_(w["logits"][:, :V].cpu())
+    dev = torch.device("cuda")
+    d_logits = torch.empty(rows, V, dtype=torch.float32, device=dev)
+    temps_h = temps_all.cpu().pin_memory()
+    keep_h = keep.cpu().pin_memory()
+    d_temps = torch.empty_like(temps_all)
+    d_keep = torch.empty_like(keep)
+    outs_h = {"argmax": torch.empty(rows, dtype=torch.int64, pin_memory=True),
+              "sample": torch.empty(rows, dtype=torch.int64, pin_memory=True),
+              "entropy": torch.empty(rows, dtype=torch.float32, pin_memory=True),
+              "ids": torch.empty(rows, k, dtype=torch.int32, pin_memory=True),
+              "lps": torch.empty(rows, k, dtype=torch.float32, pin_memory=True)}
+    argmax = torch.empty(rows, dtype=torch.int64, device=dev)
+    sample = torch.empty(rows, dtype=torch.int64, device=dev)
+    entropy = torch.empty(rows, dtype=torch.float32, device=dev)
+    probs = torch.empty(rows, V, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(rows, k, dtype=torch.int32, device=dev)
+    lps = torch.empty(rows, k, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    ws_rs = drs.workspace(drs.drs_row_stats_workspace_bytes(rows, V), dev)
+    ws_tk = drs.workspace(drs.drs_topk_workspace_bytes(rows, V, k), dev)
+    h2d = host.numel() * 4 + temps_h.numel() * 4 + keep_h.numel()
+    d2h = rows * (8 + 8 + 4) + rows * k * (4 + 4)
+
+    def step():
+        d_logits.copy_(host, non_blocking=True)
+        d_temps.copy_(temps_h, non_blocking=True)
+        d_keep.copy_(keep_h, non_blocking=True)
+        drs.drs_row_stats(d_logits, d_temps, w["canvas_len"], 0, argmax, sample, entropy,
+                          drs.DRS_PROBS_BF16, probs, ws_rs, stream, row0=row0)
+        drs.drs_topk_logprobs(d_logits, d_temps[rank * (rows // w["canvas_len"]):],
+                              w["canvas_len"], d_keep, k, ids, lps, ws_tk, stream)
+        outs_h["argmax"].copy_(argmax, non_blocking=True)
+        outs_h["sample"].copy_(sample, non_blocking=True)
+        outs_h["entropy"].copy_(entropy, non_blocking=True)
+        outs_h["ids"].copy_(ids, non_blocking=True)
+        outs_h["lps"].copy_(lps, non_blocking=True)
+
+    steps = max(2, min(args.steps, 10))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    ms = _max_over_ranks(start.elapsed_time(stop), world)
+    del host, d_logits, probs
+    return {"value": round(world * rows * steps / (ms / 1e3), 1), "unit": "rows/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms / steps, 3), "steps": steps}
+
+
+def _cpu_baseline(logits_dev, w, seconds=15.0, threads=None):
+    """The oracle, as it stands, on rows of the same batch until about
+    `seconds` of wall time; rows/s over the host threads it used."""
+    import oracle
+    threads = threads or (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                          else os.cpu_count())
+    oracle.build()
+    rows = w["rows"]
+    cl = w["canvas_len"]
+    temps = w["temps"].cpu().numpy()
+    keep = w["keep"].cpu().numpy()
+    done = 0
+    t0 = time.perf_counter()
+    batch = threads
+    while time.perf_counter() - t0 < seconds and done < rows:
+        sel = np.arange(done, min(rows, done + batch))
+        x = np.ascontiguousarray(logits_dev[torch.as_tensor(sel, device=logits_dev.device)]
+                                 .cpu().numpy())
+        tr = temps[sel // cl]
+        oracle.row_stats_rows(x, sel, tr, 0, oracle.PROBS_BF16, threads=threads)
+        kept = sel[keep[sel // cl] != 0]
+        if kept.size:
+            xk = np.ascontiguousarray(x[np.isin(sel, kept)])
+            oracle.topk_rows(xk, temps[kept // cl], w["k"], threads=threads)
+        done += sel.size
+    el = time.perf_counter() - t0
+    return {"value": round(done / el, 2), "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {done} rows of the step batch (row stats + top-k of kept rows), "
+                      f"{el:.1f} s wall"}
+
+
+# ---------------------------------------------------------- reference arm
+
+def _run_reference(args, world, rank):
+    """The CPU oracle timed on the host cores: each step a bounded sample of
+    the step workload (rows generated with the same recipe on the CPU)."""
+    import oracle
+    oracle.build()
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample_rows = max(threads, 2 * threads)
+    w = workloads.make(WORKLOAD, device="cpu", rows=sample_rows)
+    V = w["vocab"]
+    x = np.ascontiguousarray(w["logits"][:, :V].numpy())
+    temps = w["temps"].numpy()
+    keep = w["keep"].numpy()
+    cl = w["canvas_len"]
+    sel = np.arange(sample_rows)
+
+    def step():
+        oracle.row_stats_rows(x, sel, temps[sel // cl], 0, oracle.PROBS_BF16, threads=threads)
+        kept = sel[keep[sel // cl] != 0]
+        if kept.size:
+            oracle.topk_rows(np.ascontiguousarray(x[kept]), temps[kept // cl], w["k"],
+                             threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = sample_rows * args.steps / el
+    sample = (f"{sample_rows} rows of the step workload per step (row stats with bf16 probs "
+              f"+ top-k 20 of kept rows), CPU-generated with the same recipe")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "rows/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "step: 2048 x 262144 fp32 logits (bounded row sample on the "
+                                   "host), bf16 probs, top-k 20 on the converged slots",
+                       "rows_per_step": sample_rows, "vocab": V},
+            "cpu_baseline": {"value": round(value, 3), "unit": "rows/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank == 0:
+            print(json.dumps(_run_reference(args, world, rank)), flush=True)
+        return
+    world, rank, local = _dist()
+    out = _run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -48,7 +48,7 @@ typedef enum drs_probs_dtype {
 } drs_probs_dtype;
 
 /* Largest vocabulary (row length) the kernels accept. */
-#define DRS_MAX_VOCAB 1048576
+#define DRS_MAX_VOCAB 524288
 
 /*
  * Bytes of device workspace drs_row_stats needs (at least 256-byte aligned,
@@ -65,12 +65,18 @@ size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab);
  *   logits      fp32 [rows, vocab], row i at logits + i * row_stride, unit
  *               column stride. row_stride >= vocab; the columns between
  *               vocab and row_stride are never read.
- *   temps       fp32 [ceil(rows / canvas_len)]; row i uses
- *               T = temps[i / canvas_len]. The scaled logit is the IEEE fp32
+ *   row0        global index of the first row (>= 0). Row i of this call
+ *               is global row row0 + i: it keys the noise and picks the
+ *               temperature, so a batch split over several calls or GPUs
+ *               gives the results of one call. 0 for a whole batch.
+ *   temps       fp32 [ceil((row0 + rows) / canvas_len)], one per slot of the
+ *               whole batch; global row r uses T = temps[r / canvas_len].
+ *               The scaled logit is the IEEE fp32
  *               quotient x / max(T, 1e-10f). T > 0 draws Gumbel noise; T <= 0
  *               is greedy (sample = argmax). NaN temperatures, NaN or +inf
  *               logits are not supported; -inf logits are.
- *   seed        noise key. The noise of (row, col) is Philox4x32-10 with key
+ *   seed        noise key. The noise of (global row, col) is Philox4x32-10
+ *               with key
  *               (lo32(seed), hi32(seed)) and counter (lo32(col/4),
  *               hi32(col/4), lo32(row), hi32(row)), word col % 4, mapped to
  *               u = max((word >> 8) * 2^-24, 1e-20f); g = -log(-log u). The
@@ -90,7 +96,8 @@ size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab);
  */
 drs_status drs_row_stats(const float *logits, int64_t rows, int64_t vocab,
                          int64_t row_stride, const float *temps,
-                         int64_t canvas_len, uint64_t seed, int64_t *argmax,
+                         int64_t canvas_len, uint64_t seed, int64_t row0,
+                         int64_t *argmax,
                          int64_t *sample, float *entropy,
                          drs_probs_dtype probs_dtype, void *probs,
                          int64_t probs_row_stride, void *workspace,

@@ -73,11 +73,16 @@ def _load():
     lib.oracle_f32_to_f16_bits.restype = ctypes.c_uint16
     lib.oracle_row_stats.argtypes = [vp, c_i64, c_i64, c_i64, vp, c_i64, c_u64,
                                      c_i64, c_i64, vp, vp, vp, vp, ctypes.c_int,
-                                     vp, c_i64, vp]
+                                     vp, c_i64, vp, vp]
     lib.oracle_row_stats.restype = ctypes.c_int
     lib.oracle_topk_logprobs.argtypes = [vp, c_i64, c_i64, c_i64, vp, c_i64, vp,
                                          c_i32, c_i64, c_i64, vp, vp]
     lib.oracle_topk_logprobs.restype = ctypes.c_int
+    lib.oracle_row_stats_rows.argtypes = [vp, vp, vp, c_i64, c_i64, c_u64, vp, vp, vp, vp,
+                                          ctypes.c_int, vp, vp, vp]
+    lib.oracle_row_stats_rows.restype = ctypes.c_int
+    lib.oracle_topk_rows.argtypes = [vp, vp, c_i64, c_i64, c_i32, vp, vp]
+    lib.oracle_topk_rows.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -152,7 +157,8 @@ def row_stats(logits: np.ndarray, temps: np.ndarray, canvas_len: int, seed: int,
     the rows in ``rows_sel`` (default: all) are computed; the others hold
     -1 / NaN. Returns a dict with ``argmax`` and ``sample`` (int64 [rows]),
     ``entropy`` and ``entropy_check`` (float64 [rows]), ``sample_gap``
-    (float64 [rows]) and ``probs`` (uint16 codes [rows, vocab] or None).
+    and ``sample_best`` (float64 [rows]: best minus second-best noisy score,
+    and the best score) and ``probs`` (uint16 codes [rows, vocab] or None).
     """
     lib = _load()
     rows, vocab, stride = _logits_view(logits)
@@ -163,6 +169,7 @@ def row_stats(logits: np.ndarray, temps: np.ndarray, canvas_len: int, seed: int,
     entropy = np.full(rows, np.nan, dtype=np.float64)
     entropy_check = np.full(rows, np.nan, dtype=np.float64)
     gap = np.full(rows, np.nan, dtype=np.float64)
+    best = np.full(rows, np.nan, dtype=np.float64)
     probs = (np.zeros((rows, vocab), dtype=np.uint16)
              if probs_dtype != PROBS_NONE else None)
     rows_sel = list(range(rows)) if rows_sel is None else sorted(int(r) for r in rows_sel)
@@ -172,7 +179,8 @@ def row_stats(logits: np.ndarray, temps: np.ndarray, canvas_len: int, seed: int,
             rc = lib.oracle_row_stats(_ptr(logits), rows, vocab, stride, _ptr(temps),
                                       canvas_len, seed, r, r + 1, _ptr(argmax),
                                       _ptr(sample), _ptr(entropy), _ptr(entropy_check),
-                                      probs_dtype, _ptr(probs), vocab, _ptr(gap))
+                                      probs_dtype, _ptr(probs), vocab, _ptr(gap),
+                                      _ptr(best))
             if rc != 0:
                 raise MemoryError("oracle_row_stats")
 
@@ -184,7 +192,8 @@ def row_stats(logits: np.ndarray, temps: np.ndarray, canvas_len: int, seed: int,
         with ThreadPoolExecutor(len(parts)) as ex:
             list(ex.map(run, parts))
     return {"argmax": argmax, "sample": sample, "entropy": entropy,
-            "entropy_check": entropy_check, "sample_gap": gap, "probs": probs}
+            "entropy_check": entropy_check, "sample_gap": gap, "sample_best": best,
+            "probs": probs}
 
 
 def topk_logprobs(logits: np.ndarray, temps: np.ndarray, canvas_len: int,
@@ -211,6 +220,82 @@ def topk_logprobs(logits: np.ndarray, temps: np.ndarray, canvas_len: int,
     if len(parts) <= 1:
         for p in parts:
             run(p)
+    else:
+        with ThreadPoolExecutor(len(parts)) as ex:
+            list(ex.map(run, parts))
+    return ids, lps
+
+
+def _row_pointers(x: np.ndarray):
+    assert x.dtype == np.float32 and x.ndim == 2 and x.strides[1] == 4
+    base = x.ctypes.data
+    return np.array([base + t * x.strides[0] for t in range(x.shape[0])], dtype=np.uint64)
+
+
+def row_stats_rows(x: np.ndarray, row_ids, temps, seed: int,
+                   probs_dtype: int = PROBS_NONE, threads: int = 1):
+    """Oracle row statistics of rows given one by one.
+
+    ``x`` is [n, vocab] fp32: row t of it is global row ``row_ids[t]`` (the
+    index that keys the noise) with temperature ``temps[t]``. Returns the
+    same dict as ``row_stats``, indexed by t.
+    """
+    lib = _load()
+    n, vocab = x.shape
+    row_ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+    temps = np.ascontiguousarray(temps, dtype=np.float32)
+    assert row_ids.size == n and temps.size == n
+    out = {"argmax": np.full(n, -1, np.int64), "sample": np.full(n, -1, np.int64),
+           "entropy": np.full(n, np.nan), "entropy_check": np.full(n, np.nan),
+           "sample_gap": np.full(n, np.nan), "sample_best": np.full(n, np.nan),
+           "probs": (np.zeros((n, vocab), np.uint16) if probs_dtype != PROBS_NONE else None)}
+    ptrs = _row_pointers(x)
+
+    def run(part):
+        for t in part:
+            def at(a, w=1):
+                return None if a is None else ctypes.c_void_p(a.ctypes.data + t * a.strides[0])
+            rc = lib.oracle_row_stats_rows(at(ptrs), at(row_ids), at(temps), 1, vocab, seed,
+                                           at(out["argmax"]), at(out["sample"]),
+                                           at(out["entropy"]), at(out["entropy_check"]),
+                                           probs_dtype, at(out["probs"]), at(out["sample_gap"]),
+                                           at(out["sample_best"]))
+            if rc != 0:
+                raise MemoryError("oracle_row_stats_rows")
+
+    parts = _split(list(range(n)), threads)
+    if len(parts) <= 1:
+        for part in parts:
+            run(part)
+    else:
+        with ThreadPoolExecutor(len(parts)) as ex:
+            list(ex.map(run, parts))
+    return out
+
+
+def topk_rows(x: np.ndarray, temps, k: int, threads: int = 1):
+    """Oracle top-k of rows given one by one (all treated as kept):
+    (ids int32 [n, k], logprobs float64 [n, k])."""
+    lib = _load()
+    n, vocab = x.shape
+    temps = np.ascontiguousarray(temps, dtype=np.float32)
+    ids = np.full((n, k), -1, np.int32)
+    lps = np.full((n, k), np.nan)
+    ptrs = _row_pointers(x)
+
+    def run(part):
+        for t in part:
+            rc = lib.oracle_topk_rows(ctypes.c_void_p(ptrs.ctypes.data + 8 * t),
+                                      ctypes.c_void_p(temps.ctypes.data + 4 * t), 1, vocab, k,
+                                      ctypes.c_void_p(ids.ctypes.data + ids.strides[0] * t),
+                                      ctypes.c_void_p(lps.ctypes.data + lps.strides[0] * t))
+            if rc != 0:
+                raise MemoryError("oracle_topk_rows")
+
+    parts = _split(list(range(n)), threads)
+    if len(parts) <= 1:
+        for part in parts:
+            run(part)
     else:
         with ThreadPoolExecutor(len(parts)) as ex:
             list(ex.map(run, parts))

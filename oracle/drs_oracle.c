@@ -147,114 +147,143 @@ static float oracle_clamped_temp(float t) {
 }
 
 /*
- * Row statistics for rows [row_begin, row_end) of a [rows, row_stride]
- * fp32 buffer whose first `vocab` columns are the logits.
- *
- * Outputs are indexed by the global row and only that range is written:
- *   argmax[i], sample[i]  lowest index of the max of scaled / noisy;
- *   entropy[i]            log S - W / S (S, W over the finite columns);
- *   entropy_check[i]      -sum_{p>0} p log p, the PyTorch form (may be NULL);
- *   probs                 16-bit codes, row i at probs + i * probs_row_stride
- *                         (probs_dtype NONE: not touched, may be NULL);
- *   sample_gap[i]         best minus second-best noisy score (double), or
- *                         +inf when the sample is not drawn by noise
- *                         (may be NULL).
- * Returns 0, or -1 if scratch memory could not be allocated.
+ * Row statistics of one row: x[0 .. vocab-1] is row `row` (its global index,
+ * which keys the noise) and `temp` its slot's temperature. Outputs:
+ *   *argmax, *sample      lowest index of the max of scaled / noisy;
+ *   *entropy              log S - W / S (S, W over the finite columns);
+ *   *entropy_check        -sum_{p>0} p log p, the PyTorch form;
+ *   probs                 vocab 16-bit codes (probs_dtype NONE: not touched);
+ *   *sample_gap           best minus second-best noisy score, or +inf when
+ *                         the sample is not drawn by noise;
+ *   *sample_best          the best noisy score, or the max scaled logit
+ *                         when no noise is drawn.
+ * `scaled` is caller scratch of vocab floats.
+ */
+static void oracle_one_row(const float *x, int64_t vocab, int64_t row, float temp,
+                           uint64_t seed, float *scaled, int64_t *argmax,
+                           int64_t *sample, double *entropy, double *entropy_check,
+                           int probs_dtype, uint16_t *probs, double *sample_gap,
+                           double *sample_best) {
+    float te = oracle_clamped_temp(temp);
+
+    /* scaled = logits / clamp(temp, 1e-10): one fp32 division each. */
+    for (int64_t j = 0; j < vocab; ++j) scaled[j] = x[j] / te;
+
+    /* argmax of scaled: first index attaining the maximum. */
+    int64_t arg = 0;
+    float mx = scaled[0];
+    for (int64_t j = 1; j < vocab; ++j) {
+        if (scaled[j] > mx) { mx = scaled[j]; arg = j; }
+    }
+    *argmax = arg;
+
+    /* softmax statistics in double. */
+    double m = (double)mx;
+    double h = 0.0, h_check = 0.0;
+    double s_sum = 0.0;
+    if (m != -INFINITY) {
+        double w_sum = 0.0;
+        for (int64_t j = 0; j < vocab; ++j) {
+            if (scaled[j] == -INFINITY) continue; /* 0 * -inf dropped */
+            double d = (double)scaled[j] - m;
+            double e = exp(d);
+            s_sum += e;
+            w_sum += e * d;
+        }
+        double log_s = log(s_sum);
+        h = log_s - w_sum / s_sum;
+        for (int64_t j = 0; j < vocab; ++j) {
+            double d = (double)scaled[j] - m;
+            double p = exp(d) / s_sum;
+            if (p > 0.0) h_check -= p * (d - log_s);
+        }
+    } /* else: log_softmax is NaN everywhere; where(p > 0) drops it all. */
+    *entropy = h;
+    *entropy_check = h_check;
+
+    /* probs = exp(log_softmax) -> fp32 -> model dtype. */
+    if (probs_dtype != ORACLE_PROBS_NONE && probs) {
+        for (int64_t j = 0; j < vocab; ++j) {
+            float pf = (m == -INFINITY) ? NAN : (float)(exp((double)scaled[j] - m) / s_sum);
+            probs[j] = probs_dtype == ORACLE_PROBS_BF16 ? oracle_f32_to_bf16_bits(pf)
+                                                         : oracle_f32_to_f16_bits(pf);
+        }
+    }
+
+    /* Gumbel-max sample: noise only where temp > 0. */
+    if (temp > 0.0f) {
+        double best = -INFINITY, second = -INFINITY;
+        int64_t best_j = 0;
+        int have = 0;
+        for (int64_t j = 0; j < vocab; ++j) {
+            double score = (double)scaled[j] +
+                           oracle_gumbel_of_bits(oracle_noise_bits(seed, row, j));
+            if (!have || score > best) {
+                if (have) second = best > second ? best : second;
+                best = score;
+                best_j = j;
+                have = 1;
+            } else if (score > second) {
+                second = score;
+            }
+        }
+        *sample = best_j;
+        *sample_gap = (best == -INFINITY) ? INFINITY : best - second;
+        *sample_best = best;
+    } else {
+        *sample = arg;
+        *sample_gap = INFINITY;
+        *sample_best = m;
+    }
+}
+
+/*
+ * Row statistics for rows [row_begin, row_end) of a [rows, row_stride] fp32
+ * buffer whose first `vocab` columns are the logits; row i uses
+ * temps[i / canvas_len]. Outputs are indexed by the row (probs: row i at
+ * probs + i * probs_row_stride); only that range is written. NULL is
+ * allowed for entropy_check, sample_gap, sample_best and (with probs_dtype
+ * NONE) probs. Returns 0, or -1 if scratch memory could not be allocated.
  */
 int oracle_row_stats(const float *logits, int64_t rows, int64_t vocab,
                      int64_t row_stride, const float *temps, int64_t canvas_len,
                      uint64_t seed, int64_t row_begin, int64_t row_end,
                      int64_t *argmax, int64_t *sample, double *entropy,
                      double *entropy_check, int probs_dtype, uint16_t *probs,
-                     int64_t probs_row_stride, double *sample_gap) {
+                     int64_t probs_row_stride, double *sample_gap,
+                     double *sample_best) {
     (void)rows;
     float *scaled = (float *)malloc((size_t)vocab * sizeof(float));
     if (!scaled) return -1;
     for (int64_t i = row_begin; i < row_end; ++i) {
-        const float *x = logits + i * row_stride;
-        float temp = temps[i / canvas_len];
-        float te = oracle_clamped_temp(temp);
+        double hc, gap, best;
+        oracle_one_row(logits + i * row_stride, vocab, i, temps[i / canvas_len], seed, scaled,
+                       &argmax[i], &sample[i], &entropy[i], &hc, probs_dtype,
+                       probs ? probs + i * probs_row_stride : NULL, &gap, &best);
+        if (entropy_check) entropy_check[i] = hc;
+        if (sample_gap) sample_gap[i] = gap;
+        if (sample_best) sample_best[i] = best;
+    }
+    free(scaled);
+    return 0;
+}
 
-        /* scaled = logits / clamp(temp, 1e-10): one fp32 division each. */
-        for (int64_t j = 0; j < vocab; ++j) scaled[j] = x[j] / te;
-
-        /* argmax of scaled: first index attaining the maximum. */
-        int64_t arg = 0;
-        float mx = scaled[0];
-        for (int64_t j = 1; j < vocab; ++j) {
-            if (scaled[j] > mx) { mx = scaled[j]; arg = j; }
-        }
-        argmax[i] = arg;
-
-        /* softmax statistics in double. */
-        double m = (double)mx;
-        double h = 0.0, h_check = 0.0;
-        double s_sum = 0.0;
-        if (m == -INFINITY) {
-            /* log_softmax is NaN everywhere; where(p > 0) drops all. */
-            h = 0.0;
-            h_check = 0.0;
-        } else {
-            double w_sum = 0.0;
-            for (int64_t j = 0; j < vocab; ++j) {
-                if (scaled[j] == -INFINITY) continue; /* 0 * -inf dropped */
-                double d = (double)scaled[j] - m;
-                double e = exp(d);
-                s_sum += e;
-                w_sum += e * d;
-            }
-            double log_s = log(s_sum);
-            h = log_s - w_sum / s_sum;
-            for (int64_t j = 0; j < vocab; ++j) {
-                double d = (double)scaled[j] - m;
-                double p = exp(d) / s_sum;
-                if (p > 0.0) h_check -= p * (d - log_s);
-            }
-        }
-        entropy[i] = h;
-        if (entropy_check) entropy_check[i] = h_check;
-
-        /* probs = exp(log_softmax) -> fp32 -> model dtype. */
-        if (probs_dtype != ORACLE_PROBS_NONE && probs) {
-            uint16_t *out = probs + i * probs_row_stride;
-            for (int64_t j = 0; j < vocab; ++j) {
-                float pf;
-                if (m == -INFINITY) {
-                    pf = NAN;
-                } else {
-                    double p = exp((double)scaled[j] - m) / s_sum;
-                    pf = (float)p;
-                }
-                out[j] = probs_dtype == ORACLE_PROBS_BF16
-                             ? oracle_f32_to_bf16_bits(pf)
-                             : oracle_f32_to_f16_bits(pf);
-            }
-        }
-
-        /* Gumbel-max sample: noise only where temp > 0. */
-        if (temp > 0.0f) {
-            double best = -INFINITY, second = -INFINITY;
-            int64_t best_j = 0;
-            int have = 0;
-            for (int64_t j = 0; j < vocab; ++j) {
-                double score = (double)scaled[j] +
-                               oracle_gumbel_of_bits(oracle_noise_bits(seed, i, j));
-                if (!have || score > best) {
-                    if (have) second = best > second ? best : second;
-                    best = score;
-                    best_j = j;
-                    have = 1;
-                } else if (score > second) {
-                    second = score;
-                }
-            }
-            sample[i] = best_j;
-            if (sample_gap)
-                sample_gap[i] = (best == -INFINITY) ? INFINITY : best - second;
-        } else {
-            sample[i] = arg;
-            if (sample_gap) sample_gap[i] = INFINITY;
-        }
+/*
+ * The same statistics for n rows given one by one: rows[t] points at
+ * `vocab` logits of global row row_ids[t], whose temperature is temps[t].
+ * Output t of each array (probs: probs + t * vocab) receives row t.
+ */
+int oracle_row_stats_rows(const float *const *row_ptrs, const int64_t *row_ids,
+                          const float *temps, int64_t n, int64_t vocab, uint64_t seed,
+                          int64_t *argmax, int64_t *sample, double *entropy,
+                          double *entropy_check, int probs_dtype, uint16_t *probs,
+                          double *sample_gap, double *sample_best) {
+    float *scaled = (float *)malloc((size_t)vocab * sizeof(float));
+    if (!scaled) return -1;
+    for (int64_t t = 0; t < n; ++t) {
+        oracle_one_row(row_ptrs[t], vocab, row_ids[t], temps[t], seed, scaled, &argmax[t],
+                       &sample[t], &entropy[t], &entropy_check[t], probs_dtype,
+                       probs ? probs + t * vocab : NULL, &sample_gap[t], &sample_best[t]);
     }
     free(scaled);
     return 0;
@@ -279,12 +308,40 @@ static int oracle_rank_cmp(const void *pa, const void *pb) {
     return 0;
 }
 
+/* Top-k of one row x[0 .. vocab-1] scaled by clamp(temp, 1e-10): the k
+ * columns of largest scaled value (ties by lower column, -0.0 == +0.0) and
+ * their logprobs scaled - max - log(sum exp(scaled - max)). */
+static void oracle_topk_one(const float *x, int64_t vocab, float temp, int32_t k,
+                            oracle_ranked *items, int32_t *ids, double *lps) {
+    float te = oracle_clamped_temp(temp);
+    float mx = -INFINITY;
+    for (int64_t j = 0; j < vocab; ++j) {
+        float s = x[j] / te;
+        s = s + 0.0f; /* -0.0 and +0.0 are one value */
+        items[j].value = s;
+        items[j].index = j;
+        if (s > mx) mx = s;
+    }
+    double m = (double)mx;
+    double log_s = NAN;
+    if (m != -INFINITY) {
+        double s_sum = 0.0;
+        for (int64_t j = 0; j < vocab; ++j)
+            if (items[j].value != -INFINITY) s_sum += exp((double)items[j].value - m);
+        log_s = log(s_sum);
+    }
+    qsort(items, (size_t)vocab, sizeof(oracle_ranked), oracle_rank_cmp);
+    for (int32_t r = 0; r < k; ++r) {
+        ids[r] = (int32_t)items[r].index;
+        lps[r] = (m == -INFINITY) ? NAN : (double)items[r].value - m - log_s;
+    }
+}
+
 /*
  * Top-k logprobs of the rows of kept slots in [row_begin, row_end): row i is
- * kept when keep[i / canvas_len] != 0. out_ids[i * k + r] and
- * out_logprobs[i * k + r] receive the r-th largest scaled logit's column and
- * its logprob scaled - max - log(sum exp(scaled - max)). Rows of slots that
- * are not kept are not touched. Returns 0, or -1 on allocation failure.
+ * kept when keep[i / canvas_len] != 0 and then fills out_ids[i * k + r] and
+ * out_logprobs[i * k + r], r < k. Rows of slots that are not kept are not
+ * touched. Returns 0, or -1 on allocation failure.
  */
 int oracle_topk_logprobs(const float *logits, int64_t rows, int64_t vocab,
                          int64_t row_stride, const float *temps,
@@ -298,31 +355,23 @@ int oracle_topk_logprobs(const float *logits, int64_t rows, int64_t vocab,
     for (int64_t i = row_begin; i < row_end; ++i) {
         int64_t slot = i / canvas_len;
         if (!keep[slot]) continue;
-        const float *x = logits + i * row_stride;
-        float te = oracle_clamped_temp(temps[slot]);
-        float mx = -INFINITY;
-        for (int64_t j = 0; j < vocab; ++j) {
-            float s = x[j] / te;
-            s = s + 0.0f; /* -0.0 and +0.0 are one value */
-            items[j].value = s;
-            items[j].index = j;
-            if (s > mx) mx = s;
-        }
-        double m = (double)mx;
-        double log_s = NAN;
-        if (m != -INFINITY) {
-            double s_sum = 0.0;
-            for (int64_t j = 0; j < vocab; ++j)
-                if (items[j].value != -INFINITY) s_sum += exp((double)items[j].value - m);
-            log_s = log(s_sum);
-        }
-        qsort(items, (size_t)vocab, sizeof(oracle_ranked), oracle_rank_cmp);
-        for (int32_t r = 0; r < k; ++r) {
-            out_ids[i * k + r] = (int32_t)items[r].index;
-            out_logprobs[i * k + r] =
-                (m == -INFINITY) ? NAN : (double)items[r].value - m - log_s;
-        }
+        oracle_topk_one(logits + i * row_stride, vocab, temps[slot], k, items,
+                        out_ids + i * k, out_logprobs + i * k);
     }
+    free(items);
+    return 0;
+}
+
+/* Top-k of n rows given one by one (all kept): rows[t] has temperature
+ * temps[t]; out_ids / out_logprobs + t * k receive row t. */
+int oracle_topk_rows(const float *const *row_ptrs, const float *temps, int64_t n,
+                     int64_t vocab, int32_t k, int32_t *out_ids, double *out_logprobs) {
+    if (k <= 0) return 0;
+    oracle_ranked *items = (oracle_ranked *)malloc((size_t)vocab * sizeof(oracle_ranked));
+    if (!items) return -1;
+    for (int64_t t = 0; t < n; ++t)
+        oracle_topk_one(row_ptrs[t], vocab, temps[t], k, items, out_ids + t * k,
+                        out_logprobs + t * k);
     free(items);
     return 0;
 }

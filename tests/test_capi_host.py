@@ -1,0 +1,109 @@
+"""The C ABI library on the host (no GPU needed): it builds for sm_103a,
+loads, exports every entry point include/drs.h declares, and its host-side
+argument checks reject bad calls before touching the device. The calls here
+pass made-up device addresses that are never dereferenced: validation
+returns first.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import vocab_row_sampling_gb300 as drs
+from vocab_row_sampling_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x7F0000000000          # a 256-byte aligned address; never dereferenced
+INV, UNS, OK = drs.DRS_ERR_INVALID_ARG, drs.DRS_ERR_UNSUPPORTED, drs.DRS_OK
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return drs.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "drs.h")).read()
+    return sorted(set(re.findall(r"\b(drs_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    assert _declared() == sorted(drs.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "DRS_OK"), (-1, "DRS_ERR_INVALID_ARG"), (-2, "DRS_ERR_UNSUPPORTED"),
+                       (-3, "DRS_ERR_CUDA"), (-4, "DRS_ERR_DEVICE_TIMEOUT")]:
+        assert drs.status_string(code) == name
+
+
+def test_workspace_sizes(lib):
+    assert drs.drs_row_stats_workspace_bytes(2048, 262144) >= 152 * 4 * 32
+    assert drs.drs_topk_workspace_bytes(2048, 262144, 0) == 0
+    assert drs.drs_topk_workspace_bytes(2048, 262144, 64) >= 152 * 4 * (32 + 64 * 8)
+
+
+def _row_stats(lib, rows=4, vocab=16, stride=16, temps=FAKE, canvas=1, row0=0, logits=FAKE,
+               outs=FAKE, probs_dtype=1, probs=FAKE, pstride=16, ws=FAKE, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = drs.drs_row_stats_workspace_bytes(rows, vocab)
+    return lib.drs_row_stats(logits, rows, vocab, stride, temps, canvas, 0, row0, outs, outs,
+                             outs, probs_dtype, probs, pstride, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({"rows": -1}, INV), ({"vocab": 0}, INV), ({"stride": 8}, INV), ({"canvas": 0}, INV),
+    ({"row0": -1}, INV), ({"logits": None}, INV), ({"temps": None}, INV),
+    ({"outs": None}, INV), ({"probs_dtype": 0}, INV), ({"probs": None}, INV),
+    ({"probs_dtype": 3}, INV), ({"pstride": 15}, INV), ({"ws": None}, INV),
+    ({"ws_bytes": 64}, INV), ({"ws": FAKE + 16}, INV), ({"logits": FAKE + 2}, INV),
+    ({"vocab": drs.DRS_MAX_VOCAB + 1, "stride": drs.DRS_MAX_VOCAB + 1,
+      "pstride": drs.DRS_MAX_VOCAB + 1}, UNS),
+    ({"rows": 0}, OK),
+    ({"rows": 0, "probs_dtype": 0, "probs": None}, OK),
+])
+def test_row_stats_argument_checks(lib, kw, expect):
+    assert _row_stats(lib, **kw) == expect
+
+
+def _topk(lib, rows=8, vocab=16, stride=16, canvas=4, k=4, keep=FAKE, ids=FAKE, ws=FAKE,
+          ws_bytes=None, logits=FAKE):
+    if ws_bytes is None:
+        ws_bytes = drs.drs_topk_workspace_bytes(rows, vocab, k)
+    return lib.drs_topk_logprobs(logits, rows, vocab, stride, FAKE, canvas, keep, k, ids, ids,
+                                 ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({"k": -1}, INV), ({"k": 17}, INV), ({"vocab": 2048, "stride": 2048, "k": 1025}, INV),
+    ({"rows": 6}, INV), ({"canvas": 0}, INV), ({"keep": None}, INV), ({"ids": None}, INV),
+    ({"ws": None}, INV), ({"ws_bytes": 10}, INV), ({"stride": 15}, INV),
+    ({"vocab": drs.DRS_MAX_VOCAB + 1, "stride": drs.DRS_MAX_VOCAB + 1}, UNS),
+    ({"k": 0, "ws": None, "ws_bytes": 0}, OK), ({"rows": 0}, OK),
+])
+def test_topk_argument_checks(lib, kw, expect):
+    assert _topk(lib, **kw) == expect
+
+
+def test_philox_argument_checks(lib):
+    assert lib.drs_philox_gumbel(0, -1, 4, 4, FAKE, FAKE, None) == INV
+    assert lib.drs_philox_gumbel(0, 0, -1, 4, FAKE, FAKE, None) == INV
+    assert lib.drs_philox_gumbel(0, 0, 4, 0, FAKE, FAKE, None) == INV
+    assert lib.drs_philox_gumbel(0, 0, 0, 4, FAKE, FAKE, None) == OK
+    assert lib.drs_philox_gumbel(0, 0, 4, 4, None, None, None) == OK
+
+
+def test_binding_refuses_to_run_without_the_library(monkeypatch, tmp_path):
+    """No silent fallback: a missing libdrs.so raises."""
+    monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(drs, "_lib", None)
+    with pytest.raises(RuntimeError):
+        drs.load()

@@ -1,0 +1,214 @@
+"""GB300-native DiffusionGemma per-row sampler statistics.
+
+A thin ctypes binding of ``libdrs.so`` (declared in ``include/drs.h``). Every
+function here only marshals arguments: pointers of torch tensors, sizes, the
+current CUDA stream. All of the arithmetic runs in the library's CUDA kernels;
+there is no CPU fallback. Importing the package works without a GPU; calling
+into the library needs the built ``libdrs.so`` and a CUDA device, and raises
+otherwise.
+
+Entry points (same names as the C ABI):
+  drs_row_stats, drs_row_stats_workspace_bytes, drs_topk_logprobs,
+  drs_topk_workspace_bytes, drs_philox_gumbel, drs_status_string,
+  drs_get_device_error.
+Convenience wrappers that allocate outputs: row_stats, topk_logprobs,
+philox_gumbel.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+DRS_OK = 0
+DRS_ERR_INVALID_ARG = -1
+DRS_ERR_UNSUPPORTED = -2
+DRS_ERR_CUDA = -3
+DRS_ERR_DEVICE_TIMEOUT = -4
+
+DRS_PROBS_NONE, DRS_PROBS_BF16, DRS_PROBS_FP16 = 0, 1, 2
+DRS_MAX_VOCAB = 524288
+
+EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_topk_logprobs",
+            "drs_topk_workspace_bytes", "drs_philox_gumbel", "drs_status_string",
+            "drs_get_device_error")
+
+
+class DrsError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libdrs.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"libdrs.so is not built ({path}); run "
+                               "vocab_row_sampling_gb300._build.build()")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    i64, u64, i32, vp, sz = (ctypes.c_int64, ctypes.c_uint64, ctypes.c_int32,
+                             ctypes.c_void_p, ctypes.c_size_t)
+    lib.drs_row_stats_workspace_bytes.argtypes = [i64, i64]
+    lib.drs_row_stats_workspace_bytes.restype = sz
+    lib.drs_row_stats.argtypes = [vp, i64, i64, i64, vp, i64, u64, i64, vp, vp, vp,
+                                  ctypes.c_int, vp, i64, vp, sz, vp]
+    lib.drs_row_stats.restype = ctypes.c_int
+    lib.drs_topk_workspace_bytes.argtypes = [i64, i64, i32]
+    lib.drs_topk_workspace_bytes.restype = sz
+    lib.drs_topk_logprobs.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp, vp, sz, vp]
+    lib.drs_topk_logprobs.restype = ctypes.c_int
+    lib.drs_philox_gumbel.argtypes = [u64, i64, i64, i64, vp, vp, vp]
+    lib.drs_philox_gumbel.restype = ctypes.c_int
+    lib.drs_status_string.argtypes = [ctypes.c_int]
+    lib.drs_status_string.restype = ctypes.c_char_p
+    lib.drs_get_device_error.argtypes = [vp]
+    lib.drs_get_device_error.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().drs_status_string(status).decode()
+
+
+drs_status_string = status_string
+
+
+def _check(status: int, what: str):
+    if status != DRS_OK:
+        raise DrsError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _row_stride(logits) -> int:
+    assert logits.dim() == 2 and logits.stride(1) == 1, "logits: 2-D, unit column stride"
+    return logits.stride(0) if logits.shape[0] > 1 else max(logits.shape[1], logits.stride(0))
+
+
+# ------------------------------------------------------------- raw entry points
+
+def drs_row_stats_workspace_bytes(rows: int, vocab: int) -> int:
+    return int(load().drs_row_stats_workspace_bytes(rows, vocab))
+
+
+def drs_row_stats(logits, temps, canvas_len, seed, argmax, sample, entropy,
+                  probs_dtype=DRS_PROBS_NONE, probs=None, workspace=None, stream=None,
+                  row0=0):
+    """Launch drs_row_stats on torch CUDA tensors (outputs preallocated)."""
+    rows, vocab = logits.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    pstride = 0 if probs is None else probs.stride(0)
+    st = load().drs_row_stats(_ptr(logits), rows, vocab, _row_stride(logits), _ptr(temps),
+                              canvas_len, seed & (2**64 - 1), row0, _ptr(argmax), _ptr(sample),
+                              _ptr(entropy), probs_dtype, _ptr(probs), pstride,
+                              _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "drs_row_stats")
+
+
+def drs_topk_workspace_bytes(rows: int, vocab: int, k: int) -> int:
+    return int(load().drs_topk_workspace_bytes(rows, vocab, k))
+
+
+def drs_topk_logprobs(logits, temps, canvas_len, keep, k, out_ids, out_logprobs,
+                      workspace=None, stream=None):
+    rows, vocab = logits.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().drs_topk_logprobs(_ptr(logits), rows, vocab, _row_stride(logits), _ptr(temps),
+                                  canvas_len, _ptr(keep), k, _ptr(out_ids), _ptr(out_logprobs),
+                                  _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "drs_topk_logprobs")
+
+
+def drs_philox_gumbel(seed, row0, rows, vocab, out_bits=None, out_gumbel=None, stream=None):
+    st = load().drs_philox_gumbel(seed & (2**64 - 1), row0, rows, vocab, _ptr(out_bits),
+                                  _ptr(out_gumbel), _stream(stream))
+    _check(st, "drs_philox_gumbel")
+
+
+def drs_get_device_error(stream=None) -> int:
+    return int(load().drs_get_device_error(_stream(stream)))
+
+
+# ------------------------------------------------------------- conveniences
+
+_workspaces = {}
+
+
+def workspace(nbytes: int, device):
+    """A cached device workspace of at least nbytes (256-byte aligned)."""
+    import torch
+    key = (str(device), nbytes)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def row_stats(logits, temps, canvas_len: int, seed: int, probs_dtype=None, stream=None,
+              row0: int = 0):
+    """Allocate outputs and run drs_row_stats; returns (argmax, sample,
+    entropy, probs) like the page's sample_row_stats."""
+    import torch
+    rows, vocab = logits.shape
+    dev = logits.device
+    argmax = torch.empty(rows, dtype=torch.int64, device=dev)
+    sample = torch.empty(rows, dtype=torch.int64, device=dev)
+    entropy = torch.empty(rows, dtype=torch.float32, device=dev)
+    code = {None: DRS_PROBS_NONE, torch.bfloat16: DRS_PROBS_BF16,
+            torch.float16: DRS_PROBS_FP16}[probs_dtype]
+    probs = None if probs_dtype is None else torch.empty(rows, vocab, dtype=probs_dtype, device=dev)
+    if rows == 0:
+        return argmax, sample, entropy, probs
+    ws = workspace(drs_row_stats_workspace_bytes(rows, vocab), dev)
+    drs_row_stats(logits, temps, canvas_len, seed, argmax, sample, entropy, code, probs, ws,
+                  stream, row0)
+    return argmax, sample, entropy, probs
+
+
+def topk_logprobs(logits, temps, canvas_len: int, keep, k: int, out_ids=None,
+                  out_logprobs=None, stream=None):
+    """Top-k ids and logprobs of the rows of kept slots (other rows of the
+    given outputs are left as they are)."""
+    import torch
+    rows, vocab = logits.shape
+    dev = logits.device
+    if out_ids is None:
+        out_ids = torch.full((rows, k), -1, dtype=torch.int32, device=dev)
+    if out_logprobs is None:
+        out_logprobs = torch.full((rows, k), float("nan"), dtype=torch.float32, device=dev)
+    ws = workspace(drs_topk_workspace_bytes(rows, vocab, k), dev)
+    drs_topk_logprobs(logits, temps, canvas_len, keep, k, out_ids, out_logprobs, ws, stream)
+    return out_ids, out_logprobs
+
+
+def philox_gumbel(seed: int, row0: int, rows: int, vocab: int, device="cuda", stream=None):
+    import torch
+    bits = torch.empty(rows, vocab, dtype=torch.int32, device=device)
+    g = torch.empty(rows, vocab, dtype=torch.float32, device=device)
+    drs_philox_gumbel(seed, row0, rows, vocab, bits, g, stream)
+    return bits, g

@@ -1,0 +1,84 @@
+// capi.cu -- status strings, the device error flag and launch bookkeeping of
+// libdrs.
+#include <atomic>
+#include <mutex>
+
+#include "drs_internal.h"
+
+namespace drs {
+
+__device__ int g_device_error = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+int* g_flag_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::atomic<uint32_t> g_generation{0x5eed0000u};
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+}  // namespace
+
+int* device_error_flag() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_flag_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        g_flag_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_flag_ptr[dev];
+}
+
+uint32_t next_generation() {
+    uint32_t g = g_generation.fetch_add(1, std::memory_order_relaxed) + 1;
+    return g == 0 ? next_generation() : g;
+}
+
+int sm_count() {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+}  // namespace drs
+
+extern "C" const char* drs_status_string(drs_status s) {
+    switch (s) {
+        case DRS_OK: return "DRS_OK";
+        case DRS_ERR_INVALID_ARG: return "DRS_ERR_INVALID_ARG";
+        case DRS_ERR_UNSUPPORTED: return "DRS_ERR_UNSUPPORTED";
+        case DRS_ERR_CUDA: return "DRS_ERR_CUDA";
+        case DRS_ERR_DEVICE_TIMEOUT: return "DRS_ERR_DEVICE_TIMEOUT";
+    }
+    return "DRS_ERR_UNKNOWN";
+}
+
+extern "C" drs_status drs_get_device_error(void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return DRS_ERR_CUDA;
+    int* flag = drs::device_error_flag();
+    if (!flag) return DRS_ERR_CUDA;
+    int value = 0;
+    if (cudaMemcpy(&value, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DRS_ERR_CUDA;
+    if (value != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(flag, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return DRS_ERR_CUDA;
+        return DRS_ERR_DEVICE_TIMEOUT;
+    }
+    return DRS_OK;
+}

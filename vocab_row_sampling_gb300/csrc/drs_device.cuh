@@ -1,0 +1,308 @@
+// drs_device.cuh -- device building blocks shared by the libdrs kernels:
+// the Philox4x32-10 noise generator, bounded mbarrier waits, the bulk-copy
+// (TMA) loads that stage a row chunk in shared memory, warp/CTA reductions
+// and the record through which the CTAs that share one row exchange their
+// partial results.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace drs {
+
+constexpr int kThreads = 512;               // threads per CTA (16 warps)
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxVec4 = 8;                 // float4 slots per thread
+constexpr int kChunkCap = kThreads * kMaxVec4 * 4;  // floats per CTA chunk
+constexpr int kMaxTeam = 32;                // CTAs that share one row (one per lane of the merging warp)
+constexpr int kRing = 4;                    // exchange slots per CTA
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kTempFloor = 1e-10f;        // clamp(min=1e-10) of the temperature
+
+// Bounded waits: a wait that has not completed after this many nanoseconds
+// gives up, raises the device error flag and makes its kernel skip the rest
+// of its work.
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------- Philox
+
+// Philox4x32-10, the counter-based generator of Salmon, Moraes, Dror and
+// Shaw (SC'11): ten rounds of two 32x32->64 multiplications whose high
+// halves are mixed with the other two words and the round key, the key
+// advancing by a Weyl sequence between rounds.
+struct PhiloxKey {
+    uint32_t k0, k1;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
+    constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+    constexpr uint32_t kWeylA = 0x9E3779B9u, kWeylB = 0xBB67AE85u;
+    uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi_a = __umulhi(kMulA, c.x);
+        const uint32_t lo_a = kMulA * c.x;
+        const uint32_t hi_b = __umulhi(kMulB, c.z);
+        const uint32_t lo_b = kMulB * c.z;
+        c = make_uint4(hi_b ^ c.y ^ k0, lo_b, hi_a ^ c.w ^ k1, lo_a);
+        k0 += kWeylA;
+        k1 += kWeylB;
+    }
+    return c;
+}
+
+// The four noise words of columns 4*group .. 4*group+3 of `row`.
+__device__ __forceinline__ uint4 noise_words(PhiloxKey key, uint64_t row,
+                                             uint64_t group) {
+    return philox4x32_10(make_uint4(static_cast<uint32_t>(group),
+                                    static_cast<uint32_t>(group >> 32),
+                                    static_cast<uint32_t>(row),
+                                    static_cast<uint32_t>(row >> 32)),
+                         key);
+}
+
+__device__ __forceinline__ uint32_t word_of(uint4 w, int q) {
+    return q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w;
+}
+
+// Exponential variate E = -log(u), u = max((bits >> 8) * 2^-24, 1e-20f).
+// For u >= 1/2 the logarithm is taken as log1p(-(1 - u)) with 1 - u exact,
+// so E keeps its relative accuracy when u is close to 1.
+__device__ __forceinline__ float exponential_of_bits(uint32_t bits) {
+    const uint32_t n = bits >> 8;
+    if (n < (1u << 23)) {
+        const float u = fmaxf(static_cast<float>(n) * 0x1p-24f, 1e-20f);
+        return -logf(u);
+    }
+    const float one_minus_u = static_cast<float>((1u << 24) - n) * 0x1p-24f;
+    return -log1pf(-one_minus_u);
+}
+
+// The Gumbel noise -log(-log u) of one noise word, fp32.
+__device__ __forceinline__ float gumbel_of_bits(uint32_t bits) {
+    return -logf(exponential_of_bits(bits));
+}
+
+// A lower bound of E = -log(u): 1 - u <= -log(u). Exact in fp32.
+__device__ __forceinline__ float exponential_lower_bound(uint32_t bits) {
+    return static_cast<float>((1u << 24) - (bits >> 8)) * 0x1p-24f;
+}
+
+// Largest value gumbel_of_bits can return (u = 1 - 2^-24 gives 16.6355...),
+// rounded up with margin: no element whose scaled logit is below
+// best - kGumbelMax can win the Gumbel-max race against `best`.
+constexpr float kGumbelMax = 16.64f;
+
+// ------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with the given parity to complete; false if it has not
+// completed within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Bulk global -> shared copy (the non-tensor TMA path). dst and src must be
+// 16-byte aligned and bytes a multiple of 16. Completion is signalled on
+// `bar` as transaction bytes. evict_first: the logits are read once.
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes,
+                                            uint64_t* bar) {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// --------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Best (score, column): larger score wins, equal scores go to the lower
+// column. Columns of "no candidate" are INT32_MAX with score -inf.
+__device__ __forceinline__ bool beats(float s, int c, float bs, int bc) {
+    return s > bs || (s == bs && c < bc);
+}
+
+__device__ __forceinline__ void warp_best(float& s, int& c) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, s, o);
+        const int oc = __shfl_xor_sync(0xffffffffu, c, o);
+        if (beats(os, oc, s, c)) {
+            s = os;
+            c = oc;
+        }
+    }
+}
+
+// ------------------------------------------------------ row exchange
+
+// The partial result one CTA publishes for one row, with a tag written last
+// (release) so that a reader that sees the tag (acquire) sees the fields.
+struct alignas(32) Partial {
+    float m;         // max scaled logit of the CTA's columns (-inf if none)
+    float s;         // sum exp(x - m)
+    float w;         // sum exp(x - m) * (x - m)
+    int32_t arg;     // lowest column attaining m
+    float best;      // best Gumbel-perturbed score (-inf if none)
+    int32_t best_col;
+    uint64_t tag;    // (launch generation << 32) | (row sequence + 1)
+};
+static_assert(sizeof(Partial) == 32, "Partial layout");
+
+__device__ __forceinline__ void publish_partial(Partial* rec, float m, float s, float w,
+                                                int arg, float best, int best_col,
+                                                uint64_t tag) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(rec), "f"(m), "f"(s),
+                 "f"(w), "r"(arg)
+                 : "memory");
+    asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(&rec->best), "f"(best),
+                 "r"(best_col)
+                 : "memory");
+    asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(&rec->tag), "l"(tag)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t load_tag_acquire(const Partial* rec) {
+    uint64_t t;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(t) : "l"(&rec->tag) : "memory");
+    return t;
+}
+
+// Wait until rec->tag == tag, then read the fields (bypassing L1).
+// Returns false after kWaitLimitNs.
+__device__ __forceinline__ bool read_partial_bounded(const Partial* rec, uint64_t tag,
+                                                     Partial& out) {
+    if (load_tag_acquire(rec) != tag) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t it = 0;; ++it) {
+            __nanosleep(64);
+            if (load_tag_acquire(rec) == tag) break;
+            if ((it & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(rec));
+    const float2 b = __ldcg(reinterpret_cast<const float2*>(&rec->best));
+    out.m = a.x;
+    out.s = a.y;
+    out.w = a.z;
+    out.arg = __float_as_int(a.w);
+    out.best = b.x;
+    out.best_col = __float_as_int(b.y);
+    out.tag = tag;
+    return true;
+}
+
+__device__ __forceinline__ void raise_device_error(int* flag, int code) {
+    if (flag) atomicExch(flag, code);
+}
+
+// ------------------------------------------------------ work planning
+
+// How rows are split over CTAs: `team` CTAs share a row, each owning
+// `chunk` columns (a multiple of 4); `num_teams` teams take rows round
+// robin; `vec4` float4 slots per thread cover a chunk.
+struct RowPlan {
+    int team;
+    int chunk;
+    int num_teams;
+    int vec4;
+};
+
+// Choose the team size G that minimises the per-CTA work
+// ceil(rows / teams) * chunk, with teams = min(rows, capacity / G); ties go
+// to the smaller G (fewer records to merge). G ranges over the sizes whose
+// chunk fits in registers (at most kChunkCap columns).
+inline RowPlan plan_rows(int64_t rows, int vocab, int capacity) {
+    RowPlan best{0, 0, 0, 0};
+    double best_cost = 0.0;
+    const int g_min = (vocab + kChunkCap - 1) / kChunkCap;
+    for (int g = g_min; g <= kMaxTeam && g <= capacity; ++g) {
+        int chunk = (vocab + g - 1) / g;
+        chunk = (chunk + 3) & ~3;
+        if ((vocab + chunk - 1) / chunk != g) continue;  // a member would be empty
+        int64_t teams = capacity / g;
+        if (teams > rows) teams = rows;
+        if (teams < 1) continue;
+        const double cost = static_cast<double>((rows + teams - 1) / teams) * chunk;
+        if (best.team == 0 || cost < best_cost) {
+            best = RowPlan{g, chunk, static_cast<int>(teams), 0};
+            best_cost = cost;
+        }
+    }
+    if (best.team) {
+        const int per_thread = (best.chunk / 4 + kThreads - 1) / kThreads;
+        best.vec4 = per_thread <= 4 ? 4 : 8;
+    }
+    return best;
+}
+
+}  // namespace drs

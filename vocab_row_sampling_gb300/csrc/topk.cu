@@ -1,0 +1,541 @@
+// topk.cu -- top-k logprobs of the rows of converged slots (page
+// "vllm.model_executor.models.diffusion_gemma_sampler": the
+// stash_converged_logprobs docstring and _lp_topk_kernel).
+//
+// A key orders by value, then by lower column: the high word is the fp32
+// bit pattern mapped to an order-preserving int32 (b ^ ((b >> 31) &
+// 0x7FFFFFFF)), the low word 0x7FFFFFFF - column. Keys are distinct, so the
+// top-k under them is unique. -0.0 is canonicalised to +0.0 first.
+//
+// Work layout as in row_stats.cu: a team of G CTAs owns the G column chunks
+// of each row; rows of slots whose keep flag is 0 are skipped by the whole
+// team (nothing is read or written for them). Per kept row, each CTA
+//   1. stages its chunk (bulk copy), scales it (IEEE division by
+//      max(T, 1e-10)) and computes its max m and S = sum e^(s - m);
+//   2. takes as threshold the k-th largest of its 512 per-thread maximum
+//      keys: those k maxima are k distinct elements at or above it, so every
+//      element of the CTA's top-k is too (the block-max argument of
+//      _lp_topk_kernel, with one block per thread);
+//   3. ranks the candidates at or above the threshold by counting and keeps
+//      the first k (if tied values make the candidates too many, an exact
+//      bitwise search for the k-th largest key replaces the threshold);
+//   4. publishes (m, S, its k keys) in the workspace; every CTA of the team
+//      then ranks its own keys against all G*k published keys and writes
+//      those of global rank r < k to position r, with logprob
+//      s - M - log(sum_c S_c e^(m_c - M)).
+#include <cfloat>
+#include <climits>
+
+#include "drs_device.cuh"
+#include "drs_internal.h"
+
+namespace drs {
+
+namespace {
+
+constexpr int kMaxStages = 3;
+constexpr int kMaxK = 2 * kThreads;  // two keys per thread in the merge
+constexpr int kCandCap = 2048;    // shared-memory candidate slots
+constexpr int kFastCands = 512;   // above this many, use the exact search
+
+struct TopkParams {
+    const float* logits;
+    int64_t row_stride;
+    int64_t rows;
+    const float* temps;
+    int64_t canvas_len;
+    const uint8_t* keep;
+    int32_t* out_ids;
+    float* out_lp;
+    unsigned char* xchg;
+    int* err;
+    uint32_t generation;
+    int32_t k;
+    int32_t vocab;
+    int32_t team;
+    int32_t chunk;
+    int32_t num_teams;
+    int32_t nstage;
+    int32_t stage_bytes;
+    int32_t rec_bytes;
+};
+
+// Record header; the k keys follow it.
+struct alignas(32) TopkHeader {
+    uint64_t tag;
+    float m;
+    float s;
+    int32_t count;
+    int32_t pad[3];
+};
+static_assert(sizeof(TopkHeader) == 32, "header layout");
+
+struct TopkScratch {
+    uint64_t full[kMaxStages];
+    float wmax[kWarps];
+    double ws[kWarps];
+    int wcnt[kWarps];
+    unsigned long long wcnt64[kWarps];
+    int ncand;
+    int status;
+    float row_max;
+    float row_logs;
+};
+
+__device__ __forceinline__ float comp(const float4& v, int q) {
+    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ void set_comp(float4& v, int q, float x) {
+    if (q == 0) v.x = x;
+    else if (q == 1) v.y = x;
+    else if (q == 2) v.z = x;
+    else v.w = x;
+}
+
+__device__ __forceinline__ int32_t key32_of(float s) {
+    const int32_t b = __float_as_int(s);
+    return b ^ ((b >> 31) & 0x7FFFFFFF);
+}
+
+__device__ __forceinline__ float value_of_key32(int32_t k) {
+    const int32_t b = k ^ ((k >> 31) & 0x7FFFFFFF);
+    return __int_as_float(b);
+}
+
+__device__ __forceinline__ int64_t make_key(float s, int col) {
+    return (static_cast<int64_t>(key32_of(s)) << 32) |
+           static_cast<int64_t>(0x7FFFFFFF - col);
+}
+
+constexpr int64_t kNoKey = INT64_MIN;
+
+__device__ __forceinline__ int block_sum_int(int v, int* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    int r = (threadIdx.x & 31) < kWarps ? red[threadIdx.x & 31] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    __syncthreads();
+    return r;
+}
+
+}  // namespace
+
+template <int VEC4>
+__global__ void __launch_bounds__(kThreads, 1)
+    topk_kernel(const __grid_constant__ TopkParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    TopkScratch& sc = *reinterpret_cast<TopkScratch*>(smem + p.nstage * p.stage_bytes);
+    int64_t* cand = reinterpret_cast<int64_t*>(
+        smem + p.nstage * p.stage_bytes + ((sizeof(TopkScratch) + 127) & ~size_t(127)));
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int team_id = blockIdx.x / p.team;
+    const int member = blockIdx.x - team_id * p.team;
+    const int col0 = member * p.chunk;
+    const int ncols = min(p.vocab - col0, p.chunk);
+    const int nfull4 = ncols >> 2;
+    const uint32_t copy_bytes = static_cast<uint32_t>(nfull4) * 16u;
+    const int64_t nrows = team_id < p.rows ? (p.rows - 1 - team_id) / p.num_teams + 1 : 0;
+    const int K = p.k;
+    const bool use_tma = p.nstage > 0;
+
+    auto row_of = [&](int64_t j) { return team_id + j * p.num_teams; };
+    auto kept = [&](int64_t j) { return p.keep[row_of(j) / p.canvas_len] != 0; };
+    auto next_kept = [&](int64_t j) {
+        while (j < nrows && !kept(j)) ++j;
+        return j;
+    };
+
+    if (use_tma && tid == 0) {
+        for (int s = 0; s < p.nstage; ++s) mbar_init(&sc.full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // Producer state (thread 0): next team row to stage and kept rows issued.
+    int64_t issue_j = 0, issued = 0;
+    auto issue_next = [&]() {
+        issue_j = next_kept(issue_j);
+        if (issue_j >= nrows) return false;
+        const int s = static_cast<int>(issued % p.nstage);
+        mbar_arrive_expect_tx(&sc.full[s], copy_bytes);
+        if (copy_bytes)
+            tma_load_1d(smem + s * p.stage_bytes, p.logits + row_of(issue_j) * p.row_stride + col0,
+                        copy_bytes, &sc.full[s]);
+        ++issue_j;
+        ++issued;
+        return true;
+    };
+    if (use_tma && tid == 0) {
+        for (int s = 0; s < p.nstage; ++s)
+            if (!issue_next()) break;
+    }
+
+    bool aborted = false;
+    int64_t consumed = 0;
+    int64_t j = next_kept(0);
+    for (int64_t kk = 0; j < nrows; ++kk, j = next_kept(j + 1)) {
+        const int64_t row = row_of(j);
+        const float* grow = p.logits + row * p.row_stride + col0;
+
+        // ---- load and scale ------------------------------------------------
+        bool timed_out = false;
+        const int s = use_tma ? static_cast<int>(kk % p.nstage) : 0;
+        if (use_tma)
+            timed_out = !mbar_wait_bounded(&sc.full[s], static_cast<uint32_t>((kk / p.nstage) & 1));
+        const float4* stage4 = reinterpret_cast<const float4*>(smem + s * p.stage_bytes);
+        float4 v[VEC4];
+#pragma unroll
+        for (int i = 0; i < VEC4; ++i) {
+            const int f = i * kThreads + tid;
+            float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (f < nfull4) {
+                if (use_tma) {
+                    if (!timed_out) x = stage4[f];
+                } else {
+                    x.x = grow[4 * f + 0];
+                    x.y = grow[4 * f + 1];
+                    x.z = grow[4 * f + 2];
+                    x.w = grow[4 * f + 3];
+                }
+            } else if (f == nfull4) {
+                for (int q = 0; q < (ncols & 3); ++q) set_comp(x, q, grow[4 * f + q]);
+            }
+            v[i] = x;
+        }
+        if (__syncthreads_or(timed_out)) {
+            aborted = true;
+            break;
+        }
+        consumed = kk + 1;
+        if (use_tma && tid == 0) {
+            fence_proxy_async_smem();
+            issue_next();
+        }
+        const float te = fmaxf(p.temps[row / p.canvas_len], kTempFloor);
+#pragma unroll
+        for (int i = 0; i < VEC4; ++i) {
+            // x / te, then -0.0 -> +0.0 (one value for the order)
+            v[i].x = __fdiv_rn(v[i].x, te) + 0.0f;
+            v[i].y = __fdiv_rn(v[i].y, te) + 0.0f;
+            v[i].z = __fdiv_rn(v[i].z, te) + 0.0f;
+            v[i].w = __fdiv_rn(v[i].w, te) + 0.0f;
+        }
+        auto valid = [&](int i, int q) { return 4 * (i * kThreads + tid) + q < ncols; };
+        auto col_of = [&](int i, int q) { return col0 + 4 * (i * kThreads + tid) + q; };
+
+        // ---- CTA max and sum -------------------------------------------------
+        float mt = -INFINITY;
+        uint32_t tmax = 0;  // thread max key32, sign-flipped to unsigned order
+        int nvalid = 0;
+#pragma unroll
+        for (int i = 0; i < VEC4; ++i)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (valid(i, q)) {
+                    const float x = comp(v[i], q);
+                    mt = fmaxf(mt, x);
+                    tmax = max(tmax, static_cast<uint32_t>(key32_of(x)) ^ 0x80000000u);
+                    ++nvalid;
+                }
+        {
+            const float wm = warp_max(mt);
+            if (lane == 0) sc.wmax[warp] = wm;
+        }
+        __syncthreads();
+        const float mc = warp_max(lane < kWarps ? sc.wmax[lane] : -INFINITY);
+        float st = 0.0f;
+        if (mc != -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st += __expf(comp(v[i], q) - mc);
+        }
+        {
+            const double ws = warp_sum_d(static_cast<double>(st));
+            if (lane == 0) sc.ws[warp] = ws;
+        }
+
+        // ---- threshold: k-th largest thread maximum --------------------------
+        // Bitwise search for the largest t with #{threads: tmax >= t} >= K.
+        // Threads without valid columns hold 0 and never count.
+        uint32_t t = 0;
+        for (int b = 31; b >= 0; --b) {
+            const uint32_t c = t | (1u << b);
+            if (__syncthreads_count(nvalid > 0 && tmax >= c) >= K) t = c;
+        }
+        // Candidates: valid elements whose key32 (unsigned order) >= t.
+        if (tid == 0) sc.ncand = 0;
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < VEC4; ++i)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (valid(i, q)) {
+                    const float x = comp(v[i], q);
+                    if ((static_cast<uint32_t>(key32_of(x)) ^ 0x80000000u) >= t) {
+                        const int pos = atomicAdd(&sc.ncand, 1);
+                        if (pos < kCandCap) cand[pos] = make_key(x, col_of(i, q));
+                    }
+                }
+        __syncthreads();
+        int ncand = sc.ncand;
+
+        if (ncand > kFastCands) {
+            // Exact k-th largest 64-bit key over the CTA's valid elements:
+            // bitwise search on the order-preserving unsigned form.
+            uint64_t kth = 0;
+            const int want = min(K, block_sum_int(nvalid, sc.wcnt));
+            for (int b = 63; b >= 0; --b) {
+                const uint64_t c = kth | (1ull << b);
+                int cnt = 0;
+#pragma unroll
+                for (int i = 0; i < VEC4; ++i)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (valid(i, q)) {
+                            const uint64_t u = static_cast<uint64_t>(make_key(comp(v[i], q), col_of(i, q))) ^
+                                               0x8000000000000000ull;
+                            cnt += u >= c;
+                        }
+                if (block_sum_int(cnt, sc.wcnt) >= want) kth = c;
+            }
+            if (tid == 0) sc.ncand = 0;
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (valid(i, q)) {
+                        const int64_t key = make_key(comp(v[i], q), col_of(i, q));
+                        if ((static_cast<uint64_t>(key) ^ 0x8000000000000000ull) >= kth) {
+                            const int pos = atomicAdd(&sc.ncand, 1);
+                            if (pos < kCandCap) cand[pos] = key;
+                        }
+                    }
+            __syncthreads();
+            ncand = sc.ncand;
+        }
+
+        // ---- local top-k by counting ranks ------------------------------------
+        const int slot = static_cast<int>(kk % kRing);
+        unsigned char* my_rec = p.xchg + (static_cast<size_t>(blockIdx.x) * kRing + slot) * p.rec_bytes;
+        int64_t* my_keys = reinterpret_cast<int64_t*>(my_rec + sizeof(TopkHeader));
+        const int nlocal = min(K, ncand);
+        for (int c = tid; c < ncand; c += kThreads) {
+            const int64_t key = cand[c];
+            int rank = 0;
+            for (int o = 0; o < ncand; ++o) rank += cand[o] > key;
+            if (rank < nlocal) my_keys[rank] = key;
+        }
+        for (int c = nlocal + tid; c < K; c += kThreads) my_keys[c] = kNoKey;
+        const double s_cta = warp_sum_d(lane < kWarps ? sc.ws[lane] : 0.0);
+        __syncthreads();
+        const uint64_t tag = (static_cast<uint64_t>(p.generation) << 32) |
+                             static_cast<uint32_t>(kk + 1);
+        if (tid == 0) {
+            TopkHeader* h = reinterpret_cast<TopkHeader*>(my_rec);
+            h->m = mc;
+            h->s = static_cast<float>(s_cta);
+            h->count = nlocal;
+            __threadfence();
+            asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(&h->tag), "l"(tag) : "memory");
+        }
+
+        // ---- merge across the team ---------------------------------------------
+        if (warp == 0) {
+            bool ok = true;
+            float m = -INFINITY, s_m = 0.0f;
+            if (lane < p.team) {
+                const unsigned char* rec =
+                    p.xchg + (static_cast<size_t>(team_id * p.team + lane) * kRing + slot) * p.rec_bytes;
+                const TopkHeader* h = reinterpret_cast<const TopkHeader*>(rec);
+                uint64_t got;
+                asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(got) : "l"(&h->tag) : "memory");
+                if (got != tag) {
+                    const uint64_t t0 = global_timer_ns();
+                    for (uint32_t it = 0;; ++it) {
+                        __nanosleep(64);
+                        asm volatile("ld.acquire.gpu.global.b64 %0, [%1];"
+                                     : "=l"(got)
+                                     : "l"(&h->tag)
+                                     : "memory");
+                        if (got == tag) break;
+                        if ((it & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (ok) {
+                    m = __ldcg(&h->m);
+                    s_m = __ldcg(&h->s);
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            const float big_m = warp_max(m);
+            double s_d = 0.0;
+            if (m != -INFINITY) s_d = exp(static_cast<double>(m) - big_m) * s_m;
+            const double s_tot = warp_sum_d(s_d);
+            if (lane == 0) {
+                sc.status = ok ? 0 : 1;
+                sc.row_max = big_m;
+                sc.row_logs = static_cast<float>(log(s_tot));
+            }
+        }
+        __syncthreads();
+        if (sc.status != 0) {
+            aborted = true;
+            break;
+        }
+        const float big_m = sc.row_max;
+        const float logs = sc.row_logs;
+
+        // Rank my keys (thread t holds my_keys[t] and my_keys[t + 512])
+        // against all G*K published keys, staged through shared memory in
+        // tiles; global rank r < K goes to output position r.
+        const int total = p.team * K;
+        int64_t mine[2] = {kNoKey, kNoKey};
+        int grank[2] = {0, 0};
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            if (tid + h * kThreads < K) mine[h] = __ldcg(&my_keys[tid + h * kThreads]);
+        for (int base = 0; base < total; base += kCandCap) {
+            const int n = min(kCandCap, total - base);
+            __syncthreads();
+            for (int e = tid; e < n; e += kThreads) {
+                const int g = (base + e) / K;
+                const int r = (base + e) - g * K;
+                const unsigned char* rec =
+                    p.xchg + (static_cast<size_t>(team_id * p.team + g) * kRing + slot) * p.rec_bytes;
+                cand[e] = __ldcg(reinterpret_cast<const int64_t*>(rec + sizeof(TopkHeader)) + r);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (mine[h] != kNoKey)
+                    for (int e = 0; e < n; ++e) grank[h] += cand[e] > mine[h];
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t key = mine[h];
+            if (key != kNoKey && grank[h] < K) {
+                const float sv = value_of_key32(static_cast<int32_t>(key >> 32));
+                const int col = 0x7FFFFFFF - static_cast<int32_t>(key & 0xFFFFFFFF);
+                const float lp = big_m == -INFINITY ? NAN : (sv - big_m) - logs;
+                p.out_ids[row * K + grank[h]] = col;
+                p.out_lp[row * K + grank[h]] = lp;
+            }
+        }
+        __syncthreads();
+    }
+
+    if (aborted && tid == 0) raise_device_error(p.err, 2);
+    if (use_tma && tid == 0) {
+        for (int64_t seq = consumed; seq < issued; ++seq) {
+            const int st = static_cast<int>(seq % p.nstage);
+            mbar_wait_bounded(&sc.full[st], static_cast<uint32_t>((seq / p.nstage) & 1));
+        }
+    }
+}
+
+namespace {
+
+size_t record_bytes(int k) {
+    return (sizeof(TopkHeader) + static_cast<size_t>(k) * 8 + 31) & ~static_cast<size_t>(31);
+}
+
+template <int VEC4>
+drs_status launch_topk(TopkParams& prm, int grid, size_t smem, cudaStream_t stream) {
+    auto kernel = topk_kernel<VEC4>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return DRS_ERR_CUDA;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+    if (e != cudaSuccess || per_sm < 1) return DRS_ERR_CUDA;
+    if (grid > per_sm * sm_count()) return DRS_ERR_UNSUPPORTED;
+    void* args[] = {&prm};
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<void*>(kernel), dim3(grid), dim3(kThreads),
+                                    args, smem, stream);
+    return cuda_status(e);
+}
+
+}  // namespace
+
+}  // namespace drs
+
+extern "C" size_t drs_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k) {
+    (void)rows;
+    (void)vocab;
+    if (k <= 0) return 0;
+    return static_cast<size_t>(1024) * drs::kRing * drs::record_bytes(k);
+}
+
+extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64_t vocab,
+                                        int64_t row_stride, const float* temps,
+                                        int64_t canvas_len, const uint8_t* keep, int32_t k,
+                                        int32_t* out_ids, float* out_logprobs, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    using namespace drs;
+    if (rows < 0 || canvas_len < 1 || k < 0) return DRS_ERR_INVALID_ARG;
+    if (vocab < 1 || row_stride < vocab) return DRS_ERR_INVALID_ARG;
+    if (vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
+    if (k > vocab || k > kMaxK) return DRS_ERR_INVALID_ARG;
+    if (rows % canvas_len != 0) return DRS_ERR_INVALID_ARG;
+    if (k == 0 || rows == 0) return DRS_OK;
+    if (!logits || !temps || !keep || !out_ids || !out_logprobs) return DRS_ERR_INVALID_ARG;
+    if (!aligned(logits, 4)) return DRS_ERR_INVALID_ARG;
+    const size_t need = drs_topk_workspace_bytes(rows, vocab, k);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
+        return DRS_ERR_INVALID_ARG;
+
+    const int sms = sm_count();
+    if (sms <= 0) return DRS_ERR_CUDA;
+    const int capacity = sms < 1024 ? sms : 1024;
+    const RowPlan plan = plan_rows(rows, static_cast<int>(vocab), capacity);
+    if (!plan.team) return DRS_ERR_UNSUPPORTED;
+
+    TopkParams prm{};
+    prm.logits = logits;
+    prm.row_stride = row_stride;
+    prm.rows = rows;
+    prm.temps = temps;
+    prm.canvas_len = canvas_len;
+    prm.keep = keep;
+    prm.out_ids = out_ids;
+    prm.out_lp = out_logprobs;
+    prm.xchg = static_cast<unsigned char*>(workspace);
+    prm.err = device_error_flag();
+    prm.generation = next_generation();
+    prm.k = k;
+    prm.vocab = static_cast<int32_t>(vocab);
+    prm.team = plan.team;
+    prm.chunk = plan.chunk;
+    prm.num_teams = plan.num_teams;
+    prm.rec_bytes = static_cast<int32_t>(record_bytes(k));
+    if (!prm.err) return DRS_ERR_CUDA;
+
+    const bool tma = aligned(logits, 16) && (row_stride % 4 == 0);
+    const size_t scratch = ((sizeof(TopkScratch) + 127) & ~static_cast<size_t>(127)) +
+                           static_cast<size_t>(kCandCap) * sizeof(int64_t);
+    const size_t smem_limit = 227 * 1024;
+    if (tma) {
+        prm.stage_bytes = (plan.chunk * 4 + 127) & ~127;
+        int ns = static_cast<int>((smem_limit - scratch) / prm.stage_bytes);
+        prm.nstage = ns > kMaxStages ? kMaxStages : ns;
+        if (prm.nstage < 2) prm.nstage = 0;
+    }
+    if (!prm.nstage) prm.stage_bytes = 0;
+    const size_t smem = static_cast<size_t>(prm.nstage) * prm.stage_bytes + scratch;
+    const int grid = plan.team * plan.num_teams;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return plan.vec4 == 4 ? launch_topk<4>(prm, grid, smem, st)
+                          : launch_topk<8>(prm, grid, smem, st);
+}
