@@ -142,6 +142,16 @@ drs_status drs_philox_gumbel(uint64_t seed, int64_t row0, int64_t rows,
                              int64_t vocab, uint32_t *out_bits,
                              float *out_gumbel, void *stream);
 
+/*
+ * The temperature-scaled logits of sample_row_stats_reference (page above):
+ * out[i] = logits[i] / max(temp, 1e-10f) for i < n, the IEEE fp32 quotient
+ * rounded to nearest even, computed by the same routine the row kernels use
+ * (+-inf map to themselves). logits and out: device fp32 [n], 4-byte
+ * aligned; they may be the same array. n == 0 is a no-op.
+ */
+drs_status drs_scaled_logits(const float *logits, int64_t n, float temp,
+                             float *out, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *drs_status_string(drs_status s);
 

@@ -107,3 +107,10 @@ def test_binding_refuses_to_run_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(drs, "_lib", None)
     with pytest.raises(RuntimeError):
         drs.load()
+
+
+def test_scaled_logits_argument_checks(lib):
+    assert lib.drs_scaled_logits(FAKE, -1, 1.0, FAKE, None) == INV
+    assert lib.drs_scaled_logits(None, 4, 1.0, FAKE, None) == INV
+    assert lib.drs_scaled_logits(FAKE, 4, 1.0, FAKE + 2, None) == INV
+    assert lib.drs_scaled_logits(FAKE, 0, 1.0, FAKE, None) == OK

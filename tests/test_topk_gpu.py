@@ -94,7 +94,7 @@ def _full(name, n_sample):
     V = w["vocab"]
     view = w["logits"][:, :V]
     sel = sample_rows(w["rows"], n_sample, seed=2)
-    _check(view, w["temps"].numpy(), w["canvas_len"], w["keep"].cpu().numpy(), w["k"],
+    _check(view, w["temps"].cpu().numpy(), w["canvas_len"], w["keep"].cpu().numpy(), w["k"],
            rows_sel=sel, where=name)
     del w, view
     torch.cuda.empty_cache()

@@ -9,8 +9,8 @@ otherwise.
 
 Entry points (same names as the C ABI):
   drs_row_stats, drs_row_stats_workspace_bytes, drs_topk_logprobs,
-  drs_topk_workspace_bytes, drs_philox_gumbel, drs_status_string,
-  drs_get_device_error.
+  drs_topk_workspace_bytes, drs_philox_gumbel, drs_scaled_logits,
+  drs_status_string, drs_get_device_error.
 Convenience wrappers that allocate outputs: row_stats, topk_logprobs,
 philox_gumbel.
 """
@@ -31,8 +31,8 @@ DRS_PROBS_NONE, DRS_PROBS_BF16, DRS_PROBS_FP16 = 0, 1, 2
 DRS_MAX_VOCAB = 524288
 
 EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_topk_logprobs",
-            "drs_topk_workspace_bytes", "drs_philox_gumbel", "drs_status_string",
-            "drs_get_device_error")
+            "drs_topk_workspace_bytes", "drs_philox_gumbel", "drs_scaled_logits",
+            "drs_status_string", "drs_get_device_error")
 
 
 class DrsError(RuntimeError):
@@ -73,6 +73,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_topk_logprobs.restype = ctypes.c_int
     lib.drs_philox_gumbel.argtypes = [u64, i64, i64, i64, vp, vp, vp]
     lib.drs_philox_gumbel.restype = ctypes.c_int
+    lib.drs_scaled_logits.argtypes = [vp, i64, ctypes.c_float, vp, vp]
+    lib.drs_scaled_logits.restype = ctypes.c_int
     lib.drs_status_string.argtypes = [ctypes.c_int]
     lib.drs_status_string.restype = ctypes.c_char_p
     lib.drs_get_device_error.argtypes = [vp]
@@ -147,6 +149,13 @@ def drs_philox_gumbel(seed, row0, rows, vocab, out_bits=None, out_gumbel=None, s
     st = load().drs_philox_gumbel(seed & (2**64 - 1), row0, rows, vocab, _ptr(out_bits),
                                   _ptr(out_gumbel), _stream(stream))
     _check(st, "drs_philox_gumbel")
+
+
+def drs_scaled_logits(logits, temp: float, out, stream=None):
+    """out = logits / max(temp, 1e-10) elementwise (contiguous fp32 tensors)."""
+    assert logits.is_contiguous() and out.is_contiguous() and out.numel() == logits.numel()
+    st = load().drs_scaled_logits(_ptr(logits), logits.numel(), temp, _ptr(out), _stream(stream))
+    _check(st, "drs_scaled_logits")
 
 
 def drs_get_device_error(stream=None) -> int:

@@ -12,10 +12,13 @@ namespace drs {
 
 constexpr int kThreads = 512;               // threads per CTA (16 warps)
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxVec4 = 8;                 // float4 slots per thread
-constexpr int kChunkCap = kThreads * kMaxVec4 * 4;  // floats per CTA chunk
+constexpr int kMaxVec4 = 8;                 // float4 slots per thread, at most
+constexpr int kChunkCap = kThreads * kMaxVec4 * 4;  // floats per CTA chunk, at most
+constexpr size_t kSmemPerSm = 233472;       // shared memory of one SM (228 KB)
+constexpr size_t kSmemPerCta = 232448;      // largest opt-in per CTA (227 KB)
+constexpr size_t kSmemReserved = 1024;      // the driver's share of each CTA
 constexpr int kMaxTeam = 32;                // CTAs that share one row (one per lane of the merging warp)
-constexpr int kRing = 4;                    // exchange slots per CTA
+constexpr int kRing = 8;                    // exchange slots per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTempFloor = 1e-10f;        // clamp(min=1e-10) of the temperature
@@ -94,9 +97,12 @@ __device__ __forceinline__ float gumbel_of_bits(uint32_t bits) {
     return -logf(exponential_of_bits(bits));
 }
 
-// A lower bound of E = -log(u): 1 - u <= -log(u). Exact in fp32.
-__device__ __forceinline__ float exponential_lower_bound(uint32_t bits) {
-    return static_cast<float>((1u << 24) - (bits >> 8)) * 0x1p-24f;
+// A lower bound of 1 - u, itself a lower bound of E = -log(u), from the
+// top 23 bits of the word without an int-to-float conversion: with
+// u' = 1 + (bits >> 9) * 2^-23 in [1, 2), u <= u' - 1 + 2^-24, so
+// 1 - u >= (2 - 2^-24) - u'.
+__device__ __forceinline__ float one_minus_u_lower(uint32_t bits) {
+    return 0x1.fffffep0f - __uint_as_float(0x3F800000u | (bits >> 9));
 }
 
 // Largest value gumbel_of_bits can return (u = 1 - 2^-24 gives 16.6355...),
@@ -269,22 +275,36 @@ __device__ __forceinline__ void raise_device_error(int* flag, int code) {
 
 // How rows are split over CTAs: `team` CTAs share a row, each owning
 // `chunk` columns (a multiple of 4); `num_teams` teams take rows round
-// robin; `vec4` float4 slots per thread cover a chunk.
+// robin; `vec4` float4 slots per thread cover a chunk; `ctas_per_sm` CTAs
+// are resident per SM.
 struct RowPlan {
     int team;
     int chunk;
     int num_teams;
     int vec4;
+    int ctas_per_sm;
 };
+
+inline size_t smem_per_cta(int ctas_per_sm) {
+    return ctas_per_sm >= 2 ? kSmemPerSm / ctas_per_sm - kSmemReserved : kSmemPerCta;
+}
 
 // Choose the team size G that minimises the per-CTA work
 // ceil(rows / teams) * chunk, with teams = min(rows, capacity / G); ties go
-// to the smaller G (fewer records to merge). G ranges over the sizes whose
-// chunk fits in registers (at most kChunkCap columns).
-inline RowPlan plan_rows(int64_t rows, int vocab, int capacity) {
-    RowPlan best{0, 0, 0, 0};
+// to the smaller G (fewer records to merge). With two_per_sm, rows up to
+// kMaxTeam * 8192 columns use 16 logits per thread and two CTAs per SM;
+// longer rows (and two_per_sm == false) use up to 32 logits per thread and
+// one CTA per SM.
+inline RowPlan plan_rows(int64_t rows, int vocab, int sms, bool two_per_sm = true) {
+    const bool pair = two_per_sm && vocab <= kMaxTeam * kThreads * 16;
+    const int vec4 = pair ? 4 : 8;
+    const int cap_cols = kThreads * vec4 * 4;
+    const int ctas_per_sm = pair ? 2 : 1;
+    int capacity = sms * ctas_per_sm;
+    if (capacity > 1024) capacity = 1024;
+    RowPlan best{0, 0, 0, vec4, ctas_per_sm};
     double best_cost = 0.0;
-    const int g_min = (vocab + kChunkCap - 1) / kChunkCap;
+    const int g_min = (vocab + cap_cols - 1) / cap_cols;
     for (int g = g_min; g <= kMaxTeam && g <= capacity; ++g) {
         int chunk = (vocab + g - 1) / g;
         chunk = (chunk + 3) & ~3;
@@ -294,15 +314,152 @@ inline RowPlan plan_rows(int64_t rows, int vocab, int capacity) {
         if (teams < 1) continue;
         const double cost = static_cast<double>((rows + teams - 1) / teams) * chunk;
         if (best.team == 0 || cost < best_cost) {
-            best = RowPlan{g, chunk, static_cast<int>(teams), 0};
+            best = RowPlan{g, chunk, static_cast<int>(teams), vec4, ctas_per_sm};
             best_cost = cost;
         }
     }
-    if (best.team) {
-        const int per_thread = (best.chunk / 4 + kThreads - 1) / kThreads;
-        best.vec4 = per_thread <= 4 ? 4 : 8;
-    }
     return best;
+}
+
+// ------------------------------------------------------ element helpers
+
+__device__ __forceinline__ float comp(const float4& v, int q) {
+    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ float max4(const float4& v) {
+    return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+}
+
+// 2^x on the special-function unit (non-flushing: subnormal results kept).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Element b (= 4 * slot + component) of a thread's registers, by selects
+// (an indexed access would move the array to local memory).
+template <int VEC4>
+__device__ __forceinline__ float pick(const float4 (&v)[VEC4], int b) {
+    const int q = b & 3;
+    const int i = b >> 2;
+    float r = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VEC4; ++j) {
+        const float4 g = v[j];
+        const float c = q == 0 ? g.x : q == 1 ? g.y : q == 2 ? g.z : g.w;
+        r = i == j ? c : r;
+    }
+    return r;
+}
+
+// ------------------------------------------------ the temperature quotient
+
+// x / t, rounded to nearest even, for one temperature t > 0 and many x.
+// y = RN(1/t) once per row; per element q0 = x*y, then two corrections
+// q <- q + (x - q*t)*y with the remainder taken exactly by an FMA
+// (Markstein's scheme: the first correction makes q a faithful rounding of
+// x/t, the second, with y the correctly rounded reciprocal, the correctly
+// rounded quotient). A power-of-two t is a single exact multiplication and
+// t == 1 is the identity. The FMA sequence turns an infinite x into NaN;
+// `exact` maps +-inf to itself (x/t = x for finite t > 0), the row kernels
+// treat NaN like -inf instead.
+struct ScaledQuotient {
+    enum Mode { kIdentity = 0, kScale = 1, kDivide = 2 };
+    float t;
+    float y;
+    int mode;
+
+    __device__ static ScaledQuotient of(float t) {
+        ScaledQuotient q;
+        q.t = t;
+        q.y = __frcp_rn(t);
+        const uint32_t b = __float_as_uint(t);
+        const uint32_t e = (b >> 23) & 0xFFu;
+        if (t == 1.0f) q.mode = kIdentity;
+        else if ((b & 0x007FFFFFu) == 0 && e > 1 && e < 253) q.mode = kScale;
+        else q.mode = kDivide;
+        return q;
+    }
+
+    __device__ __forceinline__ float divide(float x) const {
+        float q = x * y;
+        float r = fmaf(-q, t, x);
+        q = fmaf(r, y, q);
+        r = fmaf(-q, t, x);
+        return fmaf(r, y, q);
+    }
+
+    // Scale registers in place (mode hoisted out of the element loop).
+    template <int VEC4>
+    __device__ __forceinline__ void apply(float4 (&v)[VEC4], int live_slots) const {
+        if (mode == kScale) {
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i)
+                if (i * kThreads < live_slots) {
+                    v[i].x *= y; v[i].y *= y; v[i].z *= y; v[i].w *= y;
+                }
+        } else if (mode == kDivide) {
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i)
+                if (i * kThreads < live_slots) {
+                    v[i].x = divide(v[i].x); v[i].y = divide(v[i].y);
+                    v[i].z = divide(v[i].z); v[i].w = divide(v[i].w);
+                }
+        }
+    }
+
+    // Where the corrections are exact: the quotient and the dividend both
+    // well inside the normal range, so that q*t, x*y and the remainder
+    // x - q*t neither overflow nor underflow (a subnormal remainder loses
+    // the bits the second correction needs).
+    __device__ __forceinline__ static bool fast_ok(float x, float q) {
+        const float ax = fabsf(x), aq = fabsf(q);
+        return ax >= 0x1p-96f && ax <= 0x1p96f && aq >= 0x1p-100f && aq <= 0x1p100f;
+    }
+
+    // The quotient for every x: infinities map to themselves and quotients
+    // outside the fast range take the IEEE division.
+    __device__ __forceinline__ float exact(float x) const {
+        if (mode == kIdentity) return x;
+        if (mode == kScale) return x * y;
+        if (fabsf(x) == INFINITY) return x;
+        const float q = divide(x);
+        return fast_ok(x, q) ? q : __fdiv_rn(x, t);
+    }
+};
+
+// ------------------------------------------------------- the exact race
+
+// Score the elements of `mask` exactly (s + g, g from the element's Philox
+// word) and keep the best (score, column) in (bs, bc). One rolled loop: the
+// element is selected from registers, its noise block recomputed.
+template <int VEC4>
+__device__ __forceinline__ void race_exact(const float4 (&v)[VEC4], uint32_t mask, int col0,
+                                           int tid, int64_t grow_id, PhiloxKey key, float& bs,
+                                           int& bc) {
+#pragma unroll 1
+    while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int f = (b >> 2) * kThreads + tid;
+        const float x = pick(v, b);
+        const uint4 w = noise_words(key, static_cast<uint64_t>(grow_id),
+                                    static_cast<uint64_t>((col0 >> 2) + f));
+        const float score = x + gumbel_of_bits(word_of(w, b & 3));
+        const int c = col0 + 4 * f + (b & 3);
+        if (beats(score, c, bs, bc)) {
+            bs = score;
+            bc = c;
+        }
+    }
 }
 
 }  // namespace drs

@@ -6,22 +6,24 @@
 // Layout of the work. A row of V fp32 logits is split into G contiguous
 // chunks of `chunk` columns (a multiple of 4). G CTAs -- a team -- own the G
 // chunks of every row of the team; teams take rows round robin. The kernel
-// is persistent (one CTA per SM, cooperative launch so that all CTAs are
-// resident) and a CTA walks through its team's rows:
+// is persistent (cooperative launch, so all CTAs are resident; two CTAs per
+// SM in the 16-logit layout so that one computes while the other waits) and
+// a CTA walks through its team's rows:
 //
 //   1. A bulk copy (TMA) stages the CTA's chunk of a row in shared memory,
-//      several rows ahead; each thread then holds up to 32 logits in
-//      registers (float4 slot i of thread t covers columns 4*(i*512+t)+0..3
-//      of the chunk, so shared-memory reads and global stores coalesce).
-//   2. s = x / max(T, 1e-10) as one IEEE fp32 division per element.
+//      several rows ahead; each thread then holds its logits in registers
+//      (float4 slot i of thread t covers columns 4*(i*512+t)+0..3 of the
+//      chunk, so shared-memory reads and global stores coalesce).
+//   2. s = x / max(T, 1e-10): the IEEE fp32 quotient, from a per-row
+//      reciprocal and two FMA corrections (ScaledQuotient).
 //   3. CTA max m and lowest-column argmax; S = sum e^(s-m) and
 //      W = sum e^(s-m)(s-m) (the "online max and sum" of the page).
-//   4. Gumbel-max race (T > 0): score = s + g with g from Philox keyed by
+//   4. Gumbel-max race (T > 0), score = s + g with g from Philox keyed by
 //      (seed, row, column). Elements within kNearTop of the max are scored
-//      first; their best score B bounds the rest: an element can only win
-//      if s > B - 16.64 (the largest possible g), and then only if the
-//      exact lower bound 1 - u <= -log u of its exponential variate allows
-//      it, so most of the row draws no logarithm.
+//      exactly first; their best B bounds the rest: an element can only win
+//      if s > B - 16.64 (the largest possible g), and then only if the exact
+//      bound 1 - u <= -log u of its exponential variate allows it. Only the
+//      few survivors take logarithms, in one rolled loop.
 //   5. The CTA publishes (m, S, W, argmax, best score, best column) in the
 //      workspace, waits for the team's G records of the row and merges them
 //      (M = max m, S = sum S e^(m-M), W = sum e^(m-M)(W + (m-M) S),
@@ -30,7 +32,8 @@
 //      to nearest even.
 //
 // HBM traffic: every logit is read once (by the bulk copy) and every
-// probability written once.
+// probability written once. No fp64 arithmetic (its rate on GB300 is a
+// small fraction of fp32's).
 #include <cfloat>
 #include <climits>
 
@@ -44,8 +47,8 @@ namespace drs {
 
 namespace {
 
-constexpr int kMaxStages = 4;
-constexpr float kNearTop = 2.0f;  // first-sweep window below the CTA max
+constexpr int kMaxStages = 3;
+constexpr float kNearTop = 2.0f;  // window below the CTA max scored exactly first
 
 struct RowStatsParams {
     const float* logits;
@@ -67,8 +70,9 @@ struct RowStatsParams {
     int32_t team;       // CTAs per row
     int32_t chunk;      // columns per CTA (multiple of 4)
     int32_t num_teams;
-    int32_t nstage;     // shared-memory stages (0: no bulk copy)
+    int32_t nstage;     // shared-memory stages, one chunk each (>= 3)
     int32_t stage_bytes;
+    int32_t use_tma;    // stages filled by bulk copies (rows 16-byte aligned)
     int32_t probs_dtype;
     int32_t probs_vec;  // 8-byte probability stores are aligned
 };
@@ -76,8 +80,9 @@ struct RowStatsParams {
 struct Scratch {
     uint64_t full[kMaxStages];
     float wmax[kWarps];
-    double ws[kWarps];
-    double ww[kWarps];
+    int wflag[kWarps];
+    float ws[kWarps];
+    float ww[kWarps];
     int warg[kWarps];
     float wbest[2][kWarps];
     int wbcol[2][kWarps];
@@ -86,20 +91,6 @@ struct Scratch {
     int status;
 };
 
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float max4(const float4& v) {
-    return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-}
-
-__device__ __forceinline__ float comp(const float4& v, int q) {
-    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
-}
-
 __device__ __forceinline__ void set_comp(float4& v, int q, float x) {
     if (q == 0) v.x = x;
     else if (q == 1) v.y = x;
@@ -107,18 +98,29 @@ __device__ __forceinline__ void set_comp(float4& v, int q, float x) {
     else v.w = x;
 }
 
-__device__ __forceinline__ uint16_t prob_code(float p, int dtype) {
-    if (dtype == 1) return __bfloat16_as_ushort(__float2bfloat16_rn(p));
-    return __half_as_ushort(__float2half_rn(p));
+// Two probabilities rounded to nearest even and packed (first in the low
+// half): bf16 or fp16.
+__device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
+    if (bf16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
+
+// log2(1.0001): the race's bound e^(s - best) is widened by 1e-4 so that
+// rounding in it never prunes an element whose fp32 score could win.
+constexpr float kRaceMarginLog2 = 1.4426229e-4f;
 
 }  // namespace
 
-template <int VEC4, bool kTma>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int VEC4>
+__global__ void __launch_bounds__(kThreads, VEC4 == 4 ? 2 : 1)
     row_stats_kernel(const __grid_constant__ RowStatsParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     Scratch& sc = *reinterpret_cast<Scratch*>(smem + p.nstage * p.stage_bytes);
+    const bool use_tma = p.use_tma != 0;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -128,243 +130,274 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = member * p.chunk;
     const int ncols = min(p.vocab - col0, p.chunk);
     const int nfull4 = ncols >> 2;
+    const int nslot4 = (ncols + 3) >> 2;  // float4 slots holding a column
     const uint32_t copy_bytes = static_cast<uint32_t>(nfull4) * 16u;
-    const int64_t nrows =
-        team_id < p.rows ? (p.rows - 1 - team_id) / p.num_teams + 1 : 0;
+    const int64_t nrows = team_id < p.rows ? (p.rows - 1 - team_id) / p.num_teams + 1 : 0;
+    // Stage of row k: k % nstage. Without bulk copies the scaled logits of
+    // a row still wait in "stage" buffers for the next iteration's
+    // finalisation, so nstage >= 2 in both modes.
+    const int nstage = p.nstage;
 
-    if (kTma && tid == 0) {
-        for (int s = 0; s < p.nstage; ++s) mbar_init(&sc.full[s], 1);
+    if (use_tma && tid == 0) {
+        for (int s = 0; s < nstage; ++s) mbar_init(&sc.full[s], 1);
         fence_barrier_init();
     }
     __syncthreads();
 
-    auto issue_copy = [&](int64_t seq) {
-        const int s = static_cast<int>(seq % p.nstage);
-        const int64_t row = team_id + seq * p.num_teams;
-        float* dst = reinterpret_cast<float*>(smem + s * p.stage_bytes);
+    int64_t issued = 0;  // rows whose chunk copy was issued (thread 0 only)
+    auto issue_copy = [&]() {
+        const int s = static_cast<int>(issued % nstage);
+        const int64_t row = team_id + issued * p.num_teams;
         mbar_arrive_expect_tx(&sc.full[s], copy_bytes);
         if (copy_bytes)
-            tma_load_1d(dst, p.logits + row * p.row_stride + col0, copy_bytes, &sc.full[s]);
+            tma_load_1d(smem + s * p.stage_bytes, p.logits + row * p.row_stride + col0, copy_bytes,
+                        &sc.full[s]);
+        ++issued;
     };
-
-    int64_t issued = 0;
-    if (kTma && tid == 0) {
-        for (; issued < nrows && issued < p.nstage; ++issued) issue_copy(issued);
+    if (use_tma && tid == 0) {
+        while (issued < nrows && issued < nstage) issue_copy();
     }
 
     bool aborted = false;
-    int64_t consumed = 0;  // rows whose staged chunk has been read
-    for (int64_t k = 0; k < nrows; ++k) {
-        const int64_t row = team_id + k * p.num_teams;
-        const float* grow = p.logits + row * p.row_stride + col0;
+    int64_t consumed = 0;
+    bool prev_noisy = false;
+    // Iteration k computes row k's partials (A) and then finalises row k-1
+    // (F): the team's records of row k-1 were published one row of work ago,
+    // so the exchange latency hides behind A(k).
+    for (int64_t k = 0; k <= nrows; ++k) {
+        bool cur_noisy = false;
+        if (k < nrows) {
+            const int64_t row = team_id + k * p.num_teams;
+            const int64_t grow_id = p.row0 + row;  // global row
+            const float* grow = p.logits + row * p.row_stride + col0;
+            const int s = static_cast<int>(k % nstage);
+            float4* stage4 = reinterpret_cast<float4*>(smem + s * p.stage_bytes);
 
-        // ---- 1. load the chunk into registers -----------------------------
-        bool timed_out = false;
-        const int s = kTma ? static_cast<int>(k % p.nstage) : 0;
-        if (kTma) timed_out = !mbar_wait_bounded(&sc.full[s], static_cast<uint32_t>((k / p.nstage) & 1));
-        float4 v[VEC4];
-        const float4* stage4 = reinterpret_cast<const float4*>(smem + s * p.stage_bytes);
-#pragma unroll
-        for (int i = 0; i < VEC4; ++i) {
-            const int f = i * kThreads + tid;
-            float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            if (f < nfull4) {
-                if (kTma) {
-                    if (!timed_out) x = stage4[f];
-                } else {
-                    x.x = grow[4 * f + 0];
-                    x.y = grow[4 * f + 1];
-                    x.z = grow[4 * f + 2];
-                    x.w = grow[4 * f + 3];
-                }
-            } else if (f == nfull4) {
-                for (int q = 0; q < (ncols & 3); ++q) set_comp(x, q, grow[4 * f + q]);
-            }
-            v[i] = x;
-        }
-        if (__syncthreads_or(timed_out)) {
-            aborted = true;
-            break;
-        }
-        consumed = k + 1;
-        if (kTma && tid == 0 && issued < nrows) {
-            fence_proxy_async_smem();
-            issue_copy(issued);
-            ++issued;
-        }
-
-        // ---- 2. temperature ----------------------------------------------
-        const int64_t grow_id = p.row0 + row;  // global row
-        const float temp = p.temps[grow_id / p.canvas_len];
-        const float te = fmaxf(temp, kTempFloor);
-        const bool noisy = temp > 0.0f;
-        if (te != 1.0f) {
-#pragma unroll
-            for (int i = 0; i < VEC4; ++i) {
-                v[i].x = __fdiv_rn(v[i].x, te);
-                v[i].y = __fdiv_rn(v[i].y, te);
-                v[i].z = __fdiv_rn(v[i].z, te);
-                v[i].w = __fdiv_rn(v[i].w, te);
-            }
-        }
-
-        // ---- 3. max, argmax, sums ----------------------------------------
-        float mt = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < VEC4; ++i) mt = fmaxf(mt, max4(v[i]));
-        {
-            const float wm = warp_max(mt);
-            if (lane == 0) sc.wmax[warp] = wm;
-        }
-        __syncthreads();
-        const float mc = warp_max(lane < kWarps ? sc.wmax[lane] : -INFINITY);
-
-        int arg_t = INT_MAX;
-        if (mt == mc && mc != -INFINITY) {
+            // ---- A1. load the chunk into registers ---------------------------
+            bool timed_out = false;
+            if (use_tma)
+                timed_out = !mbar_wait_bounded(&sc.full[s], static_cast<uint32_t>((k / nstage) & 1));
+            float4 v[VEC4];
 #pragma unroll
             for (int i = 0; i < VEC4; ++i) {
                 const int f = i * kThreads + tid;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (comp(v[i], q) == mc && arg_t == INT_MAX) arg_t = col0 + 4 * f + q;
-            }
-        }
-
-        float st = 0.0f, wt = 0.0f;
-#pragma unroll
-        for (int i = 0; i < VEC4; ++i) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float d = fmaxf(comp(v[i], q) - mc, -1e30f);
-                const float e = ex2_approx(d * kLog2e);
-                st += e;
-                wt = fmaf(e, d, wt);
-            }
-        }
-
-        // ---- 4a. Gumbel race near the top ----------------------------------
-        const bool race = noisy && mc != -INFINITY;
-        const float near = mc - kNearTop;
-        float bs = -INFINITY;
-        int bc = INT_MAX;
-        if (race) {
-#pragma unroll
-            for (int i = 0; i < VEC4; ++i) {
-                if (max4(v[i]) >= near) {
-                    const int f = i * kThreads + tid;
-                    const uint4 w = noise_words(p.key, static_cast<uint64_t>(grow_id),
-                                                static_cast<uint64_t>((col0 >> 2) + f));
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float x = comp(v[i], q);
-                        if (x >= near) {
-                            const float score = x + gumbel_of_bits(word_of(w, q));
-                            const int c = col0 + 4 * f + q;
-                            if (beats(score, c, bs, bc)) {
-                                bs = score;
-                                bc = c;
-                            }
+                float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                if (i * kThreads < nslot4) {  // CTA-uniform: slot i holds columns somewhere
+                    if (f < nfull4) {
+                        if (use_tma) {
+                            if (!timed_out) x = stage4[f];
+                        } else {
+                            x.x = grow[4 * f + 0];
+                            x.y = grow[4 * f + 1];
+                            x.z = grow[4 * f + 2];
+                            x.w = grow[4 * f + 3];
                         }
+                    } else if (f == nfull4) {
+                        for (int q = 0; q < (ncols & 3); ++q) set_comp(x, q, grow[4 * f + q]);
                     }
                 }
+                v[i] = x;
             }
-        }
 
-        // CTA reduction of S, W, argmax and the first-sweep best.
-        {
-            const double ws = warp_sum_d(static_cast<double>(st));
-            const double ww = warp_sum_d(static_cast<double>(wt));
-            const int wa = warp_min_i(arg_t);
-            float wbs = bs;
-            int wbc = bc;
-            warp_best(wbs, wbc);
-            if (lane == 0) {
-                sc.ws[warp] = ws;
-                sc.ww[warp] = ww;
-                sc.warg[warp] = wa;
-                sc.wbest[0][warp] = wbs;
-                sc.wbcol[0][warp] = wbc;
-            }
-        }
-        __syncthreads();
-        const double s_cta = warp_sum_d(lane < kWarps ? sc.ws[lane] : 0.0);
-        const double w_cta = warp_sum_d(lane < kWarps ? sc.ww[lane] : 0.0);
-        const int arg_cta =
-            mc == -INFINITY ? col0 : warp_min_i(lane < kWarps ? sc.warg[lane] : INT_MAX);
-        float best = lane < kWarps ? sc.wbest[0][lane] : -INFINITY;
-        int best_col = lane < kWarps ? sc.wbcol[0][lane] : INT_MAX;
-        warp_best(best, best_col);
+            // ---- A2. temperature ----------------------------------------------
+            const float temp = p.temps[grow_id / p.canvas_len];  // CTA-uniform
+            const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
+            const bool noisy = temp > 0.0f;
+            cur_noisy = noisy;
+            sq.apply(v, nslot4);
 
-        // ---- 4b. Gumbel race over the rest, pruned -------------------------
-        if (race) {
-            bs = best;
-            bc = best_col;
-            const float floor_score = best - kGumbelMax;
+            // ---- A3. CTA max ---------------------------------------------------
+            float mt = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < VEC4; ++i) {
-                const float gm = max4(v[i]);
-                if (gm > floor_score) {
-                    const int f = i * kThreads + tid;
-                    bool any = false;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float x = comp(v[i], q);
-                        any |= (x > floor_score && x < near);
-                    }
-                    if (any) {
-                        const uint4 w = noise_words(p.key, static_cast<uint64_t>(grow_id),
-                                                    static_cast<uint64_t>((col0 >> 2) + f));
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float x = comp(v[i], q);
-                            if (x > floor_score && x < near) {
-                                const uint32_t word = word_of(w, q);
-                                // x + g >= bs needs -log u <= exp(x - bs); since
-                                // 1 - u <= -log u, a larger 1 - u rules it out.
-                                const float lim = ex2_approx((x - bs) * kLog2e) * 1.0001f;
-                                if (exponential_lower_bound(word) > lim) continue;
-                                const float score = x + gumbel_of_bits(word);
-                                const int c = col0 + 4 * f + q;
-                                if (beats(score, c, bs, bc)) {
-                                    bs = score;
-                                    bc = c;
-                                }
-                            }
-                        }
-                    }
+            for (int i = 0; i < VEC4; ++i) mt = fmaxf(mt, max4(v[i]));
+            {
+                const float wm = warp_max(mt);
+                const int wf = __any_sync(0xffffffffu, timed_out);
+                if (lane == 0) {
+                    sc.wmax[warp] = wm;
+                    sc.wflag[warp] = wf;
                 }
-            }
-            float wbs = bs;
-            int wbc = bc;
-            warp_best(wbs, wbc);
-            if (lane == 0) {
-                sc.wbest[1][warp] = wbs;
-                sc.wbcol[1][warp] = wbc;
             }
             __syncthreads();
-            best = lane < kWarps ? sc.wbest[1][lane] : -INFINITY;
-            best_col = lane < kWarps ? sc.wbcol[1][lane] : INT_MAX;
+            if (__any_sync(0xffffffffu, lane < kWarps && sc.wflag[lane])) {
+                aborted = true;
+                break;
+            }
+            consumed = k + 1;
+            // The stage of row k-2 was read for the last time in iteration
+            // k-1: it now takes row k+1.
+            if (use_tma && tid == 0 && k >= 2 && issued < nrows) {
+                fence_proxy_async_smem();
+                issue_copy();
+            }
+            float mc = warp_max(lane < kWarps ? sc.wmax[lane] : -INFINITY);
+
+            // Exactness guard: the corrected quotient is exact inside
+            // ScaledQuotient::fast_ok. A CTA max outside it (zero, subnormal,
+            // huge, or a tiny dividend) decides the argmax among values that
+            // may round differently, so the chunk is re-read from global
+            // memory and divided exactly (CTA-uniform, rare).
+            if (sq.mode == ScaledQuotient::kDivide && mc != -INFINITY &&
+                !ScaledQuotient::fast_ok(mc * sq.t, mc)) {
+                mt = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < VEC4; ++i) {
+                    const int f = i * kThreads + tid;
+                    if (i * kThreads < nslot4 && f < nslot4) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (4 * f + q < ncols) set_comp(v[i], q, sq.exact(grow[4 * f + q]));
+                    }
+                    mt = fmaxf(mt, max4(v[i]));
+                }
+                __syncthreads();
+                {
+                    const float wm = warp_max(mt);
+                    if (lane == 0) sc.wmax[warp] = wm;
+                }
+                __syncthreads();
+                mc = warp_max(lane < kWarps ? sc.wmax[lane] : -INFINITY);
+            }
+            // The scaled logits wait in the stage for the finalisation of the
+            // row in the next iteration (each thread rewrites its own slots).
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i) {
+                const int f = i * kThreads + tid;
+                if (i * kThreads < nslot4 && f < nslot4) stage4[f] = v[i];
+            }
+
+            // ---- A4. argmax, sums, exact race near the top --------------------
+            // Only threads holding a value within kNearTop of the CTA max look
+            // for the argmax and the near-top elements.
+            const bool race = noisy && mc != -INFINITY;
+            const float near = mc - kNearTop;
+            int arg_t = INT_MAX;
+            uint32_t near_mask = 0;
+            if (mt >= near && mc != -INFINITY) {
+#pragma unroll
+                for (int i = 0; i < VEC4; ++i)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float x = comp(v[i], q);
+                        if (x == mc && arg_t == INT_MAX) arg_t = col0 + 4 * (i * kThreads + tid) + q;
+                        if (x >= near) near_mask |= 1u << (4 * i + q);
+                    }
+            }
+            float st = 0.0f, wt = 0.0f;
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i) {
+                if (i * kThreads < nslot4) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float d = fmaxf(comp(v[i], q) - mc, -1e30f);  // -inf, NaN -> e = 0
+                        const float e = ex2_approx(d * kLog2e);
+                        st += e;
+                        wt = fmaf(e, d, wt);
+                    }
+                }
+            }
+            float bs = -INFINITY;
+            int bc = INT_MAX;
+            if (race && near_mask) race_exact(v, near_mask, col0, tid, grow_id, p.key, bs, bc);
+            {
+                const float ws = warp_sum_f(st);
+                const float ww = warp_sum_f(wt);
+                const int wa = warp_min_i(arg_t);
+                float wbs = bs;
+                int wbc = bc;
+                warp_best(wbs, wbc);
+                if (lane == 0) {
+                    sc.ws[warp] = ws;
+                    sc.ww[warp] = ww;
+                    sc.warg[warp] = wa;
+                    sc.wbest[0][warp] = wbs;
+                    sc.wbcol[0][warp] = wbc;
+                }
+            }
+            __syncthreads();
+            const float s_cta = warp_sum_f(lane < kWarps ? sc.ws[lane] : 0.0f);
+            const float w_cta = warp_sum_f(lane < kWarps ? sc.ww[lane] : 0.0f);
+            const int arg_cta =
+                mc == -INFINITY ? col0 : warp_min_i(lane < kWarps ? sc.warg[lane] : INT_MAX);
+            float best = lane < kWarps ? sc.wbest[0][lane] : -INFINITY;
+            int best_col = lane < kWarps ? sc.wbcol[0][lane] : INT_MAX;
             warp_best(best, best_col);
+
+            // ---- A5. pruned race over the rest ----------------------------------
+            // An element can beat `best` only if s > best - 16.64, and then
+            // only if 1 - u (a lower bound of -log u) is at most e^(s - best).
+            // A float4 group is first tested as a whole (its largest s, its
+            // largest word); the few groups that pass are tested element by
+            // element, and the survivors scored exactly.
+            if (race) {
+                bs = best;
+                bc = best_col;
+                const float floor_score = best - kGumbelMax;
+                uint32_t survivors = 0;
+#pragma unroll
+                for (int i = 0; i < VEC4; ++i) {
+                    const float gm = max4(v[i]);
+                    if (i * kThreads < nslot4 && gm > floor_score) {
+                        const int f = i * kThreads + tid;
+                        const uint4 w = noise_words(p.key, static_cast<uint64_t>(grow_id),
+                                                    static_cast<uint64_t>((col0 >> 2) + f));
+                        const uint32_t wmax = max(max(w.x, w.y), max(w.z, w.w));
+                        const float lim_g = ex2_approx(fmaf(gm - best, kLog2e, kRaceMarginLog2));
+                        if (one_minus_u_lower(wmax) <= lim_g) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float x = comp(v[i], q);
+                                const float lim =
+                                    ex2_approx(fmaf(x - best, kLog2e, kRaceMarginLog2));
+                                if (!((near_mask >> (4 * i + q)) & 1u) && x > floor_score &&
+                                    one_minus_u_lower(word_of(w, q)) <= lim)
+                                    survivors |= 1u << (4 * i + q);
+                            }
+                        }
+                    }
+                }
+                if (survivors) race_exact(v, survivors, col0, tid, grow_id, p.key, bs, bc);
+                float wbs = bs;
+                int wbc = bc;
+                warp_best(wbs, wbc);
+                if (lane == 0) {
+                    sc.wbest[1][warp] = wbs;
+                    sc.wbcol[1][warp] = wbc;
+                }
+                __syncthreads();
+                best = lane < kWarps ? sc.wbest[1][lane] : -INFINITY;
+                best_col = lane < kWarps ? sc.wbcol[1][lane] : INT_MAX;
+                warp_best(best, best_col);
+            }
+
+            // ---- A6. publish the CTA's partial of row k -------------------------
+            if (tid == 0) {
+                const uint64_t tag = (static_cast<uint64_t>(p.generation) << 32) |
+                                     static_cast<uint32_t>(k + 1);
+                publish_partial(p.xchg + static_cast<size_t>(blockIdx.x) * kRing + (k & (kRing - 1)),
+                                mc, s_cta, w_cta, arg_cta, best, best_col, tag);
+            }
         }
 
-        // ---- 5. exchange with the team and merge ----------------------------
-        const int slot = static_cast<int>(k % kRing);
-        const uint64_t tag = (static_cast<uint64_t>(p.generation) << 32) |
-                             static_cast<uint32_t>(k + 1);
-        if (tid == 0) {
-            publish_partial(p.xchg + static_cast<size_t>(blockIdx.x) * kRing + slot, mc,
-                            static_cast<float>(s_cta), static_cast<float>(w_cta), arg_cta,
-                            best, best_col, tag);
+        if (k == 0) {
+            prev_noisy = cur_noisy;
+            continue;
         }
+
+        // ---- F1. merge the team's records of row k-1 -----------------------------
+        const int64_t kf = k - 1;
+        const int64_t frow = team_id + kf * p.num_teams;
         if (warp == 0) {
+            const uint64_t tag = (static_cast<uint64_t>(p.generation) << 32) |
+                                 static_cast<uint32_t>(kf + 1);
             bool ok = true;
             float m = -INFINITY, s_m = 0.0f, w_m = 0.0f, b_m = -INFINITY;
             int a_m = INT_MAX, bc_m = INT_MAX;
             if (lane < p.team) {
                 Partial rp;
-                ok = read_partial_bounded(
-                    p.xchg + static_cast<size_t>(team_id * p.team + lane) * kRing + slot, tag,
-                    rp);
+                ok = read_partial_bounded(p.xchg + static_cast<size_t>(team_id * p.team + lane) * kRing +
+                                              (kf & (kRing - 1)),
+                                          tag, rp);
                 if (ok) {
                     m = rp.m;
                     s_m = rp.s;
@@ -376,62 +409,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = __all_sync(0xffffffffu, ok);
             const float big_m = warp_max(m);
-            double s_d = 0.0, w_d = 0.0;
+            float s_l = 0.0f, w_l = 0.0f;
             if (m != -INFINITY) {
-                const double dm = static_cast<double>(m) - static_cast<double>(big_m);
-                const double f = exp(dm);
-                s_d = f * static_cast<double>(s_m);
-                w_d = f * (static_cast<double>(w_m) + dm * static_cast<double>(s_m));
+                const float dm = m - big_m;
+                const float f = ex2_approx(dm * kLog2e);
+                s_l = f * s_m;
+                w_l = f * fmaf(dm, s_m, w_m);
             }
-            const double s_tot = warp_sum_d(s_d);
-            const double w_tot = warp_sum_d(w_d);
+            const float s_tot = warp_sum_f(s_l);
+            const float w_tot = warp_sum_f(w_l);
             const int arg_row = warp_min_i(m == big_m ? a_m : INT_MAX);
             warp_best(b_m, bc_m);
             if (lane == 0) {
                 sc.row_max = big_m;
-                sc.row_log2s = s_tot > 0.0 ? static_cast<float>(log2(s_tot)) : 0.0f;
+                sc.row_log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
                 sc.status = ok ? 0 : 1;
                 if (ok && member == 0) {
-                    const bool drawn = noisy && b_m != -INFINITY;
-                    p.argmax[row] = arg_row;
-                    p.sample[row] = drawn ? bc_m : arg_row;
-                    p.entropy[row] =
-                        s_tot > 0.0 ? static_cast<float>(log(s_tot) - w_tot / s_tot) : 0.0f;
+                    const bool drawn = prev_noisy && b_m != -INFINITY;
+                    p.argmax[frow] = arg_row;
+                    p.sample[frow] = drawn ? bc_m : arg_row;
+                    p.entropy[frow] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
                 }
             }
         }
+        prev_noisy = cur_noisy;
         __syncthreads();
         if (sc.status != 0) {
             aborted = true;
             break;
         }
 
-        // ---- 6. probabilities ----------------------------------------------
+        // ---- F2. probabilities of row k-1 from its stage -------------------------
         if (p.probs_dtype != 0) {
             const float big_m = sc.row_max;
             const float l2s = sc.row_log2s;
-            uint16_t* prow = static_cast<uint16_t*>(p.probs) + row * p.probs_row_stride + col0;
+            const bool bf16 = p.probs_dtype == 1;
+            const float4* fstage =
+                reinterpret_cast<const float4*>(smem + static_cast<int>(kf % nstage) * p.stage_bytes);
+            uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
 #pragma unroll
             for (int i = 0; i < VEC4; ++i) {
                 const int f = i * kThreads + tid;
-                if (4 * f >= ncols) continue;
-                uint16_t code[4];
+                if (i * kThreads >= nslot4 || f >= nslot4) continue;
+                const float4 sv = fstage[f];
+                float pr[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    float pr;
-                    if (big_m == -INFINITY) {
-                        pr = NAN;
-                    } else {
-                        pr = ex2_approx(fmaf(comp(v[i], q) - big_m, kLog2e, -l2s));
-                    }
-                    code[q] = prob_code(pr, p.probs_dtype);
+                    // e^(s - M - log S) = 2^((s - M) log2 e - log2 S); -inf
+                    // columns (and the NaN quotient of -inf) clamp to 0.
+                    const float t = fmaxf(fmaf(comp(sv, q) - big_m, kLog2e, -l2s), -256.0f);
+                    pr[q] = ex2_approx(t);
                 }
+                if (big_m == -INFINITY) pr[0] = pr[1] = pr[2] = pr[3] = NAN;
+                const uint32_t lo = pack2(pr[0], pr[1], bf16);
+                const uint32_t hi = pack2(pr[2], pr[3], bf16);
                 if (p.probs_vec && f < nfull4) {
-                    const uint2 packed = make_uint2(
-                        static_cast<uint32_t>(code[0]) | (static_cast<uint32_t>(code[1]) << 16),
-                        static_cast<uint32_t>(code[2]) | (static_cast<uint32_t>(code[3]) << 16));
-                    __stcs(reinterpret_cast<uint2*>(prow + 4 * f), packed);
+                    __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
                 } else {
+                    const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                              static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
                     for (int q = 0; q < 4; ++q)
                         if (4 * f + q < ncols) prow[4 * f + q] = code[q];
                 }
@@ -442,20 +478,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (aborted && tid == 0) raise_device_error(p.err, 1);
     // Bulk copies still in flight must land before the CTA's shared memory
     // is released.
-    if (kTma && tid == 0) {
+    if (use_tma && tid == 0) {
         for (int64_t seq = consumed; seq < issued; ++seq) {
-            const int st = static_cast<int>(seq % p.nstage);
-            mbar_wait_bounded(&sc.full[st], static_cast<uint32_t>((seq / p.nstage) & 1));
+            const int st = static_cast<int>(seq % nstage);
+            mbar_wait_bounded(&sc.full[st], static_cast<uint32_t>((seq / nstage) & 1));
         }
     }
 }
 
 namespace {
 
-template <int VEC4, bool kTma>
-drs_status launch_row_stats(RowStatsParams& prm, int grid, size_t smem,
-                            cudaStream_t stream) {
-    auto kernel = row_stats_kernel<VEC4, kTma>;
+template <int VEC4>
+drs_status launch_row_stats(RowStatsParams& prm, int grid, size_t smem, cudaStream_t stream) {
+    auto kernel = row_stats_kernel<VEC4>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return DRS_ERR_CUDA;
@@ -483,8 +518,7 @@ extern "C" size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab) {
 extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t vocab,
                                     int64_t row_stride, const float* temps,
                                     int64_t canvas_len, uint64_t seed, int64_t row0,
-                                    int64_t* argmax,
-                                    int64_t* sample, float* entropy,
+                                    int64_t* argmax, int64_t* sample, float* entropy,
                                     drs_probs_dtype probs_dtype, void* probs,
                                     int64_t probs_row_stride, void* workspace,
                                     size_t workspace_bytes, void* stream) {
@@ -506,11 +540,9 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
 
     const int sms = sm_count();
     if (sms <= 0) return DRS_ERR_CUDA;
-    const int capacity = sms < 1024 ? sms : 1024;
-    const RowPlan plan = plan_rows(rows, static_cast<int>(vocab), capacity);
+    const RowPlan plan = plan_rows(rows, static_cast<int>(vocab), sms);
     if (!plan.team) return DRS_ERR_UNSUPPORTED;
 
-    const bool tma = aligned(logits, 16) && (row_stride % 4 == 0);
     RowStatsParams prm{};
     prm.logits = logits;
     prm.row_stride = row_stride;
@@ -535,26 +567,23 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
     prm.probs_vec = probs && aligned(probs, 8) && (probs_row_stride % 4 == 0);
     if (!prm.err) return DRS_ERR_CUDA;
 
+    // Shared memory: stages of one chunk each (filled by bulk copies when
+    // rows start 16-byte aligned; in every case they keep a row's scaled
+    // logits until its finalisation) plus the reduction scratch, within the
+    // per-CTA share of the SM. Three stages: the row being computed, the row
+    // waiting for the team, the row being loaded.
+    const bool tma = aligned(logits, 16) && (row_stride % 4 == 0);
     const size_t scratch = (sizeof(Scratch) + 127) & ~static_cast<size_t>(127);
-    const size_t smem_limit = 227 * 1024;
-    if (tma) {
-        prm.stage_bytes = (plan.chunk * 4 + 127) & ~127;
-        int ns = static_cast<int>((smem_limit - scratch) / prm.stage_bytes);
-        if (ns > kMaxStages) ns = kMaxStages;
-        prm.nstage = ns;
-    }
-    const bool use_tma = tma && prm.nstage >= 2;
-    if (!use_tma) {
-        prm.nstage = 0;
-        prm.stage_bytes = 0;
-    }
+    const size_t smem_limit = smem_per_cta(plan.ctas_per_sm);
+    prm.stage_bytes = (plan.chunk * 4 + 127) & ~127;
+    int ns = static_cast<int>((smem_limit - scratch) / prm.stage_bytes);
+    if (ns > kMaxStages) ns = kMaxStages;
+    if (ns < 3) return DRS_ERR_UNSUPPORTED;
+    prm.nstage = ns;
+    prm.use_tma = tma ? 1 : 0;
     const size_t smem = static_cast<size_t>(prm.nstage) * prm.stage_bytes + scratch;
     const int grid = plan.team * plan.num_teams;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (plan.vec4 == 4) {
-        return use_tma ? launch_row_stats<4, true>(prm, grid, smem, st)
-                       : launch_row_stats<4, false>(prm, grid, smem, st);
-    }
-    return use_tma ? launch_row_stats<8, true>(prm, grid, smem, st)
-                   : launch_row_stats<8, false>(prm, grid, smem, st);
+    return plan.vec4 == 4 ? launch_row_stats<4>(prm, grid, smem, st)
+                          : launch_row_stats<8>(prm, grid, smem, st);
 }

@@ -73,7 +73,7 @@ static_assert(sizeof(TopkHeader) == 32, "header layout");
 struct TopkScratch {
     uint64_t full[kMaxStages];
     float wmax[kWarps];
-    double ws[kWarps];
+    float ws[kWarps];
     int wcnt[kWarps];
     unsigned long long wcnt64[kWarps];
     int ncand;
@@ -81,10 +81,6 @@ struct TopkScratch {
     float row_max;
     float row_logs;
 };
-
-__device__ __forceinline__ float comp(const float4& v, int q) {
-    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
-}
 
 __device__ __forceinline__ void set_comp(float4& v, int q, float x) {
     if (q == 0) v.x = x;
@@ -218,14 +214,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             issue_next();
         }
-        const float te = fmaxf(p.temps[row / p.canvas_len], kTempFloor);
+        const ScaledQuotient sq = ScaledQuotient::of(fmaxf(p.temps[row / p.canvas_len], kTempFloor));
 #pragma unroll
         for (int i = 0; i < VEC4; ++i) {
-            // x / te, then -0.0 -> +0.0 (one value for the order)
-            v[i].x = __fdiv_rn(v[i].x, te) + 0.0f;
-            v[i].y = __fdiv_rn(v[i].y, te) + 0.0f;
-            v[i].z = __fdiv_rn(v[i].z, te) + 0.0f;
-            v[i].w = __fdiv_rn(v[i].w, te) + 0.0f;
+            // x / te exactly (infinities kept), then -0.0 -> +0.0 (one value
+            // for the order)
+            v[i].x = sq.exact(v[i].x) + 0.0f;
+            v[i].y = sq.exact(v[i].y) + 0.0f;
+            v[i].z = sq.exact(v[i].z) + 0.0f;
+            v[i].w = sq.exact(v[i].w) + 0.0f;
         }
         auto valid = [&](int i, int q) { return 4 * (i * kThreads + tid) + q < ncols; };
         auto col_of = [&](int i, int q) { return col0 + 4 * (i * kThreads + tid) + q; };
@@ -255,10 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < VEC4; ++i)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st += __expf(comp(v[i], q) - mc);
+                for (int q = 0; q < 4; ++q) st += ex2_approx((comp(v[i], q) - mc) * kLog2e);
         }
         {
-            const double ws = warp_sum_d(static_cast<double>(st));
+            const float ws = warp_sum_f(st);
             if (lane == 0) sc.ws[warp] = ws;
         }
 
@@ -335,14 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (rank < nlocal) my_keys[rank] = key;
         }
         for (int c = nlocal + tid; c < K; c += kThreads) my_keys[c] = kNoKey;
-        const double s_cta = warp_sum_d(lane < kWarps ? sc.ws[lane] : 0.0);
+        const float s_cta = warp_sum_f(lane < kWarps ? sc.ws[lane] : 0.0f);
         __syncthreads();
         const uint64_t tag = (static_cast<uint64_t>(p.generation) << 32) |
                              static_cast<uint32_t>(kk + 1);
         if (tid == 0) {
             TopkHeader* h = reinterpret_cast<TopkHeader*>(my_rec);
             h->m = mc;
-            h->s = static_cast<float>(s_cta);
+            h->s = s_cta;
             h->count = nlocal;
             __threadfence();
             asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(&h->tag), "l"(tag) : "memory");
@@ -380,13 +377,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = __all_sync(0xffffffffu, ok);
             const float big_m = warp_max(m);
-            double s_d = 0.0;
-            if (m != -INFINITY) s_d = exp(static_cast<double>(m) - big_m) * s_m;
-            const double s_tot = warp_sum_d(s_d);
+            float s_l = 0.0f;
+            if (m != -INFINITY) s_l = ex2_approx((m - big_m) * kLog2e) * s_m;
+            const float s_tot = warp_sum_f(s_l);
             if (lane == 0) {
                 sc.status = ok ? 0 : 1;
                 sc.row_max = big_m;
-                sc.row_logs = static_cast<float>(log(s_tot));
+                sc.row_logs = logf(s_tot);
             }
         }
         __syncthreads();
@@ -498,8 +495,7 @@ extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64
 
     const int sms = sm_count();
     if (sms <= 0) return DRS_ERR_CUDA;
-    const int capacity = sms < 1024 ? sms : 1024;
-    const RowPlan plan = plan_rows(rows, static_cast<int>(vocab), capacity);
+    const RowPlan plan = plan_rows(rows, static_cast<int>(vocab), sms, false);
     if (!plan.team) return DRS_ERR_UNSUPPORTED;
 
     TopkParams prm{};
@@ -525,7 +521,7 @@ extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64
     const bool tma = aligned(logits, 16) && (row_stride % 4 == 0);
     const size_t scratch = ((sizeof(TopkScratch) + 127) & ~static_cast<size_t>(127)) +
                            static_cast<size_t>(kCandCap) * sizeof(int64_t);
-    const size_t smem_limit = 227 * 1024;
+    const size_t smem_limit = kSmemPerCta;
     if (tma) {
         prm.stage_bytes = (plan.chunk * 4 + 127) & ~127;
         int ns = static_cast<int>((smem_limit - scratch) / prm.stage_bytes);
@@ -536,6 +532,5 @@ extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64
     const size_t smem = static_cast<size_t>(prm.nstage) * prm.stage_bytes + scratch;
     const int grid = plan.team * plan.num_teams;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return plan.vec4 == 4 ? launch_topk<4>(prm, grid, smem, st)
-                          : launch_topk<8>(prm, grid, smem, st);
+    return launch_topk<8>(prm, grid, smem, st);  // plan_rows(..., false): 32 logits per thread
 }
