@@ -156,6 +156,23 @@ def _make_batch(rank: int):
     return w
 
 
+def shard_layout(rank: int, rows: int, canvas_len: int):
+    """Weak scaling: rank r owns global rows [r*rows, (r+1)*rows), whose
+    slots start at r*rows/canvas_len. Returns (row0, first_slot)."""
+    assert rows % canvas_len == 0
+    return rank * rows, rank * rows // canvas_len
+
+
+def global_temps(temps_local, rank: int, rows: int, canvas_len: int):
+    """A per-slot temperature array indexed by global slot in which this
+    rank's slots hold its temperatures (the others are never read)."""
+    _, slot0 = shard_layout(rank, rows, canvas_len)
+    out = torch.zeros(slot0 + temps_local.numel(), dtype=torch.float32,
+                      device=temps_local.device)
+    out[slot0:] = temps_local
+    return out
+
+
 def _run_ours(args, world, rank, local):
     import vocab_row_sampling_gb300 as drs
     drs.load(build_if_missing=True)
@@ -165,14 +182,10 @@ def _run_ours(args, world, rank, local):
     logits = w["logits"][:, :V]
     temps, keep = w["temps"].cuda(), w["keep"].cuda()
     k = w["k"]
-    row0 = rank * rows
+    row0, _ = shard_layout(rank, rows, w["canvas_len"])
     dev = logits.device
     stream = torch.cuda.current_stream()
-    # temps of the whole (multi-rank) batch: this rank's slots sit at the
-    # offset of its first global row
-    slots = rows // w["canvas_len"]
-    temps_all = torch.zeros((rank + 1) * slots, dtype=torch.float32, device=dev)
-    temps_all[rank * slots:] = temps
+    temps_all = global_temps(temps, rank, rows, w["canvas_len"])
 
     argmax = torch.empty(rows, dtype=torch.int64, device=dev)
     sample = torch.empty(rows, dtype=torch.int64, device=dev)

@@ -152,6 +152,16 @@ drs_status drs_philox_gumbel(uint64_t seed, int64_t row0, int64_t rows,
 drs_status drs_scaled_logits(const float *logits, int64_t n, float temp,
                              float *out, void *stream);
 
+/*
+ * Test hook for the failure path (not for production use). code != 0: the
+ * next drs_row_stats launch in this process has CTA 0 withhold its first
+ * exchange record. Its teammates' bounded waits then run out (about 1 s),
+ * the kernel skips the rest of that team's rows and raises the device flag
+ * that drs_get_device_error reports; the CUDA context stays usable. The
+ * hook resets itself after one launch; code 0 clears it.
+ */
+void drs_test_inject_fault(int code);
+
 /* Static, human-readable name of a status code. */
 const char *drs_status_string(drs_status s);
 

@@ -32,7 +32,7 @@ DRS_MAX_VOCAB = 524288
 
 EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_topk_logprobs",
             "drs_topk_workspace_bytes", "drs_philox_gumbel", "drs_scaled_logits",
-            "drs_status_string", "drs_get_device_error")
+            "drs_status_string", "drs_get_device_error", "drs_test_inject_fault")
 
 
 class DrsError(RuntimeError):
@@ -77,6 +77,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_scaled_logits.restype = ctypes.c_int
     lib.drs_status_string.argtypes = [ctypes.c_int]
     lib.drs_status_string.restype = ctypes.c_char_p
+    lib.drs_test_inject_fault.argtypes = [ctypes.c_int]
+    lib.drs_test_inject_fault.restype = None
     lib.drs_get_device_error.argtypes = [vp]
     lib.drs_get_device_error.restype = ctypes.c_int
     _lib = lib
@@ -156,6 +158,12 @@ def drs_scaled_logits(logits, temp: float, out, stream=None):
     assert logits.is_contiguous() and out.is_contiguous() and out.numel() == logits.numel()
     st = load().drs_scaled_logits(_ptr(logits), logits.numel(), temp, _ptr(out), _stream(stream))
     _check(st, "drs_scaled_logits")
+
+
+def drs_test_inject_fault(code: int) -> None:
+    """Test hook: the next drs_row_stats launch withholds one exchange record
+    so that the bounded waits on it run out (see include/drs.h)."""
+    load().drs_test_inject_fault(code)
 
 
 def drs_get_device_error(stream=None) -> int:

@@ -36,6 +36,7 @@
 // small fraction of fp32's).
 #include <cfloat>
 #include <climits>
+#include <atomic>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -75,7 +76,12 @@ struct RowStatsParams {
     int32_t use_tma;    // stages filled by bulk copies (rows 16-byte aligned)
     int32_t probs_dtype;
     int32_t probs_vec;  // 8-byte probability stores are aligned
+    int32_t fault;      // test hook: CTA 0 withholds its first record
 };
+
+// Test hook state: the next launch withholds one record (see
+// drs_test_inject_fault).
+std::atomic<int> g_inject_fault{0};
 
 struct Scratch {
     uint64_t full[kMaxStages];
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, VEC4 == 4 ? 2 : 1)
             }
 
             // ---- A6. publish the CTA's partial of row k -------------------------
-            if (tid == 0) {
+            if (tid == 0 && !(p.fault && blockIdx.x == 0 && k == 0)) {
                 const uint64_t tag = (static_cast<uint64_t>(p.generation) << 32) |
                                      static_cast<uint32_t>(k + 1);
                 publish_partial(p.xchg + static_cast<size_t>(blockIdx.x) * kRing + (k & (kRing - 1)),
@@ -508,6 +514,8 @@ drs_status launch_row_stats(RowStatsParams& prm, int grid, size_t smem, cudaStre
 
 }  // namespace drs
 
+extern "C" void drs_test_inject_fault(int code) { drs::g_inject_fault.store(code); }
+
 extern "C" size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab) {
     (void)rows;
     (void)vocab;
@@ -565,6 +573,7 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
     prm.num_teams = plan.num_teams;
     prm.probs_dtype = static_cast<int32_t>(probs_dtype);
     prm.probs_vec = probs && aligned(probs, 8) && (probs_row_stride % 4 == 0);
+    prm.fault = g_inject_fault.exchange(0);
     if (!prm.err) return DRS_ERR_CUDA;
 
     // Shared memory: stages of one chunk each (filled by bulk copies when
@@ -587,3 +596,4 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
     return plan.vec4 == 4 ? launch_row_stats<4>(prm, grid, smem, st)
                           : launch_row_stats<8>(prm, grid, smem, st);
 }
+
