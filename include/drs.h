@@ -104,6 +104,32 @@ drs_status drs_row_stats(const float *logits, int64_t rows, int64_t vocab,
                          size_t workspace_bytes, void *stream);
 
 /*
+ * drs_row_stats without a caller workspace. The paper has no counterpart:
+ * this entry point exists for callers that cannot allocate device memory
+ * for the library -- plugin interfaces that hand over only input and
+ * output buffers at enqueue time, or code that must not call cudaMalloc
+ * (it can synchronise the device, or the memory budget is fixed at
+ * start-up). Arguments, results and errors are those of drs_row_stats.
+ *
+ * The exchange records live in a fixed device array inside the library
+ * (drs_row_stats_workspace_bytes() bytes, 256 KiB; every GPU that loads
+ * the library holds it until the process exits). Calls whose launch would
+ * need more return DRS_ERR_UNSUPPORTED. The call allocates nothing. Its
+ * first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture. All calls on a device share the array: two calls that can run
+ * at the same time on the GPU (different streams, overlapping) race and
+ * corrupt each other's results. The array needs no clearing: records carry
+ * a per-call tag, so what an earlier call left there is never read.
+ */
+drs_status drs_row_stats_noalloc(const float *logits, int64_t rows, int64_t vocab,
+                                 int64_t row_stride, const float *temps,
+                                 int64_t canvas_len, uint64_t seed, int64_t row0,
+                                 int64_t *argmax, int64_t *sample, float *entropy,
+                                 drs_probs_dtype probs_dtype, void *probs,
+                                 int64_t probs_row_stride, void *stream);
+
+/*
  * Bytes of device workspace drs_topk_logprobs needs (256-byte aligned,
  * contents arbitrary). Same sharing rule as the row-stats workspace.
  */

@@ -30,7 +30,8 @@ DRS_ERR_DEVICE_TIMEOUT = -4
 DRS_PROBS_NONE, DRS_PROBS_BF16, DRS_PROBS_FP16 = 0, 1, 2
 DRS_MAX_VOCAB = 524288
 
-EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_topk_logprobs",
+EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_row_stats_noalloc",
+            "drs_topk_logprobs",
             "drs_topk_workspace_bytes", "drs_philox_gumbel", "drs_scaled_logits",
             "drs_status_string", "drs_get_device_error", "drs_test_inject_fault")
 
@@ -67,6 +68,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_row_stats.argtypes = [vp, i64, i64, i64, vp, i64, u64, i64, vp, vp, vp,
                                   ctypes.c_int, vp, i64, vp, sz, vp]
     lib.drs_row_stats.restype = ctypes.c_int
+    lib.drs_row_stats_noalloc.argtypes = [vp, i64, i64, i64, vp, i64, u64, i64, vp, vp, vp,
+                                          ctypes.c_int, vp, i64, vp]
+    lib.drs_row_stats_noalloc.restype = ctypes.c_int
     lib.drs_topk_workspace_bytes.argtypes = [i64, i64, i32]
     lib.drs_topk_workspace_bytes.restype = sz
     lib.drs_topk_logprobs.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp, vp, sz, vp]
@@ -131,6 +135,20 @@ def drs_row_stats(logits, temps, canvas_len, seed, argmax, sample, entropy,
                               _ptr(entropy), probs_dtype, _ptr(probs), pstride,
                               _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "drs_row_stats")
+
+
+def drs_row_stats_noalloc(logits, temps, canvas_len, seed, argmax, sample, entropy,
+                          probs_dtype=DRS_PROBS_NONE, probs=None, stream=None, row0=0):
+    """drs_row_stats with the library's fixed device workspace: for callers
+    that cannot allocate device memory (see include/drs.h). Calls that can
+    overlap on the GPU share that workspace and race."""
+    rows, vocab = logits.shape
+    pstride = 0 if probs is None else probs.stride(0)
+    st = load().drs_row_stats_noalloc(_ptr(logits), rows, vocab, _row_stride(logits),
+                                      _ptr(temps), canvas_len, seed & (2**64 - 1), row0,
+                                      _ptr(argmax), _ptr(sample), _ptr(entropy), probs_dtype,
+                                      _ptr(probs), pstride, _stream(stream))
+    _check(st, "drs_row_stats_noalloc")
 
 
 def drs_topk_workspace_bytes(rows: int, vocab: int, k: int) -> int:

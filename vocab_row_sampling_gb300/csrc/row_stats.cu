@@ -37,6 +37,7 @@
 #include <cfloat>
 #include <climits>
 #include <atomic>
+#include <mutex>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -597,3 +598,67 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
                           : launch_row_stats<8>(prm, grid, smem, st);
 }
 
+// ---------------------------------------------------------------------------
+// drs_row_stats_noalloc: drs_row_stats with its workspace in a fixed device
+// array of this library instead of a caller buffer.
+//
+// Some callers cannot hand the library a workspace: plugin interfaces of
+// inference runtimes that pass only input and output buffers at enqueue
+// time, or code that must not call cudaMalloc because it synchronises the
+// device or draws on a memory budget fixed at start-up. For them the
+// exchange records live in g_noalloc_workspace below: every GPU that loads
+// the library holds these bytes until the process exits, and all calls on a
+// device share them.
+
+namespace {
+
+constexpr size_t kNoallocWorkspaceBytes = static_cast<size_t>(1024) * drs::kRing * sizeof(drs::Partial);
+static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoallocWorkspaceBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_workspace on the current device. In host code
+// the array's name is a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+void* noalloc_workspace(drs_status* status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *status = DRS_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_workspace);
+        if (e != cudaSuccess || !ptr) {
+            *status = DRS_ERR_CUDA;
+            return nullptr;
+        }
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *status = DRS_OK;
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" drs_status drs_row_stats_noalloc(const float* logits, int64_t rows, int64_t vocab,
+                                            int64_t row_stride, const float* temps,
+                                            int64_t canvas_len, uint64_t seed, int64_t row0,
+                                            int64_t* argmax, int64_t* sample, float* entropy,
+                                            drs_probs_dtype probs_dtype, void* probs,
+                                            int64_t probs_row_stride, void* stream) {
+    if (drs_row_stats_workspace_bytes(rows, vocab) > kNoallocWorkspaceBytes)
+        return DRS_ERR_UNSUPPORTED;
+    if (rows <= 0)  // validation and the empty call need no workspace
+        return drs_row_stats(logits, rows, vocab, row_stride, temps, canvas_len, seed, row0,
+                             argmax, sample, entropy, probs_dtype, probs, probs_row_stride,
+                             nullptr, 0, stream);
+    drs_status st = DRS_OK;
+    void* ws = noalloc_workspace(&st);
+    if (!ws) return st;
+    return drs_row_stats(logits, rows, vocab, row_stride, temps, canvas_len, seed, row0, argmax,
+                         sample, entropy, probs_dtype, probs, probs_row_stride, ws,
+                         kNoallocWorkspaceBytes, stream);
+}
