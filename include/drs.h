@@ -48,13 +48,15 @@ typedef enum drs_probs_dtype {
 } drs_probs_dtype;
 
 /* Largest vocabulary (row length) the kernels accept. */
-#define DRS_MAX_VOCAB 524288
+#define DRS_MAX_VOCAB 491520
 
 /*
  * Bytes of device workspace drs_row_stats needs (at least 256-byte aligned,
- * contents arbitrary, no initialisation needed). The workspace carries the
- * per-row partial results that the CTAs sharing one row exchange. One
- * workspace must not be used by two calls that can run at the same time.
+ * contents arbitrary: each call clears the part it uses with an
+ * asynchronous memset on its stream before its kernel runs). The workspace
+ * carries the per-row partial results that the CTAs sharing one row
+ * exchange. One workspace must not be used by two calls that can run at the
+ * same time.
  */
 size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab);
 
@@ -112,15 +114,16 @@ drs_status drs_row_stats(const float *logits, int64_t rows, int64_t vocab,
  * start-up). Arguments, results and errors are those of drs_row_stats.
  *
  * The exchange records live in a fixed device array inside the library
- * (drs_row_stats_workspace_bytes() bytes, 256 KiB; every GPU that loads
+ * (drs_row_stats_workspace_bytes() bytes, 640 KiB; every GPU that loads
  * the library holds it until the process exits). Calls whose launch would
  * need more return DRS_ERR_UNSUPPORTED. The call allocates nothing. Its
  * first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
  * capture. All calls on a device share the array: two calls that can run
  * at the same time on the GPU (different streams, overlapping) race and
- * corrupt each other's results. The array needs no clearing: records carry
- * a per-call tag, so what an earlier call left there is never read.
+ * corrupt each other's results. Each call clears the part of the array it
+ * uses (an asynchronous memset on its stream) before its kernel runs, so
+ * what an earlier call left there is never read.
  */
 drs_status drs_row_stats_noalloc(const float *logits, int64_t rows, int64_t vocab,
                                  int64_t row_stride, const float *temps,

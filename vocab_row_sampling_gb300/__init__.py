@@ -28,7 +28,7 @@ DRS_ERR_CUDA = -3
 DRS_ERR_DEVICE_TIMEOUT = -4
 
 DRS_PROBS_NONE, DRS_PROBS_BF16, DRS_PROBS_FP16 = 0, 1, 2
-DRS_MAX_VOCAB = 524288
+DRS_MAX_VOCAB = 491520
 
 EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_row_stats_noalloc",
             "drs_topk_logprobs",

@@ -65,6 +65,45 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
     return c;
 }
 
+// The ten round keys of one seed, computed once on the host: a kernel that
+// reads them from its parameters saves the key schedule per call.
+struct PhiloxRoundKeys {
+    uint32_t k0[10];
+    uint32_t k1[10];
+
+    static PhiloxRoundKeys of(uint64_t seed) {
+        PhiloxRoundKeys rk;
+        uint32_t a = static_cast<uint32_t>(seed), b = static_cast<uint32_t>(seed >> 32);
+        for (int r = 0; r < 10; ++r) {
+            rk.k0[r] = a;
+            rk.k1[r] = b;
+            a += 0x9E3779B9u;
+            b += 0xBB67AE85u;
+        }
+        return rk;
+    }
+};
+
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const PhiloxRoundKeys& rk) {
+    constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi_a = __umulhi(kMulA, c.x);
+        const uint32_t lo_a = kMulA * c.x;
+        const uint32_t hi_b = __umulhi(kMulB, c.z);
+        const uint32_t lo_b = kMulB * c.z;
+        c = make_uint4(hi_b ^ c.y ^ rk.k0[round], lo_b, hi_a ^ c.w ^ rk.k1[round], lo_a);
+    }
+    return c;
+}
+
+// Noise words of columns 4*group .. 4*group+3 of `row` (group < 2^32).
+__device__ __forceinline__ uint4 noise_words_rk(const PhiloxRoundKeys& rk, uint64_t row,
+                                                uint32_t group) {
+    return philox4x32_10_rk(
+        make_uint4(group, 0u, static_cast<uint32_t>(row), static_cast<uint32_t>(row >> 32)), rk);
+}
+
 // The four noise words of columns 4*group .. 4*group+3 of `row`.
 __device__ __forceinline__ uint4 noise_words(PhiloxKey key, uint64_t row,
                                              uint64_t group) {
@@ -211,60 +250,87 @@ __device__ __forceinline__ void warp_best(float& s, int& c) {
 
 // ------------------------------------------------------ row exchange
 
-// The partial result one CTA publishes for one row, with a tag written last
-// (release) so that a reader that sees the tag (acquire) sees the fields.
-struct alignas(32) Partial {
-    float m;         // max scaled logit of the CTA's columns (-inf if none)
-    float s;         // sum exp(x - m)
-    float w;         // sum exp(x - m) * (x - m)
-    int32_t arg;     // lowest column attaining m
-    float best;      // best Gumbel-perturbed score (-inf if none)
-    int32_t best_col;
-    uint64_t tag;    // (launch generation << 32) | (row sequence + 1)
+// The records through which the CTAs of a team exchange per-row results.
+// Each 8-byte word holds a 32-bit payload (high half) and a 32-bit tag (low
+// half): the row's sequence number + 1 within the team. 8-byte accesses are
+// single-copy atomic, so a reader that loads all words of a record (relaxed,
+// in one round trip) and finds every tag equal to the row's has the row's
+// values, whatever order the words were written or read in; no fence is
+// needed on either side. The rings are zeroed before each launch, so a tag
+// never matches a record of an earlier launch.
+struct alignas(64) RecordA {  // m, S, W, argmax, best score, best column
+    uint64_t w[8];
 };
-static_assert(sizeof(Partial) == 32, "Partial layout");
+struct alignas(16) RecordB {  // best score, best column
+    uint64_t w[2];
+};
+// Per-CTA exchange area: kRing A slots then kRing B slots.
+constexpr size_t kXchgPerCta = kRing * (sizeof(RecordA) + sizeof(RecordB));
 
-__device__ __forceinline__ void publish_partial(Partial* rec, float m, float s, float w,
-                                                int arg, float best, int best_col,
-                                                uint64_t tag) {
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(rec), "f"(m), "f"(s),
-                 "f"(w), "r"(arg)
+__device__ __forceinline__ RecordA* record_a(void* xchg, int cta, int slot) {
+    return reinterpret_cast<RecordA*>(static_cast<unsigned char*>(xchg) + cta * kXchgPerCta) + slot;
+}
+__device__ __forceinline__ RecordB* record_b(void* xchg, int cta, int slot) {
+    return reinterpret_cast<RecordB*>(static_cast<unsigned char*>(xchg) + cta * kXchgPerCta +
+                                      kRing * sizeof(RecordA)) + slot;
+}
+
+__device__ __forceinline__ uint64_t tagged(uint32_t payload, uint32_t tag) {
+    return (static_cast<uint64_t>(payload) << 32) | tag;
+}
+__device__ __forceinline__ uint64_t tagged(float payload, uint32_t tag) {
+    return tagged(__float_as_uint(payload), tag);
+}
+__device__ __forceinline__ uint32_t payload_u(uint64_t w) { return static_cast<uint32_t>(w >> 32); }
+__device__ __forceinline__ float payload_f(uint64_t w) { return __uint_as_float(payload_u(w)); }
+
+__device__ __forceinline__ void st_relaxed_v2(uint64_t* p, uint64_t a, uint64_t b) {
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b)
                  : "memory");
-    asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(&rec->best), "f"(best),
-                 "r"(best_col)
-                 : "memory");
-    asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(&rec->tag), "l"(tag)
+}
+__device__ __forceinline__ void ld_relaxed_v2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p)
                  : "memory");
 }
 
-__device__ __forceinline__ uint64_t load_tag_acquire(const Partial* rec) {
-    uint64_t t;
-    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(t) : "l"(&rec->tag) : "memory");
-    return t;
+__device__ __forceinline__ void publish_a(RecordA* r, uint32_t tag, float m, float s, float w,
+                                          int arg, float best, int best_col) {
+    st_relaxed_v2(r->w + 0, tagged(m, tag), tagged(s, tag));
+    st_relaxed_v2(r->w + 2, tagged(w, tag), tagged(static_cast<uint32_t>(arg), tag));
+    st_relaxed_v2(r->w + 4, tagged(best, tag), tagged(static_cast<uint32_t>(best_col), tag));
 }
 
-// Wait until rec->tag == tag, then read the fields (bypassing L1).
+__device__ __forceinline__ void publish_b(RecordB* r, uint32_t tag, float best, int best_col) {
+    st_relaxed_v2(r->w, tagged(best, tag), tagged(static_cast<uint32_t>(best_col), tag));
+}
+
+__device__ __forceinline__ bool tags_are(const uint64_t* w, int n, uint32_t tag) {
+    bool ok = true;
+    for (int i = 0; i < n; ++i) ok &= static_cast<uint32_t>(w[i]) == tag;
+    return ok;
+}
+
+// Read an A record and/or a B record (either may be null) whose tags must be
+// tag_a / tag_b, polling until they are; both are in flight together.
 // Returns false after kWaitLimitNs.
-__device__ __forceinline__ bool read_partial_bounded(const Partial* rec, uint64_t tag,
-                                                     Partial& out) {
-    if (load_tag_acquire(rec) != tag) {
-        const uint64_t t0 = global_timer_ns();
-        for (uint32_t it = 0;; ++it) {
-            __nanosleep(64);
-            if (load_tag_acquire(rec) == tag) break;
-            if ((it & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+__device__ __forceinline__ bool read_records(const RecordA* ra, uint32_t tag_a, uint64_t (&a)[6],
+                                             const RecordB* rb, uint32_t tag_b, uint64_t (&b)[2]) {
+    bool ok_a = ra == nullptr, ok_b = rb == nullptr;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (!ok_a) {
+            ld_relaxed_v2(ra->w + 0, a[0], a[1]);
+            ld_relaxed_v2(ra->w + 2, a[2], a[3]);
+            ld_relaxed_v2(ra->w + 4, a[4], a[5]);
         }
+        if (!ok_b) ld_relaxed_v2(rb->w, b[0], b[1]);
+        if (!ok_a) ok_a = tags_are(a, 6, tag_a);
+        if (!ok_b) ok_b = tags_are(b, 2, tag_b);
+        if (ok_a && ok_b) return true;
+        if (it == 0) t0 = global_timer_ns();
+        else if ((it & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(32);
     }
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(rec));
-    const float2 b = __ldcg(reinterpret_cast<const float2*>(&rec->best));
-    out.m = a.x;
-    out.s = a.y;
-    out.w = a.z;
-    out.arg = __float_as_int(a.w);
-    out.best = b.x;
-    out.best_col = __float_as_int(b.y);
-    out.tag = tag;
-    return true;
 }
 
 __device__ __forceinline__ void raise_device_error(int* flag, int code) {
@@ -397,19 +463,20 @@ struct ScaledQuotient {
         return fmaf(r, y, q);
     }
 
-    // Scale registers in place (mode hoisted out of the element loop).
-    template <int VEC4>
+    // Scale registers in place (mode hoisted out of the element loop); slot
+    // i of a thread is live when i * STRIDE < live_slots.
+    template <int VEC4, int STRIDE = kThreads>
     __device__ __forceinline__ void apply(float4 (&v)[VEC4], int live_slots) const {
         if (mode == kScale) {
 #pragma unroll
             for (int i = 0; i < VEC4; ++i)
-                if (i * kThreads < live_slots) {
+                if (i * STRIDE < live_slots) {
                     v[i].x *= y; v[i].y *= y; v[i].z *= y; v[i].w *= y;
                 }
         } else if (mode == kDivide) {
 #pragma unroll
             for (int i = 0; i < VEC4; ++i)
-                if (i * kThreads < live_slots) {
+                if (i * STRIDE < live_slots) {
                     v[i].x = divide(v[i].x); v[i].y = divide(v[i].y);
                     v[i].z = divide(v[i].z); v[i].w = divide(v[i].w);
                 }

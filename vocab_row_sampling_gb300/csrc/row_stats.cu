@@ -6,37 +6,40 @@
 // Layout of the work. A row of V fp32 logits is split into G contiguous
 // chunks of `chunk` columns (a multiple of 4). G CTAs -- a team -- own the G
 // chunks of every row of the team; teams take rows round robin. The kernel
-// is persistent (cooperative launch, so all CTAs are resident; two CTAs per
-// SM in the 16-logit layout so that one computes while the other waits) and
-// a CTA walks through its team's rows:
+// is persistent: one CTA per SM, cooperative launch (all CTAs resident, so
+// their bounded waits on each other cannot deadlock). A CTA has 15 compute
+// warps (480 threads, up to 32 logits each in registers: float4 slot i of
+// thread t covers chunk columns 4*(i*480+t)+0..3) and one exchange warp.
 //
-//   1. A bulk copy (TMA) stages the CTA's chunk of a row in shared memory,
-//      several rows ahead; each thread then holds its logits in registers
-//      (float4 slot i of thread t covers columns 4*(i*512+t)+0..3 of the
-//      chunk, so shared-memory reads and global stores coalesce).
-//   2. s = x / max(T, 1e-10): the IEEE fp32 quotient, from a per-row
-//      reciprocal and two FMA corrections (ScaledQuotient).
-//   3. CTA max m and lowest-column argmax; S = sum e^(s-m) and
-//      W = sum e^(s-m)(s-m) (the "online max and sum" of the page).
-//   4. Gumbel-max race (T > 0), score = s + g with g from Philox keyed by
-//      (seed, row, column). Elements within kNearTop of the max are scored
-//      exactly first; their best B bounds the rest: an element can only win
-//      if s > B - 16.64 (the largest possible g), and then only if the exact
-//      bound 1 - u <= -log u of its exponential variate allows it. Only the
-//      few survivors take logarithms, in one rolled loop.
-//   5. The CTA publishes (m, S, W, argmax, best score, best column) in the
-//      workspace, waits for the team's G records of the row and merges them
-//      (M = max m, S = sum S e^(m-M), W = sum e^(m-M)(W + (m-M) S),
-//      entropy = log S - W / S).
-//   6. Probabilities e^(s - M - log S) are written from registers, rounded
-//      to nearest even.
+// Iteration k, before its one CTA barrier:
+//   compute warps, row k: wait for the bulk copy (TMA) that staged the
+//     chunk rows ahead; s = x / max(T, 1e-10), the IEEE fp32 quotient
+//     (ScaledQuotient), written back into the stage; warp max M_w,
+//     lowest-column argmax, S_w = sum e^(s - M_w), W_w = sum e^(s - M_w)
+//     (s - M_w) (the "online max and sum" of the page); the elements within
+//     kNearTop of M_w scored exactly in the Gumbel-max race (T > 0): score =
+//     s + g, g from Philox keyed by (seed, row, column). The warp's partial
+//     goes to shared memory.
+//   exchange warp: merges the team's first records of row k-1 (M, S, W,
+//     argmax, near-top best B) and its second records of row k-3 (the best
+//     of the pruned race); member 0 writes argmax and entropy of row k-1 and
+//     the sample of row k-3.
+// After the barrier:
+//   exchange warp: combines the warp partials of row k into the CTA's first
+//     record and those of row k-2's race into its second record, publishes
+//     both (release), and issues the bulk copy of a later row.
+//   compute warps, row k-1, read back from its stage: the pruned race with
+//     the row's global near-top best B (an element can only win if
+//     s > B - 16.64, and then only if 1 - u <= -log u allows it; the few
+//     survivors are scored exactly), then its probabilities
+//     e^(s - M - log S), rounded to nearest even and written to HBM.
 //
 // HBM traffic: every logit is read once (by the bulk copy) and every
 // probability written once. No fp64 arithmetic (its rate on GB300 is a
 // small fraction of fp32's).
+#include <atomic>
 #include <cfloat>
 #include <climits>
-#include <atomic>
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -49,8 +52,18 @@ namespace drs {
 
 namespace {
 
-constexpr int kMaxStages = 3;
-constexpr float kNearTop = 2.0f;  // window below the CTA max scored exactly first
+constexpr int kComputeWarps = kWarps - 1;          // warps 0..14
+constexpr int kCompute = kComputeWarps * 32;       // 480 compute threads
+constexpr int kExchangeWarp = kWarps - 1;          // warp 15
+constexpr int kVec4 = 8;                           // float4 slots per compute thread
+constexpr int kRowChunkCap = kCompute * kVec4 * 4; // 15360 columns per CTA
+constexpr int kMaxStages = 4;
+constexpr int kInfoRing = 4;
+constexpr float kNearTop = 2.0f;  // window below the warp max scored exactly first
+
+// log2(1.0001): the race's bound e^(s - best) is widened by 1e-4 so that
+// rounding in it never prunes an element whose fp32 score could win.
+constexpr float kRaceMarginLog2 = 1.4426229e-4f;
 
 struct RowStatsParams {
     const float* logits;
@@ -64,19 +77,20 @@ struct RowStatsParams {
     float* entropy;
     void* probs;
     int64_t probs_row_stride;
-    Partial* xchg;
+    void* xchg;         // records: per CTA, kRing A slots (M, S, W, argmax,
+                        // near-top best) and kRing B slots (race best)
     int* err;
-    PhiloxKey key;
-    uint32_t generation;
+    PhiloxRoundKeys rk;
     int32_t vocab;
     int32_t team;       // CTAs per row
     int32_t chunk;      // columns per CTA (multiple of 4)
     int32_t num_teams;
-    int32_t nstage;     // shared-memory stages, one chunk each (>= 3)
+    int32_t nstage;     // shared-memory stages, one chunk each (3 or 4)
     int32_t stage_bytes;
     int32_t use_tma;    // stages filled by bulk copies (rows 16-byte aligned)
     int32_t probs_dtype;
     int32_t probs_vec;  // 8-byte probability stores are aligned
+    int32_t index32;    // global rows and canvas_len fit 32 bits
     int32_t fault;      // test hook: CTA 0 withholds its first record
 };
 
@@ -84,18 +98,33 @@ struct RowStatsParams {
 // drs_test_inject_fault).
 std::atomic<int> g_inject_fault{0};
 
+struct WarpPartial {
+    float m, s, w, best;
+    int arg, best_col;
+};
+
+struct WarpBest {
+    float best;
+    int col;
+};
+
+// What the merge of a row's first records leaves for the rest of the CTA.
+struct RowInfo {
+    float row_max;
+    float log2s;
+    float near_best;  // best near-top score of the whole row
+    int near_col;
+    int arg;
+    int noisy;
+};
+
 struct Scratch {
     uint64_t full[kMaxStages];
-    float wmax[kWarps];
-    int wflag[kWarps];
-    float ws[kWarps];
-    float ww[kWarps];
-    int warg[kWarps];
-    float wbest[2][kWarps];
-    int wbcol[2][kWarps];
-    float row_max;
-    float row_log2s;
-    int status;
+    WarpPartial p1[2][kComputeWarps];  // row k's warp partials, by row parity
+    WarpBest p2[2][kComputeWarps];     // row k's race bests, by row parity
+    RowInfo info[kInfoRing];           // merged rows, by row % 4
+    int status;                        // a merge ran out of time
+    int abort_load;                    // a bulk copy ran out of time
 };
 
 __device__ __forceinline__ void set_comp(float4& v, int q, float x) {
@@ -116,22 +145,70 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// log2(1.0001): the race's bound e^(s - best) is widened by 1e-4 so that
-// rounding in it never prunes an element whose fp32 score could win.
-constexpr float kRaceMarginLog2 = 1.4426229e-4f;
+// Temperature of a global row: temps[row / canvas_len].
+__device__ __forceinline__ float row_temperature(const RowStatsParams& p, uint64_t grow_id) {
+    const uint64_t slot = p.index32 ? static_cast<uint64_t>(static_cast<uint32_t>(grow_id) /
+                                                            static_cast<uint32_t>(p.canvas_len))
+                                    : grow_id / static_cast<uint64_t>(p.canvas_len);
+    return p.temps[slot];
+}
+
+// Tag of the records of a team's row sequence k (never 0: rings are zeroed
+// before each launch).
+__device__ __forceinline__ uint32_t record_tag(int k) { return static_cast<uint32_t>(k) + 1u; }
+
+// Score the elements of `mask` exactly and keep the best (score, column).
+__device__ __forceinline__ void race_exact8(const float4 (&v)[kVec4], uint32_t mask, int col0,
+                                            int tid, uint64_t grow_id,
+                                            const PhiloxRoundKeys& rk, float& bs, int& bc) {
+#pragma unroll 1
+    while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int f = (b >> 2) * kCompute + tid;
+        const float x = pick(v, b);
+        const uint4 w = noise_words_rk(rk, grow_id, static_cast<uint32_t>((col0 >> 2) + f));
+        const float score = x + gumbel_of_bits(word_of(w, b & 3));
+        const int c = col0 + 4 * f + (b & 3);
+        if (beats(score, c, bs, bc)) {
+            bs = score;
+            bc = c;
+        }
+    }
+}
+
+// Elements of one float4 group that could still beat `best`: 1 - u (a lower
+// bound of -log u) must be at most e^(x - best), widened by the margin. The
+// group is first tested as a whole with its largest x and largest word.
+__device__ __forceinline__ uint32_t race_group(const float4& g, uint4 w, float best,
+                                               float floor_score) {
+    const uint32_t wmax = max(max(w.x, w.y), max(w.z, w.w));
+    const float lim_g = ex2_approx(fmaf(max4(g) - best, kLog2e, kRaceMarginLog2));
+    uint32_t bits = 0;
+    if (one_minus_u_lower(wmax) <= lim_g) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float x = comp(g, q);
+            const float lim = ex2_approx(fmaf(x - best, kLog2e, kRaceMarginLog2));
+            if (x > floor_score && one_minus_u_lower(word_of(w, q)) <= lim) bits |= 1u << q;
+        }
+    }
+    return bits;
+}
 
 }  // namespace
 
-template <int VEC4>
-__global__ void __launch_bounds__(kThreads, VEC4 == 4 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, 1)
     row_stats_kernel(const __grid_constant__ RowStatsParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     Scratch& sc = *reinterpret_cast<Scratch*>(smem + p.nstage * p.stage_bytes);
     const bool use_tma = p.use_tma != 0;
+    const int nstage = p.nstage;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
+    const bool exchange = warp == kExchangeWarp;
     const int team_id = blockIdx.x / p.team;
     const int member = blockIdx.x - team_id * p.team;
     const int col0 = member * p.chunk;
@@ -139,344 +216,361 @@ __global__ void __launch_bounds__(kThreads, VEC4 == 4 ? 2 : 1)
     const int nfull4 = ncols >> 2;
     const int nslot4 = (ncols + 3) >> 2;  // float4 slots holding a column
     const uint32_t copy_bytes = static_cast<uint32_t>(nfull4) * 16u;
-    const int64_t nrows = team_id < p.rows ? (p.rows - 1 - team_id) / p.num_teams + 1 : 0;
-    // Stage of row k: k % nstage. Without bulk copies the scaled logits of
-    // a row still wait in "stage" buffers for the next iteration's
-    // finalisation, so nstage >= 2 in both modes.
-    const int nstage = p.nstage;
+    const int nrows = team_id < p.rows
+                          ? static_cast<int>((p.rows - 1 - team_id) / p.num_teams + 1)
+                          : 0;
+    auto row_of = [&](int k) { return team_id + static_cast<int64_t>(k) * p.num_teams; };
 
-    if (use_tma && tid == 0) {
-        for (int s = 0; s < nstage; ++s) mbar_init(&sc.full[s], 1);
-        fence_barrier_init();
+    if (tid == 0) {
+        if (use_tma) {
+            for (int s = 0; s < nstage; ++s) mbar_init(&sc.full[s], 1);
+            fence_barrier_init();
+        }
+        sc.abort_load = 0;
+        sc.status = 0;
     }
     __syncthreads();
 
-    int64_t issued = 0;  // rows whose chunk copy was issued (thread 0 only)
+    // Producer state, exchange-warp lane 0: rows issued to the stages.
+    int issued = 0;
     auto issue_copy = [&]() {
-        const int s = static_cast<int>(issued % nstage);
-        const int64_t row = team_id + issued * p.num_teams;
+        const int s = issued % nstage;
         mbar_arrive_expect_tx(&sc.full[s], copy_bytes);
         if (copy_bytes)
-            tma_load_1d(smem + s * p.stage_bytes, p.logits + row * p.row_stride + col0, copy_bytes,
-                        &sc.full[s]);
+            tma_load_1d(smem + s * p.stage_bytes, p.logits + row_of(issued) * p.row_stride + col0,
+                        copy_bytes, &sc.full[s]);
         ++issued;
     };
-    if (use_tma && tid == 0) {
+    if (use_tma && exchange && lane == 0) {
         while (issued < nrows && issued < nstage) issue_copy();
     }
 
+    // The temperature of the next row, loaded one iteration ahead.
+    float temp_next = 0.0f;
+    if (nrows > 0) temp_next = row_temperature(p, static_cast<uint64_t>(p.row0 + row_of(0)));
+
     bool aborted = false;
-    int64_t consumed = 0;
-    bool prev_noisy = false;
-    // Iteration k computes row k's partials (A) and then finalises row k-1
-    // (F): the team's records of row k-1 were published one row of work ago,
-    // so the exchange latency hides behind A(k).
-    for (int64_t k = 0; k <= nrows; ++k) {
-        bool cur_noisy = false;
-        if (k < nrows) {
-            const int64_t row = team_id + k * p.num_teams;
-            const int64_t grow_id = p.row0 + row;  // global row
-            const float* grow = p.logits + row * p.row_stride + col0;
-            const int s = static_cast<int>(k % nstage);
-            float4* stage4 = reinterpret_cast<float4*>(smem + s * p.stage_bytes);
+    int consumed = 0;
+    for (int k = 0; k <= nrows + 2; ++k) {
+        const int par = k & 1;
+        // ===================== before the barrier ===============================
+        if (!exchange) {
+            if (k < nrows) {
+                // ---- compute warps: row k ---------------------------------------
+                const int64_t row = row_of(k);
+                const uint64_t grow_id = static_cast<uint64_t>(p.row0 + row);  // global row
+                const float* grow = p.logits + row * p.row_stride + col0;
+                const int s = k % nstage;
+                float4* stage4 = reinterpret_cast<float4*>(smem + s * p.stage_bytes);
+                const float temp = temp_next;
+                if (k + 1 < nrows)
+                    temp_next = row_temperature(p, static_cast<uint64_t>(p.row0 + row_of(k + 1)));
 
-            // ---- A1. load the chunk into registers ---------------------------
-            bool timed_out = false;
-            if (use_tma)
-                timed_out = !mbar_wait_bounded(&sc.full[s], static_cast<uint32_t>((k / nstage) & 1));
-            float4 v[VEC4];
+                bool timed_out = false;
+                if (use_tma)
+                    timed_out =
+                        !mbar_wait_bounded(&sc.full[s], static_cast<uint32_t>((k / nstage) & 1));
+                if (timed_out) sc.abort_load = 1;
+                float4 v[kVec4];
 #pragma unroll
-            for (int i = 0; i < VEC4; ++i) {
-                const int f = i * kThreads + tid;
-                float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                if (i * kThreads < nslot4) {  // CTA-uniform: slot i holds columns somewhere
-                    if (f < nfull4) {
-                        if (use_tma) {
-                            if (!timed_out) x = stage4[f];
-                        } else {
-                            x.x = grow[4 * f + 0];
-                            x.y = grow[4 * f + 1];
-                            x.z = grow[4 * f + 2];
-                            x.w = grow[4 * f + 3];
-                        }
-                    } else if (f == nfull4) {
-                        for (int q = 0; q < (ncols & 3); ++q) set_comp(x, q, grow[4 * f + q]);
-                    }
-                }
-                v[i] = x;
-            }
-
-            // ---- A2. temperature ----------------------------------------------
-            const float temp = p.temps[grow_id / p.canvas_len];  // CTA-uniform
-            const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
-            const bool noisy = temp > 0.0f;
-            cur_noisy = noisy;
-            sq.apply(v, nslot4);
-
-            // ---- A3. CTA max ---------------------------------------------------
-            float mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < VEC4; ++i) mt = fmaxf(mt, max4(v[i]));
-            {
-                const float wm = warp_max(mt);
-                const int wf = __any_sync(0xffffffffu, timed_out);
-                if (lane == 0) {
-                    sc.wmax[warp] = wm;
-                    sc.wflag[warp] = wf;
-                }
-            }
-            __syncthreads();
-            if (__any_sync(0xffffffffu, lane < kWarps && sc.wflag[lane])) {
-                aborted = true;
-                break;
-            }
-            consumed = k + 1;
-            // The stage of row k-2 was read for the last time in iteration
-            // k-1: it now takes row k+1.
-            if (use_tma && tid == 0 && k >= 2 && issued < nrows) {
-                fence_proxy_async_smem();
-                issue_copy();
-            }
-            float mc = warp_max(lane < kWarps ? sc.wmax[lane] : -INFINITY);
-
-            // Exactness guard: the corrected quotient is exact inside
-            // ScaledQuotient::fast_ok. A CTA max outside it (zero, subnormal,
-            // huge, or a tiny dividend) decides the argmax among values that
-            // may round differently, so the chunk is re-read from global
-            // memory and divided exactly (CTA-uniform, rare).
-            if (sq.mode == ScaledQuotient::kDivide && mc != -INFINITY &&
-                !ScaledQuotient::fast_ok(mc * sq.t, mc)) {
-                mt = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < VEC4; ++i) {
-                    const int f = i * kThreads + tid;
-                    if (i * kThreads < nslot4 && f < nslot4) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (4 * f + q < ncols) set_comp(v[i], q, sq.exact(grow[4 * f + q]));
-                    }
-                    mt = fmaxf(mt, max4(v[i]));
-                }
-                __syncthreads();
-                {
-                    const float wm = warp_max(mt);
-                    if (lane == 0) sc.wmax[warp] = wm;
-                }
-                __syncthreads();
-                mc = warp_max(lane < kWarps ? sc.wmax[lane] : -INFINITY);
-            }
-            // The scaled logits wait in the stage for the finalisation of the
-            // row in the next iteration (each thread rewrites its own slots).
-#pragma unroll
-            for (int i = 0; i < VEC4; ++i) {
-                const int f = i * kThreads + tid;
-                if (i * kThreads < nslot4 && f < nslot4) stage4[f] = v[i];
-            }
-
-            // ---- A4. argmax, sums, exact race near the top --------------------
-            // Only threads holding a value within kNearTop of the CTA max look
-            // for the argmax and the near-top elements.
-            const bool race = noisy && mc != -INFINITY;
-            const float near = mc - kNearTop;
-            int arg_t = INT_MAX;
-            uint32_t near_mask = 0;
-            if (mt >= near && mc != -INFINITY) {
-#pragma unroll
-                for (int i = 0; i < VEC4; ++i)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float x = comp(v[i], q);
-                        if (x == mc && arg_t == INT_MAX) arg_t = col0 + 4 * (i * kThreads + tid) + q;
-                        if (x >= near) near_mask |= 1u << (4 * i + q);
-                    }
-            }
-            float st = 0.0f, wt = 0.0f;
-#pragma unroll
-            for (int i = 0; i < VEC4; ++i) {
-                if (i * kThreads < nslot4) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float d = fmaxf(comp(v[i], q) - mc, -1e30f);  // -inf, NaN -> e = 0
-                        const float e = ex2_approx(d * kLog2e);
-                        st += e;
-                        wt = fmaf(e, d, wt);
-                    }
-                }
-            }
-            float bs = -INFINITY;
-            int bc = INT_MAX;
-            if (race && near_mask) race_exact(v, near_mask, col0, tid, grow_id, p.key, bs, bc);
-            {
-                const float ws = warp_sum_f(st);
-                const float ww = warp_sum_f(wt);
-                const int wa = warp_min_i(arg_t);
-                float wbs = bs;
-                int wbc = bc;
-                warp_best(wbs, wbc);
-                if (lane == 0) {
-                    sc.ws[warp] = ws;
-                    sc.ww[warp] = ww;
-                    sc.warg[warp] = wa;
-                    sc.wbest[0][warp] = wbs;
-                    sc.wbcol[0][warp] = wbc;
-                }
-            }
-            __syncthreads();
-            const float s_cta = warp_sum_f(lane < kWarps ? sc.ws[lane] : 0.0f);
-            const float w_cta = warp_sum_f(lane < kWarps ? sc.ww[lane] : 0.0f);
-            const int arg_cta =
-                mc == -INFINITY ? col0 : warp_min_i(lane < kWarps ? sc.warg[lane] : INT_MAX);
-            float best = lane < kWarps ? sc.wbest[0][lane] : -INFINITY;
-            int best_col = lane < kWarps ? sc.wbcol[0][lane] : INT_MAX;
-            warp_best(best, best_col);
-
-            // ---- A5. pruned race over the rest ----------------------------------
-            // An element can beat `best` only if s > best - 16.64, and then
-            // only if 1 - u (a lower bound of -log u) is at most e^(s - best).
-            // A float4 group is first tested as a whole (its largest s, its
-            // largest word); the few groups that pass are tested element by
-            // element, and the survivors scored exactly.
-            if (race) {
-                bs = best;
-                bc = best_col;
-                const float floor_score = best - kGumbelMax;
-                uint32_t survivors = 0;
-#pragma unroll
-                for (int i = 0; i < VEC4; ++i) {
-                    const float gm = max4(v[i]);
-                    if (i * kThreads < nslot4 && gm > floor_score) {
-                        const int f = i * kThreads + tid;
-                        const uint4 w = noise_words(p.key, static_cast<uint64_t>(grow_id),
-                                                    static_cast<uint64_t>((col0 >> 2) + f));
-                        const uint32_t wmax = max(max(w.x, w.y), max(w.z, w.w));
-                        const float lim_g = ex2_approx(fmaf(gm - best, kLog2e, kRaceMarginLog2));
-                        if (one_minus_u_lower(wmax) <= lim_g) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float x = comp(v[i], q);
-                                const float lim =
-                                    ex2_approx(fmaf(x - best, kLog2e, kRaceMarginLog2));
-                                if (!((near_mask >> (4 * i + q)) & 1u) && x > floor_score &&
-                                    one_minus_u_lower(word_of(w, q)) <= lim)
-                                    survivors |= 1u << (4 * i + q);
+                for (int i = 0; i < kVec4; ++i) {
+                    const int f = i * kCompute + tid;
+                    float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                    if (i * kCompute < nslot4) {  // CTA-uniform: slot i holds columns
+                        if (f < nfull4) {
+                            if (use_tma) {
+                                if (!timed_out) x = stage4[f];
+                            } else {
+                                x.x = grow[4 * f + 0];
+                                x.y = grow[4 * f + 1];
+                                x.z = grow[4 * f + 2];
+                                x.w = grow[4 * f + 3];
                             }
+                        } else if (f == nfull4) {
+                            for (int q = 0; q < (ncols & 3); ++q) set_comp(x, q, grow[4 * f + q]);
+                        }
+                    }
+                    v[i] = x;
+                }
+
+                const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
+                const bool noisy = temp > 0.0f;
+                sq.apply<kVec4, kCompute>(v, nslot4);
+
+                float mt = fmaxf(fmaxf(fmaxf(max4(v[0]), max4(v[1])), fmaxf(max4(v[2]), max4(v[3]))),
+                                 fmaxf(fmaxf(max4(v[4]), max4(v[5])), fmaxf(max4(v[6]), max4(v[7]))));
+                float mw = warp_max(mt);
+                // Exactness guard: the corrected quotient is exact inside
+                // ScaledQuotient::fast_ok. A warp max outside it (zero,
+                // subnormal, huge, or from a tiny dividend) could decide the
+                // argmax among values that round differently, so that warp
+                // re-reads its logits and divides them exactly (rare).
+                if (sq.mode == ScaledQuotient::kDivide && mw != -INFINITY &&
+                    !ScaledQuotient::fast_ok(mw * sq.t, mw)) {
+                    mt = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < kVec4; ++i) {
+                        const int f = i * kCompute + tid;
+                        if (i * kCompute < nslot4 && f < nslot4) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (4 * f + q < ncols) set_comp(v[i], q, sq.exact(grow[4 * f + q]));
+                        }
+                        mt = fmaxf(mt, max4(v[i]));
+                    }
+                    mw = warp_max(mt);
+                }
+                // The scaled logits wait in the stage for the race and the
+                // probabilities of the next iteration.
+#pragma unroll
+                for (int i = 0; i < kVec4; ++i) {
+                    const int f = i * kCompute + tid;
+                    if (i * kCompute < nslot4 && f < nslot4) stage4[f] = v[i];
+                }
+
+                // argmax and near-top elements: threads near the warp max only
+                const float near = mw - kNearTop;
+                int arg_t = INT_MAX;
+                uint32_t near_mask = 0;
+                if (mt >= near && mw != -INFINITY) {
+#pragma unroll
+                    for (int i = 0; i < kVec4; ++i)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float x = comp(v[i], q);
+                            if (x == mw && arg_t == INT_MAX)
+                                arg_t = col0 + 4 * (i * kCompute + tid) + q;
+                            if (x >= near) near_mask |= 1u << (4 * i + q);
+                        }
+                }
+                // sums, four accumulators each
+                float st[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int i = 0; i < kVec4; ++i) {
+                    if (i * kCompute < nslot4) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float d = fmaxf(comp(v[i], q) - mw, -1e30f);  // -inf, NaN -> 0
+                            const float e = ex2_approx(d * kLog2e);
+                            st[q] += e;
+                            wt[q] = fmaf(e, d, wt[q]);
                         }
                     }
                 }
-                if (survivors) race_exact(v, survivors, col0, tid, grow_id, p.key, bs, bc);
-                float wbs = bs;
-                int wbc = bc;
-                warp_best(wbs, wbc);
-                if (lane == 0) {
-                    sc.wbest[1][warp] = wbs;
-                    sc.wbcol[1][warp] = wbc;
-                }
-                __syncthreads();
-                best = lane < kWarps ? sc.wbest[1][lane] : -INFINITY;
-                best_col = lane < kWarps ? sc.wbcol[1][lane] : INT_MAX;
-                warp_best(best, best_col);
+                float bs = -INFINITY;
+                int bc = INT_MAX;
+                if (noisy && near_mask) race_exact8(v, near_mask, col0, tid, grow_id, p.rk, bs, bc);
+                const float sw = warp_sum_f((st[0] + st[1]) + (st[2] + st[3]));
+                const float ww = warp_sum_f((wt[0] + wt[1]) + (wt[2] + wt[3]));
+                const int aw = warp_min_i(arg_t);
+                warp_best(bs, bc);
+                if (lane == 0) sc.p1[par][warp] = WarpPartial{mw, sw, ww, bs, aw, bc};
             }
-
-            // ---- A6. publish the CTA's partial of row k -------------------------
-            if (tid == 0 && !(p.fault && blockIdx.x == 0 && k == 0)) {
-                const uint64_t tag = (static_cast<uint64_t>(p.generation) << 32) |
-                                     static_cast<uint32_t>(k + 1);
-                publish_partial(p.xchg + static_cast<size_t>(blockIdx.x) * kRing + (k & (kRing - 1)),
-                                mc, s_cta, w_cta, arg_cta, best, best_col, tag);
-            }
-        }
-
-        if (k == 0) {
-            prev_noisy = cur_noisy;
-            continue;
-        }
-
-        // ---- F1. merge the team's records of row k-1 -----------------------------
-        const int64_t kf = k - 1;
-        const int64_t frow = team_id + kf * p.num_teams;
-        if (warp == 0) {
-            const uint64_t tag = (static_cast<uint64_t>(p.generation) << 32) |
-                                 static_cast<uint32_t>(kf + 1);
+        } else {
+            // ---- exchange warp: merge first records of row k-1, second of k-3 -----
+            const bool do_a = k >= 1 && k <= nrows;
+            const bool do_b = k >= 3 && k - 3 < nrows;
             bool ok = true;
-            float m = -INFINITY, s_m = 0.0f, w_m = 0.0f, b_m = -INFINITY;
-            int a_m = INT_MAX, bc_m = INT_MAX;
-            if (lane < p.team) {
-                Partial rp;
-                ok = read_partial_bounded(p.xchg + static_cast<size_t>(team_id * p.team + lane) * kRing +
-                                              (kf & (kRing - 1)),
-                                          tag, rp);
-                if (ok) {
-                    m = rp.m;
-                    s_m = rp.s;
-                    w_m = rp.w;
-                    a_m = rp.arg;
-                    b_m = rp.best;
-                    bc_m = rp.best_col;
+            uint64_t ra[6] = {0, 0, 0, 0, 0, 0}, rb[2] = {0, 0};
+            if (lane < p.team && (do_a || do_b)) {
+                const int cta = team_id * p.team + lane;
+                ok = read_records(do_a ? record_a(p.xchg, cta, (k - 1) & (kRing - 1)) : nullptr,
+                                  record_tag(k - 1), ra,
+                                  do_b ? record_b(p.xchg, cta, (k - 3) & (kRing - 1)) : nullptr,
+                                  record_tag(k - 3), rb);
+            }
+            const bool have = lane < p.team && ok;
+            if (do_a) {
+                const int kf = k - 1;
+                const int64_t frow = row_of(kf);
+                const float m = have ? payload_f(ra[0]) : -INFINITY;
+                const float s_m = have ? payload_f(ra[1]) : 0.0f;
+                const float w_m = have ? payload_f(ra[2]) : 0.0f;
+                const int a_m = have ? static_cast<int>(payload_u(ra[3])) : INT_MAX;
+                float b_m = have ? payload_f(ra[4]) : -INFINITY;
+                int bc_m = have ? static_cast<int>(payload_u(ra[5])) : INT_MAX;
+                const float big_m = warp_max(m);
+                float s_l = 0.0f, w_l = 0.0f;
+                if (m != -INFINITY) {
+                    const float dm = m - big_m;
+                    const float f = ex2_approx(dm * kLog2e);
+                    s_l = f * s_m;
+                    w_l = f * fmaf(dm, s_m, w_m);
+                }
+                const float s_tot = warp_sum_f(s_l);
+                const float w_tot = warp_sum_f(w_l);
+                const int arg_row = warp_min_i(m == big_m ? a_m : INT_MAX);
+                warp_best(b_m, bc_m);
+                const bool noisy = row_temperature(p, static_cast<uint64_t>(p.row0 + frow)) > 0.0f;
+                if (lane == 0) {
+                    RowInfo& ri = sc.info[kf & (kInfoRing - 1)];
+                    ri.row_max = big_m;
+                    ri.log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
+                    ri.near_best = b_m;
+                    ri.near_col = bc_m;
+                    ri.arg = arg_row;
+                    ri.noisy = noisy && big_m != -INFINITY;
+                    if (member == 0) {
+                        p.argmax[frow] = arg_row;
+                        p.entropy[frow] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
+                        if (!ri.noisy) p.sample[frow] = arg_row;
+                    }
+                }
+            }
+            if (do_b) {
+                const int kf = k - 3;
+                float b = have ? payload_f(rb[0]) : -INFINITY;
+                int bcol = have ? static_cast<int>(payload_u(rb[1])) : INT_MAX;
+                warp_best(b, bcol);
+                if (lane == 0) {
+                    const RowInfo& ri = sc.info[kf & (kInfoRing - 1)];
+                    if (ri.noisy && member == 0) {
+                        float bb = ri.near_best;
+                        int bbc = ri.near_col;
+                        if (beats(b, bcol, bb, bbc)) {
+                            bb = b;
+                            bbc = bcol;
+                        }
+                        p.sample[row_of(kf)] = bb != -INFINITY ? bbc : ri.arg;
+                    }
                 }
             }
             ok = __all_sync(0xffffffffu, ok);
-            const float big_m = warp_max(m);
-            float s_l = 0.0f, w_l = 0.0f;
-            if (m != -INFINITY) {
-                const float dm = m - big_m;
-                const float f = ex2_approx(dm * kLog2e);
-                s_l = f * s_m;
-                w_l = f * fmaf(dm, s_m, w_m);
-            }
-            const float s_tot = warp_sum_f(s_l);
-            const float w_tot = warp_sum_f(w_l);
-            const int arg_row = warp_min_i(m == big_m ? a_m : INT_MAX);
-            warp_best(b_m, bc_m);
-            if (lane == 0) {
-                sc.row_max = big_m;
-                sc.row_log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
-                sc.status = ok ? 0 : 1;
-                if (ok && member == 0) {
-                    const bool drawn = prev_noisy && b_m != -INFINITY;
-                    p.argmax[frow] = arg_row;
-                    p.sample[frow] = drawn ? bc_m : arg_row;
-                    p.entropy[frow] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
-                }
-            }
+            if (lane == 0) sc.status = ok ? 0 : 1;
         }
-        prev_noisy = cur_noisy;
-        __syncthreads();
-        if (sc.status != 0) {
+
+        __syncthreads();  // ============== the barrier of iteration k ===========
+
+        if (sc.abort_load || sc.status) {
             aborted = true;
             break;
         }
+        if (k < nrows) consumed = k + 1;
 
-        // ---- F2. probabilities of row k-1 from its stage -------------------------
-        if (p.probs_dtype != 0) {
-            const float big_m = sc.row_max;
-            const float l2s = sc.row_log2s;
-            const bool bf16 = p.probs_dtype == 1;
-            const float4* fstage =
-                reinterpret_cast<const float4*>(smem + static_cast<int>(kf % nstage) * p.stage_bytes);
-            uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
-#pragma unroll
-            for (int i = 0; i < VEC4; ++i) {
-                const int f = i * kThreads + tid;
-                if (i * kThreads >= nslot4 || f >= nslot4) continue;
-                const float4 sv = fstage[f];
-                float pr[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    // e^(s - M - log S) = 2^((s - M) log2 e - log2 S); -inf
-                    // columns (and the NaN quotient of -inf) clamp to 0.
-                    const float t = fmaxf(fmaf(comp(sv, q) - big_m, kLog2e, -l2s), -256.0f);
-                    pr[q] = ex2_approx(t);
+        // ===================== after the barrier ================================
+        if (exchange) {
+            if (k < nrows) {
+                // ---- first record of row k --------------------------------------
+                const WarpPartial wp = lane < kComputeWarps
+                                           ? sc.p1[par][lane]
+                                           : WarpPartial{-INFINITY, 0.0f, 0.0f, -INFINITY, INT_MAX,
+                                                         INT_MAX};
+                const float mc = warp_max(wp.m);
+                float s_l = 0.0f, w_l = 0.0f;
+                if (wp.m != -INFINITY) {
+                    const float dm = wp.m - mc;
+                    const float f = ex2_approx(dm * kLog2e);
+                    s_l = f * wp.s;
+                    w_l = f * fmaf(dm, wp.s, wp.w);
                 }
-                if (big_m == -INFINITY) pr[0] = pr[1] = pr[2] = pr[3] = NAN;
-                const uint32_t lo = pack2(pr[0], pr[1], bf16);
-                const uint32_t hi = pack2(pr[2], pr[3], bf16);
-                if (p.probs_vec && f < nfull4) {
-                    __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
-                } else {
-                    const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
-                                              static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
-                    for (int q = 0; q < 4; ++q)
-                        if (4 * f + q < ncols) prow[4 * f + q] = code[q];
+                const float s_c = warp_sum_f(s_l);
+                const float w_c = warp_sum_f(w_l);
+                const int a_c = mc == -INFINITY ? col0 : warp_min_i(wp.m == mc ? wp.arg : INT_MAX);
+                float b_c = wp.best;
+                int bcol_c = wp.best_col;
+                warp_best(b_c, bcol_c);
+                if (lane == 0 && !(p.fault && blockIdx.x == 0 && k == 0))
+                    publish_a(record_a(p.xchg, blockIdx.x, k & (kRing - 1)), record_tag(k), mc, s_c,
+                              w_c, a_c, b_c, bcol_c);
+            }
+            if (k >= 2 && k - 2 < nrows) {
+                // ---- second record of row k-2 (its race, run after barrier k-1) ----
+                const int kf = k - 2;
+                const WarpBest wb = lane < kComputeWarps ? sc.p2[kf & 1][lane]
+                                                         : WarpBest{-INFINITY, INT_MAX};
+                float b = wb.best;
+                int bcol = wb.col;
+                warp_best(b, bcol);
+                if (lane == 0)
+                    publish_b(record_b(p.xchg, blockIdx.x, kf & (kRing - 1)), record_tag(kf), b, bcol);
+            }
+            // The stage of row k-2 was read for the last time before this
+            // barrier: it takes the next row to load.
+            if (use_tma && lane == 0 && k >= 2 && issued < nrows) {
+                fence_proxy_async_smem();
+                issue_copy();
+            }
+        } else if (k >= 1 && k <= nrows) {
+            // ---- compute warps: the pruned race and the probabilities of row k-1 ----
+            const int kf = k - 1;
+            const RowInfo ri = sc.info[kf & (kInfoRing - 1)];
+            const int64_t frow = row_of(kf);
+            const uint64_t fgrow_id = static_cast<uint64_t>(p.row0 + frow);
+            const float4* fstage =
+                reinterpret_cast<const float4*>(smem + (kf % nstage) * p.stage_bytes);
+            float4 v[kVec4];
+#pragma unroll
+            for (int i = 0; i < kVec4; ++i) {
+                const int f = i * kCompute + tid;
+                v[i] = (i * kCompute < nslot4 && f < nslot4)
+                           ? fstage[f]
+                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+            if (ri.noisy) {
+                const float best = ri.near_best;
+                const float floor_score = best - kGumbelMax;
+                float bs = best;
+                int bc = ri.near_col;
+                uint32_t survivors = 0;
+                // Philox four groups at a time, so that their chains overlap.
+#pragma unroll
+                for (int i0 = 0; i0 < kVec4; i0 += 4) {
+                    bool pass[4];
+                    bool any = false;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        pass[j] = (i0 + j) * kCompute < nslot4 && max4(v[i0 + j]) > floor_score;
+                        any |= pass[j];
+                    }
+                    if (any) {
+                        uint4 w[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            w[j] = noise_words_rk(
+                                p.rk, fgrow_id,
+                                static_cast<uint32_t>((col0 >> 2) + (i0 + j) * kCompute + tid));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (pass[j])
+                                survivors |= race_group(v[i0 + j], w[j], best, floor_score)
+                                             << (4 * (i0 + j));
+                    }
+                }
+                if (survivors) race_exact8(v, survivors, col0, tid, fgrow_id, p.rk, bs, bc);
+                warp_best(bs, bc);
+                if (lane == 0) sc.p2[kf & 1][warp] = WarpBest{bs, bc};
+            } else if (lane == 0) {
+                sc.p2[kf & 1][warp] = WarpBest{-INFINITY, INT_MAX};
+            }
+
+            if (p.probs_dtype != 0) {
+                const float big_m = ri.row_max;
+                const float l2s = ri.log2s;
+                const bool bf16 = p.probs_dtype == 1;
+                uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
+#pragma unroll
+                for (int i = 0; i < kVec4; ++i) {
+                    const int f = i * kCompute + tid;
+                    if (i * kCompute >= nslot4 || f >= nslot4) continue;
+                    float pr[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        // e^(s - M - log S) = 2^((s - M) log2 e - log2 S); -inf
+                        // columns (and the NaN quotient of -inf) clamp to 0.
+                        const float t = fmaxf(fmaf(comp(v[i], q) - big_m, kLog2e, -l2s), -256.0f);
+                        pr[q] = ex2_approx(t);
+                    }
+                    if (big_m == -INFINITY) pr[0] = pr[1] = pr[2] = pr[3] = NAN;
+                    const uint32_t lo = pack2(pr[0], pr[1], bf16);
+                    const uint32_t hi = pack2(pr[2], pr[3], bf16);
+                    if (p.probs_vec && f < nfull4) {
+                        __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
+                    } else {
+                        const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                                  static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+                        for (int q = 0; q < 4; ++q)
+                            if (4 * f + q < ncols) prow[4 * f + q] = code[q];
+                    }
                 }
             }
         }
@@ -485,19 +579,49 @@ __global__ void __launch_bounds__(kThreads, VEC4 == 4 ? 2 : 1)
     if (aborted && tid == 0) raise_device_error(p.err, 1);
     // Bulk copies still in flight must land before the CTA's shared memory
     // is released.
-    if (use_tma && tid == 0) {
-        for (int64_t seq = consumed; seq < issued; ++seq) {
-            const int st = static_cast<int>(seq % nstage);
-            mbar_wait_bounded(&sc.full[st], static_cast<uint32_t>((seq / nstage) & 1));
+    if (use_tma && exchange && lane == 0) {
+        for (int seq = consumed; seq < issued; ++seq) {
+            mbar_wait_bounded(&sc.full[seq % nstage], static_cast<uint32_t>((seq / nstage) & 1));
         }
     }
 }
 
 namespace {
 
-template <int VEC4>
+// Team size G for one CTA per SM with 480 compute threads: the chunk must
+// fit the registers (15360 columns) and, for four stages, shared memory.
+// Minimises ceil(rows / teams) * chunk with teams = min(rows, sms / G); ties
+// go to the smaller G.
+RowPlan plan_row_stats(int64_t rows, int vocab, int sms, size_t scratch) {
+    const size_t budget = kSmemPerCta - scratch;
+    int cap4 = static_cast<int>(budget / (4 * 4)) & ~31;  // columns with 4 stages
+    if (cap4 > kRowChunkCap) cap4 = kRowChunkCap;
+    const int cap3 = kRowChunkCap;                        // 3 stages: 180 KB
+    RowPlan best{0, 0, 0, kVec4, 1};
+    double best_cost = 0.0;
+    const int capacity = sms > 1024 ? 1024 : sms;
+    const int g_min = (vocab + cap3 - 1) / cap3;
+    for (int g = g_min; g <= kMaxTeam && g <= capacity; ++g) {
+        int chunk = (vocab + g - 1) / g;
+        chunk = (chunk + 3) & ~3;
+        if ((vocab + chunk - 1) / chunk != g) continue;
+        int64_t teams = capacity / g;
+        if (teams > rows) teams = rows;
+        if (teams < 1) continue;
+        // three stages leave the bulk copy only part of an iteration: count
+        // such a chunk as 25% dearer
+        const double pen = chunk <= cap4 ? 1.0 : 1.25;
+        const double cost = pen * static_cast<double>((rows + teams - 1) / teams) * chunk;
+        if (best.team == 0 || cost < best_cost) {
+            best = RowPlan{g, chunk, static_cast<int>(teams), kVec4, 1};
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
 drs_status launch_row_stats(RowStatsParams& prm, int grid, size_t smem, cudaStream_t stream) {
-    auto kernel = row_stats_kernel<VEC4>;
+    auto kernel = row_stats_kernel;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return DRS_ERR_CUDA;
@@ -520,8 +644,8 @@ extern "C" void drs_test_inject_fault(int code) { drs::g_inject_fault.store(code
 extern "C" size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab) {
     (void)rows;
     (void)vocab;
-    // One ring of exchange records per resident CTA, for up to 1024 CTAs.
-    return static_cast<size_t>(1024) * drs::kRing * sizeof(drs::Partial);
+    // The exchange records of up to 1024 resident CTAs.
+    return static_cast<size_t>(1024) * drs::kXchgPerCta;
 }
 
 extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t vocab,
@@ -549,8 +673,11 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
 
     const int sms = sm_count();
     if (sms <= 0) return DRS_ERR_CUDA;
-    const RowPlan plan = plan_rows(rows, static_cast<int>(vocab), sms);
+    const size_t scratch = (sizeof(Scratch) + 127) & ~static_cast<size_t>(127);
+    const RowPlan plan = plan_row_stats(rows, static_cast<int>(vocab), sms, scratch);
     if (!plan.team) return DRS_ERR_UNSUPPORTED;
+    // per-team row counts are int
+    if ((rows + plan.num_teams - 1) / plan.num_teams > INT_MAX / 2) return DRS_ERR_UNSUPPORTED;
 
     RowStatsParams prm{};
     prm.logits = logits;
@@ -564,38 +691,38 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
     prm.entropy = entropy;
     prm.probs = probs;
     prm.probs_row_stride = probs_row_stride;
-    prm.xchg = static_cast<Partial*>(workspace);
+    prm.xchg = workspace;
     prm.err = device_error_flag();
-    prm.key = PhiloxKey{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)};
-    prm.generation = next_generation();
+    prm.rk = PhiloxRoundKeys::of(seed);
     prm.vocab = static_cast<int32_t>(vocab);
     prm.team = plan.team;
     prm.chunk = plan.chunk;
     prm.num_teams = plan.num_teams;
     prm.probs_dtype = static_cast<int32_t>(probs_dtype);
     prm.probs_vec = probs && aligned(probs, 8) && (probs_row_stride % 4 == 0);
+    prm.index32 = (row0 + rows <= static_cast<int64_t>(UINT32_MAX)) &&
+                  (canvas_len <= static_cast<int64_t>(UINT32_MAX));
     prm.fault = g_inject_fault.exchange(0);
     if (!prm.err) return DRS_ERR_CUDA;
 
     // Shared memory: stages of one chunk each (filled by bulk copies when
     // rows start 16-byte aligned; in every case they keep a row's scaled
-    // logits until its finalisation) plus the reduction scratch, within the
-    // per-CTA share of the SM. Three stages: the row being computed, the row
-    // waiting for the team, the row being loaded.
+    // logits until its finalisation) plus the scratch. Four stages when they
+    // fit: the row being finalised, the row being computed, two rows loading.
     const bool tma = aligned(logits, 16) && (row_stride % 4 == 0);
-    const size_t scratch = (sizeof(Scratch) + 127) & ~static_cast<size_t>(127);
-    const size_t smem_limit = smem_per_cta(plan.ctas_per_sm);
     prm.stage_bytes = (plan.chunk * 4 + 127) & ~127;
-    int ns = static_cast<int>((smem_limit - scratch) / prm.stage_bytes);
+    int ns = static_cast<int>((kSmemPerCta - scratch) / prm.stage_bytes);
     if (ns > kMaxStages) ns = kMaxStages;
     if (ns < 3) return DRS_ERR_UNSUPPORTED;
     prm.nstage = ns;
     prm.use_tma = tma ? 1 : 0;
     const size_t smem = static_cast<size_t>(prm.nstage) * prm.stage_bytes + scratch;
     const int grid = plan.team * plan.num_teams;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return plan.vec4 == 4 ? launch_row_stats<4>(prm, grid, smem, st)
-                          : launch_row_stats<8>(prm, grid, smem, st);
+    // Zero the records this launch uses: a zero tag matches no row.
+    if (cudaMemsetAsync(workspace, 0, static_cast<size_t>(grid) * kXchgPerCta,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DRS_ERR_CUDA;
+    return launch_row_stats(prm, grid, smem, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -612,7 +739,7 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
 
 namespace {
 
-constexpr size_t kNoallocWorkspaceBytes = static_cast<size_t>(1024) * drs::kRing * sizeof(drs::Partial);
+constexpr size_t kNoallocWorkspaceBytes = static_cast<size_t>(1024) * drs::kXchgPerCta;
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoallocWorkspaceBytes];
 
 std::mutex g_noalloc_mutex;
