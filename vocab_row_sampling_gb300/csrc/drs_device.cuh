@@ -5,6 +5,7 @@
 // partial results.
 #pragma once
 
+#include <climits>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -213,15 +214,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // --------------------------------------------------------- reductions
 
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 
 __device__ __forceinline__ int warp_min_i(int v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    int r;
+    asm volatile("redux.sync.min.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
 }
 
 __device__ __forceinline__ double warp_sum_d(double v) {
@@ -236,16 +237,27 @@ __device__ __forceinline__ bool beats(float s, int c, float bs, int bc) {
     return s > bs || (s == bs && c < bc);
 }
 
+// Warp-wide reductions in one instruction each (redux.sync): max of floats
+// (NaN inputs ignored), min of non-negative ints.
+__device__ __forceinline__ float warp_max_f(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ int warp_min_nonneg(int v) {
+    uint32_t r;
+    asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(static_cast<uint32_t>(v)));
+    return static_cast<int>(r);
+}
+
+// The best (score, column) of the warp, on every lane: the largest score,
+// then the lowest column among the lanes holding it. Scores are finite or
+// -inf (never NaN).
 __device__ __forceinline__ void warp_best(float& s, int& c) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, s, o);
-        const int oc = __shfl_xor_sync(0xffffffffu, c, o);
-        if (beats(os, oc, s, c)) {
-            s = os;
-            c = oc;
-        }
-    }
+    const float top = warp_max_f(s);
+    c = warp_min_nonneg(s == top ? c : INT_MAX);
+    s = top;
 }
 
 // ------------------------------------------------------ row exchange

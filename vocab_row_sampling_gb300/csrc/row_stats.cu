@@ -245,7 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (issued < nrows && issued < nstage) issue_copy();
     }
 
-    // The temperature of the next row, loaded one iteration ahead.
+    // The temperature of the next row, loaded one iteration ahead (compute
+    // warps: the row about to be computed; exchange warp: the row about to
+    // be merged).
     float temp_next = 0.0f;
     if (nrows > 0) temp_next = row_temperature(p, static_cast<uint64_t>(p.row0 + row_of(0)));
 
@@ -401,7 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float w_tot = warp_sum_f(w_l);
                 const int arg_row = warp_min_i(m == big_m ? a_m : INT_MAX);
                 warp_best(b_m, bc_m);
-                const bool noisy = row_temperature(p, static_cast<uint64_t>(p.row0 + frow)) > 0.0f;
+                const bool noisy = temp_next > 0.0f;  // row k-1's, loaded an iteration ago
+                if (k < nrows)
+                    temp_next = row_temperature(p, static_cast<uint64_t>(p.row0 + row_of(k)));
                 if (lane == 0) {
                     RowInfo& ri = sc.info[kf & (kInfoRing - 1)];
                     ri.row_max = big_m;
@@ -522,7 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pass[j] = (i0 + j) * kCompute < nslot4 && max4(v[i0 + j]) > floor_score;
                         any |= pass[j];
                     }
-                    if (any) {
+                    // warp-uniform: when any lane needs this quad, every lane
+                    // draws its four blocks (straight-line, no divergence)
+                    if (__any_sync(0xffffffffu, any)) {
                         uint4 w[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
