@@ -14,6 +14,8 @@ through the public API from pinned host buffers, copies included;
 `cpu_baseline` times the CPU oracle on a bounded sample of the same rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --rows 256 --no-e2e --cpu-seconds 0   (a smaller case of
+      the same workload, e.g. for a counter capture; not a headline number)
 Under torchrun each rank runs its own batch (weak scaling, rows keyed by
 global row index so results equal one big batch); no collective touches
 the data path.
@@ -151,8 +153,8 @@ def _clocks_rejected(c):
 
 # ---------------------------------------------------------------- our arm
 
-def _make_batch(rank: int):
-    w = workloads.make(WORKLOAD, device="cuda", data_seed=rank)
+def _make_batch(rank: int, rows=None):
+    w = workloads.make(WORKLOAD, device="cuda", data_seed=rank, rows=rows)
     return w
 
 
@@ -177,7 +179,7 @@ def _run_ours(args, world, rank, local):
     import vocab_row_sampling_gb300 as drs
     drs.load(build_if_missing=True)
     torch.cuda.set_device(local)
-    w = _make_batch(rank)
+    w = _make_batch(rank, args.rows)
     rows, V, stride = w["rows"], w["vocab"], w["row_stride"]
     logits = w["logits"][:, :V]
     temps, keep = w["temps"].cuda(), w["keep"].cuda()
@@ -274,8 +276,13 @@ def _run_ours(args, world, rank, local):
            "clocks": clocks}
 
     # end to end through the public API from pinned host memory
-    out["e2e"] = _e2e(args, drs, w, rank, world, row0, temps_all, keep, k)
-    if rank == 0 and world == 1:
+    if not args.no_e2e:
+        out["e2e"] = _e2e(args, drs, w, rank, world, row0, temps_all, keep, k)
+    if rows != workloads.WORKLOADS[WORKLOAD].rows:
+        out["config"]["workload"] = (f"step recipe at {rows} x {V} (a smaller case, "
+                                     "not the headline workload)")
+        out["config"]["l2"] = "no flush"
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
         out["cpu_baseline"] = _cpu_baseline(logits, w, seconds=args.cpu_seconds)
     del logits, probs
     return out
@@ -438,6 +445,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--rows", type=int, default=None,
+                    help="rows per GPU (multiple of the canvas length); default: the full batch")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     if args.impl == "reference":
