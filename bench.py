@@ -245,7 +245,7 @@ def _run_ours(args, world, rank, local):
     rs_avg_ms = sum(rs_ms) / len(rs_ms)
     tk_avg_ms = sum(tk_ms) / len(tk_ms)
     bytes_rs = rows * stride * 4 + rows * V * 2
-    kept_rows = int(keep.sum().item()) * w["canvas_len"]
+    kept_rows = int(keep[: rows // w["canvas_len"]].sum().item()) * w["canvas_len"]
     bytes_tk = kept_rows * V * 4
     peak, peak_kind = _peak_hbm()
     achieved = bytes_rs / (rs_avg_ms / 1e3) / 1e9

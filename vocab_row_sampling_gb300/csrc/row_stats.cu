@@ -14,9 +14,9 @@
 // Iteration k, before its one CTA barrier:
 //   compute warps, row k: wait for the bulk copy (TMA) that staged the
 //     chunk rows ahead; s = x / max(T, 1e-10), the IEEE fp32 quotient
-//     (ScaledQuotient), written back into the stage; warp max M_w,
-//     lowest-column argmax, S_w = sum e^(s - M_w), W_w = sum e^(s - M_w)
-//     (s - M_w) (the "online max and sum" of the page); the elements within
+//     (ScaledQuotient); warp max M_w, lowest-column argmax, e = e^(s - M_w)
+//     (written back into the stage), S_w = sum e, W_w = sum e (s - M_w)
+//     (the "online max and sum" of the page); the elements within
 //     kNearTop of M_w scored exactly in the Gumbel-max race (T > 0): score =
 //     s + g, g from Philox keyed by (seed, row, column). The warp's partial
 //     goes to shared memory.
@@ -28,11 +28,11 @@
 //   exchange warp: combines the warp partials of row k into the CTA's first
 //     record and those of row k-2's race into its second record, publishes
 //     both (release), and issues the bulk copy of a later row.
-//   compute warps, row k-1, read back from its stage: the pruned race with
-//     the row's global near-top best B (an element can only win if
-//     s > B - 16.64, and then only if 1 - u <= -log u allows it; the few
-//     survivors are scored exactly), then its probabilities
-//     e^(s - M - log S), rounded to nearest even and written to HBM.
+//   compute warps, row k-1, its e read back from the stage: the pruned race
+//     with the row's global near-top best B (an element can only win if
+//     1 - u <= -log u <= e^(s - B) = e * e^(M_w - B); the few survivors are
+//     rescored exactly from their logits), then its probabilities
+//     e * e^(M_w - M) / S, rounded to nearest even and written to HBM.
 //
 // HBM traffic: every logit is read once (by the bulk copy) and every
 // probability written once. No fp64 arithmetic (its rate on GB300 is a
@@ -177,23 +177,45 @@ __device__ __forceinline__ void race_exact8(const float4 (&v)[kVec4], uint32_t m
     }
 }
 
-// Elements of one float4 group that could still beat `best`: 1 - u (a lower
-// bound of -log u) must be at most e^(x - best), widened by the margin. The
-// group is first tested as a whole with its largest x and largest word.
-__device__ __forceinline__ uint32_t race_group(const float4& g, uint4 w, float best,
-                                               float floor_score) {
+// Elements of one float4 group that could still beat the row's best score
+// B: winning needs -log u <= e^(s - B), so 1 - u (a lower bound of -log u)
+// must be at most e^(s - B) = e * r_w (widened by the margin), with e =
+// e^(s - M_w) from the stage. The group is first tested as a whole with its
+// largest e and largest word.
+__device__ __forceinline__ uint32_t race_group(const float4& e, uint4 w, float r_w) {
     const uint32_t wmax = max(max(w.x, w.y), max(w.z, w.w));
-    const float lim_g = ex2_approx(fmaf(max4(g) - best, kLog2e, kRaceMarginLog2));
     uint32_t bits = 0;
-    if (one_minus_u_lower(wmax) <= lim_g) {
+    if (one_minus_u_lower(wmax) <= max4(e) * r_w) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float x = comp(g, q);
-            const float lim = ex2_approx(fmaf(x - best, kLog2e, kRaceMarginLog2));
-            if (x > floor_score && one_minus_u_lower(word_of(w, q)) <= lim) bits |= 1u << q;
-        }
+        for (int q = 0; q < 4; ++q)
+            if (one_minus_u_lower(word_of(w, q)) <= comp(e, q) * r_w) bits |= 1u << q;
     }
     return bits;
+}
+
+// Score the survivors of `mask` exactly: s = x / max(T, 1e-10) from the
+// logit in global memory (the stage holds e only), g from the element's
+// Philox word; keep the best (score, column). The column that set the best
+// already was scored the same way.
+__device__ __noinline__ void race_rescore(uint32_t mask, const float* row_logits, float temp,
+                                          int col0, int tid, uint64_t grow_id,
+                                          const PhiloxRoundKeys& rk, int near_col, float& bs,
+                                          int& bc) {
+    const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
+    while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int f = (b >> 2) * kCompute + tid;
+        const int c = col0 + 4 * f + (b & 3);
+        if (c == near_col) continue;
+        const float s = sq.exact(__ldg(row_logits + c));
+        const uint4 w = noise_words_rk(rk, grow_id, static_cast<uint32_t>((col0 >> 2) + f));
+        const float score = s + gumbel_of_bits(word_of(w, b & 3));
+        if (beats(score, c, bs, bc)) {
+            bs = score;
+            bc = c;
+        }
+    }
 }
 
 }  // namespace
@@ -251,12 +273,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float temp_next = 0.0f;
     if (nrows > 0) temp_next = row_temperature(p, static_cast<uint64_t>(p.row0 + row_of(0)));
 
+    // Carried from a row's first half to its second, one iteration later:
+    // the warp max (the reference of the stored e) and the temperature.
+    float mw_row = -INFINITY, mw_prev = -INFINITY;
+    float temp_row = 0.0f, temp_prev = 0.0f;
+
     bool aborted = false;
     int consumed = 0;
     for (int k = 0; k <= nrows + 2; ++k) {
         const int par = k & 1;
         // ===================== before the barrier ===============================
         if (!exchange) {
+            mw_prev = mw_row;
+            temp_prev = temp_row;
             if (k < nrows) {
                 // ---- compute warps: row k ---------------------------------------
                 const int64_t row = row_of(k);
@@ -265,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = k % nstage;
                 float4* stage4 = reinterpret_cast<float4*>(smem + s * p.stage_bytes);
                 const float temp = temp_next;
+                temp_row = temp;
                 if (k + 1 < nrows)
                     temp_next = row_temperature(p, static_cast<uint64_t>(p.row0 + row_of(k + 1)));
 
@@ -322,13 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mw = warp_max(mt);
                 }
-                // The scaled logits wait in the stage for the race and the
-                // probabilities of the next iteration.
-#pragma unroll
-                for (int i = 0; i < kVec4; ++i) {
-                    const int f = i * kCompute + tid;
-                    if (i * kCompute < nslot4 && f < nslot4) stage4[f] = v[i];
-                }
+                mw_row = mw;
 
                 // argmax and near-top elements: threads near the warp max only
                 const float near = mw - kNearTop;
@@ -345,18 +369,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (x >= near) near_mask |= 1u << (4 * i + q);
                         }
                 }
-                // sums, four accumulators each
+                // sums, four accumulators each; e = e^(s - M_w) waits in the
+                // stage for the race and the probabilities of the next
+                // iteration (the scaled logits themselves are not needed
+                // again but for the rare exact rescoring).
                 float st[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int i = 0; i < kVec4; ++i) {
                     if (i * kCompute < nslot4) {
+                        float4 ev;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float d = fmaxf(comp(v[i], q) - mw, -1e30f);  // -inf, NaN -> 0
                             const float e = ex2_approx(d * kLog2e);
+                            set_comp(ev, q, e);
                             st[q] += e;
                             wt[q] = fmaf(e, d, wt[q]);
                         }
+                        const int f = i * kCompute + tid;
+                        if (f < nslot4) stage4[f] = ev;
                     }
                 }
                 float bs = -INFINITY;
@@ -502,17 +533,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t fgrow_id = static_cast<uint64_t>(p.row0 + frow);
             const float4* fstage =
                 reinterpret_cast<const float4*>(smem + (kf % nstage) * p.stage_bytes);
-            float4 v[kVec4];
+            // e = e^(s - M_w) of row k-1, M_w = mw_prev the warp's max
+            float4 e[kVec4];
 #pragma unroll
             for (int i = 0; i < kVec4; ++i) {
                 const int f = i * kCompute + tid;
-                v[i] = (i * kCompute < nslot4 && f < nslot4)
-                           ? fstage[f]
-                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                e[i] = (i * kCompute < nslot4 && f < nslot4) ? fstage[f]
+                                                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
             if (ri.noisy) {
                 const float best = ri.near_best;
-                const float floor_score = best - kGumbelMax;
+                // e^(s - best), widened by the race margin, is e * r_w.
+                const float r_w = mw_prev == -INFINITY
+                                      ? 0.0f
+                                      : ex2_approx(fmaf(mw_prev - best, kLog2e, kRaceMarginLog2));
                 float bs = best;
                 int bc = ri.near_col;
                 uint32_t survivors = 0;
@@ -523,7 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bool any = false;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        pass[j] = (i0 + j) * kCompute < nslot4 && max4(v[i0 + j]) > floor_score;
+                        // 1 - u >= 2^-24 always: below that bound no element of
+                        // the group can win
+                        pass[j] = (i0 + j) * kCompute < nslot4 && max4(e[i0 + j]) * r_w >= 0x1p-24f;
                         any |= pass[j];
                     }
                     // warp-uniform: when any lane needs this quad, every lane
@@ -538,11 +574,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             if (pass[j])
-                                survivors |= race_group(v[i0 + j], w[j], best, floor_score)
-                                             << (4 * (i0 + j));
+                                survivors |= race_group(e[i0 + j], w[j], r_w) << (4 * (i0 + j));
                     }
                 }
-                if (survivors) race_exact8(v, survivors, col0, tid, fgrow_id, p.rk, bs, bc);
+                if (survivors)
+                    race_rescore(survivors, p.logits + frow * p.row_stride, temp_prev, col0, tid,
+                                 fgrow_id, p.rk, ri.near_col, bs, bc);
                 warp_best(bs, bc);
                 if (lane == 0) sc.p2[kf & 1][warp] = WarpBest{bs, bc};
             } else if (lane == 0) {
@@ -551,21 +588,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (p.probs_dtype != 0) {
                 const float big_m = ri.row_max;
-                const float l2s = ri.log2s;
+                // e^(s - M) / S = e * e^(M_w - M) / S
+                const float f_w = mw_prev == -INFINITY
+                                      ? 0.0f
+                                      : ex2_approx(fmaf(mw_prev - big_m, kLog2e, -ri.log2s));
                 const bool bf16 = p.probs_dtype == 1;
                 uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
 #pragma unroll
                 for (int i = 0; i < kVec4; ++i) {
                     const int f = i * kCompute + tid;
                     if (i * kCompute >= nslot4 || f >= nslot4) continue;
-                    float pr[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        // e^(s - M - log S) = 2^((s - M) log2 e - log2 S); -inf
-                        // columns (and the NaN quotient of -inf) clamp to 0.
-                        const float t = fmaxf(fmaf(comp(v[i], q) - big_m, kLog2e, -l2s), -256.0f);
-                        pr[q] = ex2_approx(t);
-                    }
+                    float pr[4] = {e[i].x * f_w, e[i].y * f_w, e[i].z * f_w, e[i].w * f_w};
                     if (big_m == -INFINITY) pr[0] = pr[1] = pr[2] = pr[3] = NAN;
                     const uint32_t lo = pack2(pr[0], pr[1], bf16);
                     const uint32_t hi = pack2(pr[2], pr[3], bf16);
