@@ -107,13 +107,32 @@ def test_repeated_calls_are_deterministic():
             assert np.array_equal(one[k], again[k]), k
 
 
-def test_max_vocab():
+@pytest.mark.parametrize("which", ["four stages", "max"])
+def test_long_rows(which):
+    """Rows too long for the two-iteration lag: 400000 columns take the
+    four-stage form, the largest supported vocabulary the three-stage one."""
     import vocab_row_sampling_gb300 as drs
-    vocab = drs.DRS_MAX_VOCAB
+    vocab = 400000 if which == "four stages" else drs.DRS_MAX_VOCAB
     rng = np.random.default_rng(1)
     x = (rng.standard_normal((3, vocab)) * 3).astype(np.float32)
     x[2, vocab - 1] = 40.0
-    _compare(_dev(x), np.array([0.9, 0.0, 1.1], np.float32), 1, 5, BF16, where="max vocab")
+    _compare(_dev(x), np.array([0.9, 0.0, 1.1], np.float32), 1, 5, BF16, where=which)
+
+
+def test_raw_and_exact_domains_in_one_row():
+    """Scaled logits around the magnitude 256 at which a warp switches from
+    working on the raw logits to dividing every logit exactly: the warps of
+    one row then mix both, with probabilities far from negligible."""
+    rng = np.random.default_rng(5)
+    rows, vocab = 8, 70001
+    x = (250.0 + rng.random((rows, vocab)) * 12.0).astype(np.float32)
+    x[1] = -x[1]                                   # negative side of the switch
+    x[2, ::7] = 256.0                              # ties at the switch itself
+    x[3] = (rng.standard_normal(vocab) * 3).astype(np.float32)
+    x[3, 40000:] += 255.0                          # half raw, half exact
+    temps = np.array([1.0, 1.0, 0.999, 1.001, 1.0, 0.5, 1.0, 2.0], np.float32)
+    for seed in (3, 4):
+        _compare(_dev(x), temps, 1, seed, BF16, where=f"domains seed {seed}")
 
 
 # ------------------------------------------------------------- full sizes

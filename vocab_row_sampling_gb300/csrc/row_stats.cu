@@ -8,30 +8,38 @@
 // chunks of every row of the team; teams take rows round robin. The kernel
 // is persistent: one CTA per SM, cooperative launch (all CTAs resident, so
 // their bounded waits on each other cannot deadlock). A CTA has 15 compute
-// warps (480 threads, up to 32 logits each in registers: float4 slot i of
-// thread t covers chunk columns 4*(i*480+t)+0..3) and one exchange warp.
+// warps (480 threads, VEC4 float4 slots each: slot i of thread t covers
+// chunk columns 4*(i*480+t)+0..3) and one exchange warp.
 //
+// A row is handled in two halves LAG iterations apart, so that the team's
+// exchange of the first half's results (a round trip through L2 that takes
+// about as long as one iteration's compute) overlaps LAG iterations of work.
 // Iteration k, before its one CTA barrier:
-//   compute warps, row k: wait for the bulk copy (TMA) that staged the
-//     chunk rows ahead; s = x / max(T, 1e-10), the IEEE fp32 quotient
-//     (ScaledQuotient); warp max M_w, lowest-column argmax, e = e^(s - M_w)
-//     (written back into the stage), S_w = sum e, W_w = sum e (s - M_w)
-//     (the "online max and sum" of the page); the elements within
-//     kNearTop of M_w scored exactly in the Gumbel-max race (T > 0): score =
-//     s + g, g from Philox keyed by (seed, row, column). The warp's partial
-//     goes to shared memory.
-//   exchange warp: merges the team's first records of row k-1 (M, S, W,
-//     argmax, near-top best B) and its second records of row k-3 (the best
-//     of the pruned race); member 0 writes argmax and entropy of row k-1 and
-//     the sample of row k-3.
+//   compute warps, first half of row k: wait for the bulk copy (TMA) that
+//     staged the chunk iterations ahead; the warp max M_w of the scaled
+//     logits s = x / Te (Te = max(T, 1e-10)) and the lowest column reaching
+//     it (the argmax), e = e^(s - M_w) written back into the stage,
+//     S_w = sum e and W_w = sum e (s - M_w) (the "online max and sum" of the
+//     page), and for T > 0 the Gumbel-max score of the warp's argmax
+//     element (a lower bound B of the row's best score). Division by Te > 0
+//     is monotone, so while |M_w| < 256 the warp works on the raw logits:
+//     the max is found among them, only the few candidates for the argmax
+//     are divided (exactly), and e = 2^((x - x_max) log2(e) / Te) is within
+//     a relative 2^-15 of e^(s - M_w). Warps with larger scaled values
+//     divide every logit exactly first.
+//   exchange warp: merges the team's first records of row k-LAG (M, S, W,
+//     argmax, B) and its second records of row k-2LAG-1 (the race best);
+//     member 0 writes argmax and entropy of row k-LAG and the sample of row
+//     k-2LAG-1.
 // After the barrier:
 //   exchange warp: combines the warp partials of row k into the CTA's first
-//     record and those of row k-2's race into its second record, publishes
-//     both (release), and issues the bulk copy of a later row.
-//   compute warps, row k-1, its e read back from the stage: the pruned race
-//     with the row's global near-top best B (an element can only win if
+//     record and those of row k-LAG-1's race into its second record,
+//     publishes both, and issues the bulk copy of a later row into the stage
+//     row k-LAG-1 left.
+//   compute warps, second half of row k-LAG, its e read back from the
+//     stage: the pruned race against the row's B (an element can only win if
 //     1 - u <= -log u <= e^(s - B) = e * e^(M_w - B); the few survivors are
-//     rescored exactly from their logits), then its probabilities
+//     rescored exactly from their logits), then the probabilities
 //     e * e^(M_w - M) / S, rounded to nearest even and written to HBM.
 //
 // HBM traffic: every logit is read once (by the bulk copy) and every
@@ -52,18 +60,27 @@ namespace drs {
 
 namespace {
 
-constexpr int kComputeWarps = kWarps - 1;          // warps 0..14
-constexpr int kCompute = kComputeWarps * 32;       // 480 compute threads
-constexpr int kExchangeWarp = kWarps - 1;          // warp 15
-constexpr int kVec4 = 8;                           // float4 slots per compute thread
-constexpr int kRowChunkCap = kCompute * kVec4 * 4; // 15360 columns per CTA
-constexpr int kMaxStages = 4;
-constexpr int kInfoRing = 4;
-constexpr float kNearTop = 2.0f;  // window below the warp max scored exactly first
+constexpr int kComputeWarps = kWarps - 1;     // warps 0..14
+constexpr int kCompute = kComputeWarps * 32;  // 480 compute threads
+constexpr int kExchangeWarp = kWarps - 1;     // warp 15
+constexpr int kInfoRing = 8;                  // merged rows kept, by row % 8
+// Three forms: LAG 2 with 5 stages of up to 6 float4 per thread (rows up to
+// 32 * 11520 columns), LAG 1 with 4 stages of up to 8, and LAG 1 with 3
+// stages (up to 32 * 15360 columns; the bulk copy then has only part of an
+// iteration to land).
+constexpr int kVec4Lag2 = 6;
+constexpr int kVec4Lag1 = 8;
+constexpr int kMaxStages = 5;
+// The ring of exchange records must outlast 2 * LAG + 2 iterations.
+static_assert(kRing >= 2 * 2 + 2, "exchange ring too short for LAG 2");
 
-// log2(1.0001): the race's bound e^(s - best) is widened by 1e-4 so that
-// rounding in it never prunes an element whose fp32 score could win.
-constexpr float kRaceMarginLog2 = 1.4426229e-4f;
+// log2(1.0002): the race's bound e^(s - best) is widened by 2e-4 so that
+// rounding in it (at most a relative 2^-15 for e taken from the raw
+// logits) never prunes an element whose fp32 score could win.
+constexpr float kRaceMarginLog2 = 2.8851e-4f;
+// Warps whose largest scaled logit is below this in magnitude work on the
+// raw logits (see above).
+constexpr float kRawDomainLimit = 256.0f;
 
 struct RowStatsParams {
     const float* logits;
@@ -78,14 +95,13 @@ struct RowStatsParams {
     void* probs;
     int64_t probs_row_stride;
     void* xchg;         // records: per CTA, kRing A slots (M, S, W, argmax,
-                        // near-top best) and kRing B slots (race best)
+                        // B) and kRing B slots (race best)
     int* err;
     PhiloxRoundKeys rk;
     int32_t vocab;
     int32_t team;       // CTAs per row
     int32_t chunk;      // columns per CTA (multiple of 4)
     int32_t num_teams;
-    int32_t nstage;     // shared-memory stages, one chunk each (3 or 4)
     int32_t stage_bytes;
     int32_t use_tma;    // stages filled by bulk copies (rows 16-byte aligned)
     int32_t probs_dtype;
@@ -112,7 +128,7 @@ struct WarpBest {
 struct RowInfo {
     float row_max;
     float log2s;
-    float near_best;  // best near-top score of the whole row
+    float near_best;  // B: the best score among the warps' argmax elements
     int near_col;
     int arg;
     int noisy;
@@ -120,11 +136,12 @@ struct RowInfo {
 
 struct Scratch {
     uint64_t full[kMaxStages];
-    WarpPartial p1[2][kComputeWarps];  // row k's warp partials, by row parity
-    WarpBest p2[2][kComputeWarps];     // row k's race bests, by row parity
-    RowInfo info[kInfoRing];           // merged rows, by row % 4
-    int status;                        // a merge ran out of time
-    int abort_load;                    // a bulk copy ran out of time
+    WarpPartial p1[2][kComputeWarps];      // row k's warp partials, by row parity
+    WarpBest p2[2][kComputeWarps];         // row j's race bests, by row parity
+    RowInfo info[kInfoRing];               // merged rows
+    float wref[kInfoRing][kComputeWarps];  // each warp's M_w, by row % 8
+    int status;                            // a merge ran out of time
+    int abort_load;                        // a bulk copy ran out of time
 };
 
 __device__ __forceinline__ void set_comp(float4& v, int q, float x) {
@@ -157,26 +174,6 @@ __device__ __forceinline__ float row_temperature(const RowStatsParams& p, uint64
 // before each launch).
 __device__ __forceinline__ uint32_t record_tag(int k) { return static_cast<uint32_t>(k) + 1u; }
 
-// Score the elements of `mask` exactly and keep the best (score, column).
-__device__ __forceinline__ void race_exact8(const float4 (&v)[kVec4], uint32_t mask, int col0,
-                                            int tid, uint64_t grow_id,
-                                            const PhiloxRoundKeys& rk, float& bs, int& bc) {
-#pragma unroll 1
-    while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int f = (b >> 2) * kCompute + tid;
-        const float x = pick(v, b);
-        const uint4 w = noise_words_rk(rk, grow_id, static_cast<uint32_t>((col0 >> 2) + f));
-        const float score = x + gumbel_of_bits(word_of(w, b & 3));
-        const int c = col0 + 4 * f + (b & 3);
-        if (beats(score, c, bs, bc)) {
-            bs = score;
-            bc = c;
-        }
-    }
-}
-
 // Elements of one float4 group that could still beat the row's best score
 // B: winning needs -log u <= e^(s - B), so 1 - u (a lower bound of -log u)
 // must be at most e^(s - B) = e * r_w (widened by the margin), with e =
@@ -193,39 +190,38 @@ __device__ __forceinline__ uint32_t race_group(const float4& e, uint4 w, float r
     return bits;
 }
 
-// Score the survivors of `mask` exactly: s = x / max(T, 1e-10) from the
-// logit in global memory (the stage holds e only), g from the element's
-// Philox word; keep the best (score, column). The column that set the best
-// already was scored the same way.
-__device__ __noinline__ void race_rescore(uint32_t mask, const float* row_logits, float temp,
-                                          int col0, int tid, uint64_t grow_id,
-                                          const PhiloxRoundKeys& rk, int near_col, float& bs,
-                                          int& bc) {
+// Score the survivors of `mask` (bit 4i+q: slot i, component q) exactly:
+// s = x / max(T, 1e-10) from the logit in global memory (the stage holds e
+// only), g from the element's Philox word; keep the best (score, column).
+// The column that set the best already was scored the same way.
+__device__ __noinline__ WarpBest race_rescore(uint32_t mask, const float* row_logits, float temp,
+                                              int col0, int tid, uint64_t grow_id,
+                                              const PhiloxRoundKeys& rk, WarpBest best) {
     const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
     while (mask) {
         const int b = __ffs(mask) - 1;
         mask &= mask - 1;
         const int f = (b >> 2) * kCompute + tid;
         const int c = col0 + 4 * f + (b & 3);
-        if (c == near_col) continue;
+        if (c == best.col) continue;
         const float s = sq.exact(__ldg(row_logits + c));
         const uint4 w = noise_words_rk(rk, grow_id, static_cast<uint32_t>((col0 >> 2) + f));
         const float score = s + gumbel_of_bits(word_of(w, b & 3));
-        if (beats(score, c, bs, bc)) {
-            bs = score;
-            bc = c;
-        }
+        if (beats(score, c, best.best, best.col)) best = WarpBest{score, c};
     }
+    return best;
 }
 
 }  // namespace
 
+template <int VEC4, int LAG, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, 1)
     row_stats_kernel(const __grid_constant__ RowStatsParams p) {
+    constexpr int kStages = NSTAGE;  // LAG + 1 rows held, the rest loading
+    static_assert(kStages <= kMaxStages && kStages >= LAG + 2, "stages");
     extern __shared__ __align__(128) unsigned char smem[];
-    Scratch& sc = *reinterpret_cast<Scratch*>(smem + p.nstage * p.stage_bytes);
+    Scratch& sc = *reinterpret_cast<Scratch*>(smem + kStages * p.stage_bytes);
     const bool use_tma = p.use_tma != 0;
-    const int nstage = p.nstage;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -242,10 +238,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                           ? static_cast<int>((p.rows - 1 - team_id) / p.num_teams + 1)
                           : 0;
     auto row_of = [&](int k) { return team_id + static_cast<int64_t>(k) * p.num_teams; };
+    auto grow_of = [&](int k) { return static_cast<uint64_t>(p.row0 + row_of(k)); };
 
     if (tid == 0) {
         if (use_tma) {
-            for (int s = 0; s < nstage; ++s) mbar_init(&sc.full[s], 1);
+            for (int s = 0; s < kStages; ++s) mbar_init(&sc.full[s], 1);
             fence_barrier_init();
         }
         sc.abort_load = 0;
@@ -256,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Producer state, exchange-warp lane 0: rows issued to the stages.
     int issued = 0;
     auto issue_copy = [&]() {
-        const int s = issued % nstage;
+        const int s = issued % kStages;
         mbar_arrive_expect_tx(&sc.full[s], copy_bytes);
         if (copy_bytes)
             tma_load_1d(smem + s * p.stage_bytes, p.logits + row_of(issued) * p.row_stride + col0,
@@ -264,48 +261,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
     };
     if (use_tma && exchange && lane == 0) {
-        while (issued < nrows && issued < nstage) issue_copy();
+        while (issued < nrows && issued < kStages) issue_copy();
     }
 
-    // The temperature of the next row, loaded one iteration ahead (compute
-    // warps: the row about to be computed; exchange warp: the row about to
-    // be merged).
+    // Compute warps: the temperature of the next row, loaded an iteration
+    // ahead.
     float temp_next = 0.0f;
-    if (nrows > 0) temp_next = row_temperature(p, static_cast<uint64_t>(p.row0 + row_of(0)));
-
-    // Carried from a row's first half to its second, one iteration later:
-    // the warp max (the reference of the stored e) and the temperature.
-    float mw_row = -INFINITY, mw_prev = -INFINITY;
-    float temp_row = 0.0f, temp_prev = 0.0f;
+    if (nrows > 0 && !exchange) temp_next = row_temperature(p, grow_of(0));
 
     bool aborted = false;
     int consumed = 0;
-    for (int k = 0; k <= nrows + 2; ++k) {
+    for (int k = 0; k <= nrows + 2 * LAG; ++k) {
         const int par = k & 1;
         // ===================== before the barrier ===============================
         if (!exchange) {
-            mw_prev = mw_row;
-            temp_prev = temp_row;
             if (k < nrows) {
-                // ---- compute warps: row k ---------------------------------------
+                // ---- compute warps: first half of row k -------------------------
                 const int64_t row = row_of(k);
-                const uint64_t grow_id = static_cast<uint64_t>(p.row0 + row);  // global row
+                const uint64_t grow_id = grow_of(k);
                 const float* grow = p.logits + row * p.row_stride + col0;
-                const int s = k % nstage;
+                const int s = k % kStages;
                 float4* stage4 = reinterpret_cast<float4*>(smem + s * p.stage_bytes);
                 const float temp = temp_next;
-                temp_row = temp;
-                if (k + 1 < nrows)
-                    temp_next = row_temperature(p, static_cast<uint64_t>(p.row0 + row_of(k + 1)));
+                if (k + 1 < nrows) temp_next = row_temperature(p, grow_of(k + 1));
 
                 bool timed_out = false;
                 if (use_tma)
                     timed_out =
-                        !mbar_wait_bounded(&sc.full[s], static_cast<uint32_t>((k / nstage) & 1));
+                        !mbar_wait_bounded(&sc.full[s], static_cast<uint32_t>((k / kStages) & 1));
                 if (timed_out) sc.abort_load = 1;
-                float4 v[kVec4];
+                float4 v[VEC4];
 #pragma unroll
-                for (int i = 0; i < kVec4; ++i) {
+                for (int i = 0; i < VEC4; ++i) {
                     const int f = i * kCompute + tid;
                     float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                     if (i * kCompute < nslot4) {  // CTA-uniform: slot i holds columns
@@ -325,63 +312,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v[i] = x;
                 }
 
-                const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
+                const float te = fmaxf(temp, kTempFloor);
+                const ScaledQuotient sq = ScaledQuotient::of(te);
                 const bool noisy = temp > 0.0f;
-                sq.apply<kVec4, kCompute>(v, nslot4);
 
-                float mt = fmaxf(fmaxf(fmaxf(max4(v[0]), max4(v[1])), fmaxf(max4(v[2]), max4(v[3]))),
-                                 fmaxf(fmaxf(max4(v[4]), max4(v[5])), fmaxf(max4(v[6]), max4(v[7]))));
-                float mw = warp_max(mt);
-                // Exactness guard: the corrected quotient is exact inside
-                // ScaledQuotient::fast_ok. A warp max outside it (zero,
-                // subnormal, huge, or from a tiny dividend) could decide the
-                // argmax among values that round differently, so that warp
-                // re-reads its logits and divides them exactly (rare).
-                if (sq.mode == ScaledQuotient::kDivide && mw != -INFINITY &&
-                    !ScaledQuotient::fast_ok(mw * sq.t, mw)) {
-                    mt = -INFINITY;
+                // max of the raw logits (division by te > 0 keeps the order)
+                float mt = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < kVec4; ++i) {
-                        const int f = i * kCompute + tid;
-                        if (i * kCompute < nslot4 && f < nslot4) {
+                for (int i = 0; i < VEC4; ++i) mt = fmaxf(mt, max4(v[i]));
+                const float mxw = warp_max(mt);
+                const float mw = mxw == -INFINITY ? -INFINITY : sq.exact(mxw);  // M_w
+                // warp-uniform: raw domain, or exact quotients first
+                const bool raw = !(fabsf(mw) >= kRawDomainLimit);
+                float ref, scale;  // d = (v - ref) * scale is s - M_w
+                float cthr;        // argmax candidates: v >= cthr
+                if (raw) {
+                    ref = mxw;
+                    scale = sq.y;
+                    // exact(x) == M_w needs x >= mxw - te * ulp(M_w)
+                    cthr = mxw - fmaxf(fabsf(mxw) * 0x1p-20f, te * 0x1p-140f);
+                } else {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                if (4 * f + q < ncols) set_comp(v[i], q, sq.exact(grow[4 * f + q]));
-                        }
-                        mt = fmaxf(mt, max4(v[i]));
+                    for (int i = 0; i < VEC4; ++i) {
+                        v[i].x = sq.exact(v[i].x);
+                        v[i].y = sq.exact(v[i].y);
+                        v[i].z = sq.exact(v[i].z);
+                        v[i].w = sq.exact(v[i].w);
                     }
-                    mw = warp_max(mt);
+                    mt = sq.exact(mt);
+                    ref = mw;
+                    scale = 1.0f;
+                    cthr = mw;
                 }
-                mw_row = mw;
 
-                // argmax and near-top elements: threads near the warp max only
-                const float near = mw - kNearTop;
+                // argmax: the lowest column whose exact quotient is M_w
                 int arg_t = INT_MAX;
-                uint32_t near_mask = 0;
-                if (mt >= near && mw != -INFINITY) {
+                if (mt >= cthr && mw != -INFINITY) {
+                    uint32_t cand = 0;  // bit 4i+q: columns in increasing order
 #pragma unroll
-                    for (int i = 0; i < kVec4; ++i)
+                    for (int i = 0; i < VEC4; ++i)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float x = comp(v[i], q);
-                            if (x == mw && arg_t == INT_MAX)
-                                arg_t = col0 + 4 * (i * kCompute + tid) + q;
-                            if (x >= near) near_mask |= 1u << (4 * i + q);
+                        for (int q = 0; q < 4; ++q)
+                            if (comp(v[i], q) >= cthr) cand |= 1u << (4 * i + q);
+#pragma unroll 1
+                    while (cand) {
+                        const int b = __ffs(cand) - 1;
+                        cand &= cand - 1;
+                        const float x = pick(v, b);
+                        if ((raw ? sq.exact(x) : x) == mw) {
+                            arg_t = col0 + 4 * ((b >> 2) * kCompute + tid) + (b & 3);
+                            break;
                         }
+                    }
                 }
+                const int aw = warp_min_i(arg_t);
+
                 // sums, four accumulators each; e = e^(s - M_w) waits in the
-                // stage for the race and the probabilities of the next
-                // iteration (the scaled logits themselves are not needed
-                // again but for the rare exact rescoring).
+                // stage for the race and the probabilities
+                const float lscale = kLog2e * scale;
                 float st[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int i = 0; i < kVec4; ++i) {
+                for (int i = 0; i < VEC4; ++i) {
                     if (i * kCompute < nslot4) {
                         float4 ev;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const float d = fmaxf(comp(v[i], q) - mw, -1e30f);  // -inf, NaN -> 0
-                            const float e = ex2_approx(d * kLog2e);
+                            // -inf -> a finite difference whose e is 0
+                            const float d = fmaxf(comp(v[i], q) - ref, -FLT_MAX);
+                            const float e = ex2_approx(d * lscale);
                             set_comp(ev, q, e);
                             st[q] += e;
                             wt[q] = fmaf(e, d, wt[q]);
@@ -390,32 +388,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (f < nslot4) stage4[f] = ev;
                     }
                 }
+                // B candidate: the Gumbel-max score of the warp's argmax element
                 float bs = -INFINITY;
                 int bc = INT_MAX;
-                if (noisy && near_mask) race_exact8(v, near_mask, col0, tid, grow_id, p.rk, bs, bc);
+                if (noisy && aw != INT_MAX && arg_t == aw) {
+                    const uint4 w = noise_words_rk(p.rk, grow_id, static_cast<uint32_t>(aw >> 2));
+                    bs = mw + gumbel_of_bits(word_of(w, aw & 3));
+                    bc = aw;
+                }
                 const float sw = warp_sum_f((st[0] + st[1]) + (st[2] + st[3]));
-                const float ww = warp_sum_f((wt[0] + wt[1]) + (wt[2] + wt[3]));
-                const int aw = warp_min_i(arg_t);
+                const float ww = warp_sum_f((wt[0] + wt[1]) + (wt[2] + wt[3])) * scale;
                 warp_best(bs, bc);
-                if (lane == 0) sc.p1[par][warp] = WarpPartial{mw, sw, ww, bs, aw, bc};
+                if (lane == 0) {
+                    sc.p1[par][warp] = WarpPartial{mw, sw, ww, bs, aw, bc};
+                    sc.wref[k & (kInfoRing - 1)][warp] = mw;
+                }
             }
         } else {
-            // ---- exchange warp: merge first records of row k-1, second of k-3 -----
-            const bool do_a = k >= 1 && k <= nrows;
-            const bool do_b = k >= 3 && k - 3 < nrows;
+            // ---- exchange warp: first records of row k-LAG, second of k-2LAG-1 ----
+            const bool do_a = k >= LAG && k - LAG < nrows;
+            const bool do_b = k >= 2 * LAG + 1 && k - (2 * LAG + 1) < nrows;
+            const int ka = k - LAG, kb = k - (2 * LAG + 1);
+            // the temperature load overlaps the polling
+            const float temp_a = (do_a && lane == 0) ? row_temperature(p, grow_of(ka)) : 0.0f;
             bool ok = true;
             uint64_t ra[6] = {0, 0, 0, 0, 0, 0}, rb[2] = {0, 0};
             if (lane < p.team && (do_a || do_b)) {
                 const int cta = team_id * p.team + lane;
-                ok = read_records(do_a ? record_a(p.xchg, cta, (k - 1) & (kRing - 1)) : nullptr,
-                                  record_tag(k - 1), ra,
-                                  do_b ? record_b(p.xchg, cta, (k - 3) & (kRing - 1)) : nullptr,
-                                  record_tag(k - 3), rb);
+                ok = read_records(do_a ? record_a(p.xchg, cta, ka & (kRing - 1)) : nullptr,
+                                  record_tag(ka), ra,
+                                  do_b ? record_b(p.xchg, cta, kb & (kRing - 1)) : nullptr,
+                                  record_tag(kb), rb);
             }
             const bool have = lane < p.team && ok;
             if (do_a) {
-                const int kf = k - 1;
-                const int64_t frow = row_of(kf);
+                const int64_t frow = row_of(ka);
                 const float m = have ? payload_f(ra[0]) : -INFINITY;
                 const float s_m = have ? payload_f(ra[1]) : 0.0f;
                 const float w_m = have ? payload_f(ra[2]) : 0.0f;
@@ -434,17 +441,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float w_tot = warp_sum_f(w_l);
                 const int arg_row = warp_min_i(m == big_m ? a_m : INT_MAX);
                 warp_best(b_m, bc_m);
-                const bool noisy = temp_next > 0.0f;  // row k-1's, loaded an iteration ago
-                if (k < nrows)
-                    temp_next = row_temperature(p, static_cast<uint64_t>(p.row0 + row_of(k)));
                 if (lane == 0) {
-                    RowInfo& ri = sc.info[kf & (kInfoRing - 1)];
+                    RowInfo& ri = sc.info[ka & (kInfoRing - 1)];
                     ri.row_max = big_m;
                     ri.log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
                     ri.near_best = b_m;
                     ri.near_col = bc_m;
                     ri.arg = arg_row;
-                    ri.noisy = noisy && big_m != -INFINITY;
+                    ri.noisy = temp_a > 0.0f && big_m != -INFINITY;
                     if (member == 0) {
                         p.argmax[frow] = arg_row;
                         p.entropy[frow] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
@@ -453,12 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (do_b) {
-                const int kf = k - 3;
                 float b = have ? payload_f(rb[0]) : -INFINITY;
                 int bcol = have ? static_cast<int>(payload_u(rb[1])) : INT_MAX;
                 warp_best(b, bcol);
                 if (lane == 0) {
-                    const RowInfo& ri = sc.info[kf & (kInfoRing - 1)];
+                    const RowInfo& ri = sc.info[kb & (kInfoRing - 1)];
                     if (ri.noisy && member == 0) {
                         float bb = ri.near_best;
                         int bbc = ri.near_col;
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             bb = b;
                             bbc = bcol;
                         }
-                        p.sample[row_of(kf)] = bb != -INFINITY ? bbc : ri.arg;
+                        p.sample[row_of(kb)] = bb != -INFINITY ? bbc : ri.arg;
                     }
                 }
             }
@@ -508,9 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     publish_a(record_a(p.xchg, blockIdx.x, k & (kRing - 1)), record_tag(k), mc, s_c,
                               w_c, a_c, b_c, bcol_c);
             }
-            if (k >= 2 && k - 2 < nrows) {
-                // ---- second record of row k-2 (its race, run after barrier k-1) ----
-                const int kf = k - 2;
+            const int kf = k - LAG - 1;
+            if (kf >= 0 && kf < nrows) {
+                // ---- second record of row k-LAG-1 (its race ran after barrier k-1)
                 const WarpBest wb = lane < kComputeWarps ? sc.p2[kf & 1][lane]
                                                          : WarpBest{-INFINITY, INT_MAX};
                 float b = wb.best;
@@ -519,83 +522,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0)
                     publish_b(record_b(p.xchg, blockIdx.x, kf & (kRing - 1)), record_tag(kf), b, bcol);
             }
-            // The stage of row k-2 was read for the last time before this
+            // The stage of row k-LAG-1 was read for the last time before this
             // barrier: it takes the next row to load.
-            if (use_tma && lane == 0 && k >= 2 && issued < nrows) {
+            if (use_tma && lane == 0 && kf >= 0 && issued < nrows) {
                 fence_proxy_async_smem();
                 issue_copy();
             }
-        } else if (k >= 1 && k <= nrows) {
-            // ---- compute warps: the pruned race and the probabilities of row k-1 ----
-            const int kf = k - 1;
-            const RowInfo ri = sc.info[kf & (kInfoRing - 1)];
-            const int64_t frow = row_of(kf);
-            const uint64_t fgrow_id = static_cast<uint64_t>(p.row0 + frow);
+        } else if (k >= LAG && k - LAG < nrows) {
+            // ---- compute warps: second half of row j = k-LAG -----------------------
+            const int j = k - LAG;
+            const RowInfo ri = sc.info[j & (kInfoRing - 1)];
+            const float mw = sc.wref[j & (kInfoRing - 1)][warp];  // M_w of row j
+            const int64_t frow = row_of(j);
+            const uint64_t fgrow_id = grow_of(j);
             const float4* fstage =
-                reinterpret_cast<const float4*>(smem + (kf % nstage) * p.stage_bytes);
-            // e = e^(s - M_w) of row k-1, M_w = mw_prev the warp's max
-            float4 e[kVec4];
+                reinterpret_cast<const float4*>(smem + (j % kStages) * p.stage_bytes);
+            float4 e[VEC4];
 #pragma unroll
-            for (int i = 0; i < kVec4; ++i) {
+            for (int i = 0; i < VEC4; ++i) {
                 const int f = i * kCompute + tid;
                 e[i] = (i * kCompute < nslot4 && f < nslot4) ? fstage[f]
                                                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
             if (ri.noisy) {
                 const float best = ri.near_best;
-                // e^(s - best), widened by the race margin, is e * r_w.
-                const float r_w = mw_prev == -INFINITY
-                                      ? 0.0f
-                                      : ex2_approx(fmaf(mw_prev - best, kLog2e, kRaceMarginLog2));
-                float bs = best;
-                int bc = ri.near_col;
+                // e^(s - B), widened by the race margin, is e * r_w.
+                const float r_w =
+                    mw == -INFINITY ? 0.0f : ex2_approx(fmaf(mw - best, kLog2e, kRaceMarginLog2));
+                WarpBest wb{best, ri.near_col};
                 uint32_t survivors = 0;
                 // Philox four groups at a time, so that their chains overlap.
 #pragma unroll
-                for (int i0 = 0; i0 < kVec4; i0 += 4) {
-                    bool pass[4];
+                for (int i0 = 0; i0 < VEC4; i0 += 4) {
+                    constexpr int kGroup = 4;
+                    bool pass[kGroup];
                     bool any = false;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int jj = 0; jj < kGroup; ++jj) {
                         // 1 - u >= 2^-24 always: below that bound no element of
                         // the group can win
-                        pass[j] = (i0 + j) * kCompute < nslot4 && max4(e[i0 + j]) * r_w >= 0x1p-24f;
-                        any |= pass[j];
+                        pass[jj] = i0 + jj < VEC4 && (i0 + jj) * kCompute < nslot4 &&
+                                   max4(e[min(i0 + jj, VEC4 - 1)]) * r_w >= 0x1p-24f;
+                        any |= pass[jj];
                     }
                     // warp-uniform: when any lane needs this quad, every lane
-                    // draws its four blocks (straight-line, no divergence)
+                    // draws its blocks (straight-line, no divergence)
                     if (__any_sync(0xffffffffu, any)) {
-                        uint4 w[4];
+                        uint4 w[kGroup];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            w[j] = noise_words_rk(
-                                p.rk, fgrow_id,
-                                static_cast<uint32_t>((col0 >> 2) + (i0 + j) * kCompute + tid));
+                        for (int jj = 0; jj < kGroup; ++jj)
+                            if (i0 + jj < VEC4)
+                                w[jj] = noise_words_rk(
+                                    p.rk, fgrow_id,
+                                    static_cast<uint32_t>((col0 >> 2) + (i0 + jj) * kCompute + tid));
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (pass[j])
-                                survivors |= race_group(e[i0 + j], w[j], r_w) << (4 * (i0 + j));
+                        for (int jj = 0; jj < kGroup; ++jj)
+                            if (i0 + jj < VEC4 && pass[jj])
+                                survivors |= race_group(e[i0 + jj], w[jj], r_w) << (4 * (i0 + jj));
                     }
                 }
                 if (survivors)
-                    race_rescore(survivors, p.logits + frow * p.row_stride, temp_prev, col0, tid,
-                                 fgrow_id, p.rk, ri.near_col, bs, bc);
-                warp_best(bs, bc);
-                if (lane == 0) sc.p2[kf & 1][warp] = WarpBest{bs, bc};
+                    wb = race_rescore(survivors, p.logits + frow * p.row_stride,
+                                      row_temperature(p, fgrow_id), col0, tid, fgrow_id, p.rk, wb);
+                warp_best(wb.best, wb.col);
+                if (lane == 0) sc.p2[j & 1][warp] = wb;
             } else if (lane == 0) {
-                sc.p2[kf & 1][warp] = WarpBest{-INFINITY, INT_MAX};
+                sc.p2[j & 1][warp] = WarpBest{-INFINITY, INT_MAX};
             }
 
             if (p.probs_dtype != 0) {
                 const float big_m = ri.row_max;
                 // e^(s - M) / S = e * e^(M_w - M) / S
-                const float f_w = mw_prev == -INFINITY
-                                      ? 0.0f
-                                      : ex2_approx(fmaf(mw_prev - big_m, kLog2e, -ri.log2s));
+                const float f_w =
+                    mw == -INFINITY ? 0.0f : ex2_approx(fmaf(mw - big_m, kLog2e, -ri.log2s));
                 const bool bf16 = p.probs_dtype == 1;
                 uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
 #pragma unroll
-                for (int i = 0; i < kVec4; ++i) {
+                for (int i = 0; i < VEC4; ++i) {
                     const int f = i * kCompute + tid;
                     if (i * kCompute >= nslot4 || f >= nslot4) continue;
                     float pr[4] = {e[i].x * f_w, e[i].y * f_w, e[i].z * f_w, e[i].w * f_w};
@@ -620,47 +623,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     // is released.
     if (use_tma && exchange && lane == 0) {
         for (int seq = consumed; seq < issued; ++seq) {
-            mbar_wait_bounded(&sc.full[seq % nstage], static_cast<uint32_t>((seq / nstage) & 1));
+            mbar_wait_bounded(&sc.full[seq % kStages], static_cast<uint32_t>((seq / kStages) & 1));
         }
     }
 }
 
 namespace {
 
-// Team size G for one CTA per SM with 480 compute threads: the chunk must
-// fit the registers (15360 columns) and, for four stages, shared memory.
-// Minimises ceil(rows / teams) * chunk with teams = min(rows, sms / G); ties
-// go to the smaller G.
-RowPlan plan_row_stats(int64_t rows, int vocab, int sms, size_t scratch) {
+struct RowStatsPlan {
+    RowPlan rows;
+    int lag;     // 2 or 1
+    int nstage;  // 5 (LAG 2), 4 or 3 (LAG 1)
+    int vec4;    // float4 slots per compute thread
+};
+
+// Team size G for one CTA per SM with 480 compute threads. The chunk must
+// fit the registers and the stages shared memory. An iteration costs about
+// max(chunk, round trip / LAG) + 1500 columns of work, the round trip of the
+// team exchange through L2 (about 2.6 us) being worth some 18000 columns;
+// the plan minimises ceil(rows / teams) times that, with teams = min(rows,
+// sms / G) and the three-stage form counted 25% dearer. Ties go to the
+// earlier form, then the smaller G.
+RowStatsPlan plan_row_stats(int64_t rows, int vocab, int sms, size_t scratch) {
     const size_t budget = kSmemPerCta - scratch;
-    int cap4 = static_cast<int>(budget / (4 * 4)) & ~31;  // columns with 4 stages
-    if (cap4 > kRowChunkCap) cap4 = kRowChunkCap;
-    const int cap3 = kRowChunkCap;                        // 3 stages: 180 KB
-    RowPlan best{0, 0, 0, kVec4, 1};
+    struct Form {
+        int lag, nstage, vec4;
+        double pen;
+    };
+    constexpr double kChainCols = 18000.0;
+    const Form forms[] = {{2, 5, kVec4Lag2, 1.0}, {1, 4, kVec4Lag1, 1.0}, {1, 3, kVec4Lag1, 1.25}};
+    RowStatsPlan plan{{0, 0, 0, 0, 1}, 0, 0, 0};
     double best_cost = 0.0;
     const int capacity = sms > 1024 ? 1024 : sms;
-    const int g_min = (vocab + cap3 - 1) / cap3;
-    for (int g = g_min; g <= kMaxTeam && g <= capacity; ++g) {
-        int chunk = (vocab + g - 1) / g;
-        chunk = (chunk + 3) & ~3;
-        if ((vocab + chunk - 1) / chunk != g) continue;
-        int64_t teams = capacity / g;
-        if (teams > rows) teams = rows;
-        if (teams < 1) continue;
-        // three stages leave the bulk copy only part of an iteration: count
-        // such a chunk as 25% dearer
-        const double pen = chunk <= cap4 ? 1.0 : 1.25;
-        const double cost = pen * static_cast<double>((rows + teams - 1) / teams) * chunk;
-        if (best.team == 0 || cost < best_cost) {
-            best = RowPlan{g, chunk, static_cast<int>(teams), kVec4, 1};
-            best_cost = cost;
+    for (const Form& fm : forms) {
+        int cap = static_cast<int>(budget / (4 * fm.nstage)) & ~31;
+        if (cap > kCompute * fm.vec4 * 4) cap = kCompute * fm.vec4 * 4;
+        const int g_min = (vocab + cap - 1) / cap;
+        for (int g = g_min; g <= kMaxTeam && g <= capacity; ++g) {
+            int chunk = (vocab + g - 1) / g;
+            chunk = (chunk + 3) & ~3;
+            if ((vocab + chunk - 1) / chunk != g) continue;
+            int64_t teams = capacity / g;
+            if (teams > rows) teams = rows;
+            if (teams < 1) continue;
+            const double per_row = (chunk > kChainCols / fm.lag ? chunk : kChainCols / fm.lag) + 1500.0;
+            const double cost = fm.pen * static_cast<double>((rows + teams - 1) / teams) * per_row;
+            if (plan.rows.team == 0 || cost < best_cost) {
+                plan = RowStatsPlan{{g, chunk, static_cast<int>(teams), fm.vec4, 1}, fm.lag,
+                                    fm.nstage, fm.vec4};
+                best_cost = cost;
+            }
         }
     }
-    return best;
+    return plan;
 }
 
+template <int VEC4, int LAG, int NSTAGE>
 drs_status launch_row_stats(RowStatsParams& prm, int grid, size_t smem, cudaStream_t stream) {
-    auto kernel = row_stats_kernel;
+    auto kernel = row_stats_kernel<VEC4, LAG, NSTAGE>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return DRS_ERR_CUDA;
@@ -713,7 +733,8 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
     const int sms = sm_count();
     if (sms <= 0) return DRS_ERR_CUDA;
     const size_t scratch = (sizeof(Scratch) + 127) & ~static_cast<size_t>(127);
-    const RowPlan plan = plan_row_stats(rows, static_cast<int>(vocab), sms, scratch);
+    const RowStatsPlan rsp = plan_row_stats(rows, static_cast<int>(vocab), sms, scratch);
+    const RowPlan& plan = rsp.rows;
     if (!plan.team) return DRS_ERR_UNSUPPORTED;
     // per-team row counts are int
     if ((rows + plan.num_teams - 1) / plan.num_teams > INT_MAX / 2) return DRS_ERR_UNSUPPORTED;
@@ -744,24 +765,23 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
     prm.fault = g_inject_fault.exchange(0);
     if (!prm.err) return DRS_ERR_CUDA;
 
-    // Shared memory: stages of one chunk each (filled by bulk copies when
-    // rows start 16-byte aligned; in every case they keep a row's scaled
-    // logits until its finalisation) plus the scratch. Four stages when they
-    // fit: the row being finalised, the row being computed, two rows loading.
+    // Shared memory: the stages of one chunk each (filled by bulk copies when
+    // rows start 16-byte aligned; in every case they keep a row's e until its
+    // second half) plus the scratch.
     const bool tma = aligned(logits, 16) && (row_stride % 4 == 0);
     prm.stage_bytes = (plan.chunk * 4 + 127) & ~127;
-    int ns = static_cast<int>((kSmemPerCta - scratch) / prm.stage_bytes);
-    if (ns > kMaxStages) ns = kMaxStages;
-    if (ns < 3) return DRS_ERR_UNSUPPORTED;
-    prm.nstage = ns;
     prm.use_tma = tma ? 1 : 0;
-    const size_t smem = static_cast<size_t>(prm.nstage) * prm.stage_bytes + scratch;
+    const size_t smem = static_cast<size_t>(rsp.nstage) * prm.stage_bytes + scratch;
+    if (smem > kSmemPerCta) return DRS_ERR_UNSUPPORTED;
     const int grid = plan.team * plan.num_teams;
     // Zero the records this launch uses: a zero tag matches no row.
     if (cudaMemsetAsync(workspace, 0, static_cast<size_t>(grid) * kXchgPerCta,
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return DRS_ERR_CUDA;
-    return launch_row_stats(prm, grid, smem, static_cast<cudaStream_t>(stream));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (rsp.lag == 2) return launch_row_stats<kVec4Lag2, 2, 5>(prm, grid, smem, st);
+    if (rsp.nstage == 4) return launch_row_stats<kVec4Lag1, 1, 4>(prm, grid, smem, st);
+    return launch_row_stats<kVec4Lag1, 1, 3>(prm, grid, smem, st);
 }
 
 // ---------------------------------------------------------------------------
