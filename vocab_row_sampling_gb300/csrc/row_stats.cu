@@ -7,40 +7,43 @@
 // chunks of `chunk` columns (a multiple of 4). G CTAs -- a team -- own the G
 // chunks of every row of the team; teams take rows round robin. The kernel
 // is persistent: one CTA per SM, cooperative launch (all CTAs resident, so
-// their bounded waits on each other cannot deadlock). A CTA has 15 compute
-// warps (480 threads, VEC4 float4 slots each: slot i of thread t covers
-// chunk columns 4*(i*480+t)+0..3) and one exchange warp.
+// their bounded waits on each other cannot deadlock). A CTA has 14 compute
+// warps (448 threads, VEC4 float4 slots each: slot i of thread t covers
+// chunk columns 4*(i*448+t)+0..3), a publisher warp and a poller warp. They
+// synchronise through mbarriers only, so that every warp runs at its own
+// pace and the latency of one warp's work hides behind the others'.
 //
-// A row is handled in two halves LAG iterations apart, so that the team's
-// exchange of the first half's results (a round trip through L2 that takes
-// about as long as one iteration's compute) overlaps LAG iterations of work.
-// Iteration k, before its one CTA barrier:
-//   compute warps, first half of row k: wait for the bulk copy (TMA) that
-//     staged the chunk iterations ahead; the warp max M_w of the scaled
-//     logits s = x / Te (Te = max(T, 1e-10)) and the lowest column reaching
-//     it (the argmax), e = e^(s - M_w) written back into the stage,
-//     S_w = sum e and W_w = sum e (s - M_w) (the "online max and sum" of the
-//     page), and for T > 0 the Gumbel-max score of the warp's argmax
-//     element (a lower bound B of the row's best score). Division by Te > 0
-//     is monotone, so while |M_w| < 256 the warp works on the raw logits:
-//     the max is found among them, only the few candidates for the argmax
-//     are divided (exactly), and e = 2^((x - x_max) log2(e) / Te) is within
+// Compute warps, in order, for k = 0, 1, ...:
+//   first half of row k: wait for the stage (bulk copy); the warp max M_w
+//     of the scaled logits s = x / Te (Te = max(T, 1e-10)) and the lowest
+//     column reaching it (the argmax), e = e^(s - M_w) written back into the
+//     stage, S_w = sum e and W_w = sum e (s - M_w) (the "online max and
+//     sum" of the page), and for T > 0 the Gumbel-max score of the warp's
+//     argmax element (a lower bound B of the row's best score); arrive on
+//     the row's first-half barrier. Division by Te > 0 is monotone, so while
+//     |M_w| < 256 the warp works on the raw logits: the max is found among
+//     them, only the few candidates for the argmax are divided (exactly),
+//     and e = 2^(x log2(e) / Te - c) with c the rounded reference is within
 //     a relative 2^-15 of e^(s - M_w). Warps with larger scaled values
 //     divide every logit exactly first.
-//   exchange warp: merges the team's first records of row k-LAG (M, S, W,
-//     argmax, B) and its second records of row k-2LAG-1 (the race best);
-//     member 0 writes argmax and entropy of row k-LAG and the sample of row
-//     k-2LAG-1.
-// After the barrier:
-//   exchange warp: combines the warp partials of row k into the CTA's first
-//     record and those of row k-LAG-1's race into its second record,
-//     publishes both, and issues the bulk copy of a later row into the stage
-//     row k-LAG-1 left.
-//   compute warps, second half of row k-LAG, its e read back from the
-//     stage: the pruned race against the row's B (an element can only win if
-//     1 - u <= -log u <= e^(s - B) = e * e^(M_w - B); the few survivors are
-//     rescored exactly from their logits), then the probabilities
-//     e * e^(M_w - M) / S, rounded to nearest even and written to HBM.
+//   second half of row k-LAG, once the poller has merged the row: the
+//     probabilities e * e^(M_w - M) / S (rounded to nearest even, written to
+//     HBM), then the pruned race against the row's B (an element can only
+//     win if 1 - u <= -log u <= e^(s - B) = e * e^(M_w - B); the float4
+//     groups that pass a bound on their largest e go on a per-warp list,
+//     shared out one Philox call per lane; the few survivors are rescored
+//     exactly from their logits); arrive on the row's second-half barrier,
+//     which also frees the stage.
+// Publisher warp: per row, combines the compute warps' first-half partials
+//   into the CTA's first record and publishes it; two rows later combines
+//   their race bests into the second record, publishes it, and refills the
+//   freed stage with a later row (bulk copy), with that row's temperature
+//   quotient computed once for the CTA.
+// Poller warp: per row, reads the team's first records (M, S, W, argmax, B)
+//   and merges them for the compute warps, and reads the second records of
+//   an earlier row; member 0 writes argmax, entropy and sample.
+// LAG rows between a row's halves cover the team exchange, a round trip
+// through L2.
 //
 // HBM traffic: every logit is read once (by the bulk copy) and every
 // probability written once. No fp64 arithmetic (its rate on GB300 is a
@@ -60,18 +63,20 @@ namespace drs {
 
 namespace {
 
-constexpr int kComputeWarps = kWarps - 1;     // warps 0..14
-constexpr int kCompute = kComputeWarps * 32;  // 480 compute threads
-constexpr int kExchangeWarp = kWarps - 1;     // warp 15
-constexpr int kInfoRing = 8;                  // merged rows kept, by row % 8
+constexpr int kComputeWarps = kWarps - 2;     // warps 0..13
+constexpr int kCompute = kComputeWarps * 32;  // 448 compute threads
+constexpr int kPublisherWarp = kWarps - 2;    // warp 14
+constexpr int kPollerWarp = kWarps - 1;       // warp 15
+static_assert(kPublisherWarp == kComputeWarps && kPollerWarp == kComputeWarps + 1, "warp roles");
+constexpr int kRowRing = 8;                   // per-row shared state, by row % 8
 // Three forms: LAG 2 with 5 stages of up to 6 float4 per thread (rows up to
-// 32 * 11520 columns), LAG 1 with 4 stages of up to 8, and LAG 1 with 3
-// stages (up to 32 * 15360 columns; the bulk copy then has only part of an
-// iteration to land).
+// 32 * 10752 columns), LAG 1 with 4 stages of up to 9, and LAG 1 with 3
+// stages (up to 32 * 16128 columns; the bulk copy then has less time to
+// land).
 constexpr int kVec4Lag2 = 6;
-constexpr int kVec4Lag1 = 8;
+constexpr int kVec4Lag1 = 9;
 constexpr int kMaxStages = 5;
-// The ring of exchange records must outlast 2 * LAG + 2 iterations.
+constexpr int kMaxVec4Slots = 9;
 static_assert(kRing >= 2 * 2 + 2, "exchange ring too short for LAG 2");
 
 // log2(1.0002): the race's bound e^(s - best) is widened by 2e-4 so that
@@ -134,14 +139,25 @@ struct RowInfo {
     int noisy;
 };
 
+// A row's temperature and its quotient, set once by the publisher.
+struct RowQuotient {
+    float temp;
+    float t, y;
+    int mode;
+};
+
 struct Scratch {
-    uint64_t full[kMaxStages];
-    WarpPartial p1[2][kComputeWarps];      // row k's warp partials, by row parity
-    WarpBest p2[2][kComputeWarps];         // row j's race bests, by row parity
-    RowInfo info[kInfoRing];               // merged rows
-    float wref[kInfoRing][kComputeWarps];  // each warp's M_w, by row % 8
-    int status;                            // a merge ran out of time
-    int abort_load;                        // a bulk copy ran out of time
+    uint64_t full[kMaxStages];          // the stage holds the row (bulk copy landed)
+    uint64_t a_done[kRowRing];          // the compute warps' first-half partials are in p1
+    uint64_t b_done[kRowRing];          // second half done: race bests in p2, stage free
+    uint64_t info_ready[kRowRing];      // the row's merged first records are in info
+    WarpPartial p1[kRowRing][kComputeWarps];
+    WarpBest p2[kRowRing][kComputeWarps];
+    RowInfo info[kRowRing];
+    RowQuotient rq[kRowRing];
+    float wref[kRowRing][kComputeWarps];                   // each warp's M_w
+    uint16_t worklist[kComputeWarps][32 * kMaxVec4Slots];  // race groups of a warp
+    int abort;                                             // a wait ran out of time
 };
 
 __device__ __forceinline__ void set_comp(float4& v, int q, float x) {
@@ -160,6 +176,12 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
     }
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
 }
 
 // Temperature of a global row: temps[row / canvas_len].
@@ -190,23 +212,24 @@ __device__ __forceinline__ uint32_t race_group(const float4& e, uint4 w, float r
     return bits;
 }
 
-// Score the survivors of `mask` (bit 4i+q: slot i, component q) exactly:
-// s = x / max(T, 1e-10) from the logit in global memory (the stage holds e
-// only), g from the element's Philox word; keep the best (score, column).
+// Score the survivors `bits` of the float4 group starting at column c4
+// exactly: s = x / Te from the logit in global memory (the stage holds e
+// only), g from the group's Philox words; keep the best (score, column).
 // The column that set the best already was scored the same way.
-__device__ __noinline__ WarpBest race_rescore(uint32_t mask, const float* row_logits, float temp,
-                                              int col0, int tid, uint64_t grow_id,
-                                              const PhiloxRoundKeys& rk, WarpBest best) {
-    const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
-    while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int f = (b >> 2) * kCompute + tid;
-        const int c = col0 + 4 * f + (b & 3);
-        if (c == best.col) continue;
+__device__ __noinline__ WarpBest race_rescore(uint32_t bits, const float* row_logits, int c4,
+                                              uint4 w, const RowQuotient rq, int skip_col,
+                                              WarpBest best) {
+    ScaledQuotient sq;
+    sq.t = rq.t;
+    sq.y = rq.y;
+    sq.mode = rq.mode;
+    while (bits) {
+        const int q = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int c = c4 + q;
+        if (c == skip_col) continue;
         const float s = sq.exact(__ldg(row_logits + c));
-        const uint4 w = noise_words_rk(rk, grow_id, static_cast<uint32_t>((col0 >> 2) + f));
-        const float score = s + gumbel_of_bits(word_of(w, b & 3));
+        const float score = s + gumbel_of_bits(word_of(w, q));
         if (beats(score, c, best.best, best.col)) best = WarpBest{score, c};
     }
     return best;
@@ -217,16 +240,16 @@ __device__ __noinline__ WarpBest race_rescore(uint32_t mask, const float* row_lo
 template <int VEC4, int LAG, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, 1)
     row_stats_kernel(const __grid_constant__ RowStatsParams p) {
-    constexpr int kStages = NSTAGE;  // LAG + 1 rows held, the rest loading
-    static_assert(kStages <= kMaxStages && kStages >= LAG + 2, "stages");
+    static_assert(NSTAGE <= kMaxStages && NSTAGE >= LAG + 2, "stages");
+    static_assert(VEC4 <= kMaxVec4Slots, "slots");
     extern __shared__ __align__(128) unsigned char smem[];
-    Scratch& sc = *reinterpret_cast<Scratch*>(smem + kStages * p.stage_bytes);
+    Scratch& sc = *reinterpret_cast<Scratch*>(smem + NSTAGE * p.stage_bytes);
+    volatile int* abort_flag = &sc.abort;
     const bool use_tma = p.use_tma != 0;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const bool exchange = warp == kExchangeWarp;
     const int team_id = blockIdx.x / p.team;
     const int member = blockIdx.x - team_id * p.team;
     const int col0 = member * p.chunk;
@@ -239,57 +262,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                           : 0;
     auto row_of = [&](int k) { return team_id + static_cast<int64_t>(k) * p.num_teams; };
     auto grow_of = [&](int k) { return static_cast<uint64_t>(p.row0 + row_of(k)); };
+    auto fail = [&]() {
+        *abort_flag = 1;
+        raise_device_error(p.err, 1);
+    };
 
     if (tid == 0) {
-        if (use_tma) {
-            for (int s = 0; s < kStages; ++s) mbar_init(&sc.full[s], 1);
-            fence_barrier_init();
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(&sc.full[s], 1);
+        for (int r = 0; r < kRowRing; ++r) {
+            mbar_init(&sc.a_done[r], kComputeWarps);
+            mbar_init(&sc.b_done[r], kComputeWarps);
+            mbar_init(&sc.info_ready[r], 1);
         }
-        sc.abort_load = 0;
-        sc.status = 0;
+        fence_barrier_init();
+        sc.abort = 0;
     }
-    __syncthreads();
+    __syncthreads();  // the only CTA barrier: everything after is mbarriers
 
-    // Producer state, exchange-warp lane 0: rows issued to the stages.
-    int issued = 0;
-    auto issue_copy = [&]() {
-        const int s = issued % kStages;
-        mbar_arrive_expect_tx(&sc.full[s], copy_bytes);
-        if (copy_bytes)
-            tma_load_1d(smem + s * p.stage_bytes, p.logits + row_of(issued) * p.row_stride + col0,
-                        copy_bytes, &sc.full[s]);
-        ++issued;
-    };
-    if (use_tma && exchange && lane == 0) {
-        while (issued < nrows && issued < kStages) issue_copy();
-    }
-
-    // Compute warps: the temperature of the next row, loaded an iteration
-    // ahead.
-    float temp_next = 0.0f;
-    if (nrows > 0 && !exchange) temp_next = row_temperature(p, grow_of(0));
-
-    bool aborted = false;
-    int consumed = 0;
-    for (int k = 0; k <= nrows + 2 * LAG; ++k) {
-        const int par = k & 1;
-        // ===================== before the barrier ===============================
-        if (!exchange) {
+    if (warp < kComputeWarps) {
+        // ======================= compute warps ==================================
+        for (int k = 0; k < nrows + LAG; ++k) {
+            if (*abort_flag) break;
             if (k < nrows) {
-                // ---- compute warps: first half of row k -------------------------
+                // ---- first half of row k ---------------------------------------
                 const int64_t row = row_of(k);
                 const uint64_t grow_id = grow_of(k);
                 const float* grow = p.logits + row * p.row_stride + col0;
-                const int s = k % kStages;
-                float4* stage4 = reinterpret_cast<float4*>(smem + s * p.stage_bytes);
-                const float temp = temp_next;
-                if (k + 1 < nrows) temp_next = row_temperature(p, grow_of(k + 1));
-
-                bool timed_out = false;
-                if (use_tma)
-                    timed_out =
-                        !mbar_wait_bounded(&sc.full[s], static_cast<uint32_t>((k / kStages) & 1));
-                if (timed_out) sc.abort_load = 1;
+                float4* stage4 = reinterpret_cast<float4*>(smem + (k % NSTAGE) * p.stage_bytes);
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sc.full[k % NSTAGE],
+                                                               static_cast<uint32_t>((k / NSTAGE) & 1)))) {
+                    if (lane == 0) fail();
+                    break;
+                }
+                const RowQuotient rq = sc.rq[k & (kRowRing - 1)];
+                ScaledQuotient sq;
+                sq.t = rq.t;
+                sq.y = rq.y;
+                sq.mode = rq.mode;
+                const bool noisy = rq.temp > 0.0f;
                 float4 v[VEC4];
 #pragma unroll
                 for (int i = 0; i < VEC4; ++i) {
@@ -298,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (i * kCompute < nslot4) {  // CTA-uniform: slot i holds columns
                         if (f < nfull4) {
                             if (use_tma) {
-                                if (!timed_out) x = stage4[f];
+                                x = stage4[f];
                             } else {
                                 x.x = grow[4 * f + 0];
                                 x.y = grow[4 * f + 1];
@@ -312,11 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     v[i] = x;
                 }
 
-                const float te = fmaxf(temp, kTempFloor);
-                const ScaledQuotient sq = ScaledQuotient::of(te);
-                const bool noisy = temp > 0.0f;
-
-                // max of the raw logits (division by te > 0 keeps the order)
+                // max of the raw logits (division by Te > 0 keeps the order)
                 float mt = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < VEC4; ++i) mt = fmaxf(mt, max4(v[i]));
@@ -324,13 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mw = mxw == -INFINITY ? -INFINITY : sq.exact(mxw);  // M_w
                 // warp-uniform: raw domain, or exact quotients first
                 const bool raw = !(fabsf(mw) >= kRawDomainLimit);
-                float ref, scale;  // d = (v - ref) * scale is s - M_w
-                float cthr;        // argmax candidates: v >= cthr
+                float cthr;  // argmax candidates: v >= cthr
                 if (raw) {
-                    ref = mxw;
-                    scale = sq.y;
-                    // exact(x) == M_w needs x >= mxw - te * ulp(M_w)
-                    cthr = mxw - fmaxf(fabsf(mxw) * 0x1p-20f, te * 0x1p-140f);
+                    // exact(x) == M_w needs x >= mxw - Te * ulp(M_w)
+                    cthr = mxw - fmaxf(fabsf(mxw) * 0x1p-20f, rq.t * 0x1p-140f);
                 } else {
 #pragma unroll
                     for (int i = 0; i < VEC4; ++i) {
@@ -340,23 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         v[i].w = sq.exact(v[i].w);
                     }
                     mt = sq.exact(mt);
-                    ref = mw;
-                    scale = 1.0f;
                     cthr = mw;
                 }
 
                 // argmax: the lowest column whose exact quotient is M_w
                 int arg_t = INT_MAX;
                 if (mt >= cthr && mw != -INFINITY) {
-                    uint32_t cand = 0;  // bit 4i+q: columns in increasing order
+                    uint64_t cand = 0;  // bit 4i+q: columns in increasing order
 #pragma unroll
                     for (int i = 0; i < VEC4; ++i)
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            if (comp(v[i], q) >= cthr) cand |= 1u << (4 * i + q);
+                            if (comp(v[i], q) >= cthr) cand |= 1ull << (4 * i + q);
 #pragma unroll 1
                     while (cand) {
-                        const int b = __ffs(cand) - 1;
+                        const int b = __ffsll(static_cast<long long>(cand)) - 1;
                         cand &= cand - 1;
                         const float x = pick(v, b);
                         if ((raw ? sq.exact(x) : x) == mw) {
@@ -367,9 +368,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int aw = warp_min_i(arg_t);
 
-                // sums, four accumulators each; e = e^(s - M_w) waits in the
-                // stage for the race and the probabilities
-                const float lscale = kLog2e * scale;
+                // t = (s - M_w) log2(e): raw domain x * log2(e)/Te - c with
+                // c = RN(mxw * log2(e)/Te), else (s - M_w) * log2(e); -inf
+                // gives a finite t whose e is 0
+                float lscale, cref;
+                if (raw) {
+                    lscale = kLog2e * sq.y;
+                    cref = mxw * lscale;
+                } else {
+                    lscale = kLog2e;
+                    cref = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < VEC4; ++i) {
+                        v[i].x -= mw;
+                        v[i].y -= mw;
+                        v[i].z -= mw;
+                        v[i].w -= mw;
+                    }
+                }
+                // sums, four accumulators each; e waits in the stage
                 float st[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int i = 0; i < VEC4; ++i) {
@@ -377,12 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float4 ev;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            // -inf -> a finite difference whose e is 0
-                            const float d = fmaxf(comp(v[i], q) - ref, -FLT_MAX);
-                            const float e = ex2_approx(d * lscale);
+                            const float t = fmaxf(fmaf(comp(v[i], q), lscale, -cref), -FLT_MAX);
+                            const float e = ex2_approx(t);
                             set_comp(ev, q, e);
                             st[q] += e;
-                            wt[q] = fmaf(e, d, wt[q]);
+                            wt[q] = fmaf(e, t, wt[q]);
                         }
                         const int f = i * kCompute + tid;
                         if (f < nslot4) stage4[f] = ev;
@@ -397,100 +413,141 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bc = aw;
                 }
                 const float sw = warp_sum_f((st[0] + st[1]) + (st[2] + st[3]));
-                const float ww = warp_sum_f((wt[0] + wt[1]) + (wt[2] + wt[3])) * scale;
+                const float ww = warp_sum_f((wt[0] + wt[1]) + (wt[2] + wt[3])) * kLn2;
                 warp_best(bs, bc);
                 if (lane == 0) {
-                    sc.p1[par][warp] = WarpPartial{mw, sw, ww, bs, aw, bc};
-                    sc.wref[k & (kInfoRing - 1)][warp] = mw;
+                    sc.p1[k & (kRowRing - 1)][warp] = WarpPartial{mw, sw, ww, bs, aw, bc};
+                    sc.wref[k & (kRowRing - 1)][warp] = mw;
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sc.a_done[k & (kRowRing - 1)]);
             }
-        } else {
-            // ---- exchange warp: first records of row k-LAG, second of k-2LAG-1 ----
-            const bool do_a = k >= LAG && k - LAG < nrows;
-            const bool do_b = k >= 2 * LAG + 1 && k - (2 * LAG + 1) < nrows;
-            const int ka = k - LAG, kb = k - (2 * LAG + 1);
-            // the temperature load overlaps the polling
-            const float temp_a = (do_a && lane == 0) ? row_temperature(p, grow_of(ka)) : 0.0f;
-            bool ok = true;
-            uint64_t ra[6] = {0, 0, 0, 0, 0, 0}, rb[2] = {0, 0};
-            if (lane < p.team && (do_a || do_b)) {
-                const int cta = team_id * p.team + lane;
-                ok = read_records(do_a ? record_a(p.xchg, cta, ka & (kRing - 1)) : nullptr,
-                                  record_tag(ka), ra,
-                                  do_b ? record_b(p.xchg, cta, kb & (kRing - 1)) : nullptr,
-                                  record_tag(kb), rb);
-            }
-            const bool have = lane < p.team && ok;
-            if (do_a) {
-                const int64_t frow = row_of(ka);
-                const float m = have ? payload_f(ra[0]) : -INFINITY;
-                const float s_m = have ? payload_f(ra[1]) : 0.0f;
-                const float w_m = have ? payload_f(ra[2]) : 0.0f;
-                const int a_m = have ? static_cast<int>(payload_u(ra[3])) : INT_MAX;
-                float b_m = have ? payload_f(ra[4]) : -INFINITY;
-                int bc_m = have ? static_cast<int>(payload_u(ra[5])) : INT_MAX;
-                const float big_m = warp_max(m);
-                float s_l = 0.0f, w_l = 0.0f;
-                if (m != -INFINITY) {
-                    const float dm = m - big_m;
-                    const float f = ex2_approx(dm * kLog2e);
-                    s_l = f * s_m;
-                    w_l = f * fmaf(dm, s_m, w_m);
+
+            const int j = k - LAG;
+            if (j >= 0) {
+                // ---- second half of row j --------------------------------------
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sc.info_ready[j & (kRowRing - 1)],
+                                                               static_cast<uint32_t>((j / kRowRing) & 1)))) {
+                    if (lane == 0) fail();
+                    break;
                 }
-                const float s_tot = warp_sum_f(s_l);
-                const float w_tot = warp_sum_f(w_l);
-                const int arg_row = warp_min_i(m == big_m ? a_m : INT_MAX);
-                warp_best(b_m, bc_m);
-                if (lane == 0) {
-                    RowInfo& ri = sc.info[ka & (kInfoRing - 1)];
-                    ri.row_max = big_m;
-                    ri.log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
-                    ri.near_best = b_m;
-                    ri.near_col = bc_m;
-                    ri.arg = arg_row;
-                    ri.noisy = temp_a > 0.0f && big_m != -INFINITY;
-                    if (member == 0) {
-                        p.argmax[frow] = arg_row;
-                        p.entropy[frow] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
-                        if (!ri.noisy) p.sample[frow] = arg_row;
-                    }
+                const RowInfo ri = sc.info[j & (kRowRing - 1)];
+                const float mw = sc.wref[j & (kRowRing - 1)][warp];
+                const int64_t frow = row_of(j);
+                const float4* fstage =
+                    reinterpret_cast<const float4*>(smem + (j % NSTAGE) * p.stage_bytes);
+                float4 e[VEC4];
+#pragma unroll
+                for (int i = 0; i < VEC4; ++i) {
+                    const int f = i * kCompute + tid;
+                    e[i] = (i * kCompute < nslot4 && f < nslot4)
+                               ? fstage[f]
+                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 }
-            }
-            if (do_b) {
-                float b = have ? payload_f(rb[0]) : -INFINITY;
-                int bcol = have ? static_cast<int>(payload_u(rb[1])) : INT_MAX;
-                warp_best(b, bcol);
-                if (lane == 0) {
-                    const RowInfo& ri = sc.info[kb & (kInfoRing - 1)];
-                    if (ri.noisy && member == 0) {
-                        float bb = ri.near_best;
-                        int bbc = ri.near_col;
-                        if (beats(b, bcol, bb, bbc)) {
-                            bb = b;
-                            bbc = bcol;
+                // e^(s - B), widened by the race margin, is e * r_w; a group
+                // whose largest e * r_w is below 2^-24 (<= 1 - u always) has
+                // no element that can win.
+                const float r_w = ri.noisy && mw != -INFINITY
+                                      ? ex2_approx(fmaf(mw - ri.near_best, kLog2e, kRaceMarginLog2))
+                                      : 0.0f;
+                uint32_t pmask = 0;
+#pragma unroll
+                for (int i = 0; i < VEC4; ++i)
+                    if (max4(e[i]) * r_w >= 0x1p-24f) pmask |= 1u << i;
+
+                if (p.probs_dtype != 0) {
+                    const float big_m = ri.row_max;
+                    // e^(s - M) / S = e * e^(M_w - M) / S
+                    const float f_w =
+                        mw == -INFINITY ? 0.0f : ex2_approx(fmaf(mw - big_m, kLog2e, -ri.log2s));
+                    const bool bf16 = p.probs_dtype == 1;
+                    uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
+#pragma unroll
+                    for (int i = 0; i < VEC4; ++i) {
+                        const int f = i * kCompute + tid;
+                        if (i * kCompute >= nslot4 || f >= nslot4) continue;
+                        float pr[4] = {e[i].x * f_w, e[i].y * f_w, e[i].z * f_w, e[i].w * f_w};
+                        if (big_m == -INFINITY) pr[0] = pr[1] = pr[2] = pr[3] = NAN;
+                        const uint32_t lo = pack2(pr[0], pr[1], bf16);
+                        const uint32_t hi = pack2(pr[2], pr[3], bf16);
+                        if (p.probs_vec && f < nfull4) {
+                            __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
+                        } else {
+                            const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                                      static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+                            for (int q = 0; q < 4; ++q)
+                                if (4 * f + q < ncols) prow[4 * f + q] = code[q];
                         }
-                        p.sample[row_of(kb)] = bb != -INFINITY ? bbc : ri.arg;
                     }
                 }
+
+                WarpBest wb{-INFINITY, INT_MAX};
+                if (ri.noisy) {
+                    wb = WarpBest{ri.near_best, ri.near_col};
+                    // the groups that pass, listed warp-wide, one per lane
+                    uint16_t* list = sc.worklist[warp];
+                    const uint32_t lt = lanemask_lt();
+                    int total = 0;
+#pragma unroll
+                    for (int i = 0; i < VEC4; ++i) {
+                        const bool pass = (pmask >> i) & 1u;
+                        const uint32_t b = __ballot_sync(0xffffffffu, pass);
+                        if (pass) list[total + __popc(b & lt)] = static_cast<uint16_t>(i * kCompute + tid);
+                        total += __popc(b);
+                    }
+                    __syncwarp();
+                    const uint64_t fgrow_id = grow_of(j);
+                    for (int n = lane; n < total; n += 32) {
+                        const int f = list[n];
+                        const float4 e4 = fstage[f];
+                        const uint4 w = noise_words_rk(p.rk, fgrow_id, static_cast<uint32_t>((col0 >> 2) + f));
+                        const uint32_t bits = race_group(e4, w, r_w);
+                        if (bits)
+                            wb = race_rescore(bits, p.logits + frow * p.row_stride, col0 + 4 * f, w,
+                                              sc.rq[j & (kRowRing - 1)], ri.near_col, wb);
+                    }
+                    __syncwarp();  // the list is rewritten for the next row
+                    warp_best(wb.best, wb.col);
+                }
+                if (lane == 0) sc.p2[j & (kRowRing - 1)][warp] = wb;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sc.b_done[j & (kRowRing - 1)]);
             }
-            ok = __all_sync(0xffffffffu, ok);
-            if (lane == 0) sc.status = ok ? 0 : 1;
         }
-
-        __syncthreads();  // ============== the barrier of iteration k ===========
-
-        if (sc.abort_load || sc.status) {
-            aborted = true;
-            break;
-        }
-        if (k < nrows) consumed = k + 1;
-
-        // ===================== after the barrier ================================
-        if (exchange) {
+    } else if (warp == kPublisherWarp) {
+        // ======================= publisher warp ==================================
+        // Stage a row: its temperature quotient for the CTA, then the bulk
+        // copy (or, for rows that are not 16-byte aligned, a plain arrival:
+        // the compute warps read global memory).
+        auto issue_row = [&](int r) {
+            if (lane == 0) {
+                const float temp = row_temperature(p, grow_of(r));
+                const ScaledQuotient q = ScaledQuotient::of(fmaxf(temp, kTempFloor));
+                sc.rq[r & (kRowRing - 1)] = RowQuotient{temp, q.t, q.y, q.mode};
+                uint64_t* bar = &sc.full[r % NSTAGE];
+                if (use_tma) {
+                    mbar_arrive_expect_tx(bar, copy_bytes);
+                    if (copy_bytes)
+                        tma_load_1d(smem + (r % NSTAGE) * p.stage_bytes,
+                                    p.logits + row_of(r) * p.row_stride + col0, copy_bytes, bar);
+                } else {
+                    mbar_arrive(bar);
+                }
+            }
+        };
+        int issued = 0;
+        while (issued < nrows && issued < NSTAGE) issue_row(issued++);
+        for (int k = 0; k < nrows + LAG; ++k) {
+            if (*abort_flag) break;
             if (k < nrows) {
-                // ---- first record of row k --------------------------------------
+                // ---- first record of row k ---------------------------------------
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sc.a_done[k & (kRowRing - 1)],
+                                                               static_cast<uint32_t>((k / kRowRing) & 1)))) {
+                    if (lane == 0) fail();
+                    break;
+                }
                 const WarpPartial wp = lane < kComputeWarps
-                                           ? sc.p1[par][lane]
+                                           ? sc.p1[k & (kRowRing - 1)][lane]
                                            : WarpPartial{-INFINITY, 0.0f, 0.0f, -INFINITY, INT_MAX,
                                                          INT_MAX};
                 const float mc = warp_max(wp.m);
@@ -511,119 +568,112 @@ __global__ void __launch_bounds__(kThreads, 1)
                     publish_a(record_a(p.xchg, blockIdx.x, k & (kRing - 1)), record_tag(k), mc, s_c,
                               w_c, a_c, b_c, bcol_c);
             }
-            const int kf = k - LAG - 1;
-            if (kf >= 0 && kf < nrows) {
-                // ---- second record of row k-LAG-1 (its race ran after barrier k-1)
-                const WarpBest wb = lane < kComputeWarps ? sc.p2[kf & 1][lane]
+            const int j = k - LAG;
+            if (j >= 0) {
+                // ---- second record of row j; its stage takes a later row ----------
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sc.b_done[j & (kRowRing - 1)],
+                                                               static_cast<uint32_t>((j / kRowRing) & 1)))) {
+                    if (lane == 0) fail();
+                    break;
+                }
+                const WarpBest wb = lane < kComputeWarps ? sc.p2[j & (kRowRing - 1)][lane]
                                                          : WarpBest{-INFINITY, INT_MAX};
                 float b = wb.best;
                 int bcol = wb.col;
                 warp_best(b, bcol);
                 if (lane == 0)
-                    publish_b(record_b(p.xchg, blockIdx.x, kf & (kRing - 1)), record_tag(kf), b, bcol);
-            }
-            // The stage of row k-LAG-1 was read for the last time before this
-            // barrier: it takes the next row to load.
-            if (use_tma && lane == 0 && kf >= 0 && issued < nrows) {
-                fence_proxy_async_smem();
-                issue_copy();
-            }
-        } else if (k >= LAG && k - LAG < nrows) {
-            // ---- compute warps: second half of row j = k-LAG -----------------------
-            const int j = k - LAG;
-            const RowInfo ri = sc.info[j & (kInfoRing - 1)];
-            const float mw = sc.wref[j & (kInfoRing - 1)][warp];  // M_w of row j
-            const int64_t frow = row_of(j);
-            const uint64_t fgrow_id = grow_of(j);
-            const float4* fstage =
-                reinterpret_cast<const float4*>(smem + (j % kStages) * p.stage_bytes);
-            float4 e[VEC4];
-#pragma unroll
-            for (int i = 0; i < VEC4; ++i) {
-                const int f = i * kCompute + tid;
-                e[i] = (i * kCompute < nslot4 && f < nslot4) ? fstage[f]
-                                                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            }
-            if (ri.noisy) {
-                const float best = ri.near_best;
-                // e^(s - B), widened by the race margin, is e * r_w.
-                const float r_w =
-                    mw == -INFINITY ? 0.0f : ex2_approx(fmaf(mw - best, kLog2e, kRaceMarginLog2));
-                WarpBest wb{best, ri.near_col};
-                uint32_t survivors = 0;
-                // Philox four groups at a time, so that their chains overlap.
-#pragma unroll
-                for (int i0 = 0; i0 < VEC4; i0 += 4) {
-                    constexpr int kGroup = 4;
-                    bool pass[kGroup];
-                    bool any = false;
-#pragma unroll
-                    for (int jj = 0; jj < kGroup; ++jj) {
-                        // 1 - u >= 2^-24 always: below that bound no element of
-                        // the group can win
-                        pass[jj] = i0 + jj < VEC4 && (i0 + jj) * kCompute < nslot4 &&
-                                   max4(e[min(i0 + jj, VEC4 - 1)]) * r_w >= 0x1p-24f;
-                        any |= pass[jj];
-                    }
-                    // warp-uniform: when any lane needs this quad, every lane
-                    // draws its blocks (straight-line, no divergence)
-                    if (__any_sync(0xffffffffu, any)) {
-                        uint4 w[kGroup];
-#pragma unroll
-                        for (int jj = 0; jj < kGroup; ++jj)
-                            if (i0 + jj < VEC4)
-                                w[jj] = noise_words_rk(
-                                    p.rk, fgrow_id,
-                                    static_cast<uint32_t>((col0 >> 2) + (i0 + jj) * kCompute + tid));
-#pragma unroll
-                        for (int jj = 0; jj < kGroup; ++jj)
-                            if (i0 + jj < VEC4 && pass[jj])
-                                survivors |= race_group(e[i0 + jj], w[jj], r_w) << (4 * (i0 + jj));
-                    }
-                }
-                if (survivors)
-                    wb = race_rescore(survivors, p.logits + frow * p.row_stride,
-                                      row_temperature(p, fgrow_id), col0, tid, fgrow_id, p.rk, wb);
-                warp_best(wb.best, wb.col);
-                if (lane == 0) sc.p2[j & 1][warp] = wb;
-            } else if (lane == 0) {
-                sc.p2[j & 1][warp] = WarpBest{-INFINITY, INT_MAX};
-            }
-
-            if (p.probs_dtype != 0) {
-                const float big_m = ri.row_max;
-                // e^(s - M) / S = e * e^(M_w - M) / S
-                const float f_w =
-                    mw == -INFINITY ? 0.0f : ex2_approx(fmaf(mw - big_m, kLog2e, -ri.log2s));
-                const bool bf16 = p.probs_dtype == 1;
-                uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
-#pragma unroll
-                for (int i = 0; i < VEC4; ++i) {
-                    const int f = i * kCompute + tid;
-                    if (i * kCompute >= nslot4 || f >= nslot4) continue;
-                    float pr[4] = {e[i].x * f_w, e[i].y * f_w, e[i].z * f_w, e[i].w * f_w};
-                    if (big_m == -INFINITY) pr[0] = pr[1] = pr[2] = pr[3] = NAN;
-                    const uint32_t lo = pack2(pr[0], pr[1], bf16);
-                    const uint32_t hi = pack2(pr[2], pr[3], bf16);
-                    if (p.probs_vec && f < nfull4) {
-                        __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
-                    } else {
-                        const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
-                                                  static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
-                        for (int q = 0; q < 4; ++q)
-                            if (4 * f + q < ncols) prow[4 * f + q] = code[q];
-                    }
+                    publish_b(record_b(p.xchg, blockIdx.x, j & (kRing - 1)), record_tag(j), b, bcol);
+                if (issued < nrows) {
+                    if (lane == 0) fence_proxy_async_smem();
+                    issue_row(issued++);
                 }
             }
         }
-    }
-
-    if (aborted && tid == 0) raise_device_error(p.err, 1);
-    // Bulk copies still in flight must land before the CTA's shared memory
-    // is released.
-    if (use_tma && exchange && lane == 0) {
-        for (int seq = consumed; seq < issued; ++seq) {
-            mbar_wait_bounded(&sc.full[seq % kStages], static_cast<uint32_t>((seq / kStages) & 1));
+        // Bulk copies still in flight must land before the CTA's shared
+        // memory is released.
+        if (use_tma && lane == 0) {
+            for (int r = issued > NSTAGE ? issued - NSTAGE : 0; r < issued; ++r)
+                mbar_wait_bounded(&sc.full[r % NSTAGE], static_cast<uint32_t>((r / NSTAGE) & 1));
+        }
+    } else {
+        // ======================= poller warp =====================================
+        // Row m's first records, and the second records of row m-LAG-1. The
+        // temperature (for the noise flag) is loaded a row ahead.
+        float temp_m = nrows > 0 ? row_temperature(p, grow_of(0)) : 0.0f;
+        for (int m = 0; m < nrows + LAG + 1; ++m) {
+            if (*abort_flag) break;
+            const float temp = temp_m;
+            if (m + 1 < nrows) temp_m = row_temperature(p, grow_of(m + 1));
+            const bool do_a = m < nrows;
+            const int kb = m - (LAG + 1);
+            const bool do_b = kb >= 0 && kb < nrows;
+            bool ok = true;
+            uint64_t ra[6] = {0, 0, 0, 0, 0, 0}, rb[2] = {0, 0};
+            if (lane < p.team && (do_a || do_b)) {
+                const int cta = team_id * p.team + lane;
+                ok = read_records(do_a ? record_a(p.xchg, cta, m & (kRing - 1)) : nullptr,
+                                  record_tag(m), ra,
+                                  do_b ? record_b(p.xchg, cta, kb & (kRing - 1)) : nullptr,
+                                  record_tag(kb), rb);
+            }
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) fail();
+                break;
+            }
+            const bool have = lane < p.team;
+            if (do_a) {
+                const int64_t frow = row_of(m);
+                const float m_ = have ? payload_f(ra[0]) : -INFINITY;
+                const float s_m = have ? payload_f(ra[1]) : 0.0f;
+                const float w_m = have ? payload_f(ra[2]) : 0.0f;
+                const int a_m = have ? static_cast<int>(payload_u(ra[3])) : INT_MAX;
+                float b_m = have ? payload_f(ra[4]) : -INFINITY;
+                int bc_m = have ? static_cast<int>(payload_u(ra[5])) : INT_MAX;
+                const float big_m = warp_max(m_);
+                float s_l = 0.0f, w_l = 0.0f;
+                if (m_ != -INFINITY) {
+                    const float dm = m_ - big_m;
+                    const float f = ex2_approx(dm * kLog2e);
+                    s_l = f * s_m;
+                    w_l = f * fmaf(dm, s_m, w_m);
+                }
+                const float s_tot = warp_sum_f(s_l);
+                const float w_tot = warp_sum_f(w_l);
+                const int arg_row = warp_min_i(m_ == big_m ? a_m : INT_MAX);
+                warp_best(b_m, bc_m);
+                if (lane == 0) {
+                    RowInfo& ri = sc.info[m & (kRowRing - 1)];
+                    ri.row_max = big_m;
+                    ri.log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
+                    ri.near_best = b_m;
+                    ri.near_col = bc_m;
+                    ri.arg = arg_row;
+                    ri.noisy = temp > 0.0f && big_m != -INFINITY;
+                    mbar_arrive(&sc.info_ready[m & (kRowRing - 1)]);
+                    if (member == 0) {
+                        p.argmax[frow] = arg_row;
+                        p.entropy[frow] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
+                        if (!ri.noisy) p.sample[frow] = arg_row;
+                    }
+                }
+            }
+            if (do_b) {
+                float b = have ? payload_f(rb[0]) : -INFINITY;
+                int bcol = have ? static_cast<int>(payload_u(rb[1])) : INT_MAX;
+                warp_best(b, bcol);
+                if (lane == 0) {
+                    const RowInfo& ri = sc.info[kb & (kRowRing - 1)];
+                    if (ri.noisy && member == 0) {
+                        float bb = ri.near_best;
+                        int bbc = ri.near_col;
+                        if (beats(b, bcol, bb, bbc)) {
+                            bb = b;
+                            bbc = bcol;
+                        }
+                        p.sample[row_of(kb)] = bb != -INFINITY ? bbc : ri.arg;
+                    }
+                }
+            }
         }
     }
 }
@@ -637,7 +687,7 @@ struct RowStatsPlan {
     int vec4;    // float4 slots per compute thread
 };
 
-// Team size G for one CTA per SM with 480 compute threads. The chunk must
+// Team size G for one CTA per SM with 448 compute threads. The chunk must
 // fit the registers and the stages shared memory. An iteration costs about
 // max(chunk, round trip / LAG) + 1500 columns of work, the round trip of the
 // team exchange through L2 (about 2.6 us) being worth some 18000 columns;
