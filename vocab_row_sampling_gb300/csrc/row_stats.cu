@@ -120,8 +120,8 @@ struct RowStatsParams {
 std::atomic<int> g_inject_fault{0};
 
 struct WarpPartial {
-    float m, s, w, best;
-    int arg, best_col;
+    float m, s, w;
+    int arg;
 };
 
 struct WarpBest {
@@ -286,7 +286,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k < nrows) {
                 // ---- first half of row k ---------------------------------------
                 const int64_t row = row_of(k);
-                const uint64_t grow_id = grow_of(k);
                 const float* grow = p.logits + row * p.row_stride + col0;
                 float4* stage4 = reinterpret_cast<float4*>(smem + (k % NSTAGE) * p.stage_bytes);
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sc.full[k % NSTAGE],
@@ -299,7 +298,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sq.t = rq.t;
                 sq.y = rq.y;
                 sq.mode = rq.mode;
-                const bool noisy = rq.temp > 0.0f;
                 float4 v[VEC4];
 #pragma unroll
                 for (int i = 0; i < VEC4; ++i) {
@@ -323,18 +321,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 
                 // max of the raw logits (division by Te > 0 keeps the order)
+                float m4[VEC4];
                 float mt = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < VEC4; ++i) mt = fmaxf(mt, max4(v[i]));
+                for (int i = 0; i < VEC4; ++i) {
+                    m4[i] = max4(v[i]);
+                    mt = fmaxf(mt, m4[i]);
+                }
                 const float mxw = warp_max(mt);
                 const float mw = mxw == -INFINITY ? -INFINITY : sq.exact(mxw);  // M_w
                 // warp-uniform: raw domain, or exact quotients first
                 const bool raw = !(fabsf(mw) >= kRawDomainLimit);
-                float cthr;  // argmax candidates: v >= cthr
-                if (raw) {
-                    // exact(x) == M_w needs x >= mxw - Te * ulp(M_w)
-                    cthr = mxw - fmaxf(fabsf(mxw) * 0x1p-20f, rq.t * 0x1p-140f);
-                } else {
+                // argmax: the lowest column whose exact quotient is M_w.
+                // exact(x) == M_w needs x >= mxw - Te * ulp(M_w), so only the
+                // slots whose max reaches that are searched, their logits
+                // read again (the stage still holds them).
+                const float cthr = mxw - fmaxf(fabsf(mxw) * 0x1p-20f, rq.t * 0x1p-140f);
+                int arg_t = INT_MAX;
+                if (mt >= cthr && mw != -INFINITY) {
+                    uint32_t smask = 0;
+#pragma unroll
+                    for (int i = 0; i < VEC4; ++i)
+                        if (m4[i] >= cthr) smask |= 1u << i;
+#pragma unroll 1
+                    while (smask && arg_t == INT_MAX) {
+                        const int i = __ffs(smask) - 1;
+                        smask &= smask - 1;
+                        const int f = i * kCompute + tid;
+                        float4 x4;
+                        if (use_tma && f < nfull4) {
+                            x4 = stage4[f];
+                        } else {
+                            x4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                            for (int q = 0; q < 4 && 4 * f + q < ncols; ++q) set_comp(x4, q, grow[4 * f + q]);
+                        }
+#pragma unroll 1
+                        for (int q = 0; q < 4; ++q) {
+                            const float x = comp(x4, q);
+                            if (x >= cthr && sq.exact(x) == mw) {
+                                arg_t = col0 + 4 * f + q;
+                                break;
+                            }
+                        }
+                    }
+                }
+                const int aw = warp_min_i(arg_t);
+                if (!raw) {
 #pragma unroll
                     for (int i = 0; i < VEC4; ++i) {
                         v[i].x = sq.exact(v[i].x);
@@ -342,31 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         v[i].z = sq.exact(v[i].z);
                         v[i].w = sq.exact(v[i].w);
                     }
-                    mt = sq.exact(mt);
-                    cthr = mw;
                 }
-
-                // argmax: the lowest column whose exact quotient is M_w
-                int arg_t = INT_MAX;
-                if (mt >= cthr && mw != -INFINITY) {
-                    uint64_t cand = 0;  // bit 4i+q: columns in increasing order
-#pragma unroll
-                    for (int i = 0; i < VEC4; ++i)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (comp(v[i], q) >= cthr) cand |= 1ull << (4 * i + q);
-#pragma unroll 1
-                    while (cand) {
-                        const int b = __ffsll(static_cast<long long>(cand)) - 1;
-                        cand &= cand - 1;
-                        const float x = pick(v, b);
-                        if ((raw ? sq.exact(x) : x) == mw) {
-                            arg_t = col0 + 4 * ((b >> 2) * kCompute + tid) + (b & 3);
-                            break;
-                        }
-                    }
-                }
-                const int aw = warp_min_i(arg_t);
 
                 // t = (s - M_w) log2(e): raw domain x * log2(e)/Te - c with
                 // c = RN(mxw * log2(e)/Te), else (s - M_w) * log2(e); -inf
@@ -404,19 +412,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (f < nslot4) stage4[f] = ev;
                     }
                 }
-                // B candidate: the Gumbel-max score of the warp's argmax element
-                float bs = -INFINITY;
-                int bc = INT_MAX;
-                if (noisy && aw != INT_MAX && arg_t == aw) {
-                    const uint4 w = noise_words_rk(p.rk, grow_id, static_cast<uint32_t>(aw >> 2));
-                    bs = mw + gumbel_of_bits(word_of(w, aw & 3));
-                    bc = aw;
-                }
                 const float sw = warp_sum_f((st[0] + st[1]) + (st[2] + st[3]));
                 const float ww = warp_sum_f((wt[0] + wt[1]) + (wt[2] + wt[3])) * kLn2;
-                warp_best(bs, bc);
                 if (lane == 0) {
-                    sc.p1[k & (kRowRing - 1)][warp] = WarpPartial{mw, sw, ww, bs, aw, bc};
+                    sc.p1[k & (kRowRing - 1)][warp] = WarpPartial{mw, sw, ww, aw};
                     sc.wref[k & (kRowRing - 1)][warp] = mw;
                 }
                 __syncwarp();
@@ -519,9 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Stage a row: its temperature quotient for the CTA, then the bulk
         // copy (or, for rows that are not 16-byte aligned, a plain arrival:
         // the compute warps read global memory).
+        float temp_next = nrows > 0 && lane == 0 ? row_temperature(p, grow_of(0)) : 0.0f;
         auto issue_row = [&](int r) {
             if (lane == 0) {
-                const float temp = row_temperature(p, grow_of(r));
+                const float temp = temp_next;
+                if (r + 1 < nrows) temp_next = row_temperature(p, grow_of(r + 1));
                 const ScaledQuotient q = ScaledQuotient::of(fmaxf(temp, kTempFloor));
                 sc.rq[r & (kRowRing - 1)] = RowQuotient{temp, q.t, q.y, q.mode};
                 uint64_t* bar = &sc.full[r % NSTAGE];
@@ -548,8 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const WarpPartial wp = lane < kComputeWarps
                                            ? sc.p1[k & (kRowRing - 1)][lane]
-                                           : WarpPartial{-INFINITY, 0.0f, 0.0f, -INFINITY, INT_MAX,
-                                                         INT_MAX};
+                                           : WarpPartial{-INFINITY, 0.0f, 0.0f, INT_MAX};
                 const float mc = warp_max(wp.m);
                 float s_l = 0.0f, w_l = 0.0f;
                 if (wp.m != -INFINITY) {
@@ -561,8 +561,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float s_c = warp_sum_f(s_l);
                 const float w_c = warp_sum_f(w_l);
                 const int a_c = mc == -INFINITY ? col0 : warp_min_i(wp.m == mc ? wp.arg : INT_MAX);
-                float b_c = wp.best;
-                int bcol_c = wp.best_col;
+                // B candidates: the Gumbel-max score of each warp's argmax
+                // element, one lane per warp
+                float b_c = -INFINITY;
+                int bcol_c = INT_MAX;
+                if (sc.rq[k & (kRowRing - 1)].temp > 0.0f && wp.arg != INT_MAX) {
+                    const uint4 w = noise_words_rk(p.rk, grow_of(k), static_cast<uint32_t>(wp.arg >> 2));
+                    b_c = wp.m + gumbel_of_bits(word_of(w, wp.arg & 3));
+                    bcol_c = wp.arg;
+                }
                 warp_best(b_c, bcol_c);
                 if (lane == 0 && !(p.fault && blockIdx.x == 0 && k == 0))
                     publish_a(record_a(p.xchg, blockIdx.x, k & (kRing - 1)), record_tag(k), mc, s_c,
