@@ -288,13 +288,28 @@ def _run_ours(args, world, rank, local):
     return out
 
 
+def kernel_source_hash():
+    """sha256 over the sources of the row-statistics kernel: a traffic figure
+    taken from an ncu capture is used only while they are unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in ("vocab_row_sampling_gb300/csrc/row_stats.cu",
+                "vocab_row_sampling_gb300/csrc/drs_device.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _traffic_from_profile():
-    """DRAM bytes per launch of the row-stats kernel from the committed ncu
-    summary, if one matches the current kernel (else null)."""
+    """DRAM bytes (read + write) per launch of the row-stats kernel from the
+    committed ncu capture of the step workload, if it was taken on the
+    current kernel sources (else null)."""
     path = os.path.join(ROOT, "profiles", "row_stats_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
+        if d.get("source_sha256") != kernel_source_hash():
+            return None
         return d.get("dram_bytes_per_launch")
     except Exception:
         return None
