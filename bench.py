@@ -1,17 +1,20 @@
 """Benchmark of the DiffusionGemma row-statistics hot path on GB300.
 
-One step = one pass of the whole path over one batch: drs_row_stats (argmax,
-Gumbel-max sample, entropy, bf16 softmax) over 2048 x 262144 fp32 logits,
-then drs_topk_logprobs (k = 20) over the rows of the converged (even)
-slots. Inputs are synthetic (workloads.py, "step") and resident in HBM when
-the timed region starts; at 2.1 GB they are larger than L2, so no flush is
-needed between steps.
+One step = one pass of the whole path over one batch: drs_row_stats_topk,
+the row statistics (argmax, Gumbel-max sample, entropy, bf16 softmax) of
+2048 x 262144 fp32 logits and the top-k logprobs (k = 20) of the rows of the
+converged (even) slots, from one read of the logits. Inputs are synthetic
+(workloads.py, "step") and resident in HBM when the timed region starts; at
+2.1 GB they are larger than L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0). `value` is rows/s over all GPUs; `roofline`
-describes the row-statistics kernel (algorithmic bytes rows*stride*4 read +
-rows*V*2 written per launch over its CUDA-event time); `e2e` repeats the step
-through the public API from pinned host buffers, copies included;
-`cpu_baseline` times the CPU oracle on a bounded sample of the same rows.
+describes the row kernel (algorithmic bytes rows*stride*4 read + rows*V*2
+written per call over the call's CUDA-event time, which also covers the
+exact top-k kernel that follows it and exits at once when no row needs
+it); `kernels` adds the two separate calls (drs_row_stats, then
+drs_topk_logprobs) timed briefly; `e2e` repeats the step through the public
+API from pinned host buffers, copies included; `cpu_baseline` times the CPU
+oracle on a bounded sample of the same rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --rows 256 --no-e2e --cpu-seconds 0   (a smaller case of
@@ -175,6 +178,14 @@ def global_temps(temps_local, rank: int, rows: int, canvas_len: int):
     return out
 
 
+def global_keep(keep_local, rank: int, rows: int, canvas_len: int):
+    """The keep flags indexed by global slot, like global_temps."""
+    _, slot0 = shard_layout(rank, rows, canvas_len)
+    out = torch.zeros(slot0 + keep_local.numel(), dtype=torch.uint8, device=keep_local.device)
+    out[slot0:] = keep_local
+    return out
+
+
 def _run_ours(args, world, rank, local):
     import vocab_row_sampling_gb300 as drs
     drs.load(build_if_missing=True)
@@ -188,6 +199,7 @@ def _run_ours(args, world, rank, local):
     dev = logits.device
     stream = torch.cuda.current_stream()
     temps_all = global_temps(temps, rank, rows, w["canvas_len"])
+    keep_all = global_keep(keep, rank, rows, w["canvas_len"])
 
     argmax = torch.empty(rows, dtype=torch.int64, device=dev)
     sample = torch.empty(rows, dtype=torch.int64, device=dev)
@@ -197,17 +209,32 @@ def _run_ours(args, world, rank, local):
     lps = torch.empty(rows, k, dtype=torch.float32, device=dev)
     ws_rs = drs.workspace(drs.drs_row_stats_workspace_bytes(rows, V), dev)
     ws_tk = drs.workspace(drs.drs_topk_workspace_bytes(rows, V, k), dev)
+    ws_fused = drs.workspace(drs.drs_row_stats_topk_workspace_bytes(rows, V, k), dev)
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        drs.drs_row_stats(logits, temps_all, w["canvas_len"], 0, argmax, sample, entropy,
-                          drs.DRS_PROBS_BF16, probs, ws_rs, stream, row0=row0)
+        drs.drs_row_stats_topk(logits, temps_all, w["canvas_len"], 0, argmax, sample, entropy,
+                               drs.DRS_PROBS_BF16, probs, keep_all, k, ids, lps, ws_fused,
+                               stream, row0=row0)
         if ev is not None:
             ev[1].record(stream)
-        drs.drs_topk_logprobs(logits, temps, w["canvas_len"], keep, k, ids, lps, ws_tk, stream)
-        if ev is not None:
-            ev[2].record(stream)
+
+    def separate(n=3):
+        """The two separate calls, timed briefly (context for the fused one)."""
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        rs, tk = [], []
+        for _ in range(n + 1):
+            evs[0].record(stream)
+            drs.drs_row_stats(logits, temps_all, w["canvas_len"], 0, argmax, sample, entropy,
+                              drs.DRS_PROBS_BF16, probs, ws_rs, stream, row0=row0)
+            evs[1].record(stream)
+            drs.drs_topk_logprobs(logits, temps, w["canvas_len"], keep, k, ids, lps, ws_tk, stream)
+            evs[2].record(stream)
+            torch.cuda.synchronize()
+            rs.append(evs[0].elapsed_time(evs[1]))
+            tk.append(evs[1].elapsed_time(evs[2]))
+        return sum(rs[1:]) / n, sum(tk[1:]) / n
 
     for _ in range(args.warmup):
         step()
@@ -216,7 +243,7 @@ def _run_ours(args, world, rank, local):
         raise RuntimeError("device-side wait timed out during warm-up")
 
     def timed():
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         _barrier(world)
         torch.cuda.synchronize()
@@ -229,12 +256,11 @@ def _run_ours(args, world, rank, local):
         _barrier(world)
         total_ms = start.elapsed_time(stop)
         rs_ms = [e[0].elapsed_time(e[1]) for e in evs]
-        tk_ms = [e[1].elapsed_time(e[2]) for e in evs]
-        return total_ms, rs_ms, tk_ms, clk.summary()
+        return total_ms, rs_ms, clk.summary()
 
-    total_ms, rs_ms, tk_ms, clocks = timed()
+    total_ms, rs_ms, clocks = timed()
     if _clocks_rejected(clocks):
-        total_ms, rs_ms, tk_ms, clocks = timed()
+        total_ms, rs_ms, clocks = timed()
         clocks["remeasured"] = True
     if drs.drs_get_device_error() != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
@@ -243,7 +269,7 @@ def _run_ours(args, world, rank, local):
     value = world * rows * args.steps / (total_ms / 1e3)
 
     rs_avg_ms = sum(rs_ms) / len(rs_ms)
-    tk_avg_ms = sum(tk_ms) / len(tk_ms)
+    sep_rs_ms, tk_avg_ms = separate()
     bytes_rs = rows * stride * 4 + rows * V * 2
     kept_rows = int(keep[: rows // w["canvas_len"]].sum().item()) * w["canvas_len"]
     bytes_tk = kept_rows * V * 4
@@ -251,7 +277,8 @@ def _run_ours(args, world, rank, local):
     achieved = bytes_rs / (rs_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(),
-                "kernel": "row_stats_kernel", "peak_kind": f"{peak_kind} copy bandwidth",
+                "kernel": "row_stats_kernel (drs_row_stats_topk call)",
+                "peak_kind": f"{peak_kind} copy bandwidth",
                 "bytes_per_launch": bytes_rs, "avg_launch_ms": round(rs_avg_ms, 4)}
 
     out = {"metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
@@ -264,20 +291,24 @@ def _run_ours(args, world, rank, local):
                       "kept_rows": kept_rows,
                       "l2": "inputs (2.1 GB) larger than L2 (126 MB); no flush"},
            "roofline": roofline,
-           "kernels": {"row_stats": {"avg_ms": round(rs_avg_ms, 4),
-                                     "rows_per_s": round(rows / (rs_avg_ms / 1e3), 1),
-                                     "gbs": round(achieved, 1),
-                                     "frac_of_peak": round(achieved / peak, 4)},
+           "kernels": {"row_stats_topk": {"avg_ms": round(rs_avg_ms, 4),
+                                          "rows_per_s": round(rows / (rs_avg_ms / 1e3), 1),
+                                          "gbs": round(achieved, 1),
+                                          "frac_of_peak": round(achieved / peak, 4)},
+                       "row_stats_alone": {"avg_ms": round(sep_rs_ms, 4),
+                                           "gbs": round(bytes_rs / (sep_rs_ms / 1e3) / 1e9, 1),
+                                           "frac_of_peak": round(bytes_rs / (sep_rs_ms / 1e3)
+                                                                 / 1e9 / peak, 4)},
                        "topk_logprobs": {"avg_ms": round(tk_avg_ms, 4),
                                          "gbs_read": round(bytes_tk / (tk_avg_ms / 1e3) / 1e9, 1),
                                          "frac_of_peak": round(bytes_tk / (tk_avg_ms / 1e3) / 1e9
                                                                / peak, 4)}},
-           "gpu_launches": 2 * args.steps,
+           "gpu_launches": 2 * args.steps,  # the row kernel and the exact top-k kernel
            "clocks": clocks}
 
     # end to end through the public API from pinned host memory
     if not args.no_e2e:
-        out["e2e"] = _e2e(args, drs, w, rank, world, row0, temps_all, keep, k)
+        out["e2e"] = _e2e(args, drs, w, rank, world, row0, temps_all, keep_all, k)
     if rows != workloads.WORKLOADS[WORKLOAD].rows:
         out["config"]["workload"] = (f"step recipe at {rows} x {V} (a smaller case, "
                                      "not the headline workload)")
@@ -337,8 +368,7 @@ def _e2e(args, drs, w, rank, world, row0, temps_all, keep, k):
     ids = torch.empty(rows, k, dtype=torch.int32, device=dev)
     lps = torch.empty(rows, k, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    ws_rs = drs.workspace(drs.drs_row_stats_workspace_bytes(rows, V), dev)
-    ws_tk = drs.workspace(drs.drs_topk_workspace_bytes(rows, V, k), dev)
+    ws = drs.workspace(drs.drs_row_stats_topk_workspace_bytes(rows, V, k), dev)
     h2d = host.numel() * 4 + temps_h.numel() * 4 + keep_h.numel()
     d2h = rows * (8 + 8 + 4) + rows * k * (4 + 4)
 
@@ -346,10 +376,9 @@ def _e2e(args, drs, w, rank, world, row0, temps_all, keep, k):
         d_logits.copy_(host, non_blocking=True)
         d_temps.copy_(temps_h, non_blocking=True)
         d_keep.copy_(keep_h, non_blocking=True)
-        drs.drs_row_stats(d_logits, d_temps, w["canvas_len"], 0, argmax, sample, entropy,
-                          drs.DRS_PROBS_BF16, probs, ws_rs, stream, row0=row0)
-        drs.drs_topk_logprobs(d_logits, d_temps[rank * (rows // w["canvas_len"]):],
-                              w["canvas_len"], d_keep, k, ids, lps, ws_tk, stream)
+        drs.drs_row_stats_topk(d_logits, d_temps, w["canvas_len"], 0, argmax, sample, entropy,
+                               drs.DRS_PROBS_BF16, probs, d_keep, k, ids, lps, ws, stream,
+                               row0=row0)
         outs_h["argmax"].copy_(argmax, non_blocking=True)
         outs_h["sample"].copy_(sample, non_blocking=True)
         outs_h["entropy"].copy_(entropy, non_blocking=True)

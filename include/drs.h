@@ -133,6 +133,50 @@ drs_status drs_row_stats_noalloc(const float *logits, int64_t rows, int64_t voca
                                  int64_t probs_row_stride, void *stream);
 
 /*
+ * Bytes of device workspace drs_row_stats_topk needs for k > 0 (256-byte
+ * aligned, contents arbitrary: each call clears what it uses with
+ * asynchronous memsets on its stream). 0 for k <= 0, where the call needs
+ * drs_row_stats_workspace_bytes() instead. Same sharing rule as the
+ * row-stats workspace.
+ */
+size_t drs_row_stats_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k);
+
+/*
+ * drs_row_stats and the top-k logprobs of the rows of converged slots in
+ * one read of the logits (the module docstring's one read per row, and
+ * stash_converged_logprobs / _lp_topk_kernel on the page above, whose
+ * stash reads the kept rows again). Every argument of drs_row_stats has its
+ * meaning there; in addition:
+ *
+ *   keep        uint8 [ceil((row0 + rows) / canvas_len)], one per slot of
+ *               the whole batch like temps: global row r is converged when
+ *               keep[r / canvas_len] != 0.
+ *   k           0 <= k <= min(vocab, 1024); k == 0 is drs_row_stats (with
+ *               its workspace size).
+ *   out_ids     int32 [rows, k]: for a converged row, the columns of the k
+ *               largest scaled logits, ordered by value and then by lower
+ *               column (-0.0 equals +0.0). Rows of other slots are not
+ *               written.
+ *   out_logprobs fp32 [rows, k]: scaled - max - log(sum exp(scaled - max))
+ *               of those columns (NaN for a row that is -inf everywhere).
+ *   workspace   drs_row_stats_topk_workspace_bytes(rows, vocab, k) bytes.
+ *
+ * For k <= 64 one kernel reads each row once; rows whose top-k candidates
+ * overflow its fixed buffers (many equal values) are finished by a second,
+ * exact kernel on the same stream that reads only those rows. For k > 64
+ * the row statistics and the exact top-k kernel run one after the other.
+ */
+drs_status drs_row_stats_topk(const float *logits, int64_t rows, int64_t vocab,
+                              int64_t row_stride, const float *temps,
+                              int64_t canvas_len, uint64_t seed, int64_t row0,
+                              int64_t *argmax, int64_t *sample, float *entropy,
+                              drs_probs_dtype probs_dtype, void *probs,
+                              int64_t probs_row_stride, const uint8_t *keep,
+                              int32_t k, int32_t *out_ids, float *out_logprobs,
+                              void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
  * Bytes of device workspace drs_topk_logprobs needs (256-byte aligned,
  * contents arbitrary). Same sharing rule as the row-stats workspace.
  */
@@ -153,6 +197,11 @@ size_t drs_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k);
  *               column (-0.0 equals +0.0).
  *   out_logprobs fp32 [rows, k]: scaled - max - log(sum exp(scaled - max))
  *               of those columns (NaN for a row that is -inf everywhere).
+ *
+ * For k <= 64 this runs the kernel of drs_row_stats_topk with the row
+ * statistics off (rows of unconverged slots are neither read nor
+ * exchanged); larger k, and rows with many equal values, use the exact
+ * top-k kernel.
  */
 drs_status drs_topk_logprobs(const float *logits, int64_t rows, int64_t vocab,
                              int64_t row_stride, const float *temps,

@@ -8,11 +8,12 @@ into the library needs the built ``libdrs.so`` and a CUDA device, and raises
 otherwise.
 
 Entry points (same names as the C ABI):
-  drs_row_stats, drs_row_stats_workspace_bytes, drs_topk_logprobs,
+  drs_row_stats, drs_row_stats_workspace_bytes, drs_row_stats_noalloc,
+  drs_row_stats_topk, drs_row_stats_topk_workspace_bytes, drs_topk_logprobs,
   drs_topk_workspace_bytes, drs_philox_gumbel, drs_scaled_logits,
   drs_status_string, drs_get_device_error.
-Convenience wrappers that allocate outputs: row_stats, topk_logprobs,
-philox_gumbel.
+Convenience wrappers that allocate outputs: row_stats, row_stats_topk,
+topk_logprobs, philox_gumbel.
 """
 from __future__ import annotations
 
@@ -31,7 +32,7 @@ DRS_PROBS_NONE, DRS_PROBS_BF16, DRS_PROBS_FP16 = 0, 1, 2
 DRS_MAX_VOCAB = 491520
 
 EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_row_stats_noalloc",
-            "drs_topk_logprobs",
+            "drs_row_stats_topk", "drs_row_stats_topk_workspace_bytes", "drs_topk_logprobs",
             "drs_topk_workspace_bytes", "drs_philox_gumbel", "drs_scaled_logits",
             "drs_status_string", "drs_get_device_error", "drs_test_inject_fault")
 
@@ -71,6 +72,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_row_stats_noalloc.argtypes = [vp, i64, i64, i64, vp, i64, u64, i64, vp, vp, vp,
                                           ctypes.c_int, vp, i64, vp]
     lib.drs_row_stats_noalloc.restype = ctypes.c_int
+    lib.drs_row_stats_topk_workspace_bytes.argtypes = [i64, i64, i32]
+    lib.drs_row_stats_topk_workspace_bytes.restype = sz
+    lib.drs_row_stats_topk.argtypes = [vp, i64, i64, i64, vp, i64, u64, i64, vp, vp, vp,
+                                       ctypes.c_int, vp, i64, vp, i32, vp, vp, vp, sz, vp]
+    lib.drs_row_stats_topk.restype = ctypes.c_int
     lib.drs_topk_workspace_bytes.argtypes = [i64, i64, i32]
     lib.drs_topk_workspace_bytes.restype = sz
     lib.drs_topk_logprobs.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp, vp, sz, vp]
@@ -151,6 +157,25 @@ def drs_row_stats_noalloc(logits, temps, canvas_len, seed, argmax, sample, entro
     _check(st, "drs_row_stats_noalloc")
 
 
+def drs_row_stats_topk_workspace_bytes(rows: int, vocab: int, k: int) -> int:
+    return int(load().drs_row_stats_topk_workspace_bytes(rows, vocab, k))
+
+
+def drs_row_stats_topk(logits, temps, canvas_len, seed, argmax, sample, entropy, probs_dtype,
+                       probs, keep, k, out_ids, out_logprobs, workspace=None, stream=None, row0=0):
+    """Launch drs_row_stats_topk (row statistics and the top-k logprobs of
+    converged rows, one read of the logits) on torch CUDA tensors."""
+    rows, vocab = logits.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    pstride = 0 if probs is None else probs.stride(0)
+    st = load().drs_row_stats_topk(_ptr(logits), rows, vocab, _row_stride(logits), _ptr(temps),
+                                   canvas_len, seed & (2**64 - 1), row0, _ptr(argmax),
+                                   _ptr(sample), _ptr(entropy), probs_dtype, _ptr(probs), pstride,
+                                   _ptr(keep), k, _ptr(out_ids), _ptr(out_logprobs),
+                                   _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "drs_row_stats_topk")
+
+
 def drs_topk_workspace_bytes(rows: int, vocab: int, k: int) -> int:
     return int(load().drs_topk_workspace_bytes(rows, vocab, k))
 
@@ -223,6 +248,33 @@ def row_stats(logits, temps, canvas_len: int, seed: int, probs_dtype=None, strea
     drs_row_stats(logits, temps, canvas_len, seed, argmax, sample, entropy, code, probs, ws,
                   stream, row0)
     return argmax, sample, entropy, probs
+
+
+def row_stats_topk(logits, temps, canvas_len: int, seed: int, keep, k: int, probs_dtype=None,
+                   out_ids=None, out_logprobs=None, stream=None, row0: int = 0):
+    """Allocate outputs and run drs_row_stats_topk; returns (argmax, sample,
+    entropy, probs, out_ids, out_logprobs). Rows of unconverged slots keep
+    the given (or -1 / NaN filled) top-k outputs."""
+    import torch
+    rows, vocab = logits.shape
+    dev = logits.device
+    argmax = torch.empty(rows, dtype=torch.int64, device=dev)
+    sample = torch.empty(rows, dtype=torch.int64, device=dev)
+    entropy = torch.empty(rows, dtype=torch.float32, device=dev)
+    code = {None: DRS_PROBS_NONE, torch.bfloat16: DRS_PROBS_BF16,
+            torch.float16: DRS_PROBS_FP16}[probs_dtype]
+    probs = None if probs_dtype is None else torch.empty(rows, vocab, dtype=probs_dtype, device=dev)
+    if out_ids is None:
+        out_ids = torch.full((rows, k), -1, dtype=torch.int32, device=dev)
+    if out_logprobs is None:
+        out_logprobs = torch.full((rows, k), float("nan"), dtype=torch.float32, device=dev)
+    if rows == 0:
+        return argmax, sample, entropy, probs, out_ids, out_logprobs
+    ws = workspace(max(drs_row_stats_topk_workspace_bytes(rows, vocab, k),
+                       drs_row_stats_workspace_bytes(rows, vocab)), dev)
+    drs_row_stats_topk(logits, temps, canvas_len, seed, argmax, sample, entropy, code, probs,
+                       keep, k, out_ids, out_logprobs, ws, stream, row0)
+    return argmax, sample, entropy, probs, out_ids, out_logprobs
 
 
 def topk_logprobs(logits, temps, canvas_len: int, keep, k: int, out_ids=None,

@@ -32,4 +32,15 @@ inline bool aligned(const void* p, size_t a) {
 
 constexpr size_t kWorkspaceAlign = 256;
 
+// The exact top-k kernel (topk.cu): every converged row of the call, or
+// only the rows of a device list (row_list[0] the count, the rows from
+// row_list[64]) that an earlier kernel on the stream wrote. Temperatures and
+// keep flags are indexed by global slot (row0 + row) / canvas_len.
+size_t exact_topk_workspace_bytes(int32_t k);
+int32_t exact_topk_max_k();
+drs_status exact_topk(const float* logits, int64_t rows, int64_t vocab, int64_t row_stride,
+                      int64_t row0, const float* temps, int64_t canvas_len, const uint8_t* keep,
+                      const int32_t* row_list, int32_t k, int32_t* out_ids, float* out_logprobs,
+                      void* workspace, cudaStream_t stream);
+
 }  // namespace drs

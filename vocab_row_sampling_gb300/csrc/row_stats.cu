@@ -1,7 +1,9 @@
 // row_stats.cu -- one-read row statistics of temperature-scaled logits:
 // argmax, Gumbel-max sample, softmax entropy and (optionally) the softmax in
 // bf16/fp16 (page "vllm.model_executor.models.diffusion_gemma_sampler",
-// module docstring, sample_row_stats and sample_row_stats_reference).
+// module docstring, sample_row_stats and sample_row_stats_reference), and in
+// the same read the top-k logprobs of the rows of converged slots
+// (stash_converged_logprobs, _lp_topk_kernel).
 //
 // Layout of the work. A row of V fp32 logits is split into G contiguous
 // chunks of `chunk` columns (a multiple of 4). G CTAs -- a team -- own the G
@@ -18,32 +20,46 @@
 //     of the scaled logits s = x / Te (Te = max(T, 1e-10)) and the lowest
 //     column reaching it (the argmax), e = e^(s - M_w) written back into the
 //     stage, S_w = sum e and W_w = sum e (s - M_w) (the "online max and
-//     sum" of the page), and for T > 0 the Gumbel-max score of the warp's
-//     argmax element (a lower bound B of the row's best score); arrive on
-//     the row's first-half barrier. Division by Te > 0 is monotone, so while
-//     |M_w| < 256 the warp works on the raw logits: the max is found among
-//     them, only the few candidates for the argmax are divided (exactly),
-//     and e = 2^(x log2(e) / Te - c) with c the rounded reference is within
-//     a relative 2^-15 of e^(s - M_w). Warps with larger scaled values
-//     divide every logit exactly first.
-//   second half of row k-LAG, once the poller has merged the row: the
-//     probabilities e * e^(M_w - M) / S (rounded to nearest even, written to
-//     HBM), then the pruned race against the row's B (an element can only
-//     win if 1 - u <= -log u <= e^(s - B) = e * e^(M_w - B); the float4
-//     groups that pass a bound on their largest e go on a per-warp list,
-//     shared out one Philox call per lane; the few survivors are rescored
-//     exactly from their logits); arrive on the row's second-half barrier,
-//     which also frees the stage.
+//     sum" of the page); arrive on the row's first-half barrier. Division by
+//     Te > 0 is monotone, so while |M_w| < 256 the warp works on the raw
+//     logits: the max is found among them, only the few candidates for the
+//     argmax are divided (exactly), and e = 2^(x log2(e) / Te - c) with c the
+//     rounded reference is within a relative 2^-15 of e^(s - M_w). Warps
+//     with larger scaled values divide every logit exactly first.
+//   second half of row k-LAG, once the poller has merged the row:
+//     - the probabilities e * e^(M_w - M) / S (rounded to nearest even,
+//       written to HBM);
+//     - the pruned race against the row's B, the best Gumbel-max score of
+//       the warps' argmax elements (an element can only win if
+//       1 - u <= -log u <= e^(s - B) = e * e^(M_w - B); the float4 groups
+//       that pass a bound on their largest e go on a per-warp list, shared
+//       out one Philox call per lane; the few survivors are rescored
+//       exactly from their logits);
+//     - for a converged row, the top-k candidates: the logits at or above
+//       the row's threshold, rescored exactly and keyed by (value, lower
+//       column) into the CTA's list. The threshold is the least, over the
+//       team's G CTAs, of each CTA's r-th largest warp maximum, r =
+//       ceil(k / G): G * r >= k distinct elements reach it, so the row's top
+//       k all do;
+//     then arrive on the row's second-half barrier, which frees the stage.
 // Publisher warp: per row, combines the compute warps' first-half partials
-//   into the CTA's first record and publishes it; two rows later combines
-//   their race bests into the second record, publishes it, and refills the
-//   freed stage with a later row (bulk copy), with that row's temperature
-//   quotient computed once for the CTA.
-// Poller warp: per row, reads the team's first records (M, S, W, argmax, B)
-//   and merges them for the compute warps, and reads the second records of
-//   an earlier row; member 0 writes argmax, entropy and sample.
+//   into the CTA's first record (with the Gumbel-max scores of the warps'
+//   argmax elements, one lane per warp, and the CTA's r-th largest raw warp
+//   maximum when top-k is on) and publishes it; LAG rows later publishes the race best
+//   and the CTA's top-k candidates (the k best when there are more), and
+//   refills the freed stage with a later row (bulk copy), that row's
+//   temperature quotient computed once for the CTA.
+// Poller warp: per row, reads the team's first records (M, S, W, argmax, B,
+//   the threshold candidates) and merges them for the compute warps; member 0 writes
+//   argmax and entropy. For the row LAG+1 earlier it reads the race bests
+//   (member 0 writes the sample) and the team's top-k candidates: every CTA
+//   ranks its own candidates among all of them and writes rank r < k to
+//   position r with logprob s - M - log S. A row whose candidates overflow
+//   the fixed buffers (many equal values, or too few warp maxima for a
+//   threshold) goes on a list that the exact top-k kernel finishes.
 // LAG rows between a row's halves cover the team exchange, a round trip
-// through L2.
+// through L2. In top-k-only mode the rows of unconverged slots are skipped
+// (no read, no exchange) but keep their place in the barrier protocol.
 //
 // HBM traffic: every logit is read once (by the bulk copy) and every
 // probability written once. No fp64 arithmetic (its rate on GB300 is a
@@ -76,8 +92,17 @@ constexpr int kRowRing = 8;                   // per-row shared state, by row % 
 constexpr int kVec4Lag2 = 6;
 constexpr int kVec4Lag1 = 9;
 constexpr int kMaxStages = 5;
-constexpr int kMaxVec4Slots = 9;
 static_assert(kRing >= 2 * 2 + 2, "exchange ring too short for LAG 2");
+
+// Top-k in the row kernel.
+constexpr int kTopkMaxK = 64;          // larger k use the exact top-k kernel
+constexpr int kTopkCtaCap = 128;       // candidates of one CTA row
+constexpr int kTopkRowCap = 512;       // candidates of one team row
+constexpr int kTopkRing = 4;           // CTA candidate lists, by row % 4
+constexpr uint32_t kHardRow = 0xFFFFFFFFu;  // count word: candidates overflowed
+constexpr int kAWords = 6;             // first record: M, S, W, argmax, B, B column
+constexpr int kAWordsTopk = kAWords + 2;  // + the CTA's threshold candidate (and a pad word)
+constexpr int kHardListOffset = 64;    // int32 index of the first row of the hard-row list
 
 // log2(1.0002): the race's bound e^(s - best) is widened by 2e-4 so that
 // rounding in it (at most a relative 2^-15 for e taken from the raw
@@ -99,9 +124,12 @@ struct RowStatsParams {
     float* entropy;
     void* probs;
     int64_t probs_row_stride;
-    void* xchg;         // records: per CTA, kRing A slots (M, S, W, argmax,
-                        // B) and kRing B slots (race best)
+    uint64_t* xchg;     // exchange records, xstride words per CTA
     int* err;
+    const uint8_t* keep;  // per global slot (top-k rows), or null: every row
+    int32_t* out_ids;
+    float* out_lp;
+    int32_t* hard;        // [0]: count; rows from [kHardListOffset]
     PhiloxRoundKeys rk;
     int32_t vocab;
     int32_t team;       // CTAs per row
@@ -113,6 +141,10 @@ struct RowStatsParams {
     int32_t probs_vec;  // 8-byte probability stores are aligned
     int32_t index32;    // global rows and canvas_len fit 32 bits
     int32_t fault;      // test hook: CTA 0 withholds its first record
+    int32_t stats;      // argmax / sample / entropy / probs wanted
+    int32_t k;          // top-k of converged rows (0: none)
+    int32_t a_words;    // words of a first record
+    int32_t xstride;    // words of a CTA's exchange area
 };
 
 // Test hook state: the next launch withholds one record (see
@@ -120,7 +152,7 @@ struct RowStatsParams {
 std::atomic<int> g_inject_fault{0};
 
 struct WarpPartial {
-    float m, s, w;
+    float m, s, w, xmax;
     int arg;
 };
 
@@ -134,16 +166,27 @@ struct RowInfo {
     float row_max;
     float log2s;
     float near_best;  // B: the best score among the warps' argmax elements
+    float thr;        // top-k threshold (raw logit)
     int near_col;
     int arg;
     int noisy;
+    int skip;         // no work (an unconverged row in top-k-only mode)
+    int topk;         // top-k candidates wanted (a converged row)
 };
 
-// A row's temperature and its quotient, set once by the publisher.
+// A row's temperature and its quotient, and whether it is worked on, set
+// once by the publisher.
 struct RowQuotient {
     float temp;
     float t, y;
     int mode;
+    int work;
+};
+
+struct WarpRef {
+    float mw;    // M_w
+    float mxw;   // the raw max
+    int raw;     // e taken from the raw logits
 };
 
 struct Scratch {
@@ -155,10 +198,24 @@ struct Scratch {
     WarpBest p2[kRowRing][kComputeWarps];
     RowInfo info[kRowRing];
     RowQuotient rq[kRowRing];
-    float wref[kRowRing][kComputeWarps];                   // each warp's M_w
-    uint16_t worklist[kComputeWarps][32 * kMaxVec4Slots];  // race groups of a warp
-    int abort;                                             // a wait ran out of time
+    WarpRef wref[kRowRing][kComputeWarps];
+    int tk_count[kTopkRing];            // CTA candidate lists (top-k)
+    int tk_hard[kTopkRing];
+    int abort;                          // a wait ran out of time
 };
+
+// Shared memory after the stages: the Scratch, the warps' race lists, then
+// (top-k only) the CTA candidate lists and the poller's merge buffer.
+__host__ __device__ constexpr size_t scratch_bytes() {
+    return (sizeof(Scratch) + 127) & ~static_cast<size_t>(127);
+}
+__host__ __device__ constexpr size_t worklist_bytes(int vec4) {
+    return (static_cast<size_t>(kComputeWarps) * 32 * vec4 * sizeof(uint16_t) + 127) &
+           ~static_cast<size_t>(127);
+}
+__host__ __device__ constexpr size_t topk_smem_bytes() {
+    return static_cast<size_t>(kTopkRing) * kTopkCtaCap * 8 + static_cast<size_t>(kTopkRowCap) * 8;
+}
 
 __device__ __forceinline__ void set_comp(float4& v, int q, float x) {
     if (q == 0) v.x = x;
@@ -184,17 +241,75 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+__device__ __forceinline__ int warp_sum_i(int v) {
+    int r;
+    asm volatile("redux.sync.add.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+// Order-preserving unsigned form of an fp32 value (-inf lowest).
+__device__ __forceinline__ uint32_t ord32(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Top-k key: value (with -0.0 as +0.0) in the high word, then the lower
+// column first (the _lp_topk_kernel key order).
+__device__ __forceinline__ uint64_t topk_key(float s, int col) {
+    return (static_cast<uint64_t>(ord32(s + 0.0f)) << 32) |
+           static_cast<uint32_t>(0x7FFFFFFF - col);
+}
+__device__ __forceinline__ float key_value(uint64_t key) {
+    const uint32_t o = static_cast<uint32_t>(key >> 32);
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+__device__ __forceinline__ int key_col(uint64_t key) {
+    return 0x7FFFFFFF - static_cast<int>(static_cast<uint32_t>(key));
+}
+
 // Temperature of a global row: temps[row / canvas_len].
-__device__ __forceinline__ float row_temperature(const RowStatsParams& p, uint64_t grow_id) {
-    const uint64_t slot = p.index32 ? static_cast<uint64_t>(static_cast<uint32_t>(grow_id) /
-                                                            static_cast<uint32_t>(p.canvas_len))
-                                    : grow_id / static_cast<uint64_t>(p.canvas_len);
-    return p.temps[slot];
+__device__ __forceinline__ uint64_t row_slot(const RowStatsParams& p, uint64_t grow_id) {
+    return p.index32 ? static_cast<uint64_t>(static_cast<uint32_t>(grow_id) /
+                                             static_cast<uint32_t>(p.canvas_len))
+                     : grow_id / static_cast<uint64_t>(p.canvas_len);
 }
 
 // Tag of the records of a team's row sequence k (never 0: rings are zeroed
 // before each launch).
 __device__ __forceinline__ uint32_t record_tag(int k) { return static_cast<uint32_t>(k) + 1u; }
+
+// A CTA's exchange area: kRing first records (a_words words each), kRing
+// second records (2 words) and, with top-k, kRing candidate records
+// (2 + 2k words: count, pad, then each key as two tagged halves).
+__device__ __forceinline__ uint64_t* rec_a(const RowStatsParams& p, int cta, int slot) {
+    return p.xchg + static_cast<size_t>(cta) * p.xstride + slot * p.a_words;
+}
+__device__ __forceinline__ uint64_t* rec_b(const RowStatsParams& p, int cta, int slot) {
+    return p.xchg + static_cast<size_t>(cta) * p.xstride + kRing * p.a_words + slot * 2;
+}
+__device__ __forceinline__ uint64_t* rec_k(const RowStatsParams& p, int cta, int slot) {
+    return p.xchg + static_cast<size_t>(cta) * p.xstride + kRing * (p.a_words + 2) +
+           static_cast<size_t>(slot) * (2 + 2 * p.k);
+}
+
+// Poll n words (n even, 16-byte aligned) until every tag is `tag`.
+template <int N>
+__device__ __forceinline__ bool poll_words(const uint64_t* w, int n, uint32_t tag, uint64_t (&out)[N],
+                                           uint64_t t0) {
+    for (uint32_t it = 0;; ++it) {
+        bool ok = true;
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
+            if (i < n) {
+                ld_relaxed_v2(w + i, out[i], out[i + 1]);
+                ok &= static_cast<uint32_t>(out[i]) == tag && static_cast<uint32_t>(out[i + 1]) == tag;
+            }
+        }
+        if (ok) return true;
+        if ((it & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(32);
+    }
+}
 
 // Elements of one float4 group that could still beat the row's best score
 // B: winning needs -log u <= e^(s - B), so 1 - u (a lower bound of -log u)
@@ -212,6 +327,14 @@ __device__ __forceinline__ uint32_t race_group(const float4& e, uint4 w, float r
     return bits;
 }
 
+__device__ __forceinline__ ScaledQuotient quotient_of(const RowQuotient& rq) {
+    ScaledQuotient sq;
+    sq.t = rq.t;
+    sq.y = rq.y;
+    sq.mode = rq.mode;
+    return sq;
+}
+
 // Score the survivors `bits` of the float4 group starting at column c4
 // exactly: s = x / Te from the logit in global memory (the stage holds e
 // only), g from the group's Philox words; keep the best (score, column).
@@ -219,10 +342,7 @@ __device__ __forceinline__ uint32_t race_group(const float4& e, uint4 w, float r
 __device__ __noinline__ WarpBest race_rescore(uint32_t bits, const float* row_logits, int c4,
                                               uint4 w, const RowQuotient rq, int skip_col,
                                               WarpBest best) {
-    ScaledQuotient sq;
-    sq.t = rq.t;
-    sq.y = rq.y;
-    sq.mode = rq.mode;
+    const ScaledQuotient sq = quotient_of(rq);
     while (bits) {
         const int q = __ffs(bits) - 1;
         bits &= bits - 1;
@@ -235,17 +355,44 @@ __device__ __noinline__ WarpBest race_rescore(uint32_t bits, const float* row_lo
     return best;
 }
 
+// Top-k candidates of one thread: the elements of `mask` (bit 4i+q: slot
+// i, component q) whose logit reaches the row's threshold, rescored exactly
+// and appended to the CTA list. Returns false if the list overflowed.
+__device__ __noinline__ bool topk_collect(uint64_t mask, const float* row_logits, int col0, int tid,
+                                          float thr, const RowQuotient rq, int* count,
+                                          uint64_t* list) {
+    const ScaledQuotient sq = quotient_of(rq);
+    bool ok = true;
+    while (mask) {
+        const int b = __ffsll(static_cast<long long>(mask)) - 1;
+        mask &= mask - 1;
+        const int c = col0 + 4 * ((b >> 2) * kCompute + tid) + (b & 3);
+        const float x = __ldg(row_logits + c);
+        if (!(x >= thr)) continue;
+        const int pos = atomicAdd(count, 1);
+        if (pos < kTopkCtaCap) list[pos] = topk_key(sq.exact(x), c);
+        else ok = false;
+    }
+    return ok;
+}
+
 }  // namespace
 
 template <int VEC4, int LAG, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, 1)
     row_stats_kernel(const __grid_constant__ RowStatsParams p) {
     static_assert(NSTAGE <= kMaxStages && NSTAGE >= LAG + 2, "stages");
-    static_assert(VEC4 <= kMaxVec4Slots, "slots");
     extern __shared__ __align__(128) unsigned char smem[];
     Scratch& sc = *reinterpret_cast<Scratch*>(smem + NSTAGE * p.stage_bytes);
+    uint16_t* worklists =
+        reinterpret_cast<uint16_t*>(smem + NSTAGE * p.stage_bytes + scratch_bytes());
+    uint64_t* tk_lists = reinterpret_cast<uint64_t*>(smem + NSTAGE * p.stage_bytes +
+                                                     scratch_bytes() + worklist_bytes(VEC4));
+    uint64_t* tk_merge = tk_lists + kTopkRing * kTopkCtaCap;
     volatile int* abort_flag = &sc.abort;
     const bool use_tma = p.use_tma != 0;
+    const bool stats = p.stats != 0;
+    const int K = p.k;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -262,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           : 0;
     auto row_of = [&](int k) { return team_id + static_cast<int64_t>(k) * p.num_teams; };
     auto grow_of = [&](int k) { return static_cast<uint64_t>(p.row0 + row_of(k)); };
+    auto kept = [&](int k) { return p.keep == nullptr || p.keep[row_slot(p, grow_of(k))] != 0; };
     auto fail = [&]() {
         *abort_flag = 1;
         raise_device_error(p.err, 1);
@@ -274,6 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sc.b_done[r], kComputeWarps);
             mbar_init(&sc.info_ready[r], 1);
         }
+        for (int r = 0; r < kTopkRing; ++r) {
+            sc.tk_count[r] = 0;
+            sc.tk_hard[r] = 0;
+        }
         fence_barrier_init();
         sc.abort = 0;
     }
@@ -281,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kComputeWarps) {
         // ======================= compute warps ==================================
+        uint16_t* list = worklists + warp * 32 * VEC4;
         for (int k = 0; k < nrows + LAG; ++k) {
             if (*abort_flag) break;
             if (k < nrows) {
@@ -294,129 +447,120 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const RowQuotient rq = sc.rq[k & (kRowRing - 1)];
-                ScaledQuotient sq;
-                sq.t = rq.t;
-                sq.y = rq.y;
-                sq.mode = rq.mode;
-                float4 v[VEC4];
+                if (rq.work) {
+                    const ScaledQuotient sq = quotient_of(rq);
+                    float4 v[VEC4];
 #pragma unroll
-                for (int i = 0; i < VEC4; ++i) {
-                    const int f = i * kCompute + tid;
-                    float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                    if (i * kCompute < nslot4) {  // CTA-uniform: slot i holds columns
-                        if (f < nfull4) {
-                            if (use_tma) {
-                                x = stage4[f];
+                    for (int i = 0; i < VEC4; ++i) {
+                        const int f = i * kCompute + tid;
+                        float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                        if (i * kCompute < nslot4) {  // CTA-uniform: slot i holds columns
+                            if (f < nfull4) {
+                                if (use_tma) {
+                                    x = stage4[f];
+                                } else {
+                                    x.x = grow[4 * f + 0];
+                                    x.y = grow[4 * f + 1];
+                                    x.z = grow[4 * f + 2];
+                                    x.w = grow[4 * f + 3];
+                                }
+                            } else if (f == nfull4) {
+                                for (int q = 0; q < (ncols & 3); ++q) set_comp(x, q, grow[4 * f + q]);
+                            }
+                        }
+                        v[i] = x;
+                    }
+
+                    // max of the raw logits (division by Te > 0 keeps the order)
+                    float m4[VEC4];
+                    float mt = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < VEC4; ++i) {
+                        m4[i] = max4(v[i]);
+                        mt = fmaxf(mt, m4[i]);
+                    }
+                    const float mxw = warp_max(mt);
+                    const float mw = mxw == -INFINITY ? -INFINITY : sq.exact(mxw);  // M_w
+                    // warp-uniform: raw domain, or exact quotients first
+                    const bool raw = !(fabsf(mw) >= kRawDomainLimit);
+
+                    // argmax: the lowest column whose exact quotient is M_w.
+                    // exact(x) == M_w needs x >= mxw - Te * ulp(M_w), so only
+                    // the slots whose max reaches that are searched, their
+                    // logits read again (the stage still holds them).
+                    const float cthr = mxw - fmaxf(fabsf(mxw) * 0x1p-20f, rq.t * 0x1p-140f);
+                    int arg_t = INT_MAX;
+                    if (stats && mt >= cthr && mw != -INFINITY) {
+                        uint32_t smask = 0;
+#pragma unroll
+                        for (int i = 0; i < VEC4; ++i)
+                            if (m4[i] >= cthr) smask |= 1u << i;
+#pragma unroll 1
+                        while (smask && arg_t == INT_MAX) {
+                            const int i = __ffs(smask) - 1;
+                            smask &= smask - 1;
+                            const int f = i * kCompute + tid;
+                            float4 x4;
+                            if (use_tma && f < nfull4) {
+                                x4 = stage4[f];
                             } else {
-                                x.x = grow[4 * f + 0];
-                                x.y = grow[4 * f + 1];
-                                x.z = grow[4 * f + 2];
-                                x.w = grow[4 * f + 3];
+                                x4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                                for (int q = 0; q < 4 && 4 * f + q < ncols; ++q) set_comp(x4, q, grow[4 * f + q]);
                             }
-                        } else if (f == nfull4) {
-                            for (int q = 0; q < (ncols & 3); ++q) set_comp(x, q, grow[4 * f + q]);
-                        }
-                    }
-                    v[i] = x;
-                }
-
-                // max of the raw logits (division by Te > 0 keeps the order)
-                float m4[VEC4];
-                float mt = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < VEC4; ++i) {
-                    m4[i] = max4(v[i]);
-                    mt = fmaxf(mt, m4[i]);
-                }
-                const float mxw = warp_max(mt);
-                const float mw = mxw == -INFINITY ? -INFINITY : sq.exact(mxw);  // M_w
-                // warp-uniform: raw domain, or exact quotients first
-                const bool raw = !(fabsf(mw) >= kRawDomainLimit);
-                // argmax: the lowest column whose exact quotient is M_w.
-                // exact(x) == M_w needs x >= mxw - Te * ulp(M_w), so only the
-                // slots whose max reaches that are searched, their logits
-                // read again (the stage still holds them).
-                const float cthr = mxw - fmaxf(fabsf(mxw) * 0x1p-20f, rq.t * 0x1p-140f);
-                int arg_t = INT_MAX;
-                if (mt >= cthr && mw != -INFINITY) {
-                    uint32_t smask = 0;
-#pragma unroll
-                    for (int i = 0; i < VEC4; ++i)
-                        if (m4[i] >= cthr) smask |= 1u << i;
 #pragma unroll 1
-                    while (smask && arg_t == INT_MAX) {
-                        const int i = __ffs(smask) - 1;
-                        smask &= smask - 1;
-                        const int f = i * kCompute + tid;
-                        float4 x4;
-                        if (use_tma && f < nfull4) {
-                            x4 = stage4[f];
-                        } else {
-                            x4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                            for (int q = 0; q < 4 && 4 * f + q < ncols; ++q) set_comp(x4, q, grow[4 * f + q]);
-                        }
-#pragma unroll 1
-                        for (int q = 0; q < 4; ++q) {
-                            const float x = comp(x4, q);
-                            if (x >= cthr && sq.exact(x) == mw) {
-                                arg_t = col0 + 4 * f + q;
-                                break;
+                            for (int q = 0; q < 4; ++q) {
+                                const float x = comp(x4, q);
+                                if (x >= cthr && sq.exact(x) == mw) {
+                                    arg_t = col0 + 4 * f + q;
+                                    break;
+                                }
                             }
                         }
                     }
-                }
-                const int aw = warp_min_i(arg_t);
-                if (!raw) {
-#pragma unroll
-                    for (int i = 0; i < VEC4; ++i) {
-                        v[i].x = sq.exact(v[i].x);
-                        v[i].y = sq.exact(v[i].y);
-                        v[i].z = sq.exact(v[i].z);
-                        v[i].w = sq.exact(v[i].w);
-                    }
-                }
+                    const int aw = stats ? warp_min_i(arg_t) : INT_MAX;
 
-                // t = (s - M_w) log2(e): raw domain x * log2(e)/Te - c with
-                // c = RN(mxw * log2(e)/Te), else (s - M_w) * log2(e); -inf
-                // gives a finite t whose e is 0
-                float lscale, cref;
-                if (raw) {
-                    lscale = kLog2e * sq.y;
-                    cref = mxw * lscale;
-                } else {
-                    lscale = kLog2e;
-                    cref = 0.0f;
+                    // t = (s - M_w) log2(e): raw domain x * log2(e)/Te - c with
+                    // c = RN(mxw * log2(e)/Te), else (s - M_w) * log2(e); -inf
+                    // gives a finite t whose e is 0
+                    float lscale, cref;
+                    if (raw) {
+                        lscale = kLog2e * sq.y;
+                        cref = mxw * lscale;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < VEC4; ++i) {
+                            v[i].x = sq.exact(v[i].x) - mw;
+                            v[i].y = sq.exact(v[i].y) - mw;
+                            v[i].z = sq.exact(v[i].z) - mw;
+                            v[i].w = sq.exact(v[i].w) - mw;
+                        }
+                        lscale = kLog2e;
+                        cref = 0.0f;
+                    }
+                    // sums, four accumulators each; e waits in the stage
+                    float st[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int i = 0; i < VEC4; ++i) {
-                        v[i].x -= mw;
-                        v[i].y -= mw;
-                        v[i].z -= mw;
-                        v[i].w -= mw;
-                    }
-                }
-                // sums, four accumulators each; e waits in the stage
-                float st[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        if (i * kCompute < nslot4) {
+                            float4 ev;
 #pragma unroll
-                for (int i = 0; i < VEC4; ++i) {
-                    if (i * kCompute < nslot4) {
-                        float4 ev;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float t = fmaxf(fmaf(comp(v[i], q), lscale, -cref), -FLT_MAX);
-                            const float e = ex2_approx(t);
-                            set_comp(ev, q, e);
-                            st[q] += e;
-                            wt[q] = fmaf(e, t, wt[q]);
+                            for (int q = 0; q < 4; ++q) {
+                                const float t = fmaxf(fmaf(comp(v[i], q), lscale, -cref), -FLT_MAX);
+                                const float e = ex2_approx(t);
+                                set_comp(ev, q, e);
+                                st[q] += e;
+                                wt[q] = fmaf(e, t, wt[q]);
+                            }
+                            const int f = i * kCompute + tid;
+                            if (f < nslot4) stage4[f] = ev;
                         }
-                        const int f = i * kCompute + tid;
-                        if (f < nslot4) stage4[f] = ev;
                     }
-                }
-                const float sw = warp_sum_f((st[0] + st[1]) + (st[2] + st[3]));
-                const float ww = warp_sum_f((wt[0] + wt[1]) + (wt[2] + wt[3])) * kLn2;
-                if (lane == 0) {
-                    sc.p1[k & (kRowRing - 1)][warp] = WarpPartial{mw, sw, ww, aw};
-                    sc.wref[k & (kRowRing - 1)][warp] = mw;
+                    const float sw = warp_sum_f((st[0] + st[1]) + (st[2] + st[3]));
+                    const float ww = warp_sum_f((wt[0] + wt[1]) + (wt[2] + wt[3])) * kLn2;
+                    if (lane == 0) {
+                        sc.p1[k & (kRowRing - 1)][warp] = WarpPartial{mw, sw, ww, mxw, aw};
+                        sc.wref[k & (kRowRing - 1)][warp] = WarpRef{mw, mxw, raw ? 1 : 0};
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sc.a_done[k & (kRowRing - 1)]);
@@ -431,82 +575,130 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const RowInfo ri = sc.info[j & (kRowRing - 1)];
-                const float mw = sc.wref[j & (kRowRing - 1)][warp];
-                const int64_t frow = row_of(j);
-                const float4* fstage =
-                    reinterpret_cast<const float4*>(smem + (j % NSTAGE) * p.stage_bytes);
-                float4 e[VEC4];
-#pragma unroll
-                for (int i = 0; i < VEC4; ++i) {
-                    const int f = i * kCompute + tid;
-                    e[i] = (i * kCompute < nslot4 && f < nslot4)
-                               ? fstage[f]
-                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                }
-                // e^(s - B), widened by the race margin, is e * r_w; a group
-                // whose largest e * r_w is below 2^-24 (<= 1 - u always) has
-                // no element that can win.
-                const float r_w = ri.noisy && mw != -INFINITY
-                                      ? ex2_approx(fmaf(mw - ri.near_best, kLog2e, kRaceMarginLog2))
-                                      : 0.0f;
-                uint32_t pmask = 0;
-#pragma unroll
-                for (int i = 0; i < VEC4; ++i)
-                    if (max4(e[i]) * r_w >= 0x1p-24f) pmask |= 1u << i;
-
-                if (p.probs_dtype != 0) {
-                    const float big_m = ri.row_max;
-                    // e^(s - M) / S = e * e^(M_w - M) / S
-                    const float f_w =
-                        mw == -INFINITY ? 0.0f : ex2_approx(fmaf(mw - big_m, kLog2e, -ri.log2s));
-                    const bool bf16 = p.probs_dtype == 1;
-                    uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
+                WarpBest wb{-INFINITY, INT_MAX};
+                if (!ri.skip) {
+                    const WarpRef wr = sc.wref[j & (kRowRing - 1)][warp];
+                    const float mw = wr.mw;
+                    const int64_t frow = row_of(j);
+                    const float* frow_logits = p.logits + frow * p.row_stride;
+                    const float4* fstage =
+                        reinterpret_cast<const float4*>(smem + (j % NSTAGE) * p.stage_bytes);
+                    float4 e[VEC4];
 #pragma unroll
                     for (int i = 0; i < VEC4; ++i) {
                         const int f = i * kCompute + tid;
-                        if (i * kCompute >= nslot4 || f >= nslot4) continue;
-                        float pr[4] = {e[i].x * f_w, e[i].y * f_w, e[i].z * f_w, e[i].w * f_w};
-                        if (big_m == -INFINITY) pr[0] = pr[1] = pr[2] = pr[3] = NAN;
-                        const uint32_t lo = pack2(pr[0], pr[1], bf16);
-                        const uint32_t hi = pack2(pr[2], pr[3], bf16);
-                        if (p.probs_vec && f < nfull4) {
-                            __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
+                        e[i] = (i * kCompute < nslot4 && f < nslot4)
+                                   ? fstage[f]
+                                   : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    }
+                    // e^(s - B), widened by the race margin, is e * r_w; a group
+                    // whose largest e * r_w is below 2^-24 (<= 1 - u always) has
+                    // no element that can win.
+                    const float r_w = ri.noisy && mw != -INFINITY
+                                          ? ex2_approx(fmaf(mw - ri.near_best, kLog2e, kRaceMarginLog2))
+                                          : 0.0f;
+                    uint32_t pmask = 0;
+#pragma unroll
+                    for (int i = 0; i < VEC4; ++i)
+                        if (max4(e[i]) * r_w >= 0x1p-24f) pmask |= 1u << i;
+
+                    // top-k candidates: e >= e_thr is implied by x >= thr (the
+                    // exponent lowered by 2^-8 for rounding); too low an e_thr
+                    // leaves the row to the exact kernel.
+                    uint64_t kmask = 0;
+                    bool khard = false;
+                    if (ri.topk) {
+                        const RowQuotient rq = sc.rq[j & (kRowRing - 1)];
+                        float t_thr;
+                        if (ri.thr == -INFINITY) {
+                            t_thr = -INFINITY;
+                        } else if (wr.raw) {
+                            const float lscale = kLog2e * rq.y;
+                            t_thr = fmaf(ri.thr, lscale, -(wr.mxw * lscale));
                         } else {
-                            const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
-                                                      static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
-                            for (int q = 0; q < 4; ++q)
-                                if (4 * f + q < ncols) prow[4 * f + q] = code[q];
+                            t_thr = (quotient_of(rq).exact(ri.thr) - mw) * kLog2e;
+                        }
+                        // no threshold (fewer warp maxima than k, or the k-th
+                        // is -inf): the whole row goes to the exact kernel;
+                        // an all -inf warp has no candidate above a finite one
+                        if (ri.thr == -INFINITY) {
+                            khard = true;
+                        } else if (mw != -INFINITY) {
+                            if (!(t_thr - 0x1p-8f >= -120.0f)) {
+                                khard = true;
+                            } else {
+                                const float e_thr = ex2_approx(t_thr - 0x1p-8f);
+#pragma unroll
+                                for (int i = 0; i < VEC4; ++i)
+                                    if (max4(e[i]) >= e_thr)
+#pragma unroll
+                                        for (int q = 0; q < 4; ++q)
+                                            if (comp(e[i], q) >= e_thr) kmask |= 1ull << (4 * i + q);
+                            }
                         }
                     }
-                }
 
-                WarpBest wb{-INFINITY, INT_MAX};
-                if (ri.noisy) {
-                    wb = WarpBest{ri.near_best, ri.near_col};
-                    // the groups that pass, listed warp-wide, one per lane
-                    uint16_t* list = sc.worklist[warp];
-                    const uint32_t lt = lanemask_lt();
-                    int total = 0;
+                    if (stats && p.probs_dtype != 0) {
+                        const float big_m = ri.row_max;
+                        // e^(s - M) / S = e * e^(M_w - M) / S
+                        const float f_w =
+                            mw == -INFINITY ? 0.0f : ex2_approx(fmaf(mw - big_m, kLog2e, -ri.log2s));
+                        const bool bf16 = p.probs_dtype == 1;
+                        uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
 #pragma unroll
-                    for (int i = 0; i < VEC4; ++i) {
-                        const bool pass = (pmask >> i) & 1u;
-                        const uint32_t b = __ballot_sync(0xffffffffu, pass);
-                        if (pass) list[total + __popc(b & lt)] = static_cast<uint16_t>(i * kCompute + tid);
-                        total += __popc(b);
+                        for (int i = 0; i < VEC4; ++i) {
+                            const int f = i * kCompute + tid;
+                            if (i * kCompute >= nslot4 || f >= nslot4) continue;
+                            float pr[4] = {e[i].x * f_w, e[i].y * f_w, e[i].z * f_w, e[i].w * f_w};
+                            if (big_m == -INFINITY) pr[0] = pr[1] = pr[2] = pr[3] = NAN;
+                            const uint32_t lo = pack2(pr[0], pr[1], bf16);
+                            const uint32_t hi = pack2(pr[2], pr[3], bf16);
+                            if (p.probs_vec && f < nfull4) {
+                                __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
+                            } else {
+                                const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                                          static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+                                for (int q = 0; q < 4; ++q)
+                                    if (4 * f + q < ncols) prow[4 * f + q] = code[q];
+                            }
+                        }
                     }
-                    __syncwarp();
-                    const uint64_t fgrow_id = grow_of(j);
-                    for (int n = lane; n < total; n += 32) {
-                        const int f = list[n];
-                        const float4 e4 = fstage[f];
-                        const uint4 w = noise_words_rk(p.rk, fgrow_id, static_cast<uint32_t>((col0 >> 2) + f));
-                        const uint32_t bits = race_group(e4, w, r_w);
-                        if (bits)
-                            wb = race_rescore(bits, p.logits + frow * p.row_stride, col0 + 4 * f, w,
-                                              sc.rq[j & (kRowRing - 1)], ri.near_col, wb);
+
+                    if (stats && ri.noisy) {
+                        wb = WarpBest{ri.near_best, ri.near_col};
+                        // the groups that pass, listed warp-wide, one per lane
+                        const uint32_t lt = lanemask_lt();
+                        int total = 0;
+#pragma unroll
+                        for (int i = 0; i < VEC4; ++i) {
+                            const bool pass = (pmask >> i) & 1u;
+                            const uint32_t b = __ballot_sync(0xffffffffu, pass);
+                            if (pass) list[total + __popc(b & lt)] = static_cast<uint16_t>(i * kCompute + tid);
+                            total += __popc(b);
+                        }
+                        __syncwarp();
+                        const uint64_t fgrow_id = grow_of(j);
+                        for (int n = lane; n < total; n += 32) {
+                            const int f = list[n];
+                            const float4 e4 = fstage[f];
+                            const uint4 w = noise_words_rk(p.rk, fgrow_id, static_cast<uint32_t>((col0 >> 2) + f));
+                            const uint32_t bits = race_group(e4, w, r_w);
+                            if (bits)
+                                wb = race_rescore(bits, frow_logits, col0 + 4 * f, w,
+                                                  sc.rq[j & (kRowRing - 1)], ri.near_col, wb);
+                        }
+                        __syncwarp();  // the list is rewritten for the next row
+                        warp_best(wb.best, wb.col);
                     }
-                    __syncwarp();  // the list is rewritten for the next row
-                    warp_best(wb.best, wb.col);
+
+                    if (ri.topk) {
+                        bool ok = !khard;
+                        if (ok && kmask)
+                            ok = topk_collect(kmask, frow_logits, col0, tid, ri.thr, sc.rq[j & (kRowRing - 1)],
+                                              &sc.tk_count[j & (kTopkRing - 1)],
+                                              tk_lists + (j & (kTopkRing - 1)) * kTopkCtaCap);
+                        if (!__all_sync(0xffffffffu, ok) && lane == 0) sc.tk_hard[j & (kTopkRing - 1)] = 1;
+                    }
                 }
                 if (lane == 0) sc.p2[j & (kRowRing - 1)][warp] = wb;
                 __syncwarp();
@@ -516,17 +708,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kPublisherWarp) {
         // ======================= publisher warp ==================================
         // Stage a row: its temperature quotient for the CTA, then the bulk
-        // copy (or, for rows that are not 16-byte aligned, a plain arrival:
-        // the compute warps read global memory).
-        float temp_next = nrows > 0 && lane == 0 ? row_temperature(p, grow_of(0)) : 0.0f;
+        // copy (or, for rows that are not 16-byte aligned, or not worked on,
+        // a plain arrival: the compute warps read global memory).
+        float temp_next = nrows > 0 && lane == 0 ? p.temps[row_slot(p, grow_of(0))] : 0.0f;
         auto issue_row = [&](int r) {
             if (lane == 0) {
                 const float temp = temp_next;
-                if (r + 1 < nrows) temp_next = row_temperature(p, grow_of(r + 1));
+                if (r + 1 < nrows) temp_next = p.temps[row_slot(p, grow_of(r + 1))];
+                const bool work = stats || kept(r);
                 const ScaledQuotient q = ScaledQuotient::of(fmaxf(temp, kTempFloor));
-                sc.rq[r & (kRowRing - 1)] = RowQuotient{temp, q.t, q.y, q.mode};
+                sc.rq[r & (kRowRing - 1)] = RowQuotient{temp, q.t, q.y, q.mode, work ? 1 : 0};
                 uint64_t* bar = &sc.full[r % NSTAGE];
-                if (use_tma) {
+                if (use_tma && work) {
                     mbar_arrive_expect_tx(bar, copy_bytes);
                     if (copy_bytes)
                         tma_load_1d(smem + (r % NSTAGE) * p.stage_bytes,
@@ -547,49 +740,110 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) fail();
                     break;
                 }
-                const WarpPartial wp = lane < kComputeWarps
-                                           ? sc.p1[k & (kRowRing - 1)][lane]
-                                           : WarpPartial{-INFINITY, 0.0f, 0.0f, INT_MAX};
-                const float mc = warp_max(wp.m);
-                float s_l = 0.0f, w_l = 0.0f;
-                if (wp.m != -INFINITY) {
-                    const float dm = wp.m - mc;
-                    const float f = ex2_approx(dm * kLog2e);
-                    s_l = f * wp.s;
-                    w_l = f * fmaf(dm, wp.s, wp.w);
+                const RowQuotient rq = sc.rq[k & (kRowRing - 1)];
+                if (rq.work) {
+                    const WarpPartial wp = lane < kComputeWarps
+                                               ? sc.p1[k & (kRowRing - 1)][lane]
+                                               : WarpPartial{-INFINITY, 0.0f, 0.0f, -INFINITY, INT_MAX};
+                    const float mc = warp_max(wp.m);
+                    float s_l = 0.0f, w_l = 0.0f;
+                    if (wp.m != -INFINITY) {
+                        const float dm = wp.m - mc;
+                        const float f = ex2_approx(dm * kLog2e);
+                        s_l = f * wp.s;
+                        w_l = f * fmaf(dm, wp.s, wp.w);
+                    }
+                    const float s_c = warp_sum_f(s_l);
+                    const float w_c = warp_sum_f(w_l);
+                    const int a_c = mc == -INFINITY ? col0 : warp_min_i(wp.m == mc ? wp.arg : INT_MAX);
+                    // B candidates: the Gumbel-max score of each warp's argmax
+                    // element, one lane per warp
+                    float b_c = -INFINITY;
+                    int bcol_c = INT_MAX;
+                    if (stats && rq.temp > 0.0f && wp.arg != INT_MAX) {
+                        const uint4 w = noise_words_rk(p.rk, grow_of(k), static_cast<uint32_t>(wp.arg >> 2));
+                        b_c = wp.m + gumbel_of_bits(word_of(w, wp.arg & 3));
+                        bcol_c = wp.arg;
+                    }
+                    warp_best(b_c, bcol_c);
+                    const bool withhold = p.fault && blockIdx.x == 0 && k == 0;
+                    uint64_t* ra = rec_a(p, blockIdx.x, k & (kRing - 1));
+                    const uint32_t tag = record_tag(k);
+                    if (lane == 0 && !withhold) {
+                        st_relaxed_v2(ra + 0, tagged(mc, tag), tagged(s_c, tag));
+                        st_relaxed_v2(ra + 2, tagged(w_c, tag), tagged(static_cast<uint32_t>(a_c), tag));
+                        st_relaxed_v2(ra + 4, tagged(b_c, tag), tagged(static_cast<uint32_t>(bcol_c), tag));
+                    }
+                    if (p.a_words > kAWords) {
+                        // the r-th largest raw warp maximum of the CTA (order
+                        // key), r = ceil(k / G); warps holding no column are
+                        // absent (0), and fewer than r present warps give 0
+                        const uint32_t o =
+                            lane < kComputeWarps && lane * 32 < nslot4 ? ord32(wp.xmax) : 0u;
+                        int rank = 0;  // distinct: ties go to the lower lane
+#pragma unroll
+                        for (int l = 0; l < kComputeWarps; ++l) {
+                            const uint32_t ol = __shfl_sync(0xffffffffu, o, l);
+                            rank += ol > o || (ol == o && l < lane);
+                        }
+                        const int r = (K + p.team - 1) / p.team;
+                        const uint32_t hit = __ballot_sync(0xffffffffu, lane < kComputeWarps && rank == r - 1);
+                        const uint32_t rth = hit ? __shfl_sync(0xffffffffu, o, __ffs(hit) - 1) : 0u;
+                        if (lane == 0 && !withhold)
+                            st_relaxed_v2(ra + kAWords, tagged(rth, tag), tagged(0u, tag));
+                    }
                 }
-                const float s_c = warp_sum_f(s_l);
-                const float w_c = warp_sum_f(w_l);
-                const int a_c = mc == -INFINITY ? col0 : warp_min_i(wp.m == mc ? wp.arg : INT_MAX);
-                // B candidates: the Gumbel-max score of each warp's argmax
-                // element, one lane per warp
-                float b_c = -INFINITY;
-                int bcol_c = INT_MAX;
-                if (sc.rq[k & (kRowRing - 1)].temp > 0.0f && wp.arg != INT_MAX) {
-                    const uint4 w = noise_words_rk(p.rk, grow_of(k), static_cast<uint32_t>(wp.arg >> 2));
-                    b_c = wp.m + gumbel_of_bits(word_of(w, wp.arg & 3));
-                    bcol_c = wp.arg;
-                }
-                warp_best(b_c, bcol_c);
-                if (lane == 0 && !(p.fault && blockIdx.x == 0 && k == 0))
-                    publish_a(record_a(p.xchg, blockIdx.x, k & (kRing - 1)), record_tag(k), mc, s_c,
-                              w_c, a_c, b_c, bcol_c);
             }
             const int j = k - LAG;
             if (j >= 0) {
-                // ---- second record of row j; its stage takes a later row ----------
+                // ---- second records of row j; its stage takes a later row --------
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sc.b_done[j & (kRowRing - 1)],
                                                                static_cast<uint32_t>((j / kRowRing) & 1)))) {
                     if (lane == 0) fail();
                     break;
                 }
-                const WarpBest wb = lane < kComputeWarps ? sc.p2[j & (kRowRing - 1)][lane]
-                                                         : WarpBest{-INFINITY, INT_MAX};
-                float b = wb.best;
-                int bcol = wb.col;
-                warp_best(b, bcol);
-                if (lane == 0)
-                    publish_b(record_b(p.xchg, blockIdx.x, j & (kRing - 1)), record_tag(j), b, bcol);
+                const RowQuotient rq = sc.rq[j & (kRowRing - 1)];
+                if (rq.work) {
+                    const uint32_t tag = record_tag(j);
+                    const WarpBest wb = lane < kComputeWarps ? sc.p2[j & (kRowRing - 1)][lane]
+                                                             : WarpBest{-INFINITY, INT_MAX};
+                    float b = wb.best;
+                    int bcol = wb.col;
+                    warp_best(b, bcol);
+                    if (lane == 0)
+                        st_relaxed_v2(rec_b(p, blockIdx.x, j & (kRing - 1)), tagged(b, tag),
+                                      tagged(static_cast<uint32_t>(bcol), tag));
+                    if (K > 0 && kept(j)) {
+                        // the CTA's candidates: all of them, or the K best
+                        const int slot = j & (kTopkRing - 1);
+                        const int n = sc.tk_count[slot];
+                        const bool hard = sc.tk_hard[slot] != 0 || n > kTopkCtaCap;
+                        uint64_t* rk_ = rec_k(p, blockIdx.x, j & (kRing - 1));
+                        const uint64_t* cl = tk_lists + slot * kTopkCtaCap;
+                        int kept_n = 0;
+                        if (!hard) {
+                            kept_n = n < K ? n : K;
+                            for (int a = lane; a < n; a += 32) {
+                                const uint64_t key = cl[a];
+                                int rank = 0;
+                                if (n > K)
+                                    for (int o = 0; o < n; ++o) rank += cl[o] > key;
+                                else
+                                    rank = a;
+                                if (rank < K)
+                                    st_relaxed_v2(rk_ + 2 + 2 * rank, tagged(static_cast<uint32_t>(key >> 32), tag),
+                                                  tagged(static_cast<uint32_t>(key), tag));
+                            }
+                        }
+                        __syncwarp();
+                        if (lane == 0) {
+                            st_relaxed_v2(rk_, tagged(hard ? kHardRow : static_cast<uint32_t>(kept_n), tag),
+                                          tagged(0u, tag));
+                            sc.tk_count[slot] = 0;
+                            sc.tk_hard[slot] = 0;
+                        }
+                    }
+                }
                 if (issued < nrows) {
                     if (lane == 0) fence_proxy_async_smem();
                     issue_row(issued++);
@@ -605,23 +859,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ======================= poller warp =====================================
         // Row m's first records, and the second records of row m-LAG-1. The
-        // temperature (for the noise flag) is loaded a row ahead.
-        float temp_m = nrows > 0 ? row_temperature(p, grow_of(0)) : 0.0f;
+        // temperature (for the noise flag) and the keep flag are loaded a row
+        // ahead.
+        float temp_m = nrows > 0 ? p.temps[row_slot(p, grow_of(0))] : 0.0f;
+        bool kept_m = nrows > 0 ? kept(0) : false;
+        const int a_words = p.a_words;
         for (int m = 0; m < nrows + LAG + 1; ++m) {
             if (*abort_flag) break;
             const float temp = temp_m;
-            if (m + 1 < nrows) temp_m = row_temperature(p, grow_of(m + 1));
+            const bool kept_a = kept_m;
+            if (m + 1 < nrows) {
+                temp_m = p.temps[row_slot(p, grow_of(m + 1))];
+                kept_m = kept(m + 1);
+            }
             const bool do_a = m < nrows;
+            const bool work_a = do_a && (stats || kept_a);
             const int kb = m - (LAG + 1);
-            const bool do_b = kb >= 0 && kb < nrows;
+            const bool do_b = kb >= 0 && kb < nrows && !sc.info[kb & (kRowRing - 1)].skip;
+            const bool topk_b = do_b && sc.info[kb & (kRowRing - 1)].topk;
             bool ok = true;
-            uint64_t ra[6] = {0, 0, 0, 0, 0, 0}, rb[2] = {0, 0};
-            if (lane < p.team && (do_a || do_b)) {
+            uint64_t ra[kAWordsTopk], rb[2] = {0, 0}, rk8[8];
+#pragma unroll
+            for (int i = 0; i < kAWordsTopk; ++i) ra[i] = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rk8[i] = 0;
+            if (do_a && !work_a) {
+                // an unconverged row in top-k-only mode: no exchange, but the
+                // compute warps' first half of it is awaited so that this
+                // warp never runs ahead of the ring
+                ok = mbar_wait_bounded(&sc.a_done[m & (kRowRing - 1)],
+                                       static_cast<uint32_t>((m / kRowRing) & 1));
+            }
+            const bool need_b = do_b && stats;
+            if (lane < p.team && (work_a || need_b || topk_b)) {
+                // one polling loop over the member's first record of row m,
+                // second record and candidate head (count and up to three
+                // keys) of row kb: all in flight together
                 const int cta = team_id * p.team + lane;
-                ok = read_records(do_a ? record_a(p.xchg, cta, m & (kRing - 1)) : nullptr,
-                                  record_tag(m), ra,
-                                  do_b ? record_b(p.xchg, cta, kb & (kRing - 1)) : nullptr,
-                                  record_tag(kb), rb);
+                const uint64_t* wa = rec_a(p, cta, m & (kRing - 1));
+                const uint64_t* wb2 = rec_b(p, cta, kb & (kRing - 1));
+                const uint64_t* wk = rec_k(p, cta, kb & (kRing - 1));
+                const uint32_t ta = record_tag(m), tb = record_tag(kb);
+                bool done_a = !work_a, done_b = !need_b, done_k = !topk_b;
+                const uint64_t t0 = global_timer_ns();
+                for (uint32_t it = 0;; ++it) {
+                    if (!done_a) {
+                        bool g = true;
+#pragma unroll
+                        for (int i = 0; i < kAWordsTopk; i += 2)
+                            if (i < a_words) {
+                                ld_relaxed_v2(wa + i, ra[i], ra[i + 1]);
+                                g &= static_cast<uint32_t>(ra[i]) == ta && static_cast<uint32_t>(ra[i + 1]) == ta;
+                            }
+                        done_a = g;
+                    }
+                    if (!done_b) {
+                        ld_relaxed_v2(wb2, rb[0], rb[1]);
+                        done_b = static_cast<uint32_t>(rb[0]) == tb && static_cast<uint32_t>(rb[1]) == tb;
+                    }
+                    if (!done_k) {
+#pragma unroll
+                        for (int i = 0; i < 8; i += 2) ld_relaxed_v2(wk + i, rk8[i], rk8[i + 1]);
+                        if (static_cast<uint32_t>(rk8[0]) == tb && static_cast<uint32_t>(rk8[1]) == tb) {
+                            const uint32_t c = payload_u(rk8[0]);
+                            const int nk = c == kHardRow ? 0 : (c < 3u ? static_cast<int>(c) : 3);
+                            bool g = true;
+#pragma unroll
+                            for (int i = 0; i < 3; ++i)
+                                if (i < nk)
+                                    g &= static_cast<uint32_t>(rk8[2 + 2 * i]) == tb &&
+                                         static_cast<uint32_t>(rk8[3 + 2 * i]) == tb;
+                            done_k = g;
+                        }
+                    }
+                    if (done_a && done_b && done_k) break;
+                    if ((it & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(32);
+                }
             }
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) fail();
@@ -629,48 +946,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool have = lane < p.team;
             if (do_a) {
-                const int64_t frow = row_of(m);
-                const float m_ = have ? payload_f(ra[0]) : -INFINITY;
-                const float s_m = have ? payload_f(ra[1]) : 0.0f;
-                const float w_m = have ? payload_f(ra[2]) : 0.0f;
-                const int a_m = have ? static_cast<int>(payload_u(ra[3])) : INT_MAX;
-                float b_m = have ? payload_f(ra[4]) : -INFINITY;
-                int bc_m = have ? static_cast<int>(payload_u(ra[5])) : INT_MAX;
-                const float big_m = warp_max(m_);
-                float s_l = 0.0f, w_l = 0.0f;
-                if (m_ != -INFINITY) {
-                    const float dm = m_ - big_m;
-                    const float f = ex2_approx(dm * kLog2e);
-                    s_l = f * s_m;
-                    w_l = f * fmaf(dm, s_m, w_m);
-                }
-                const float s_tot = warp_sum_f(s_l);
-                const float w_tot = warp_sum_f(w_l);
-                const int arg_row = warp_min_i(m_ == big_m ? a_m : INT_MAX);
-                warp_best(b_m, bc_m);
-                if (lane == 0) {
-                    RowInfo& ri = sc.info[m & (kRowRing - 1)];
+                RowInfo ri{};
+                ri.skip = work_a ? 0 : 1;
+                if (work_a) {
+                    const int64_t frow = row_of(m);
+                    const float m_ = have ? payload_f(ra[0]) : -INFINITY;
+                    const float s_m = have ? payload_f(ra[1]) : 0.0f;
+                    const float w_m = have ? payload_f(ra[2]) : 0.0f;
+                    const int a_m = have ? static_cast<int>(payload_u(ra[3])) : INT_MAX;
+                    float b_m = have ? payload_f(ra[4]) : -INFINITY;
+                    int bc_m = have ? static_cast<int>(payload_u(ra[5])) : INT_MAX;
+                    const float big_m = warp_max(m_);
+                    float s_l = 0.0f, w_l = 0.0f;
+                    if (m_ != -INFINITY) {
+                        const float dm = m_ - big_m;
+                        const float f = ex2_approx(dm * kLog2e);
+                        s_l = f * s_m;
+                        w_l = f * fmaf(dm, s_m, w_m);
+                    }
+                    const float s_tot = warp_sum_f(s_l);
+                    const float w_tot = warp_sum_f(w_l);
+                    const int arg_row = warp_min_i(m_ == big_m ? a_m : INT_MAX);
+                    warp_best(b_m, bc_m);
                     ri.row_max = big_m;
                     ri.log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
                     ri.near_best = b_m;
                     ri.near_col = bc_m;
                     ri.arg = arg_row;
-                    ri.noisy = temp > 0.0f && big_m != -INFINITY;
-                    mbar_arrive(&sc.info_ready[m & (kRowRing - 1)]);
-                    if (member == 0) {
+                    ri.noisy = stats && temp > 0.0f && big_m != -INFINITY;
+                    ri.topk = K > 0 && kept_a;
+                    ri.thr = -INFINITY;
+                    if (ri.topk) {
+                        // the least of the team's threshold candidates
+                        const uint32_t t = warp_min_nonneg(static_cast<int>(
+                            have ? payload_u(ra[kAWords]) : 0xFFFFFFFFu));
+                        // absent, or below the order key of -inf: no threshold
+                        if (t > 0x007FFFFFu)
+                            ri.thr = __uint_as_float((t & 0x80000000u) ? (t & 0x7FFFFFFFu) : ~t);
+                    }
+                    if (lane == 0 && member == 0 && stats) {
                         p.argmax[frow] = arg_row;
                         p.entropy[frow] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
                         if (!ri.noisy) p.sample[frow] = arg_row;
                     }
                 }
+                if (lane == 0) {
+                    sc.info[m & (kRowRing - 1)] = ri;
+                    mbar_arrive(&sc.info_ready[m & (kRowRing - 1)]);
+                }
             }
             if (do_b) {
-                float b = have ? payload_f(rb[0]) : -INFINITY;
-                int bcol = have ? static_cast<int>(payload_u(rb[1])) : INT_MAX;
-                warp_best(b, bcol);
-                if (lane == 0) {
-                    const RowInfo& ri = sc.info[kb & (kRowRing - 1)];
-                    if (ri.noisy && member == 0) {
+                const RowInfo ri = sc.info[kb & (kRowRing - 1)];
+                if (stats) {
+                    float b = have ? payload_f(rb[0]) : -INFINITY;
+                    int bcol = have ? static_cast<int>(payload_u(rb[1])) : INT_MAX;
+                    warp_best(b, bcol);
+                    if (lane == 0 && ri.noisy && member == 0) {
                         float bb = ri.near_best;
                         int bbc = ri.near_col;
                         if (beats(b, bcol, bb, bbc)) {
@@ -680,11 +1011,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.sample[row_of(kb)] = bb != -INFINITY ? bbc : ri.arg;
                     }
                 }
+                if (topk_b) {
+                    // the team's candidates: counts first, then the keys into
+                    // the merge buffer at each member's offset
+                    const uint32_t tag = record_tag(kb);
+                    bool okk = true;
+                    const uint32_t cnt = have ? payload_u(rk8[0]) : 0u;
+                    const bool any_hard = __any_sync(0xffffffffu, cnt == kHardRow);
+                    const int c = any_hard ? 0 : static_cast<int>(cnt);
+                    const int total = warp_sum_i(c);
+                    int off = c;  // inclusive scan
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, off, d);
+                        if (lane >= d) off += y;
+                    }
+                    off -= c;
+                    const int own_off = __shfl_sync(0xffffffffu, off, member);
+                    const int own_n = __shfl_sync(0xffffffffu, c, member);
+                    if (any_hard || total > kTopkRowCap || total < K) {
+                        if (lane == 0 && member == 0) {
+                            const int idx = atomicAdd(p.hard, 1);
+                            p.hard[kHardListOffset + idx] = static_cast<int32_t>(row_of(kb));
+                        }
+                    } else {
+                        if (have && c > 0) {
+                            // the first three keys came with the head; the rest
+                            // are read four at a time
+#pragma unroll
+                            for (int r = 0; r < 3; ++r)
+                                if (r < c)
+                                    tk_merge[off + r] = (static_cast<uint64_t>(payload_u(rk8[2 + 2 * r])) << 32) |
+                                                        payload_u(rk8[3 + 2 * r]);
+                            const uint64_t* src = rec_k(p, team_id * p.team + lane, kb & (kRing - 1)) + 2;
+                            const uint64_t t0 = global_timer_ns();
+                            for (int r0 = 3; r0 < c && okk; r0 += 4) {
+                                uint64_t kw[8];
+                                const int nw = 2 * (c - r0 < 4 ? c - r0 : 4);
+                                okk = poll_words(src + 2 * r0, nw, tag, kw, t0);
+#pragma unroll
+                                for (int r = 0; r < 4; ++r)
+                                    if (2 * r < nw)
+                                        tk_merge[off + r0 + r] =
+                                            (static_cast<uint64_t>(payload_u(kw[2 * r])) << 32) | payload_u(kw[2 * r + 1]);
+                            }
+                        }
+                        if (!__all_sync(0xffffffffu, okk)) {
+                            if (lane == 0) fail();
+                            break;
+                        }
+                        __syncwarp();
+                        // rank this CTA's candidates among the team's, one
+                        // candidate at a time, the count spread over the lanes
+                        const int64_t frow = row_of(kb);
+                        const float lns = ri.log2s * kLn2;
+                        for (int a = 0; a < own_n; ++a) {
+                            const uint64_t key = tk_merge[own_off + a];
+                            int cnt = 0;
+                            for (int o = lane; o < total; o += 32) cnt += tk_merge[o] > key;
+                            const int rank = warp_sum_i(cnt);
+                            if (lane == 0 && rank < K) {
+                                const float sv = key_value(key);
+                                p.out_ids[frow * K + rank] = key_col(key);
+                                p.out_lp[frow * K + rank] =
+                                    ri.row_max == -INFINITY ? NAN : (sv - ri.row_max) - lns;
+                            }
+                        }
+                        __syncwarp();  // the buffer is refilled for the next row
+                    }
+                }
             }
         }
     }
 }
 
+}  // namespace drs
+
+namespace drs {
 namespace {
 
 struct RowStatsPlan {
@@ -694,6 +1097,10 @@ struct RowStatsPlan {
     int vec4;    // float4 slots per compute thread
 };
 
+size_t fixed_smem(int vec4, bool topk) {
+    return scratch_bytes() + worklist_bytes(vec4) + (topk ? topk_smem_bytes() : 0);
+}
+
 // Team size G for one CTA per SM with 448 compute threads. The chunk must
 // fit the registers and the stages shared memory. An iteration costs about
 // max(chunk, round trip / LAG) + 1500 columns of work, the round trip of the
@@ -701,8 +1108,7 @@ struct RowStatsPlan {
 // the plan minimises ceil(rows / teams) times that, with teams = min(rows,
 // sms / G) and the three-stage form counted 25% dearer. Ties go to the
 // earlier form, then the smaller G.
-RowStatsPlan plan_row_stats(int64_t rows, int vocab, int sms, size_t scratch) {
-    const size_t budget = kSmemPerCta - scratch;
+RowStatsPlan plan_row_stats(int64_t rows, int vocab, int sms, bool topk) {
     struct Form {
         int lag, nstage, vec4;
         double pen;
@@ -713,6 +1119,7 @@ RowStatsPlan plan_row_stats(int64_t rows, int vocab, int sms, size_t scratch) {
     double best_cost = 0.0;
     const int capacity = sms > 1024 ? 1024 : sms;
     for (const Form& fm : forms) {
+        const size_t budget = kSmemPerCta - fixed_smem(fm.vec4, topk);
         int cap = static_cast<int>(budget / (4 * fm.nstage)) & ~31;
         if (cap > kCompute * fm.vec4 * 4) cap = kCompute * fm.vec4 * 4;
         const int g_min = (vocab + cap - 1) / cap;
@@ -736,7 +1143,7 @@ RowStatsPlan plan_row_stats(int64_t rows, int vocab, int sms, size_t scratch) {
 }
 
 template <int VEC4, int LAG, int NSTAGE>
-drs_status launch_row_stats(RowStatsParams& prm, int grid, size_t smem, cudaStream_t stream) {
+drs_status launch_form(RowStatsParams& prm, int grid, size_t smem, cudaStream_t stream) {
     auto kernel = row_stats_kernel<VEC4, LAG, NSTAGE>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -751,8 +1158,149 @@ drs_status launch_row_stats(RowStatsParams& prm, int grid, size_t smem, cudaStre
     return cuda_status(e);
 }
 
-}  // namespace
+// Words of a CTA's exchange area.
+size_t xchg_words(int32_t k) {
+    const size_t a = k > 0 ? kAWordsTopk : kAWords;
+    return kRing * (a + 2) + (k > 0 ? kRing * (2 + 2 * static_cast<size_t>(k)) : 0);
+}
+size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+size_t hard_list_bytes(int64_t rows) {
+    return round_up(4 * (static_cast<size_t>(kHardListOffset) + static_cast<size_t>(rows)), kWorkspaceAlign);
+}
+size_t xchg_bytes(int32_t k) { return round_up(1024 * xchg_words(k) * 8, kWorkspaceAlign); }
 
+// One call of the row kernel. stats: argmax, sample, entropy (and probs)
+// of every row; k > 0: top-k of the converged rows (every row when keep is
+// null), hard rows listed in `hard`. xchg: the exchange records.
+struct RowCall {
+    const float* logits;
+    int64_t rows, vocab, row_stride;
+    const float* temps;
+    int64_t canvas_len;
+    uint64_t seed;
+    int64_t row0;
+    int64_t* argmax;
+    int64_t* sample;
+    float* entropy;
+    drs_probs_dtype probs_dtype;
+    void* probs;
+    int64_t probs_row_stride;
+    const uint8_t* keep;
+    int32_t k;
+    int32_t* out_ids;
+    float* out_lp;
+    bool stats;
+};
+
+drs_status run_rows(const RowCall& c, void* xchg, int32_t* hard, cudaStream_t stream) {
+    const int sms = sm_count();
+    if (sms <= 0) return DRS_ERR_CUDA;
+    const bool topk = c.k > 0;
+    const RowStatsPlan rsp = plan_row_stats(c.rows, static_cast<int>(c.vocab), sms, topk);
+    const RowPlan& plan = rsp.rows;
+    if (!plan.team) return DRS_ERR_UNSUPPORTED;
+    // per-team row counts are int
+    if ((c.rows + plan.num_teams - 1) / plan.num_teams > INT_MAX / 2) return DRS_ERR_UNSUPPORTED;
+
+    RowStatsParams prm{};
+    prm.logits = c.logits;
+    prm.row_stride = c.row_stride;
+    prm.rows = c.rows;
+    prm.row0 = c.row0;
+    prm.temps = c.temps;
+    prm.canvas_len = c.canvas_len;
+    prm.argmax = c.argmax;
+    prm.sample = c.sample;
+    prm.entropy = c.entropy;
+    prm.probs = c.probs;
+    prm.probs_row_stride = c.probs_row_stride;
+    prm.xchg = static_cast<uint64_t*>(xchg);
+    prm.err = device_error_flag();
+    prm.keep = c.keep;
+    prm.out_ids = c.out_ids;
+    prm.out_lp = c.out_lp;
+    prm.hard = hard;
+    prm.rk = PhiloxRoundKeys::of(c.seed);
+    prm.vocab = static_cast<int32_t>(c.vocab);
+    prm.team = plan.team;
+    prm.chunk = plan.chunk;
+    prm.num_teams = plan.num_teams;
+    prm.probs_dtype = static_cast<int32_t>(c.probs_dtype);
+    prm.probs_vec = c.probs && aligned(c.probs, 8) && (c.probs_row_stride % 4 == 0);
+    prm.index32 = (c.row0 + c.rows <= static_cast<int64_t>(UINT32_MAX)) &&
+                  (c.canvas_len <= static_cast<int64_t>(UINT32_MAX));
+    prm.fault = g_inject_fault.exchange(0);
+    prm.stats = c.stats ? 1 : 0;
+    prm.k = c.k;
+    prm.a_words = topk ? kAWordsTopk : kAWords;
+    prm.xstride = static_cast<int32_t>(xchg_words(c.k));
+    if (!prm.err) return DRS_ERR_CUDA;
+
+    // Shared memory: the stages of one chunk each (filled by bulk copies when
+    // rows start 16-byte aligned; in every case they keep a row's e until its
+    // second half), the scratch, the race lists, the top-k buffers.
+    const bool tma = aligned(c.logits, 16) && (c.row_stride % 4 == 0);
+    prm.stage_bytes = (plan.chunk * 4 + 127) & ~127;
+    prm.use_tma = tma ? 1 : 0;
+    const size_t smem =
+        static_cast<size_t>(rsp.nstage) * prm.stage_bytes + fixed_smem(rsp.vec4, topk);
+    if (smem > kSmemPerCta) return DRS_ERR_UNSUPPORTED;
+    const int grid = plan.team * plan.num_teams;
+    // Zero the records this launch uses (a zero tag matches no row) and the
+    // count of the hard-row list.
+    if (cudaMemsetAsync(xchg, 0, static_cast<size_t>(grid) * xchg_words(c.k) * 8, stream) != cudaSuccess)
+        return DRS_ERR_CUDA;
+    if (hard && cudaMemsetAsync(hard, 0, 4, stream) != cudaSuccess) return DRS_ERR_CUDA;
+    if (rsp.lag == 2) return launch_form<kVec4Lag2, 2, 5>(prm, grid, smem, stream);
+    if (rsp.nstage == 4) return launch_form<kVec4Lag1, 1, 4>(prm, grid, smem, stream);
+    return launch_form<kVec4Lag1, 1, 3>(prm, grid, smem, stream);
+}
+
+drs_status check_stats_args(const float* logits, int64_t rows, int64_t vocab, int64_t row_stride,
+                            const float* temps, int64_t canvas_len, int64_t row0, int64_t* argmax,
+                            int64_t* sample, float* entropy, drs_probs_dtype probs_dtype,
+                            void* probs, int64_t probs_row_stride) {
+    if (rows < 0 || row0 < 0 || canvas_len < 1) return DRS_ERR_INVALID_ARG;
+    if (vocab < 1 || row_stride < vocab) return DRS_ERR_INVALID_ARG;
+    if (vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
+    if (!logits || !temps || !argmax || !sample || !entropy) return DRS_ERR_INVALID_ARG;
+    if (probs_dtype != DRS_PROBS_NONE && probs_dtype != DRS_PROBS_BF16 &&
+        probs_dtype != DRS_PROBS_FP16)
+        return DRS_ERR_INVALID_ARG;
+    if ((probs_dtype == DRS_PROBS_NONE) != (probs == nullptr)) return DRS_ERR_INVALID_ARG;
+    if (probs && probs_row_stride < vocab) return DRS_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(probs, 2)) return DRS_ERR_INVALID_ARG;
+    return DRS_OK;
+}
+
+// Top-k of the converged rows into a workspace laid out as: the hard-row
+// list, the row kernel's exchange records, the exact kernel's records.
+drs_status run_topk(RowCall c, void* workspace, cudaStream_t stream) {
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    int32_t* hard = reinterpret_cast<int32_t*>(ws);
+    void* xchg = ws + hard_list_bytes(c.rows);
+    void* exact_ws = ws + hard_list_bytes(c.rows) + xchg_bytes(c.k);
+    if (c.k > kTopkMaxK) {
+        // larger k: the row statistics alone, then the exact kernel on every
+        // converged row
+        if (c.stats) {
+            RowCall s = c;
+            s.k = 0;
+            s.keep = nullptr;
+            const drs_status st = run_rows(s, xchg, nullptr, stream);
+            if (st != DRS_OK) return st;
+        }
+        return exact_topk(c.logits, c.rows, c.vocab, c.row_stride, c.row0, c.temps, c.canvas_len,
+                          c.keep, nullptr, c.k, c.out_ids, c.out_lp, exact_ws, stream);
+    }
+    const drs_status st = run_rows(c, xchg, hard, stream);
+    if (st != DRS_OK) return st;
+    // the rows the row kernel left (candidate buffers overflowed)
+    return exact_topk(c.logits, c.rows, c.vocab, c.row_stride, c.row0, c.temps, c.canvas_len,
+                      c.keep, hard, c.k, c.out_ids, c.out_lp, exact_ws, stream);
+}
+
+}  // namespace
 }  // namespace drs
 
 extern "C" void drs_test_inject_fault(int code) { drs::g_inject_fault.store(code); }
@@ -772,73 +1320,79 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
                                     int64_t probs_row_stride, void* workspace,
                                     size_t workspace_bytes, void* stream) {
     using namespace drs;
-    if (rows < 0 || row0 < 0 || canvas_len < 1) return DRS_ERR_INVALID_ARG;
-    if (vocab < 1 || row_stride < vocab) return DRS_ERR_INVALID_ARG;
-    if (vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
-    if (!logits || !temps || !argmax || !sample || !entropy) return DRS_ERR_INVALID_ARG;
-    if (probs_dtype != DRS_PROBS_NONE && probs_dtype != DRS_PROBS_BF16 &&
-        probs_dtype != DRS_PROBS_FP16)
-        return DRS_ERR_INVALID_ARG;
-    if ((probs_dtype == DRS_PROBS_NONE) != (probs == nullptr)) return DRS_ERR_INVALID_ARG;
-    if (probs && probs_row_stride < vocab) return DRS_ERR_INVALID_ARG;
-    if (!aligned(logits, 4) || !aligned(probs, 2)) return DRS_ERR_INVALID_ARG;
+    const drs_status chk = check_stats_args(logits, rows, vocab, row_stride, temps, canvas_len,
+                                            row0, argmax, sample, entropy, probs_dtype, probs,
+                                            probs_row_stride);
+    if (chk != DRS_OK) return chk;
     if (rows == 0) return DRS_OK;
     const size_t need = drs_row_stats_workspace_bytes(rows, vocab);
     if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
         return DRS_ERR_INVALID_ARG;
+    static_assert(1024 * kAWords * 8 * kRing + 1024 * 16 * kRing <= 1024 * kXchgPerCta,
+                  "row-stats workspace");
+    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, seed, row0, argmax, sample,
+              entropy, probs_dtype, probs, probs_row_stride, nullptr, 0, nullptr, nullptr, true};
+    return run_rows(c, workspace, nullptr, static_cast<cudaStream_t>(stream));
+}
 
-    const int sms = sm_count();
-    if (sms <= 0) return DRS_ERR_CUDA;
-    const size_t scratch = (sizeof(Scratch) + 127) & ~static_cast<size_t>(127);
-    const RowStatsPlan rsp = plan_row_stats(rows, static_cast<int>(vocab), sms, scratch);
-    const RowPlan& plan = rsp.rows;
-    if (!plan.team) return DRS_ERR_UNSUPPORTED;
-    // per-team row counts are int
-    if ((rows + plan.num_teams - 1) / plan.num_teams > INT_MAX / 2) return DRS_ERR_UNSUPPORTED;
+extern "C" size_t drs_row_stats_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k) {
+    (void)vocab;
+    if (k <= 0 || rows < 0) return 0;
+    return drs::hard_list_bytes(rows) + drs::xchg_bytes(k) + drs::exact_topk_workspace_bytes(k);
+}
 
-    RowStatsParams prm{};
-    prm.logits = logits;
-    prm.row_stride = row_stride;
-    prm.rows = rows;
-    prm.row0 = row0;
-    prm.temps = temps;
-    prm.canvas_len = canvas_len;
-    prm.argmax = argmax;
-    prm.sample = sample;
-    prm.entropy = entropy;
-    prm.probs = probs;
-    prm.probs_row_stride = probs_row_stride;
-    prm.xchg = workspace;
-    prm.err = device_error_flag();
-    prm.rk = PhiloxRoundKeys::of(seed);
-    prm.vocab = static_cast<int32_t>(vocab);
-    prm.team = plan.team;
-    prm.chunk = plan.chunk;
-    prm.num_teams = plan.num_teams;
-    prm.probs_dtype = static_cast<int32_t>(probs_dtype);
-    prm.probs_vec = probs && aligned(probs, 8) && (probs_row_stride % 4 == 0);
-    prm.index32 = (row0 + rows <= static_cast<int64_t>(UINT32_MAX)) &&
-                  (canvas_len <= static_cast<int64_t>(UINT32_MAX));
-    prm.fault = g_inject_fault.exchange(0);
-    if (!prm.err) return DRS_ERR_CUDA;
+extern "C" drs_status drs_row_stats_topk(const float* logits, int64_t rows, int64_t vocab,
+                                         int64_t row_stride, const float* temps,
+                                         int64_t canvas_len, uint64_t seed, int64_t row0,
+                                         int64_t* argmax, int64_t* sample, float* entropy,
+                                         drs_probs_dtype probs_dtype, void* probs,
+                                         int64_t probs_row_stride, const uint8_t* keep, int32_t k,
+                                         int32_t* out_ids, float* out_logprobs, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+    using namespace drs;
+    const drs_status chk = check_stats_args(logits, rows, vocab, row_stride, temps, canvas_len,
+                                            row0, argmax, sample, entropy, probs_dtype, probs,
+                                            probs_row_stride);
+    if (chk != DRS_OK) return chk;
+    if (k < 0 || k > vocab || k > exact_topk_max_k()) return DRS_ERR_INVALID_ARG;
+    if (k > 0 && (!keep || !out_ids || !out_logprobs)) return DRS_ERR_INVALID_ARG;
+    if (rows == 0) return DRS_OK;
+    if (k == 0)
+        return drs_row_stats(logits, rows, vocab, row_stride, temps, canvas_len, seed, row0,
+                             argmax, sample, entropy, probs_dtype, probs, probs_row_stride,
+                             workspace, workspace_bytes, stream);
+    const size_t need = drs_row_stats_topk_workspace_bytes(rows, vocab, k);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
+        return DRS_ERR_INVALID_ARG;
+    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, seed, row0, argmax, sample,
+              entropy, probs_dtype, probs, probs_row_stride, keep, k, out_ids, out_logprobs, true};
+    return run_topk(c, workspace, static_cast<cudaStream_t>(stream));
+}
 
-    // Shared memory: the stages of one chunk each (filled by bulk copies when
-    // rows start 16-byte aligned; in every case they keep a row's e until its
-    // second half) plus the scratch.
-    const bool tma = aligned(logits, 16) && (row_stride % 4 == 0);
-    prm.stage_bytes = (plan.chunk * 4 + 127) & ~127;
-    prm.use_tma = tma ? 1 : 0;
-    const size_t smem = static_cast<size_t>(rsp.nstage) * prm.stage_bytes + scratch;
-    if (smem > kSmemPerCta) return DRS_ERR_UNSUPPORTED;
-    const int grid = plan.team * plan.num_teams;
-    // Zero the records this launch uses: a zero tag matches no row.
-    if (cudaMemsetAsync(workspace, 0, static_cast<size_t>(grid) * kXchgPerCta,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return DRS_ERR_CUDA;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (rsp.lag == 2) return launch_row_stats<kVec4Lag2, 2, 5>(prm, grid, smem, st);
-    if (rsp.nstage == 4) return launch_row_stats<kVec4Lag1, 1, 4>(prm, grid, smem, st);
-    return launch_row_stats<kVec4Lag1, 1, 3>(prm, grid, smem, st);
+extern "C" size_t drs_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k) {
+    return drs_row_stats_topk_workspace_bytes(rows, vocab, k);
+}
+
+extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64_t vocab,
+                                        int64_t row_stride, const float* temps,
+                                        int64_t canvas_len, const uint8_t* keep, int32_t k,
+                                        int32_t* out_ids, float* out_logprobs, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    using namespace drs;
+    if (rows < 0 || canvas_len < 1 || k < 0) return DRS_ERR_INVALID_ARG;
+    if (vocab < 1 || row_stride < vocab) return DRS_ERR_INVALID_ARG;
+    if (vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
+    if (k > vocab || k > exact_topk_max_k()) return DRS_ERR_INVALID_ARG;
+    if (rows % canvas_len != 0) return DRS_ERR_INVALID_ARG;
+    if (k == 0 || rows == 0) return DRS_OK;
+    if (!logits || !temps || !keep || !out_ids || !out_logprobs) return DRS_ERR_INVALID_ARG;
+    if (!aligned(logits, 4)) return DRS_ERR_INVALID_ARG;
+    const size_t need = drs_topk_workspace_bytes(rows, vocab, k);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
+        return DRS_ERR_INVALID_ARG;
+    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, 0, 0, nullptr, nullptr,
+              nullptr, DRS_PROBS_NONE, nullptr, 0, keep, k, out_ids, out_logprobs, false};
+    return run_topk(c, workspace, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------

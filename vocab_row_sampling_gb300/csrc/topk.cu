@@ -42,6 +42,8 @@ struct TopkParams {
     const float* logits;
     int64_t row_stride;
     int64_t rows;
+    int64_t row0;             // global index of row 0 (temperature and keep slot)
+    const int32_t* row_list;  // null, or [0] the count and the rows from [64]
     const float* temps;
     int64_t canvas_len;
     const uint8_t* keep;
@@ -137,12 +139,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ncols = min(p.vocab - col0, p.chunk);
     const int nfull4 = ncols >> 2;
     const uint32_t copy_bytes = static_cast<uint32_t>(nfull4) * 16u;
-    const int64_t nrows = team_id < p.rows ? (p.rows - 1 - team_id) / p.num_teams + 1 : 0;
+    // the rows: every row of the call (those of unconverged slots skipped),
+    // or the rows of a list whose length a previous kernel left on the device
+    const int64_t nlisted = p.row_list ? static_cast<int64_t>(p.row_list[0]) : p.rows;
+    const int64_t nrows = team_id < nlisted ? (nlisted - 1 - team_id) / p.num_teams + 1 : 0;
     const int K = p.k;
     const bool use_tma = p.nstage > 0;
 
-    auto row_of = [&](int64_t j) { return team_id + j * p.num_teams; };
-    auto kept = [&](int64_t j) { return p.keep[row_of(j) / p.canvas_len] != 0; };
+    auto row_of = [&](int64_t j) {
+        const int64_t r = team_id + j * p.num_teams;
+        return p.row_list ? static_cast<int64_t>(p.row_list[64 + r]) : r;
+    };
+    auto kept = [&](int64_t j) {
+        return p.row_list != nullptr || p.keep[(p.row0 + row_of(j)) / p.canvas_len] != 0;
+    };
     auto next_kept = [&](int64_t j) {
         while (j < nrows && !kept(j)) ++j;
         return j;
@@ -214,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             issue_next();
         }
-        const ScaledQuotient sq = ScaledQuotient::of(fmaxf(p.temps[row / p.canvas_len], kTempFloor));
+        const ScaledQuotient sq =
+            ScaledQuotient::of(fmaxf(p.temps[(p.row0 + row) / p.canvas_len], kTempFloor));
 #pragma unroll
         for (int i = 0; i < VEC4; ++i) {
             // x / te exactly (infinities kept), then -0.0 -> +0.0 (one value
@@ -466,33 +477,15 @@ drs_status launch_topk(TopkParams& prm, int grid, size_t smem, cudaStream_t stre
 
 }  // namespace
 
-}  // namespace drs
-
-extern "C" size_t drs_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k) {
-    (void)rows;
-    (void)vocab;
+size_t exact_topk_workspace_bytes(int32_t k) {
     if (k <= 0) return 0;
-    return static_cast<size_t>(1024) * drs::kRing * drs::record_bytes(k);
+    return static_cast<size_t>(1024) * kRing * record_bytes(k);
 }
 
-extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64_t vocab,
-                                        int64_t row_stride, const float* temps,
-                                        int64_t canvas_len, const uint8_t* keep, int32_t k,
-                                        int32_t* out_ids, float* out_logprobs, void* workspace,
-                                        size_t workspace_bytes, void* stream) {
-    using namespace drs;
-    if (rows < 0 || canvas_len < 1 || k < 0) return DRS_ERR_INVALID_ARG;
-    if (vocab < 1 || row_stride < vocab) return DRS_ERR_INVALID_ARG;
-    if (vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
-    if (k > vocab || k > kMaxK) return DRS_ERR_INVALID_ARG;
-    if (rows % canvas_len != 0) return DRS_ERR_INVALID_ARG;
-    if (k == 0 || rows == 0) return DRS_OK;
-    if (!logits || !temps || !keep || !out_ids || !out_logprobs) return DRS_ERR_INVALID_ARG;
-    if (!aligned(logits, 4)) return DRS_ERR_INVALID_ARG;
-    const size_t need = drs_topk_workspace_bytes(rows, vocab, k);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
-        return DRS_ERR_INVALID_ARG;
-
+drs_status exact_topk(const float* logits, int64_t rows, int64_t vocab, int64_t row_stride,
+                      int64_t row0, const float* temps, int64_t canvas_len, const uint8_t* keep,
+                      const int32_t* row_list, int32_t k, int32_t* out_ids, float* out_logprobs,
+                      void* workspace, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return DRS_ERR_CUDA;
     const RowPlan plan = plan_rows(rows, static_cast<int>(vocab), sms, false);
@@ -502,6 +495,8 @@ extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64
     prm.logits = logits;
     prm.row_stride = row_stride;
     prm.rows = rows;
+    prm.row0 = row0;
+    prm.row_list = row_list;
     prm.temps = temps;
     prm.canvas_len = canvas_len;
     prm.keep = keep;
@@ -531,6 +526,9 @@ extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64
     if (!prm.nstage) prm.stage_bytes = 0;
     const size_t smem = static_cast<size_t>(prm.nstage) * prm.stage_bytes + scratch;
     const int grid = plan.team * plan.num_teams;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return launch_topk<8>(prm, grid, smem, st);  // plan_rows(..., false): 32 logits per thread
+    return launch_topk<8>(prm, grid, smem, stream);  // plan_rows(..., false): 32 logits per thread
 }
+
+int32_t exact_topk_max_k() { return kMaxK; }
+
+}  // namespace drs
