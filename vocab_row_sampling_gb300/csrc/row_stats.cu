@@ -226,13 +226,36 @@ __device__ __forceinline__ void set_comp(float4& v, int q, float x) {
 
 // Two probabilities rounded to nearest even and packed (first in the low
 // half): bf16 or fp16.
-__device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
-    if (bf16) {
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if (BF16) {
         const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
         return *reinterpret_cast<const uint32_t*>(&h);
     }
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// A thread's probabilities of one row: e * f_w for its float4 slots,
+// rounded and stored (8-byte stores when the row allows them).
+template <bool BF16, int VEC4>
+__device__ __forceinline__ void write_probs(const float4 (&e)[VEC4], float f_w, uint16_t* prow,
+                                            bool vec, int nslot4, int nfull4, int ncols, int tid) {
+#pragma unroll
+    for (int i = 0; i < VEC4; ++i) {
+        const int f = i * kCompute + tid;
+        if (i * kCompute >= nslot4 || f >= nslot4) continue;
+        const uint32_t lo = pack2<BF16>(e[i].x * f_w, e[i].y * f_w);
+        const uint32_t hi = pack2<BF16>(e[i].z * f_w, e[i].w * f_w);
+        if (vec && f < nfull4) {
+            __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
+        } else {
+            const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                      static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+            for (int q = 0; q < 4; ++q)
+                if (4 * f + q < ncols) prow[4 * f + q] = code[q];
+        }
+    }
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -598,9 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           ? ex2_approx(fmaf(mw - ri.near_best, kLog2e, kRaceMarginLog2))
                                           : 0.0f;
                     uint32_t pmask = 0;
+                    if (stats && ri.noisy) {
 #pragma unroll
-                    for (int i = 0; i < VEC4; ++i)
-                        if (max4(e[i]) * r_w >= 0x1p-24f) pmask |= 1u << i;
+                        for (int i = 0; i < VEC4; ++i)
+                            if (max4(e[i]) * r_w >= 0x1p-24f) pmask |= 1u << i;
+                    }
 
                     // top-k candidates: e >= e_thr is implied by x >= thr (the
                     // exponent lowered by 2^-8 for rounding); too low an e_thr
@@ -639,29 +664,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 
                     if (stats && p.probs_dtype != 0) {
+                        // e^(s - M) / S = e * e^(M_w - M) / S; a row that is -inf
+                        // everywhere gives NaN (every e is finite)
                         const float big_m = ri.row_max;
-                        // e^(s - M) / S = e * e^(M_w - M) / S
-                        const float f_w =
-                            mw == -INFINITY ? 0.0f : ex2_approx(fmaf(mw - big_m, kLog2e, -ri.log2s));
-                        const bool bf16 = p.probs_dtype == 1;
+                        const float f_w = big_m == -INFINITY ? NAN
+                                          : mw == -INFINITY ? 0.0f
+                                                            : ex2_approx(fmaf(mw - big_m, kLog2e, -ri.log2s));
                         uint16_t* prow = static_cast<uint16_t*>(p.probs) + frow * p.probs_row_stride + col0;
-#pragma unroll
-                        for (int i = 0; i < VEC4; ++i) {
-                            const int f = i * kCompute + tid;
-                            if (i * kCompute >= nslot4 || f >= nslot4) continue;
-                            float pr[4] = {e[i].x * f_w, e[i].y * f_w, e[i].z * f_w, e[i].w * f_w};
-                            if (big_m == -INFINITY) pr[0] = pr[1] = pr[2] = pr[3] = NAN;
-                            const uint32_t lo = pack2(pr[0], pr[1], bf16);
-                            const uint32_t hi = pack2(pr[2], pr[3], bf16);
-                            if (p.probs_vec && f < nfull4) {
-                                __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
-                            } else {
-                                const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
-                                                          static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
-                                for (int q = 0; q < 4; ++q)
-                                    if (4 * f + q < ncols) prow[4 * f + q] = code[q];
-                            }
-                        }
+                        if (p.probs_dtype == 1)
+                            write_probs<true, VEC4>(e, f_w, prow, p.probs_vec != 0, nslot4, nfull4, ncols, tid);
+                        else
+                            write_probs<false, VEC4>(e, f_w, prow, p.probs_vec != 0, nslot4, nfull4, ncols, tid);
                     }
 
                     if (stats && ri.noisy) {
