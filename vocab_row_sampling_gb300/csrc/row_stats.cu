@@ -103,6 +103,8 @@ constexpr uint32_t kHardRow = 0xFFFFFFFFu;  // count word: candidates overflowed
 constexpr int kAWords = 6;             // first record: M, S, W, argmax, B, B column
 constexpr int kAWordsTopk = kAWords + 2;  // + the CTA's threshold candidate (and a pad word)
 constexpr int kHardListOffset = 64;    // int32 index of the first row of the hard-row list
+constexpr int kHeadKeys = 7;           // candidate keys read with a candidate record's count
+constexpr int kHeadWords = 2 + 2 * kHeadKeys;
 
 // log2(1.0002): the race's bound e^(s - best) is widened by 2e-4 so that
 // rounding in it (at most a relative 2^-15 for e taken from the raw
@@ -891,11 +893,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool do_b = kb >= 0 && kb < nrows && !sc.info[kb & (kRowRing - 1)].skip;
             const bool topk_b = do_b && sc.info[kb & (kRowRing - 1)].topk;
             bool ok = true;
-            uint64_t ra[kAWordsTopk], rb[2] = {0, 0}, rk8[8];
+            uint64_t ra[kAWordsTopk], rb[2] = {0, 0}, rk8[kHeadWords];
 #pragma unroll
             for (int i = 0; i < kAWordsTopk; ++i) ra[i] = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) rk8[i] = 0;
+            for (int i = 0; i < kHeadWords; ++i) rk8[i] = 0;
             if (do_a && !work_a) {
                 // an unconverged row in top-k-only mode: no exchange, but the
                 // compute warps' first half of it is awaited so that this
@@ -906,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool need_b = do_b && stats;
             if (lane < p.team && (work_a || need_b || topk_b)) {
                 // one polling loop over the member's first record of row m,
-                // second record and candidate head (count and up to three
+                // second record and candidate head (count and up to seven
                 // keys) of row kb: all in flight together
                 const int cta = team_id * p.team + lane;
                 const uint64_t* wa = rec_a(p, cta, m & (kRing - 1));
@@ -932,13 +934,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!done_k) {
 #pragma unroll
-                        for (int i = 0; i < 8; i += 2) ld_relaxed_v2(wk + i, rk8[i], rk8[i + 1]);
+                        for (int i = 0; i < kHeadWords; i += 2) ld_relaxed_v2(wk + i, rk8[i], rk8[i + 1]);
                         if (static_cast<uint32_t>(rk8[0]) == tb && static_cast<uint32_t>(rk8[1]) == tb) {
                             const uint32_t c = payload_u(rk8[0]);
-                            const int nk = c == kHardRow ? 0 : (c < 3u ? static_cast<int>(c) : 3);
+                            const int nk = c == kHardRow ? 0 : (c < static_cast<uint32_t>(kHeadKeys) ? static_cast<int>(c) : kHeadKeys);
                             bool g = true;
 #pragma unroll
-                            for (int i = 0; i < 3; ++i)
+                            for (int i = 0; i < kHeadKeys; ++i)
                                 if (i < nk)
                                     g &= static_cast<uint32_t>(rk8[2 + 2 * i]) == tb &&
                                          static_cast<uint32_t>(rk8[3 + 2 * i]) == tb;
@@ -1049,16 +1051,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     } else {
                         if (have && c > 0) {
-                            // the first three keys came with the head; the rest
-                            // are read four at a time
+                            // the first keys came with the head; the rest are
+                            // read four at a time
 #pragma unroll
-                            for (int r = 0; r < 3; ++r)
+                            for (int r = 0; r < kHeadKeys; ++r)
                                 if (r < c)
                                     tk_merge[off + r] = (static_cast<uint64_t>(payload_u(rk8[2 + 2 * r])) << 32) |
                                                         payload_u(rk8[3 + 2 * r]);
                             const uint64_t* src = rec_k(p, team_id * p.team + lane, kb & (kRing - 1)) + 2;
                             const uint64_t t0 = global_timer_ns();
-                            for (int r0 = 3; r0 < c && okk; r0 += 4) {
+                            for (int r0 = kHeadKeys; r0 < c && okk; r0 += 4) {
                                 uint64_t kw[8];
                                 const int nw = 2 * (c - r0 < 4 ? c - r0 : 4);
                                 okk = poll_words(src + 2 * r0, nw, tag, kw, t0);
