@@ -231,12 +231,13 @@ drs_status drs_scaled_logits(const float *logits, int64_t n, float temp,
                              float *out, void *stream);
 
 /*
- * Test hook for the failure path (not for production use). code != 0: the
- * next drs_row_stats launch in this process has CTA 0 withhold its first
- * exchange record. Its teammates' bounded waits then run out (about 1 s),
- * the kernel skips the rest of that team's rows and raises the device flag
- * that drs_get_device_error reports; the CUDA context stays usable. The
- * hook resets itself after one launch; code 0 clears it.
+ * Test hook for the failure path (not for production use). code != 0: in
+ * the next row-statistics call of this process, CTA 0 of the first pass
+ * never fills its first shared-memory stage. Its warps' bounded waits on the
+ * stage run out (about 1 s), the CTA stops and raises the device flag that
+ * drs_get_device_error reports; the call's results are not valid, the CUDA
+ * context stays usable. The hook resets itself after one call; code 0
+ * clears it.
  */
 void drs_test_inject_fault(int code);
 

@@ -43,4 +43,39 @@ drs_status exact_topk(const float* logits, int64_t rows, int64_t vocab, int64_t 
                       const int32_t* row_list, int32_t k, int32_t* out_ids, float* out_logprobs,
                       void* workspace, cudaStream_t stream);
 
+// One call of the row statistics path: stats (argmax, sample, entropy and
+// optionally probs) of every row, and with k > 0 the top-k logprobs of the
+// converged rows (every row when keep is null). Temperatures and keep flags
+// are indexed by global slot (row0 + row) / canvas_len.
+struct RowCall {
+    const float* logits;
+    int64_t rows, vocab, row_stride;
+    const float* temps;
+    int64_t canvas_len;
+    uint64_t seed;
+    int64_t row0;
+    int64_t* argmax;
+    int64_t* sample;
+    float* entropy;
+    drs_probs_dtype probs_dtype;
+    void* probs;
+    int64_t probs_row_stride;
+    const uint8_t* keep;
+    int32_t k;
+    int32_t* out_ids;
+    float* out_lp;
+    bool stats;
+};
+
+// The fault-injection test hook (drs_test_inject_fault): the pending code,
+// cleared by reading it.
+int take_injected_fault();
+
+// The two-pass row kernels (row_split.cu). The workspace starts with the
+// hard-row list (count at [0], rows from [64]): rows whose top-k the exact
+// kernel must finish. k is at most split_max_k().
+size_t split_workspace_bytes(int64_t rows, int64_t vocab, int32_t k);
+int32_t split_max_k();
+drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream);
+
 }  // namespace drs

@@ -1,0 +1,1164 @@
+// row_split.cu -- the row statistics of temperature-scaled logits (argmax,
+// Gumbel-max sample, softmax entropy, optionally the softmax in bf16/fp16)
+// and the top-k logprobs of the rows of converged slots, in two streaming
+// passes over the logits (page "vllm.model_executor.models.
+// diffusion_gemma_sampler": module docstring, sample_row_stats,
+// sample_row_stats_reference, stash_converged_logprobs, _lp_topk_kernel).
+//
+// Layout of the work. A row of V fp32 logits is cut into tiles of 8192
+// columns. A CTA of 256 threads works on one tile at a time (slot i of
+// thread t holds columns 4*(i*256+t)+0..3 of the tile, i < 8); the CTAs of
+// a persistent grid take the tiles of the rows of a work list round robin.
+// No CTA ever waits for another: the tiles of a row meet through records in
+// global memory that a later kernel on the stream merges.
+//
+// Kernels, in stream order:
+//   prep   the rows that pass 1 works on (all rows, or the rows of converged
+//          slots in top-k-only calls) into a list, with each row's
+//          temperature and its quotient constants.
+//   pass 1 per tile, per warp: the warp max M_w of the scaled logits s = x /
+//          Te (Te = max(T, 1e-10)) and the lowest column reaching it;
+//          S_w = sum e^(s - M_w), W_w = sum e^(s - M_w) (s - M_w) (the online
+//          max and sum of the page). While |M_w| < 256 the warp works on the
+//          raw logits: the max is found among them, only the candidates for
+//          the argmax are divided (exactly), and e^(s - M_w) = 2^(x log2(e) /
+//          Te - c), c the rounded reference; warps with larger scaled values
+//          divide every logit exactly first. The tile's record combines the
+//          warps, with the Gumbel-max score of each warp's argmax element and
+//          the warps' raw maxima.
+//   merge  one warp per row: max M, S, W (entropy log S - W / S), argmax, B =
+//          the best of the warps' argmax scores, and the top-k threshold thr
+//          = the k-th largest raw warp maximum (k distinct elements reach it,
+//          so the row's top k all do); the row's record, and the list of rows
+//          that pass 2 works on.
+//   pass 2 per tile: the probabilities 2^(x log2(e) / Te - c2) (c2 the rounded
+//          log2 of e^M S), rounded to nearest even; the pruned race against B
+//          (an element can only win if 1 - u <= -log u <= e^(s - B): float4
+//          groups whose largest e^(s - B) is below 2^-24 are dropped, the
+//          others go on a per-warp list shared out one Philox call per lane,
+//          and the few survivors are rescored exactly); the top-k candidates
+//          x >= thr, keyed by (exact scaled value, lower column).
+//   finish one warp per row: the sample (the best of the tiles' race winners
+//          and B); the top k of the row's candidates by rank, logprob
+//          s - M - log S. Rows whose candidates overflow the lists, or that
+//          have no threshold, go on a device list for the exact top-k kernel.
+//
+// The passes stream their tiles through three shared-memory stages filled by
+// bulk copies (TMA), the row's record riding along with each tile. Warps run
+// freely: a warp waits for a stage's copy, works on the tile and counts
+// itself out of the stage; the warp that counts out last finishes the tile
+// (combines the warps' results) and refills the stage. No CTA-wide barrier
+// in the loop.
+//
+// HBM traffic: every logit is read twice (once per pass) and every
+// probability written once; the records are a few bytes per thousand
+// logits. No fp64 arithmetic.
+#include <cfloat>
+#include <climits>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "drs_device.cuh"
+#include "drs_internal.h"
+
+namespace drs {
+namespace {
+
+constexpr int kSThreads = 256;
+constexpr int kSWarps = kSThreads / 32;
+constexpr int kSVec4 = 8;
+constexpr int kTileCols = kSThreads * kSVec4 * 4;  // 8192
+constexpr int kMaxTiles = (DRS_MAX_VOCAB + kTileCols - 1) / kTileCols;
+constexpr int kOrdPerLane = (kMaxTiles * kSWarps + 31) / 32;
+constexpr int kStages = 3;                         // tiles in flight per CTA
+constexpr int kStageF4 = kTileCols / 4;             // float4 per stage
+constexpr size_t kStageBytes = kTileCols * 4;       // 32 KiB
+constexpr int kMap = 64;                            // tile -> row map, a ring
+constexpr int kTileKeys = 32;     // top-k candidates a tile keeps
+constexpr int kRowKeys = 512;     // top-k candidates a row merges
+constexpr int kSplitMaxK = 64;    // larger k: the exact kernel
+constexpr int kHardOffset = 64;   // hard-row list: count at [0], rows from [64]
+constexpr int kCount1 = 1;        // header words: pass-1 list length
+constexpr int kCount2 = 2;        //               pass-2 list length
+constexpr float kRawLimit = 256.0f;
+// Slack (log2 units) of the race bounds: covers the roundings of the
+// reference c and of x * log2(e) / Te (a few 1e-5 for |s| up to a few
+// hundred).
+constexpr float kRaceSlack = 0x1p-10f;
+
+// A pass-1 row: its temperature and the quotient constants (16 bytes).
+struct alignas(16) RowTemp {
+    float temp;
+    float qt;
+    float qy;
+    int qmode;
+};
+
+// Pass-1 record of a tile (64 bytes).
+struct alignas(16) TileStats {
+    float m;      // max exact quotient (-inf: none)
+    float s;      // sum e^(s - m)
+    float w;      // sum e^(s - m) (s - m)
+    int arg;      // lowest column of the max (the tile's first column if none)
+    float b;      // best Gumbel-max score of the warps' argmax elements
+    int bcol;
+    float xmax;   // raw max
+    int pad;
+    uint32_t wmax[kSWarps];  // order keys of the warps' raw maxima, 0: no columns
+};
+static_assert(sizeof(TileStats) == 64, "tile record");
+
+enum : int { kFNoisy = 1, kFTopk = 2, kFRaw = 4 };
+
+// A row after the merge (64 bytes).
+struct alignas(64) RowRecord {
+    float M;      // max scaled logit (exact), -inf: the row is -inf everywhere
+    float log2s;  // log2 S
+    float ls;     // RN(log2(e) * RN(1/Te))
+    float c2;     // raw rows: RN(RN(Mraw * ls) + log2 S) - 64
+    float cB;     // raw rows: RN(RN(Mraw * ls) + (B - M) log2(e)) - slack
+    float B;      // best score among the warps' argmax elements
+    float thr;    // top-k threshold (raw logit)
+    float lns;    // log S
+    int bcol;
+    int arg;
+    int flags;
+    float qt, qy;
+    int qmode;
+    int pad[2];
+};
+static_assert(sizeof(RowRecord) == 64, "row record");
+
+// Pass-2 record of a tile: race winner and candidate count (16 bytes).
+struct alignas(16) TileEnd {
+    float b;
+    int col;
+    int nk;
+    int pad;
+};
+
+struct SplitParams {
+    const float* logits;
+    int64_t row_stride;
+    int64_t rows;
+    int64_t row0;
+    int64_t canvas_len;
+    const float* temps;
+    const uint8_t* keep;
+    int64_t* argmax;
+    int64_t* sample;
+    float* entropy;
+    void* probs;
+    int64_t probs_row_stride;
+    int32_t* out_ids;
+    float* out_lp;
+    int32_t* hard;    // header (hard count, list lengths), then hard rows
+    int32_t* list1;   // rows of pass 1
+    int32_t* list2;   // rows of pass 2
+    RowTemp* rt;
+    TileStats* ts;    // by pass-1 tile
+    RowRecord* rr;    // by row
+    TileEnd* te;      // by pass-2 tile
+    uint64_t* keys;   // by pass-2 tile
+    int* err;
+    PhiloxRoundKeys rk;
+    int vocab;
+    int tiles_per_row;
+    int vec;          // rows start 16-byte aligned: bulk copies
+    int probs_dtype;  // 0 none, 1 bf16, 2 fp16
+    int probs_vec;    // 8-byte probability stores
+    int index32;
+    int stats;
+    int k;
+    int fault;        // test hook: CTA 0 withholds its first tile of pass 1
+};
+
+// ------------------------------------------------------------ helpers
+
+__device__ __forceinline__ uint64_t slot_of(const SplitParams& p, uint64_t grow) {
+    return p.index32 ? static_cast<uint64_t>(static_cast<uint32_t>(grow) /
+                                             static_cast<uint32_t>(p.canvas_len))
+                     : grow / static_cast<uint64_t>(p.canvas_len);
+}
+
+__device__ __forceinline__ void set_comp(float4& v, int q, float x) {
+    if (q == 0) v.x = x;
+    else if (q == 1) v.y = x;
+    else if (q == 2) v.z = x;
+    else v.w = x;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ float max4f(const float4& v) { return max3(v.x, v.y, fmaxf(v.z, v.w)); }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// 2^x with subnormal results flushed to zero (a single special-function
+// instruction).
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Order-preserving unsigned form of an fp32 value (-inf lowest, above 0).
+__device__ __forceinline__ uint32_t ord32(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unord32(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+constexpr uint32_t kOrdNegInf = 0x007FFFFFu;
+
+// Top-k key: the value (-0.0 as +0.0) in the high word, then the lower
+// column first (the _lp_topk_kernel key order).
+__device__ __forceinline__ uint64_t topk_key(float s, int col) {
+    return (static_cast<uint64_t>(ord32(s + 0.0f)) << 32) |
+           static_cast<uint32_t>(0x7FFFFFFF - col);
+}
+__device__ __forceinline__ float key_value(uint64_t key) {
+    return unord32(static_cast<uint32_t>(key >> 32));
+}
+__device__ __forceinline__ int key_col(uint64_t key) {
+    return 0x7FFFFFFF - static_cast<int>(static_cast<uint32_t>(key));
+}
+
+// Two values rounded to nearest even and packed (a in the low half), in one
+// conversion instruction.
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    uint32_t r;
+    if (BF16) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// Philox4x32-10 of (group, 0, row) with the per-seed round keys: each round's
+// two 32x32->64 products taken as one wide multiplication each.
+__device__ __forceinline__ uint4 noise_group(const PhiloxRoundKeys& rk, uint64_t row,
+                                             uint32_t group) {
+    uint32_t c0 = group, c1 = 0u, c2 = static_cast<uint32_t>(row), c3 = static_cast<uint32_t>(row >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        uint64_t pa, pb;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(pa) : "r"(c0), "r"(0xD2511F53u));
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(pb) : "r"(c2), "r"(0xCD9E8D57u));
+        const uint32_t hi_a = static_cast<uint32_t>(pa >> 32), lo_a = static_cast<uint32_t>(pa);
+        const uint32_t hi_b = static_cast<uint32_t>(pb >> 32), lo_b = static_cast<uint32_t>(pb);
+        c0 = hi_b ^ c1 ^ rk.k0[r];
+        c1 = lo_b;
+        c2 = hi_a ^ c3 ^ rk.k1[r];
+        c3 = lo_a;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
+// ------------------------------------------------------- tile pipeline
+
+// Shared state of a CTA's pipeline. Tile n of the CTA is t_n = blockIdx.x +
+// n * grid of its pass's tile space (list index * G + tile of the row); it
+// goes through stage n % kStages. The ring `row`/`col` maps tile n (entry n
+// % kMap) to its row and tile of the row, -1 past the end.
+struct Pipe {
+    uint64_t full[kStages];
+    int count[kStages];
+    int last_n[kStages];  // last tile issued into each stage
+    int abort;
+    int row[kMap];
+    int col[kMap];
+};
+
+// Map tiles first .. first + nfill - 1 (one per lane or thread).
+__device__ __forceinline__ void map_tiles(Pipe& pp, const int32_t* list, int64_t tiles, int G,
+                                          int first, int nfill, int idx) {
+    if (idx >= nfill) return;
+    const int n = first + idx;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+    int row = -1, c = 0;
+    if (t < tiles) {
+        const uint32_t li = static_cast<uint32_t>(t) / static_cast<uint32_t>(G);
+        c = static_cast<int>(static_cast<uint32_t>(t) - li * static_cast<uint32_t>(G));
+        row = list[li];
+    }
+    pp.row[n % kMap] = row;
+    pp.col[n % kMap] = c;
+}
+
+// Issue tile n into its stage: the row's record (`rec_bytes` of `rec_table`)
+// and the tile's whole float4s by bulk copy when rows start 16-byte aligned
+// (else the warps read global memory themselves). Past the end: a plain
+// arrival.
+__device__ __forceinline__ void issue_tile(const SplitParams& p, Pipe& pp, int n, float4* stage,
+                                           void* rec_dst, const void* rec_table, uint32_t rec_bytes,
+                                           bool tma) {
+    const int st = n % kStages;
+    const int row = pp.row[n % kMap];
+    pp.last_n[st] = n;
+    if (p.fault && n == 0 && blockIdx.x == 0 && rec_bytes == sizeof(RowTemp)) {
+        // the test hook: the stage never fills, its waits run out
+        pp.last_n[st] = -1;
+        return;
+    }
+    if (row < 0) {
+        mbar_arrive(&pp.full[st]);
+        return;
+    }
+    const int col0 = pp.col[n % kMap] * kTileCols;
+    const int ncols = min(p.vocab - col0, kTileCols);
+    const uint32_t bytes = tma ? static_cast<uint32_t>(ncols >> 2) * 16u : 0u;
+    mbar_arrive_expect_tx(&pp.full[st], bytes + rec_bytes);
+    tma_load_1d(rec_dst, static_cast<const unsigned char*>(rec_table) + static_cast<size_t>(row) * rec_bytes,
+                rec_bytes, &pp.full[st]);
+    if (bytes) tma_load_1d(stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, bytes, &pp.full[st]);
+}
+
+// Count a warp out of a stage; true on the warp that counted out last (the
+// count is reset for the stage's next tile).
+__device__ __forceinline__ bool release_stage(int* count, int lane) {
+    int last = 0;
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(count, 1) == kSWarps - 1;
+        if (last) *count = 0;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) __threadfence_block();
+    return last != 0;
+}
+
+// Pipeline start: barriers, the first kMap tiles mapped, the first kStages
+// issued.
+__device__ __forceinline__ void pipe_start(const SplitParams& p, Pipe& pp, const int32_t* list,
+                                           int64_t tiles, float4* stages, void* recs,
+                                           const void* rec_table, uint32_t rec_bytes, bool tma) {
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&pp.full[s], 1);
+            pp.count[s] = 0;
+        }
+        pp.abort = 0;
+        fence_barrier_init();
+    }
+    map_tiles(pp, list, tiles, p.tiles_per_row, 0, kMap, tid);
+    __syncthreads();
+    if (tid == 0)
+        for (int s = 0; s < kStages; ++s)
+            issue_tile(p, pp, s, stages + s * kStageF4, static_cast<unsigned char*>(recs) + s * rec_bytes,
+                       rec_table, rec_bytes, tma);
+}
+
+// The last warp out of tile n: refill its stage with tile n + kStages, and
+// every 32 tiles map 32 more (over tiles that every warp is done with).
+__device__ __forceinline__ void pipe_advance(const SplitParams& p, Pipe& pp, int n, const int32_t* list,
+                                             int64_t tiles, float4* stage, void* rec_dst,
+                                             const void* rec_table, uint32_t rec_bytes, bool tma,
+                                             int lane) {
+    if (lane == 0) {
+        fence_proxy_async_smem();
+        issue_tile(p, pp, n + kStages, stage, rec_dst, rec_table, rec_bytes, tma);
+    }
+    if ((n & 31) == 31) map_tiles(pp, list, tiles, p.tiles_per_row, n + 33, 32, lane);
+}
+
+// After the loop: if a wait ran out, copies still in flight land before the
+// CTA's shared memory is released.
+__device__ __forceinline__ void pipe_end(Pipe& pp) {
+    __syncthreads();
+    if (threadIdx.x == 0 && pp.abort)
+        for (int s = 0; s < kStages; ++s)
+            if (pp.last_n[s] >= 0)
+                mbar_wait_bounded(&pp.full[s], static_cast<uint32_t>((pp.last_n[s] / kStages) & 1));
+}
+
+// A thread's float4 slots of the tile (-inf past the row's end): from the
+// stage; the ragged last float4 and (without bulk copies) everything from
+// global memory, stored into the stage as well, so that the stage always
+// holds the whole tile.
+__device__ __forceinline__ void read_tile(float4 (&v)[kSVec4], float4* stage, const float* tp,
+                                          int ncols, int tid, bool tma) {
+    if (tma && ncols == kTileCols) {
+#pragma unroll
+        for (int i = 0; i < kSVec4; ++i) v[i] = stage[i * kSThreads + tid];
+        return;
+    }
+    const int nfull4 = ncols >> 2;
+#pragma unroll
+    for (int i = 0; i < kSVec4; ++i) {
+        const int f = i * kSThreads + tid;
+        float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (f < nfull4) {
+            if (tma) {
+                x = stage[f];
+            } else {
+                x = make_float4(__ldcs(tp + 4 * f), __ldcs(tp + 4 * f + 1), __ldcs(tp + 4 * f + 2),
+                                __ldcs(tp + 4 * f + 3));
+                stage[f] = x;
+            }
+        } else if (f == nfull4 && (ncols & 3)) {
+            for (int q = 0; q < (ncols & 3); ++q) set_comp(x, q, __ldcs(tp + 4 * f + q));
+            stage[f] = x;
+        }
+        v[i] = x;
+    }
+}
+
+// ================================================================ prep
+
+__global__ void __launch_bounds__(256) split_prep(const __grid_constant__ SplitParams p) {
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    bool work = false;
+    if (row < p.rows) {
+        const uint64_t slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
+        const bool kept = p.keep == nullptr || p.keep[slot] != 0;
+        work = p.stats || (p.k > 0 && kept);
+        if (work) {
+            const float temp = p.temps[slot];
+            const ScaledQuotient q = ScaledQuotient::of(fmaxf(temp, kTempFloor));
+            p.rt[row] = RowTemp{temp, q.t, q.y, q.mode};
+        }
+    }
+    const uint32_t b = __ballot_sync(0xffffffffu, work);
+    int base = 0;
+    if (lane == 0 && b) base = atomicAdd(p.hard + kCount1, __popc(b));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (work) p.list1[base + __popc(b & lanemask_lt())] = static_cast<int32_t>(row);
+}
+
+// ============================================================== pass 1
+
+struct WarpPart {
+    float m, s, w, xmax;
+    int arg;
+};
+
+__global__ void __launch_bounds__(kSThreads, 2) split_pass1(const __grid_constant__ SplitParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    float4* stages = reinterpret_cast<float4*>(smem);
+    __shared__ Pipe pp;
+    __shared__ RowTemp rts[kStages];
+    __shared__ WarpPart parts[2][kStages][kSWarps];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const bool stats = p.stats != 0;
+    const bool tma = p.vec != 0;
+    const int G = p.tiles_per_row;
+    const int64_t tiles = static_cast<int64_t>(p.hard[kCount1]) * G;
+    pipe_start(p, pp, p.list1, tiles, stages, rts, p.rt, sizeof(RowTemp), tma);
+    for (int n = 0;; ++n) {
+        const int st = n % kStages;
+        const int par = (n / kStages) & 1;
+        float4* stage = stages + st * kStageF4;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pp.full[st], static_cast<uint32_t>(par)))) {
+            if (lane == 0) {
+                pp.abort = 1;
+                raise_device_error(p.err, 1);
+            }
+            break;
+        }
+        const int row = pp.row[n % kMap];
+        if (row < 0) break;
+        const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+        const int col0 = pp.col[n % kMap] * kTileCols;
+        const int ncols = min(p.vocab - col0, kTileCols);
+        const float temp = rts[st].temp;
+        ScaledQuotient sq;
+        sq.t = rts[st].qt;
+        sq.y = rts[st].qy;
+        sq.mode = rts[st].qmode;
+        {
+            float4 v[kSVec4];
+            read_tile(v, stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, ncols, tid, tma);
+
+            // max of the raw logits (division by Te > 0 keeps the order)
+            float m4[kSVec4];
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kSVec4; ++i) {
+                m4[i] = max4f(v[i]);
+                mt = fmaxf(mt, m4[i]);
+            }
+            const float mxw = warp_max_f(mt);
+            const float mw = mxw == -INFINITY ? -INFINITY : sq.exact(mxw);  // M_w
+            const bool raw = !(fabsf(mw) >= kRawLimit);
+
+            // argmax: the lowest column whose exact quotient is M_w; exact(x)
+            // == M_w needs x >= mxw - Te * ulp(M_w). The few candidates are
+            // read again from the stage.
+            const float cthr = mxw - fmaxf(fabsf(mxw) * 0x1p-20f, sq.t * 0x1p-140f);
+            int arg_t = INT_MAX;
+            if (stats && mt >= cthr && mw != -INFINITY) {
+                uint32_t smask = 0;
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i) smask |= (m4[i] >= cthr ? 1u : 0u) << i;
+#pragma unroll 1
+                while (smask && arg_t == INT_MAX) {
+                    const int f = (__ffs(smask) - 1) * kSThreads + tid;
+                    smask &= smask - 1;
+                    const float4 x4 = stage[f];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float x = comp(x4, q);
+                        if (arg_t == INT_MAX && x >= cthr && 4 * f + q < ncols && sq.exact(x) == mw)
+                            arg_t = col0 + 4 * f + q;
+                    }
+                }
+            }
+            const int aw = stats ? warp_min_nonneg(arg_t) : INT_MAX;
+
+            // t = (s - M_w) log2(e): raw x * log2(e)/Te - c, c = RN(mxw *
+            // log2(e)/Te), else (s - M_w) * log2(e). Terms below 2^-126 of
+            // S >= 1 are flushed. A -inf logit (e = 0, t = -inf) makes W NaN:
+            // such warps sum again with t clamped to a finite value.
+            float lscale, cref;
+            if (raw) {
+                lscale = kLog2e * sq.y;
+                cref = mxw * lscale;
+            } else {
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i) {
+                    v[i].x = sq.exact(v[i].x) - mw;
+                    v[i].y = sq.exact(v[i].y) - mw;
+                    v[i].z = sq.exact(v[i].z) - mw;
+                    v[i].w = sq.exact(v[i].w) - mw;
+                }
+                lscale = kLog2e;
+                cref = 0.0f;
+            }
+            float sw, ww;
+            for (int pass = 0;; ++pass) {
+                const float clamp = pass ? -FLT_MAX : -INFINITY;
+                float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wa[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float tq = fmaf(comp(v[i], q), lscale, -cref);
+                        if (pass) tq = fmaxf(tq, clamp);
+                        const float e = ex2_ftz(tq);
+                        sa[q] += e;
+                        wa[q] = fmaf(e, tq, wa[q]);
+                    }
+                }
+                sw = warp_sum_f((sa[0] + sa[1]) + (sa[2] + sa[3]));
+                ww = warp_sum_f((wa[0] + wa[1]) + (wa[2] + wa[3])) * kLn2;
+                if (pass || !isnan(ww)) break;
+            }
+            if (lane == 0) parts[par][st][warp] = WarpPart{mw, sw, ww, mxw, aw};
+        }
+        if (!release_stage(&pp.count[st], lane)) continue;
+
+        // the last warp out: refill the stage, then the tile's record (the
+        // warps combined, one lane each)
+        const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
+        pipe_advance(p, pp, n, p.list1, tiles, stage, &rts[st], p.rt, sizeof(RowTemp), tma, lane);
+        const bool hv = lane < kSWarps;
+        const WarpPart wp = hv ? parts[par][st][lane] : WarpPart{-INFINITY, 0.0f, 0.0f, -INFINITY, INT_MAX};
+        const float mc = warp_max_f(wp.m);
+        float s_l = 0.0f, w_l = 0.0f;
+        if (wp.m != -INFINITY) {
+            const float dm = wp.m - mc;
+            const float f = ex2_approx(dm * kLog2e);
+            s_l = f * wp.s;
+            w_l = f * fmaf(dm, wp.s, wp.w);
+        }
+        const float s_c = warp_sum_f(s_l);
+        const float w_c = warp_sum_f(w_l);
+        const int a_c = mc == -INFINITY ? col0 : warp_min_nonneg(wp.m == mc ? wp.arg : INT_MAX);
+        // Gumbel-max scores of the warps' argmax elements
+        float b_c = -INFINITY;
+        int bcol_c = INT_MAX;
+        if (stats && temp > 0.0f && wp.arg != INT_MAX) {
+            const uint4 nw = noise_group(p.rk, grow, static_cast<uint32_t>(wp.arg >> 2));
+            b_c = wp.m + gumbel_of_bits(word_of(nw, wp.arg & 3));
+            bcol_c = wp.arg;
+        }
+        warp_best(b_c, bcol_c);
+        const float xm = warp_max_f(wp.xmax);
+        TileStats* dst = p.ts + t;
+        if (hv) dst->wmax[lane] = lane * 128 < ncols ? ord32(wp.xmax) : 0u;
+        if (lane == 0) {
+            dst->m = mc;
+            dst->s = s_c;
+            dst->w = w_c;
+            dst->arg = a_c;
+            dst->b = b_c;
+            dst->bcol = bcol_c;
+            dst->xmax = xm;
+        }
+    }
+    pipe_end(pp);
+}
+
+// ============================================================== merge
+
+constexpr int kRowWarps = 8;  // rows per CTA of the merge and finish kernels
+
+__global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_constant__ SplitParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t li = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+    if (li >= p.hard[kCount1]) return;
+    const int64_t row = p.list1[li];
+    const uint64_t slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
+    const bool kept = p.keep == nullptr || p.keep[slot] != 0;
+    const RowTemp rt = p.rt[row];
+    const float temp = rt.temp;
+    const int G = p.tiles_per_row;
+    const TileStats* tr = p.ts + li * G;
+    float m = -INFINITY, s = 0.0f, w = 0.0f, xm = -INFINITY, b = -INFINITY;
+    int arg = INT_MAX, bc = INT_MAX;
+    for (int c = lane; c < G; c += 32) {
+        const TileStats r = tr[c];
+        xm = fmaxf(xm, r.xmax);
+        if (r.m != -INFINITY) {
+            if (m == -INFINITY) {
+                m = r.m;
+                s = r.s;
+                w = r.w;
+                arg = r.arg;
+            } else {
+                const float nm = fmaxf(m, r.m);
+                const float d1 = m - nm, d2 = r.m - nm;
+                const float f1 = ex2_approx(d1 * kLog2e), f2 = ex2_approx(d2 * kLog2e);
+                w = f1 * fmaf(d1, s, w) + f2 * fmaf(d2, r.s, r.w);
+                s = f1 * s + f2 * r.s;
+                arg = r.m > m ? r.arg : (r.m == m ? min(arg, r.arg) : arg);
+                m = nm;
+            }
+        } else if (m == -INFINITY) {
+            arg = min(arg, r.arg);
+        }
+        if (beats(r.b, r.bcol, b, bc)) {
+            b = r.b;
+            bc = r.bcol;
+        }
+    }
+    const float big_m = warp_max_f(m);
+    float s_l = 0.0f, w_l = 0.0f;
+    if (m != -INFINITY) {
+        const float dm = m - big_m;
+        const float f = ex2_approx(dm * kLog2e);
+        s_l = f * s;
+        w_l = f * fmaf(dm, s, w);
+    }
+    const float s_tot = warp_sum_f(s_l);
+    const float w_tot = warp_sum_f(w_l);
+    const int arg_row = warp_min_nonneg(m == big_m ? arg : INT_MAX);
+    warp_best(b, bc);
+    const float mraw = warp_max_f(xm);
+
+    const bool topk = p.k > 0 && kept;
+    float thr = -INFINITY;
+    bool hard = false;
+    if (topk) {
+        // the k-th largest of the row's warp maxima (absent warps are 0,
+        // below every value): k rounds of a warp max, each removing one
+        // occurrence
+        uint32_t o[kOrdPerLane];
+#pragma unroll
+        for (int u = 0; u < kOrdPerLane; ++u) {
+            const int jx = lane + 32 * u;
+            o[u] = jx < kSWarps * G ? tr[jx / kSWarps].wmax[jx % kSWarps] : 0u;
+        }
+        uint32_t kth = 0;
+        for (int r = 0; r < p.k; ++r) {
+            uint32_t lm = 0;
+#pragma unroll
+            for (int u = 0; u < kOrdPerLane; ++u) lm = max(lm, o[u]);
+            uint32_t top;
+            asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(top) : "r"(lm));
+            kth = top;
+            const uint32_t holders = __ballot_sync(0xffffffffu, lm == top);
+            if (lane == __ffs(holders) - 1) {
+                bool done = false;
+#pragma unroll
+                for (int u = 0; u < kOrdPerLane; ++u)
+                    if (!done && o[u] == top) {
+                        o[u] = 0;
+                        done = true;
+                    }
+            }
+        }
+        // absent, or -inf: no threshold, the exact kernel takes the row.
+        // Lowered by Te ulp(s): a logit below thr whose exact quotient
+        // equals thr's is a candidate too (equal values rank by column).
+        if (kth > kOrdNegInf) {
+            const float x = unord32(kth);
+            thr = x - fmaxf(fabsf(x) * 0x1p-20f, rt.qt * 0x1p-140f);
+        } else {
+            hard = true;
+        }
+    }
+
+    if (lane == 0) {
+        RowRecord rec{};
+        rec.M = big_m;
+        rec.log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
+        rec.lns = rec.log2s * kLn2;
+        rec.ls = kLog2e * rt.qy;
+        const bool raw = !(fabsf(big_m) >= kRawLimit);
+        const float c0 = mraw * rec.ls;
+        rec.c2 = (c0 + rec.log2s) - 64.0f;
+        rec.B = b;
+        rec.bcol = bc;
+        rec.cB = (c0 + (b - big_m) * kLog2e) - kRaceSlack;
+        rec.thr = thr;
+        rec.arg = arg_row;
+        rec.qt = rt.qt;
+        rec.qy = rt.qy;
+        rec.qmode = rt.qmode;
+        const bool noisy = p.stats && temp > 0.0f && big_m != -INFINITY;
+        rec.flags = (noisy ? kFNoisy : 0) | (topk && !hard ? kFTopk : 0) | (raw ? kFRaw : 0);
+        p.rr[row] = rec;
+        if (p.stats) {
+            p.argmax[row] = arg_row;
+            p.entropy[row] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
+            if (!noisy) p.sample[row] = arg_row;
+        }
+        if (hard) {
+            const int idx = atomicAdd(p.hard, 1);
+            p.hard[kHardOffset + idx] = static_cast<int32_t>(row);
+        }
+        // the rows that want probabilities, the race or candidates
+        if ((p.stats && p.probs_dtype != 0) || (rec.flags & (kFNoisy | kFTopk))) {
+            const int idx = atomicAdd(p.hard + kCount2, 1);
+            p.list2[idx] = static_cast<int32_t>(row);
+        }
+    }
+}
+
+// ============================================================== pass 2
+
+// Probabilities 2^t of a tile, t = x ls - c2 (raw rows) or (s - M) log2(e) -
+// log2 S: taken as 2^(t + 64) * 2^-64, so that the flushing 2^x keeps the
+// subnormal results (bf16 and fp16 can hold some); -inf logits give 0.
+template <bool BF16, bool RAW>
+__device__ __forceinline__ void write_probs(const float4 (&v)[kSVec4], const RowRecord& rec,
+                                            const ScaledQuotient& sq, uint16_t* prow, bool vec,
+                                            int ncols, int tid) {
+    const bool full_tile = vec && ncols == kTileCols;
+    const float ls = rec.ls, c2 = rec.c2, big_m = rec.M;
+    const float c64 = rec.log2s - 64.0f;
+#pragma unroll
+    for (int i = 0; i < kSVec4; ++i) {
+        const int f = i * kSThreads + tid;
+        if (!full_tile && 4 * f >= ncols) continue;
+        float pr[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float x = comp(v[i], q);
+            const float tq = RAW ? fmaf(x, ls, -c2) : fmaf(sq.exact(x) - big_m, kLog2e, -c64);
+            pr[q] = ex2_ftz(tq) * 0x1p-64f;
+        }
+        const uint32_t lo = pack2<BF16>(pr[0], pr[1]);
+        const uint32_t hi = pack2<BF16>(pr[2], pr[3]);
+        if (full_tile || (vec && 4 * f + 4 <= ncols)) {
+            __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
+        } else {
+            const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                      static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (4 * f + q < ncols) prow[4 * f + q] = code[q];
+        }
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void probs_of_tile(const float4 (&v)[kSVec4], const RowRecord& rec,
+                                              const ScaledQuotient& sq, uint16_t* prow, bool vec,
+                                              int ncols, int tid) {
+    if (rec.M == -INFINITY) {
+        // a row that is -inf everywhere: NaN
+        const uint16_t code = static_cast<uint16_t>(pack2<BF16>(NAN, NAN));
+        for (int cidx = tid; cidx < ncols; cidx += kSThreads) prow[cidx] = code;
+    } else if (rec.flags & kFRaw) {
+        write_probs<BF16, true>(v, rec, sq, prow, vec, ncols, tid);
+    } else {
+        write_probs<BF16, false>(v, rec, sq, prow, vec, ncols, tid);
+    }
+}
+
+// e^(s - B) of a group, over-estimated by the slack: 2^(x ls - cB) on raw
+// rows, else from the exact quotients (flushed below 2^-126: such elements
+// cannot win).
+__device__ __forceinline__ float4 race_e(const float4& x, const RowRecord& rec,
+                                         const ScaledQuotient& sq) {
+    float4 e;
+    if (rec.flags & kFRaw) {
+        e.x = ex2_ftz(fmaf(x.x, rec.ls, -rec.cB));
+        e.y = ex2_ftz(fmaf(x.y, rec.ls, -rec.cB));
+        e.z = ex2_ftz(fmaf(x.z, rec.ls, -rec.cB));
+        e.w = ex2_ftz(fmaf(x.w, rec.ls, -rec.cB));
+    } else {
+        e.x = ex2_ftz(fmaf(sq.exact(x.x) - rec.B, kLog2e, kRaceSlack));
+        e.y = ex2_ftz(fmaf(sq.exact(x.y) - rec.B, kLog2e, kRaceSlack));
+        e.z = ex2_ftz(fmaf(sq.exact(x.z) - rec.B, kLog2e, kRaceSlack));
+        e.w = ex2_ftz(fmaf(sq.exact(x.w) - rec.B, kLog2e, kRaceSlack));
+    }
+    return e;
+}
+
+// Survivors of a group: elements whose lower bound of 1 - u is at most
+// their e^(s - B).
+__device__ __forceinline__ uint32_t race_group(const float4& e, uint4 w) {
+    const uint32_t wmax = max(max(w.x, w.y), max(w.z, w.w));
+    uint32_t bits = 0;
+    if (one_minus_u_lower(wmax) <= max4f(e)) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (one_minus_u_lower(word_of(w, q)) <= comp(e, q)) bits |= 1u << q;
+    }
+    return bits;
+}
+
+__global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constant__ SplitParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    float4* stages = reinterpret_cast<float4*>(smem);
+    __shared__ Pipe pp;
+    __shared__ RowRecord recs[kStages];
+    __shared__ uint16_t race_at[kSWarps][kSVec4 * 32];
+    __shared__ float best_s[2][kStages][kSWarps];
+    __shared__ int best_c[2][kStages][kSWarps];
+    __shared__ int tile_nk[2][kStages];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const bool probs = p.stats != 0 && p.probs_dtype != 0;
+    const bool tma = p.vec != 0;
+    const int G = p.tiles_per_row;
+    const int64_t tiles = static_cast<int64_t>(p.hard[kCount2]) * G;
+    if (tid < 2 * kStages) tile_nk[tid / kStages][tid % kStages] = 0;
+    pipe_start(p, pp, p.list2, tiles, stages, recs, p.rr, sizeof(RowRecord), tma);
+    for (int n = 0;; ++n) {
+        const int st = n % kStages;
+        const int par = (n / kStages) & 1;
+        float4* stage = stages + st * kStageF4;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pp.full[st], static_cast<uint32_t>(par)))) {
+            if (lane == 0) {
+                pp.abort = 1;
+                raise_device_error(p.err, 1);
+            }
+            break;
+        }
+        const int row = pp.row[n % kMap];
+        if (row < 0) break;
+        const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+        const int col0 = pp.col[n % kMap] * kTileCols;
+        const int ncols = min(p.vocab - col0, kTileCols);
+        const RowRecord& rec = recs[st];
+        const int flags = rec.flags;
+        const bool noisy = (flags & kFNoisy) != 0;
+        const bool topk = (flags & kFTopk) != 0;
+        {
+            const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
+            ScaledQuotient sq;
+            sq.t = rec.qt;
+            sq.y = rec.qy;
+            sq.mode = rec.qmode;
+            float4 v[kSVec4];
+            read_tile(v, stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, ncols, tid, tma);
+
+            if (probs) {
+                uint16_t* prow = static_cast<uint16_t*>(p.probs) + static_cast<int64_t>(row) * p.probs_row_stride + col0;
+                if (p.probs_dtype == 1) probs_of_tile<true>(v, rec, sq, prow, p.probs_vec != 0, ncols, tid);
+                else probs_of_tile<false>(v, rec, sq, prow, p.probs_vec != 0, ncols, tid);
+            }
+
+            float wb = rec.B;
+            int wc = rec.bcol;
+            if (noisy) {
+                // groups whose largest e^(s - B) reaches 2^-24, listed
+                // warp-wide by their float4 index in the stage
+                uint32_t pass = 0;
+                if (flags & kFRaw) {
+                    const float ls = rec.ls, cB = rec.cB;
+#pragma unroll
+                    for (int i = 0; i < kSVec4; ++i)
+                        if (fmaf(max4f(v[i]), ls, -cB) >= -24.0f) pass |= 1u << i;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kSVec4; ++i)
+                        if (fmaf(sq.exact(max4f(v[i])) - rec.B, kLog2e, kRaceSlack) >= -24.0f) pass |= 1u << i;
+                }
+                const uint32_t lt = lanemask_lt();
+                int total = 0;
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i) {
+                    const bool on = (pass >> i) & 1u;
+                    const uint32_t bl = __ballot_sync(0xffffffffu, on);
+                    if (on) race_at[warp][total + __popc(bl & lt)] = static_cast<uint16_t>(i * kSThreads + tid);
+                    total += __popc(bl);
+                }
+                __syncwarp();
+                for (int m = lane; m < total; m += 32) {
+                    const int f = race_at[warp][m];
+                    const float4 x4 = stage[f];
+                    const int c4 = col0 + 4 * f;
+                    const uint4 nw = noise_group(p.rk, grow, static_cast<uint32_t>(c4 >> 2));
+                    uint32_t bits = race_group(race_e(x4, rec, sq), nw);
+                    while (bits) {
+                        const int q = __ffs(bits) - 1;
+                        bits &= bits - 1;
+                        const int col = c4 + q;
+                        if (col == rec.bcol) continue;  // scored already: B
+                        const float score = sq.exact(comp(x4, q)) + gumbel_of_bits(word_of(nw, q));
+                        if (beats(score, col, wb, wc)) {
+                            wb = score;
+                            wc = col;
+                        }
+                    }
+                }
+                warp_best(wb, wc);
+            }
+
+            if (topk) {
+                // candidates x >= thr, keyed by (exact value, lower column)
+                uint64_t* kdst = p.keys + t * kTileKeys;
+                const float thr = rec.thr;
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i) {
+                    if (max4f(v[i]) >= thr) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float x = comp(v[i], q);
+                            if (x >= thr) {
+                                const int col = col0 + 4 * (i * kSThreads + tid) + q;
+                                const int pos = atomicAdd(&tile_nk[par][st], 1);
+                                if (pos < kTileKeys) kdst[pos] = topk_key(sq.exact(x), col);
+                            }
+                        }
+                    }
+                }
+            }
+            if (lane == 0) {
+                best_s[par][st][warp] = wb;
+                best_c[par][st][warp] = wc;
+            }
+        }
+        if (!release_stage(&pp.count[st], lane)) continue;
+
+        // the last warp out: the tile's record, then refill the stage (the
+        // row record in it is read first)
+        float b = lane < kSWarps ? best_s[par][st][lane] : -INFINITY;
+        int bc = lane < kSWarps ? best_c[par][st][lane] : INT_MAX;
+        warp_best(b, bc);
+        if (lane == 0) {
+            p.te[t] = TileEnd{b, bc, topk ? tile_nk[par][st] : 0, 0};
+            tile_nk[par][st] = 0;
+        }
+        __syncwarp();
+        pipe_advance(p, pp, n, p.list2, tiles, stage, &recs[st], p.rr, sizeof(RowRecord), tma, lane);
+    }
+    pipe_end(pp);
+}
+
+// ============================================================== finish
+
+__global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_constant__ SplitParams p) {
+    __shared__ uint64_t keys[kRowWarps][kRowKeys];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t li = static_cast<int64_t>(blockIdx.x) * kRowWarps + warp;
+    if (li >= p.hard[kCount2]) return;
+    const int64_t row = p.list2[li];
+    const int G = p.tiles_per_row;
+    const RowRecord rec = p.rr[row];
+    const TileEnd* te = p.te + li * G;
+    if (rec.flags & kFNoisy) {
+        float b = rec.B;
+        int bc = rec.bcol;
+        for (int c = lane; c < G; c += 32) {
+            const float tb = te[c].b;
+            const int tc = te[c].col;
+            if (beats(tb, tc, b, bc)) {
+                b = tb;
+                bc = tc;
+            }
+        }
+        warp_best(b, bc);
+        if (lane == 0) p.sample[row] = b != -INFINITY ? bc : rec.arg;
+    }
+    if (!(rec.flags & kFTopk)) return;
+    // the row's candidates: counts, then the keys gathered in tile order
+    int n[2] = {0, 0};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c = lane + 32 * u;
+        n[u] = c < G ? te[c].nk : 0;
+    }
+    const bool over = __any_sync(0xffffffffu, n[0] > kTileKeys || n[1] > kTileKeys);
+    int total = 0, off[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        int incl = n[u];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        off[u] = total + incl - n[u];
+        total += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (over || total > kRowKeys || total < p.k) {
+        if (lane == 0) {
+            const int idx = atomicAdd(p.hard, 1);
+            p.hard[kHardOffset + idx] = static_cast<int32_t>(row);
+        }
+        return;
+    }
+    uint64_t* kw = keys[warp];
+    for (int c = 0; c < G; ++c) {
+        const int nc = __shfl_sync(0xffffffffu, c < 32 ? n[0] : n[1], c & 31);
+        const int oc = __shfl_sync(0xffffffffu, c < 32 ? off[0] : off[1], c & 31);
+        const uint64_t* src = p.keys + (li * G + c) * kTileKeys;
+        if (lane < nc) kw[oc + lane] = src[lane];
+    }
+    __syncwarp();
+    const int K = p.k;
+    for (int a = lane; a < total; a += 32) {
+        const uint64_t key = kw[a];
+        int rank = 0;
+        for (int o = 0; o < total; ++o) rank += kw[o] > key;
+        if (rank < K) {
+            p.out_ids[row * K + rank] = key_col(key);
+            p.out_lp[row * K + rank] = rec.M == -INFINITY ? NAN : (key_value(key) - rec.M) - rec.lns;
+        }
+    }
+}
+
+// ================================================================ host
+
+size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+struct SplitLayout {
+    size_t hard, list1, list2, rt, ts, rr, te, keys, total;
+};
+
+SplitLayout split_layout(int64_t rows, int64_t vocab, int32_t k) {
+    const size_t R = static_cast<size_t>(rows);
+    const size_t G = static_cast<size_t>((vocab + kTileCols - 1) / kTileCols);
+    SplitLayout l{};
+    size_t at = 0;
+    l.hard = at;
+    at += round_up(4 * (kHardOffset + R), kWorkspaceAlign);
+    l.list1 = at;
+    at += round_up(4 * R, kWorkspaceAlign);
+    l.list2 = at;
+    at += round_up(4 * R, kWorkspaceAlign);
+    l.rt = at;
+    at += round_up(sizeof(RowTemp) * R, kWorkspaceAlign);
+    l.ts = at;
+    at += round_up(sizeof(TileStats) * R * G, kWorkspaceAlign);
+    l.rr = at;
+    at += round_up(sizeof(RowRecord) * R, kWorkspaceAlign);
+    l.te = at;
+    at += round_up(sizeof(TileEnd) * R * G, kWorkspaceAlign);
+    l.keys = at;
+    if (k > 0) at += round_up(8 * R * G * kTileKeys, kWorkspaceAlign);
+    l.total = at;
+    return l;
+}
+
+template <typename Kernel>
+int resident_grid(Kernel kernel, int threads, size_t smem) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess)
+        return 0;
+    return per_sm * sm_count();
+}
+
+}  // namespace
+
+size_t split_workspace_bytes(int64_t rows, int64_t vocab, int32_t k) {
+    return split_layout(rows, vocab, k).total;
+}
+
+int32_t split_max_k() { return kSplitMaxK; }
+
+drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
+    if (c.rows <= 0) return DRS_OK;
+    if (c.k > kSplitMaxK || c.vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
+    const int G = static_cast<int>((c.vocab + kTileCols - 1) / kTileCols);
+    // tile indices of a pass are 32-bit, list lengths int
+    if (c.rows > INT_MAX / G) return DRS_ERR_UNSUPPORTED;
+    const SplitLayout l = split_layout(c.rows, c.vocab, c.k);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    SplitParams p{};
+    p.logits = c.logits;
+    p.row_stride = c.row_stride;
+    p.rows = c.rows;
+    p.row0 = c.row0;
+    p.canvas_len = c.canvas_len;
+    p.temps = c.temps;
+    p.keep = c.keep;
+    p.argmax = c.argmax;
+    p.sample = c.sample;
+    p.entropy = c.entropy;
+    p.probs = c.probs;
+    p.probs_row_stride = c.probs_row_stride;
+    p.out_ids = c.out_ids;
+    p.out_lp = c.out_lp;
+    p.hard = reinterpret_cast<int32_t*>(ws + l.hard);
+    p.list1 = reinterpret_cast<int32_t*>(ws + l.list1);
+    p.list2 = reinterpret_cast<int32_t*>(ws + l.list2);
+    p.rt = reinterpret_cast<RowTemp*>(ws + l.rt);
+    p.ts = reinterpret_cast<TileStats*>(ws + l.ts);
+    p.rr = reinterpret_cast<RowRecord*>(ws + l.rr);
+    p.te = reinterpret_cast<TileEnd*>(ws + l.te);
+    p.keys = reinterpret_cast<uint64_t*>(ws + l.keys);
+    p.err = device_error_flag();
+    if (!p.err) return DRS_ERR_CUDA;
+    p.rk = PhiloxRoundKeys::of(c.seed);
+    p.tiles_per_row = G;
+    p.vocab = static_cast<int>(c.vocab);
+    p.vec = aligned(c.logits, 16) && (c.row_stride % 4 == 0);
+    p.probs_dtype = static_cast<int>(c.probs_dtype);
+    p.probs_vec = c.probs && aligned(c.probs, 8) && (c.probs_row_stride % 4 == 0);
+    p.index32 = (c.row0 + c.rows <= static_cast<int64_t>(UINT32_MAX)) &&
+                (c.canvas_len <= static_cast<int64_t>(UINT32_MAX));
+    p.stats = c.stats ? 1 : 0;
+    p.k = c.k;
+    p.fault = take_injected_fault();
+    // the header of the hard-row list: its count and the two list lengths
+    if (cudaMemsetAsync(ws + l.hard, 0, 16, stream) != cudaSuccess) return DRS_ERR_CUDA;
+    const size_t smem = kStages * kStageBytes;
+    if (cudaFuncSetAttribute(split_pass1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(split_pass2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return DRS_ERR_CUDA;
+    const int g1 = resident_grid(split_pass1, kSThreads, smem);
+    const int g2 = resident_grid(split_pass2, kSThreads, smem);
+    if (g1 < 1 || g2 < 1) return DRS_ERR_CUDA;
+    const int64_t gp = (c.rows + 255) / 256;
+    const int64_t gr = (c.rows + kRowWarps - 1) / kRowWarps;
+    if (gr > INT_MAX) return DRS_ERR_UNSUPPORTED;
+    split_prep<<<static_cast<int>(gp), 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    split_pass1<<<g1, kSThreads, smem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    split_merge<<<static_cast<int>(gr), kRowWarps * 32, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    split_pass2<<<g2, kSThreads, smem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    split_finish<<<static_cast<int>(gr), kRowWarps * 32, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    return DRS_OK;
+}
+
+}  // namespace drs

@@ -1184,29 +1184,6 @@ size_t hard_list_bytes(int64_t rows) {
 }
 size_t xchg_bytes(int32_t k) { return round_up(1024 * xchg_words(k) * 8, kWorkspaceAlign); }
 
-// One call of the row kernel. stats: argmax, sample, entropy (and probs)
-// of every row; k > 0: top-k of the converged rows (every row when keep is
-// null), hard rows listed in `hard`. xchg: the exchange records.
-struct RowCall {
-    const float* logits;
-    int64_t rows, vocab, row_stride;
-    const float* temps;
-    int64_t canvas_len;
-    uint64_t seed;
-    int64_t row0;
-    int64_t* argmax;
-    int64_t* sample;
-    float* entropy;
-    drs_probs_dtype probs_dtype;
-    void* probs;
-    int64_t probs_row_stride;
-    const uint8_t* keep;
-    int32_t k;
-    int32_t* out_ids;
-    float* out_lp;
-    bool stats;
-};
-
 drs_status run_rows(const RowCall& c, void* xchg, int32_t* hard, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return DRS_ERR_CUDA;
@@ -1288,29 +1265,28 @@ drs_status check_stats_args(const float* logits, int64_t rows, int64_t vocab, in
     return DRS_OK;
 }
 
-// Top-k of the converged rows into a workspace laid out as: the hard-row
-// list, the row kernel's exchange records, the exact kernel's records.
+// Top-k of the converged rows into a workspace laid out as: the split
+// kernels' workspace (the hard-row list first), the exact kernel's records.
 drs_status run_topk(RowCall c, void* workspace, cudaStream_t stream) {
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    int32_t* hard = reinterpret_cast<int32_t*>(ws);
-    void* xchg = ws + hard_list_bytes(c.rows);
-    void* exact_ws = ws + hard_list_bytes(c.rows) + xchg_bytes(c.k);
-    if (c.k > kTopkMaxK) {
+    const int32_t* hard = reinterpret_cast<const int32_t*>(ws);
+    void* exact_ws = ws + split_workspace_bytes(c.rows, c.vocab, c.k > split_max_k() ? 0 : c.k);
+    if (c.k > split_max_k()) {
         // larger k: the row statistics alone, then the exact kernel on every
         // converged row
         if (c.stats) {
             RowCall s = c;
             s.k = 0;
             s.keep = nullptr;
-            const drs_status st = run_rows(s, xchg, nullptr, stream);
+            const drs_status st = split_rows(s, workspace, stream);
             if (st != DRS_OK) return st;
         }
         return exact_topk(c.logits, c.rows, c.vocab, c.row_stride, c.row0, c.temps, c.canvas_len,
                           c.keep, nullptr, c.k, c.out_ids, c.out_lp, exact_ws, stream);
     }
-    const drs_status st = run_rows(c, xchg, hard, stream);
+    const drs_status st = split_rows(c, workspace, stream);
     if (st != DRS_OK) return st;
-    // the rows the row kernel left (candidate buffers overflowed)
+    // the rows the split kernels left (no threshold, or too many candidates)
     return exact_topk(c.logits, c.rows, c.vocab, c.row_stride, c.row0, c.temps, c.canvas_len,
                       c.keep, hard, c.k, c.out_ids, c.out_lp, exact_ws, stream);
 }
@@ -1318,13 +1294,13 @@ drs_status run_topk(RowCall c, void* workspace, cudaStream_t stream) {
 }  // namespace
 }  // namespace drs
 
+int drs::take_injected_fault() { return drs::g_inject_fault.exchange(0); }
+
 extern "C" void drs_test_inject_fault(int code) { drs::g_inject_fault.store(code); }
 
 extern "C" size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab) {
-    (void)rows;
-    (void)vocab;
-    // The exchange records of up to 1024 resident CTAs.
-    return static_cast<size_t>(1024) * drs::kXchgPerCta;
+    if (rows < 0 || vocab < 1) return 0;
+    return drs::split_workspace_bytes(rows, vocab, 0);
 }
 
 extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t vocab,
@@ -1343,17 +1319,15 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
     const size_t need = drs_row_stats_workspace_bytes(rows, vocab);
     if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
         return DRS_ERR_INVALID_ARG;
-    static_assert(1024 * kAWords * 8 * kRing + 1024 * 16 * kRing <= 1024 * kXchgPerCta,
-                  "row-stats workspace");
     RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, seed, row0, argmax, sample,
               entropy, probs_dtype, probs, probs_row_stride, nullptr, 0, nullptr, nullptr, true};
-    return run_rows(c, workspace, nullptr, static_cast<cudaStream_t>(stream));
+    return split_rows(c, workspace, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t drs_row_stats_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k) {
-    (void)vocab;
-    if (k <= 0 || rows < 0) return 0;
-    return drs::hard_list_bytes(rows) + drs::xchg_bytes(k) + drs::exact_topk_workspace_bytes(k);
+    if (k <= 0 || rows < 0 || vocab < 1) return 0;
+    const int32_t ks = k > drs::split_max_k() ? 0 : k;
+    return drs::split_workspace_bytes(rows, vocab, ks) + drs::exact_topk_workspace_bytes(k);
 }
 
 extern "C" drs_status drs_row_stats_topk(const float* logits, int64_t rows, int64_t vocab,
@@ -1424,7 +1398,7 @@ extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64
 
 namespace {
 
-constexpr size_t kNoallocWorkspaceBytes = static_cast<size_t>(1024) * drs::kXchgPerCta;
+constexpr size_t kNoallocWorkspaceBytes = static_cast<size_t>(640) * 1024;
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoallocWorkspaceBytes];
 
 std::mutex g_noalloc_mutex;
@@ -1461,16 +1435,30 @@ extern "C" drs_status drs_row_stats_noalloc(const float* logits, int64_t rows, i
                                             int64_t* argmax, int64_t* sample, float* entropy,
                                             drs_probs_dtype probs_dtype, void* probs,
                                             int64_t probs_row_stride, void* stream) {
-    if (drs_row_stats_workspace_bytes(rows, vocab) > kNoallocWorkspaceBytes)
+    const drs_status chk = drs::check_stats_args(logits, rows, vocab, row_stride, temps,
+                                                 canvas_len, row0, argmax, sample, entropy,
+                                                 probs_dtype, probs, probs_row_stride);
+    if (chk != DRS_OK) return chk;
+    if (rows == 0) return DRS_OK;
+    // rows in batches whose workspace fits the array (one row always does)
+    int64_t batch = rows;
+    while (batch > 1 && drs_row_stats_workspace_bytes(batch, vocab) > kNoallocWorkspaceBytes)
+        batch = (batch + 1) / 2;
+    if (drs_row_stats_workspace_bytes(batch, vocab) > kNoallocWorkspaceBytes)
         return DRS_ERR_UNSUPPORTED;
-    if (rows <= 0)  // validation and the empty call need no workspace
-        return drs_row_stats(logits, rows, vocab, row_stride, temps, canvas_len, seed, row0,
-                             argmax, sample, entropy, probs_dtype, probs, probs_row_stride,
-                             nullptr, 0, stream);
     drs_status st = DRS_OK;
     void* ws = noalloc_workspace(&st);
     if (!ws) return st;
-    return drs_row_stats(logits, rows, vocab, row_stride, temps, canvas_len, seed, row0, argmax,
-                         sample, entropy, probs_dtype, probs, probs_row_stride, ws,
-                         kNoallocWorkspaceBytes, stream);
+    const size_t pbytes = probs_dtype == DRS_PROBS_NONE ? 0 : 2;
+    for (int64_t r = 0; r < rows; r += batch) {
+        const int64_t n = rows - r < batch ? rows - r : batch;
+        void* pr = probs ? static_cast<unsigned char*>(probs) +
+                               static_cast<size_t>(r) * static_cast<size_t>(probs_row_stride) * pbytes
+                         : nullptr;
+        st = drs_row_stats(logits + r * row_stride, n, vocab, row_stride, temps, canvas_len, seed,
+                           row0 + r, argmax + r, sample + r, entropy + r, probs_dtype, pr,
+                           probs_row_stride, ws, kNoallocWorkspaceBytes, stream);
+        if (st != DRS_OK) return st;
+    }
+    return DRS_OK;
 }
