@@ -3,18 +3,20 @@
 One step = one pass of the whole path over one batch: drs_row_stats_topk,
 the row statistics (argmax, Gumbel-max sample, entropy, bf16 softmax) of
 2048 x 262144 fp32 logits and the top-k logprobs (k = 20) of the rows of the
-converged (even) slots, from one read of the logits. Inputs are synthetic
-(workloads.py, "step") and resident in HBM when the timed region starts; at
-2.1 GB they are larger than L2, so no flush is needed between steps.
+converged (even) slots. Inputs are synthetic (workloads.py, "step") and
+resident in HBM when the timed region starts; at 2.1 GB they are larger than
+L2, so no flush is needed between steps.
 
-Prints ONE JSON line (rank 0). `value` is rows/s over all GPUs; `roofline`
-describes the row kernel (algorithmic bytes rows*stride*4 read + rows*V*2
-written per call over the call's CUDA-event time, which also covers the
-exact top-k kernel that follows it and exits at once when no row needs
-it); `kernels` adds the two separate calls (drs_row_stats, then
-drs_topk_logprobs) timed briefly; `e2e` repeats the step through the public
-API from pinned host buffers, copies included; `cpu_baseline` times the CPU
-oracle on a bounded sample of the same rows.
+Prints ONE JSON line (rank 0). `value` is rows/s over all GPUs. `roofline`
+describes the dominant kernel, pass 2 (probabilities, Gumbel race, top-k
+candidates): its algorithmic bytes (every logit read once, every probability
+written once: rows*V*4 + rows*V*2) over its average CUDA-event duration,
+the events recorded on the call's stream around each kernel by the
+library's measurement hook during the timed region. `kernels` gives every
+kernel of the call the same way and the whole call, plus the two separate
+calls (drs_row_stats, then drs_topk_logprobs) timed briefly; `e2e` repeats
+the step through the public API from pinned host buffers, copies included;
+`cpu_baseline` times the CPU oracle on a bounded sample of the same rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --rows 256 --no-e2e --cpu-seconds 0   (a smaller case of
@@ -247,21 +249,24 @@ def _run_ours(args, world, rank, local):
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         _barrier(world)
         torch.cuda.synchronize()
+        drs.drs_kernel_timing(True)
         with ClockSampler(torch.cuda.current_device()) as clk:
             start.record(stream)
             for i in range(args.steps):
                 step(evs[i])
             stop.record(stream)
             torch.cuda.synchronize()
+        drs.drs_kernel_timing(False)
         _barrier(world)
         total_ms = start.elapsed_time(stop)
         rs_ms = [e[0].elapsed_time(e[1]) for e in evs]
-        return total_ms, rs_ms, clk.summary()
+        return total_ms, rs_ms, clk.summary(), drs.drs_kernel_times()
 
-    total_ms, rs_ms, clocks = timed()
+    total_ms, rs_ms, clocks, ktimes = timed()
     if _clocks_rejected(clocks):
-        total_ms, rs_ms, clocks = timed()
+        total_ms, rs_ms, clocks, ktimes = timed()
         clocks["remeasured"] = True
+    kernel_ms, kernel_calls = ktimes
     if drs.drs_get_device_error() != 0:
         raise RuntimeError("device-side wait timed out during the timed region")
     total_ms = _max_over_ranks(total_ms, world)
@@ -270,16 +275,20 @@ def _run_ours(args, world, rank, local):
 
     rs_avg_ms = sum(rs_ms) / len(rs_ms)
     sep_rs_ms, tk_avg_ms = separate()
-    bytes_rs = rows * stride * 4 + rows * V * 2
+    bytes_rs = rows * V * 4 + rows * V * 2      # each logit read once, each probability written once
     kept_rows = int(keep[: rows // w["canvas_len"]].sum().item()) * w["canvas_len"]
     bytes_tk = kept_rows * V * 4
     peak, peak_kind = _peak_hbm()
     achieved = bytes_rs / (rs_avg_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(),
-                "kernel": "row_stats_kernel (drs_row_stats_topk call)",
+    p2_ms = kernel_ms["split_pass2"]
+    p1_ms = kernel_ms["split_pass1"]
+    achieved_p2 = bytes_rs / (p2_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved_p2, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved_p2 / peak, 4), "traffic": _traffic_from_profile(),
+                "kernel": "split_pass2 (probabilities, Gumbel race, top-k candidates)",
                 "peak_kind": f"{peak_kind} copy bandwidth",
-                "bytes_per_launch": bytes_rs, "avg_launch_ms": round(rs_avg_ms, 4)}
+                "bytes_per_launch": bytes_rs, "avg_launch_ms": round(p2_ms, 4),
+                "launches_averaged": kernel_calls}
 
     out = {"metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -294,7 +303,14 @@ def _run_ours(args, world, rank, local):
            "kernels": {"row_stats_topk": {"avg_ms": round(rs_avg_ms, 4),
                                           "rows_per_s": round(rows / (rs_avg_ms / 1e3), 1),
                                           "gbs": round(achieved, 1),
-                                          "frac_of_peak": round(achieved / peak, 4)},
+                                          "frac_of_peak": round(achieved / peak, 4),
+                                          "note": "the whole call over the algorithmic bytes of "
+                                                  "one read and one write"},
+                       "per_kernel_ms": {k_: round(v_, 4) for k_, v_ in kernel_ms.items()},
+                       "split_pass1": {"avg_ms": round(p1_ms, 4),
+                                       "gbs_read": round(rows * V * 4 / (p1_ms / 1e3) / 1e9, 1),
+                                       "frac_of_peak": round(rows * V * 4 / (p1_ms / 1e3) / 1e9
+                                                             / peak, 4)},
                        "row_stats_alone": {"avg_ms": round(sep_rs_ms, 4),
                                            "gbs": round(bytes_rs / (sep_rs_ms / 1e3) / 1e9, 1),
                                            "frac_of_peak": round(bytes_rs / (sep_rs_ms / 1e3)
@@ -303,7 +319,8 @@ def _run_ours(args, world, rank, local):
                                          "gbs_read": round(bytes_tk / (tk_avg_ms / 1e3) / 1e9, 1),
                                          "frac_of_peak": round(bytes_tk / (tk_avg_ms / 1e3) / 1e9
                                                                / peak, 4)}},
-           "gpu_launches": 2 * args.steps,  # the row kernel and the exact top-k kernel
+           # per step: list of rows, pass 1, merge, pass 2, finish, exact top-k
+           "gpu_launches": 6 * args.steps,
            "clocks": clocks}
 
     # end to end through the public API from pinned host memory
@@ -320,11 +337,11 @@ def _run_ours(args, world, rank, local):
 
 
 def kernel_source_hash():
-    """sha256 over the sources of the row-statistics kernel: a traffic figure
-    taken from an ncu capture is used only while they are unchanged."""
+    """sha256 over the sources of the row kernels: a traffic figure taken
+    from an ncu capture is used only while they are unchanged."""
     import hashlib
     h = hashlib.sha256()
-    for rel in ("vocab_row_sampling_gb300/csrc/row_stats.cu",
+    for rel in ("vocab_row_sampling_gb300/csrc/row_split.cu",
                 "vocab_row_sampling_gb300/csrc/drs_device.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
@@ -332,10 +349,10 @@ def kernel_source_hash():
 
 
 def _traffic_from_profile():
-    """DRAM bytes (read + write) per launch of the row-stats kernel from the
-    committed ncu capture of the step workload, if it was taken on the
-    current kernel sources (else null)."""
-    path = os.path.join(ROOT, "profiles", "row_stats_traffic.json")
+    """DRAM bytes (read + write) per launch of pass 2 on the step workload,
+    from the committed ncu capture, if it was taken on the current kernel
+    sources (else null)."""
+    path = os.path.join(ROOT, "profiles", "split_pass2_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)

@@ -4,7 +4,7 @@
  *
  * The operations follow the page "vllm.model_executor.models.
  * diffusion_gemma_sampler": the module docstring (argmax, Gumbel-max sample,
- * softmax entropy and the softmax in the model dtype, one read of each row),
+ * softmax entropy and the softmax in the model dtype, the noise drawn inline),
  * sample_row_stats and its PyTorch definition sample_row_stats_reference,
  * and stash_converged_logprobs / _lp_topk_kernel (top-k logprobs of the rows
  * of converged slots, keys ordered by value then by lower index).
@@ -52,11 +52,12 @@ typedef enum drs_probs_dtype {
 
 /*
  * Bytes of device workspace drs_row_stats needs (at least 256-byte aligned,
- * contents arbitrary: each call clears the part it uses with an
- * asynchronous memset on its stream before its kernel runs). The workspace
- * carries the per-row partial results that the CTAs sharing one row
- * exchange. One workspace must not be used by two calls that can run at the
- * same time.
+ * contents arbitrary: each call clears the counters it uses with an
+ * asynchronous memset on its stream before its kernels run). The workspace
+ * carries the row lists and the per-tile and per-row records through which
+ * the kernels of one call pass their partial results: about 2.6 KiB per row
+ * of 262144 columns, growing with rows and vocab. One workspace must not be
+ * used by two calls that can run at the same time.
  */
 size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab);
 
@@ -113,10 +114,11 @@ drs_status drs_row_stats(const float *logits, int64_t rows, int64_t vocab,
  * (it can synchronise the device, or the memory budget is fixed at
  * start-up). Arguments, results and errors are those of drs_row_stats.
  *
- * The exchange records live in a fixed device array inside the library
- * (drs_row_stats_workspace_bytes() bytes, 640 KiB; every GPU that loads
- * the library holds it until the process exits). Calls whose launch would
- * need more return DRS_ERR_UNSUPPORTED. The call allocates nothing. Its
+ * The kernels' records live in a fixed device array inside the library
+ * (640 KiB; every GPU that loads the library holds it until the process
+ * exits). A call whose rows need a larger workspace runs in batches of rows
+ * that fit, one after the other on the stream (about 240 rows of 262144
+ * columns per batch). The call allocates nothing. Its
  * first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
  * capture. All calls on a device share the array: two calls that can run
@@ -143,10 +145,10 @@ size_t drs_row_stats_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k
 
 /*
  * drs_row_stats and the top-k logprobs of the rows of converged slots in
- * one read of the logits (the module docstring's one read per row, and
- * stash_converged_logprobs / _lp_topk_kernel on the page above, whose
- * stash reads the kept rows again). Every argument of drs_row_stats has its
- * meaning there; in addition:
+ * the same passes over the logits (stash_converged_logprobs /
+ * _lp_topk_kernel on the page above, whose stash reads the kept rows again
+ * in a kernel of its own). Every argument of drs_row_stats has its meaning
+ * there; in addition:
  *
  *   keep        uint8 [ceil((row0 + rows) / canvas_len)], one per slot of
  *               the whole batch like temps: global row r is converged when
@@ -161,10 +163,12 @@ size_t drs_row_stats_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k
  *               of those columns (NaN for a row that is -inf everywhere).
  *   workspace   drs_row_stats_topk_workspace_bytes(rows, vocab, k) bytes.
  *
- * For k <= 64 one kernel reads each row once; rows whose top-k candidates
- * overflow its fixed buffers (many equal values) are finished by a second,
- * exact kernel on the same stream that reads only those rows. For k > 64
- * the row statistics and the exact top-k kernel run one after the other.
+ * For k <= 64 the top-k candidates come out of the row statistics' own two
+ * passes over the logits (the threshold from the first, the candidates in
+ * the second); rows whose candidates overflow the fixed lists (many equal
+ * values) or that have no threshold are finished by the exact top-k kernel
+ * on the same stream, which reads only those rows. For k > 64 the row
+ * statistics and the exact top-k kernel run one after the other.
  */
 drs_status drs_row_stats_topk(const float *logits, int64_t rows, int64_t vocab,
                               int64_t row_stride, const float *temps,
@@ -198,10 +202,9 @@ size_t drs_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k);
  *   out_logprobs fp32 [rows, k]: scaled - max - log(sum exp(scaled - max))
  *               of those columns (NaN for a row that is -inf everywhere).
  *
- * For k <= 64 this runs the kernel of drs_row_stats_topk with the row
- * statistics off (rows of unconverged slots are neither read nor
- * exchanged); larger k, and rows with many equal values, use the exact
- * top-k kernel.
+ * For k <= 64 this runs the kernels of drs_row_stats_topk with the row
+ * statistics off (rows of unconverged slots are not read); larger k, and
+ * rows with many equal values, use the exact top-k kernel.
  */
 drs_status drs_topk_logprobs(const float *logits, int64_t rows, int64_t vocab,
                              int64_t row_stride, const float *temps,
@@ -240,6 +243,26 @@ drs_status drs_scaled_logits(const float *logits, int64_t n, float temp,
  * clears it.
  */
 void drs_test_inject_fault(int code);
+
+/*
+ * Measurement hook (not part of the sampler). enable != 0: from now on every
+ * row-statistics call on the current device (drs_row_stats, its no-alloc and
+ * top-k variants, drs_topk_logprobs for k <= 64) records a CUDA event on
+ * its stream before each of its five kernels (list of rows, pass 1, merge,
+ * pass 2, finish) and after the last; the count of recorded calls restarts
+ * at 0. enable == 0 stops recording. The events of the last 64 calls are
+ * kept. Returns DRS_OK or DRS_ERR_CUDA (event creation failed).
+ */
+drs_status drs_kernel_timing(int enable);
+
+/*
+ * Average device time in ms of each kernel of the recorded calls (see
+ * drs_kernel_timing), in the order above, into the HOST array avg_ms[n]
+ * (entries past the fifth are 0); *calls (HOST) receives the number of
+ * calls averaged (at most 64). Waits for the recorded events. Returns
+ * DRS_OK, DRS_ERR_INVALID_ARG (null pointer, n < 0) or DRS_ERR_CUDA.
+ */
+drs_status drs_kernel_times(float *avg_ms, int32_t n, int32_t *calls);
 
 /* Static, human-readable name of a status code. */
 const char *drs_status_string(drs_status s);

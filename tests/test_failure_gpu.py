@@ -1,7 +1,8 @@
-"""Failure detection without a GPU fault: a CTA withholds one exchange
-record (host-side hook), the bounded waits on it run out after about a
-second, the kernel raises the device flag and returns; the host reads
-DRS_ERR_DEVICE_TIMEOUT and the context keeps working."""
+"""Failure detection without a GPU fault: a CTA of the first pass never
+fills its first shared-memory stage (host-side hook), its warps' bounded
+waits on the stage run out after about a second, the CTA raises the device
+flag and stops; the host reads DRS_ERR_DEVICE_TIMEOUT and the context keeps
+working."""
 import time
 
 import numpy as np

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads
-from gpu_util import gpu_row_stats, oracle_rows, sample_rows, subset
+from gpu_util import drs, gpu_row_stats, oracle_rows, sample_rows, subset
 from parity import check_row_stats
 
 pytestmark = pytest.mark.gpu
@@ -58,8 +58,8 @@ def test_shapes_and_strides(vocab, pad):
 
 
 def test_special_rows_on_a_shared_row():
-    """One-hot, constant, all -inf and ordinary rows at V = 131072 (8 CTAs
-    share a row) under every temperature regime."""
+    """One-hot, constant, all -inf and ordinary rows at V = 131072 (16
+    tiles of a row merged) under every temperature regime."""
     vocab = 131072
     rng = np.random.default_rng(5)
     rows = 16
@@ -107,12 +107,12 @@ def test_repeated_calls_are_deterministic():
             assert np.array_equal(one[k], again[k]), k
 
 
-@pytest.mark.parametrize("which", ["four stages", "max"])
+@pytest.mark.parametrize("which", ["400000", "max"])
 def test_long_rows(which):
-    """Rows too long for the two-iteration lag: 400000 columns take the
-    four-stage form, the largest supported vocabulary the three-stage one."""
+    """Rows of many tiles with a ragged last one: 400000 columns (49 tiles,
+    the last 6784 wide) and the largest supported vocabulary (60 tiles)."""
     import vocab_row_sampling_gb300 as drs
-    vocab = 400000 if which == "four stages" else drs.DRS_MAX_VOCAB
+    vocab = 400000 if which == "400000" else drs.DRS_MAX_VOCAB
     rng = np.random.default_rng(1)
     x = (rng.standard_normal((3, vocab)) * 3).astype(np.float32)
     x[2, vocab - 1] = 40.0
@@ -180,3 +180,21 @@ def test_large_workload_sampled_rows():
     zero_slots = np.flatnonzero(w.numpy() == 0)
     always = [int(s) * 256 + 3 for s in zero_slots[:3]]
     _full("large", 12, always=always)
+
+
+def test_kernel_timing_hook_counts_calls():
+    """The measurement hook: with timing on, each call records its five row
+    kernels; the averages are positive and the count is the number of calls;
+    with timing off, calls are not recorded."""
+    lib = drs()
+    w = workloads.make("tiny")
+    x, t = w["logits"].cuda(), w["temps"].cuda()
+    lib.drs_kernel_timing(True)
+    for _ in range(3):
+        lib.row_stats(x, t, 16, 0, torch.bfloat16)
+    lib.drs_kernel_timing(False)
+    lib.row_stats(x, t, 16, 0, torch.bfloat16)
+    times, calls = lib.drs_kernel_times()
+    assert calls == 3
+    assert set(times) == set(lib.KERNEL_NAMES)
+    assert all(v > 0.0 for v in times.values()), times

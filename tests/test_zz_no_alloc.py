@@ -1,7 +1,8 @@
 """drs_row_stats_noalloc: the row statistics for callers that cannot
 allocate device memory for the library (plugin interfaces that receive only
 input and output buffers, or code that must not call cudaMalloc). It keeps
-its exchange records in a fixed device array of the library.
+its kernels' records in a fixed device array of the library, and runs calls
+whose rows need more in batches of rows.
 
 The test calls it through the C ABI twice in a row (the second call reuses
 the array the first one left behind) and compares every output with
@@ -32,11 +33,17 @@ def _cases():
     w = workloads.make("tiny")
     yield "tiny", w["logits"].cuda(), w["temps"].cuda(), w["canvas_len"]
     rng = np.random.default_rng(3)
-    x = (rng.standard_normal((40, 131072)) * 3).astype(np.float32)   # 8+ CTAs per row
+    x = (rng.standard_normal((40, 131072)) * 3).astype(np.float32)   # 16 tiles per row
     x[5] = -np.inf
     x[5, 70000] = 1.0
     t = torch.tensor([0.0, 0.8, 1.0, 1e-3, 1.4], dtype=torch.float32, device="cuda")
     yield "shared rows", torch.as_tensor(x).cuda(), t, 8
+    # more rows than one batch of the fixed array holds (about 240 rows of
+    # 262144 columns): the call runs in batches, row0 and the outputs offset
+    g = torch.Generator(device="cuda").manual_seed(4)
+    xb = 3.0 * torch.randn(300, 262144, generator=g, device="cuda")
+    tb = torch.tensor([0.9, 0.0, 1.2], dtype=torch.float32, device="cuda")
+    yield "batched rows", xb, tb, 100
 
 
 @pytest.mark.parametrize("with_probs", [True, False])

@@ -34,7 +34,8 @@ DRS_MAX_VOCAB = 491520
 EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_row_stats_noalloc",
             "drs_row_stats_topk", "drs_row_stats_topk_workspace_bytes", "drs_topk_logprobs",
             "drs_topk_workspace_bytes", "drs_philox_gumbel", "drs_scaled_logits",
-            "drs_status_string", "drs_get_device_error", "drs_test_inject_fault")
+            "drs_status_string", "drs_get_device_error", "drs_test_inject_fault",
+            "drs_kernel_timing", "drs_kernel_times")
 
 
 class DrsError(RuntimeError):
@@ -91,6 +92,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_test_inject_fault.restype = None
     lib.drs_get_device_error.argtypes = [vp]
     lib.drs_get_device_error.restype = ctypes.c_int
+    lib.drs_kernel_timing.argtypes = [ctypes.c_int]
+    lib.drs_kernel_timing.restype = ctypes.c_int
+    lib.drs_kernel_times.argtypes = [vp, i32, vp]
+    lib.drs_kernel_times.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -203,9 +208,29 @@ def drs_scaled_logits(logits, temp: float, out, stream=None):
     _check(st, "drs_scaled_logits")
 
 
+KERNEL_NAMES = ("split_prep", "split_pass1", "split_merge", "split_pass2", "split_finish")
+
+
+def drs_kernel_timing(enable: bool) -> None:
+    """Measurement hook: record CUDA events around the row kernels of every
+    following call on the current device (see include/drs.h)."""
+    _check(load().drs_kernel_timing(1 if enable else 0), "drs_kernel_timing")
+
+
+def drs_kernel_times():
+    """Average ms of each row kernel over the calls recorded since timing was
+    switched on: ({kernel name: ms}, number of calls averaged)."""
+    out = (ctypes.c_float * len(KERNEL_NAMES))()
+    calls = ctypes.c_int32(0)
+    _check(load().drs_kernel_times(ctypes.cast(out, ctypes.c_void_p), len(KERNEL_NAMES),
+                                   ctypes.cast(ctypes.pointer(calls), ctypes.c_void_p)),
+           "drs_kernel_times")
+    return dict(zip(KERNEL_NAMES, (float(v) for v in out))), int(calls.value)
+
+
 def drs_test_inject_fault(code: int) -> None:
-    """Test hook: the next drs_row_stats launch withholds one exchange record
-    so that the bounded waits on it run out (see include/drs.h)."""
+    """Test hook: in the next row-statistics call a CTA never fills its first
+    stage, so that the bounded waits on it run out (see include/drs.h)."""
     load().drs_test_inject_fault(code)
 
 

@@ -53,7 +53,79 @@ int sm_count() {
     return g_sms[dev];
 }
 
+// ------------------------------------------------------- kernel timing
+
+namespace {
+// Events around the kernels of the last kTimedCalls row-statistics calls
+// (ring), on the device that was current when timing was switched on.
+struct KernelTimer {
+    bool on = false;
+    int device = -1;
+    int calls = 0;
+    cudaEvent_t ev[kTimedCalls][kTimedKernels + 1] = {};
+};
+KernelTimer g_timer;
+std::mutex g_timer_mutex;
+}  // namespace
+
+int kernel_timer_slot() {
+    std::lock_guard<std::mutex> lock(g_timer_mutex);
+    if (!g_timer.on || current_device() != g_timer.device) return -1;
+    return g_timer.calls++ % kTimedCalls;
+}
+
+cudaEvent_t kernel_timer_event(int slot, int i) { return g_timer.ev[slot][i]; }
+
 }  // namespace drs
+
+extern "C" drs_status drs_kernel_timing(int enable) {
+    using namespace drs;
+    std::lock_guard<std::mutex> lock(g_timer_mutex);
+    if (!enable) {
+        g_timer.on = false;
+        return DRS_OK;
+    }
+    const int dev = current_device();
+    if (dev < 0) return DRS_ERR_CUDA;
+    if (g_timer.device != dev) {
+        if (g_timer.device >= 0) {
+            int prev = 0;
+            if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(g_timer.device) != cudaSuccess)
+                return DRS_ERR_CUDA;
+            for (auto& call : g_timer.ev)
+                for (cudaEvent_t& e : call)
+                    if (e) cudaEventDestroy(e), e = nullptr;
+            if (cudaSetDevice(prev) != cudaSuccess) return DRS_ERR_CUDA;
+        }
+        for (auto& call : g_timer.ev)
+            for (cudaEvent_t& e : call)
+                if (cudaEventCreate(&e) != cudaSuccess) return DRS_ERR_CUDA;
+        g_timer.device = dev;
+    }
+    g_timer.calls = 0;
+    g_timer.on = true;
+    return DRS_OK;
+}
+
+extern "C" drs_status drs_kernel_times(float* avg_ms, int32_t n, int32_t* calls) {
+    using namespace drs;
+    if (!avg_ms || n < 0 || !calls) return DRS_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_timer_mutex);
+    const int m = g_timer.calls < kTimedCalls ? g_timer.calls : kTimedCalls;
+    *calls = m;
+    for (int i = 0; i < n; ++i) avg_ms[i] = 0.0f;
+    if (m == 0) return DRS_OK;
+    for (int c = 0; c < m; ++c) {
+        if (cudaEventSynchronize(g_timer.ev[c][kTimedKernels]) != cudaSuccess) return DRS_ERR_CUDA;
+        for (int i = 0; i < n && i < kTimedKernels; ++i) {
+            float ms = 0.0f;
+            if (cudaEventElapsedTime(&ms, g_timer.ev[c][i], g_timer.ev[c][i + 1]) != cudaSuccess)
+                return DRS_ERR_CUDA;
+            avg_ms[i] += ms / static_cast<float>(m);
+        }
+    }
+    return DRS_OK;
+}
 
 extern "C" const char* drs_status_string(drs_status s) {
     switch (s) {

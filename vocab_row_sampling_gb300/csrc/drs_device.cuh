@@ -1,8 +1,8 @@
 // drs_device.cuh -- device building blocks shared by the libdrs kernels:
-// the Philox4x32-10 noise generator, bounded mbarrier waits, the bulk-copy
-// (TMA) loads that stage a row chunk in shared memory, warp/CTA reductions
-// and the record through which the CTAs that share one row exchange their
-// partial results.
+// the Philox4x32-10 noise generator and the Gumbel noise of a word, bounded
+// mbarrier waits, the bulk-copy (TMA) loads that stage data in shared
+// memory, warp reductions, the exact temperature quotient, and the team
+// plan of the exact top-k kernel (CTAs that share one row).
 #pragma once
 
 #include <climits>
@@ -11,10 +11,8 @@
 
 namespace drs {
 
-constexpr int kThreads = 512;               // threads per CTA (16 warps)
+constexpr int kThreads = 512;               // threads per CTA of the exact top-k kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxVec4 = 8;                 // float4 slots per thread, at most
-constexpr int kChunkCap = kThreads * kMaxVec4 * 4;  // floats per CTA chunk, at most
 constexpr size_t kSmemPerSm = 233472;       // shared memory of one SM (228 KB)
 constexpr size_t kSmemPerCta = 232448;      // largest opt-in per CTA (227 KB)
 constexpr size_t kSmemReserved = 1024;      // the driver's share of each CTA
@@ -85,26 +83,6 @@ struct PhiloxRoundKeys {
     }
 };
 
-__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const PhiloxRoundKeys& rk) {
-    constexpr uint32_t kMulA = 0xD2511F53u, kMulB = 0xCD9E8D57u;
-#pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        const uint32_t hi_a = __umulhi(kMulA, c.x);
-        const uint32_t lo_a = kMulA * c.x;
-        const uint32_t hi_b = __umulhi(kMulB, c.z);
-        const uint32_t lo_b = kMulB * c.z;
-        c = make_uint4(hi_b ^ c.y ^ rk.k0[round], lo_b, hi_a ^ c.w ^ rk.k1[round], lo_a);
-    }
-    return c;
-}
-
-// Noise words of columns 4*group .. 4*group+3 of `row` (group < 2^32).
-__device__ __forceinline__ uint4 noise_words_rk(const PhiloxRoundKeys& rk, uint64_t row,
-                                                uint32_t group) {
-    return philox4x32_10_rk(
-        make_uint4(group, 0u, static_cast<uint32_t>(row), static_cast<uint32_t>(row >> 32)), rk);
-}
-
 // The four noise words of columns 4*group .. 4*group+3 of `row`.
 __device__ __forceinline__ uint4 noise_words(PhiloxKey key, uint64_t row,
                                              uint64_t group) {
@@ -145,10 +123,6 @@ __device__ __forceinline__ float one_minus_u_lower(uint32_t bits) {
     return 0x1.fffffep0f - __uint_as_float(0x3F800000u | (bits >> 9));
 }
 
-// Largest value gumbel_of_bits can return (u = 1 - 2^-24 gives 16.6355...),
-// rounded up with margin: no element whose scaled logit is below
-// best - kGumbelMax can win the Gumbel-max race against `best`.
-constexpr float kGumbelMax = 16.64f;
 
 // ------------------------------------------------------------- mbarrier
 
@@ -240,18 +214,6 @@ __device__ __forceinline__ float warp_max(float v) {
     return r;
 }
 
-__device__ __forceinline__ int warp_min_i(int v) {
-    int r;
-    asm volatile("redux.sync.min.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
-    return r;
-}
-
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 // Best (score, column): larger score wins, equal scores go to the lower
 // column. Columns of "no candidate" are INT32_MAX with score -inf.
 __device__ __forceinline__ bool beats(float s, int c, float bs, int bc) {
@@ -279,91 +241,6 @@ __device__ __forceinline__ void warp_best(float& s, int& c) {
     const float top = warp_max_f(s);
     c = warp_min_nonneg(s == top ? c : INT_MAX);
     s = top;
-}
-
-// ------------------------------------------------------ row exchange
-
-// The records through which the CTAs of a team exchange per-row results.
-// Each 8-byte word holds a 32-bit payload (high half) and a 32-bit tag (low
-// half): the row's sequence number + 1 within the team. 8-byte accesses are
-// single-copy atomic, so a reader that loads all words of a record (relaxed,
-// in one round trip) and finds every tag equal to the row's has the row's
-// values, whatever order the words were written or read in; no fence is
-// needed on either side. The rings are zeroed before each launch, so a tag
-// never matches a record of an earlier launch.
-struct alignas(64) RecordA {  // m, S, W, argmax, best score, best column
-    uint64_t w[8];
-};
-struct alignas(16) RecordB {  // best score, best column
-    uint64_t w[2];
-};
-// Per-CTA exchange area: kRing A slots then kRing B slots.
-constexpr size_t kXchgPerCta = kRing * (sizeof(RecordA) + sizeof(RecordB));
-
-__device__ __forceinline__ RecordA* record_a(void* xchg, int cta, int slot) {
-    return reinterpret_cast<RecordA*>(static_cast<unsigned char*>(xchg) + cta * kXchgPerCta) + slot;
-}
-__device__ __forceinline__ RecordB* record_b(void* xchg, int cta, int slot) {
-    return reinterpret_cast<RecordB*>(static_cast<unsigned char*>(xchg) + cta * kXchgPerCta +
-                                      kRing * sizeof(RecordA)) + slot;
-}
-
-__device__ __forceinline__ uint64_t tagged(uint32_t payload, uint32_t tag) {
-    return (static_cast<uint64_t>(payload) << 32) | tag;
-}
-__device__ __forceinline__ uint64_t tagged(float payload, uint32_t tag) {
-    return tagged(__float_as_uint(payload), tag);
-}
-__device__ __forceinline__ uint32_t payload_u(uint64_t w) { return static_cast<uint32_t>(w >> 32); }
-__device__ __forceinline__ float payload_f(uint64_t w) { return __uint_as_float(payload_u(w)); }
-
-__device__ __forceinline__ void st_relaxed_v2(uint64_t* p, uint64_t a, uint64_t b) {
-    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b)
-                 : "memory");
-}
-__device__ __forceinline__ void ld_relaxed_v2(const uint64_t* p, uint64_t& a, uint64_t& b) {
-    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p)
-                 : "memory");
-}
-
-__device__ __forceinline__ void publish_a(RecordA* r, uint32_t tag, float m, float s, float w,
-                                          int arg, float best, int best_col) {
-    st_relaxed_v2(r->w + 0, tagged(m, tag), tagged(s, tag));
-    st_relaxed_v2(r->w + 2, tagged(w, tag), tagged(static_cast<uint32_t>(arg), tag));
-    st_relaxed_v2(r->w + 4, tagged(best, tag), tagged(static_cast<uint32_t>(best_col), tag));
-}
-
-__device__ __forceinline__ void publish_b(RecordB* r, uint32_t tag, float best, int best_col) {
-    st_relaxed_v2(r->w, tagged(best, tag), tagged(static_cast<uint32_t>(best_col), tag));
-}
-
-__device__ __forceinline__ bool tags_are(const uint64_t* w, int n, uint32_t tag) {
-    bool ok = true;
-    for (int i = 0; i < n; ++i) ok &= static_cast<uint32_t>(w[i]) == tag;
-    return ok;
-}
-
-// Read an A record and/or a B record (either may be null) whose tags must be
-// tag_a / tag_b, polling until they are; both are in flight together.
-// Returns false after kWaitLimitNs.
-__device__ __forceinline__ bool read_records(const RecordA* ra, uint32_t tag_a, uint64_t (&a)[6],
-                                             const RecordB* rb, uint32_t tag_b, uint64_t (&b)[2]) {
-    bool ok_a = ra == nullptr, ok_b = rb == nullptr;
-    uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        if (!ok_a) {
-            ld_relaxed_v2(ra->w + 0, a[0], a[1]);
-            ld_relaxed_v2(ra->w + 2, a[2], a[3]);
-            ld_relaxed_v2(ra->w + 4, a[4], a[5]);
-        }
-        if (!ok_b) ld_relaxed_v2(rb->w, b[0], b[1]);
-        if (!ok_a) ok_a = tags_are(a, 6, tag_a);
-        if (!ok_b) ok_b = tags_are(b, 2, tag_b);
-        if (ok_a && ok_b) return true;
-        if (it == 0) t0 = global_timer_ns();
-        else if ((it & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) return false;
-        __nanosleep(32);
-    }
 }
 
 __device__ __forceinline__ void raise_device_error(int* flag, int code) {
@@ -426,10 +303,6 @@ __device__ __forceinline__ float comp(const float4& v, int q) {
     return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-__device__ __forceinline__ float max4(const float4& v) {
-    return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-}
-
 // 2^x on the special-function unit (non-flushing: subnormal results kept).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
@@ -441,22 +314,6 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
-}
-
-// Element b (= 4 * slot + component) of a thread's registers, by selects
-// (an indexed access would move the array to local memory).
-template <int VEC4>
-__device__ __forceinline__ float pick(const float4 (&v)[VEC4], int b) {
-    const int q = b & 3;
-    const int i = b >> 2;
-    float r = 0.0f;
-#pragma unroll
-    for (int j = 0; j < VEC4; ++j) {
-        const float4 g = v[j];
-        const float c = q == 0 ? g.x : q == 1 ? g.y : q == 2 ? g.z : g.w;
-        r = i == j ? c : r;
-    }
-    return r;
 }
 
 // ------------------------------------------------ the temperature quotient
@@ -535,31 +392,5 @@ struct ScaledQuotient {
         return fast_ok(x, q) ? q : __fdiv_rn(x, t);
     }
 };
-
-// ------------------------------------------------------- the exact race
-
-// Score the elements of `mask` exactly (s + g, g from the element's Philox
-// word) and keep the best (score, column) in (bs, bc). One rolled loop: the
-// element is selected from registers, its noise block recomputed.
-template <int VEC4>
-__device__ __forceinline__ void race_exact(const float4 (&v)[VEC4], uint32_t mask, int col0,
-                                           int tid, int64_t grow_id, PhiloxKey key, float& bs,
-                                           int& bc) {
-#pragma unroll 1
-    while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const int f = (b >> 2) * kThreads + tid;
-        const float x = pick(v, b);
-        const uint4 w = noise_words(key, static_cast<uint64_t>(grow_id),
-                                    static_cast<uint64_t>((col0 >> 2) + f));
-        const float score = x + gumbel_of_bits(word_of(w, b & 3));
-        const int c = col0 + 4 * f + (b & 3);
-        if (beats(score, c, bs, bc)) {
-            bs = score;
-            bc = c;
-        }
-    }
-}
 
 }  // namespace drs

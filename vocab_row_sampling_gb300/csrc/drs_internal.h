@@ -71,6 +71,14 @@ struct RowCall {
 // cleared by reading it.
 int take_injected_fault();
 
+// Kernel timing (drs_kernel_timing): the ring slot of the calling row
+// statistics call, or -1 when timing is off; the event to record before its
+// kernel i (after the last kernel: i = kTimedKernels).
+constexpr int kTimedKernels = 5;  // prep, pass 1, merge, pass 2, finish
+constexpr int kTimedCalls = 64;
+int kernel_timer_slot();
+cudaEvent_t kernel_timer_event(int slot, int i);
+
 // The two-pass row kernels (row_split.cu). The workspace starts with the
 // hard-row list (count at [0], rows from [64]): rows whose top-k the exact
 // kernel must finish. k is at most split_max_k().

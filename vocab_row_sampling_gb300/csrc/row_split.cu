@@ -67,11 +67,17 @@ namespace {
 
 constexpr int kSThreads = 256;
 constexpr int kSWarps = kSThreads / 32;
-constexpr int kSVec4 = 8;
+#ifndef DRS_SPLIT_VEC4
+#define DRS_SPLIT_VEC4 8
+#endif
+#ifndef DRS_SPLIT_STAGES
+#define DRS_SPLIT_STAGES 3
+#endif
+constexpr int kSVec4 = DRS_SPLIT_VEC4;             // float4 slots per thread
 constexpr int kTileCols = kSThreads * kSVec4 * 4;  // 8192
 constexpr int kMaxTiles = (DRS_MAX_VOCAB + kTileCols - 1) / kTileCols;
 constexpr int kOrdPerLane = (kMaxTiles * kSWarps + 31) / 32;
-constexpr int kStages = 3;                         // tiles in flight per CTA
+constexpr int kStages = DRS_SPLIT_STAGES;          // tiles in flight per CTA
 constexpr int kStageF4 = kTileCols / 4;             // float4 per stage
 constexpr size_t kStageBytes = kTileCols * 4;       // 32 KiB
 constexpr int kMap = 64;                            // tile -> row map, a ring
@@ -95,19 +101,18 @@ struct alignas(16) RowTemp {
     int qmode;
 };
 
-// Pass-1 record of a tile (64 bytes).
+// Pass-1 record of a tile (96 bytes).
 struct alignas(16) TileStats {
     float m;      // max exact quotient (-inf: none)
     float s;      // sum e^(s - m)
     float w;      // sum e^(s - m) (s - m)
-    int arg;      // lowest column of the max (the tile's first column if none)
-    float b;      // best Gumbel-max score of the warps' argmax elements
-    int bcol;
+    int arg;      // lowest column holding the raw max (the tile's first column if none)
     float xmax;   // raw max
-    int pad;
+    int pad[3];
     uint32_t wmax[kSWarps];  // order keys of the warps' raw maxima, 0: no columns
+    int wcol[kSWarps];       // lowest column holding each warp's raw max (INT_MAX: none)
 };
-static_assert(sizeof(TileStats) == 64, "tile record");
+static_assert(sizeof(TileStats) == 96, "tile record");
 
 enum : int { kFNoisy = 1, kFTopk = 2, kFRaw = 4 };
 
@@ -122,20 +127,22 @@ struct alignas(64) RowRecord {
     float thr;    // top-k threshold (raw logit)
     float lns;    // log S
     int bcol;
-    int arg;
+    int arg;      // lowest column holding the raw row max
     int flags;
     float qt, qy;
     int qmode;
-    int pad[2];
+    float cthr;   // a logit whose exact quotient equals M is at least this
+    int pad;
 };
 static_assert(sizeof(RowRecord) == 64, "row record");
 
-// Pass-2 record of a tile: race winner and candidate count (16 bytes).
+// Pass-2 record of a tile: race winner, candidate count, and the lowest
+// column below the raw max whose exact quotient is M (16 bytes).
 struct alignas(16) TileEnd {
     float b;
     int col;
     int nk;
-    int pad;
+    int acol;
 };
 
 struct SplitParams {
@@ -493,30 +500,25 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass1(const __grid_constan
                 mt = fmaxf(mt, m4[i]);
             }
             const float mxw = warp_max_f(mt);
-            const float mw = mxw == -INFINITY ? -INFINITY : sq.exact(mxw);  // M_w
-            const bool raw = !(fabsf(mw) >= kRawLimit);
+            // the warp works on the raw logits while |M_w| < 256 for sure:
+            // |mxw * RN(1/Te)| < 255 bounds the exact quotient M_w (computed
+            // once per tile for all warps by the warp that finishes it)
+            const bool raw = fabsf(mxw * sq.y) < kRawLimit - 1.0f;
 
-            // argmax: the lowest column whose exact quotient is M_w; exact(x)
-            // == M_w needs x >= mxw - Te * ulp(M_w). The few candidates are
-            // read again from the stage.
-            const float cthr = mxw - fmaxf(fabsf(mxw) * 0x1p-20f, sq.t * 0x1p-140f);
+            // the lowest column holding mxw (its exact quotient is M_w): the
+            // warp's Gumbel-max candidate, and the argmax unless a lower
+            // logit has the same exact quotient (pass 2 looks for those).
+            // The lane's first slot reaching mxw is read again from the stage.
             int arg_t = INT_MAX;
-            if (stats && mt >= cthr && mw != -INFINITY) {
-                uint32_t smask = 0;
+            if (stats && mt == mxw && mxw != -INFINITY) {
+                int i0 = 0;
 #pragma unroll
-                for (int i = 0; i < kSVec4; ++i) smask |= (m4[i] >= cthr ? 1u : 0u) << i;
-#pragma unroll 1
-                while (smask && arg_t == INT_MAX) {
-                    const int f = (__ffs(smask) - 1) * kSThreads + tid;
-                    smask &= smask - 1;
-                    const float4 x4 = stage[f];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float x = comp(x4, q);
-                        if (arg_t == INT_MAX && x >= cthr && 4 * f + q < ncols && sq.exact(x) == mw)
-                            arg_t = col0 + 4 * f + q;
-                    }
-                }
+                for (int i = kSVec4 - 1; i >= 0; --i)
+                    if (m4[i] == mxw) i0 = i;
+                const int f = i0 * kSThreads + tid;
+                const float4 x4 = stage[f];
+                const int q = x4.x == mxw ? 0 : x4.y == mxw ? 1 : x4.z == mxw ? 2 : 3;
+                arg_t = col0 + 4 * f + q;
             }
             const int aw = stats ? warp_min_nonneg(arg_t) : INT_MAX;
 
@@ -529,6 +531,7 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass1(const __grid_constan
                 lscale = kLog2e * sq.y;
                 cref = mxw * lscale;
             } else {
+                const float mw = sq.exact(mxw);
 #pragma unroll
                 for (int i = 0; i < kSVec4; ++i) {
                     v[i].x = sq.exact(v[i].x) - mw;
@@ -539,8 +542,8 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass1(const __grid_constan
                 lscale = kLog2e;
                 cref = 0.0f;
             }
-            float sw, ww;
-            for (int pass = 0;; ++pass) {
+            float sw = 0.0f, ww = 0.0f;  // a warp of -inf only: nothing to sum
+            for (int pass = 0; mxw != -INFINITY; ++pass) {
                 const float clamp = pass ? -FLT_MAX : -INFINITY;
                 float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wa[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -558,16 +561,16 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass1(const __grid_constan
                 ww = warp_sum_f((wa[0] + wa[1]) + (wa[2] + wa[3])) * kLn2;
                 if (pass || !isnan(ww)) break;
             }
-            if (lane == 0) parts[par][st][warp] = WarpPart{mw, sw, ww, mxw, aw};
+            if (lane == 0) parts[par][st][warp] = WarpPart{0.0f, sw, ww, mxw, aw};
         }
         if (!release_stage(&pp.count[st], lane)) continue;
 
         // the last warp out: refill the stage, then the tile's record (the
         // warps combined, one lane each)
-        const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
         pipe_advance(p, pp, n, p.list1, tiles, stage, &rts[st], p.rt, sizeof(RowTemp), tma, lane);
         const bool hv = lane < kSWarps;
-        const WarpPart wp = hv ? parts[par][st][lane] : WarpPart{-INFINITY, 0.0f, 0.0f, -INFINITY, INT_MAX};
+        WarpPart wp = hv ? parts[par][st][lane] : WarpPart{-INFINITY, 0.0f, 0.0f, -INFINITY, INT_MAX};
+        wp.m = wp.xmax == -INFINITY ? -INFINITY : sq.exact(wp.xmax);  // M_w of each warp
         const float mc = warp_max_f(wp.m);
         float s_l = 0.0f, w_l = 0.0f;
         if (wp.m != -INFINITY) {
@@ -578,26 +581,18 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass1(const __grid_constan
         }
         const float s_c = warp_sum_f(s_l);
         const float w_c = warp_sum_f(w_l);
-        const int a_c = mc == -INFINITY ? col0 : warp_min_nonneg(wp.m == mc ? wp.arg : INT_MAX);
-        // Gumbel-max scores of the warps' argmax elements
-        float b_c = -INFINITY;
-        int bcol_c = INT_MAX;
-        if (stats && temp > 0.0f && wp.arg != INT_MAX) {
-            const uint4 nw = noise_group(p.rk, grow, static_cast<uint32_t>(wp.arg >> 2));
-            b_c = wp.m + gumbel_of_bits(word_of(nw, wp.arg & 3));
-            bcol_c = wp.arg;
-        }
-        warp_best(b_c, bcol_c);
         const float xm = warp_max_f(wp.xmax);
+        const int a_c = xm == -INFINITY ? col0 : warp_min_nonneg(wp.xmax == xm ? wp.arg : INT_MAX);
         TileStats* dst = p.ts + t;
-        if (hv) dst->wmax[lane] = lane * 128 < ncols ? ord32(wp.xmax) : 0u;
+        if (hv) {
+            dst->wmax[lane] = lane * 128 < ncols ? ord32(wp.xmax) : 0u;
+            dst->wcol[lane] = wp.arg;
+        }
         if (lane == 0) {
             dst->m = mc;
             dst->s = s_c;
             dst->w = w_c;
             dst->arg = a_c;
-            dst->b = b_c;
-            dst->bcol = bcol_c;
             dst->xmax = xm;
         }
     }
@@ -621,30 +616,41 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
     const TileStats* tr = p.ts + li * G;
     float m = -INFINITY, s = 0.0f, w = 0.0f, xm = -INFINITY, b = -INFINITY;
     int arg = INT_MAX, bc = INT_MAX;
+    // B: the best Gumbel-max score of the warps' candidates (the lowest
+    // column holding each warp's raw max, whose exact quotient is M_w)
+    if (p.stats && temp > 0.0f) {
+        const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
+        const ScaledQuotient sq{rt.qt, rt.qy, rt.qmode};
+        for (int jx = lane; jx < kSWarps * G; jx += 32) {
+            const int col = tr[jx / kSWarps].wcol[jx % kSWarps];
+            if (col == INT_MAX) continue;
+            const float mw = sq.exact(unord32(tr[jx / kSWarps].wmax[jx % kSWarps]));
+            const uint4 nw = noise_group(p.rk, grow, static_cast<uint32_t>(col >> 2));
+            const float sc = mw + gumbel_of_bits(word_of(nw, col & 3));
+            if (beats(sc, col, b, bc)) {
+                b = sc;
+                bc = col;
+            }
+        }
+    }
     for (int c = lane; c < G; c += 32) {
         const TileStats r = tr[c];
+        // the lowest column holding the raw max (-inf rows: the first)
+        arg = r.xmax > xm ? r.arg : (r.xmax == xm ? min(arg, r.arg) : arg);
         xm = fmaxf(xm, r.xmax);
         if (r.m != -INFINITY) {
             if (m == -INFINITY) {
                 m = r.m;
                 s = r.s;
                 w = r.w;
-                arg = r.arg;
             } else {
                 const float nm = fmaxf(m, r.m);
                 const float d1 = m - nm, d2 = r.m - nm;
                 const float f1 = ex2_approx(d1 * kLog2e), f2 = ex2_approx(d2 * kLog2e);
                 w = f1 * fmaf(d1, s, w) + f2 * fmaf(d2, r.s, r.w);
                 s = f1 * s + f2 * r.s;
-                arg = r.m > m ? r.arg : (r.m == m ? min(arg, r.arg) : arg);
                 m = nm;
             }
-        } else if (m == -INFINITY) {
-            arg = min(arg, r.arg);
-        }
-        if (beats(r.b, r.bcol, b, bc)) {
-            b = r.b;
-            bc = r.bcol;
         }
     }
     const float big_m = warp_max_f(m);
@@ -657,9 +663,9 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
     }
     const float s_tot = warp_sum_f(s_l);
     const float w_tot = warp_sum_f(w_l);
-    const int arg_row = warp_min_nonneg(m == big_m ? arg : INT_MAX);
     warp_best(b, bc);
     const float mraw = warp_max_f(xm);
+    const int arg_row = warp_min_nonneg(xm == mraw ? arg : INT_MAX);
 
     const bool topk = p.k > 0 && kept;
     float thr = -INFINITY;
@@ -718,23 +724,21 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
         rec.cB = (c0 + (b - big_m) * kLog2e) - kRaceSlack;
         rec.thr = thr;
         rec.arg = arg_row;
+        rec.cthr = mraw - fmaxf(fabsf(mraw) * 0x1p-20f, rt.qt * 0x1p-140f);
         rec.qt = rt.qt;
         rec.qy = rt.qy;
         rec.qmode = rt.qmode;
         const bool noisy = p.stats && temp > 0.0f && big_m != -INFINITY;
         rec.flags = (noisy ? kFNoisy : 0) | (topk && !hard ? kFTopk : 0) | (raw ? kFRaw : 0);
         p.rr[row] = rec;
-        if (p.stats) {
-            p.argmax[row] = arg_row;
-            p.entropy[row] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
-            if (!noisy) p.sample[row] = arg_row;
-        }
+        if (p.stats) p.entropy[row] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
         if (hard) {
             const int idx = atomicAdd(p.hard, 1);
             p.hard[kHardOffset + idx] = static_cast<int32_t>(row);
         }
-        // the rows that want probabilities, the race or candidates
-        if ((p.stats && p.probs_dtype != 0) || (rec.flags & (kFNoisy | kFTopk))) {
+        // the rows that pass 2 reads: every row of a statistics call (the
+        // argmax is settled there), and rows that want candidates
+        if (p.stats || (rec.flags & kFTopk)) {
             const int idx = atomicAdd(p.hard + kCount2, 1);
             p.list2[idx] = static_cast<int32_t>(row);
         }
@@ -834,11 +838,13 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constan
     __shared__ uint16_t race_at[kSWarps][kSVec4 * 32];
     __shared__ float best_s[2][kStages][kSWarps];
     __shared__ int best_c[2][kStages][kSWarps];
+    __shared__ int best_a[2][kStages][kSWarps];
     __shared__ int tile_nk[2][kStages];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const bool probs = p.stats != 0 && p.probs_dtype != 0;
+    const bool stats = p.stats != 0;
+    const bool probs = stats && p.probs_dtype != 0;
     const bool tma = p.vec != 0;
     const int G = p.tiles_per_row;
     const int64_t tiles = static_cast<int64_t>(p.hard[kCount2]) * G;
@@ -879,6 +885,36 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constan
                 else probs_of_tile<false>(v, rec, sq, prow, p.probs_vec != 0, ncols, tid);
             }
 
+            float m4[kSVec4];
+#pragma unroll
+            for (int i = 0; i < kSVec4; ++i) m4[i] = max4f(v[i]);
+
+            // argmax: logits below the raw max whose exact quotient is M
+            // (rare: the float4s reaching the bound are read again from the
+            // stage); the lowest column of the thread, then of the warp
+            int acand = INT_MAX;
+            if (stats && rec.M != -INFINITY) {
+                const float cthr = rec.cthr;
+                uint32_t am = 0;
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i) am |= (m4[i] >= cthr ? 1u : 0u) << i;
+#pragma unroll 1
+                while (am && acand == INT_MAX) {
+                    const int f = (__ffs(am) - 1) * kSThreads + tid;
+                    am &= am - 1;
+                    const float4 x4 = stage[f];
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        const float x = comp(x4, q);
+                        if (4 * f + q < ncols && x >= cthr && sq.exact(x) == rec.M) {
+                            acand = col0 + 4 * f + q;
+                            break;
+                        }
+                    }
+                }
+                acand = warp_min_nonneg(acand);
+            }
+
             float wb = rec.B;
             int wc = rec.bcol;
             if (noisy) {
@@ -889,11 +925,11 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constan
                     const float ls = rec.ls, cB = rec.cB;
 #pragma unroll
                     for (int i = 0; i < kSVec4; ++i)
-                        if (fmaf(max4f(v[i]), ls, -cB) >= -24.0f) pass |= 1u << i;
+                        if (fmaf(m4[i], ls, -cB) >= -24.0f) pass |= 1u << i;
                 } else {
 #pragma unroll
                     for (int i = 0; i < kSVec4; ++i)
-                        if (fmaf(sq.exact(max4f(v[i])) - rec.B, kLog2e, kRaceSlack) >= -24.0f) pass |= 1u << i;
+                        if (fmaf(sq.exact(m4[i]) - rec.B, kLog2e, kRaceSlack) >= -24.0f) pass |= 1u << i;
                 }
                 const uint32_t lt = lanemask_lt();
                 int total = 0;
@@ -932,7 +968,7 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constan
                 const float thr = rec.thr;
 #pragma unroll
                 for (int i = 0; i < kSVec4; ++i) {
-                    if (max4f(v[i]) >= thr) {
+                    if (m4[i] >= thr) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float x = comp(v[i], q);
@@ -948,6 +984,7 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constan
             if (lane == 0) {
                 best_s[par][st][warp] = wb;
                 best_c[par][st][warp] = wc;
+                best_a[par][st][warp] = acand;
             }
         }
         if (!release_stage(&pp.count[st], lane)) continue;
@@ -957,8 +994,9 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constan
         float b = lane < kSWarps ? best_s[par][st][lane] : -INFINITY;
         int bc = lane < kSWarps ? best_c[par][st][lane] : INT_MAX;
         warp_best(b, bc);
+        const int ac = warp_min_nonneg(lane < kSWarps ? best_a[par][st][lane] : INT_MAX);
         if (lane == 0) {
-            p.te[t] = TileEnd{b, bc, topk ? tile_nk[par][st] : 0, 0};
+            p.te[t] = TileEnd{b, bc, topk ? tile_nk[par][st] : 0, ac};
             tile_nk[par][st] = 0;
         }
         __syncwarp();
@@ -979,32 +1017,43 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_cons
     const int G = p.tiles_per_row;
     const RowRecord rec = p.rr[row];
     const TileEnd* te = p.te + li * G;
-    if (rec.flags & kFNoisy) {
+    if (p.stats) {
+        // argmax: the lowest column holding the raw max, or a lower one
+        // whose exact quotient ties it; the sample: the best of the tiles'
+        // race winners and B (greedy rows: the argmax)
+        int a = rec.arg;
         float b = rec.B;
         int bc = rec.bcol;
         for (int c = lane; c < G; c += 32) {
-            const float tb = te[c].b;
-            const int tc = te[c].col;
-            if (beats(tb, tc, b, bc)) {
-                b = tb;
-                bc = tc;
+            const TileEnd e = te[c];
+            a = min(a, e.acol);
+            if (beats(e.b, e.col, b, bc)) {
+                b = e.b;
+                bc = e.col;
             }
         }
+        a = warp_min_nonneg(a);
         warp_best(b, bc);
-        if (lane == 0) p.sample[row] = b != -INFINITY ? bc : rec.arg;
+        if (lane == 0) {
+            p.argmax[row] = a;
+            p.sample[row] = (rec.flags & kFNoisy) && b != -INFINITY ? bc : a;
+        }
     }
     if (!(rec.flags & kFTopk)) return;
     // the row's candidates: counts, then the keys gathered in tile order
-    int n[2] = {0, 0};
+    constexpr int kU = (kMaxTiles + 31) / 32;
+    int n[kU], off[kU];
+    bool over_l = false;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < kU; ++u) {
         const int c = lane + 32 * u;
         n[u] = c < G ? te[c].nk : 0;
+        over_l |= n[u] > kTileKeys;
     }
-    const bool over = __any_sync(0xffffffffu, n[0] > kTileKeys || n[1] > kTileKeys);
-    int total = 0, off[2];
+    const bool over = __any_sync(0xffffffffu, over_l);
+    int total = 0;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < kU; ++u) {
         int incl = n[u];
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -1023,8 +1072,15 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_cons
     }
     uint64_t* kw = keys[warp];
     for (int c = 0; c < G; ++c) {
-        const int nc = __shfl_sync(0xffffffffu, c < 32 ? n[0] : n[1], c & 31);
-        const int oc = __shfl_sync(0xffffffffu, c < 32 ? off[0] : off[1], c & 31);
+        int nsel = 0, osel = 0;
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if ((c >> 5) == u) {
+                nsel = n[u];
+                osel = off[u];
+            }
+        const int nc = __shfl_sync(0xffffffffu, nsel, c & 31);
+        const int oc = __shfl_sync(0xffffffffu, osel, c & 31);
         const uint64_t* src = p.keys + (li * G + c) * kTileKeys;
         if (lane < nc) kw[oc + lane] = src[lane];
     }
@@ -1148,16 +1204,22 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     const int64_t gp = (c.rows + 255) / 256;
     const int64_t gr = (c.rows + kRowWarps - 1) / kRowWarps;
     if (gr > INT_MAX) return DRS_ERR_UNSUPPORTED;
+    // with kernel timing on, an event before each kernel and after the last
+    const int slot = kernel_timer_slot();
+    auto mark = [&](int i) {
+        return slot < 0 || cudaEventRecord(kernel_timer_event(slot, i), stream) == cudaSuccess;
+    };
+    if (!mark(0)) return DRS_ERR_CUDA;
     split_prep<<<static_cast<int>(gp), 256, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess || !mark(1)) return DRS_ERR_CUDA;
     split_pass1<<<g1, kSThreads, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess || !mark(2)) return DRS_ERR_CUDA;
     split_merge<<<static_cast<int>(gr), kRowWarps * 32, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess || !mark(3)) return DRS_ERR_CUDA;
     split_pass2<<<g2, kSThreads, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess || !mark(4)) return DRS_ERR_CUDA;
     split_finish<<<static_cast<int>(gr), kRowWarps * 32, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess || !mark(5)) return DRS_ERR_CUDA;
     return DRS_OK;
 }
 

@@ -7,9 +7,11 @@
 // 0x7FFFFFFF)), the low word 0x7FFFFFFF - column. Keys are distinct, so the
 // top-k under them is unique. -0.0 is canonicalised to +0.0 first.
 //
-// Work layout as in row_stats.cu: a team of G CTAs owns the G column chunks
-// of each row; rows of slots whose keep flag is 0 are skipped by the whole
-// team (nothing is read or written for them). Per kept row, each CTA
+// Work layout: a team of G CTAs owns the G column chunks of each row (one
+// CTA per SM, all resident, so their bounded waits on each other cannot
+// deadlock); teams take rows round robin. Rows of slots whose keep flag is 0
+// are skipped by the whole team (nothing is read or written for them). Per
+// kept row, each CTA
 //   1. stages its chunk (bulk copy), scales it (IEEE division by
 //      max(T, 1e-10)) and computes its max m and S = sum e^(s - m);
 //   2. takes as threshold the k-th largest of its 512 per-thread maximum
