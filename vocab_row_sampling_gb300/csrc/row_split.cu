@@ -71,7 +71,13 @@ constexpr int kSWarps = kSThreads / 32;
 #define DRS_SPLIT_VEC4 8
 #endif
 #ifndef DRS_SPLIT_STAGES
-#define DRS_SPLIT_STAGES 3
+#define DRS_SPLIT_STAGES 2
+#endif
+#ifndef DRS_P1_MINB
+#define DRS_P1_MINB 3
+#endif
+#ifndef DRS_P2_MINB
+#define DRS_P2_MINB 3
 #endif
 constexpr int kSVec4 = DRS_SPLIT_VEC4;             // float4 slots per thread
 constexpr int kTileCols = kSThreads * kSVec4 * 4;  // 8192
@@ -121,7 +127,7 @@ struct alignas(64) RowRecord {
     float M;      // max scaled logit (exact), -inf: the row is -inf everywhere
     float log2s;  // log2 S
     float ls;     // RN(log2(e) * RN(1/Te))
-    float c2;     // raw rows: RN(RN(Mraw * ls) + log2 S) - 64
+    float c2;     // raw rows: RN(RN(Mraw * ls) + log2 S)
     float cB;     // raw rows: RN(RN(Mraw * ls) + (B - M) log2(e)) - slack
     float B;      // best score among the warps' argmax elements
     float thr;    // top-k threshold (raw logit)
@@ -452,7 +458,7 @@ struct WarpPart {
     int arg;
 };
 
-__global__ void __launch_bounds__(kSThreads, 2) split_pass1(const __grid_constant__ SplitParams p) {
+__global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __grid_constant__ SplitParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     float4* stages = reinterpret_cast<float4*>(smem);
     __shared__ Pipe pp;
@@ -482,7 +488,6 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass1(const __grid_constan
         const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
         const int col0 = pp.col[n % kMap] * kTileCols;
         const int ncols = min(p.vocab - col0, kTileCols);
-        const float temp = rts[st].temp;
         ScaledQuotient sq;
         sq.t = rts[st].qt;
         sq.y = rts[st].qy;
@@ -718,7 +723,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
         rec.ls = kLog2e * rt.qy;
         const bool raw = !(fabsf(big_m) >= kRawLimit);
         const float c0 = mraw * rec.ls;
-        rec.c2 = (c0 + rec.log2s) - 64.0f;
+        rec.c2 = c0 + rec.log2s;
         rec.B = b;
         rec.bcol = bc;
         rec.cB = (c0 + (b - big_m) * kLog2e) - kRaceSlack;
@@ -748,15 +753,14 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
 // ============================================================== pass 2
 
 // Probabilities 2^t of a tile, t = x ls - c2 (raw rows) or (s - M) log2(e) -
-// log2 S: taken as 2^(t + 64) * 2^-64, so that the flushing 2^x keeps the
-// subnormal results (bf16 and fp16 can hold some); -inf logits give 0.
+// log2 S, subnormal results kept (bf16 and fp16 can hold some); -inf logits
+// give 0.
 template <bool BF16, bool RAW>
 __device__ __forceinline__ void write_probs(const float4 (&v)[kSVec4], const RowRecord& rec,
                                             const ScaledQuotient& sq, uint16_t* prow, bool vec,
                                             int ncols, int tid) {
     const bool full_tile = vec && ncols == kTileCols;
-    const float ls = rec.ls, c2 = rec.c2, big_m = rec.M;
-    const float c64 = rec.log2s - 64.0f;
+    const float ls = rec.ls, c2 = rec.c2, big_m = rec.M, l2s = rec.log2s;
 #pragma unroll
     for (int i = 0; i < kSVec4; ++i) {
         const int f = i * kSThreads + tid;
@@ -765,8 +769,8 @@ __device__ __forceinline__ void write_probs(const float4 (&v)[kSVec4], const Row
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float x = comp(v[i], q);
-            const float tq = RAW ? fmaf(x, ls, -c2) : fmaf(sq.exact(x) - big_m, kLog2e, -c64);
-            pr[q] = ex2_ftz(tq) * 0x1p-64f;
+            const float tq = RAW ? fmaf(x, ls, -c2) : fmaf(sq.exact(x) - big_m, kLog2e, -l2s);
+            pr[q] = ex2_approx(tq);
         }
         const uint32_t lo = pack2<BF16>(pr[0], pr[1]);
         const uint32_t hi = pack2<BF16>(pr[2], pr[3]);
@@ -817,20 +821,47 @@ __device__ __forceinline__ float4 race_e(const float4& x, const RowRecord& rec,
     return e;
 }
 
-// Survivors of a group: elements whose lower bound of 1 - u is at most
-// their e^(s - B).
-__device__ __forceinline__ uint32_t race_group(const float4& e, uint4 w) {
-    const uint32_t wmax = max(max(w.x, w.y), max(w.z, w.w));
-    uint32_t bits = 0;
-    if (one_minus_u_lower(wmax) <= max4f(e)) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (one_minus_u_lower(word_of(w, q)) <= comp(e, q)) bits |= 1u << q;
+struct Best {
+    float s;
+    int c;
+};
+
+// The survivors `bits` of the group at column c4 scored exactly (s + g)
+// against the best so far; the column of B was scored already.
+__device__ __noinline__ Best race_rescore(uint32_t bits, const float4 x4, uint4 nw, int c4,
+                                          int bcol, ScaledQuotient sq, Best best) {
+    while (bits) {
+        const int q = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int col = c4 + q;
+        if (col == bcol) continue;
+        const float score = sq.exact(comp(x4, q)) + gumbel_of_bits(word_of(nw, q));
+        if (beats(score, col, best.s, best.c)) best = Best{score, col};
     }
-    return bits;
+    return best;
 }
 
-__global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constant__ SplitParams p) {
+// The top-k candidates of a thread's slots in `smask` (slot i: bit i): the
+// logits x >= thr, read again from the stage, keyed by (exact value, lower
+// column) into the tile's list.
+__device__ __noinline__ void topk_collect(uint32_t smask, const float4* stage, int tid, int col0,
+                                          int ncols, float thr, ScaledQuotient sq, int* count,
+                                          uint64_t* kdst) {
+    while (smask) {
+        const int f = (__ffs(smask) - 1) * kSThreads + tid;
+        smask &= smask - 1;
+        const float4 x4 = stage[f];
+        for (int q = 0; q < 4; ++q) {
+            const float x = comp(x4, q);
+            if (4 * f + q < ncols && x >= thr) {
+                const int pos = atomicAdd(count, 1);
+                if (pos < kTileKeys) kdst[pos] = topk_key(sq.exact(x), col0 + 4 * f + q);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __grid_constant__ SplitParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     float4* stages = reinterpret_cast<float4*>(smem);
     __shared__ Pipe pp;
@@ -941,21 +972,28 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constan
                     total += __popc(bl);
                 }
                 __syncwarp();
+                // each listed group: its noise, then the group's largest e
+                // against its largest word (one 2^x); the elements one by
+                // one only when that passes
                 for (int m = lane; m < total; m += 32) {
                     const int f = race_at[warp][m];
                     const float4 x4 = stage[f];
                     const int c4 = col0 + 4 * f;
                     const uint4 nw = noise_group(p.rk, grow, static_cast<uint32_t>(c4 >> 2));
-                    uint32_t bits = race_group(race_e(x4, rec, sq), nw);
-                    while (bits) {
-                        const int q = __ffs(bits) - 1;
-                        bits &= bits - 1;
-                        const int col = c4 + q;
-                        if (col == rec.bcol) continue;  // scored already: B
-                        const float score = sq.exact(comp(x4, q)) + gumbel_of_bits(word_of(nw, q));
-                        if (beats(score, col, wb, wc)) {
-                            wb = score;
-                            wc = col;
+                    const uint32_t wmax = max(max(nw.x, nw.y), max(nw.z, nw.w));
+                    const float mx = max4f(x4);
+                    const float emax = (rec.flags & kFRaw) ? ex2_ftz(fmaf(mx, rec.ls, -rec.cB))
+                                                           : ex2_ftz(fmaf(sq.exact(mx) - rec.B, kLog2e, kRaceSlack));
+                    if (one_minus_u_lower(wmax) <= emax) {
+                        const float4 e = race_e(x4, rec, sq);
+                        uint32_t bits = 0;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (one_minus_u_lower(word_of(nw, q)) <= comp(e, q)) bits |= 1u << q;
+                        if (bits) {
+                            const Best b2 = race_rescore(bits, x4, nw, c4, rec.bcol, sq, Best{wb, wc});
+                            wb = b2.s;
+                            wc = b2.c;
                         }
                     }
                 }
@@ -963,23 +1001,14 @@ __global__ void __launch_bounds__(kSThreads, 2) split_pass2(const __grid_constan
             }
 
             if (topk) {
-                // candidates x >= thr, keyed by (exact value, lower column)
-                uint64_t* kdst = p.keys + t * kTileKeys;
+                // candidates x >= thr (rare: the slots reaching it)
                 const float thr = rec.thr;
+                uint32_t km = 0;
 #pragma unroll
-                for (int i = 0; i < kSVec4; ++i) {
-                    if (m4[i] >= thr) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float x = comp(v[i], q);
-                            if (x >= thr) {
-                                const int col = col0 + 4 * (i * kSThreads + tid) + q;
-                                const int pos = atomicAdd(&tile_nk[par][st], 1);
-                                if (pos < kTileKeys) kdst[pos] = topk_key(sq.exact(x), col);
-                            }
-                        }
-                    }
-                }
+                for (int i = 0; i < kSVec4; ++i) km |= (m4[i] >= thr ? 1u : 0u) << i;
+                if (km)
+                    topk_collect(km, stage, tid, col0, ncols, thr, sq, &tile_nk[par][st],
+                                 p.keys + t * kTileKeys);
             }
             if (lane == 0) {
                 best_s[par][st][warp] = wb;
