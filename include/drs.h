@@ -135,6 +135,38 @@ drs_status drs_row_stats_noalloc(const float *logits, int64_t rows, int64_t voca
                                  int64_t probs_row_stride, void *stream);
 
 /*
+ * Bytes of device workspace drs_row_stats_seeds needs for n_seeds seeds
+ * (1 <= n_seeds <= 8; 0 otherwise). Same alignment and sharing rules as the
+ * row-stats workspace.
+ */
+size_t drs_row_stats_seeds_workspace_bytes(int64_t rows, int64_t vocab, int32_t n_seeds);
+
+/*
+ * drs_row_stats for several noise seeds in one call: the argmax, entropy and
+ * probabilities once, and a Gumbel-max sample per seed, from the same two
+ * passes over the logits (the race of each seed runs on the tile already in
+ * shared memory). Every argument of drs_row_stats has its meaning there;
+ * in addition:
+ *
+ *   seeds       HOST uint64 [n_seeds], 1 <= n_seeds <= 8: the noise keys.
+ *   samples     int64 [n_seeds, rows]: samples + s * rows is the sample of
+ *               every row under seeds[s] (what drs_row_stats gives with that
+ *               seed).
+ *   workspace   drs_row_stats_seeds_workspace_bytes(rows, vocab, n_seeds).
+ *
+ * Returns DRS_ERR_INVALID_ARG for a null seeds array or n_seeds outside
+ * [1, 8], otherwise as drs_row_stats.
+ */
+drs_status drs_row_stats_seeds(const float *logits, int64_t rows, int64_t vocab,
+                               int64_t row_stride, const float *temps,
+                               int64_t canvas_len, const uint64_t *seeds,
+                               int32_t n_seeds, int64_t row0, int64_t *argmax,
+                               int64_t *samples, float *entropy,
+                               drs_probs_dtype probs_dtype, void *probs,
+                               int64_t probs_row_stride, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace drs_row_stats_topk needs for k > 0 (256-byte
  * aligned, contents arbitrary: each call clears what it uses with
  * asynchronous memsets on its stream). 0 for k <= 0, where the call needs

@@ -35,7 +35,8 @@ EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_row_stats_noa
             "drs_row_stats_topk", "drs_row_stats_topk_workspace_bytes", "drs_topk_logprobs",
             "drs_topk_workspace_bytes", "drs_philox_gumbel", "drs_scaled_logits",
             "drs_status_string", "drs_get_device_error", "drs_test_inject_fault",
-            "drs_kernel_timing", "drs_kernel_times")
+            "drs_kernel_timing", "drs_kernel_times", "drs_row_stats_seeds",
+            "drs_row_stats_seeds_workspace_bytes")
 
 
 class DrsError(RuntimeError):
@@ -92,6 +93,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_test_inject_fault.restype = None
     lib.drs_get_device_error.argtypes = [vp]
     lib.drs_get_device_error.restype = ctypes.c_int
+    lib.drs_row_stats_seeds_workspace_bytes.argtypes = [i64, i64, i32]
+    lib.drs_row_stats_seeds_workspace_bytes.restype = sz
+    lib.drs_row_stats_seeds.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i64, vp, vp, vp,
+                                        ctypes.c_int, vp, i64, vp, sz, vp]
+    lib.drs_row_stats_seeds.restype = ctypes.c_int
     lib.drs_kernel_timing.argtypes = [ctypes.c_int]
     lib.drs_kernel_timing.restype = ctypes.c_int
     lib.drs_kernel_times.argtypes = [vp, i32, vp]
@@ -160,6 +166,28 @@ def drs_row_stats_noalloc(logits, temps, canvas_len, seed, argmax, sample, entro
                                       _ptr(argmax), _ptr(sample), _ptr(entropy), probs_dtype,
                                       _ptr(probs), pstride, _stream(stream))
     _check(st, "drs_row_stats_noalloc")
+
+
+def drs_row_stats_seeds_workspace_bytes(rows: int, vocab: int, n_seeds: int) -> int:
+    return int(load().drs_row_stats_seeds_workspace_bytes(rows, vocab, n_seeds))
+
+
+def drs_row_stats_seeds(logits, temps, canvas_len, seeds, argmax, samples, entropy,
+                        probs_dtype=DRS_PROBS_NONE, probs=None, workspace=None, stream=None,
+                        row0=0):
+    """Launch drs_row_stats_seeds: `seeds` a sequence of ints (host), samples
+    an int64 CUDA tensor [len(seeds), rows]."""
+    rows, vocab = logits.shape
+    n = len(seeds)
+    keys = (ctypes.c_uint64 * max(n, 1))(*[int(x) & (2**64 - 1) for x in seeds])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    pstride = 0 if probs is None else probs.stride(0)
+    st = load().drs_row_stats_seeds(_ptr(logits), rows, vocab, _row_stride(logits), _ptr(temps),
+                                    canvas_len, ctypes.cast(keys, ctypes.c_void_p), n, row0,
+                                    _ptr(argmax), _ptr(samples), _ptr(entropy), probs_dtype,
+                                    _ptr(probs), pstride, _ptr(workspace), ws_bytes,
+                                    _stream(stream))
+    _check(st, "drs_row_stats_seeds")
 
 
 def drs_row_stats_topk_workspace_bytes(rows: int, vocab: int, k: int) -> int:
@@ -273,6 +301,27 @@ def row_stats(logits, temps, canvas_len: int, seed: int, probs_dtype=None, strea
     drs_row_stats(logits, temps, canvas_len, seed, argmax, sample, entropy, code, probs, ws,
                   stream, row0)
     return argmax, sample, entropy, probs
+
+
+def row_stats_seeds(logits, temps, canvas_len: int, seeds, probs_dtype=None, stream=None,
+                    row0: int = 0):
+    """Allocate outputs and run drs_row_stats_seeds; returns (argmax,
+    samples [len(seeds), rows], entropy, probs)."""
+    import torch
+    rows, vocab = logits.shape
+    dev = logits.device
+    argmax = torch.empty(rows, dtype=torch.int64, device=dev)
+    samples = torch.empty(len(seeds), rows, dtype=torch.int64, device=dev)
+    entropy = torch.empty(rows, dtype=torch.float32, device=dev)
+    code = {None: DRS_PROBS_NONE, torch.bfloat16: DRS_PROBS_BF16,
+            torch.float16: DRS_PROBS_FP16}[probs_dtype]
+    probs = None if probs_dtype is None else torch.empty(rows, vocab, dtype=probs_dtype, device=dev)
+    if rows == 0:
+        return argmax, samples, entropy, probs
+    ws = workspace(drs_row_stats_seeds_workspace_bytes(rows, vocab, len(seeds)), dev)
+    drs_row_stats_seeds(logits, temps, canvas_len, seeds, argmax, samples, entropy, code, probs,
+                        ws, stream, row0)
+    return argmax, samples, entropy, probs
 
 
 def row_stats_topk(logits, temps, canvas_len: int, seed: int, keep, k: int, probs_dtype=None,

@@ -53,6 +53,8 @@ struct RowCall {
     const float* temps;
     int64_t canvas_len;
     uint64_t seed;
+    const uint64_t* seeds;  // null: one seed (`seed`); else n_seeds of them (HOST)
+    int32_t n_seeds;
     int64_t row0;
     int64_t* argmax;
     int64_t* sample;
@@ -82,8 +84,9 @@ cudaEvent_t kernel_timer_event(int slot, int i);
 // The two-pass row kernels (row_split.cu). The workspace starts with the
 // hard-row list (count at [0], rows from [64]): rows whose top-k the exact
 // kernel must finish. k is at most split_max_k().
-size_t split_workspace_bytes(int64_t rows, int64_t vocab, int32_t k);
+size_t split_workspace_bytes(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds);
 int32_t split_max_k();
+int32_t split_max_seeds();
 drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream);
 
 }  // namespace drs

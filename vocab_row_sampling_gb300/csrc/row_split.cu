@@ -91,8 +91,8 @@ constexpr int kTileKeys = 32;     // top-k candidates a tile keeps
 constexpr int kRowKeys = 512;     // top-k candidates a row merges
 constexpr int kSplitMaxK = 64;    // larger k: the exact kernel
 constexpr int kHardOffset = 64;   // hard-row list: count at [0], rows from [64]
-constexpr int kCount1 = 1;        // header words: pass-1 list length
-constexpr int kCount2 = 2;        //               pass-2 list length
+constexpr int kCount1 = 1;        // header word: length of the row list
+constexpr int kMaxSeeds = 8;      // noise seeds of one call
 constexpr float kRawLimit = 256.0f;
 // Slack (log2 units) of the race bounds: covers the roundings of the
 // reference c and of x * log2(e) / Te (a few 1e-5 for |s| up to a few
@@ -122,33 +122,42 @@ static_assert(sizeof(TileStats) == 96, "tile record");
 
 enum : int { kFNoisy = 1, kFTopk = 2, kFRaw = 4 };
 
-// A row after the merge (64 bytes).
-struct alignas(64) RowRecord {
+// A row after the merge (64 bytes), followed in the row's entry by one
+// SeedRec per noise seed.
+struct alignas(16) RowRecord {
     float M;      // max scaled logit (exact), -inf: the row is -inf everywhere
     float log2s;  // log2 S
     float ls;     // RN(log2(e) * RN(1/Te))
     float c2;     // raw rows: RN(RN(Mraw * ls) + log2 S)
-    float cB;     // raw rows: RN(RN(Mraw * ls) + (B - M) log2(e)) - slack
-    float B;      // best score among the warps' argmax elements
     float thr;    // top-k threshold (raw logit)
     float lns;    // log S
-    int bcol;
     int arg;      // lowest column holding the raw row max
     int flags;
     float qt, qy;
     int qmode;
     float cthr;   // a logit whose exact quotient equals M is at least this
-    int pad;
+    int pad[4];
 };
 static_assert(sizeof(RowRecord) == 64, "row record");
 
-// Pass-2 record of a tile: race winner, candidate count, and the lowest
-// column below the raw max whose exact quotient is M (16 bytes).
-struct alignas(16) TileEnd {
-    float b;
-    int col;
+// The race bound of one seed for a row (16 bytes).
+struct alignas(16) SeedRec {
+    float B;      // best Gumbel-max score among the warps' candidates
+    float cB;     // raw rows: RN(RN(Mraw * ls) + (B - M) log2(e)) - slack
+    int bcol;     // its column
+    int pad;
+};
+constexpr size_t kRowEntryMax = sizeof(RowRecord) + kMaxSeeds * sizeof(SeedRec);
+
+// Pass-2 record of a tile: candidate count and the lowest column below the
+// raw max whose exact quotient is M (8 bytes); per seed, the race winner.
+struct alignas(8) TileEnd {
     int nk;
     int acol;
+};
+struct alignas(8) TileSeed {
+    float b;
+    int col;
 };
 
 struct SplitParams {
@@ -160,22 +169,26 @@ struct SplitParams {
     const float* temps;
     const uint8_t* keep;
     int64_t* argmax;
-    int64_t* sample;
+    int64_t* sample;      // [n_seeds, rows]
     float* entropy;
     void* probs;
     int64_t probs_row_stride;
     int32_t* out_ids;
     float* out_lp;
     int32_t* hard;    // header (hard count, list lengths), then hard rows
-    int32_t* list1;   // rows of pass 1
-    int32_t* list2;   // rows of pass 2
+    int32_t* list1;   // the rows the passes work on
     RowTemp* rt;
-    TileStats* ts;    // by pass-1 tile
-    RowRecord* rr;    // by row
-    TileEnd* te;      // by pass-2 tile
-    uint64_t* keys;   // by pass-2 tile
+    TileStats* ts;    // by tile (list index * G + tile of the row)
+    unsigned char* rr;  // by row: RowRecord + n_seeds SeedRec (rec_bytes each)
+    TileEnd* te;      // by tile
+    TileSeed* tb;     // by tile and seed
+    uint64_t* keys;   // by tile
+    int li_begin;     // the list entries of this launch: [li_begin, li_end),
+    int li_end;       // li_end < 0: to the end of the list
     int* err;
-    PhiloxRoundKeys rk;
+    PhiloxRoundKeys rk[kMaxSeeds];
+    int n_seeds;
+    int rec_bytes;    // sizeof(RowRecord) + n_seeds * sizeof(SeedRec)
     int vocab;
     int tiles_per_row;
     int vec;          // rows start 16-byte aligned: bulk copies
@@ -292,14 +305,19 @@ struct Pipe {
     int col[kMap];
 };
 
+// The tiles of a launch: [t_begin, t_end) of the list's tile space.
+struct TileRange {
+    int64_t t_begin, t_end;
+};
+
 // Map tiles first .. first + nfill - 1 (one per lane or thread).
-__device__ __forceinline__ void map_tiles(Pipe& pp, const int32_t* list, int64_t tiles, int G,
+__device__ __forceinline__ void map_tiles(Pipe& pp, const int32_t* list, TileRange tr, int G,
                                           int first, int nfill, int idx) {
     if (idx >= nfill) return;
     const int n = first + idx;
-    const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+    const int64_t t = tr.t_begin + static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
     int row = -1, c = 0;
-    if (t < tiles) {
+    if (t < tr.t_end) {
         const uint32_t li = static_cast<uint32_t>(t) / static_cast<uint32_t>(G);
         c = static_cast<int>(static_cast<uint32_t>(t) - li * static_cast<uint32_t>(G));
         row = list[li];
@@ -336,6 +354,16 @@ __device__ __forceinline__ void issue_tile(const SplitParams& p, Pipe& pp, int n
     if (bytes) tma_load_1d(stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, bytes, &pp.full[st]);
 }
 
+// The list entries and tiles of this launch.
+__device__ __forceinline__ int list_end(const SplitParams& p) {
+    const int n = p.hard[kCount1];
+    return p.li_end < 0 || p.li_end > n ? n : p.li_end;
+}
+__device__ __forceinline__ TileRange launch_tiles(const SplitParams& p) {
+    const int G = p.tiles_per_row;
+    return TileRange{static_cast<int64_t>(p.li_begin) * G, static_cast<int64_t>(list_end(p)) * G};
+}
+
 // Count a warp out of a stage; true on the warp that counted out last (the
 // count is reset for the stage's next tile).
 __device__ __forceinline__ bool release_stage(int* count, int lane) {
@@ -352,10 +380,11 @@ __device__ __forceinline__ bool release_stage(int* count, int lane) {
 }
 
 // Pipeline start: barriers, the first kMap tiles mapped, the first kStages
-// issued.
+// issued (the row record of stage s at recs + s * rec_stride).
 __device__ __forceinline__ void pipe_start(const SplitParams& p, Pipe& pp, const int32_t* list,
-                                           int64_t tiles, float4* stages, void* recs,
-                                           const void* rec_table, uint32_t rec_bytes, bool tma) {
+                                           TileRange tiles, float4* stages, void* recs,
+                                           size_t rec_stride, const void* rec_table,
+                                           uint32_t rec_bytes, bool tma) {
     const int tid = threadIdx.x;
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -369,14 +398,14 @@ __device__ __forceinline__ void pipe_start(const SplitParams& p, Pipe& pp, const
     __syncthreads();
     if (tid == 0)
         for (int s = 0; s < kStages; ++s)
-            issue_tile(p, pp, s, stages + s * kStageF4, static_cast<unsigned char*>(recs) + s * rec_bytes,
+            issue_tile(p, pp, s, stages + s * kStageF4, static_cast<unsigned char*>(recs) + s * rec_stride,
                        rec_table, rec_bytes, tma);
 }
 
 // The last warp out of tile n: refill its stage with tile n + kStages, and
 // every 32 tiles map 32 more (over tiles that every warp is done with).
 __device__ __forceinline__ void pipe_advance(const SplitParams& p, Pipe& pp, int n, const int32_t* list,
-                                             int64_t tiles, float4* stage, void* rec_dst,
+                                             TileRange tiles, float4* stage, void* rec_dst,
                                              const void* rec_table, uint32_t rec_bytes, bool tma,
                                              int lane) {
     if (lane == 0) {
@@ -458,6 +487,28 @@ struct WarpPart {
     int arg;
 };
 
+// A warp's S = sum 2^t and W = ln2 * sum 2^t t, t = x * lscale - cref, over
+// the thread's slots; with CLAMP, t is kept finite (a -inf logit gives e = 0
+// and e * t = 0 instead of NaN).
+template <bool CLAMP>
+__device__ __forceinline__ void tile_sums(const float4 (&v)[kSVec4], float lscale, float cref,
+                                          float& sw, float& ww) {
+    float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wa[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < kSVec4; ++i) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float tq = fmaf(comp(v[i], q), lscale, -cref);
+            if (CLAMP) tq = fmaxf(tq, -FLT_MAX);
+            const float e = ex2_ftz(tq);
+            sa[q] += e;
+            wa[q] = fmaf(e, tq, wa[q]);
+        }
+    }
+    sw = warp_sum_f((sa[0] + sa[1]) + (sa[2] + sa[3]));
+    ww = warp_sum_f((wa[0] + wa[1]) + (wa[2] + wa[3])) * kLn2;
+}
+
 __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __grid_constant__ SplitParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     float4* stages = reinterpret_cast<float4*>(smem);
@@ -469,9 +520,8 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
     const int warp = tid >> 5;
     const bool stats = p.stats != 0;
     const bool tma = p.vec != 0;
-    const int G = p.tiles_per_row;
-    const int64_t tiles = static_cast<int64_t>(p.hard[kCount1]) * G;
-    pipe_start(p, pp, p.list1, tiles, stages, rts, p.rt, sizeof(RowTemp), tma);
+    const TileRange tiles = launch_tiles(p);
+    pipe_start(p, pp, p.list1, tiles, stages, rts, sizeof(RowTemp), p.rt, sizeof(RowTemp), tma);
     for (int n = 0;; ++n) {
         const int st = n % kStages;
         const int par = (n / kStages) & 1;
@@ -485,7 +535,7 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
         }
         const int row = pp.row[n % kMap];
         if (row < 0) break;
-        const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+        const int64_t t = tiles.t_begin + static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
         const int col0 = pp.col[n % kMap] * kTileCols;
         const int ncols = min(p.vocab - col0, kTileCols);
         ScaledQuotient sq;
@@ -548,23 +598,9 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
                 cref = 0.0f;
             }
             float sw = 0.0f, ww = 0.0f;  // a warp of -inf only: nothing to sum
-            for (int pass = 0; mxw != -INFINITY; ++pass) {
-                const float clamp = pass ? -FLT_MAX : -INFINITY;
-                float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wa[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                for (int i = 0; i < kSVec4; ++i) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float tq = fmaf(comp(v[i], q), lscale, -cref);
-                        if (pass) tq = fmaxf(tq, clamp);
-                        const float e = ex2_ftz(tq);
-                        sa[q] += e;
-                        wa[q] = fmaf(e, tq, wa[q]);
-                    }
-                }
-                sw = warp_sum_f((sa[0] + sa[1]) + (sa[2] + sa[3]));
-                ww = warp_sum_f((wa[0] + wa[1]) + (wa[2] + wa[3])) * kLn2;
-                if (pass || !isnan(ww)) break;
+            if (mxw != -INFINITY) {
+                tile_sums<false>(v, lscale, cref, sw, ww);
+                if (isnan(ww)) tile_sums<true>(v, lscale, cref, sw, ww);
             }
             if (lane == 0) parts[par][st][warp] = WarpPart{0.0f, sw, ww, mxw, aw};
         }
@@ -610,8 +646,8 @@ constexpr int kRowWarps = 8;  // rows per CTA of the merge and finish kernels
 
 __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_constant__ SplitParams p) {
     const int lane = threadIdx.x & 31;
-    const int64_t li = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
-    if (li >= p.hard[kCount1]) return;
+    const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+    if (li >= list_end(p)) return;
     const int64_t row = p.list1[li];
     const uint64_t slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
     const bool kept = p.keep == nullptr || p.keep[slot] != 0;
@@ -619,25 +655,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
     const float temp = rt.temp;
     const int G = p.tiles_per_row;
     const TileStats* tr = p.ts + li * G;
-    float m = -INFINITY, s = 0.0f, w = 0.0f, xm = -INFINITY, b = -INFINITY;
-    int arg = INT_MAX, bc = INT_MAX;
-    // B: the best Gumbel-max score of the warps' candidates (the lowest
-    // column holding each warp's raw max, whose exact quotient is M_w)
-    if (p.stats && temp > 0.0f) {
-        const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
-        const ScaledQuotient sq{rt.qt, rt.qy, rt.qmode};
-        for (int jx = lane; jx < kSWarps * G; jx += 32) {
-            const int col = tr[jx / kSWarps].wcol[jx % kSWarps];
-            if (col == INT_MAX) continue;
-            const float mw = sq.exact(unord32(tr[jx / kSWarps].wmax[jx % kSWarps]));
-            const uint4 nw = noise_group(p.rk, grow, static_cast<uint32_t>(col >> 2));
-            const float sc = mw + gumbel_of_bits(word_of(nw, col & 3));
-            if (beats(sc, col, b, bc)) {
-                b = sc;
-                bc = col;
-            }
-        }
-    }
+    float m = -INFINITY, s = 0.0f, w = 0.0f, xm = -INFINITY;
+    int arg = INT_MAX;
     for (int c = lane; c < G; c += 32) {
         const TileStats r = tr[c];
         // the lowest column holding the raw max (-inf rows: the first)
@@ -668,7 +687,6 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
     }
     const float s_tot = warp_sum_f(s_l);
     const float w_tot = warp_sum_f(w_l);
-    warp_best(b, bc);
     const float mraw = warp_max_f(xm);
     const int arg_row = warp_min_nonneg(xm == mraw ? arg : INT_MAX);
 
@@ -715,37 +733,57 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
         }
     }
 
+    // B per seed: the best Gumbel-max score of the warps' candidates (the
+    // lowest column holding each warp's raw max, whose exact quotient is
+    // M_w)
+    const bool noisy = p.stats && temp > 0.0f && big_m != -INFINITY;
+    const float ls = kLog2e * rt.qy;
+    const float c0 = mraw * ls;
+    unsigned char* entry = p.rr + row * p.rec_bytes;
+    for (int sd = 0; sd < p.n_seeds; ++sd) {
+        float b = -INFINITY;
+        int bc = INT_MAX;
+        if (noisy) {
+            const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
+            const ScaledQuotient sq{rt.qt, rt.qy, rt.qmode};
+            for (int jx = lane; jx < kSWarps * G; jx += 32) {
+                const int col = tr[jx / kSWarps].wcol[jx % kSWarps];
+                if (col == INT_MAX) continue;
+                const float mw = sq.exact(unord32(tr[jx / kSWarps].wmax[jx % kSWarps]));
+                const uint4 nw = noise_group(p.rk[sd], grow, static_cast<uint32_t>(col >> 2));
+                const float sc = mw + gumbel_of_bits(word_of(nw, col & 3));
+                if (beats(sc, col, b, bc)) {
+                    b = sc;
+                    bc = col;
+                }
+            }
+        }
+        warp_best(b, bc);
+        if (lane == 0)
+            reinterpret_cast<SeedRec*>(entry + sizeof(RowRecord))[sd] =
+                SeedRec{b, (c0 + (b - big_m) * kLog2e) - kRaceSlack, bc, 0};
+    }
+
     if (lane == 0) {
         RowRecord rec{};
         rec.M = big_m;
         rec.log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
         rec.lns = rec.log2s * kLn2;
-        rec.ls = kLog2e * rt.qy;
+        rec.ls = ls;
         const bool raw = !(fabsf(big_m) >= kRawLimit);
-        const float c0 = mraw * rec.ls;
         rec.c2 = c0 + rec.log2s;
-        rec.B = b;
-        rec.bcol = bc;
-        rec.cB = (c0 + (b - big_m) * kLog2e) - kRaceSlack;
         rec.thr = thr;
         rec.arg = arg_row;
         rec.cthr = mraw - fmaxf(fabsf(mraw) * 0x1p-20f, rt.qt * 0x1p-140f);
         rec.qt = rt.qt;
         rec.qy = rt.qy;
         rec.qmode = rt.qmode;
-        const bool noisy = p.stats && temp > 0.0f && big_m != -INFINITY;
         rec.flags = (noisy ? kFNoisy : 0) | (topk && !hard ? kFTopk : 0) | (raw ? kFRaw : 0);
-        p.rr[row] = rec;
+        *reinterpret_cast<RowRecord*>(entry) = rec;
         if (p.stats) p.entropy[row] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
         if (hard) {
             const int idx = atomicAdd(p.hard, 1);
             p.hard[kHardOffset + idx] = static_cast<int32_t>(row);
-        }
-        // the rows that pass 2 reads: every row of a statistics call (the
-        // argmax is settled there), and rows that want candidates
-        if (p.stats || (rec.flags & kFTopk)) {
-            const int idx = atomicAdd(p.hard + kCount2, 1);
-            p.list2[idx] = static_cast<int32_t>(row);
         }
     }
 }
@@ -804,19 +842,19 @@ __device__ __forceinline__ void probs_of_tile(const float4 (&v)[kSVec4], const R
 // e^(s - B) of a group, over-estimated by the slack: 2^(x ls - cB) on raw
 // rows, else from the exact quotients (flushed below 2^-126: such elements
 // cannot win).
-__device__ __forceinline__ float4 race_e(const float4& x, const RowRecord& rec,
+__device__ __forceinline__ float4 race_e(const float4& x, bool raw, float ls, const SeedRec& sr,
                                          const ScaledQuotient& sq) {
     float4 e;
-    if (rec.flags & kFRaw) {
-        e.x = ex2_ftz(fmaf(x.x, rec.ls, -rec.cB));
-        e.y = ex2_ftz(fmaf(x.y, rec.ls, -rec.cB));
-        e.z = ex2_ftz(fmaf(x.z, rec.ls, -rec.cB));
-        e.w = ex2_ftz(fmaf(x.w, rec.ls, -rec.cB));
+    if (raw) {
+        e.x = ex2_ftz(fmaf(x.x, ls, -sr.cB));
+        e.y = ex2_ftz(fmaf(x.y, ls, -sr.cB));
+        e.z = ex2_ftz(fmaf(x.z, ls, -sr.cB));
+        e.w = ex2_ftz(fmaf(x.w, ls, -sr.cB));
     } else {
-        e.x = ex2_ftz(fmaf(sq.exact(x.x) - rec.B, kLog2e, kRaceSlack));
-        e.y = ex2_ftz(fmaf(sq.exact(x.y) - rec.B, kLog2e, kRaceSlack));
-        e.z = ex2_ftz(fmaf(sq.exact(x.z) - rec.B, kLog2e, kRaceSlack));
-        e.w = ex2_ftz(fmaf(sq.exact(x.w) - rec.B, kLog2e, kRaceSlack));
+        e.x = ex2_ftz(fmaf(sq.exact(x.x) - sr.B, kLog2e, kRaceSlack));
+        e.y = ex2_ftz(fmaf(sq.exact(x.y) - sr.B, kLog2e, kRaceSlack));
+        e.z = ex2_ftz(fmaf(sq.exact(x.z) - sr.B, kLog2e, kRaceSlack));
+        e.w = ex2_ftz(fmaf(sq.exact(x.w) - sr.B, kLog2e, kRaceSlack));
     }
     return e;
 }
@@ -861,14 +899,18 @@ __device__ __noinline__ void topk_collect(uint32_t smask, const float4* stage, i
     }
 }
 
+// MULTI: several noise seeds (a race per seed); else one, its round keys
+// read as constants.
+template <bool MULTI>
 __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __grid_constant__ SplitParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     float4* stages = reinterpret_cast<float4*>(smem);
     __shared__ Pipe pp;
-    __shared__ RowRecord recs[kStages];
+    __shared__ __align__(16) unsigned char recs[kStages][kRowEntryMax];
     __shared__ uint16_t race_at[kSWarps][kSVec4 * 32];
-    __shared__ float best_s[2][kStages][kSWarps];
-    __shared__ int best_c[2][kStages][kSWarps];
+    constexpr int kSeedSlots = MULTI ? kMaxSeeds : 1;
+    __shared__ float best_s[2][kStages][kSeedSlots][kSWarps];
+    __shared__ int best_c[2][kStages][kSeedSlots][kSWarps];
     __shared__ int best_a[2][kStages][kSWarps];
     __shared__ int tile_nk[2][kStages];
     const int tid = threadIdx.x;
@@ -877,10 +919,10 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
     const bool stats = p.stats != 0;
     const bool probs = stats && p.probs_dtype != 0;
     const bool tma = p.vec != 0;
-    const int G = p.tiles_per_row;
-    const int64_t tiles = static_cast<int64_t>(p.hard[kCount2]) * G;
+    const TileRange tiles = launch_tiles(p);
     if (tid < 2 * kStages) tile_nk[tid / kStages][tid % kStages] = 0;
-    pipe_start(p, pp, p.list2, tiles, stages, recs, p.rr, sizeof(RowRecord), tma);
+    pipe_start(p, pp, p.list1, tiles, stages, &recs[0][0], kRowEntryMax, p.rr,
+               static_cast<uint32_t>(p.rec_bytes), tma);
     for (int n = 0;; ++n) {
         const int st = n % kStages;
         const int par = (n / kStages) & 1;
@@ -894,13 +936,17 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
         }
         const int row = pp.row[n % kMap];
         if (row < 0) break;
-        const int64_t t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
+        const int64_t t = tiles.t_begin + static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
         const int col0 = pp.col[n % kMap] * kTileCols;
         const int ncols = min(p.vocab - col0, kTileCols);
-        const RowRecord& rec = recs[st];
+        const RowRecord& rec = *reinterpret_cast<const RowRecord*>(&recs[st][0]);
+        const SeedRec* seeds = reinterpret_cast<const SeedRec*>(&recs[st][sizeof(RowRecord)]);
         const int flags = rec.flags;
         const bool noisy = (flags & kFNoisy) != 0;
         const bool topk = (flags & kFTopk) != 0;
+        // (a row of a top-k-only call without a threshold, which the exact
+        // kernel takes, runs through here with nothing to produce: it is
+        // rare, and a branch around the block slowed every tile)
         {
             const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
             ScaledQuotient sq;
@@ -946,21 +992,27 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
                 acand = warp_min_nonneg(acand);
             }
 
-            float wb = rec.B;
-            int wc = rec.bcol;
+            // the race, once per seed
+            const bool rawr = (flags & kFRaw) != 0;
+            const int nsd = MULTI ? p.n_seeds : 1;
+            for (int sd = 0; sd < nsd; ++sd) {
+            const SeedRec sr = seeds[sd];
+            const PhiloxRoundKeys& rk = MULTI ? p.rk[sd] : p.rk[0];
+            float wb = sr.B;
+            int wc = sr.bcol;
             if (noisy) {
                 // groups whose largest e^(s - B) reaches 2^-24, listed
                 // warp-wide by their float4 index in the stage
                 uint32_t pass = 0;
-                if (flags & kFRaw) {
-                    const float ls = rec.ls, cB = rec.cB;
+                if (rawr) {
+                    const float ls = rec.ls, cB = sr.cB;
 #pragma unroll
                     for (int i = 0; i < kSVec4; ++i)
                         if (fmaf(m4[i], ls, -cB) >= -24.0f) pass |= 1u << i;
                 } else {
 #pragma unroll
                     for (int i = 0; i < kSVec4; ++i)
-                        if (fmaf(sq.exact(m4[i]) - rec.B, kLog2e, kRaceSlack) >= -24.0f) pass |= 1u << i;
+                        if (fmaf(sq.exact(m4[i]) - sr.B, kLog2e, kRaceSlack) >= -24.0f) pass |= 1u << i;
                 }
                 const uint32_t lt = lanemask_lt();
                 int total = 0;
@@ -979,25 +1031,31 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
                     const int f = race_at[warp][m];
                     const float4 x4 = stage[f];
                     const int c4 = col0 + 4 * f;
-                    const uint4 nw = noise_group(p.rk, grow, static_cast<uint32_t>(c4 >> 2));
+                    const uint4 nw = noise_group(rk, grow, static_cast<uint32_t>(c4 >> 2));
                     const uint32_t wmax = max(max(nw.x, nw.y), max(nw.z, nw.w));
                     const float mx = max4f(x4);
-                    const float emax = (rec.flags & kFRaw) ? ex2_ftz(fmaf(mx, rec.ls, -rec.cB))
-                                                           : ex2_ftz(fmaf(sq.exact(mx) - rec.B, kLog2e, kRaceSlack));
+                    const float emax = rawr ? ex2_ftz(fmaf(mx, rec.ls, -sr.cB))
+                                            : ex2_ftz(fmaf(sq.exact(mx) - sr.B, kLog2e, kRaceSlack));
                     if (one_minus_u_lower(wmax) <= emax) {
-                        const float4 e = race_e(x4, rec, sq);
+                        const float4 e = race_e(x4, rawr, rec.ls, sr, sq);
                         uint32_t bits = 0;
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             if (one_minus_u_lower(word_of(nw, q)) <= comp(e, q)) bits |= 1u << q;
                         if (bits) {
-                            const Best b2 = race_rescore(bits, x4, nw, c4, rec.bcol, sq, Best{wb, wc});
+                            const Best b2 = race_rescore(bits, x4, nw, c4, sr.bcol, sq, Best{wb, wc});
                             wb = b2.s;
                             wc = b2.c;
                         }
                     }
                 }
                 warp_best(wb, wc);
+                if (MULTI) __syncwarp();  // the list is rewritten for the next seed
+            }
+            if (lane == 0) {
+                best_s[par][st][sd][warp] = wb;
+                best_c[par][st][sd][warp] = wc;
+            }
             }
 
             if (topk) {
@@ -1010,26 +1068,29 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
                     topk_collect(km, stage, tid, col0, ncols, thr, sq, &tile_nk[par][st],
                                  p.keys + t * kTileKeys);
             }
-            if (lane == 0) {
-                best_s[par][st][warp] = wb;
-                best_c[par][st][warp] = wc;
-                best_a[par][st][warp] = acand;
-            }
+            if (lane == 0) best_a[par][st][warp] = acand;
         }
         if (!release_stage(&pp.count[st], lane)) continue;
 
-        // the last warp out: the tile's record, then refill the stage (the
-        // row record in it is read first)
-        float b = lane < kSWarps ? best_s[par][st][lane] : -INFINITY;
-        int bc = lane < kSWarps ? best_c[par][st][lane] : INT_MAX;
-        warp_best(b, bc);
+        // the last warp out: the tile's records (the row entry in the stage
+        // is read first), then refill the stage
+        if (stats || topk) {
+            const int nsd = MULTI ? p.n_seeds : 1;
+            for (int sd = 0; sd < nsd; ++sd) {
+                float b = lane < kSWarps ? best_s[par][st][sd][lane] : -INFINITY;
+                int bc = lane < kSWarps ? best_c[par][st][sd][lane] : INT_MAX;
+                warp_best(b, bc);
+                if (lane == 0) p.tb[t * p.n_seeds + sd] = TileSeed{b, bc};
+            }
+        }
         const int ac = warp_min_nonneg(lane < kSWarps ? best_a[par][st][lane] : INT_MAX);
         if (lane == 0) {
-            p.te[t] = TileEnd{b, bc, topk ? tile_nk[par][st] : 0, ac};
+            p.te[t] = TileEnd{topk ? tile_nk[par][st] : 0, ac};
             tile_nk[par][st] = 0;
         }
         __syncwarp();
-        pipe_advance(p, pp, n, p.list2, tiles, stage, &recs[st], p.rr, sizeof(RowRecord), tma, lane);
+        pipe_advance(p, pp, n, p.list1, tiles, stage, &recs[st][0], p.rr,
+                     static_cast<uint32_t>(p.rec_bytes), tma, lane);
     }
     pipe_end(pp);
 }
@@ -1041,31 +1102,34 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_cons
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int64_t li = static_cast<int64_t>(blockIdx.x) * kRowWarps + warp;
-    if (li >= p.hard[kCount2]) return;
-    const int64_t row = p.list2[li];
+    if (li >= p.hard[kCount1]) return;
+    const int64_t row = p.list1[li];
     const int G = p.tiles_per_row;
-    const RowRecord rec = p.rr[row];
+    const unsigned char* entry = p.rr + row * p.rec_bytes;
+    const RowRecord rec = *reinterpret_cast<const RowRecord*>(entry);
+    const SeedRec* seeds = reinterpret_cast<const SeedRec*>(entry + sizeof(RowRecord));
     const TileEnd* te = p.te + li * G;
     if (p.stats) {
         // argmax: the lowest column holding the raw max, or a lower one
-        // whose exact quotient ties it; the sample: the best of the tiles'
-        // race winners and B (greedy rows: the argmax)
+        // whose exact quotient ties it; per seed the sample: the best of the
+        // tiles' race winners and B (greedy rows: the argmax)
         int a = rec.arg;
-        float b = rec.B;
-        int bc = rec.bcol;
-        for (int c = lane; c < G; c += 32) {
-            const TileEnd e = te[c];
-            a = min(a, e.acol);
-            if (beats(e.b, e.col, b, bc)) {
-                b = e.b;
-                bc = e.col;
-            }
-        }
+        for (int c = lane; c < G; c += 32) a = min(a, te[c].acol);
         a = warp_min_nonneg(a);
-        warp_best(b, bc);
-        if (lane == 0) {
-            p.argmax[row] = a;
-            p.sample[row] = (rec.flags & kFNoisy) && b != -INFINITY ? bc : a;
+        if (lane == 0) p.argmax[row] = a;
+        for (int sd = 0; sd < p.n_seeds; ++sd) {
+            float b = seeds[sd].B;
+            int bc = seeds[sd].bcol;
+            for (int c = lane; c < G; c += 32) {
+                const TileSeed e = p.tb[(li * G + c) * p.n_seeds + sd];
+                if (beats(e.b, e.col, b, bc)) {
+                    b = e.b;
+                    bc = e.col;
+                }
+            }
+            warp_best(b, bc);
+            if (lane == 0)
+                p.sample[sd * p.rows + row] = (rec.flags & kFNoisy) && b != -INFINITY ? bc : a;
         }
     }
     if (!(rec.flags & kFTopk)) return;
@@ -1131,10 +1195,14 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_cons
 size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
 
 struct SplitLayout {
-    size_t hard, list1, list2, rt, ts, rr, te, keys, total;
+    size_t hard, list1, rt, ts, rr, te, tb, keys, total;
 };
 
-SplitLayout split_layout(int64_t rows, int64_t vocab, int32_t k) {
+size_t row_entry_bytes(int32_t n_seeds) {
+    return sizeof(RowRecord) + static_cast<size_t>(n_seeds) * sizeof(SeedRec);
+}
+
+SplitLayout split_layout(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds) {
     const size_t R = static_cast<size_t>(rows);
     const size_t G = static_cast<size_t>((vocab + kTileCols - 1) / kTileCols);
     SplitLayout l{};
@@ -1143,16 +1211,16 @@ SplitLayout split_layout(int64_t rows, int64_t vocab, int32_t k) {
     at += round_up(4 * (kHardOffset + R), kWorkspaceAlign);
     l.list1 = at;
     at += round_up(4 * R, kWorkspaceAlign);
-    l.list2 = at;
-    at += round_up(4 * R, kWorkspaceAlign);
     l.rt = at;
     at += round_up(sizeof(RowTemp) * R, kWorkspaceAlign);
     l.ts = at;
     at += round_up(sizeof(TileStats) * R * G, kWorkspaceAlign);
     l.rr = at;
-    at += round_up(sizeof(RowRecord) * R, kWorkspaceAlign);
+    at += round_up(row_entry_bytes(n_seeds) * R, kWorkspaceAlign);
     l.te = at;
     at += round_up(sizeof(TileEnd) * R * G, kWorkspaceAlign);
+    l.tb = at;
+    at += round_up(sizeof(TileSeed) * R * G * static_cast<size_t>(n_seeds), kWorkspaceAlign);
     l.keys = at;
     if (k > 0) at += round_up(8 * R * G * kTileKeys, kWorkspaceAlign);
     l.total = at;
@@ -1169,19 +1237,23 @@ int resident_grid(Kernel kernel, int threads, size_t smem) {
 
 }  // namespace
 
-size_t split_workspace_bytes(int64_t rows, int64_t vocab, int32_t k) {
-    return split_layout(rows, vocab, k).total;
+size_t split_workspace_bytes(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds) {
+    return split_layout(rows, vocab, k, n_seeds).total;
 }
+
+int32_t split_max_seeds() { return kMaxSeeds; }
 
 int32_t split_max_k() { return kSplitMaxK; }
 
 drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     if (c.rows <= 0) return DRS_OK;
     if (c.k > kSplitMaxK || c.vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
+    const int32_t n_seeds = c.seeds ? c.n_seeds : 1;
+    if (n_seeds < 1 || n_seeds > kMaxSeeds) return DRS_ERR_UNSUPPORTED;
     const int G = static_cast<int>((c.vocab + kTileCols - 1) / kTileCols);
     // tile indices of a pass are 32-bit, list lengths int
     if (c.rows > INT_MAX / G) return DRS_ERR_UNSUPPORTED;
-    const SplitLayout l = split_layout(c.rows, c.vocab, c.k);
+    const SplitLayout l = split_layout(c.rows, c.vocab, c.k, n_seeds);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     SplitParams p{};
     p.logits = c.logits;
@@ -1200,15 +1272,18 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     p.out_lp = c.out_lp;
     p.hard = reinterpret_cast<int32_t*>(ws + l.hard);
     p.list1 = reinterpret_cast<int32_t*>(ws + l.list1);
-    p.list2 = reinterpret_cast<int32_t*>(ws + l.list2);
     p.rt = reinterpret_cast<RowTemp*>(ws + l.rt);
     p.ts = reinterpret_cast<TileStats*>(ws + l.ts);
-    p.rr = reinterpret_cast<RowRecord*>(ws + l.rr);
+    p.rr = ws + l.rr;
     p.te = reinterpret_cast<TileEnd*>(ws + l.te);
+    p.tb = reinterpret_cast<TileSeed*>(ws + l.tb);
     p.keys = reinterpret_cast<uint64_t*>(ws + l.keys);
     p.err = device_error_flag();
     if (!p.err) return DRS_ERR_CUDA;
-    p.rk = PhiloxRoundKeys::of(c.seed);
+    for (int sd = 0; sd < n_seeds; ++sd)
+        p.rk[sd] = PhiloxRoundKeys::of(c.seeds ? c.seeds[sd] : c.seed);
+    p.n_seeds = n_seeds;
+    p.rec_bytes = static_cast<int>(row_entry_bytes(n_seeds));
     p.tiles_per_row = G;
     p.vocab = static_cast<int>(c.vocab);
     p.vec = aligned(c.logits, 16) && (c.row_stride % 4 == 0);
@@ -1218,17 +1293,20 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
                 (c.canvas_len <= static_cast<int64_t>(UINT32_MAX));
     p.stats = c.stats ? 1 : 0;
     p.k = c.k;
+    p.li_begin = 0;
+    p.li_end = -1;
     p.fault = take_injected_fault();
     // the header of the hard-row list: its count and the two list lengths
     if (cudaMemsetAsync(ws + l.hard, 0, 16, stream) != cudaSuccess) return DRS_ERR_CUDA;
     const size_t smem = kStages * kStageBytes;
+    auto pass2 = n_seeds > 1 ? split_pass2<true> : split_pass2<false>;
     if (cudaFuncSetAttribute(split_pass1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess ||
-        cudaFuncSetAttribute(split_pass2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(pass2, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return DRS_ERR_CUDA;
     const int g1 = resident_grid(split_pass1, kSThreads, smem);
-    const int g2 = resident_grid(split_pass2, kSThreads, smem);
+    const int g2 = resident_grid(pass2, kSThreads, smem);
     if (g1 < 1 || g2 < 1) return DRS_ERR_CUDA;
     const int64_t gp = (c.rows + 255) / 256;
     const int64_t gr = (c.rows + kRowWarps - 1) / kRowWarps;
@@ -1245,7 +1323,7 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     if (cudaGetLastError() != cudaSuccess || !mark(2)) return DRS_ERR_CUDA;
     split_merge<<<static_cast<int>(gr), kRowWarps * 32, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess || !mark(3)) return DRS_ERR_CUDA;
-    split_pass2<<<g2, kSThreads, smem, stream>>>(p);
+    pass2<<<g2, kSThreads, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess || !mark(4)) return DRS_ERR_CUDA;
     split_finish<<<static_cast<int>(gr), kRowWarps * 32, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess || !mark(5)) return DRS_ERR_CUDA;

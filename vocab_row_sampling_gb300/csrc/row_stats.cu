@@ -44,7 +44,7 @@ drs_status check_stats_args(const float* logits, int64_t rows, int64_t vocab, in
 drs_status run_topk(RowCall c, void* workspace, cudaStream_t stream) {
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     const int32_t* hard = reinterpret_cast<const int32_t*>(ws);
-    void* exact_ws = ws + split_workspace_bytes(c.rows, c.vocab, c.k > split_max_k() ? 0 : c.k);
+    void* exact_ws = ws + split_workspace_bytes(c.rows, c.vocab, c.k > split_max_k() ? 0 : c.k, 1);
     if (c.k > split_max_k()) {
         // larger k: the row statistics alone, then the exact kernel on every
         // converged row
@@ -74,7 +74,7 @@ extern "C" void drs_test_inject_fault(int code) { drs::g_inject_fault.store(code
 
 extern "C" size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab) {
     if (rows < 0 || vocab < 1) return 0;
-    return drs::split_workspace_bytes(rows, vocab, 0);
+    return drs::split_workspace_bytes(rows, vocab, 0, 1);
 }
 
 extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t vocab,
@@ -93,15 +93,46 @@ extern "C" drs_status drs_row_stats(const float* logits, int64_t rows, int64_t v
     const size_t need = drs_row_stats_workspace_bytes(rows, vocab);
     if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
         return DRS_ERR_INVALID_ARG;
-    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, seed, row0, argmax, sample,
-              entropy, probs_dtype, probs, probs_row_stride, nullptr, 0, nullptr, nullptr, true};
+    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, seed, nullptr, 1, row0, argmax,
+              sample, entropy, probs_dtype, probs, probs_row_stride, nullptr, 0, nullptr, nullptr,
+              true};
+    return split_rows(c, workspace, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t drs_row_stats_seeds_workspace_bytes(int64_t rows, int64_t vocab,
+                                                     int32_t n_seeds) {
+    if (rows < 0 || vocab < 1 || n_seeds < 1 || n_seeds > drs::split_max_seeds()) return 0;
+    return drs::split_workspace_bytes(rows, vocab, 0, n_seeds);
+}
+
+extern "C" drs_status drs_row_stats_seeds(const float* logits, int64_t rows, int64_t vocab,
+                                          int64_t row_stride, const float* temps,
+                                          int64_t canvas_len, const uint64_t* seeds,
+                                          int32_t n_seeds, int64_t row0, int64_t* argmax,
+                                          int64_t* samples, float* entropy,
+                                          drs_probs_dtype probs_dtype, void* probs,
+                                          int64_t probs_row_stride, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+    using namespace drs;
+    const drs_status chk = check_stats_args(logits, rows, vocab, row_stride, temps, canvas_len,
+                                            row0, argmax, samples, entropy, probs_dtype, probs,
+                                            probs_row_stride);
+    if (chk != DRS_OK) return chk;
+    if (!seeds || n_seeds < 1 || n_seeds > split_max_seeds()) return DRS_ERR_INVALID_ARG;
+    if (rows == 0) return DRS_OK;
+    const size_t need = drs_row_stats_seeds_workspace_bytes(rows, vocab, n_seeds);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
+        return DRS_ERR_INVALID_ARG;
+    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, seeds[0], seeds, n_seeds, row0,
+              argmax, samples, entropy, probs_dtype, probs, probs_row_stride, nullptr, 0, nullptr,
+              nullptr, true};
     return split_rows(c, workspace, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" size_t drs_row_stats_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k) {
     if (k <= 0 || rows < 0 || vocab < 1) return 0;
     const int32_t ks = k > drs::split_max_k() ? 0 : k;
-    return drs::split_workspace_bytes(rows, vocab, ks) + drs::exact_topk_workspace_bytes(k);
+    return drs::split_workspace_bytes(rows, vocab, ks, 1) + drs::exact_topk_workspace_bytes(k);
 }
 
 extern "C" drs_status drs_row_stats_topk(const float* logits, int64_t rows, int64_t vocab,
@@ -127,8 +158,9 @@ extern "C" drs_status drs_row_stats_topk(const float* logits, int64_t rows, int6
     const size_t need = drs_row_stats_topk_workspace_bytes(rows, vocab, k);
     if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
         return DRS_ERR_INVALID_ARG;
-    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, seed, row0, argmax, sample,
-              entropy, probs_dtype, probs, probs_row_stride, keep, k, out_ids, out_logprobs, true};
+    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, seed, nullptr, 1, row0, argmax,
+              sample, entropy, probs_dtype, probs, probs_row_stride, keep, k, out_ids, out_logprobs,
+              true};
     return run_topk(c, workspace, static_cast<cudaStream_t>(stream));
 }
 
@@ -153,8 +185,8 @@ extern "C" drs_status drs_topk_logprobs(const float* logits, int64_t rows, int64
     const size_t need = drs_topk_workspace_bytes(rows, vocab, k);
     if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
         return DRS_ERR_INVALID_ARG;
-    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, 0, 0, nullptr, nullptr,
-              nullptr, DRS_PROBS_NONE, nullptr, 0, keep, k, out_ids, out_logprobs, false};
+    RowCall c{logits, rows, vocab, row_stride, temps, canvas_len, 0, nullptr, 1, 0, nullptr,
+              nullptr, nullptr, DRS_PROBS_NONE, nullptr, 0, keep, k, out_ids, out_logprobs, false};
     return run_topk(c, workspace, static_cast<cudaStream_t>(stream));
 }
 
