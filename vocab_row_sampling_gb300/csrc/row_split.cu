@@ -509,6 +509,106 @@ __device__ __forceinline__ void tile_sums(const float4 (&v)[kSVec4], float lscal
     ww = warp_sum_f((wa[0] + wa[1]) + (wa[2] + wa[3])) * kLn2;
 }
 
+// One warp's share of a pass-1 tile: M_w's raw max and its lowest column,
+// S_w and W_w relative to it.
+__device__ __forceinline__ WarpPart p1_warp(const SplitParams& p, float4* stage, const ScaledQuotient& sq,
+                                            int row, int col0, int ncols, int tid, int lane, bool stats,
+                                            bool tma) {
+    float4 v[kSVec4];
+    read_tile(v, stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, ncols, tid, tma);
+
+    // max of the raw logits (division by Te > 0 keeps the order)
+    float m4[kSVec4];
+    float mt = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kSVec4; ++i) {
+        m4[i] = max4f(v[i]);
+        mt = fmaxf(mt, m4[i]);
+    }
+    const float mxw = warp_max_f(mt);
+    // the warp works on the raw logits while |M_w| < 256 for sure:
+    // |mxw * RN(1/Te)| < 255 bounds the exact quotient M_w (computed
+    // once per tile for all warps by the warp that finishes it)
+    const bool raw = fabsf(mxw * sq.y) < kRawLimit - 1.0f;
+
+    // the lowest column holding mxw (its exact quotient is M_w): the
+    // warp's Gumbel-max candidate, and the argmax unless a lower
+    // logit has the same exact quotient (pass 2 looks for those).
+    // The lane's first slot reaching mxw is read again from the stage.
+    int arg_t = INT_MAX;
+    if (stats && mt == mxw && mxw != -INFINITY) {
+        int i0 = 0;
+#pragma unroll
+        for (int i = kSVec4 - 1; i >= 0; --i)
+            if (m4[i] == mxw) i0 = i;
+        const int f = i0 * kSThreads + tid;
+        const float4 x4 = stage[f];
+        const int q = x4.x == mxw ? 0 : x4.y == mxw ? 1 : x4.z == mxw ? 2 : 3;
+        arg_t = col0 + 4 * f + q;
+    }
+    const int aw = stats ? warp_min_nonneg(arg_t) : INT_MAX;
+
+    // t = (s - M_w) log2(e): raw x * log2(e)/Te - c, c = RN(mxw *
+    // log2(e)/Te), else (s - M_w) * log2(e). Terms below 2^-126 of
+    // S >= 1 are flushed. A -inf logit (e = 0, t = -inf) makes W NaN:
+    // such warps sum again with t clamped to a finite value.
+    float lscale, cref;
+    if (raw) {
+        lscale = kLog2e * sq.y;
+        cref = mxw * lscale;
+    } else {
+        const float mw = sq.exact(mxw);
+#pragma unroll
+        for (int i = 0; i < kSVec4; ++i) {
+            v[i].x = sq.exact(v[i].x) - mw;
+            v[i].y = sq.exact(v[i].y) - mw;
+            v[i].z = sq.exact(v[i].z) - mw;
+            v[i].w = sq.exact(v[i].w) - mw;
+        }
+        lscale = kLog2e;
+        cref = 0.0f;
+    }
+    float sw = 0.0f, ww = 0.0f;  // a warp of -inf only: nothing to sum
+    if (mxw != -INFINITY) {
+        tile_sums<false>(v, lscale, cref, sw, ww);
+        if (isnan(ww)) tile_sums<true>(v, lscale, cref, sw, ww);
+    }
+    return WarpPart{0.0f, sw, ww, mxw, aw};
+}
+
+// The record of a pass-1 tile from its warps' parts (one lane each).
+__device__ __forceinline__ void p1_combine(const SplitParams& p, const WarpPart (&parts)[kSWarps],
+                                           const ScaledQuotient& sq, int64_t t, int col0, int ncols,
+                                           int lane) {
+    const bool hv = lane < kSWarps;
+    WarpPart wp = hv ? parts[lane] : WarpPart{-INFINITY, 0.0f, 0.0f, -INFINITY, INT_MAX};
+    wp.m = wp.xmax == -INFINITY ? -INFINITY : sq.exact(wp.xmax);  // M_w of each warp
+    const float mc = warp_max_f(wp.m);
+    float s_l = 0.0f, w_l = 0.0f;
+    if (wp.m != -INFINITY) {
+        const float dm = wp.m - mc;
+        const float f = ex2_approx(dm * kLog2e);
+        s_l = f * wp.s;
+        w_l = f * fmaf(dm, wp.s, wp.w);
+    }
+    const float s_c = warp_sum_f(s_l);
+    const float w_c = warp_sum_f(w_l);
+    const float xm = warp_max_f(wp.xmax);
+    const int a_c = xm == -INFINITY ? col0 : warp_min_nonneg(wp.xmax == xm ? wp.arg : INT_MAX);
+    TileStats* dst = p.ts + t;
+    if (hv) {
+        dst->wmax[lane] = lane * 128 < ncols ? ord32(wp.xmax) : 0u;
+        dst->wcol[lane] = wp.arg;
+    }
+    if (lane == 0) {
+        dst->m = mc;
+        dst->s = s_c;
+        dst->w = w_c;
+        dst->arg = a_c;
+        dst->xmax = xm;
+    }
+}
+
 __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __grid_constant__ SplitParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     float4* stages = reinterpret_cast<float4*>(smem);
@@ -542,100 +642,14 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
         sq.t = rts[st].qt;
         sq.y = rts[st].qy;
         sq.mode = rts[st].qmode;
-        {
-            float4 v[kSVec4];
-            read_tile(v, stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, ncols, tid, tma);
-
-            // max of the raw logits (division by Te > 0 keeps the order)
-            float m4[kSVec4];
-            float mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < kSVec4; ++i) {
-                m4[i] = max4f(v[i]);
-                mt = fmaxf(mt, m4[i]);
-            }
-            const float mxw = warp_max_f(mt);
-            // the warp works on the raw logits while |M_w| < 256 for sure:
-            // |mxw * RN(1/Te)| < 255 bounds the exact quotient M_w (computed
-            // once per tile for all warps by the warp that finishes it)
-            const bool raw = fabsf(mxw * sq.y) < kRawLimit - 1.0f;
-
-            // the lowest column holding mxw (its exact quotient is M_w): the
-            // warp's Gumbel-max candidate, and the argmax unless a lower
-            // logit has the same exact quotient (pass 2 looks for those).
-            // The lane's first slot reaching mxw is read again from the stage.
-            int arg_t = INT_MAX;
-            if (stats && mt == mxw && mxw != -INFINITY) {
-                int i0 = 0;
-#pragma unroll
-                for (int i = kSVec4 - 1; i >= 0; --i)
-                    if (m4[i] == mxw) i0 = i;
-                const int f = i0 * kSThreads + tid;
-                const float4 x4 = stage[f];
-                const int q = x4.x == mxw ? 0 : x4.y == mxw ? 1 : x4.z == mxw ? 2 : 3;
-                arg_t = col0 + 4 * f + q;
-            }
-            const int aw = stats ? warp_min_nonneg(arg_t) : INT_MAX;
-
-            // t = (s - M_w) log2(e): raw x * log2(e)/Te - c, c = RN(mxw *
-            // log2(e)/Te), else (s - M_w) * log2(e). Terms below 2^-126 of
-            // S >= 1 are flushed. A -inf logit (e = 0, t = -inf) makes W NaN:
-            // such warps sum again with t clamped to a finite value.
-            float lscale, cref;
-            if (raw) {
-                lscale = kLog2e * sq.y;
-                cref = mxw * lscale;
-            } else {
-                const float mw = sq.exact(mxw);
-#pragma unroll
-                for (int i = 0; i < kSVec4; ++i) {
-                    v[i].x = sq.exact(v[i].x) - mw;
-                    v[i].y = sq.exact(v[i].y) - mw;
-                    v[i].z = sq.exact(v[i].z) - mw;
-                    v[i].w = sq.exact(v[i].w) - mw;
-                }
-                lscale = kLog2e;
-                cref = 0.0f;
-            }
-            float sw = 0.0f, ww = 0.0f;  // a warp of -inf only: nothing to sum
-            if (mxw != -INFINITY) {
-                tile_sums<false>(v, lscale, cref, sw, ww);
-                if (isnan(ww)) tile_sums<true>(v, lscale, cref, sw, ww);
-            }
-            if (lane == 0) parts[par][st][warp] = WarpPart{0.0f, sw, ww, mxw, aw};
-        }
+        const WarpPart wp = p1_warp(p, stage, sq, row, col0, ncols, tid, lane, stats, tma);
+        if (lane == 0) parts[par][st][warp] = wp;
         if (!release_stage(&pp.count[st], lane)) continue;
 
         // the last warp out: refill the stage, then the tile's record (the
         // warps combined, one lane each)
         pipe_advance(p, pp, n, p.list1, tiles, stage, &rts[st], p.rt, sizeof(RowTemp), tma, lane);
-        const bool hv = lane < kSWarps;
-        WarpPart wp = hv ? parts[par][st][lane] : WarpPart{-INFINITY, 0.0f, 0.0f, -INFINITY, INT_MAX};
-        wp.m = wp.xmax == -INFINITY ? -INFINITY : sq.exact(wp.xmax);  // M_w of each warp
-        const float mc = warp_max_f(wp.m);
-        float s_l = 0.0f, w_l = 0.0f;
-        if (wp.m != -INFINITY) {
-            const float dm = wp.m - mc;
-            const float f = ex2_approx(dm * kLog2e);
-            s_l = f * wp.s;
-            w_l = f * fmaf(dm, wp.s, wp.w);
-        }
-        const float s_c = warp_sum_f(s_l);
-        const float w_c = warp_sum_f(w_l);
-        const float xm = warp_max_f(wp.xmax);
-        const int a_c = xm == -INFINITY ? col0 : warp_min_nonneg(wp.xmax == xm ? wp.arg : INT_MAX);
-        TileStats* dst = p.ts + t;
-        if (hv) {
-            dst->wmax[lane] = lane * 128 < ncols ? ord32(wp.xmax) : 0u;
-            dst->wcol[lane] = wp.arg;
-        }
-        if (lane == 0) {
-            dst->m = mc;
-            dst->s = s_c;
-            dst->w = w_c;
-            dst->arg = a_c;
-            dst->xmax = xm;
-        }
+        p1_combine(p, parts[par][st], sq, t, col0, ncols, lane);
     }
     pipe_end(pp);
 }
@@ -644,10 +658,11 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
 
 constexpr int kRowWarps = 8;  // rows per CTA of the merge and finish kernels
 
-__global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_constant__ SplitParams p) {
-    const int lane = threadIdx.x & 31;
-    const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
-    if (li >= list_end(p)) return;
+// The merge of list entry li by one warp: the row's M, S, W, argmax, the
+// warps' Gumbel-max candidates scored per seed (B), the top-k threshold, the
+// row record for pass 2, the entropy; rows without a threshold go on the
+// hard-row list.
+__device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int lane) {
     const int64_t row = p.list1[li];
     const uint64_t slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
     const bool kept = p.keep == nullptr || p.keep[slot] != 0;
@@ -788,6 +803,12 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
     }
 }
 
+__global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_constant__ SplitParams p) {
+    const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+    if (li >= list_end(p)) return;
+    merge_row(p, li, threadIdx.x & 31);
+}
+
 // ============================================================== pass 2
 
 // Probabilities 2^t of a tile, t = x ls - c2 (raw rows) or (s - M) log2(e) -
@@ -797,12 +818,30 @@ template <bool BF16, bool RAW>
 __device__ __forceinline__ void write_probs(const float4 (&v)[kSVec4], const RowRecord& rec,
                                             const ScaledQuotient& sq, uint16_t* prow, bool vec,
                                             int ncols, int tid) {
-    const bool full_tile = vec && ncols == kTileCols;
     const float ls = rec.ls, c2 = rec.c2, big_m = rec.M, l2s = rec.log2s;
+    // a whole tile with aligned rows: no per-slot checks (measured 6% of
+    // pass 2 against the same loop with the checks)
+    if (vec && ncols == kTileCols) {
+#pragma unroll
+        for (int i = 0; i < kSVec4; ++i) {
+            const int f = i * kSThreads + tid;
+            float pr[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float x = comp(v[i], q);
+                const float tq = RAW ? fmaf(x, ls, -c2) : fmaf(sq.exact(x) - big_m, kLog2e, -l2s);
+                pr[q] = ex2_approx(tq);
+            }
+            __stcs(reinterpret_cast<uint2*>(prow + 4 * f),
+                   make_uint2(pack2<BF16>(pr[0], pr[1]), pack2<BF16>(pr[2], pr[3])));
+        }
+        return;
+    }
+    // ragged tiles and rows without aligned 8-byte stores
 #pragma unroll
     for (int i = 0; i < kSVec4; ++i) {
         const int f = i * kSThreads + tid;
-        if (!full_tile && 4 * f >= ncols) continue;
+        if (4 * f >= ncols) continue;
         float pr[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -812,7 +851,7 @@ __device__ __forceinline__ void write_probs(const float4 (&v)[kSVec4], const Row
         }
         const uint32_t lo = pack2<BF16>(pr[0], pr[1]);
         const uint32_t hi = pack2<BF16>(pr[2], pr[3]);
-        if (full_tile || (vec && 4 * f + 4 <= ncols)) {
+        if (vec && 4 * f + 4 <= ncols) {
             __stcs(reinterpret_cast<uint2*>(prow + 4 * f), make_uint2(lo, hi));
         } else {
             const uint16_t code[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
@@ -899,20 +938,190 @@ __device__ __noinline__ void topk_collect(uint32_t smask, const float4* stage, i
     }
 }
 
-// MULTI: several noise seeds (a race per seed); else one, its round keys
-// read as constants.
+// Shared memory of the pass-2 tile work: the race lists of the warps, and
+// per tile in flight (parity of the tile's round, stage) the warps' race
+// winners per seed, argmax ties and the tile's candidate count.
+template <bool MULTI>
+struct P2Shared {
+    static constexpr int kSeedSlots = MULTI ? kMaxSeeds : 1;
+    uint16_t race_at[kSWarps][kSVec4 * 32];
+    float best_s[2][kStages][kSeedSlots][kSWarps];
+    int best_c[2][kStages][kSeedSlots][kSWarps];
+    int best_a[2][kStages][kSWarps];
+    int tile_nk[2][kStages];
+};
+
+// One warp's share of a pass-2 tile (the row entry at `entry`: RowRecord,
+// then one SeedRec per seed). Returns whether the row collects top-k
+// candidates. MULTI: several noise seeds (a race per seed); else one, its
+// round keys read as constants.
+template <bool MULTI>
+__device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& sh, float4* stage,
+                                        const unsigned char* entry, int row, int64_t t, int col0,
+                                        int ncols, int st, int par, int tid, int lane, int warp,
+                                        bool stats, bool probs, bool tma) {
+    const RowRecord& rec = *reinterpret_cast<const RowRecord*>(entry);
+    const SeedRec* seeds = reinterpret_cast<const SeedRec*>(entry + sizeof(RowRecord));
+    const int flags = rec.flags;
+    const bool noisy = (flags & kFNoisy) != 0;
+    const bool topk = (flags & kFTopk) != 0;
+    // (a row of a top-k-only call without a threshold, which the exact
+    // kernel takes, runs through here with nothing to produce: it is
+    // rare, and a branch around the block slowed every tile)
+    {
+        const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
+        ScaledQuotient sq;
+        sq.t = rec.qt;
+        sq.y = rec.qy;
+        sq.mode = rec.qmode;
+        float4 v[kSVec4];
+        read_tile(v, stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, ncols, tid, tma);
+
+        if (probs) {
+            uint16_t* prow = static_cast<uint16_t*>(p.probs) + static_cast<int64_t>(row) * p.probs_row_stride + col0;
+            if (p.probs_dtype == 1) probs_of_tile<true>(v, rec, sq, prow, p.probs_vec != 0, ncols, tid);
+            else probs_of_tile<false>(v, rec, sq, prow, p.probs_vec != 0, ncols, tid);
+        }
+
+        float m4[kSVec4];
+#pragma unroll
+        for (int i = 0; i < kSVec4; ++i) m4[i] = max4f(v[i]);
+
+        // argmax: logits below the raw max whose exact quotient is M
+        // (rare: the float4s reaching the bound are read again from the
+        // stage); the lowest column of the thread, then of the warp
+        int acand = INT_MAX;
+        if (stats && rec.M != -INFINITY) {
+            const float cthr = rec.cthr;
+            uint32_t am = 0;
+#pragma unroll
+            for (int i = 0; i < kSVec4; ++i) am |= (m4[i] >= cthr ? 1u : 0u) << i;
+#pragma unroll 1
+            while (am && acand == INT_MAX) {
+                const int f = (__ffs(am) - 1) * kSThreads + tid;
+                am &= am - 1;
+                const float4 x4 = stage[f];
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    const float x = comp(x4, q);
+                    if (4 * f + q < ncols && x >= cthr && sq.exact(x) == rec.M) {
+                        acand = col0 + 4 * f + q;
+                        break;
+                    }
+                }
+            }
+            acand = warp_min_nonneg(acand);
+        }
+
+        // the race, once per seed
+        const bool rawr = (flags & kFRaw) != 0;
+        const int nsd = MULTI ? p.n_seeds : 1;
+        for (int sd = 0; sd < nsd; ++sd) {
+        const SeedRec sr = seeds[sd];
+        const PhiloxRoundKeys& rk = MULTI ? p.rk[sd] : p.rk[0];
+        float wb = sr.B;
+        int wc = sr.bcol;
+        if (noisy) {
+            // groups whose largest e^(s - B) reaches 2^-24, listed
+            // warp-wide by their float4 index in the stage
+            uint32_t pass = 0;
+            if (rawr) {
+                const float ls = rec.ls, cB = sr.cB;
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i)
+                    if (fmaf(m4[i], ls, -cB) >= -24.0f) pass |= 1u << i;
+            } else {
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i)
+                    if (fmaf(sq.exact(m4[i]) - sr.B, kLog2e, kRaceSlack) >= -24.0f) pass |= 1u << i;
+            }
+            const uint32_t lt = lanemask_lt();
+            int total = 0;
+#pragma unroll
+            for (int i = 0; i < kSVec4; ++i) {
+                const bool on = (pass >> i) & 1u;
+                const uint32_t bl = __ballot_sync(0xffffffffu, on);
+                if (on) sh.race_at[warp][total + __popc(bl & lt)] = static_cast<uint16_t>(i * kSThreads + tid);
+                total += __popc(bl);
+            }
+            __syncwarp();
+            // each listed group: its noise, then the group's largest e
+            // against its largest word (one 2^x); the elements one by
+            // one only when that passes
+            for (int m = lane; m < total; m += 32) {
+                const int f = sh.race_at[warp][m];
+                const float4 x4 = stage[f];
+                const int c4 = col0 + 4 * f;
+                const uint4 nw = noise_group(rk, grow, static_cast<uint32_t>(c4 >> 2));
+                const uint32_t wmax = max(max(nw.x, nw.y), max(nw.z, nw.w));
+                const float mx = max4f(x4);
+                const float emax = rawr ? ex2_ftz(fmaf(mx, rec.ls, -sr.cB))
+                                        : ex2_ftz(fmaf(sq.exact(mx) - sr.B, kLog2e, kRaceSlack));
+                if (one_minus_u_lower(wmax) <= emax) {
+                    const float4 e = race_e(x4, rawr, rec.ls, sr, sq);
+                    uint32_t bits = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (one_minus_u_lower(word_of(nw, q)) <= comp(e, q)) bits |= 1u << q;
+                    if (bits) {
+                        const Best b2 = race_rescore(bits, x4, nw, c4, sr.bcol, sq, Best{wb, wc});
+                        wb = b2.s;
+                        wc = b2.c;
+                    }
+                }
+            }
+            warp_best(wb, wc);
+            if (MULTI) __syncwarp();  // the list is rewritten for the next seed
+        }
+        if (lane == 0) {
+            sh.best_s[par][st][sd][warp] = wb;
+            sh.best_c[par][st][sd][warp] = wc;
+        }
+        }
+
+        if (topk) {
+            // candidates x >= thr (rare: the slots reaching it)
+            const float thr = rec.thr;
+            uint32_t km = 0;
+#pragma unroll
+            for (int i = 0; i < kSVec4; ++i) km |= (m4[i] >= thr ? 1u : 0u) << i;
+            if (km)
+                topk_collect(km, stage, tid, col0, ncols, thr, sq, &sh.tile_nk[par][st],
+                             p.keys + t * kTileKeys);
+        }
+        if (lane == 0) sh.best_a[par][st][warp] = acand;
+    }
+    return topk;
+}
+
+// The last warp out of a pass-2 tile: the tile's records (race winner per
+// seed, candidate count, argmax tie).
+template <bool MULTI>
+__device__ __forceinline__ void p2_combine(const SplitParams& p, P2Shared<MULTI>& sh, int64_t t, int st,
+                                           int par, bool stats, bool topk, int lane) {
+    if (stats || topk) {
+        const int nsd = MULTI ? p.n_seeds : 1;
+        for (int sd = 0; sd < nsd; ++sd) {
+            float b = lane < kSWarps ? sh.best_s[par][st][sd][lane] : -INFINITY;
+            int bc = lane < kSWarps ? sh.best_c[par][st][sd][lane] : INT_MAX;
+            warp_best(b, bc);
+            if (lane == 0) p.tb[t * p.n_seeds + sd] = TileSeed{b, bc};
+        }
+    }
+    const int ac = warp_min_nonneg(lane < kSWarps ? sh.best_a[par][st][lane] : INT_MAX);
+    if (lane == 0) {
+        p.te[t] = TileEnd{topk ? sh.tile_nk[par][st] : 0, ac};
+        sh.tile_nk[par][st] = 0;
+    }
+}
+
 template <bool MULTI>
 __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __grid_constant__ SplitParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     float4* stages = reinterpret_cast<float4*>(smem);
     __shared__ Pipe pp;
     __shared__ __align__(16) unsigned char recs[kStages][kRowEntryMax];
-    __shared__ uint16_t race_at[kSWarps][kSVec4 * 32];
-    constexpr int kSeedSlots = MULTI ? kMaxSeeds : 1;
-    __shared__ float best_s[2][kStages][kSeedSlots][kSWarps];
-    __shared__ int best_c[2][kStages][kSeedSlots][kSWarps];
-    __shared__ int best_a[2][kStages][kSWarps];
-    __shared__ int tile_nk[2][kStages];
+    __shared__ P2Shared<MULTI> sh;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -920,7 +1129,7 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
     const bool probs = stats && p.probs_dtype != 0;
     const bool tma = p.vec != 0;
     const TileRange tiles = launch_tiles(p);
-    if (tid < 2 * kStages) tile_nk[tid / kStages][tid % kStages] = 0;
+    if (tid < 2 * kStages) sh.tile_nk[tid / kStages][tid % kStages] = 0;
     pipe_start(p, pp, p.list1, tiles, stages, &recs[0][0], kRowEntryMax, p.rr,
                static_cast<uint32_t>(p.rec_bytes), tma);
     for (int n = 0;; ++n) {
@@ -939,155 +1148,13 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
         const int64_t t = tiles.t_begin + static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
         const int col0 = pp.col[n % kMap] * kTileCols;
         const int ncols = min(p.vocab - col0, kTileCols);
-        const RowRecord& rec = *reinterpret_cast<const RowRecord*>(&recs[st][0]);
-        const SeedRec* seeds = reinterpret_cast<const SeedRec*>(&recs[st][sizeof(RowRecord)]);
-        const int flags = rec.flags;
-        const bool noisy = (flags & kFNoisy) != 0;
-        const bool topk = (flags & kFTopk) != 0;
-        // (a row of a top-k-only call without a threshold, which the exact
-        // kernel takes, runs through here with nothing to produce: it is
-        // rare, and a branch around the block slowed every tile)
-        {
-            const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
-            ScaledQuotient sq;
-            sq.t = rec.qt;
-            sq.y = rec.qy;
-            sq.mode = rec.qmode;
-            float4 v[kSVec4];
-            read_tile(v, stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, ncols, tid, tma);
-
-            if (probs) {
-                uint16_t* prow = static_cast<uint16_t*>(p.probs) + static_cast<int64_t>(row) * p.probs_row_stride + col0;
-                if (p.probs_dtype == 1) probs_of_tile<true>(v, rec, sq, prow, p.probs_vec != 0, ncols, tid);
-                else probs_of_tile<false>(v, rec, sq, prow, p.probs_vec != 0, ncols, tid);
-            }
-
-            float m4[kSVec4];
-#pragma unroll
-            for (int i = 0; i < kSVec4; ++i) m4[i] = max4f(v[i]);
-
-            // argmax: logits below the raw max whose exact quotient is M
-            // (rare: the float4s reaching the bound are read again from the
-            // stage); the lowest column of the thread, then of the warp
-            int acand = INT_MAX;
-            if (stats && rec.M != -INFINITY) {
-                const float cthr = rec.cthr;
-                uint32_t am = 0;
-#pragma unroll
-                for (int i = 0; i < kSVec4; ++i) am |= (m4[i] >= cthr ? 1u : 0u) << i;
-#pragma unroll 1
-                while (am && acand == INT_MAX) {
-                    const int f = (__ffs(am) - 1) * kSThreads + tid;
-                    am &= am - 1;
-                    const float4 x4 = stage[f];
-#pragma unroll 1
-                    for (int q = 0; q < 4; ++q) {
-                        const float x = comp(x4, q);
-                        if (4 * f + q < ncols && x >= cthr && sq.exact(x) == rec.M) {
-                            acand = col0 + 4 * f + q;
-                            break;
-                        }
-                    }
-                }
-                acand = warp_min_nonneg(acand);
-            }
-
-            // the race, once per seed
-            const bool rawr = (flags & kFRaw) != 0;
-            const int nsd = MULTI ? p.n_seeds : 1;
-            for (int sd = 0; sd < nsd; ++sd) {
-            const SeedRec sr = seeds[sd];
-            const PhiloxRoundKeys& rk = MULTI ? p.rk[sd] : p.rk[0];
-            float wb = sr.B;
-            int wc = sr.bcol;
-            if (noisy) {
-                // groups whose largest e^(s - B) reaches 2^-24, listed
-                // warp-wide by their float4 index in the stage
-                uint32_t pass = 0;
-                if (rawr) {
-                    const float ls = rec.ls, cB = sr.cB;
-#pragma unroll
-                    for (int i = 0; i < kSVec4; ++i)
-                        if (fmaf(m4[i], ls, -cB) >= -24.0f) pass |= 1u << i;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < kSVec4; ++i)
-                        if (fmaf(sq.exact(m4[i]) - sr.B, kLog2e, kRaceSlack) >= -24.0f) pass |= 1u << i;
-                }
-                const uint32_t lt = lanemask_lt();
-                int total = 0;
-#pragma unroll
-                for (int i = 0; i < kSVec4; ++i) {
-                    const bool on = (pass >> i) & 1u;
-                    const uint32_t bl = __ballot_sync(0xffffffffu, on);
-                    if (on) race_at[warp][total + __popc(bl & lt)] = static_cast<uint16_t>(i * kSThreads + tid);
-                    total += __popc(bl);
-                }
-                __syncwarp();
-                // each listed group: its noise, then the group's largest e
-                // against its largest word (one 2^x); the elements one by
-                // one only when that passes
-                for (int m = lane; m < total; m += 32) {
-                    const int f = race_at[warp][m];
-                    const float4 x4 = stage[f];
-                    const int c4 = col0 + 4 * f;
-                    const uint4 nw = noise_group(rk, grow, static_cast<uint32_t>(c4 >> 2));
-                    const uint32_t wmax = max(max(nw.x, nw.y), max(nw.z, nw.w));
-                    const float mx = max4f(x4);
-                    const float emax = rawr ? ex2_ftz(fmaf(mx, rec.ls, -sr.cB))
-                                            : ex2_ftz(fmaf(sq.exact(mx) - sr.B, kLog2e, kRaceSlack));
-                    if (one_minus_u_lower(wmax) <= emax) {
-                        const float4 e = race_e(x4, rawr, rec.ls, sr, sq);
-                        uint32_t bits = 0;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (one_minus_u_lower(word_of(nw, q)) <= comp(e, q)) bits |= 1u << q;
-                        if (bits) {
-                            const Best b2 = race_rescore(bits, x4, nw, c4, sr.bcol, sq, Best{wb, wc});
-                            wb = b2.s;
-                            wc = b2.c;
-                        }
-                    }
-                }
-                warp_best(wb, wc);
-                if (MULTI) __syncwarp();  // the list is rewritten for the next seed
-            }
-            if (lane == 0) {
-                best_s[par][st][sd][warp] = wb;
-                best_c[par][st][sd][warp] = wc;
-            }
-            }
-
-            if (topk) {
-                // candidates x >= thr (rare: the slots reaching it)
-                const float thr = rec.thr;
-                uint32_t km = 0;
-#pragma unroll
-                for (int i = 0; i < kSVec4; ++i) km |= (m4[i] >= thr ? 1u : 0u) << i;
-                if (km)
-                    topk_collect(km, stage, tid, col0, ncols, thr, sq, &tile_nk[par][st],
-                                 p.keys + t * kTileKeys);
-            }
-            if (lane == 0) best_a[par][st][warp] = acand;
-        }
+        const bool topk = p2_warp<MULTI>(p, sh, stage, &recs[st][0], row, t, col0, ncols, st, par, tid, lane,
+                                         warp, stats, probs, tma);
         if (!release_stage(&pp.count[st], lane)) continue;
 
         // the last warp out: the tile's records (the row entry in the stage
         // is read first), then refill the stage
-        if (stats || topk) {
-            const int nsd = MULTI ? p.n_seeds : 1;
-            for (int sd = 0; sd < nsd; ++sd) {
-                float b = lane < kSWarps ? best_s[par][st][sd][lane] : -INFINITY;
-                int bc = lane < kSWarps ? best_c[par][st][sd][lane] : INT_MAX;
-                warp_best(b, bc);
-                if (lane == 0) p.tb[t * p.n_seeds + sd] = TileSeed{b, bc};
-            }
-        }
-        const int ac = warp_min_nonneg(lane < kSWarps ? best_a[par][st][lane] : INT_MAX);
-        if (lane == 0) {
-            p.te[t] = TileEnd{topk ? tile_nk[par][st] : 0, ac};
-            tile_nk[par][st] = 0;
-        }
+        p2_combine<MULTI>(p, sh, t, st, par, stats, topk, lane);
         __syncwarp();
         pipe_advance(p, pp, n, p.list1, tiles, stage, &recs[st][0], p.rr,
                      static_cast<uint32_t>(p.rec_bytes), tma, lane);
@@ -1299,6 +1366,14 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     // the header of the hard-row list: its count and the two list lengths
     if (cudaMemsetAsync(ws + l.hard, 0, 16, stream) != cudaSuccess) return DRS_ERR_CUDA;
     const size_t smem = kStages * kStageBytes;
+    const int64_t gp = (c.rows + 255) / 256;
+    const int64_t gr = (c.rows + kRowWarps - 1) / kRowWarps;
+    if (gr > INT_MAX) return DRS_ERR_UNSUPPORTED;
+    // with kernel timing on, an event before each kernel and after the last
+    const int slot = kernel_timer_slot();
+    auto mark = [&](int i) {
+        return slot < 0 || cudaEventRecord(kernel_timer_event(slot, i), stream) == cudaSuccess;
+    };
     auto pass2 = n_seeds > 1 ? split_pass2<true> : split_pass2<false>;
     if (cudaFuncSetAttribute(split_pass1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess ||
@@ -1308,14 +1383,6 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     const int g1 = resident_grid(split_pass1, kSThreads, smem);
     const int g2 = resident_grid(pass2, kSThreads, smem);
     if (g1 < 1 || g2 < 1) return DRS_ERR_CUDA;
-    const int64_t gp = (c.rows + 255) / 256;
-    const int64_t gr = (c.rows + kRowWarps - 1) / kRowWarps;
-    if (gr > INT_MAX) return DRS_ERR_UNSUPPORTED;
-    // with kernel timing on, an event before each kernel and after the last
-    const int slot = kernel_timer_slot();
-    auto mark = [&](int i) {
-        return slot < 0 || cudaEventRecord(kernel_timer_event(slot, i), stream) == cudaSuccess;
-    };
     if (!mark(0)) return DRS_ERR_CUDA;
     split_prep<<<static_cast<int>(gp), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess || !mark(1)) return DRS_ERR_CUDA;
