@@ -609,7 +609,13 @@ __device__ __forceinline__ void p1_combine(const SplitParams& p, const WarpPart 
     }
 }
 
+// Pass 1, the merge, pass 2 and the finish are launched as programmatic
+// dependents: each may be scheduled while its predecessor drains, waits for
+// it to complete (griddepcontrol.wait, a no-op without the launch attribute)
+// before anything else, and lets its own dependent launch once a CTA's work
+// is done.
 __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __grid_constant__ SplitParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ __align__(128) unsigned char smem[];
     float4* stages = reinterpret_cast<float4*>(smem);
     __shared__ Pipe pp;
@@ -651,6 +657,7 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
         pipe_advance(p, pp, n, p.list1, tiles, stage, &rts[st], p.rt, sizeof(RowTemp), tma, lane);
         p1_combine(p, parts[par][st], sq, t, col0, ncols, lane);
     }
+    asm volatile("griddepcontrol.launch_dependents;");
     pipe_end(pp);
 }
 
@@ -804,9 +811,11 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
 }
 
 __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_constant__ SplitParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
     if (li >= list_end(p)) return;
     merge_row(p, li, threadIdx.x & 31);
+    asm volatile("griddepcontrol.launch_dependents;");
 }
 
 // ============================================================== pass 2
@@ -986,6 +995,11 @@ __device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& s
         float m4[kSVec4];
 #pragma unroll
         for (int i = 0; i < kSVec4; ++i) m4[i] = max4f(v[i]);
+        // the thread's max: most threads hold nothing that reaches the
+        // argmax or top-k bounds and skip both per-slot tests
+        float mthr = m4[0];
+#pragma unroll
+        for (int i = 1; i < kSVec4; ++i) mthr = fmaxf(mthr, m4[i]);
 
         // argmax: logits below the raw max whose exact quotient is M
         // (rare: the float4s reaching the bound are read again from the
@@ -994,8 +1008,10 @@ __device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& s
         if (stats && rec.M != -INFINITY) {
             const float cthr = rec.cthr;
             uint32_t am = 0;
+            if (mthr >= cthr) {
 #pragma unroll
-            for (int i = 0; i < kSVec4; ++i) am |= (m4[i] >= cthr ? 1u : 0u) << i;
+                for (int i = 0; i < kSVec4; ++i) am |= (m4[i] >= cthr ? 1u : 0u) << i;
+            }
 #pragma unroll 1
             while (am && acand == INT_MAX) {
                 const int f = (__ffs(am) - 1) * kSThreads + tid;
@@ -1079,7 +1095,7 @@ __device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& s
         }
         }
 
-        if (topk) {
+        if (topk && mthr >= rec.thr) {
             // candidates x >= thr (rare: the slots reaching it)
             const float thr = rec.thr;
             uint32_t km = 0;
@@ -1117,6 +1133,7 @@ __device__ __forceinline__ void p2_combine(const SplitParams& p, P2Shared<MULTI>
 
 template <bool MULTI>
 __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __grid_constant__ SplitParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ __align__(128) unsigned char smem[];
     float4* stages = reinterpret_cast<float4*>(smem);
     __shared__ Pipe pp;
@@ -1159,12 +1176,14 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
         pipe_advance(p, pp, n, p.list1, tiles, stage, &recs[st][0], p.rr,
                      static_cast<uint32_t>(p.rec_bytes), tma, lane);
     }
+    asm volatile("griddepcontrol.launch_dependents;");
     pipe_end(pp);
 }
 
 // ============================================================== finish
 
 __global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_constant__ SplitParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ uint64_t keys[kRowWarps][kRowKeys];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -1386,14 +1405,25 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     if (!mark(0)) return DRS_ERR_CUDA;
     split_prep<<<static_cast<int>(gp), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess || !mark(1)) return DRS_ERR_CUDA;
-    split_pass1<<<g1, kSThreads, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess || !mark(2)) return DRS_ERR_CUDA;
-    split_merge<<<static_cast<int>(gr), kRowWarps * 32, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess || !mark(3)) return DRS_ERR_CUDA;
-    pass2<<<g2, kSThreads, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess || !mark(4)) return DRS_ERR_CUDA;
-    split_finish<<<static_cast<int>(gr), kRowWarps * 32, 0, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess || !mark(5)) return DRS_ERR_CUDA;
+    // pass 1, merge, pass 2 and finish may launch while their predecessor
+    // drains (each waits for it before its first access)
+    auto pdl = [&](auto kernel, int grid, int block, size_t dsmem) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(block);
+        cfg.dynamicSmemBytes = dsmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess;
+    };
+    if (!pdl(split_pass1, g1, kSThreads, smem) || !mark(2)) return DRS_ERR_CUDA;
+    if (!pdl(split_merge, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(3)) return DRS_ERR_CUDA;
+    if (!pdl(pass2, g2, kSThreads, smem) || !mark(4)) return DRS_ERR_CUDA;
+    if (!pdl(split_finish, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(5)) return DRS_ERR_CUDA;
     return DRS_OK;
 }
 
