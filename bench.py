@@ -47,7 +47,12 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 METRIC = "rows/s and achieved HBM GB/s (% of roofline) for row_stats at 2048x262144 fp32"
-WORKLOAD = "step"
+WORKLOAD = "step"  # set from --workload
+WORKLOAD_TEXT = {
+    "step": "step: 2048 x 262144 fp32 logits, bf16 probs, top-k 20 on the even (converged) slots",
+    "wide": "wide: 512 x 2097152 fp32 logits (the step recipe on rows of 2^21 columns), bf16 "
+            "probs, top-k 20 on the even (converged) slots; not the headline workload",
+}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -302,11 +307,11 @@ def _run_ours(args, world, rank, local):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
            "data": "synthetic (seeded N(0,3^2) + one +8 spike per row, temps U[0.5,1.5])",
-           "config": {"workload": "step: 2048 x 262144 fp32 logits, bf16 probs, top-k 20 on "
-                                  "the even (converged) slots",
+           "config": {"workload": WORKLOAD_TEXT[WORKLOAD],
                       "rows": rows, "vocab": V, "row_stride": stride, "k": k,
                       "kept_rows": kept_rows,
-                      "l2": "inputs (2.1 GB) larger than L2 (126 MB); no flush"},
+                      "l2": f"inputs ({rows * V * 4 / 1e9:.1f} GB) larger than L2 (126 MB); "
+                            "no flush"},
            "roofline": roofline,
            "kernels": {"row_stats_topk": {"avg_ms": round(rs_avg_ms, 4),
                                           "rows_per_s": round(rows / (rs_avg_ms / 1e3), 1),
@@ -335,7 +340,7 @@ def _run_ours(args, world, rank, local):
     if not args.no_e2e:
         out["e2e"] = _e2e(args, drs, w, rank, world, row0, temps_all, keep_all, k)
     if rows != workloads.WORKLOADS[WORKLOAD].rows:
-        out["config"]["workload"] = (f"step recipe at {rows} x {V} (a smaller case, "
+        out["config"]["workload"] = (f"{WORKLOAD} recipe at {rows} x {V} (a smaller case, "
                                      "not the headline workload)")
         out["config"]["l2"] = "no flush"
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
@@ -456,7 +461,7 @@ def _cpu_baseline(logits_dev, w, seconds=15.0, threads=None):
         done += sel.size
     el = time.perf_counter() - t0
     return {"value": round(done / el, 2), "unit": "rows/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {done} rows of the step batch (row stats + top-k of kept rows), "
+            "sample": f"first {done} rows of the {WORKLOAD} batch (row stats + top-k of kept rows), "
                       f"{el:.1f} s wall"}
 
 
@@ -517,7 +522,11 @@ def main():
     ap.add_argument("--rows", type=int, default=None,
                     help="rows per GPU (multiple of the canvas length); default: the full batch")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--workload", default="step", choices=sorted(WORKLOAD_TEXT),
+                    help="step (the headline) or wide (rows of 2^21 columns)")
     args = ap.parse_args()
+    global WORKLOAD
+    WORKLOAD = args.workload
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -47,8 +47,8 @@ typedef enum drs_probs_dtype {
     DRS_PROBS_FP16 = 2
 } drs_probs_dtype;
 
-/* Largest vocabulary (row length) the kernels accept. */
-#define DRS_MAX_VOCAB 491520
+/* Largest vocabulary (row length) the kernels accept (2^21). */
+#define DRS_MAX_VOCAB 2097152
 
 /*
  * Bytes of device workspace drs_row_stats needs (at least 256-byte aligned,

@@ -107,12 +107,14 @@ def test_repeated_calls_are_deterministic():
             assert np.array_equal(one[k], again[k]), k
 
 
-@pytest.mark.parametrize("which", ["400000", "max"])
+@pytest.mark.parametrize("which", ["400000", "491520", "491521", "1000003", "max"])
 def test_long_rows(which):
     """Rows of many tiles with a ragged last one: 400000 columns (49 tiles,
-    the last 6784 wide) and the largest supported vocabulary (60 tiles)."""
+    the last 6784 wide); 60 tiles, the longest rows of the merge's short-row
+    instantiation, and one column more (61 tiles, the last one column wide);
+    1000003 columns; the largest supported vocabulary (256 tiles)."""
     import vocab_row_sampling_gb300 as drs
-    vocab = 400000 if which == "400000" else drs.DRS_MAX_VOCAB
+    vocab = drs.DRS_MAX_VOCAB if which == "max" else int(which)
     rng = np.random.default_rng(1)
     x = (rng.standard_normal((3, vocab)) * 3).astype(np.float32)
     x[2, vocab - 1] = 40.0

@@ -29,7 +29,7 @@ DRS_ERR_CUDA = -3
 DRS_ERR_DEVICE_TIMEOUT = -4
 
 DRS_PROBS_NONE, DRS_PROBS_BF16, DRS_PROBS_FP16 = 0, 1, 2
-DRS_MAX_VOCAB = 491520
+DRS_MAX_VOCAB = 2097152
 
 EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_row_stats_noalloc",
             "drs_row_stats_topk", "drs_row_stats_topk_workspace_bytes", "drs_topk_logprobs",

@@ -82,7 +82,12 @@ constexpr int kSWarps = kSThreads / 32;
 constexpr int kSVec4 = DRS_SPLIT_VEC4;             // float4 slots per thread
 constexpr int kTileCols = kSThreads * kSVec4 * 4;  // 8192
 constexpr int kMaxTiles = (DRS_MAX_VOCAB + kTileCols - 1) / kTileCols;
-constexpr int kOrdPerLane = (kMaxTiles * kSWarps + 31) / 32;
+// warp maxima per lane in the merge: rows of up to 60 tiles (491520
+// columns), and the longest rows
+constexpr int kOrdSmall = (60 * kSWarps + 31) / 32;
+constexpr int kOrdLarge = (kMaxTiles * kSWarps + 31) / 32;
+constexpr int kTilesSmall = (60 + 31) / 32;  // tiles per lane in the finish
+constexpr int kTilesLarge = (kMaxTiles + 31) / 32;
 constexpr int kStages = DRS_SPLIT_STAGES;          // tiles in flight per CTA
 constexpr int kStageF4 = kTileCols / 4;             // float4 per stage
 constexpr size_t kStageBytes = kTileCols * 4;       // 32 KiB
@@ -669,6 +674,7 @@ constexpr int kRowWarps = 8;  // rows per CTA of the merge and finish kernels
 // warps' Gumbel-max candidates scored per seed (B), the top-k threshold, the
 // row record for pass 2, the entropy; rows without a threshold go on the
 // hard-row list.
+template <int NU>
 __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int lane) {
     const int64_t row = p.list1[li];
     const uint64_t slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
@@ -719,9 +725,9 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
         // the k-th largest of the row's warp maxima (absent warps are 0,
         // below every value): k rounds of a warp max, each removing one
         // occurrence
-        uint32_t o[kOrdPerLane];
+        uint32_t o[NU];
 #pragma unroll
-        for (int u = 0; u < kOrdPerLane; ++u) {
+        for (int u = 0; u < NU; ++u) {
             const int jx = lane + 32 * u;
             o[u] = jx < kSWarps * G ? tr[jx / kSWarps].wmax[jx % kSWarps] : 0u;
         }
@@ -729,7 +735,7 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
         for (int r = 0; r < p.k; ++r) {
             uint32_t lm = 0;
 #pragma unroll
-            for (int u = 0; u < kOrdPerLane; ++u) lm = max(lm, o[u]);
+            for (int u = 0; u < NU; ++u) lm = max(lm, o[u]);
             uint32_t top;
             asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(top) : "r"(lm));
             kth = top;
@@ -737,7 +743,7 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
             if (lane == __ffs(holders) - 1) {
                 bool done = false;
 #pragma unroll
-                for (int u = 0; u < kOrdPerLane; ++u)
+                for (int u = 0; u < NU; ++u)
                     if (!done && o[u] == top) {
                         o[u] = 0;
                         done = true;
@@ -810,11 +816,12 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
     }
 }
 
+template <int NU>
 __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_constant__ SplitParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
     if (li >= list_end(p)) return;
-    merge_row(p, li, threadIdx.x & 31);
+    merge_row<NU>(p, li, threadIdx.x & 31);
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
@@ -1182,6 +1189,8 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
 
 // ============================================================== finish
 
+// KU: tile counts per lane (rows of up to 60 tiles, and the longest rows)
+template <int KU>
 __global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_constant__ SplitParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     __shared__ uint64_t keys[kRowWarps][kRowKeys];
@@ -1220,7 +1229,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_cons
     }
     if (!(rec.flags & kFTopk)) return;
     // the row's candidates: counts, then the keys gathered in tile order
-    constexpr int kU = (kMaxTiles + 31) / 32;
+    constexpr int kU = KU;
     int n[kU], off[kU];
     bool over_l = false;
 #pragma unroll
@@ -1421,9 +1430,11 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
         return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess;
     };
     if (!pdl(split_pass1, g1, kSThreads, smem) || !mark(2)) return DRS_ERR_CUDA;
-    if (!pdl(split_merge, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(3)) return DRS_ERR_CUDA;
+    auto merge = G * kSWarps <= 32 * kOrdSmall ? split_merge<kOrdSmall> : split_merge<kOrdLarge>;
+    if (!pdl(merge, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(3)) return DRS_ERR_CUDA;
     if (!pdl(pass2, g2, kSThreads, smem) || !mark(4)) return DRS_ERR_CUDA;
-    if (!pdl(split_finish, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(5)) return DRS_ERR_CUDA;
+    auto finish = G <= 32 * kTilesSmall ? split_finish<kTilesSmall> : split_finish<kTilesLarge>;
+    if (!pdl(finish, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(5)) return DRS_ERR_CUDA;
     return DRS_OK;
 }
 

@@ -25,6 +25,7 @@
 //      then ranks its own keys against all G*k published keys and writes
 //      those of global rank r < k to position r, with logprob
 //      s - M - log(sum_c S_c e^(m_c - M)).
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 
@@ -455,6 +456,208 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Rows longer than a team can stage (more than kMaxTeam chunks of 16384
+// columns): one CTA per row, reading the row from global memory in five
+// passes. Rows needing this are those the row-statistics passes could not
+// finish, or every kept row when k > 64; the passes are
+//   1. the row max m, and the histogram of the top 8 bits of the value keys;
+//   2. S = sum e^(s - m), and the next 8 bits among the keys that share the
+//      chosen top bits; 3-4. the last two bytes the same way (a radix select
+//      of the k-th largest value key);
+//   5. the keys above that value, and the lowest columns holding it until k
+//      keys are collected, in column order.
+// The k keys are then ranked by counting and written with the logprob
+// s - m - log S.
+
+constexpr int kWideCtasPerSm = 2;
+
+struct WideShared {
+    unsigned int hist[256];
+    float red[kWarps];
+    int ired[kWarps];
+    int ncand;
+    int bin;
+    int need;
+    int taken;
+    float m;
+    float logs;
+    int64_t cand[kMaxK];
+};
+
+// The row's columns c = base + 4 * tid + q of the chunk at `base` (4 *
+// kThreads columns): scaled exactly, -0.0 as +0.0; -inf past the end.
+__device__ __forceinline__ void wide_load(const float* xr, int vocab, int base, bool vec,
+                                          const ScaledQuotient& sq, float (&s)[4]) {
+    const int c0 = base + 4 * threadIdx.x;
+    if (vec && c0 + 4 <= vocab) {
+        const float4 x = __ldcs(reinterpret_cast<const float4*>(xr + c0));
+        s[0] = x.x;
+        s[1] = x.y;
+        s[2] = x.z;
+        s[3] = x.w;
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s[q] = c0 + q < vocab ? __ldcs(xr + c0 + q) : -INFINITY;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s[q] = sq.exact(s[q]) + 0.0f;
+}
+
+__device__ __forceinline__ uint32_t ukey_of(float s) {
+    return static_cast<uint32_t>(key32_of(s)) ^ 0x80000000u;
+}
+
+// Add the lane's bin (256: none) to the shared histogram, one atomic per
+// distinct bin of the warp.
+__device__ __forceinline__ void hist_add(unsigned int* hist, unsigned int bin) {
+    const unsigned int peers = __match_any_sync(0xffffffffu, bin);
+    if (bin < 256u && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+}
+
+__global__ void __launch_bounds__(kThreads, kWideCtasPerSm)
+    topk_wide_kernel(const __grid_constant__ TopkParams p) {
+    __shared__ WideShared sh;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int K = p.k;
+    const int V = p.vocab;
+    const bool vec = p.nstage != 0;  // rows start 16-byte aligned
+    const int64_t nlisted = p.row_list ? static_cast<int64_t>(p.row_list[0]) : p.rows;
+    for (int64_t j = blockIdx.x; j < nlisted; j += gridDim.x) {
+        const int64_t row = p.row_list ? static_cast<int64_t>(p.row_list[64 + j]) : j;
+        const int64_t slot = (p.row0 + row) / p.canvas_len;
+        if (!p.row_list && p.keep[slot] == 0) continue;
+        const float* xr = p.logits + row * p.row_stride;
+        const ScaledQuotient sq = ScaledQuotient::of(fmaxf(p.temps[slot], kTempFloor));
+
+        // ---- radix select of the k-th largest value key, with m and S ----
+        uint32_t prefix = 0, pmask = 0;
+        int need = K;
+        float m = -INFINITY;
+        for (int d = 3; d >= 0; --d) {
+            for (int b = tid; b < 256; b += kThreads) sh.hist[b] = 0;
+            __syncthreads();
+            const int shift = 8 * d;
+            float acc = d == 3 ? -INFINITY : 0.0f;
+            for (int base = 0; base < V; base += 4 * kThreads) {
+                float s[4];
+                wide_load(xr, V, base, vec, sq, s);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const bool in = base + 4 * tid + q < V;
+                    if (d == 3) acc = fmaxf(acc, s[q]);
+                    else if (d == 2 && in && m != -INFINITY) acc += ex2_approx((s[q] - m) * kLog2e);
+                    const uint32_t u = ukey_of(s[q]);
+                    hist_add(sh.hist, in && (u & pmask) == prefix ? (u >> shift) & 0xFFu : 256u);
+                }
+            }
+            if (d == 3) {
+                const float wm = warp_max(acc);
+                if (lane == 0) sh.red[warp] = wm;
+            } else if (d == 2) {
+                const float ws = warp_sum_f(acc);
+                if (lane == 0) sh.red[warp] = ws;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                // the bin holding the need-th largest key under the prefix
+                int above = 0, b = 255;
+                for (; b > 0; --b) {
+                    if (above + static_cast<int>(sh.hist[b]) >= need) break;
+                    above += static_cast<int>(sh.hist[b]);
+                }
+                sh.bin = b;
+                sh.need = need - above;
+                if (d == 3) {
+                    float r = -INFINITY;
+                    for (int w = 0; w < kWarps; ++w) r = fmaxf(r, sh.red[w]);
+                    sh.m = r;
+                } else if (d == 2) {
+                    float r = 0.0f;
+                    for (int w = 0; w < kWarps; ++w) r += sh.red[w];
+                    sh.logs = logf(r);
+                }
+            }
+            __syncthreads();
+            prefix |= static_cast<uint32_t>(sh.bin) << shift;
+            pmask |= 0xFFu << shift;
+            need = sh.need;
+            if (d == 3) m = sh.m;
+            __syncthreads();
+        }
+        const uint32_t vt = prefix;  // the k-th largest value key; `need` of its holders are taken
+
+        // ---- the keys: all above vt, the lowest `need` columns holding vt ----
+        if (tid == 0) {
+            sh.ncand = 0;
+            sh.taken = 0;
+        }
+        __syncthreads();
+        for (int base = 0; base < V; base += 4 * kThreads) {
+            float s[4];
+            wide_load(xr, V, base, vec, sq, s);
+            int neq = 0;
+            bool eq[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c = base + 4 * tid + q;
+                const uint32_t u = ukey_of(s[q]);
+                eq[q] = c < V && u == vt;
+                neq += eq[q];
+                if (c < V && u > vt) {
+                    const int pos = atomicAdd(&sh.ncand, 1);  // < K: fewer than K keys exceed vt
+                    if (pos < kMaxK) sh.cand[pos] = make_key(s[q], c);
+                }
+            }
+            // the holders of vt in column order: the warp's, then the CTA's
+            int incl = neq;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) sh.ired[warp] = incl;
+            __syncthreads();
+            int before = sh.taken;
+            int chunk_total = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                const int c = sh.ired[w];
+                if (w < warp) before += c;
+                chunk_total += c;
+            }
+            int order = before + incl - neq;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (eq[q]) {
+                    if (order < need) {
+                        const int pos = atomicAdd(&sh.ncand, 1);
+                        if (pos < kMaxK) sh.cand[pos] = make_key(s[q], base + 4 * tid + q);
+                    }
+                    ++order;
+                }
+            __syncthreads();
+            if (tid == 0) sh.taken += chunk_total;
+            __syncthreads();
+        }
+
+        // ---- rank the k keys and write them -------------------------------
+        const float logs = sh.logs;
+        for (int c = tid; c < K; c += kThreads) {
+            const int64_t key = sh.cand[c];
+            int rank = 0;
+            for (int o = 0; o < K; ++o) rank += sh.cand[o] > key;
+            const float sv = value_of_key32(static_cast<int32_t>(key >> 32));
+            const int col = 0x7FFFFFFF - static_cast<int32_t>(key & 0xFFFFFFFF);
+            p.out_ids[row * K + rank] = col;
+            p.out_lp[row * K + rank] = m == -INFINITY ? NAN : (sv - m) - logs;
+        }
+        __syncthreads();
+    }
+}
+
 namespace {
 
 size_t record_bytes(int k) {
@@ -491,7 +694,27 @@ drs_status exact_topk(const float* logits, int64_t rows, int64_t vocab, int64_t 
     const int sms = sm_count();
     if (sms <= 0) return DRS_ERR_CUDA;
     const RowPlan plan = plan_rows(rows, static_cast<int>(vocab), sms, false);
-    if (!plan.team) return DRS_ERR_UNSUPPORTED;
+    if (!plan.team) {
+        // rows too long for a team: one CTA per row
+        TopkParams w{};
+        w.logits = logits;
+        w.row_stride = row_stride;
+        w.rows = rows;
+        w.row0 = row0;
+        w.row_list = row_list;
+        w.temps = temps;
+        w.canvas_len = canvas_len;
+        w.keep = keep;
+        w.out_ids = out_ids;
+        w.out_lp = out_logprobs;
+        w.k = k;
+        w.vocab = static_cast<int32_t>(vocab);
+        w.nstage = aligned(logits, 16) && (row_stride % 4 == 0) ? 1 : 0;
+        const int64_t g = row_list ? static_cast<int64_t>(kWideCtasPerSm) * sms
+                                   : std::min<int64_t>(rows, static_cast<int64_t>(kWideCtasPerSm) * sms);
+        topk_wide_kernel<<<static_cast<int>(g), kThreads, 0, stream>>>(w);
+        return cuda_status(cudaGetLastError());
+    }
 
     TopkParams prm{};
     prm.logits = logits;

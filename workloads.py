@@ -7,8 +7,8 @@ workload is reproducible bit for bit on one device type. (CPU and CUDA
 generators give different streams; a test that compares the two paths feeds
 both the same bytes.)
 
-The five workloads (the pages print no benchmark; these stand in for the
-shapes the sampler runs on):
+The workloads (the pages print no benchmark; these stand in for the shapes
+the sampler runs on; "wide" exercises rows longer than the configurations'):
 
   tiny         4 slots x canvas 16 = 64 rows, V = 8192, x ~ N(0, 2^2) with 5%
                of the entries rounded to multiples of 0.25 (ties), temps
@@ -23,6 +23,8 @@ shapes the sampler runs on):
   strided      2048 rows (8 x 256) of V = 262144 inside a buffer with row
                stride 262208 whose pad columns hold NaN, x ~ N(0, 3^2),
                temps all 1.0, no probs, k = 0, noise seeds 0..7.
+  wide         2 x 256 = 512 rows, V = 2097152 (2^21): the step recipe on
+               rows eight times longer (slot 0 kept).
   adversarial  8 x 128 = 1024 rows, V = 131072: 10% of rows constant (one
                N(0,1) value), 10% one-hot (0 at one column, -inf elsewhere),
                the rest N(0, 3^2) with 30% of the entries -inf; temps cycle
@@ -65,6 +67,8 @@ WORKLOADS = {
     "strided": Workload("strided", 8, 256, 262144, 262208, PROBS_NONE, 0,
                         seeds=list(range(8)),
                         description="2048 rows, stride 262208 NaN pad, no probs, 8 seeds"),
+    "wide": Workload("wide", 2, 256, 2097152, 2097152, PROBS_BF16, 20,
+                     description="512x2097152 fp32 N(0,9)+spike, bf16, k=20"),
     "adversarial": Workload("adversarial", 8, 128, 131072, 131072, PROBS_BF16, 64,
                             description="1024x131072 fp32 with -inf/constant/one-hot rows, k=64"),
 }
@@ -83,7 +87,7 @@ def make_temps_keep(name: str, data_seed: int = 0):
     if name == "tiny":
         temps = torch.tensor([0.0, 0.7, 1.0, 1.3], dtype=torch.float32)
         keep = torch.ones(w.slots, dtype=torch.uint8)
-    elif name == "step":
+    elif name in ("step", "wide"):
         temps = 0.5 + torch.rand(w.slots, generator=g, dtype=torch.float32)
         keep = (torch.arange(w.slots) % 2 == 0).to(torch.uint8)
     elif name == "large":
@@ -117,12 +121,12 @@ def make_logits(name: str, device="cpu", data_seed: int = 0, rows: int | None = 
         pick = torch.rand(R, V, generator=g, device=device) < 0.05
         x = torch.where(pick, torch.round(x * 4.0) / 4.0, x)
         buf = x
-    elif name in ("step", "strided"):
+    elif name in ("step", "strided", "wide"):
         buf = torch.empty(R, stride, device=device, dtype=torch.float32)
         buf[:, :V].normal_(0.0, 3.0, generator=g)
         if stride > V:
             buf[:, V:] = float("nan")
-        if name == "step":
+        if name in ("step", "wide"):
             col = torch.randint(0, V, (R,), generator=g, device=device)
             buf[torch.arange(R, device=device), col] += 8.0
     elif name == "large":
