@@ -83,6 +83,9 @@ def _load():
     lib.oracle_row_stats_rows.restype = ctypes.c_int
     lib.oracle_topk_rows.argtypes = [vp, vp, c_i64, c_i64, c_i32, vp, vp]
     lib.oracle_topk_rows.restype = ctypes.c_int
+    lib.oracle_stash.argtypes = [vp, c_i64, c_i64, c_i64, c_i64, vp, vp, vp, vp, vp, c_i32,
+                                 vp, vp, c_i64, c_i32, ctypes.c_int, vp, vp, vp]
+    lib.oracle_stash.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -304,3 +307,32 @@ def topk_rows(x: np.ndarray, temps, k: int, threads: int = 1):
 
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))
+
+
+def stash(logits: np.ndarray, canvas_len: int, src, slots, keep, valid, temps,
+          num_topk: int, num_token_ids, token_ids, out_slots: int, width: int,
+          logits_mode: bool = False):
+    """Oracle stash (see oracle_stash in drs_oracle.c): (ids int32 [out_slots,
+    canvas_len, width], values float64 [same], ranks int32 [out_slots,
+    canvas_len]). Entries the stash does not write hold -1, NaN and -1.
+    token_ids: None, or int32 [m, n] (n >= max num_token_ids)."""
+    lib = _load()
+    rows, vocab, stride = _logits_view(logits)
+    i32 = lambda a: np.ascontiguousarray(a, dtype=np.int32)
+    src, slots, valid = i32(src), i32(slots), i32(valid)
+    keep = np.ascontiguousarray(keep, dtype=np.uint8)
+    temps = np.ascontiguousarray(temps, dtype=np.float32)
+    m = src.shape[0]
+    nti = i32(num_token_ids) if num_token_ids is not None else None
+    tid = i32(token_ids) if token_ids is not None else None
+    ids_stride = tid.shape[1] if tid is not None else 0
+    ids = np.full((out_slots, canvas_len, width), -1, dtype=np.int32)
+    vals = np.full((out_slots, canvas_len, width), np.nan, dtype=np.float64)
+    ranks = np.full((out_slots, canvas_len), -1, dtype=np.int32)
+    rc = lib.oracle_stash(_ptr(logits), stride, vocab, canvas_len, m, _ptr(src), _ptr(slots),
+                          _ptr(keep), _ptr(valid), _ptr(temps), num_topk, _ptr(nti), _ptr(tid),
+                          ids_stride, width, 1 if logits_mode else 0, _ptr(ids), _ptr(vals),
+                          _ptr(ranks))
+    if rc != 0:
+        raise MemoryError("oracle_stash")
+    return ids, vals, ranks

@@ -19,7 +19,9 @@
  *     entropy = -sum over p > 0 of p log p, argmax of scaled and of noisy);
  *   - stash_converged_logprobs docstring and _lp_topk_kernel docstring: the
  *     num_topk largest scaled logits of kept rows, ordered by value and then
- *     by lower index, and their logprobs.
+ *     by lower index, and their logprobs; the stash layout (request rows
+ *     src * canvas_len + p for p < valid, stash row (slots, p), the argmax,
+ *     then token_ids or the num_topk largest, padding with id 0 at -inf).
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - the noise: the reference draws it with an unseeded rand_like; the
@@ -32,7 +34,12 @@
  *   - -0.0 and +0.0 are the same value for the top-k order;
  *   - the top-k logprob clamps T at 1e-10 like the row statistics;
  *   - a row that is -inf everywhere: argmax = sample = 0, entropy = 0,
- *     probs = NaN, top-k logprobs = NaN (what the PyTorch definition gives).
+ *     probs = NaN, top-k logprobs = NaN (what the PyTorch definition gives);
+ *   - the stash: temps[j] is clamped at 1e-10; a token id outside the
+ *     vocabulary gets NaN; logits mode writes the scaled logit instead of
+ *     the logprob; out_ranks holds, per stash row, 1 + the number of
+ *     columns whose scaled logit exceeds column 0's (the pages do not say
+ *     what the rank counts: parity unpinned beyond this reading).
  *
  * Floating point: the scaled logit is one IEEE fp32 division; everything
  * after it is in double. Build with -ffp-contract=off and without fast-math.
@@ -372,6 +379,112 @@ int oracle_topk_rows(const float *const *row_ptrs, const float *temps, int64_t n
     for (int64_t t = 0; t < n; ++t)
         oracle_topk_one(row_ptrs[t], vocab, temps[t], k, items, out_ids + t * k,
                         out_logprobs + t * k);
+    free(items);
+    return 0;
+}
+
+/*
+ * The stash written by stash_converged_logprobs (page
+ * "vllm.model_executor.models.diffusion_gemma_sampler", its docstring).
+ * Request j < m owns logits rows src[j] * canvas_len + p for p < valid[j]
+ * (at most canvas_len), scaled by clamp(temps[j], 1e-10). Where keep[j],
+ * stash row (slots[j], p) -- row slots[j] * canvas_len + p of the outputs --
+ * receives `width` columns of (id, value):
+ *   column 0              the argmax (lowest column of the max);
+ *   the next columns      token_ids[j * ids_stride + c] for c < n_j when
+ *                         token_ids is given and n_j = num_token_ids[j] > 0,
+ *                         else the num_topk largest (value descending, lower
+ *                         column first);
+ *   the rest              id 0 with value -inf.
+ * value = scaled - max - log(sum exp(scaled - max)) (NaN when the row is
+ * -inf everywhere, and for a token id outside [0, vocab)), or the scaled
+ * logit itself when logits_mode. out_ranks[stash row] = 1 + #{k : scaled_k >
+ * scaled of column 0's id}. -0.0 is taken as +0.0. Stash rows of requests
+ * that are not kept, and positions p >= valid[j], are not touched; out_ids,
+ * out_vals hold width entries per stash row. Returns 0, or -1 on
+ * allocation failure.
+ */
+int oracle_stash(const float *logits, int64_t row_stride, int64_t vocab, int64_t canvas_len,
+                 int64_t m, const int32_t *src, const int32_t *slots, const uint8_t *keep,
+                 const int32_t *valid, const float *temps, int32_t num_topk,
+                 const int32_t *num_token_ids, const int32_t *token_ids, int64_t ids_stride,
+                 int32_t width, int logits_mode, int32_t *out_ids, double *out_vals,
+                 int32_t *out_ranks) {
+    float *scaled = (float *)malloc((size_t)vocab * sizeof(float));
+    oracle_ranked *items = (oracle_ranked *)malloc((size_t)vocab * sizeof(oracle_ranked));
+    if (!scaled || !items) {
+        free(scaled);
+        free(items);
+        return -1;
+    }
+    for (int64_t j = 0; j < m; ++j) {
+        if (!keep[j]) continue;
+        float te = oracle_clamped_temp(temps[j]);
+        int64_t npos = valid[j] < canvas_len ? valid[j] : canvas_len;
+        for (int64_t p = 0; p < npos; ++p) {
+            const float *x = logits + ((int64_t)src[j] * canvas_len + p) * row_stride;
+            int64_t out_row = (int64_t)slots[j] * canvas_len + p;
+            int32_t *ids = out_ids + out_row * width;
+            double *vals = out_vals + out_row * width;
+
+            /* scaled logits, their max, log of the sum of exponentials */
+            float mx = -INFINITY;
+            int64_t arg = 0;
+            for (int64_t c = 0; c < vocab; ++c) {
+                scaled[c] = x[c] / te + 0.0f;
+                if (scaled[c] > mx) {
+                    mx = scaled[c];
+                    arg = c;
+                }
+            }
+            double big_m = (double)mx, log_s = NAN;
+            if (mx != -INFINITY) {
+                double s_sum = 0.0;
+                for (int64_t c = 0; c < vocab; ++c)
+                    if (scaled[c] != -INFINITY) s_sum += exp((double)scaled[c] - big_m);
+                log_s = log(s_sum);
+            }
+#define ORACLE_VALUE(col)                                                              \
+    ((col) < 0 || (col) >= vocab ? NAN                                                 \
+     : logits_mode              ? (double)scaled[(col)]                               \
+     : mx == -INFINITY          ? NAN                                                 \
+                                : (double)scaled[(col)] - big_m - log_s)
+
+            int32_t w = 0;
+            if (w < width) {
+                ids[w] = (int32_t)arg;
+                vals[w] = ORACLE_VALUE(arg);
+                ++w;
+            }
+            int32_t n_ids = token_ids && num_token_ids ? num_token_ids[j] : 0;
+            if (n_ids > 0) {
+                for (int32_t c = 0; c < n_ids && w < width; ++c, ++w) {
+                    int32_t id = token_ids[j * ids_stride + c];
+                    ids[w] = id;
+                    vals[w] = ORACLE_VALUE(id);
+                }
+            } else if (num_topk > 0) {
+                for (int64_t c = 0; c < vocab; ++c) {
+                    items[c].value = scaled[c];
+                    items[c].index = c;
+                }
+                qsort(items, (size_t)vocab, sizeof(oracle_ranked), oracle_rank_cmp);
+                for (int32_t r = 0; r < num_topk && r < vocab && w < width; ++r, ++w) {
+                    ids[w] = (int32_t)items[r].index;
+                    vals[w] = ORACLE_VALUE(items[r].index);
+                }
+            }
+            for (; w < width; ++w) {
+                ids[w] = 0;
+                vals[w] = -INFINITY;
+            }
+#undef ORACLE_VALUE
+            int32_t above = 0;
+            for (int64_t c = 0; c < vocab; ++c) above += scaled[c] > scaled[arg];
+            out_ranks[out_row] = 1 + above;
+        }
+    }
+    free(scaled);
     free(items);
     return 0;
 }
