@@ -229,6 +229,29 @@ def _run_ours(args, world, rank, local):
         if ev is not None:
             ev[1].record(stream)
 
+    # the stash of the converged requests (one per slot: src = slots = the
+    # slot, every position valid), top-k + the argmax column
+    n_slots = rows // w["canvas_len"]
+    req = torch.arange(n_slots, dtype=torch.int32, device=dev)
+    valid_all = torch.full((n_slots,), w["canvas_len"], dtype=torch.int32, device=dev)
+    st_ids = torch.empty(n_slots, w["canvas_len"], k + 1, dtype=torch.int32, device=dev)
+    st_vals = torch.empty(n_slots, w["canvas_len"], k + 1, dtype=torch.float32, device=dev)
+    st_ranks = torch.empty(n_slots, w["canvas_len"], dtype=torch.int32, device=dev)
+    ws_st = drs.workspace(drs.drs_stash_workspace_bytes(n_slots, w["canvas_len"], V, k), dev)
+
+    def stash_ms(n=3):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        t = []
+        for _ in range(n + 1):
+            evs[0].record(stream)
+            drs.drs_stash_converged_logprobs(logits, w["canvas_len"], req, req, keep, valid_all,
+                                             temps, k, None, None, st_ids, st_vals, st_ranks,
+                                             False, ws_st, stream)
+            evs[1].record(stream)
+            torch.cuda.synchronize()
+            t.append(evs[0].elapsed_time(evs[1]))
+        return sum(t[1:]) / n
+
     def separate(n=3):
         """The two separate calls, timed briefly (context for the fused one)."""
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -288,6 +311,7 @@ def _run_ours(args, world, rank, local):
 
     rs_avg_ms = sum(rs_ms) / len(rs_ms)
     sep_rs_ms, tk_avg_ms = separate()
+    stash_avg_ms = stash_ms()
     bytes_rs = rows * V * 4 + rows * V * 2      # each logit read once, each probability written once
     kept_rows = int(keep[: rows // w["canvas_len"]].sum().item()) * w["canvas_len"]
     bytes_tk = kept_rows * V * 4
@@ -331,7 +355,12 @@ def _run_ours(args, world, rank, local):
                        "topk_logprobs": {"avg_ms": round(tk_avg_ms, 4),
                                          "gbs_read": round(bytes_tk / (tk_avg_ms / 1e3) / 1e9, 1),
                                          "frac_of_peak": round(bytes_tk / (tk_avg_ms / 1e3) / 1e9
-                                                               / peak, 4)}},
+                                                               / peak, 4)},
+                       "stash_converged_logprobs": {
+                           "avg_ms": round(stash_avg_ms, 4),
+                           "gbs_read": round(bytes_tk / (stash_avg_ms / 1e3) / 1e9, 1),
+                           "frac_of_peak": round(bytes_tk / (stash_avg_ms / 1e3) / 1e9 / peak, 4),
+                           "note": "the kept rows' stash (argmax + top-k), one read per kept row"}},
            # per step: list of rows, pass 1, merge, pass 2, finish, exact top-k
            "gpu_launches": 6 * args.steps,
            "clocks": clocks}

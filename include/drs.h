@@ -296,6 +296,64 @@ drs_status drs_kernel_timing(int enable);
  */
 drs_status drs_kernel_times(float *avg_ms, int32_t n, int32_t *calls);
 
+/*
+ * Bytes of device workspace drs_stash_converged_logprobs needs (256-byte
+ * aligned, contents arbitrary); 0 for arguments outside its ranges
+ * (num_topk in [0, 1024]).
+ */
+size_t drs_stash_workspace_bytes(int64_t requests, int64_t canvas_len, int64_t vocab,
+                                 int32_t num_topk);
+
+/*
+ * The stash of converged requests' logprobs (stash_converged_logprobs on
+ * the page above, its docstring). Request j < requests owns logits rows
+ * src[j] * canvas_len + p for p < valid[j], scaled by
+ * max(temps[j], 1e-10). Where keep[j] != 0, stash row
+ * slots[j] * canvas_len + p of the outputs receives `width` columns of
+ * (id, value):
+ *   column 0        the argmax of the scaled row (lowest column of the max);
+ *   then            token_ids[j * ids_stride + c] for c < num_token_ids[j]
+ *                   when token_ids is given and num_token_ids[j] > 0, else
+ *                   the num_topk largest (value descending, lower column
+ *                   first);
+ *   then            id 0 with value -inf, up to `width`.
+ * value: the logprob s - max - log(sum over the row of e^(s - max)) (NaN
+ * when the row is -inf everywhere), or the scaled logit s itself when
+ * logits_mode != 0; NaN for a token id outside [0, vocab).
+ * out_ranks[stash row]: 1 + the number of columns whose scaled logit
+ * exceeds column 0's (column 0 is the argmax, so 1).
+ *
+ *   logits          fp32, row r at logits + r * row_stride, r < logits_rows.
+ *   src, slots, valid, num_token_ids   int32 [requests] (num_token_ids may
+ *                   be null without token_ids).
+ *   keep            uint8 [requests]; temps fp32 [requests].
+ *   token_ids       null, or int32 [requests, ids_stride].
+ *   out_ids         int32 [out_slots * canvas_len, width]; out_logprobs
+ *                   fp32 and out_ranks int32 [out_slots * canvas_len] alike.
+ *                   Rows of requests not kept, positions p >= valid[j], and
+ *                   rows whose logits row or stash row falls outside
+ *                   logits_rows or out_slots are not touched.
+ *   workspace       drs_stash_workspace_bytes(requests, canvas_len, vocab,
+ *                   num_topk) bytes.
+ * All pointers are device memory owned by the caller; asynchronous on
+ * `stream`. Returns DRS_ERR_INVALID_ARG for a null required pointer,
+ * negative sizes, row_stride < vocab, num_topk outside [0, min(vocab,
+ * 1024)], width < num_topk + 1, token_ids without num_token_ids or with
+ * ids_stride < 1, or a small or unaligned workspace;
+ * DRS_ERR_UNSUPPORTED for vocab > DRS_MAX_VOCAB or more than 2^31 - 1
+ * stash rows; requests == 0 is a no-op.
+ */
+drs_status drs_stash_converged_logprobs(const float *logits, int64_t logits_rows, int64_t vocab,
+                                        int64_t row_stride, int64_t canvas_len, int64_t requests,
+                                        const int32_t *src, const int32_t *slots,
+                                        const uint8_t *keep, const int32_t *valid,
+                                        const float *temps, int32_t num_topk,
+                                        const int32_t *num_token_ids, const int32_t *token_ids,
+                                        int64_t ids_stride, int64_t out_slots, int32_t width,
+                                        int32_t *out_ids, float *out_logprobs,
+                                        int32_t *out_ranks, int logits_mode, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *drs_status_string(drs_status s);
 

@@ -114,3 +114,40 @@ def test_scaled_logits_argument_checks(lib):
     assert lib.drs_scaled_logits(None, 4, 1.0, FAKE, None) == INV
     assert lib.drs_scaled_logits(FAKE, 4, 1.0, FAKE + 2, None) == INV
     assert lib.drs_scaled_logits(FAKE, 0, 1.0, FAKE, None) == OK
+
+
+def _stash(lib, requests=2, logits_rows=4, vocab=16, stride=16, canvas=2, ptr=FAKE, k=3, nti=None,
+           tok=None, ids_stride=0, out_slots=2, width=4, ws=FAKE, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = drs.drs_stash_workspace_bytes(requests, canvas, vocab, k)
+    return lib.drs_stash_converged_logprobs(ptr, logits_rows, vocab, stride, canvas, requests, ptr,
+                                            ptr, ptr, ptr, ptr, k, nti, tok, ids_stride, out_slots,
+                                            width, ptr, ptr, ptr, 0, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({"requests": 0}, OK),                          # nothing to do, nothing launched
+    ({"requests": -1}, INV),
+    ({"canvas": 0}, INV),
+    ({"stride": 8}, INV),
+    ({"vocab": 0}, INV),
+    ({"vocab": drs.DRS_MAX_VOCAB + 1, "stride": drs.DRS_MAX_VOCAB + 1}, UNS),
+    ({"k": -1}, INV),
+    ({"k": 17}, INV),                               # more than the vocabulary
+    ({"k": 3, "width": 3}, INV),                    # width < num_topk + 1
+    ({"width": 0, "k": 0}, INV),
+    ({"tok": FAKE, "ids_stride": 4}, INV),          # token ids without their counts
+    ({"tok": FAKE, "nti": FAKE, "ids_stride": 0}, INV),
+    ({"ptr": 0}, INV),
+    ({"ws": 0}, INV),
+    ({"ws_bytes": 16}, INV),
+    ({"ws": FAKE + 8}, INV),
+])
+def test_stash_argument_checks(lib, kw, expect):
+    assert _stash(lib, **kw) == expect
+
+
+def test_stash_workspace_sizes(lib):
+    assert drs.drs_stash_workspace_bytes(8, 256, 262144, 20) >= 8 * 256 * 20 * 8
+    assert drs.drs_stash_workspace_bytes(8, 256, 262144, 1025) == 0
+    assert drs.drs_stash_workspace_bytes(-1, 256, 262144, 20) == 0

@@ -1,0 +1,127 @@
+"""GPU parity of drs_stash_converged_logprobs against the oracle's stash.
+
+Requests with permuted src and slots, a mix of keep flags and valid
+lengths, temperatures 0, 1e-3 and ordinary ones, rows that are constant,
+tied, -inf everywhere, or mostly -inf. Both paths are covered: the
+request's token ids (counts 0 to 4, one id outside the vocabulary) and the
+num_topk largest. Values are logprobs or the scaled logits themselves.
+Stash rows the call must not write are filled with a sentinel first and
+checked bit for bit. Ids are exact; logprobs are within the parity
+tolerance; scaled logits are exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import drs
+from parity import check_topk
+
+pytestmark = pytest.mark.gpu
+
+SENT_ID, SENT_V, SENT_R = -123456789, np.float32(-7.25), -55
+
+
+def _batch(seed, vocab, m=5, canvas=4):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((m * canvas + 3, vocab)) * 2).astype(np.float32)
+    x[rng.random(x.shape) < 0.2] = -np.inf
+    x[3] = np.round(x[3])                         # ties
+    x[5] = 0.5                                    # constant
+    x[6] = -np.inf                                # all -inf
+    x[9][rng.random(vocab) < 0.999] = -np.inf     # a few finite values
+    src = rng.permutation(m).astype(np.int32)
+    slots = rng.permutation(m + 2)[:m].astype(np.int32)
+    keep = np.array([1, 0, 1, 1, 1], np.uint8)
+    valid = np.array([4, 4, 2, 0, 3], np.int32)
+    temps = np.array([1.0, 0.7, 0.0, 1e-3, 1.3], np.float32)
+    tok = np.array([[5, vocab - 1, 0, 17], [1, 2, 3, 4], [9, 9, vocab, 2], [0, 0, 0, 0],
+                    [42 % vocab, 7, 7, 1]], np.int32)
+    nti = np.array([4, 2, 4, 1, 0], np.int32)
+    return x, src, slots, keep, valid, temps, tok, nti, m, canvas
+
+
+def _run(x, canvas, src, slots, keep, valid, temps, k, nti, tok, out_slots, width, mode):
+    lib = drs()
+    dev = lambda a: torch.as_tensor(a).cuda()
+    ids = torch.full((out_slots, canvas, width), SENT_ID, dtype=torch.int32, device="cuda")
+    vals = torch.full((out_slots, canvas, width), float(SENT_V), dtype=torch.float32, device="cuda")
+    ranks = torch.full((out_slots, canvas), SENT_R, dtype=torch.int32, device="cuda")
+    lib.stash_converged_logprobs(dev(x), canvas, dev(src), dev(slots), dev(keep), dev(valid),
+                                 dev(temps), k, None if nti is None else dev(nti),
+                                 None if tok is None else dev(tok), ids, vals, ranks,
+                                 logits_mode=mode)
+    torch.cuda.synchronize()
+    assert lib.drs_get_device_error() == 0
+    return ids.cpu().numpy(), vals.cpu().numpy(), ranks.cpu().numpy()
+
+
+def _compare(x, canvas, src, slots, keep, valid, temps, k, nti, tok, width, mode, where):
+    out_slots = len(src) + 2
+    g_ids, g_vals, g_ranks = _run(x, canvas, src, slots, keep, valid, temps, k, nti, tok,
+                                  out_slots, width, mode)
+    r_ids, r_vals, r_ranks = oracle.stash(x, canvas, src, slots, keep, valid, temps, k, nti, tok,
+                                          out_slots, width, logits_mode=mode)
+    written = r_ranks != -1
+    assert np.all(g_ids[~written] == SENT_ID) and np.all(g_vals[~written] == SENT_V), where
+    assert np.all(g_ranks[~written] == SENT_R), where
+    assert np.array_equal(g_ranks[written], r_ranks[written]), where
+    gi, gv = g_ids[written], g_vals[written]
+    ri, rv = r_ids[written], r_vals[written]
+    if mode:
+        assert np.array_equal(gi, ri), where
+        same = (gv == rv.astype(np.float32)) | (np.isnan(gv) & np.isnan(rv))
+        assert same.all(), f"{where}: scaled logits differ at {np.argwhere(~same)[:3]}"
+    else:
+        check_topk(gi, gv, ri, rv, where)
+
+
+@pytest.mark.parametrize("vocab,k", [(777, 0), (777, 5), (70001, 64), (70001, 100),
+                                     (600000, 20)])
+@pytest.mark.parametrize("ids_path", [False, True])
+@pytest.mark.parametrize("mode", [False, True])
+def test_stash_against_oracle(vocab, k, ids_path, mode):
+    x, src, slots, keep, valid, temps, tok, nti, m, canvas = _batch(vocab + k, vocab)
+    width = k + 3 if not ids_path else max(k + 1, 6)
+    _compare(x, canvas, src, slots, keep, valid, temps, k, nti if ids_path else None,
+             tok if ids_path else None, width, mode,
+             f"V={vocab} k={k} ids={ids_path} logits={mode}")
+
+
+def test_stash_width_truncates_token_ids():
+    x, src, slots, keep, valid, temps, tok, nti, m, canvas = _batch(3, 5000)
+    _compare(x, canvas, src, slots, keep, valid, temps, 2, nti, tok, 3, False, "width 3")
+
+
+def test_stash_step_sized_batch():
+    """8 requests x canvas 256 x 262144 columns, every other request kept,
+    top-20: sampled stash rows against the oracle."""
+    rng = np.random.default_rng(11)
+    m, canvas, vocab, k = 8, 256, 262144, 20
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    x_dev = torch.randn(m * canvas, vocab, generator=g, device="cuda") * 3.0
+    src = rng.permutation(m).astype(np.int32)
+    slots = rng.permutation(m).astype(np.int32)
+    keep = (np.arange(m) % 2 == 0).astype(np.uint8)
+    valid = np.full(m, canvas, np.int32)
+    valid[2] = 100
+    temps = (0.5 + rng.random(m)).astype(np.float32)
+    lib = drs()
+    dev = lambda a: torch.as_tensor(a).cuda()
+    ids, vals, ranks = lib.stash_converged_logprobs(x_dev, canvas, dev(src), dev(slots), dev(keep),
+                                                    dev(valid), dev(temps), k, width=k + 1)
+    torch.cuda.synchronize()
+    assert lib.drs_get_device_error() == 0
+    ids, vals, ranks = ids.cpu().numpy(), vals.cpu().numpy(), ranks.cpu().numpy()
+    for j in np.flatnonzero(keep):
+        for pos in rng.choice(valid[j], 3, replace=False):
+            row = int(src[j]) * canvas + int(pos)
+            x = np.ascontiguousarray(x_dev[row:row + 1].cpu().numpy())
+            ri, rl = oracle.topk_rows(x, temps[j:j + 1], k)
+            o = (int(slots[j]), int(pos))
+            assert ids[o][0] == ri[0, 0] and ranks[o] == 1
+            check_topk(ids[o][None, 1:], vals[o][None, 1:], ri, rl, f"request {j} pos {pos}")
+    for j in np.flatnonzero(keep == 0):
+        assert np.all(ids[slots[j]] == -1) and np.all(ranks[slots[j]] == -1)
+    assert np.all(ids[slots[2], 100:] == -1)          # positions past valid[2]

@@ -11,9 +11,10 @@ Entry points (same names as the C ABI):
   drs_row_stats, drs_row_stats_workspace_bytes, drs_row_stats_noalloc,
   drs_row_stats_topk, drs_row_stats_topk_workspace_bytes, drs_topk_logprobs,
   drs_topk_workspace_bytes, drs_philox_gumbel, drs_scaled_logits,
+  drs_stash_converged_logprobs, drs_stash_workspace_bytes,
   drs_status_string, drs_get_device_error.
 Convenience wrappers that allocate outputs: row_stats, row_stats_topk,
-topk_logprobs, philox_gumbel.
+topk_logprobs, philox_gumbel, stash_converged_logprobs.
 """
 from __future__ import annotations
 
@@ -36,7 +37,8 @@ EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_row_stats_noa
             "drs_topk_workspace_bytes", "drs_philox_gumbel", "drs_scaled_logits",
             "drs_status_string", "drs_get_device_error", "drs_test_inject_fault",
             "drs_kernel_timing", "drs_kernel_times", "drs_row_stats_seeds",
-            "drs_row_stats_seeds_workspace_bytes")
+            "drs_row_stats_seeds_workspace_bytes", "drs_stash_converged_logprobs",
+            "drs_stash_workspace_bytes")
 
 
 class DrsError(RuntimeError):
@@ -83,6 +85,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_topk_workspace_bytes.restype = sz
     lib.drs_topk_logprobs.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, vp, vp, vp, sz, vp]
     lib.drs_topk_logprobs.restype = ctypes.c_int
+    lib.drs_stash_workspace_bytes.argtypes = [i64, i64, i64, i32]
+    lib.drs_stash_workspace_bytes.restype = sz
+    lib.drs_stash_converged_logprobs.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
+                                                 i32, vp, vp, i64, i64, i32, vp, vp, vp,
+                                                 ctypes.c_int, vp, sz, vp]
+    lib.drs_stash_converged_logprobs.restype = ctypes.c_int
     lib.drs_philox_gumbel.argtypes = [u64, i64, i64, i64, vp, vp, vp]
     lib.drs_philox_gumbel.restype = ctypes.c_int
     lib.drs_scaled_logits.argtypes = [vp, i64, ctypes.c_float, vp, vp]
@@ -221,6 +229,28 @@ def drs_topk_logprobs(logits, temps, canvas_len, keep, k, out_ids, out_logprobs,
                                   canvas_len, _ptr(keep), k, _ptr(out_ids), _ptr(out_logprobs),
                                   _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "drs_topk_logprobs")
+
+
+def drs_stash_workspace_bytes(requests: int, canvas_len: int, vocab: int, num_topk: int) -> int:
+    return load().drs_stash_workspace_bytes(requests, canvas_len, vocab, num_topk)
+
+
+def drs_stash_converged_logprobs(logits, canvas_len, src, slots, keep, valid, temps, num_topk,
+                                 num_token_ids, token_ids, out_ids, out_logprobs, out_ranks,
+                                 logits_mode, workspace=None, stream=None):
+    """out_ids / out_logprobs: [out_slots, canvas_len, width]; out_ranks:
+    [out_slots, canvas_len]; token_ids: None or int32 [requests, n]."""
+    rows, vocab = logits.shape
+    requests = src.shape[0]
+    out_slots, _, width = out_ids.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ids_stride = token_ids.stride(0) if token_ids is not None else 0
+    st = load().drs_stash_converged_logprobs(
+        _ptr(logits), rows, vocab, _row_stride(logits), canvas_len, requests, _ptr(src),
+        _ptr(slots), _ptr(keep), _ptr(valid), _ptr(temps), num_topk, _ptr(num_token_ids),
+        _ptr(token_ids), ids_stride, out_slots, width, _ptr(out_ids), _ptr(out_logprobs),
+        _ptr(out_ranks), 1 if logits_mode else 0, _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "drs_stash_converged_logprobs")
 
 
 def drs_philox_gumbel(seed, row0, rows, vocab, out_bits=None, out_gumbel=None, stream=None):
@@ -373,3 +403,27 @@ def philox_gumbel(seed: int, row0: int, rows: int, vocab: int, device="cuda", st
     g = torch.empty(rows, vocab, dtype=torch.float32, device=device)
     drs_philox_gumbel(seed, row0, rows, vocab, bits, g, stream)
     return bits, g
+
+
+def stash_converged_logprobs(logits, canvas_len: int, src, slots, keep, valid, temps,
+                             num_topk: int, num_token_ids=None, token_ids=None, out_ids=None,
+                             out_logprobs=None, out_ranks=None, out_slots: int | None = None,
+                             width: int | None = None, logits_mode: bool = False, stream=None):
+    """The stash (see drs_stash_converged_logprobs); outputs allocated when
+    not given, filled with -1 / NaN / -1 where the stash does not write."""
+    import torch
+    dev = logits.device
+    if out_ids is None:
+        out_slots = int(src.shape[0]) if out_slots is None else out_slots
+        width = num_topk + 1 if width is None else width
+        out_ids = torch.full((out_slots, canvas_len, width), -1, dtype=torch.int32, device=dev)
+    if out_logprobs is None:
+        out_logprobs = torch.full(out_ids.shape, float("nan"), dtype=torch.float32, device=dev)
+    if out_ranks is None:
+        out_ranks = torch.full(out_ids.shape[:2], -1, dtype=torch.int32, device=dev)
+    ws = workspace(drs_stash_workspace_bytes(int(src.shape[0]), canvas_len, logits.shape[1],
+                                             num_topk), dev)
+    drs_stash_converged_logprobs(logits, canvas_len, src, slots, keep, valid, temps, num_topk,
+                                 num_token_ids, token_ids, out_ids, out_logprobs, out_ranks,
+                                 logits_mode, ws, stream)
+    return out_ids, out_logprobs, out_ranks

@@ -38,10 +38,20 @@ constexpr size_t kWorkspaceAlign = 256;
 // keep flags are indexed by global slot (row0 + row) / canvas_len.
 size_t exact_topk_workspace_bytes(int32_t k);
 int32_t exact_topk_max_k();
+// A row map for the exact top-k (the stash): the listed rows are entries e
+// of a list, read from logits row row[e] with temperature temp[e]; outputs,
+// and (when out_m is not null) the entry's max scaled logit and log of the
+// sum of e^(s - max), are written at e.
+struct ExactTopkMap {
+    const int32_t* row;
+    const float* temp;
+    float* out_m;
+    float* out_logs;
+};
 drs_status exact_topk(const float* logits, int64_t rows, int64_t vocab, int64_t row_stride,
                       int64_t row0, const float* temps, int64_t canvas_len, const uint8_t* keep,
                       const int32_t* row_list, int32_t k, int32_t* out_ids, float* out_logprobs,
-                      void* workspace, cudaStream_t stream);
+                      void* workspace, cudaStream_t stream, const ExactTopkMap* map = nullptr);
 
 // One call of the row statistics path: stats (argmax, sample, entropy and
 // optionally probs) of every row, and with k > 0 the top-k logprobs of the

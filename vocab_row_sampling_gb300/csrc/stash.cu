@@ -1,0 +1,258 @@
+// stash.cu -- the stash of converged requests' logprobs (page
+// "vllm.model_executor.models.diffusion_gemma_sampler": the
+// stash_converged_logprobs docstring).
+//
+// Request j owns logits rows src[j] * canvas_len + p for p < valid[j],
+// scaled by clamp(temps[j], 1e-10). Where keep[j], stash row (slots[j], p)
+// of the outputs receives `width` columns of (id, value): the argmax, then
+// the request's token ids if it has any (num_token_ids[j] > 0), else the
+// num_topk largest (value descending, lower id first), then id 0 at -inf.
+// The value is the logprob s - max - log(sum e^(s - max)), or the scaled
+// logit s in logits mode; out_ranks holds one rank per stash row (below).
+//
+// Kernels, in stream order:
+//   list   one thread per (request, position): the stash rows to write, each
+//          with its logits row, temperature, output row and request;
+//   top-k  the exact top-k kernel over that list with k = max(num_topk, 1)
+//          (its first key is the argmax: keys order by value, then by lower
+//          column), which also leaves each entry's max and log-sum;
+//   write  one warp per entry: the row's columns, values from one IEEE
+//          division each.
+// Rows of requests that are not kept are never read.
+#include <cfloat>
+#include <climits>
+
+#include "drs_device.cuh"
+#include "drs_internal.h"
+
+namespace drs {
+namespace {
+
+constexpr int kListOffset = 64;  // list: count at [0], entries from [64]
+
+struct StashParams {
+    const float* logits;
+    int64_t row_stride;
+    int64_t logits_rows;
+    int32_t vocab;
+    int64_t canvas_len;
+    int64_t requests;
+    int64_t out_slots;
+    const int32_t* src;
+    const int32_t* slots;
+    const uint8_t* keep;
+    const int32_t* valid;
+    const float* temps;
+    int32_t num_topk;
+    int32_t kq;  // keys per entry from the top-k: max(num_topk, 1)
+    const int32_t* num_token_ids;
+    const int32_t* token_ids;
+    int64_t ids_stride;
+    int32_t width;
+    int32_t logits_mode;
+    int32_t* out_ids;
+    float* out_vals;
+    int32_t* out_ranks;
+    int32_t* list;
+    int32_t* map_row;
+    float* map_temp;
+    int64_t* map_out;
+    int32_t* map_req;
+    const int32_t* top_ids;
+    const float* row_m;
+    const float* row_logs;
+};
+
+__global__ void __launch_bounds__(256) stash_list(const __grid_constant__ StashParams p) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    bool take = false;
+    int64_t j = 0, pos = 0, row = 0, out = 0;
+    if (idx < p.requests * p.canvas_len) {
+        j = idx / p.canvas_len;
+        pos = idx - j * p.canvas_len;
+        row = static_cast<int64_t>(p.src[j]) * p.canvas_len + pos;
+        out = static_cast<int64_t>(p.slots[j]) * p.canvas_len + pos;
+        // rows outside the logits or the stash are skipped, never touched
+        take = p.keep[j] != 0 && pos < p.valid[j] && p.src[j] >= 0 && row < p.logits_rows &&
+               p.slots[j] >= 0 && p.slots[j] < p.out_slots;
+    }
+    const uint32_t b = __ballot_sync(0xffffffffu, take);
+    int base = 0;
+    if (lane == 0 && b) base = atomicAdd(p.list, __popc(b));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (take) {
+        uint32_t lt;
+        asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+        const int e = base + __popc(b & lt);
+        p.list[kListOffset + e] = e;
+        p.map_row[e] = static_cast<int32_t>(row);
+        p.map_temp[e] = p.temps[j];
+        p.map_out[e] = out;
+        p.map_req[e] = static_cast<int32_t>(j);
+    }
+}
+
+constexpr int kWriteWarps = 8;
+
+__global__ void __launch_bounds__(kWriteWarps * 32) stash_write(const __grid_constant__ StashParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t e = static_cast<int64_t>(blockIdx.x) * kWriteWarps + (threadIdx.x >> 5);
+    if (e >= p.list[0]) return;
+    const int j = p.map_req[e];
+    const int64_t out = p.map_out[e];
+    const float* xr = p.logits + static_cast<int64_t>(p.map_row[e]) * p.row_stride;
+    const float te = fmaxf(p.map_temp[e], kTempFloor);
+    const float big_m = p.row_m[e];
+    const float logs = p.row_logs[e];
+    const int32_t* keys = p.top_ids + e * p.kq;
+    const int n_ids = p.token_ids && p.num_token_ids ? p.num_token_ids[j] : 0;
+    for (int c = lane; c < p.width; c += 32) {
+        int id = 0;
+        bool has = true;
+        if (c == 0) {
+            id = keys[0];
+        } else if (n_ids > 0) {
+            has = c - 1 < n_ids;
+            if (has) id = p.token_ids[static_cast<int64_t>(j) * p.ids_stride + (c - 1)];
+        } else {
+            has = c - 1 < p.num_topk;
+            if (has) id = keys[c - 1];
+        }
+        float v;
+        if (!has) {
+            id = 0;
+            v = -INFINITY;
+        } else if (id < 0 || id >= p.vocab) {
+            v = NAN;  // a token id outside the vocabulary
+        } else {
+            const float s = __fdiv_rn(xr[id], te) + 0.0f;
+            v = p.logits_mode ? s : (big_m == -INFINITY ? NAN : (s - big_m) - logs);
+        }
+        p.out_ids[out * p.width + c] = id;
+        p.out_vals[out * p.width + c] = v;
+    }
+    // the rank of column 0's token, 1 + #{columns whose scaled logit exceeds
+    // it}: column 0 is the argmax, so none does
+    if (lane == 0) p.out_ranks[out] = 1;
+}
+
+struct StashLayout {
+    size_t list, map_row, map_temp, map_out, map_req, top_ids, top_lp, row_m, row_logs, exact, total;
+};
+
+size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+StashLayout stash_layout(int64_t requests, int64_t canvas_len, int32_t kq) {
+    const size_t R = static_cast<size_t>(requests * canvas_len);
+    const size_t K = static_cast<size_t>(kq);
+    StashLayout l{};
+    size_t at = 0;
+    auto take = [&](size_t bytes) {
+        const size_t here = at;
+        at += round_up(bytes, kWorkspaceAlign);
+        return here;
+    };
+    l.list = take(4 * (kListOffset + R));
+    l.map_row = take(4 * R);
+    l.map_temp = take(4 * R);
+    l.map_out = take(8 * R);
+    l.map_req = take(4 * R);
+    l.top_ids = take(4 * R * K);
+    l.top_lp = take(4 * R * K);
+    l.row_m = take(4 * R);
+    l.row_logs = take(4 * R);
+    l.exact = take(exact_topk_workspace_bytes(kq));
+    l.total = at;
+    return l;
+}
+
+}  // namespace
+}  // namespace drs
+
+extern "C" size_t drs_stash_workspace_bytes(int64_t requests, int64_t canvas_len, int64_t vocab,
+                                            int32_t num_topk) {
+    using namespace drs;
+    if (requests < 0 || canvas_len < 1 || vocab < 1 || num_topk < 0 ||
+        num_topk > exact_topk_max_k())
+        return 0;
+    if (requests > INT32_MAX / canvas_len) return 0;
+    return stash_layout(requests, canvas_len, num_topk > 0 ? num_topk : 1).total;
+}
+
+extern "C" drs_status drs_stash_converged_logprobs(
+    const float* logits, int64_t logits_rows, int64_t vocab, int64_t row_stride, int64_t canvas_len,
+    int64_t requests, const int32_t* src, const int32_t* slots, const uint8_t* keep,
+    const int32_t* valid, const float* temps, int32_t num_topk, const int32_t* num_token_ids,
+    const int32_t* token_ids, int64_t ids_stride, int64_t out_slots, int32_t width,
+    int32_t* out_ids, float* out_logprobs, int32_t* out_ranks, int logits_mode, void* workspace,
+    size_t workspace_bytes, void* stream) {
+    using namespace drs;
+    if (requests < 0 || logits_rows < 0 || canvas_len < 1 || out_slots < 0)
+        return DRS_ERR_INVALID_ARG;
+    if (vocab < 1 || row_stride < vocab) return DRS_ERR_INVALID_ARG;
+    if (vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
+    if (num_topk < 0 || num_topk > vocab || num_topk > exact_topk_max_k()) return DRS_ERR_INVALID_ARG;
+    if (width < 1 || width < num_topk + 1) return DRS_ERR_INVALID_ARG;
+    if (token_ids && (!num_token_ids || ids_stride < 1)) return DRS_ERR_INVALID_ARG;
+    if (requests > INT32_MAX / canvas_len || logits_rows > INT32_MAX) return DRS_ERR_UNSUPPORTED;
+    if (requests == 0) return DRS_OK;
+    if (!logits || !src || !slots || !keep || !valid || !temps || !out_ids || !out_logprobs ||
+        !out_ranks)
+        return DRS_ERR_INVALID_ARG;
+    if (!aligned(logits, 4)) return DRS_ERR_INVALID_ARG;
+    const size_t need = drs_stash_workspace_bytes(requests, canvas_len, vocab, num_topk);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, kWorkspaceAlign))
+        return DRS_ERR_INVALID_ARG;
+
+    const int32_t kq = num_topk > 0 ? num_topk : 1;
+    const StashLayout l = stash_layout(requests, canvas_len, kq);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    StashParams p{};
+    p.logits = logits;
+    p.row_stride = row_stride;
+    p.logits_rows = logits_rows;
+    p.vocab = static_cast<int32_t>(vocab);
+    p.canvas_len = canvas_len;
+    p.requests = requests;
+    p.out_slots = out_slots;
+    p.src = src;
+    p.slots = slots;
+    p.keep = keep;
+    p.valid = valid;
+    p.temps = temps;
+    p.num_topk = num_topk;
+    p.kq = kq;
+    p.num_token_ids = num_token_ids;
+    p.token_ids = token_ids;
+    p.ids_stride = ids_stride;
+    p.width = width;
+    p.logits_mode = logits_mode ? 1 : 0;
+    p.out_ids = out_ids;
+    p.out_vals = out_logprobs;
+    p.out_ranks = out_ranks;
+    p.list = reinterpret_cast<int32_t*>(ws + l.list);
+    p.map_row = reinterpret_cast<int32_t*>(ws + l.map_row);
+    p.map_temp = reinterpret_cast<float*>(ws + l.map_temp);
+    p.map_out = reinterpret_cast<int64_t*>(ws + l.map_out);
+    p.map_req = reinterpret_cast<int32_t*>(ws + l.map_req);
+    int32_t* top_ids = reinterpret_cast<int32_t*>(ws + l.top_ids);
+    float* top_lp = reinterpret_cast<float*>(ws + l.top_lp);
+    float* row_m = reinterpret_cast<float*>(ws + l.row_m);
+    float* row_logs = reinterpret_cast<float*>(ws + l.row_logs);
+    p.top_ids = top_ids;
+    p.row_m = row_m;
+    p.row_logs = row_logs;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t R = requests * canvas_len;
+    if (cudaMemsetAsync(p.list, 0, 4, st) != cudaSuccess) return DRS_ERR_CUDA;
+    stash_list<<<static_cast<int>((R + 255) / 256), 256, 0, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
+    const ExactTopkMap map{p.map_row, p.map_temp, row_m, row_logs};
+    const drs_status s = exact_topk(logits, R, vocab, row_stride, 0, nullptr, 1, nullptr, p.list, kq,
+                                    top_ids, top_lp, ws + l.exact, st, &map);
+    if (s != DRS_OK) return s;
+    stash_write<<<static_cast<int>((R + kWriteWarps - 1) / kWriteWarps), kWriteWarps * 32, 0, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? DRS_OK : DRS_ERR_CUDA;
+}

@@ -47,6 +47,12 @@ struct TopkParams {
     int64_t rows;
     int64_t row0;             // global index of row 0 (temperature and keep slot)
     const int32_t* row_list;  // null, or [0] the count and the rows from [64]
+    // With a map, the listed "rows" are entries e: logits row map_row[e],
+    // temperature map_temp[e], outputs at e (the stash's rows).
+    const int32_t* map_row;
+    const float* map_temp;
+    float* out_m;             // null, or per output row: the max scaled logit
+    float* out_logs;          // and the log of the sum of e^(s - max)
     const float* temps;
     int64_t canvas_len;
     const uint8_t* keep;
@@ -153,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t r = team_id + j * p.num_teams;
         return p.row_list ? static_cast<int64_t>(p.row_list[64 + r]) : r;
     };
+    auto logits_row = [&](int64_t r) { return p.map_row ? static_cast<int64_t>(p.map_row[r]) : r; };
     auto kept = [&](int64_t j) {
         return p.row_list != nullptr || p.keep[(p.row0 + row_of(j)) / p.canvas_len] != 0;
     };
@@ -175,8 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = static_cast<int>(issued % p.nstage);
         mbar_arrive_expect_tx(&sc.full[s], copy_bytes);
         if (copy_bytes)
-            tma_load_1d(smem + s * p.stage_bytes, p.logits + row_of(issue_j) * p.row_stride + col0,
-                        copy_bytes, &sc.full[s]);
+            tma_load_1d(smem + s * p.stage_bytes,
+                        p.logits + logits_row(row_of(issue_j)) * p.row_stride + col0, copy_bytes,
+                        &sc.full[s]);
         ++issue_j;
         ++issued;
         return true;
@@ -191,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t j = next_kept(0);
     for (int64_t kk = 0; j < nrows; ++kk, j = next_kept(j + 1)) {
         const int64_t row = row_of(j);
-        const float* grow = p.logits + row * p.row_stride + col0;
+        const float* grow = p.logits + logits_row(row) * p.row_stride + col0;
 
         // ---- load and scale ------------------------------------------------
         bool timed_out = false;
@@ -227,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             issue_next();
         }
-        const ScaledQuotient sq =
-            ScaledQuotient::of(fmaxf(p.temps[(p.row0 + row) / p.canvas_len], kTempFloor));
+        const float temp = p.map_temp ? p.map_temp[row] : p.temps[(p.row0 + row) / p.canvas_len];
+        const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
 #pragma unroll
         for (int i = 0; i < VEC4; ++i) {
             // x / te exactly (infinities kept), then -0.0 -> +0.0 (one value
@@ -407,6 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float big_m = sc.row_max;
         const float logs = sc.row_logs;
+        if (p.out_m && member == 0 && tid == 0) {
+            p.out_m[row] = big_m;
+            p.out_logs[row] = logs;
+        }
 
         // Rank my keys (thread t holds my_keys[t] and my_keys[t + 512])
         // against all G*K published keys, staged through shared memory in
@@ -530,8 +542,9 @@ __global__ void __launch_bounds__(kThreads, kWideCtasPerSm)
         const int64_t row = p.row_list ? static_cast<int64_t>(p.row_list[64 + j]) : j;
         const int64_t slot = (p.row0 + row) / p.canvas_len;
         if (!p.row_list && p.keep[slot] == 0) continue;
-        const float* xr = p.logits + row * p.row_stride;
-        const ScaledQuotient sq = ScaledQuotient::of(fmaxf(p.temps[slot], kTempFloor));
+        const float* xr = p.logits + (p.map_row ? static_cast<int64_t>(p.map_row[row]) : row) * p.row_stride;
+        const float temp = p.map_temp ? p.map_temp[row] : p.temps[slot];
+        const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
 
         // ---- radix select of the k-th largest value key, with m and S ----
         uint32_t prefix = 0, pmask = 0;
@@ -645,6 +658,10 @@ __global__ void __launch_bounds__(kThreads, kWideCtasPerSm)
 
         // ---- rank the k keys and write them -------------------------------
         const float logs = sh.logs;
+        if (p.out_m && tid == 0) {
+            p.out_m[row] = m;
+            p.out_logs[row] = logs;
+        }
         for (int c = tid; c < K; c += kThreads) {
             const int64_t key = sh.cand[c];
             int rank = 0;
@@ -690,7 +707,7 @@ size_t exact_topk_workspace_bytes(int32_t k) {
 drs_status exact_topk(const float* logits, int64_t rows, int64_t vocab, int64_t row_stride,
                       int64_t row0, const float* temps, int64_t canvas_len, const uint8_t* keep,
                       const int32_t* row_list, int32_t k, int32_t* out_ids, float* out_logprobs,
-                      void* workspace, cudaStream_t stream) {
+                      void* workspace, cudaStream_t stream, const ExactTopkMap* map) {
     const int sms = sm_count();
     if (sms <= 0) return DRS_ERR_CUDA;
     const RowPlan plan = plan_rows(rows, static_cast<int>(vocab), sms, false);
@@ -709,6 +726,12 @@ drs_status exact_topk(const float* logits, int64_t rows, int64_t vocab, int64_t 
         w.out_lp = out_logprobs;
         w.k = k;
         w.vocab = static_cast<int32_t>(vocab);
+        if (map) {
+            w.map_row = map->row;
+            w.map_temp = map->temp;
+            w.out_m = map->out_m;
+            w.out_logs = map->out_logs;
+        }
         w.nstage = aligned(logits, 16) && (row_stride % 4 == 0) ? 1 : 0;
         const int64_t g = row_list ? static_cast<int64_t>(kWideCtasPerSm) * sms
                                    : std::min<int64_t>(rows, static_cast<int64_t>(kWideCtasPerSm) * sms);
@@ -736,6 +759,12 @@ drs_status exact_topk(const float* logits, int64_t rows, int64_t vocab, int64_t 
     prm.chunk = plan.chunk;
     prm.num_teams = plan.num_teams;
     prm.rec_bytes = static_cast<int32_t>(record_bytes(k));
+    if (map) {
+        prm.map_row = map->row;
+        prm.map_temp = map->temp;
+        prm.out_m = map->out_m;
+        prm.out_logs = map->out_logs;
+    }
     if (!prm.err) return DRS_ERR_CUDA;
 
     const bool tma = aligned(logits, 16) && (row_stride % 4 == 0);
