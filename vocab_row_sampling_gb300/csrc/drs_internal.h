@@ -77,6 +77,15 @@ struct RowCall {
     int32_t* out_ids;
     float* out_lp;
     bool stats;
+    // Row map (the stash; all null otherwise): the call's rows are entries e
+    // < *map_count (device) of a list, read from logits row map_row[e] with
+    // temperature map_temp[e], every entry kept (keep and temps unused);
+    // out_m / out_logs receive each entry's max scaled logit and log S.
+    const int32_t* map_row;
+    const float* map_temp;
+    const int32_t* map_count;
+    float* out_m;
+    float* out_logs;
 };
 
 // The fault-injection test hook (drs_test_inject_fault): the pending code,

@@ -188,6 +188,15 @@ struct SplitParams {
     TileEnd* te;      // by tile
     TileSeed* tb;     // by tile and seed
     uint64_t* keys;   // by tile
+    // Row map (the stash): rows are entries e < *map_count of a list, read
+    // from logits row map_row[e] with temperature map_temp[e], all kept;
+    // null for the ordinary calls. out_m / out_logs (or null) receive each
+    // row's max scaled logit and log S from the merge.
+    const int32_t* map_row;
+    const float* map_temp;
+    const int32_t* map_count;
+    float* out_m;
+    float* out_logs;
     int li_begin;     // the list entries of this launch: [li_begin, li_end),
     int li_end;       // li_end < 0: to the end of the list
     int* err;
@@ -308,6 +317,7 @@ struct Pipe {
     int abort;
     int row[kMap];
     int col[kMap];
+    int lrow[kMap];  // the logits row of `row` (differs under a row map)
 };
 
 // The tiles of a launch: [t_begin, t_end) of the list's tile space.
@@ -316,19 +326,21 @@ struct TileRange {
 };
 
 // Map tiles first .. first + nfill - 1 (one per lane or thread).
-__device__ __forceinline__ void map_tiles(Pipe& pp, const int32_t* list, TileRange tr, int G,
-                                          int first, int nfill, int idx) {
+__device__ __forceinline__ void map_tiles(Pipe& pp, const int32_t* list, const int32_t* map_row,
+                                          TileRange tr, int G, int first, int nfill, int idx) {
     if (idx >= nfill) return;
     const int n = first + idx;
     const int64_t t = tr.t_begin + static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
-    int row = -1, c = 0;
+    int row = -1, c = 0, lrow = -1;
     if (t < tr.t_end) {
         const uint32_t li = static_cast<uint32_t>(t) / static_cast<uint32_t>(G);
         c = static_cast<int>(static_cast<uint32_t>(t) - li * static_cast<uint32_t>(G));
         row = list[li];
+        lrow = map_row ? map_row[row] : row;
     }
     pp.row[n % kMap] = row;
     pp.col[n % kMap] = c;
+    pp.lrow[n % kMap] = lrow;
 }
 
 // Issue tile n into its stage: the row's record (`rec_bytes` of `rec_table`)
@@ -356,7 +368,9 @@ __device__ __forceinline__ void issue_tile(const SplitParams& p, Pipe& pp, int n
     mbar_arrive_expect_tx(&pp.full[st], bytes + rec_bytes);
     tma_load_1d(rec_dst, static_cast<const unsigned char*>(rec_table) + static_cast<size_t>(row) * rec_bytes,
                 rec_bytes, &pp.full[st]);
-    if (bytes) tma_load_1d(stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, bytes, &pp.full[st]);
+    if (bytes)
+        tma_load_1d(stage, p.logits + static_cast<int64_t>(pp.lrow[n % kMap]) * p.row_stride + col0, bytes,
+                    &pp.full[st]);
 }
 
 // The list entries and tiles of this launch.
@@ -399,7 +413,7 @@ __device__ __forceinline__ void pipe_start(const SplitParams& p, Pipe& pp, const
         pp.abort = 0;
         fence_barrier_init();
     }
-    map_tiles(pp, list, tiles, p.tiles_per_row, 0, kMap, tid);
+    map_tiles(pp, list, p.map_row, tiles, p.tiles_per_row, 0, kMap, tid);
     __syncthreads();
     if (tid == 0)
         for (int s = 0; s < kStages; ++s)
@@ -417,7 +431,7 @@ __device__ __forceinline__ void pipe_advance(const SplitParams& p, Pipe& pp, int
         fence_proxy_async_smem();
         issue_tile(p, pp, n + kStages, stage, rec_dst, rec_table, rec_bytes, tma);
     }
-    if ((n & 31) == 31) map_tiles(pp, list, tiles, p.tiles_per_row, n + 33, 32, lane);
+    if ((n & 31) == 31) map_tiles(pp, list, p.map_row, tiles, p.tiles_per_row, n + 33, 32, lane);
 }
 
 // After the loop: if a wait ran out, copies still in flight land before the
@@ -469,11 +483,17 @@ __global__ void __launch_bounds__(256) split_prep(const __grid_constant__ SplitP
     const int lane = threadIdx.x & 31;
     bool work = false;
     if (row < p.rows) {
-        const uint64_t slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
-        const bool kept = p.keep == nullptr || p.keep[slot] != 0;
-        work = p.stats || (p.k > 0 && kept);
+        uint64_t slot = 0;
+        bool kept;
+        if (p.map_row) {
+            kept = row < *p.map_count;  // every listed entry is kept
+        } else {
+            slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
+            kept = p.keep == nullptr || p.keep[slot] != 0;
+        }
+        work = (p.stats && !p.map_row) || (p.k > 0 && kept);
         if (work) {
-            const float temp = p.temps[slot];
+            const float temp = p.map_row ? p.map_temp[row] : p.temps[slot];
             const ScaledQuotient q = ScaledQuotient::of(fmaxf(temp, kTempFloor));
             p.rt[row] = RowTemp{temp, q.t, q.y, q.mode};
         }
@@ -517,10 +537,10 @@ __device__ __forceinline__ void tile_sums(const float4 (&v)[kSVec4], float lscal
 // One warp's share of a pass-1 tile: M_w's raw max and its lowest column,
 // S_w and W_w relative to it.
 __device__ __forceinline__ WarpPart p1_warp(const SplitParams& p, float4* stage, const ScaledQuotient& sq,
-                                            int row, int col0, int ncols, int tid, int lane, bool stats,
+                                            int lrow, int col0, int ncols, int tid, int lane, bool stats,
                                             bool tma) {
     float4 v[kSVec4];
-    read_tile(v, stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, ncols, tid, tma);
+    read_tile(v, stage, p.logits + static_cast<int64_t>(lrow) * p.row_stride + col0, ncols, tid, tma);
 
     // max of the raw logits (division by Te > 0 keeps the order)
     float m4[kSVec4];
@@ -653,7 +673,7 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
         sq.t = rts[st].qt;
         sq.y = rts[st].qy;
         sq.mode = rts[st].qmode;
-        const WarpPart wp = p1_warp(p, stage, sq, row, col0, ncols, tid, lane, stats, tma);
+        const WarpPart wp = p1_warp(p, stage, sq, pp.lrow[n % kMap], col0, ncols, tid, lane, stats, tma);
         if (lane == 0) parts[par][st][warp] = wp;
         if (!release_stage(&pp.count[st], lane)) continue;
 
@@ -677,8 +697,8 @@ constexpr int kRowWarps = 8;  // rows per CTA of the merge and finish kernels
 template <int NU>
 __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int lane) {
     const int64_t row = p.list1[li];
-    const uint64_t slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
-    const bool kept = p.keep == nullptr || p.keep[slot] != 0;
+    const bool kept =
+        p.map_row || p.keep == nullptr || p.keep[slot_of(p, static_cast<uint64_t>(p.row0 + row))] != 0;
     const RowTemp rt = p.rt[row];
     const float temp = rt.temp;
     const int G = p.tiles_per_row;
@@ -809,6 +829,10 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
         rec.flags = (noisy ? kFNoisy : 0) | (topk && !hard ? kFTopk : 0) | (raw ? kFRaw : 0);
         *reinterpret_cast<RowRecord*>(entry) = rec;
         if (p.stats) p.entropy[row] = s_tot > 0.0f ? logf(s_tot) - w_tot / s_tot : 0.0f;
+        if (p.out_m) {
+            p.out_m[row] = big_m;
+            p.out_logs[row] = rec.lns;
+        }
         if (hard) {
             const int idx = atomicAdd(p.hard, 1);
             p.hard[kHardOffset + idx] = static_cast<int32_t>(row);
@@ -973,7 +997,7 @@ struct P2Shared {
 // round keys read as constants.
 template <bool MULTI>
 __device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& sh, float4* stage,
-                                        const unsigned char* entry, int row, int64_t t, int col0,
+                                        const unsigned char* entry, int row, int lrow, int64_t t, int col0,
                                         int ncols, int st, int par, int tid, int lane, int warp,
                                         bool stats, bool probs, bool tma) {
     const RowRecord& rec = *reinterpret_cast<const RowRecord*>(entry);
@@ -991,7 +1015,7 @@ __device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& s
         sq.y = rec.qy;
         sq.mode = rec.qmode;
         float4 v[kSVec4];
-        read_tile(v, stage, p.logits + static_cast<int64_t>(row) * p.row_stride + col0, ncols, tid, tma);
+        read_tile(v, stage, p.logits + static_cast<int64_t>(lrow) * p.row_stride + col0, ncols, tid, tma);
 
         if (probs) {
             uint16_t* prow = static_cast<uint16_t*>(p.probs) + static_cast<int64_t>(row) * p.probs_row_stride + col0;
@@ -1172,8 +1196,8 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
         const int64_t t = tiles.t_begin + static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
         const int col0 = pp.col[n % kMap] * kTileCols;
         const int ncols = min(p.vocab - col0, kTileCols);
-        const bool topk = p2_warp<MULTI>(p, sh, stage, &recs[st][0], row, t, col0, ncols, st, par, tid, lane,
-                                         warp, stats, probs, tma);
+        const bool topk = p2_warp<MULTI>(p, sh, stage, &recs[st][0], row, pp.lrow[n % kMap], t, col0, ncols, st,
+                                         par, tid, lane, warp, stats, probs, tma);
         if (!release_stage(&pp.count[st], lane)) continue;
 
         // the last warp out: the tile's records (the row entry in the stage
@@ -1373,6 +1397,11 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     p.te = reinterpret_cast<TileEnd*>(ws + l.te);
     p.tb = reinterpret_cast<TileSeed*>(ws + l.tb);
     p.keys = reinterpret_cast<uint64_t*>(ws + l.keys);
+    p.map_row = c.map_row;
+    p.map_temp = c.map_temp;
+    p.map_count = c.map_count;
+    p.out_m = c.out_m;
+    p.out_logs = c.out_logs;
     p.err = device_error_flag();
     if (!p.err) return DRS_ERR_CUDA;
     for (int sd = 0; sd < n_seeds; ++sd)

@@ -13,9 +13,12 @@
 // Kernels, in stream order:
 //   list   one thread per (request, position): the stash rows to write, each
 //          with its logits row, temperature, output row and request;
-//   top-k  the exact top-k kernel over that list with k = max(num_topk, 1)
-//          (its first key is the argmax: keys order by value, then by lower
-//          column), which also leaves each entry's max and log-sum;
+//   top-k  k = max(num_topk, 1) keys per entry (the first is the argmax:
+//          keys order by value, then by lower column), with each entry's max
+//          and log-sum: for k <= 64 the two streaming passes over the listed
+//          rows (row_split.cu, with the list as a row map), then the exact
+//          kernel on the rows they leave; for larger k the exact kernel on
+//          every entry;
 //   write  one warp per entry: the row's columns, values from one IEEE
 //          division each.
 // Rows of requests that are not kept are never read.
@@ -138,12 +141,13 @@ __global__ void __launch_bounds__(kWriteWarps * 32) stash_write(const __grid_con
 }
 
 struct StashLayout {
-    size_t list, map_row, map_temp, map_out, map_req, top_ids, top_lp, row_m, row_logs, exact, total;
+    size_t list, map_row, map_temp, map_out, map_req, top_ids, top_lp, row_m, row_logs, split, exact,
+        total;
 };
 
 size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
 
-StashLayout stash_layout(int64_t requests, int64_t canvas_len, int32_t kq) {
+StashLayout stash_layout(int64_t requests, int64_t canvas_len, int64_t vocab, int32_t kq) {
     const size_t R = static_cast<size_t>(requests * canvas_len);
     const size_t K = static_cast<size_t>(kq);
     StashLayout l{};
@@ -162,6 +166,7 @@ StashLayout stash_layout(int64_t requests, int64_t canvas_len, int32_t kq) {
     l.top_lp = take(4 * R * K);
     l.row_m = take(4 * R);
     l.row_logs = take(4 * R);
+    l.split = take(kq <= split_max_k() ? split_workspace_bytes(static_cast<int64_t>(R), vocab, kq, 1) : 0);
     l.exact = take(exact_topk_workspace_bytes(kq));
     l.total = at;
     return l;
@@ -177,7 +182,7 @@ extern "C" size_t drs_stash_workspace_bytes(int64_t requests, int64_t canvas_len
         num_topk > exact_topk_max_k())
         return 0;
     if (requests > INT32_MAX / canvas_len) return 0;
-    return stash_layout(requests, canvas_len, num_topk > 0 ? num_topk : 1).total;
+    return stash_layout(requests, canvas_len, vocab, num_topk > 0 ? num_topk : 1).total;
 }
 
 extern "C" drs_status drs_stash_converged_logprobs(
@@ -206,7 +211,7 @@ extern "C" drs_status drs_stash_converged_logprobs(
         return DRS_ERR_INVALID_ARG;
 
     const int32_t kq = num_topk > 0 ? num_topk : 1;
-    const StashLayout l = stash_layout(requests, canvas_len, kq);
+    const StashLayout l = stash_layout(requests, canvas_len, vocab, kq);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     StashParams p{};
     p.logits = logits;
@@ -250,8 +255,34 @@ extern "C" drs_status drs_stash_converged_logprobs(
     stash_list<<<static_cast<int>((R + 255) / 256), 256, 0, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
     const ExactTopkMap map{p.map_row, p.map_temp, row_m, row_logs};
-    const drs_status s = exact_topk(logits, R, vocab, row_stride, 0, nullptr, 1, nullptr, p.list, kq,
-                                    top_ids, top_lp, ws + l.exact, st, &map);
+    const int32_t* exact_list = p.list;
+    if (kq <= split_max_k()) {
+        // the two passes over the listed rows; the rows they leave (no
+        // threshold, too many candidates) are on the hard-row list at the
+        // start of their workspace
+        RowCall c{};
+        c.logits = logits;
+        c.rows = R;
+        c.vocab = vocab;
+        c.row_stride = row_stride;
+        c.canvas_len = 1;
+        c.n_seeds = 1;
+        c.probs_dtype = DRS_PROBS_NONE;
+        c.k = kq;
+        c.out_ids = top_ids;
+        c.out_lp = top_lp;
+        c.stats = false;
+        c.map_row = p.map_row;
+        c.map_temp = p.map_temp;
+        c.map_count = p.list;
+        c.out_m = row_m;
+        c.out_logs = row_logs;
+        const drs_status s = split_rows(c, ws + l.split, st);
+        if (s != DRS_OK) return s;
+        exact_list = reinterpret_cast<const int32_t*>(ws + l.split);
+    }
+    const drs_status s = exact_topk(logits, R, vocab, row_stride, 0, nullptr, 1, nullptr, exact_list,
+                                    kq, top_ids, top_lp, ws + l.exact, st, &map);
     if (s != DRS_OK) return s;
     stash_write<<<static_cast<int>((R + kWriteWarps - 1) / kWriteWarps), kWriteWarps * 32, 0, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? DRS_OK : DRS_ERR_CUDA;
