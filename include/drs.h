@@ -335,6 +335,8 @@ size_t drs_stash_workspace_bytes(int64_t requests, int64_t canvas_len, int64_t v
  *                   logits_rows or out_slots are not touched.
  *   workspace       drs_stash_workspace_bytes(requests, canvas_len, vocab,
  *                   num_topk) bytes.
+ * The slots of kept requests must be distinct: two requests writing one
+ * stash row race (which one lands is not defined).
  * All pointers are device memory owned by the caller; asynchronous on
  * `stream`. Returns DRS_ERR_INVALID_ARG for a null required pointer,
  * negative sizes, row_stride < vocab, num_topk outside [0, min(vocab,
