@@ -69,6 +69,7 @@ struct TopkParams {
     int32_t nstage;
     int32_t stage_bytes;
     int32_t rec_bytes;
+    int32_t vec;              // the one-CTA kernel: rows start 16-byte aligned (float4 loads)
 };
 
 // Record header; the k keys follow it.
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, kWideCtasPerSm)
     const int warp = tid >> 5;
     const int K = p.k;
     const int V = p.vocab;
-    const bool vec = p.nstage != 0;  // rows start 16-byte aligned
+    const bool vec = p.vec != 0;
     const int64_t nlisted = p.row_list ? static_cast<int64_t>(p.row_list[0]) : p.rows;
     for (int64_t j = blockIdx.x; j < nlisted; j += gridDim.x) {
         const int64_t row = p.row_list ? static_cast<int64_t>(p.row_list[64 + j]) : j;
@@ -732,7 +733,7 @@ drs_status exact_topk(const float* logits, int64_t rows, int64_t vocab, int64_t 
             w.out_m = map->out_m;
             w.out_logs = map->out_logs;
         }
-        w.nstage = aligned(logits, 16) && (row_stride % 4 == 0) ? 1 : 0;
+        w.vec = aligned(logits, 16) && (row_stride % 4 == 0) ? 1 : 0;
         const int64_t g = row_list ? static_cast<int64_t>(kWideCtasPerSm) * sms
                                    : std::min<int64_t>(rows, static_cast<int64_t>(kWideCtasPerSm) * sms);
         topk_wide_kernel<<<static_cast<int>(g), kThreads, 0, stream>>>(w);
