@@ -1060,9 +1060,10 @@ __device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& s
             acand = warp_min_nonneg(acand);
         }
 
-        // the race, once per seed
+        // the race
         const bool rawr = (flags & kFRaw) != 0;
-        const int nsd = MULTI ? p.n_seeds : 1;
+        if constexpr (!MULTI) {
+        const int nsd = 1;
         for (int sd = 0; sd < nsd; ++sd) {
         const SeedRec sr = seeds[sd];
         const PhiloxRoundKeys& rk = MULTI ? p.rk[sd] : p.rk[0];
@@ -1123,6 +1124,88 @@ __device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& s
         if (lane == 0) {
             sh.best_s[par][st][sd][warp] = wb;
             sh.best_c[par][st][sd][warp] = wc;
+        }
+        }
+        } else {
+        // several seeds: one list of the groups that some seed can still use
+        // (the bound of the seed with the smallest cB, or B: the bound falls
+        // with both), each listed group then raced for every seed in turn
+        // (its float4 read once; a seed whose own bound drops the group skips
+        // its noise)
+        const int nsd = p.n_seeds;
+        float wbs[kMaxSeeds];
+        int wcs[kMaxSeeds];
+#pragma unroll
+        for (int sd = 0; sd < kMaxSeeds; ++sd) {
+            wbs[sd] = sd < nsd ? seeds[sd].B : -INFINITY;
+            wcs[sd] = sd < nsd ? seeds[sd].bcol : INT_MAX;
+        }
+        if (noisy) {
+            float c_lo = INFINITY, b_lo = INFINITY;
+            for (int sd = 0; sd < nsd; ++sd) {
+                c_lo = fminf(c_lo, seeds[sd].cB);
+                b_lo = fminf(b_lo, seeds[sd].B);
+            }
+            uint32_t pass = 0;
+            if (rawr) {
+                const float ls = rec.ls;
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i)
+                    if (fmaf(m4[i], ls, -c_lo) >= -24.0f) pass |= 1u << i;
+            } else {
+#pragma unroll
+                for (int i = 0; i < kSVec4; ++i)
+                    if (fmaf(sq.exact(m4[i]) - b_lo, kLog2e, kRaceSlack) >= -24.0f) pass |= 1u << i;
+            }
+            const uint32_t lt = lanemask_lt();
+            int total = 0;
+#pragma unroll
+            for (int i = 0; i < kSVec4; ++i) {
+                const bool on = (pass >> i) & 1u;
+                const uint32_t bl = __ballot_sync(0xffffffffu, on);
+                if (on) sh.race_at[warp][total + __popc(bl & lt)] = static_cast<uint16_t>(i * kSThreads + tid);
+                total += __popc(bl);
+            }
+            __syncwarp();
+            for (int m = lane; m < total; m += 32) {
+                const int f = sh.race_at[warp][m];
+                const float4 x4 = stage[f];
+                const int c4 = col0 + 4 * f;
+                const float mx = max4f(x4);
+                const float ex = rawr ? 0.0f : sq.exact(mx);
+#pragma unroll
+                for (int sd = 0; sd < kMaxSeeds; ++sd) {
+                    if (sd >= nsd) break;
+                    const SeedRec& sr = seeds[sd];
+                    const float t = rawr ? fmaf(mx, rec.ls, -sr.cB) : fmaf(ex - sr.B, kLog2e, kRaceSlack);
+                    if (!(t >= -24.0f)) continue;  // this seed's bound drops the group
+                    const uint4 nw = noise_group(p.rk[sd], grow, static_cast<uint32_t>(c4 >> 2));
+                    const uint32_t wmax = max(max(nw.x, nw.y), max(nw.z, nw.w));
+                    if (one_minus_u_lower(wmax) <= ex2_ftz(t)) {
+                        const float4 e = race_e(x4, rawr, rec.ls, sr, sq);
+                        uint32_t bits = 0;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (one_minus_u_lower(word_of(nw, q)) <= comp(e, q)) bits |= 1u << q;
+                        if (bits) {
+                            const Best b2 = race_rescore(bits, x4, nw, c4, sr.bcol, sq, Best{wbs[sd], wcs[sd]});
+                            wbs[sd] = b2.s;
+                            wcs[sd] = b2.c;
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int sd = 0; sd < kMaxSeeds; ++sd) {
+            if (sd >= nsd) break;
+            float wb = wbs[sd];
+            int wc = wcs[sd];
+            warp_best(wb, wc);
+            if (lane == 0) {
+                sh.best_s[par][st][sd][warp] = wb;
+                sh.best_c[par][st][sd][warp] = wc;
+            }
         }
         }
 
