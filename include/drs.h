@@ -55,7 +55,7 @@ typedef enum drs_probs_dtype {
  * contents arbitrary: each call clears the counters it uses with an
  * asynchronous memset on its stream before its kernels run). The workspace
  * carries the row lists and the per-tile and per-row records through which
- * the kernels of one call pass their partial results: about 2.6 KiB per row
+ * the kernels of one call pass their partial results: about 3.6 KiB per row
  * of 262144 columns, growing with rows and vocab. One workspace must not be
  * used by two calls that can run at the same time.
  */
