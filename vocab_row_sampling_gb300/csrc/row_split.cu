@@ -1130,8 +1130,9 @@ __device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& s
         // several seeds: one list of the groups that some seed can still use
         // (the bound of the seed with the smallest cB, or B: the bound falls
         // with both), each listed group then raced for every seed in turn
-        // (its float4 read once; a seed whose own bound drops the group skips
-        // its noise)
+        // (its float4 read once; each seed's noise drawn without a branch
+        // before it, so the chains of consecutive seeds overlap, and a seed
+        // whose own bound drops the group only fails the test)
         const int nsd = p.n_seeds;
         float wbs[kMaxSeeds];
         int wcs[kMaxSeeds];
@@ -1178,10 +1179,9 @@ __device__ __forceinline__ bool p2_warp(const SplitParams& p, P2Shared<MULTI>& s
                     if (sd >= nsd) break;
                     const SeedRec& sr = seeds[sd];
                     const float t = rawr ? fmaf(mx, rec.ls, -sr.cB) : fmaf(ex - sr.B, kLog2e, kRaceSlack);
-                    if (!(t >= -24.0f)) continue;  // this seed's bound drops the group
                     const uint4 nw = noise_group(p.rk[sd], grow, static_cast<uint32_t>(c4 >> 2));
                     const uint32_t wmax = max(max(nw.x, nw.y), max(nw.z, nw.w));
-                    if (one_minus_u_lower(wmax) <= ex2_ftz(t)) {
+                    if (t >= -24.0f && one_minus_u_lower(wmax) <= ex2_ftz(t)) {
                         const float4 e = race_e(x4, rawr, rec.ls, sr, sq);
                         uint32_t bits = 0;
 #pragma unroll
