@@ -360,7 +360,8 @@ def _run_ours(args, world, rank, local):
                            "avg_ms": round(stash_avg_ms, 4),
                            "gbs_read": round(bytes_tk / (stash_avg_ms / 1e3) / 1e9, 1),
                            "frac_of_peak": round(bytes_tk / (stash_avg_ms / 1e3) / 1e9 / peak, 4),
-                           "note": "the kept rows' stash (argmax + top-k), one read per kept row"}},
+                           "note": "the kept rows' stash (argmax + top-k) over its algorithmic bytes, one "
+                                   "read per kept row (the two passes read it twice)"}},
            # per step: list of rows, pass 1, merge, pass 2, finish, exact top-k
            "gpu_launches": 6 * args.steps,
            "clocks": clocks}
