@@ -353,26 +353,6 @@ struct ScaledQuotient {
         return fmaf(r, y, q);
     }
 
-    // Scale registers in place (mode hoisted out of the element loop); slot
-    // i of a thread is live when i * STRIDE < live_slots.
-    template <int VEC4, int STRIDE = kThreads>
-    __device__ __forceinline__ void apply(float4 (&v)[VEC4], int live_slots) const {
-        if (mode == kScale) {
-#pragma unroll
-            for (int i = 0; i < VEC4; ++i)
-                if (i * STRIDE < live_slots) {
-                    v[i].x *= y; v[i].y *= y; v[i].z *= y; v[i].w *= y;
-                }
-        } else if (mode == kDivide) {
-#pragma unroll
-            for (int i = 0; i < VEC4; ++i)
-                if (i * STRIDE < live_slots) {
-                    v[i].x = divide(v[i].x); v[i].y = divide(v[i].y);
-                    v[i].z = divide(v[i].z); v[i].w = divide(v[i].w);
-                }
-        }
-    }
-
     // Where the corrections are exact: the quotient and the dividend both
     // well inside the normal range, so that q*t, x*y and the remainder
     // x - q*t neither overflow nor underflow (a subnormal remainder loses

@@ -43,16 +43,20 @@
 //          s - M - log S. Rows whose candidates overflow the lists, or that
 //          have no threshold, go on a device list for the exact top-k kernel.
 //
-// The passes stream their tiles through three shared-memory stages filled by
-// bulk copies (TMA), the row's record riding along with each tile. Warps run
-// freely: a warp waits for a stage's copy, works on the tile and counts
-// itself out of the stage; the warp that counts out last finishes the tile
-// (combines the warps' results) and refills the stage. No CTA-wide barrier
-// in the loop.
+// The passes stream their tiles through two shared-memory stages per CTA
+// (three CTAs per SM) filled by bulk copies (TMA), the row's record riding
+// along with each tile. Warps run freely: a warp waits for a stage's copy,
+// works on the tile and counts itself out of the stage; the warp that
+// counts out last finishes the tile (combines the warps' results) and
+// refills the stage. No CTA-wide barrier in the loop.
 //
 // HBM traffic: every logit is read twice (once per pass) and every
 // probability written once; the records are a few bytes per thousand
 // logits. No fp64 arithmetic.
+//
+// A call can also pass a row map (the stash): its rows are then the entries
+// of a device list, each read from a mapped logits row with a mapped
+// temperature.
 #include <cfloat>
 #include <climits>
 
