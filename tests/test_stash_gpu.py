@@ -125,3 +125,24 @@ def test_stash_step_sized_batch():
     for j in np.flatnonzero(keep == 0):
         assert np.all(ids[slots[j]] == -1) and np.all(ranks[slots[j]] == -1)
     assert np.all(ids[slots[2], 100:] == -1)          # positions past valid[2]
+
+
+def test_stash_skips_requests_outside_the_buffers():
+    """A request whose logits rows lie past the logits, or whose slot lies
+    past the stash, is skipped without touching any output; the others are
+    those of the oracle run without it."""
+    x, src, slots, keep, valid, temps, tok, nti, m, canvas = _batch(21, 999)
+    keep = np.ones(m, np.uint8)
+    bad_src, bad_slot = src.copy(), slots.copy()
+    bad_src[1] = 10**6                      # rows far past the logits
+    bad_slot[4] = m + 2                     # one past the stash's slots (valid[4] = 3)
+    out_slots, width, k = m + 2, 6, 4
+    g_ids, g_vals, g_ranks = _run(x, canvas, bad_src, bad_slot, keep, valid, temps, k, None, None,
+                                  out_slots, width, False)
+    ok = np.array([j not in (1, 4) for j in range(m)])
+    r_ids, r_vals, r_ranks = oracle.stash(x, canvas, src[ok], slots[ok], keep[ok], valid[ok],
+                                          temps[ok], k, None, None, out_slots, width)
+    written = r_ranks != -1
+    assert np.all(g_ids[~written] == SENT_ID) and np.all(g_ranks[~written] == SENT_R)
+    assert np.array_equal(g_ranks[written], r_ranks[written])
+    check_topk(g_ids[written], g_vals[written], r_ids[written], r_vals[written], "skipped requests")
