@@ -107,12 +107,12 @@ def test_repeated_calls_are_deterministic():
             assert np.array_equal(one[k], again[k]), k
 
 
-@pytest.mark.parametrize("which", ["400000", "491520", "491521", "1000003", "max"])
+@pytest.mark.parametrize("which", ["400000", "368640", "368641", "491520", "1000003", "max"])
 def test_long_rows(which):
-    """Rows of many tiles with a ragged last one: 400000 columns (49 tiles,
-    the last 6784 wide); 60 tiles, the longest rows of the merge's short-row
-    instantiation, and one column more (61 tiles, the last one column wide);
-    1000003 columns; the largest supported vocabulary (256 tiles)."""
+    """Rows of many tiles with a ragged last one: 400000 columns; 368640, the
+    longest rows of the merge's short-row instantiation (60 pass-1 tiles),
+    and one column more; 491520 (60 pass-2 tiles); 1000003 columns; the
+    largest supported vocabulary."""
     import vocab_row_sampling_gb300 as drs
     vocab = drs.DRS_MAX_VOCAB if which == "max" else int(which)
     rng = np.random.default_rng(1)

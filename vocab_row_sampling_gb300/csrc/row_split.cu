@@ -83,13 +83,21 @@ constexpr int kSWarps = kSThreads / 32;
 #ifndef DRS_P2_MINB
 #define DRS_P2_MINB 3
 #endif
-constexpr int kSVec4 = DRS_SPLIT_VEC4;             // float4 slots per thread
-constexpr int kTileCols = kSThreads * kSVec4 * 4;  // 8192
+#ifndef DRS_P1_VEC4
+#define DRS_P1_VEC4 6
+#endif
+constexpr int kSVec4 = DRS_SPLIT_VEC4;             // pass 2: float4 slots per thread
+constexpr int kTileCols = kSThreads * kSVec4 * 4;  // 8192 columns per pass-2 tile
 constexpr int kMaxTiles = (DRS_MAX_VOCAB + kTileCols - 1) / kTileCols;
-// warp maxima per lane in the merge: rows of up to 60 tiles (491520
+// Pass 1 has tiles of its own (measured: it streams faster with 24 KiB tiles
+// than with pass 2's 32 KiB ones, pass 2 the other way round).
+constexpr int kP1Vec4 = DRS_P1_VEC4;
+constexpr int kP1Cols = kSThreads * kP1Vec4 * 4;   // 6144 columns per pass-1 tile
+constexpr int kMaxTiles1 = (DRS_MAX_VOCAB + kP1Cols - 1) / kP1Cols;
+// warp maxima per lane in the merge: rows of up to 60 pass-1 tiles (368640
 // columns), and the longest rows
 constexpr int kOrdSmall = (60 * kSWarps + 31) / 32;
-constexpr int kOrdLarge = (kMaxTiles * kSWarps + 31) / 32;
+constexpr int kOrdLarge = (kMaxTiles1 * kSWarps + 31) / 32;
 constexpr int kTilesSmall = (60 + 31) / 32;  // tiles per lane in the finish
 constexpr int kTilesLarge = (kMaxTiles + 31) / 32;
 constexpr int kStages = DRS_SPLIT_STAGES;          // tiles in flight per CTA
@@ -208,7 +216,8 @@ struct SplitParams {
     int n_seeds;
     int rec_bytes;    // sizeof(RowRecord) + n_seeds * sizeof(SeedRec)
     int vocab;
-    int tiles_per_row;
+    int tiles_per_row;  // pass-2 tiles of a row (the finish's records)
+    int tiles1;         // pass-1 tiles of a row (the merge's records)
     int vec;          // rows start 16-byte aligned: bulk copies
     int probs_dtype;  // 0 none, 1 bf16, 2 fp16
     int probs_vec;    // 8-byte probability stores
@@ -350,7 +359,8 @@ __device__ __forceinline__ void map_tiles(Pipe& pp, const int32_t* list, const i
 // Issue tile n into its stage: the row's record (`rec_bytes` of `rec_table`)
 // and the tile's whole float4s by bulk copy when rows start 16-byte aligned
 // (else the warps read global memory themselves). Past the end: a plain
-// arrival.
+// arrival. COLS: the pass's tile width.
+template <int COLS>
 __device__ __forceinline__ void issue_tile(const SplitParams& p, Pipe& pp, int n, float4* stage,
                                            void* rec_dst, const void* rec_table, uint32_t rec_bytes,
                                            bool tma) {
@@ -366,8 +376,8 @@ __device__ __forceinline__ void issue_tile(const SplitParams& p, Pipe& pp, int n
         mbar_arrive(&pp.full[st]);
         return;
     }
-    const int col0 = pp.col[n % kMap] * kTileCols;
-    const int ncols = min(p.vocab - col0, kTileCols);
+    const int col0 = pp.col[n % kMap] * COLS;
+    const int ncols = min(p.vocab - col0, COLS);
     const uint32_t bytes = tma ? static_cast<uint32_t>(ncols >> 2) * 16u : 0u;
     mbar_arrive_expect_tx(&pp.full[st], bytes + rec_bytes);
     tma_load_1d(rec_dst, static_cast<const unsigned char*>(rec_table) + static_cast<size_t>(row) * rec_bytes,
@@ -382,8 +392,7 @@ __device__ __forceinline__ int list_end(const SplitParams& p) {
     const int n = p.hard[kCount1];
     return p.li_end < 0 || p.li_end > n ? n : p.li_end;
 }
-__device__ __forceinline__ TileRange launch_tiles(const SplitParams& p) {
-    const int G = p.tiles_per_row;
+__device__ __forceinline__ TileRange launch_tiles(const SplitParams& p, int G) {
     return TileRange{static_cast<int64_t>(p.li_begin) * G, static_cast<int64_t>(list_end(p)) * G};
 }
 
@@ -403,9 +412,11 @@ __device__ __forceinline__ bool release_stage(int* count, int lane) {
 }
 
 // Pipeline start: barriers, the first kMap tiles mapped, the first kStages
-// issued (the row record of stage s at recs + s * rec_stride).
+// issued (the row record of stage s at recs + s * rec_stride). COLS: the
+// pass's tile width; G: its tiles per row.
+template <int COLS>
 __device__ __forceinline__ void pipe_start(const SplitParams& p, Pipe& pp, const int32_t* list,
-                                           TileRange tiles, float4* stages, void* recs,
+                                           TileRange tiles, int G, float4* stages, void* recs,
                                            size_t rec_stride, const void* rec_table,
                                            uint32_t rec_bytes, bool tma) {
     const int tid = threadIdx.x;
@@ -417,25 +428,26 @@ __device__ __forceinline__ void pipe_start(const SplitParams& p, Pipe& pp, const
         pp.abort = 0;
         fence_barrier_init();
     }
-    map_tiles(pp, list, p.map_row, tiles, p.tiles_per_row, 0, kMap, tid);
+    map_tiles(pp, list, p.map_row, tiles, G, 0, kMap, tid);
     __syncthreads();
     if (tid == 0)
         for (int s = 0; s < kStages; ++s)
-            issue_tile(p, pp, s, stages + s * kStageF4, static_cast<unsigned char*>(recs) + s * rec_stride,
-                       rec_table, rec_bytes, tma);
+            issue_tile<COLS>(p, pp, s, stages + s * (COLS / 4), static_cast<unsigned char*>(recs) + s * rec_stride,
+                             rec_table, rec_bytes, tma);
 }
 
 // The last warp out of tile n: refill its stage with tile n + kStages, and
 // every 32 tiles map 32 more (over tiles that every warp is done with).
+template <int COLS>
 __device__ __forceinline__ void pipe_advance(const SplitParams& p, Pipe& pp, int n, const int32_t* list,
-                                             TileRange tiles, float4* stage, void* rec_dst,
+                                             TileRange tiles, int G, float4* stage, void* rec_dst,
                                              const void* rec_table, uint32_t rec_bytes, bool tma,
                                              int lane) {
     if (lane == 0) {
         fence_proxy_async_smem();
-        issue_tile(p, pp, n + kStages, stage, rec_dst, rec_table, rec_bytes, tma);
+        issue_tile<COLS>(p, pp, n + kStages, stage, rec_dst, rec_table, rec_bytes, tma);
     }
-    if ((n & 31) == 31) map_tiles(pp, list, p.map_row, tiles, p.tiles_per_row, n + 33, 32, lane);
+    if ((n & 31) == 31) map_tiles(pp, list, p.map_row, tiles, G, n + 33, 32, lane);
 }
 
 // After the loop: if a wait ran out, copies still in flight land before the
@@ -452,16 +464,17 @@ __device__ __forceinline__ void pipe_end(Pipe& pp) {
 // stage; the ragged last float4 and (without bulk copies) everything from
 // global memory, stored into the stage as well, so that the stage always
 // holds the whole tile.
-__device__ __forceinline__ void read_tile(float4 (&v)[kSVec4], float4* stage, const float* tp,
+template <int VEC>
+__device__ __forceinline__ void read_tile(float4 (&v)[VEC], float4* stage, const float* tp,
                                           int ncols, int tid, bool tma) {
-    if (tma && ncols == kTileCols) {
+    if (tma && ncols == kSThreads * VEC * 4) {
 #pragma unroll
-        for (int i = 0; i < kSVec4; ++i) v[i] = stage[i * kSThreads + tid];
+        for (int i = 0; i < VEC; ++i) v[i] = stage[i * kSThreads + tid];
         return;
     }
     const int nfull4 = ncols >> 2;
 #pragma unroll
-    for (int i = 0; i < kSVec4; ++i) {
+    for (int i = 0; i < VEC; ++i) {
         const int f = i * kSThreads + tid;
         float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         if (f < nfull4) {
@@ -519,12 +532,12 @@ struct WarpPart {
 // A warp's S = sum 2^t and W = ln2 * sum 2^t t, t = x * lscale - cref, over
 // the thread's slots; with CLAMP, t is kept finite (a -inf logit gives e = 0
 // and e * t = 0 instead of NaN).
-template <bool CLAMP>
-__device__ __forceinline__ void tile_sums(const float4 (&v)[kSVec4], float lscale, float cref,
+template <bool CLAMP, int VEC>
+__device__ __forceinline__ void tile_sums(const float4 (&v)[VEC], float lscale, float cref,
                                           float& sw, float& ww) {
     float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f}, wa[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int i = 0; i < kSVec4; ++i) {
+    for (int i = 0; i < VEC; ++i) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float tq = fmaf(comp(v[i], q), lscale, -cref);
@@ -543,14 +556,14 @@ __device__ __forceinline__ void tile_sums(const float4 (&v)[kSVec4], float lscal
 __device__ __forceinline__ WarpPart p1_warp(const SplitParams& p, float4* stage, const ScaledQuotient& sq,
                                             int lrow, int col0, int ncols, int tid, int lane, bool stats,
                                             bool tma) {
-    float4 v[kSVec4];
+    float4 v[kP1Vec4];
     read_tile(v, stage, p.logits + static_cast<int64_t>(lrow) * p.row_stride + col0, ncols, tid, tma);
 
     // max of the raw logits (division by Te > 0 keeps the order)
-    float m4[kSVec4];
+    float m4[kP1Vec4];
     float mt = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kSVec4; ++i) {
+    for (int i = 0; i < kP1Vec4; ++i) {
         m4[i] = max4f(v[i]);
         mt = fmaxf(mt, m4[i]);
     }
@@ -568,7 +581,7 @@ __device__ __forceinline__ WarpPart p1_warp(const SplitParams& p, float4* stage,
     if (stats && mt == mxw && mxw != -INFINITY) {
         int i0 = 0;
 #pragma unroll
-        for (int i = kSVec4 - 1; i >= 0; --i)
+        for (int i = kP1Vec4 - 1; i >= 0; --i)
             if (m4[i] == mxw) i0 = i;
         const int f = i0 * kSThreads + tid;
         const float4 x4 = stage[f];
@@ -588,7 +601,7 @@ __device__ __forceinline__ WarpPart p1_warp(const SplitParams& p, float4* stage,
     } else {
         const float mw = sq.exact(mxw);
 #pragma unroll
-        for (int i = 0; i < kSVec4; ++i) {
+        for (int i = 0; i < kP1Vec4; ++i) {
             v[i].x = sq.exact(v[i].x) - mw;
             v[i].y = sq.exact(v[i].y) - mw;
             v[i].z = sq.exact(v[i].z) - mw;
@@ -599,8 +612,8 @@ __device__ __forceinline__ WarpPart p1_warp(const SplitParams& p, float4* stage,
     }
     float sw = 0.0f, ww = 0.0f;  // a warp of -inf only: nothing to sum
     if (mxw != -INFINITY) {
-        tile_sums<false>(v, lscale, cref, sw, ww);
-        if (isnan(ww)) tile_sums<true>(v, lscale, cref, sw, ww);
+        tile_sums<false, kP1Vec4>(v, lscale, cref, sw, ww);
+        if (isnan(ww)) tile_sums<true, kP1Vec4>(v, lscale, cref, sw, ww);
     }
     return WarpPart{0.0f, sw, ww, mxw, aw};
 }
@@ -655,12 +668,13 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
     const int warp = tid >> 5;
     const bool stats = p.stats != 0;
     const bool tma = p.vec != 0;
-    const TileRange tiles = launch_tiles(p);
-    pipe_start(p, pp, p.list1, tiles, stages, rts, sizeof(RowTemp), p.rt, sizeof(RowTemp), tma);
+    const TileRange tiles = launch_tiles(p, p.tiles1);
+    pipe_start<kP1Cols>(p, pp, p.list1, tiles, p.tiles1, stages, rts, sizeof(RowTemp), p.rt, sizeof(RowTemp),
+                        tma);
     for (int n = 0;; ++n) {
         const int st = n % kStages;
         const int par = (n / kStages) & 1;
-        float4* stage = stages + st * kStageF4;
+        float4* stage = stages + st * (kP1Cols / 4);
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pp.full[st], static_cast<uint32_t>(par)))) {
             if (lane == 0) {
                 pp.abort = 1;
@@ -671,8 +685,8 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
         const int row = pp.row[n % kMap];
         if (row < 0) break;
         const int64_t t = tiles.t_begin + static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(n) * gridDim.x;
-        const int col0 = pp.col[n % kMap] * kTileCols;
-        const int ncols = min(p.vocab - col0, kTileCols);
+        const int col0 = pp.col[n % kMap] * kP1Cols;
+        const int ncols = min(p.vocab - col0, kP1Cols);
         ScaledQuotient sq;
         sq.t = rts[st].qt;
         sq.y = rts[st].qy;
@@ -683,7 +697,8 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
 
         // the last warp out: refill the stage, then the tile's record (the
         // warps combined, one lane each)
-        pipe_advance(p, pp, n, p.list1, tiles, stage, &rts[st], p.rt, sizeof(RowTemp), tma, lane);
+        pipe_advance<kP1Cols>(p, pp, n, p.list1, tiles, p.tiles1, stage, &rts[st], p.rt, sizeof(RowTemp), tma,
+                              lane);
         p1_combine(p, parts[par][st], sq, t, col0, ncols, lane);
     }
     asm volatile("griddepcontrol.launch_dependents;");
@@ -705,7 +720,7 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
         p.map_row || p.keep == nullptr || p.keep[slot_of(p, static_cast<uint64_t>(p.row0 + row))] != 0;
     const RowTemp rt = p.rt[row];
     const float temp = rt.temp;
-    const int G = p.tiles_per_row;
+    const int G = p.tiles1;  // the row's pass-1 tile records
     const TileStats* tr = p.ts + li * G;
     float m = -INFINITY, s = 0.0f, w = 0.0f, xm = -INFINITY;
     int arg = INT_MAX;
@@ -1263,9 +1278,9 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
     const bool stats = p.stats != 0;
     const bool probs = stats && p.probs_dtype != 0;
     const bool tma = p.vec != 0;
-    const TileRange tiles = launch_tiles(p);
+    const TileRange tiles = launch_tiles(p, p.tiles_per_row);
     if (tid < 2 * kStages) sh.tile_nk[tid / kStages][tid % kStages] = 0;
-    pipe_start(p, pp, p.list1, tiles, stages, &recs[0][0], kRowEntryMax, p.rr,
+    pipe_start<kTileCols>(p, pp, p.list1, tiles, p.tiles_per_row, stages, &recs[0][0], kRowEntryMax, p.rr,
                static_cast<uint32_t>(p.rec_bytes), tma);
     for (int n = 0;; ++n) {
         const int st = n % kStages;
@@ -1291,7 +1306,7 @@ __global__ void __launch_bounds__(kSThreads, DRS_P2_MINB) split_pass2(const __gr
         // is read first), then refill the stage
         p2_combine<MULTI>(p, sh, t, st, par, stats, topk, lane);
         __syncwarp();
-        pipe_advance(p, pp, n, p.list1, tiles, stage, &recs[st][0], p.rr,
+        pipe_advance<kTileCols>(p, pp, n, p.list1, tiles, p.tiles_per_row, stage, &recs[st][0], p.rr,
                      static_cast<uint32_t>(p.rec_bytes), tma, lane);
     }
     asm volatile("griddepcontrol.launch_dependents;");
@@ -1410,7 +1425,8 @@ size_t row_entry_bytes(int32_t n_seeds) {
 
 SplitLayout split_layout(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds) {
     const size_t R = static_cast<size_t>(rows);
-    const size_t G = static_cast<size_t>((vocab + kTileCols - 1) / kTileCols);
+    const size_t G = static_cast<size_t>((vocab + kTileCols - 1) / kTileCols);  // pass-2 tiles
+    const size_t G1 = static_cast<size_t>((vocab + kP1Cols - 1) / kP1Cols);      // pass-1 tiles
     SplitLayout l{};
     size_t at = 0;
     l.hard = at;
@@ -1420,7 +1436,7 @@ SplitLayout split_layout(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds
     l.rt = at;
     at += round_up(sizeof(RowTemp) * R, kWorkspaceAlign);
     l.ts = at;
-    at += round_up(sizeof(TileStats) * R * G, kWorkspaceAlign);
+    at += round_up(sizeof(TileStats) * R * G1, kWorkspaceAlign);
     l.rr = at;
     at += round_up(row_entry_bytes(n_seeds) * R, kWorkspaceAlign);
     l.te = at;
@@ -1456,9 +1472,10 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     if (c.k > kSplitMaxK || c.vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
     const int32_t n_seeds = c.seeds ? c.n_seeds : 1;
     if (n_seeds < 1 || n_seeds > kMaxSeeds) return DRS_ERR_UNSUPPORTED;
-    const int G = static_cast<int>((c.vocab + kTileCols - 1) / kTileCols);
+    const int G = static_cast<int>((c.vocab + kTileCols - 1) / kTileCols);  // pass-2 tiles per row
+    const int G1 = static_cast<int>((c.vocab + kP1Cols - 1) / kP1Cols);     // pass-1 tiles per row
     // tile indices of a pass are 32-bit, list lengths int
-    if (c.rows > INT_MAX / G) return DRS_ERR_UNSUPPORTED;
+    if (c.rows > INT_MAX / G1) return DRS_ERR_UNSUPPORTED;
     const SplitLayout l = split_layout(c.rows, c.vocab, c.k, n_seeds);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     SplitParams p{};
@@ -1496,6 +1513,7 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     p.n_seeds = n_seeds;
     p.rec_bytes = static_cast<int>(row_entry_bytes(n_seeds));
     p.tiles_per_row = G;
+    p.tiles1 = G1;
     p.vocab = static_cast<int>(c.vocab);
     p.vec = aligned(c.logits, 16) && (c.row_stride % 4 == 0);
     p.probs_dtype = static_cast<int>(c.probs_dtype);
@@ -1509,7 +1527,8 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     p.fault = take_injected_fault();
     // the header of the hard-row list: its count and the two list lengths
     if (cudaMemsetAsync(ws + l.hard, 0, 16, stream) != cudaSuccess) return DRS_ERR_CUDA;
-    const size_t smem = kStages * kStageBytes;
+    const size_t smem = kStages * kStageBytes;                       // pass 2
+    const size_t smem1 = static_cast<size_t>(kStages) * kP1Cols * 4;  // pass 1
     const int64_t gp = (c.rows + 255) / 256;
     const int64_t gr = (c.rows + kRowWarps - 1) / kRowWarps;
     if (gr > INT_MAX) return DRS_ERR_UNSUPPORTED;
@@ -1520,11 +1539,11 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     };
     auto pass2 = n_seeds > 1 ? split_pass2<true> : split_pass2<false>;
     if (cudaFuncSetAttribute(split_pass1, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
+                             static_cast<int>(smem1)) != cudaSuccess ||
         cudaFuncSetAttribute(pass2, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return DRS_ERR_CUDA;
-    const int g1 = resident_grid(split_pass1, kSThreads, smem);
+    const int g1 = resident_grid(split_pass1, kSThreads, smem1);
     const int g2 = resident_grid(pass2, kSThreads, smem);
     if (g1 < 1 || g2 < 1) return DRS_ERR_CUDA;
     if (!mark(0)) return DRS_ERR_CUDA;
@@ -1545,8 +1564,8 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess;
     };
-    if (!pdl(split_pass1, g1, kSThreads, smem) || !mark(2)) return DRS_ERR_CUDA;
-    auto merge = G * kSWarps <= 32 * kOrdSmall ? split_merge<kOrdSmall> : split_merge<kOrdLarge>;
+    if (!pdl(split_pass1, g1, kSThreads, smem1) || !mark(2)) return DRS_ERR_CUDA;
+    auto merge = G1 * kSWarps <= 32 * kOrdSmall ? split_merge<kOrdSmall> : split_merge<kOrdLarge>;
     if (!pdl(merge, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(3)) return DRS_ERR_CUDA;
     if (!pdl(pass2, g2, kSThreads, smem) || !mark(4)) return DRS_ERR_CUDA;
     auto finish = G <= 32 * kTilesSmall ? split_finish<kTilesSmall> : split_finish<kTilesLarge>;
