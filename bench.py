@@ -321,7 +321,7 @@ def _run_ours(args, world, rank, local):
     p1_ms = kernel_ms["split_pass1"]
     achieved_p2 = bytes_rs / (p2_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved_p2, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved_p2 / peak, 4), "traffic": _traffic_from_profile(),
+                "frac": round(achieved_p2 / peak, 4), "traffic": _traffic_from_profile(WORKLOAD, rows),
                 "kernel": "split_pass2 (probabilities, Gumbel race, top-k candidates)",
                 "peak_kind": f"{peak_kind} copy bandwidth",
                 "bytes_per_launch": bytes_rs, "avg_launch_ms": round(p2_ms, 4),
@@ -391,15 +391,17 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def _traffic_from_profile():
-    """DRAM bytes (read + write) per launch of pass 2 on the step workload,
-    from the committed ncu capture, if it was taken on the current kernel
-    sources (else null)."""
+def _traffic_from_profile(workload, rows):
+    """DRAM bytes (read + write) per launch of pass 2, from the committed
+    ncu capture, if it was taken on the current kernel sources and covers
+    this workload at this number of rows (else null)."""
     path = os.path.join(ROOT, "profiles", "split_pass2_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         if d.get("source_sha256") != kernel_source_hash():
+            return None
+        if d.get("workload_key") != workload or d.get("rows") != rows:
             return None
         return d.get("dram_bytes_per_launch")
     except Exception:

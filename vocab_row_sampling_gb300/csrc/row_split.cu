@@ -97,7 +97,8 @@ constexpr int kMaxTiles1 = (DRS_MAX_VOCAB + kP1Cols - 1) / kP1Cols;
 // warp maxima per lane in the merge: rows of up to 60 pass-1 tiles (368640
 // columns), and the longest rows
 constexpr int kOrdSmall = (60 * kSWarps + 31) / 32;
-constexpr int kOrdLarge = (kMaxTiles1 * kSWarps + 31) / 32;
+constexpr int kWideMergeWarps = 8;  // warps sharing one long row in the merge
+constexpr int kOrdWide = (kMaxTiles1 * kSWarps + 32 * kWideMergeWarps - 1) / (32 * kWideMergeWarps);
 constexpr int kTilesSmall = (60 + 31) / 32;  // tiles per lane in the finish
 constexpr int kTilesLarge = (kMaxTiles + 31) / 32;
 constexpr int kStages = DRS_SPLIT_STAGES;          // tiles in flight per CTA
@@ -709,12 +710,45 @@ __global__ void __launch_bounds__(kSThreads, DRS_P1_MINB) split_pass1(const __gr
 
 constexpr int kRowWarps = 8;  // rows per CTA of the merge and finish kernels
 
-// The merge of list entry li by one warp: the row's M, S, W, argmax, the
-// warps' Gumbel-max candidates scored per seed (B), the top-k threshold, the
-// row record for pass 2, the entropy; rows without a threshold go on the
-// hard-row list.
-template <int NU>
-__device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int lane) {
+// Shared memory of a merge CTA whose W warps share one row (W > 1): one slot
+// per warp for each cross-warp reduction, and each warp's k largest warp
+// maxima.
+template <int W>
+struct MergeShared {
+    float f[4][W];
+    int i[W];
+    float bs[W];
+    int bc[W];
+    uint32_t lists[W][kSplitMaxK];
+    uint32_t kth;
+};
+
+// A warp-reduced value combined over the W warps of a row (W = 1: itself).
+// Every thread of the CTA calls it; slot `red` is free again on return.
+template <int W, typename T, typename Op>
+__device__ __forceinline__ T across_warps(T v, T* red, int lane, int warp, Op op) {
+    if constexpr (W == 1) {
+        return v;
+    } else {
+        if (lane == 0) red[warp] = v;
+        __syncthreads();
+        T r = red[0];
+#pragma unroll
+        for (int i = 1; i < W; ++i) r = op(r, red[i]);
+        __syncthreads();
+        return r;
+    }
+}
+
+// The merge of list entry li by W warps (thread r of 32 W): the row's M, S,
+// W, argmax, the warps' Gumbel-max candidates scored per seed (B), the top-k
+// threshold, the row record for pass 2, the entropy; rows without a
+// threshold go on the hard-row list. NU: warp maxima per thread.
+template <int NU, int W>
+__device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int r, MergeShared<W>* sh) {
+    const int lane = r & 31;
+    const int warp = r >> 5;
+    constexpr int kStride = 32 * W;
     const int64_t row = p.list1[li];
     const bool kept =
         p.map_row || p.keep == nullptr || p.keep[slot_of(p, static_cast<uint64_t>(p.row0 + row))] != 0;
@@ -724,27 +758,35 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
     const TileStats* tr = p.ts + li * G;
     float m = -INFINITY, s = 0.0f, w = 0.0f, xm = -INFINITY;
     int arg = INT_MAX;
-    for (int c = lane; c < G; c += 32) {
-        const TileStats r = tr[c];
+    for (int c = r; c < G; c += kStride) {
+        const TileStats ti = tr[c];
         // the lowest column holding the raw max (-inf rows: the first)
-        arg = r.xmax > xm ? r.arg : (r.xmax == xm ? min(arg, r.arg) : arg);
-        xm = fmaxf(xm, r.xmax);
-        if (r.m != -INFINITY) {
+        arg = ti.xmax > xm ? ti.arg : (ti.xmax == xm ? min(arg, ti.arg) : arg);
+        xm = fmaxf(xm, ti.xmax);
+        if (ti.m != -INFINITY) {
             if (m == -INFINITY) {
-                m = r.m;
-                s = r.s;
-                w = r.w;
+                m = ti.m;
+                s = ti.s;
+                w = ti.w;
             } else {
-                const float nm = fmaxf(m, r.m);
-                const float d1 = m - nm, d2 = r.m - nm;
+                const float nm = fmaxf(m, ti.m);
+                const float d1 = m - nm, d2 = ti.m - nm;
                 const float f1 = ex2_approx(d1 * kLog2e), f2 = ex2_approx(d2 * kLog2e);
-                w = f1 * fmaf(d1, s, w) + f2 * fmaf(d2, r.s, r.w);
-                s = f1 * s + f2 * r.s;
+                w = f1 * fmaf(d1, s, w) + f2 * fmaf(d2, ti.s, ti.w);
+                s = f1 * s + f2 * ti.s;
                 m = nm;
             }
         }
     }
-    const float big_m = warp_max_f(m);
+    auto fmax_op = [](float a, float b) { return fmaxf(a, b); };
+    auto fsum_op = [](float a, float b) { return a + b; };
+    auto imin_op = [](int a, int b) { return min(a, b); };
+    float* redf0 = W > 1 ? sh->f[0] : nullptr;
+    float* redf1 = W > 1 ? sh->f[1] : nullptr;
+    float* redf2 = W > 1 ? sh->f[2] : nullptr;
+    float* redf3 = W > 1 ? sh->f[3] : nullptr;
+    int* redi = W > 1 ? sh->i : nullptr;
+    const float big_m = across_warps<W>(warp_max_f(m), redf0, lane, warp, fmax_op);
     float s_l = 0.0f, w_l = 0.0f;
     if (m != -INFINITY) {
         const float dm = m - big_m;
@@ -752,10 +794,10 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
         s_l = f * s;
         w_l = f * fmaf(dm, s, w);
     }
-    const float s_tot = warp_sum_f(s_l);
-    const float w_tot = warp_sum_f(w_l);
-    const float mraw = warp_max_f(xm);
-    const int arg_row = warp_min_nonneg(xm == mraw ? arg : INT_MAX);
+    const float s_tot = across_warps<W>(warp_sum_f(s_l), redf1, lane, warp, fsum_op);
+    const float w_tot = across_warps<W>(warp_sum_f(w_l), redf2, lane, warp, fsum_op);
+    const float mraw = across_warps<W>(warp_max_f(xm), redf3, lane, warp, fmax_op);
+    const int arg_row = across_warps<W>(warp_min_nonneg(xm == mraw ? arg : INT_MAX), redi, lane, warp, imin_op);
 
     const bool topk = p.k > 0 && kept;
     float thr = -INFINITY;
@@ -763,21 +805,23 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
     if (topk) {
         // the k-th largest of the row's warp maxima (absent warps are 0,
         // below every value): k rounds of a warp max, each removing one
-        // occurrence
+        // occurrence; with W warps, each warp's k largest, then the k-th
+        // largest of their union (a merge of W sorted lists)
         uint32_t o[NU];
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
-            const int jx = lane + 32 * u;
+            const int jx = r + kStride * u;
             o[u] = jx < kSWarps * G ? tr[jx / kSWarps].wmax[jx % kSWarps] : 0u;
         }
         uint32_t kth = 0;
-        for (int r = 0; r < p.k; ++r) {
+        for (int rd = 0; rd < p.k; ++rd) {
             uint32_t lm = 0;
 #pragma unroll
             for (int u = 0; u < NU; ++u) lm = max(lm, o[u]);
             uint32_t top;
             asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(top) : "r"(lm));
             kth = top;
+            if (W > 1 && lane == 0) sh->lists[warp][rd] = top;
             const uint32_t holders = __ballot_sync(0xffffffffu, lm == top);
             if (lane == __ffs(holders) - 1) {
                 bool done = false;
@@ -788,6 +832,28 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
                         done = true;
                     }
             }
+        }
+        if constexpr (W > 1) {
+            // lane j < W of warp 0 holds the head of warp j's list; each
+            // round takes the largest head
+            __syncthreads();
+            if (warp == 0) {
+                int at = 0;
+                uint32_t head = lane < W ? sh->lists[lane][0] : 0u;
+                for (int rd = 0; rd < p.k; ++rd) {
+                    uint32_t top;
+                    asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(top) : "r"(head));
+                    kth = top;
+                    const uint32_t holders = __ballot_sync(0xffffffffu, lane < W && head == top);
+                    if (lane == __ffs(holders) - 1) {
+                        ++at;
+                        head = at < p.k ? sh->lists[lane][at] : 0u;
+                    }
+                }
+                if (lane == 0) sh->kth = kth;
+            }
+            __syncthreads();
+            kth = sh->kth;
         }
         // absent, or -inf: no threshold, the exact kernel takes the row.
         // Lowered by Te ulp(s): a logit below thr whose exact quotient
@@ -813,7 +879,7 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
         if (noisy) {
             const uint64_t grow = static_cast<uint64_t>(p.row0 + row);
             const ScaledQuotient sq{rt.qt, rt.qy, rt.qmode};
-            for (int jx = lane; jx < kSWarps * G; jx += 32) {
+            for (int jx = r; jx < kSWarps * G; jx += kStride) {
                 const int col = tr[jx / kSWarps].wcol[jx % kSWarps];
                 if (col == INT_MAX) continue;
                 const float mw = sq.exact(unord32(tr[jx / kSWarps].wmax[jx % kSWarps]));
@@ -826,12 +892,25 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
             }
         }
         warp_best(b, bc);
-        if (lane == 0)
+        if constexpr (W > 1) {
+            if (lane == 0) {
+                sh->bs[warp] = b;
+                sh->bc[warp] = bc;
+            }
+            __syncthreads();
+            for (int j = 0; j < W; ++j)
+                if (beats(sh->bs[j], sh->bc[j], b, bc)) {
+                    b = sh->bs[j];
+                    bc = sh->bc[j];
+                }
+            __syncthreads();
+        }
+        if (r == 0)
             reinterpret_cast<SeedRec*>(entry + sizeof(RowRecord))[sd] =
                 SeedRec{b, (c0 + (b - big_m) * kLog2e) - kRaceSlack, bc, 0};
     }
 
-    if (lane == 0) {
+    if (r == 0) {
         RowRecord rec{};
         rec.M = big_m;
         rec.log2s = s_tot > 0.0f ? log2f(s_tot) : 0.0f;
@@ -859,12 +938,22 @@ __device__ __forceinline__ void merge_row(const SplitParams& p, int64_t li, int 
     }
 }
 
-template <int NU>
+// W = 1: a row per warp, kRowWarps rows per CTA; W = kRowWarps: a row per
+// CTA (long rows: the row's serial work split W ways)
+template <int NU, int W>
 __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_constant__ SplitParams p) {
+    static_assert(W == 1 || W == kRowWarps, "a merge CTA holds kRowWarps rows or one row");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
-    if (li >= list_end(p)) return;
-    merge_row<NU>(p, li, threadIdx.x & 31);
+    if constexpr (W == 1) {
+        const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+        if (li >= list_end(p)) return;
+        merge_row<NU, 1>(p, li, threadIdx.x & 31, nullptr);
+    } else {
+        __shared__ MergeShared<W> sh;
+        const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x);
+        if (li >= list_end(p)) return;  // the whole CTA
+        merge_row<NU, W>(p, li, threadIdx.x, &sh);
+    }
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
@@ -1565,8 +1654,11 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
         return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess;
     };
     if (!pdl(split_pass1, g1, kSThreads, smem1) || !mark(2)) return DRS_ERR_CUDA;
-    auto merge = G1 * kSWarps <= 32 * kOrdSmall ? split_merge<kOrdSmall> : split_merge<kOrdLarge>;
-    if (!pdl(merge, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(3)) return DRS_ERR_CUDA;
+    const bool short_merge = G1 * kSWarps <= 32 * kOrdSmall;
+    const bool ok3 = short_merge ? pdl(split_merge<kOrdSmall, 1>, static_cast<int>(gr), kRowWarps * 32, 0)
+                                 : pdl(split_merge<kOrdWide, kWideMergeWarps>, static_cast<int>(c.rows),
+                                       kRowWarps * 32, 0);
+    if (!ok3 || !mark(3)) return DRS_ERR_CUDA;
     if (!pdl(pass2, g2, kSThreads, smem) || !mark(4)) return DRS_ERR_CUDA;
     auto finish = G <= 32 * kTilesSmall ? split_finish<kTilesSmall> : split_finish<kTilesLarge>;
     if (!pdl(finish, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(5)) return DRS_ERR_CUDA;
