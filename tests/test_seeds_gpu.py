@@ -88,3 +88,26 @@ def test_strided_workload_eight_seeds():
              "entropy": e.cpu().numpy(), "probs": None}
         ref = oracle_rows(x, w["temps"].cpu().numpy(), w["canvas_len"], sd, 0, sel)
         check_row_stats(subset(g, sel), ref, 0, f"strided seed {sd}")
+
+
+@pytest.mark.parametrize("vocab", [600000, 2097152])
+def test_long_rows_equal_single_seed_calls(vocab):
+    """Rows long enough that the merge shares each row among the warps of a
+    CTA: every seed's sample equals a single-seed call's, and each seed's
+    statistics equal the oracle's on every row."""
+    rng = np.random.default_rng(vocab)
+    x = (rng.standard_normal((6, vocab)) * 3).astype(np.float32)
+    x[1] = 0.5                                  # constant
+    x[2, vocab - 1] = 40.0                      # the max in the last column
+    x[3][rng.random(vocab) < 0.999] = -np.inf   # a few finite values
+    temps = np.array([1.0, 0.6, 1.4], np.float32)
+    dev = torch.as_tensor(x).cuda()
+    seeds = SEEDS[:3]
+    a, smp, e, p = _compare_to_single(dev, torch.as_tensor(temps).cuda(), 2, seeds, torch.bfloat16)
+    sel = np.arange(x.shape[0])
+    for i, sd in enumerate(seeds):
+        g = {"argmax": a.cpu().numpy(), "sample": smp[i].cpu().numpy(),
+             "entropy": e.cpu().numpy(),
+             "probs": p.view(torch.int16).cpu().numpy().view(np.uint16)}
+        ref = oracle_rows(dev, temps, 2, sd, 1, sel)
+        assert check_row_stats(g, ref, 1, f"V={vocab} seed {sd}") <= 1
