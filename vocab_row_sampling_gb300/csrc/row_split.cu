@@ -5,10 +5,11 @@
 // diffusion_gemma_sampler": module docstring, sample_row_stats,
 // sample_row_stats_reference, stash_converged_logprobs, _lp_topk_kernel).
 //
-// Layout of the work. A row of V fp32 logits is cut into tiles of 8192
-// columns. A CTA of 256 threads works on one tile at a time (slot i of
-// thread t holds columns 4*(i*256+t)+0..3 of the tile, i < 8); the CTAs of
-// a persistent grid take the tiles of the rows of a work list round robin.
+// Layout of the work. A row of V fp32 logits is cut into tiles: 6144
+// columns in pass 1, 8192 in pass 2. A CTA of 256 threads works on one tile
+// at a time (slot i of thread t holds columns 4*(i*256+t)+0..3 of the tile,
+// i < 6 or 8); the CTAs of a persistent grid take the tiles of the rows of a
+// work list round robin.
 // No CTA ever waits for another: the tiles of a row meet through records in
 // global memory that a later kernel on the stream merges.
 //
@@ -26,7 +27,8 @@
 //          divide every logit exactly first. The tile's record combines the
 //          warps, with the Gumbel-max score of each warp's argmax element and
 //          the warps' raw maxima.
-//   merge  one warp per row: max M, S, W (entropy log S - W / S), argmax, B =
+//   merge  one warp per row (one CTA of 8 warps per row for rows of more
+//          than 60 pass-1 tiles): max M, S, W (entropy log S - W / S), argmax, B =
 //          the best of the warps' argmax scores, and the top-k threshold thr
 //          = the k-th largest raw warp maximum (k distinct elements reach it,
 //          so the row's top k all do); the row's record, and the list of rows
@@ -94,10 +96,11 @@ constexpr int kMaxTiles = (DRS_MAX_VOCAB + kTileCols - 1) / kTileCols;
 constexpr int kP1Vec4 = DRS_P1_VEC4;
 constexpr int kP1Cols = kSThreads * kP1Vec4 * 4;   // 6144 columns per pass-1 tile
 constexpr int kMaxTiles1 = (DRS_MAX_VOCAB + kP1Cols - 1) / kP1Cols;
-// warp maxima per lane in the merge: rows of up to 60 pass-1 tiles (368640
-// columns), and the longest rows
+// warp maxima per thread in the merge: rows of up to 60 pass-1 tiles
+// (368640 columns) take one warp; longer rows, up to the longest, share the
+// kWideMergeWarps warps of a CTA
 constexpr int kOrdSmall = (60 * kSWarps + 31) / 32;
-constexpr int kWideMergeWarps = 8;  // warps sharing one long row in the merge
+constexpr int kWideMergeWarps = 8;
 constexpr int kOrdWide = (kMaxTiles1 * kSWarps + 32 * kWideMergeWarps - 1) / (32 * kWideMergeWarps);
 constexpr int kTilesSmall = (60 + 31) / 32;  // tiles per lane in the finish
 constexpr int kTilesLarge = (kMaxTiles + 31) / 32;
