@@ -107,7 +107,7 @@ drs_status drs_row_stats(const float *logits, int64_t rows, int64_t vocab,
                          size_t workspace_bytes, void *stream);
 
 /*
- * drs_row_stats without a caller workspace. The paper has no counterpart:
+ * drs_row_stats without a caller workspace. The page has no counterpart:
  * this entry point exists for callers that cannot allocate device memory
  * for the library -- plugin interfaces that hand over only input and
  * output buffers at enqueue time, or code that must not call cudaMalloc
