@@ -254,6 +254,12 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 
 __device__ __forceinline__ float max4f(const float4& v) { return max3(v.x, v.y, fmaxf(v.z, v.w)); }
 
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -962,9 +968,30 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
 
 // ============================================================== pass 2
 
+// The probabilities of a whole tile with aligned rows, no per-slot checks.
+// FTZ: by the exponential that flushes subnormal results (one instruction),
+// for threads none of whose probabilities is subnormal in fp32.
+template <bool BF16, bool RAW, bool FTZ>
+__device__ __forceinline__ void store_tile_probs(const float4 (&v)[kSVec4], const RowRecord& rec,
+                                                 const ScaledQuotient& sq, uint16_t* prow, int tid) {
+    const float ls = rec.ls, c2 = rec.c2, big_m = rec.M, l2s = rec.log2s;
+#pragma unroll
+    for (int i = 0; i < kSVec4; ++i) {
+        const int f = i * kSThreads + tid;
+        float pr[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float x = comp(v[i], q);
+            const float tq = RAW ? fmaf(x, ls, -c2) : fmaf(sq.exact(x) - big_m, kLog2e, -l2s);
+            pr[q] = FTZ ? ex2_ftz(tq) : ex2_approx(tq);
+        }
+        __stcs(reinterpret_cast<uint2*>(prow + 4 * f),
+               make_uint2(pack2<BF16>(pr[0], pr[1]), pack2<BF16>(pr[2], pr[3])));
+    }
+}
+
 // Probabilities 2^t of a tile, t = x ls - c2 (raw rows) or (s - M) log2(e) -
-// log2 S, subnormal results kept (bf16 and fp16 can hold some); -inf logits
-// give 0.
+// log2 S, subnormal results kept (bf16 can hold some); -inf logits give 0.
 template <bool BF16, bool RAW>
 __device__ __forceinline__ void write_probs(const float4 (&v)[kSVec4], const RowRecord& rec,
                                             const ScaledQuotient& sq, uint16_t* prow, bool vec,
@@ -973,19 +1000,20 @@ __device__ __forceinline__ void write_probs(const float4 (&v)[kSVec4], const Row
     // a whole tile with aligned rows: no per-slot checks (measured 6% of
     // pass 2 against the same loop with the checks)
     if (vec && ncols == kTileCols) {
+        // fp16 holds nothing below 2^-25, so flushing fp32 subnormals
+        // changes no fp16 code; for bf16 the thread's smallest logit tells
+        // whether any of its probabilities is below 2^-126 (a NaN is
+        // skipped by min; -inf gives t = -inf and the exact form)
+        bool ftz = !BF16;
+        if (BF16) {
+            float xmin = min3(v[0].x, v[0].y, fminf(v[0].z, v[0].w));
 #pragma unroll
-        for (int i = 0; i < kSVec4; ++i) {
-            const int f = i * kSThreads + tid;
-            float pr[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float x = comp(v[i], q);
-                const float tq = RAW ? fmaf(x, ls, -c2) : fmaf(sq.exact(x) - big_m, kLog2e, -l2s);
-                pr[q] = ex2_approx(tq);
-            }
-            __stcs(reinterpret_cast<uint2*>(prow + 4 * f),
-                   make_uint2(pack2<BF16>(pr[0], pr[1]), pack2<BF16>(pr[2], pr[3])));
+            for (int i = 1; i < kSVec4; ++i) xmin = min3(xmin, min3(v[i].x, v[i].y, v[i].z), v[i].w);
+            const float tmin = RAW ? fmaf(xmin, ls, -c2) : fmaf(sq.exact(xmin) - big_m, kLog2e, -l2s);
+            ftz = tmin >= -126.0f;
         }
+        if (ftz) store_tile_probs<BF16, RAW, true>(v, rec, sq, prow, tid);
+        else store_tile_probs<BF16, RAW, false>(v, rec, sq, prow, tid);
         return;
     }
     // ragged tiles and rows without aligned 8-byte stores
