@@ -55,7 +55,7 @@ typedef enum drs_probs_dtype {
  * contents arbitrary: each call clears the counters it uses with an
  * asynchronous memset on its stream before its kernels run). The workspace
  * carries the row lists and the per-tile and per-row records through which
- * the kernels of one call pass their partial results: about 3.6 KiB per row
+ * the kernels of one call pass their partial results: about 4.6 KiB per row
  * of 262144 columns, growing with rows and vocab. One workspace must not be
  * used by two calls that can run at the same time.
  */
@@ -117,7 +117,7 @@ drs_status drs_row_stats(const float *logits, int64_t rows, int64_t vocab,
  * The kernels' records live in a fixed device array inside the library
  * (640 KiB; every GPU that loads the library holds it until the process
  * exits). A call whose rows need a larger workspace runs in batches of rows
- * that fit, one after the other on the stream (at most 177 rows of 262144
+ * that fit, one after the other on the stream (at most 137 rows of 262144
  * columns per batch). The call allocates nothing. Its
  * first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream

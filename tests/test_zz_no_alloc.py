@@ -33,12 +33,12 @@ def _cases():
     w = workloads.make("tiny")
     yield "tiny", w["logits"].cuda(), w["temps"].cuda(), w["canvas_len"]
     rng = np.random.default_rng(3)
-    x = (rng.standard_normal((40, 131072)) * 3).astype(np.float32)   # 16 tiles per row
+    x = (rng.standard_normal((40, 131072)) * 3).astype(np.float32)   # 22 + 16 tiles per row
     x[5] = -np.inf
     x[5, 70000] = 1.0
     t = torch.tensor([0.0, 0.8, 1.0, 1e-3, 1.4], dtype=torch.float32, device="cuda")
     yield "shared rows", torch.as_tensor(x).cuda(), t, 8
-    # more rows than one batch of the fixed array holds (at most 177 rows of
+    # more rows than one batch of the fixed array holds (at most 137 rows of
     # 262144 columns): the call runs in batches, row0 and the outputs offset
     g = torch.Generator(device="cuda").manual_seed(4)
     xb = 3.0 * torch.randn(300, 262144, generator=g, device="cuda")
