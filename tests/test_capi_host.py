@@ -51,6 +51,18 @@ def test_workspace_sizes(lib):
     assert drs.drs_topk_workspace_bytes(2048, 262144, 64) >= 152 * 4 * (32 + 64 * 8)
 
 
+def test_header_sizes_match_the_library(lib):
+    """The workspace per row and the no-alloc batch that include/drs.h
+    states for rows of 262144 columns are the ones the library computes."""
+    with open(os.path.join(_build.INCLUDE, "drs.h")) as f:
+        text = " ".join(f.read().split())
+    per_row = drs.drs_row_stats_workspace_bytes(2048, 262144) / 2048 / 1024
+    stated = float(re.search(r"about ([0-9.]+) KiB per row \* of 262144 columns", text).group(1))
+    assert abs(stated - per_row) < 0.1
+    fits = max(n for n in range(1, 1024) if drs.drs_row_stats_workspace_bytes(n, 262144) <= 640 * 1024)
+    assert int(re.search(r"at most ([0-9]+) rows of 262144 \* columns per batch", text).group(1)) == fits
+
+
 def _row_stats(lib, rows=4, vocab=16, stride=16, temps=FAKE, canvas=1, row0=0, logits=FAKE,
                outs=FAKE, probs_dtype=1, probs=FAKE, pstride=16, ws=FAKE, ws_bytes=None):
     if ws_bytes is None:
