@@ -1,0 +1,352 @@
+// row_common.cuh -- definitions shared by the two implementations of the row
+// statistics (row_split.cu: two streaming passes; row_cluster.cu: one read
+// per row by a thread-block cluster): tile geometry, the per-row and
+// per-tile records, the launch parameters, and device helpers (order keys,
+// top-k keys, rounding to bf16/fp16, the Philox noise of a group of four
+// columns, the exact rescoring of Gumbel-race survivors, top-k candidate
+// collection).
+#pragma once
+
+#include <cfloat>
+#include <climits>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "drs_device.cuh"
+#include "drs_internal.h"
+
+namespace drs {
+namespace rs {
+
+constexpr int kSThreads = 256;
+constexpr int kSWarps = kSThreads / 32;
+#ifndef DRS_SPLIT_VEC4
+#define DRS_SPLIT_VEC4 8
+#endif
+#ifndef DRS_SPLIT_STAGES
+#define DRS_SPLIT_STAGES 2
+#endif
+#ifndef DRS_P1_MINB
+#define DRS_P1_MINB 3
+#endif
+#ifndef DRS_P2_MINB
+#define DRS_P2_MINB 3
+#endif
+#ifndef DRS_P1_VEC4
+#define DRS_P1_VEC4 6
+#endif
+constexpr int kSVec4 = DRS_SPLIT_VEC4;             // pass 2: float4 slots per thread
+constexpr int kTileCols = kSThreads * kSVec4 * 4;  // 8192 columns per pass-2 tile
+constexpr int kMaxTiles = (DRS_MAX_VOCAB + kTileCols - 1) / kTileCols;
+// Pass 1 has tiles of its own (measured: it streams faster with 24 KiB tiles
+// than with pass 2's 32 KiB ones, pass 2 the other way round).
+constexpr int kP1Vec4 = DRS_P1_VEC4;
+constexpr int kP1Cols = kSThreads * kP1Vec4 * 4;   // 6144 columns per pass-1 tile
+constexpr int kMaxTiles1 = (DRS_MAX_VOCAB + kP1Cols - 1) / kP1Cols;
+// warp maxima per thread in the merge: rows of up to 60 pass-1 tiles
+// (368640 columns) take one warp; longer rows, up to the longest, share the
+// kWideMergeWarps warps of a CTA
+constexpr int kOrdSmall = (60 * kSWarps + 31) / 32;
+constexpr int kWideMergeWarps = 8;
+constexpr int kOrdWide = (kMaxTiles1 * kSWarps + 32 * kWideMergeWarps - 1) / (32 * kWideMergeWarps);
+constexpr int kTilesSmall = (60 + 31) / 32;  // tiles per lane in the finish
+constexpr int kTilesLarge = (kMaxTiles + 31) / 32;
+constexpr int kStages = DRS_SPLIT_STAGES;          // tiles in flight per CTA
+constexpr int kStageF4 = kTileCols / 4;             // float4 per stage
+constexpr size_t kStageBytes = kTileCols * 4;       // 32 KiB
+constexpr int kMap = 64;                            // tile -> row map, a ring
+constexpr int kTileKeys = 32;     // top-k candidates a tile keeps
+constexpr int kRowKeys = 512;     // top-k candidates a row merges
+constexpr int kSplitMaxK = 64;    // larger k: the exact kernel
+constexpr int kHardOffset = 64;   // hard-row list: count at [0], rows from [64]
+constexpr int kCount1 = 1;        // header word: length of the row list
+constexpr int kMaxSeeds = 8;      // noise seeds of one call
+constexpr float kRawLimit = 256.0f;
+// Slack (log2 units) of the race bounds: covers the roundings of the
+// reference c and of x * log2(e) / Te (a few 1e-5 for |s| up to a few
+// hundred).
+constexpr float kRaceSlack = 0x1p-10f;
+
+// A pass-1 row: its temperature and the quotient constants (16 bytes).
+struct alignas(16) RowTemp {
+    float temp;
+    float qt;
+    float qy;
+    int qmode;
+};
+
+// Pass-1 record of a tile (96 bytes).
+struct alignas(16) TileStats {
+    float m;      // max exact quotient (-inf: none)
+    float s;      // sum e^(s - m)
+    float w;      // sum e^(s - m) (s - m)
+    int arg;      // lowest column holding the raw max (the tile's first column if none)
+    float xmax;   // raw max
+    int pad[3];
+    uint32_t wmax[kSWarps];  // order keys of the warps' raw maxima, 0: no columns
+    int wcol[kSWarps];       // lowest column holding each warp's raw max (INT_MAX: none)
+};
+static_assert(sizeof(TileStats) == 96, "tile record");
+
+enum : int { kFNoisy = 1, kFTopk = 2, kFRaw = 4 };
+
+// A row after the merge (64 bytes), followed in the row's entry by one
+// SeedRec per noise seed.
+struct alignas(16) RowRecord {
+    float M;      // max scaled logit (exact), -inf: the row is -inf everywhere
+    float log2s;  // log2 S
+    float ls;     // RN(log2(e) * RN(1/Te))
+    float c2;     // raw rows: RN(RN(Mraw * ls) + log2 S)
+    float thr;    // top-k threshold (raw logit)
+    float lns;    // log S
+    int arg;      // lowest column holding the raw row max
+    int flags;
+    float qt, qy;
+    int qmode;
+    float cthr;   // a logit whose exact quotient equals M is at least this
+    int pad[4];
+};
+static_assert(sizeof(RowRecord) == 64, "row record");
+
+// The race bound of one seed for a row (16 bytes).
+struct alignas(16) SeedRec {
+    float B;      // best Gumbel-max score among the warps' candidates
+    float cB;     // raw rows: RN(RN(Mraw * ls) + (B - M) log2(e)) - slack
+    int bcol;     // its column
+    int pad;
+};
+constexpr size_t kRowEntryMax = sizeof(RowRecord) + kMaxSeeds * sizeof(SeedRec);
+
+// Pass-2 record of a tile: candidate count and the lowest column below the
+// raw max whose exact quotient is M (8 bytes); per seed, the race winner.
+struct alignas(8) TileEnd {
+    int nk;
+    int acol;
+};
+struct alignas(8) TileSeed {
+    float b;
+    int col;
+};
+
+struct SplitParams {
+    const float* logits;
+    int64_t row_stride;
+    int64_t rows;
+    int64_t row0;
+    int64_t canvas_len;
+    const float* temps;
+    const uint8_t* keep;
+    int64_t* argmax;
+    int64_t* sample;      // [n_seeds, rows]
+    float* entropy;
+    void* probs;
+    int64_t probs_row_stride;
+    int32_t* out_ids;
+    float* out_lp;
+    int32_t* hard;    // header (hard count, list lengths), then hard rows
+    int32_t* list1;   // the rows the passes work on
+    RowTemp* rt;
+    TileStats* ts;    // by tile (list index * G + tile of the row)
+    unsigned char* rr;  // by row: RowRecord + n_seeds SeedRec (rec_bytes each)
+    TileEnd* te;      // by tile
+    TileSeed* tb;     // by tile and seed
+    uint64_t* keys;   // by tile
+    // Row map (the stash): rows are entries e < *map_count of a list, read
+    // from logits row map_row[e] with temperature map_temp[e], all kept;
+    // null for the ordinary calls. out_m / out_logs (or null) receive each
+    // row's max scaled logit and log S from the merge.
+    const int32_t* map_row;
+    const float* map_temp;
+    const int32_t* map_count;
+    float* out_m;
+    float* out_logs;
+    int li_begin;     // the list entries of this launch: [li_begin, li_end),
+    int li_end;       // li_end < 0: to the end of the list
+    int* err;
+    PhiloxRoundKeys rk[kMaxSeeds];
+    int n_seeds;
+    int rec_bytes;    // sizeof(RowRecord) + n_seeds * sizeof(SeedRec)
+    int vocab;
+    int tiles_per_row;  // pass-2 tiles of a row (the finish's records)
+    int tiles1;         // pass-1 tiles of a row (the merge's records)
+    int vec;          // rows start 16-byte aligned: bulk copies
+    int probs_dtype;  // 0 none, 1 bf16, 2 fp16
+    int probs_vec;    // 8-byte probability stores
+    int index32;
+    int stats;
+    int k;
+    int fault;        // test hook: CTA 0 withholds its first tile of pass 1
+};
+
+// ------------------------------------------------------------ helpers
+
+__device__ __forceinline__ uint64_t slot_of(const SplitParams& p, uint64_t grow) {
+    return p.index32 ? static_cast<uint64_t>(static_cast<uint32_t>(grow) /
+                                             static_cast<uint32_t>(p.canvas_len))
+                     : grow / static_cast<uint64_t>(p.canvas_len);
+}
+
+__device__ __forceinline__ void set_comp(float4& v, int q, float x) {
+    if (q == 0) v.x = x;
+    else if (q == 1) v.y = x;
+    else if (q == 2) v.z = x;
+    else v.w = x;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ float max4f(const float4& v) { return max3(v.x, v.y, fmaxf(v.z, v.w)); }
+
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// 2^x with subnormal results flushed to zero (a single special-function
+// instruction).
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Order-preserving unsigned form of an fp32 value (-inf lowest, above 0).
+__device__ __forceinline__ uint32_t ord32(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unord32(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+constexpr uint32_t kOrdNegInf = 0x007FFFFFu;
+
+// Top-k key: the value (-0.0 as +0.0) in the high word, then the lower
+// column first (the _lp_topk_kernel key order).
+__device__ __forceinline__ uint64_t topk_key(float s, int col) {
+    return (static_cast<uint64_t>(ord32(s + 0.0f)) << 32) |
+           static_cast<uint32_t>(0x7FFFFFFF - col);
+}
+__device__ __forceinline__ float key_value(uint64_t key) {
+    return unord32(static_cast<uint32_t>(key >> 32));
+}
+__device__ __forceinline__ int key_col(uint64_t key) {
+    return 0x7FFFFFFF - static_cast<int>(static_cast<uint32_t>(key));
+}
+
+// Two values rounded to nearest even and packed (a in the low half), in one
+// conversion instruction.
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    uint32_t r;
+    if (BF16) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// Philox4x32-10 of (group, 0, row) with the per-seed round keys: each round's
+// two 32x32->64 products taken as one wide multiplication each.
+__device__ __forceinline__ uint4 noise_group(const PhiloxRoundKeys& rk, uint64_t row,
+                                             uint32_t group) {
+    uint32_t c0 = group, c1 = 0u, c2 = static_cast<uint32_t>(row), c3 = static_cast<uint32_t>(row >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        uint64_t pa, pb;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(pa) : "r"(c0), "r"(0xD2511F53u));
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(pb) : "r"(c2), "r"(0xCD9E8D57u));
+        const uint32_t hi_a = static_cast<uint32_t>(pa >> 32), lo_a = static_cast<uint32_t>(pa);
+        const uint32_t hi_b = static_cast<uint32_t>(pb >> 32), lo_b = static_cast<uint32_t>(pb);
+        c0 = hi_b ^ c1 ^ rk.k0[r];
+        c1 = lo_b;
+        c2 = hi_a ^ c3 ^ rk.k1[r];
+        c3 = lo_a;
+    }
+    return make_uint4(c0, c1, c2, c3);
+}
+
+// The list entries of this launch: [li_begin, list_end).
+__device__ __forceinline__ int list_end(const SplitParams& p) {
+    const int n = p.hard[kCount1];
+    return p.li_end < 0 || p.li_end > n ? n : p.li_end;
+}
+
+// A warp's part of a tile's statistics: the raw max and its lowest column,
+// S and W relative to the reference of the warp.
+struct WarpPart {
+    float m, s, w, xmax;
+    int arg;
+};
+
+// e^(s - B) of a group, over-estimated by the slack: 2^(x ls - cB) on raw
+// rows, else from the exact quotients (flushed below 2^-126: such elements
+// cannot win).
+__device__ __forceinline__ float4 race_e(const float4& x, bool raw, float ls, const SeedRec& sr,
+                                         const ScaledQuotient& sq) {
+    float4 e;
+    if (raw) {
+        e.x = ex2_ftz(fmaf(x.x, ls, -sr.cB));
+        e.y = ex2_ftz(fmaf(x.y, ls, -sr.cB));
+        e.z = ex2_ftz(fmaf(x.z, ls, -sr.cB));
+        e.w = ex2_ftz(fmaf(x.w, ls, -sr.cB));
+    } else {
+        e.x = ex2_ftz(fmaf(sq.exact(x.x) - sr.B, kLog2e, kRaceSlack));
+        e.y = ex2_ftz(fmaf(sq.exact(x.y) - sr.B, kLog2e, kRaceSlack));
+        e.z = ex2_ftz(fmaf(sq.exact(x.z) - sr.B, kLog2e, kRaceSlack));
+        e.w = ex2_ftz(fmaf(sq.exact(x.w) - sr.B, kLog2e, kRaceSlack));
+    }
+    return e;
+}
+
+struct Best {
+    float s;
+    int c;
+};
+
+// The survivors `bits` of the group at column c4 scored exactly (s + g)
+// against the best so far; the column of B was scored already.
+static __device__ __noinline__ Best race_rescore(uint32_t bits, const float4 x4, uint4 nw, int c4,
+                                          int bcol, ScaledQuotient sq, Best best) {
+    while (bits) {
+        const int q = __ffs(bits) - 1;
+        bits &= bits - 1;
+        const int col = c4 + q;
+        if (col == bcol) continue;
+        const float score = sq.exact(comp(x4, q)) + gumbel_of_bits(word_of(nw, q));
+        if (beats(score, col, best.s, best.c)) best = Best{score, col};
+    }
+    return best;
+}
+
+// The top-k candidates of a thread's slots in `smask` (slot i: bit i): the
+// logits x >= thr, read again from the stage, keyed by (exact value, lower
+// column) into the tile's list.
+static __device__ __noinline__ void topk_collect(uint32_t smask, const float4* stage, int tid, int col0,
+                                          int ncols, float thr, ScaledQuotient sq, int* count,
+                                          uint64_t* kdst) {
+    while (smask) {
+        const int f = (__ffs(smask) - 1) * kSThreads + tid;
+        smask &= smask - 1;
+        const float4 x4 = stage[f];
+        for (int q = 0; q < 4; ++q) {
+            const float x = comp(x4, q);
+            if (4 * f + q < ncols && x >= thr) {
+                const int pos = atomicAdd(count, 1);
+                if (pos < kTileKeys) kdst[pos] = topk_key(sq.exact(x), col0 + 4 * f + q);
+            }
+        }
+    }
+}
+
+}  // namespace rs
+}  // namespace drs
