@@ -123,9 +123,14 @@ drs_status drs_row_stats(const float *logits, int64_t rows, int64_t vocab,
  * device current) and caches it; make that first call before any stream
  * capture. All calls on a device share the array: two calls that can run
  * at the same time on the GPU (different streams, overlapping) race and
- * corrupt each other's results. Each call clears the part of the array it
- * uses (an asynchronous memset on its stream) before its kernel runs, so
- * what an earlier call left there is never read.
+ * corrupt each other's results. Each call resets the list counters at the
+ * start of the array (an asynchronous memset on its stream) before its
+ * kernels run; every other record in the array is written before it is read
+ * within the same call, so what an earlier call left there is never used.
+ * The cached address belongs to the device's CUDA context: after
+ * cudaDeviceReset (or anything else that destroys the primary context) the
+ * library must be unloaded and loaded again before this entry point is
+ * called on that device.
  */
 drs_status drs_row_stats_noalloc(const float *logits, int64_t rows, int64_t vocab,
                                  int64_t row_stride, const float *temps,
@@ -277,20 +282,34 @@ drs_status drs_scaled_logits(const float *logits, int64_t n, float temp,
 void drs_test_inject_fault(int code);
 
 /*
+ * Test hook (not for production use). on != 0: from now on every
+ * row-statistics call of this process takes the two streaming passes over
+ * the logits (list of rows, pass 1, merge, pass 2, finish) even where the
+ * one-read cluster kernel would take it (rows that start 16-byte aligned,
+ * vocab a multiple of 4 and at most 262144, one seed, k <= 64). Results are
+ * the same within the tolerances of the method; the hook exists so that
+ * both implementations can be tested and timed on the same inputs. on == 0
+ * restores the automatic choice.
+ */
+void drs_test_two_pass(int on);
+
+/*
  * Measurement hook (not part of the sampler). enable != 0: from now on every
  * row-statistics call on the current device (drs_row_stats, its no-alloc and
  * top-k variants, drs_topk_logprobs for k <= 64) records a CUDA event on
- * its stream before each of its five kernels (list of rows, pass 1, merge,
- * pass 2, finish) and after the last; the count of recorded calls restarts
- * at 0. enable == 0 stops recording. The events of the last 64 calls are
- * kept. Returns DRS_OK or DRS_ERR_CUDA (event creation failed).
+ * its stream before each of six kernel slots (list of rows, pass 1, merge,
+ * pass 2, cluster, finish) and after the last; the slots a call does not
+ * launch (the two passes or the cluster kernel) measure about 0. The count
+ * of recorded calls restarts at 0. enable == 0 stops recording. The events
+ * of the last 64 calls are kept. Returns DRS_OK or DRS_ERR_CUDA (event
+ * creation failed).
  */
 drs_status drs_kernel_timing(int enable);
 
 /*
- * Average device time in ms of each kernel of the recorded calls (see
+ * Average device time in ms of each kernel slot of the recorded calls (see
  * drs_kernel_timing), in the order above, into the HOST array avg_ms[n]
- * (entries past the fifth are 0); *calls (HOST) receives the number of
+ * (entries past the sixth are 0); *calls (HOST) receives the number of
  * calls averaged (at most 64). Waits for the recorded events. Returns
  * DRS_OK, DRS_ERR_INVALID_ARG (null pointer, n < 0) or DRS_ERR_CUDA.
  */
@@ -312,8 +331,10 @@ size_t drs_stash_workspace_bytes(int64_t requests, int64_t canvas_len, int64_t v
  * slots[j] * canvas_len + p of the outputs receives `width` columns of
  * (id, value):
  *   column 0        the argmax of the scaled row (lowest column of the max);
- *   then            token_ids[j * ids_stride + c] for c < num_token_ids[j]
- *                   when token_ids is given and num_token_ids[j] > 0, else
+ *   then            token_ids[j * ids_stride + c] for c < n_j =
+ *                   min(num_token_ids[j], ids_stride) when token_ids is
+ *                   given and n_j > 0 (a request's list holds ids_stride
+ *                   ids; a larger count reads no further), else
  *                   the num_topk largest (value descending, lower column
  *                   first);
  *   then            id 0 with value -inf, up to `width`.

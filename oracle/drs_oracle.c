@@ -13,10 +13,13 @@
  *     in the model dtype;
  *   - sample_row_stats docstring: row i uses temps[i // canvas_len]; a zero
  *     temperature is greedy, and the entropy clamps T at 1e-10;
- *   - sample_row_stats_reference: the PyTorch definition followed step by
- *     step below (divide by clamp(T, 1e-10), uniform noise clamped at 1e-20,
- *     noisy = scaled + (-log(-log u)) * (T > 0), log_softmax, exp,
- *     entropy = -sum over p > 0 of p log p, argmax of scaled and of noisy);
+ *   - sample_row_stats_reference, read for its definitions (not transcribed):
+ *     the scaled logit is the logit over the temperature clamped at 1e-10;
+ *     the noise is a Gumbel variate -log(-log u) of a uniform u clamped
+ *     below at 1e-20, added only where T > 0; the sample is the Gumbel-max
+ *     argmax of scaled + noise; the entropy is that of the softmax of the
+ *     scaled row, masked columns contributing nothing; the probabilities are
+ *     the softmax in the model dtype; ties go to the lowest column;
  *   - stash_converged_logprobs docstring and _lp_topk_kernel docstring: the
  *     num_topk largest scaled logits of kept rows, ordered by value and then
  *     by lower index, and their logprobs; the stash layout (request rows
@@ -392,7 +395,9 @@ int oracle_topk_rows(const float *const *row_ptrs, const float *temps, int64_t n
  * receives `width` columns of (id, value):
  *   column 0              the argmax (lowest column of the max);
  *   the next columns      token_ids[j * ids_stride + c] for c < n_j when
- *                         token_ids is given and n_j = num_token_ids[j] > 0,
+ *                         token_ids is given and n_j = min(num_token_ids[j],
+ *                         ids_stride) > 0 (a request's list has ids_stride
+ *                         entries),
  *                         else the num_topk largest (value descending, lower
  *                         column first);
  *   the rest              id 0 with value -inf.
@@ -456,9 +461,10 @@ int oracle_stash(const float *logits, int64_t row_stride, int64_t vocab, int64_t
                 vals[w] = ORACLE_VALUE(arg);
                 ++w;
             }
-            int32_t n_ids = token_ids && num_token_ids ? num_token_ids[j] : 0;
+            int64_t n_ids = token_ids && num_token_ids ? num_token_ids[j] : 0;
+            if (n_ids > ids_stride) n_ids = ids_stride;
             if (n_ids > 0) {
-                for (int32_t c = 0; c < n_ids && w < width; ++c, ++w) {
+                for (int64_t c = 0; c < n_ids && w < width; ++c, ++w) {
                     int32_t id = token_ids[j * ids_stride + c];
                     ids[w] = id;
                     vals[w] = ORACLE_VALUE(id);

@@ -324,6 +324,33 @@ def test_gumbel_max_constant_row_is_uniform():
     assert np.all(r["argmax"] == 0)
 
 
+def test_sample_gap_and_best_match_a_numpy_ranking():
+    """The near-tie classifier the parity tests rely on: for every noisy row
+    the oracle's sample, best score and gap (best minus second-best) equal a
+    numpy ranking of the scores x / T (fp32 quotient) + g, with g computed
+    here from the Philox words (u = max((w >> 8) 2^-24, 1e-20f), g =
+    -log(-log u)); greedy rows report an infinite gap and the max."""
+    x, temps, W = _tiny_inputs()
+    rows, vocab = x.shape
+    seed = 31
+    r = oracle.row_stats(x, temps, W, seed=seed, threads=8)
+    bits, _ = oracle.philox_gumbel(seed, 0, rows, vocab)
+    u = np.maximum((bits >> 8).astype(np.float32) * np.float32(2.0 ** -24), np.float32(1e-20))
+    g = -np.log(-np.log(u.astype(np.float64)))
+    for i in range(rows):
+        t = temps[i // W]
+        s = (x[i] / np.float32(max(t, 1e-10))).astype(np.float32).astype(np.float64)
+        if t <= 0:
+            assert r["sample_gap"][i] == np.inf and r["sample_best"][i] == s.max()
+            continue
+        score = s + g[i]
+        order = np.argsort(-score, kind="stable")
+        best, second = score[order[0]], score[order[1]]
+        assert r["sample"][i] == order[0]
+        assert abs(r["sample_best"][i] - best) <= 1e-12 * max(1.0, abs(best))
+        assert abs(r["sample_gap"][i] - (best - second)) <= 1e-12 * max(1.0, abs(best))
+
+
 # ------------------------------------------------------------------ top-k
 
 def _stable_topk(x, te, k):

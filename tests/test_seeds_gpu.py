@@ -1,9 +1,12 @@
 """GPU parity of drs_row_stats_seeds: several noise seeds in one call.
 
-The argmax, entropy and probabilities equal drs_row_stats's; the sample of
-seed s equals drs_row_stats with that seed (bit for bit: the race of every
-seed runs on the same tile, with the same B rule), and the oracle's on
-sampled rows. The strided workload is the multi-seed configuration of the
+The argmax equals drs_row_stats's and the sample of seed s equals
+drs_row_stats with that seed, bit for bit (every implementation scores the
+race's survivors exactly: s = x / Te by the exact quotient plus the fp32
+noise); the entropy and the probabilities agree within the parity
+tolerances (one-seed calls may take the one-read cluster kernel, several
+seeds the two passes, whose roundings of the exponent differ), and all of
+them match the oracle on sampled rows. The strided workload is the multi-seed configuration of the
 task (eight seeds, no probabilities, T = 1).
 """
 import numpy as np
@@ -29,7 +32,8 @@ def _compare_to_single(x, temps, canvas, seeds, probs_dtype, row0=0):
         assert torch.equal(smp[i], s1), f"seed {sd}"
         assert float((e - e1).abs().max()) <= ENTROPY_ABS if e.numel() else True
         if p is not None:
-            assert torch.equal(p, p1)
+            c, c1 = p.view(torch.int16).int(), p1.view(torch.int16).int()
+            assert int((c - c1).abs().max()) <= 1
     assert lib.drs_get_device_error() == 0
     return a, smp, e, p
 

@@ -88,6 +88,17 @@ def test_stash_against_oracle(vocab, k, ids_path, mode):
              f"V={vocab} k={k} ids={ids_path} logits={mode}")
 
 
+def test_stash_token_counts_past_the_list():
+    """num_token_ids larger than ids_stride: a request's list holds ids_stride
+    ids, the rest of the count is padding. The last request's count runs
+    past the end of the token-id array, which must not be read."""
+    x, src, slots, keep, valid, temps, tok, nti, m, canvas = _batch(4, 5000)
+    keep = np.ones(m, np.uint8)
+    valid = np.full(m, canvas, np.int32)
+    nti = np.array([4, 9, 4, 1, 7], np.int32)
+    _compare(x, canvas, src, slots, keep, valid, temps, 2, nti, tok, 12, False, "counts past the list")
+
+
 def test_stash_width_truncates_token_ids():
     x, src, slots, keep, valid, temps, tok, nti, m, canvas = _batch(3, 5000)
     _compare(x, canvas, src, slots, keep, valid, temps, 2, nti, tok, 3, False, "width 3")

@@ -38,7 +38,7 @@ EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_row_stats_noa
             "drs_status_string", "drs_get_device_error", "drs_test_inject_fault",
             "drs_kernel_timing", "drs_kernel_times", "drs_row_stats_seeds",
             "drs_row_stats_seeds_workspace_bytes", "drs_stash_converged_logprobs",
-            "drs_stash_workspace_bytes")
+            "drs_stash_workspace_bytes", "drs_test_two_pass")
 
 
 class DrsError(RuntimeError):
@@ -99,6 +99,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_status_string.restype = ctypes.c_char_p
     lib.drs_test_inject_fault.argtypes = [ctypes.c_int]
     lib.drs_test_inject_fault.restype = None
+    lib.drs_test_two_pass.argtypes = [ctypes.c_int]
+    lib.drs_test_two_pass.restype = None
     lib.drs_get_device_error.argtypes = [vp]
     lib.drs_get_device_error.restype = ctypes.c_int
     lib.drs_row_stats_seeds_workspace_bytes.argtypes = [i64, i64, i32]
@@ -266,7 +268,8 @@ def drs_scaled_logits(logits, temp: float, out, stream=None):
     _check(st, "drs_scaled_logits")
 
 
-KERNEL_NAMES = ("split_prep", "split_pass1", "split_merge", "split_pass2", "split_finish")
+KERNEL_NAMES = ("split_prep", "split_pass1", "split_merge", "split_pass2", "split_cluster",
+                "split_finish")
 
 
 def drs_kernel_timing(enable: bool) -> None:
@@ -290,6 +293,13 @@ def drs_test_inject_fault(code: int) -> None:
     """Test hook: in the next row-statistics call a CTA never fills its first
     stage, so that the bounded waits on it run out (see include/drs.h)."""
     load().drs_test_inject_fault(code)
+
+
+def drs_test_two_pass(on: bool) -> None:
+    """Test hook: every following row-statistics call takes the two passes
+    over the logits instead of the one-read cluster kernel (see
+    include/drs.h)."""
+    load().drs_test_two_pass(1 if on else 0)
 
 
 def drs_get_device_error(stream=None) -> int:

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libdrs.so")
 
-SOURCES = ["capi.cu", "row_stats.cu", "row_split.cu", "topk.cu", "stash.cu", "philox_gumbel.cu", "scale.cu"]
+SOURCES = ["capi.cu", "row_stats.cu", "row_split.cu", "row_cluster.cu", "topk.cu", "stash.cu", "philox_gumbel.cu", "scale.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No fast-math: IEEE division, denormals kept (the probabilities can be
 # fp32 subnormals that are still representable in bf16).

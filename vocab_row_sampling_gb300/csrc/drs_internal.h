@@ -92,10 +92,14 @@ struct RowCall {
 // cleared by reading it.
 int take_injected_fault();
 
+// The test hook drs_test_two_pass: every row-statistics call takes the two
+// passes, even where the one-read cluster kernel would.
+bool two_pass_forced();
+
 // Kernel timing (drs_kernel_timing): the ring slot of the calling row
 // statistics call, or -1 when timing is off; the event to record before its
 // kernel i (after the last kernel: i = kTimedKernels).
-constexpr int kTimedKernels = 5;  // prep, pass 1, merge, pass 2, finish
+constexpr int kTimedKernels = 6;  // prep, pass 1, merge, pass 2, cluster, finish
 constexpr int kTimedCalls = 64;
 int kernel_timer_slot();
 cudaEvent_t kernel_timer_event(int slot, int i);

@@ -348,5 +348,40 @@ static __device__ __noinline__ void topk_collect(uint32_t smask, const float4* s
     }
 }
 
+// Count a warp out of a stage; true on the warp that counted out last (the
+// count is reset for the stage's next tile).
+__device__ __forceinline__ bool release_stage(int* count, int lane) {
+    int last = 0;
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(count, 1) == kSWarps - 1;
+        if (last) *count = 0;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) __threadfence_block();
+    return last != 0;
+}
+
+// The one-read path (row_cluster.cu): a row split over the CTAs of a
+// thread-block cluster, the CTAs' partial results merged through distributed
+// shared memory. ClusterShape: columns per CTA (a multiple of 4), pieces of
+// 8192 columns per CTA, and how many of its largest group maxima each CTA
+// contributes to the row's top-k threshold.
+struct ClusterShape {
+    int chunk_cols;
+    int pieces;
+    int top_m;
+};
+// Whether the cluster path takes a call (rows start 16-byte aligned, vocab a
+// multiple of 4 and at most 262144, one seed, k <= 64); its shape and cluster
+// size.
+bool cluster_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16, ClusterShape* out,
+                  int* cluster_size);
+// Launch the cluster kernel on the rows of the list (after split_prep, before
+// split_finish with tiles_per_row = cluster size).
+drs_status cluster_launch(const SplitParams& p, const ClusterShape& cs, int cluster_size, int64_t rows,
+                          cudaStream_t stream);
+
 }  // namespace rs
 }  // namespace drs

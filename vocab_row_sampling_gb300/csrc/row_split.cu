@@ -141,21 +141,6 @@ __device__ __forceinline__ TileRange launch_tiles(const SplitParams& p, int G) {
     return TileRange{static_cast<int64_t>(p.li_begin) * G, static_cast<int64_t>(list_end(p)) * G};
 }
 
-// Count a warp out of a stage; true on the warp that counted out last (the
-// count is reset for the stage's next tile).
-__device__ __forceinline__ bool release_stage(int* count, int lane) {
-    int last = 0;
-    __syncwarp();
-    if (lane == 0) {
-        __threadfence_block();
-        last = atomicAdd(count, 1) == kSWarps - 1;
-        if (last) *count = 0;
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) __threadfence_block();
-    return last != 0;
-}
-
 // Pipeline start: barriers, the first kMap tiles mapped, the first kStages
 // issued (the row record of stage s at recs + s * rec_stride). COLS: the
 // pass's tile width; G: its tiles per row.
@@ -1153,7 +1138,9 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_cons
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
         const int c = lane + 32 * u;
-        n[u] = c < G ? te[c].nk : 0;
+        // (clamped: records of a call whose bounded waits ran out may hold
+        // anything; a count past kTileKeys sends the row to the exact kernel)
+        n[u] = c < G ? min(max(te[c].nk, 0), kTileKeys + 1) : 0;
         over_l |= n[u] > kTileKeys;
     }
     const bool over = __any_sync(0xffffffffu, over_l);
@@ -1356,15 +1343,27 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess;
     };
+    // one read per row where the cluster kernel takes the call, else the two
+    // passes; the finish reduces the per-tile records of either
+    ClusterShape cshape{};
+    int csize = 0;
+    if (!two_pass_forced() && cluster_plan(c.rows, c.vocab, c.k, n_seeds, p.vec != 0, &cshape, &csize)) {
+        if (!mark(2) || !mark(3) || !mark(4)) return DRS_ERR_CUDA;
+        if (cluster_launch(p, cshape, csize, c.rows, stream) != DRS_OK || !mark(5)) return DRS_ERR_CUDA;
+        p.tiles_per_row = csize;
+        if (!pdl(split_finish<kTilesSmall>, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(6))
+            return DRS_ERR_CUDA;
+        return DRS_OK;
+    }
     if (!pdl(split_pass1, g1, kSThreads, smem1) || !mark(2)) return DRS_ERR_CUDA;
     const bool short_merge = G1 * kSWarps <= 32 * kOrdSmall;
     const bool ok3 = short_merge ? pdl(split_merge<kOrdSmall, 1>, static_cast<int>(gr), kRowWarps * 32, 0)
                                  : pdl(split_merge<kOrdWide, kWideMergeWarps>, static_cast<int>(c.rows),
                                        kRowWarps * 32, 0);
     if (!ok3 || !mark(3)) return DRS_ERR_CUDA;
-    if (!pdl(pass2, g2, kSThreads, smem) || !mark(4)) return DRS_ERR_CUDA;
+    if (!pdl(pass2, g2, kSThreads, smem) || !mark(4) || !mark(5)) return DRS_ERR_CUDA;
     auto finish = G <= 32 * kTilesSmall ? split_finish<kTilesSmall> : split_finish<kTilesLarge>;
-    if (!pdl(finish, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(5)) return DRS_ERR_CUDA;
+    if (!pdl(finish, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(6)) return DRS_ERR_CUDA;
     return DRS_OK;
 }
 

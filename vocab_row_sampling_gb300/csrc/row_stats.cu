@@ -21,6 +21,8 @@ namespace {
 
 // The fault-injection hook (drs_test_inject_fault).
 std::atomic<int> g_inject_fault{0};
+// The two-pass hook (drs_test_two_pass).
+std::atomic<int> g_two_pass{0};
 
 drs_status check_stats_args(const float* logits, int64_t rows, int64_t vocab, int64_t row_stride,
                             const float* temps, int64_t canvas_len, int64_t row0, int64_t* argmax,
@@ -71,6 +73,10 @@ drs_status run_topk(RowCall c, void* workspace, cudaStream_t stream) {
 int drs::take_injected_fault() { return drs::g_inject_fault.exchange(0); }
 
 extern "C" void drs_test_inject_fault(int code) { drs::g_inject_fault.store(code); }
+
+bool drs::two_pass_forced() { return drs::g_two_pass.load() != 0; }
+
+extern "C" void drs_test_two_pass(int on) { drs::g_two_pass.store(on ? 1 : 0); }
 
 extern "C" size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab) {
     if (rows < 0 || vocab < 1) return 0;

@@ -109,7 +109,11 @@ __global__ void __launch_bounds__(kWriteWarps * 32) stash_write(const __grid_con
     const float big_m = p.row_m[e];
     const float logs = p.row_logs[e];
     const int32_t* keys = p.top_ids + e * p.kq;
-    const int n_ids = p.token_ids && p.num_token_ids ? p.num_token_ids[j] : 0;
+    // a request's list holds ids_stride ids at most: a larger count reads no
+    // further (the columns past the list are padding)
+    const int n_ids = p.token_ids && p.num_token_ids
+                          ? static_cast<int>(min(static_cast<int64_t>(p.num_token_ids[j]), p.ids_stride))
+                          : 0;
     for (int c = lane; c < p.width; c += 32) {
         int id = 0;
         bool has = true;
