@@ -40,6 +40,36 @@ uint32_t next_generation() {
     return g == 0 ? next_generation() : g;
 }
 
+// A second stream per device and a pair of events for the row calls that
+// split their rows between the cluster kernel and the two passes (the two
+// parts run at the same time on different SMs): created on first use, kept
+// until the process exits.
+namespace {
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join = nullptr;
+};
+SideStream g_side[kMaxDevices];
+}  // namespace
+
+bool side_stream(cudaStream_t* stream, cudaEvent_t* fork, cudaEvent_t* join) {
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    SideStream& s = g_side[dev];
+    if (!s.stream) {
+        if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) return false;
+        if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess)
+            return false;
+    }
+    *stream = s.stream;
+    *fork = s.fork;
+    *join = s.join;
+    return true;
+}
+
 int sm_count() {
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return 0;

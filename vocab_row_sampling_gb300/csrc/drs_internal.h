@@ -21,6 +21,12 @@ uint32_t next_generation();
 // Streaming multiprocessors of the current device.
 int sm_count();
 
+// The current device's second stream and its fork and join events (created on
+// first use): a call that runs part of its work beside the caller's stream
+// records `fork` on it, makes the second stream wait for `fork`, and makes the
+// caller's stream wait for `join` recorded after the second part.
+bool side_stream(cudaStream_t* stream, cudaEvent_t* fork, cudaEvent_t* join);
+
 // Map a CUDA error to a status.
 inline drs_status cuda_status(cudaError_t e) {
     return e == cudaSuccess ? DRS_OK : DRS_ERR_CUDA;

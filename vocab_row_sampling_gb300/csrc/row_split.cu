@@ -59,6 +59,8 @@
 // A call can also pass a row map (the stash): its rows are then the entries
 // of a device list, each read from a mapped logits row with a mapped
 // temperature.
+#include <algorithm>
+
 #include "row_common.cuh"
 
 namespace drs {
@@ -1343,16 +1345,69 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kernel, p) == cudaSuccess;
     };
-    // one read per row where the cluster kernel takes the call, else the two
-    // passes; the finish reduces the per-tile records of either
+    // One read per row where the cluster kernel takes the call. Its clusters
+    // of up to 16 CTAs (one per SM) fit only the GPU's larger SM groups; on a
+    // large enough call the SMs they leave free run the two passes over the
+    // tail of the row list at the same time, on a second stream (the two
+    // parts fill one workspace, one finish kernel reduces both). Else the two
+    // passes alone.
     ClusterShape cshape{};
     int csize = 0;
     if (!two_pass_forced() && cluster_plan(c.rows, c.vocab, c.k, n_seeds, p.vec != 0, &cshape, &csize)) {
+        const int active = cluster_active(p.probs_dtype, csize);
+        if (active < 1) return DRS_ERR_CUDA;
+        const int free_sms = sm_count() - active * csize;
+        // rows per SM and time: the two passes about 4/5 of the cluster
+        // kernel's (the step workload), so the tail gets that share of the
+        // free SMs' weight
+        int64_t tail = 0;
+        cudaStream_t side = nullptr;
+        cudaEvent_t fork = nullptr, join = nullptr;
+        if (free_sms >= 8 && c.rows >= 8 * static_cast<int64_t>(active) && side_stream(&side, &fork, &join))
+            tail = c.rows * (4 * free_sms) / (4 * free_sms + 5 * active * csize);
+        const int64_t head = c.rows - tail;
+        p.tiles_per_row = G;
         if (!mark(2) || !mark(3) || !mark(4)) return DRS_ERR_CUDA;
-        if (cluster_launch(p, cshape, csize, c.rows, stream) != DRS_OK || !mark(5)) return DRS_ERR_CUDA;
-        p.tiles_per_row = csize;
-        if (!pdl(split_finish<kTilesSmall>, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(6))
-            return DRS_ERR_CUDA;
+        if (tail > 0) {
+            // the two passes over list entries [head, end) beside the cluster
+            // kernel, their persistent grids sized for the free SMs
+            if (cudaEventRecord(fork, stream) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
+                return DRS_ERR_CUDA;
+            SplitParams q = p;
+            q.li_begin = static_cast<int>(head);
+            q.li_end = -1;
+            q.tiles_per_row = G;
+            auto pdl_side = [&](auto kernel, int grid, int block, size_t dsmem) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(grid);
+                cfg.blockDim = dim3(block);
+                cfg.dynamicSmemBytes = dsmem;
+                cfg.stream = side;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                return cudaLaunchKernelEx(&cfg, kernel, q) == cudaSuccess;
+            };
+            const int gq1 = std::min(g1, 3 * free_sms);
+            const int gq2 = std::min(g2, 3 * free_sms);
+            const int64_t gt = (tail + kRowWarps - 1) / kRowWarps;
+            const bool short_m = G1 * kSWarps <= 32 * kOrdSmall;
+            if (!pdl_side(split_pass1, gq1, kSThreads, smem1) ||
+                !(short_m ? pdl_side(split_merge<kOrdSmall, 1>, static_cast<int>(gt), kRowWarps * 32, 0)
+                          : pdl_side(split_merge<kOrdWide, kWideMergeWarps>, static_cast<int>(tail), kRowWarps * 32,
+                                     0)) ||
+                !pdl_side(pass2, gq2, kSThreads, smem) || cudaEventRecord(join, side) != cudaSuccess)
+                return DRS_ERR_CUDA;
+        }
+        SplitParams pc = p;
+        pc.li_begin = 0;
+        pc.li_end = static_cast<int>(head);
+        if (cluster_launch(pc, cshape, csize, head, stream) != DRS_OK || !mark(5)) return DRS_ERR_CUDA;
+        if (tail > 0 && cudaStreamWaitEvent(stream, join, 0) != cudaSuccess) return DRS_ERR_CUDA;
+        auto finish = G <= 32 * kTilesSmall ? split_finish<kTilesSmall> : split_finish<kTilesLarge>;
+        if (!pdl(finish, static_cast<int>(gr), kRowWarps * 32, 0) || !mark(6)) return DRS_ERR_CUDA;
         return DRS_OK;
     }
     if (!pdl(split_pass1, g1, kSThreads, smem1) || !mark(2)) return DRS_ERR_CUDA;
