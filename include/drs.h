@@ -294,6 +294,24 @@ void drs_test_inject_fault(int code);
 void drs_test_two_pass(int on);
 
 /*
+ * Introspection (not part of the sampler): how a row-statistics call of
+ * these sizes shares its rows on the current device. Calls whose rows start
+ * 16-byte aligned, with vocab a multiple of 4 and at most 262144, one seed
+ * and k <= 64 read each row once, split over the CTAs of a thread-block
+ * cluster (*cluster_size CTAs per row, *clusters clusters resident at once,
+ * one CTA per SM); such clusters fit only some of the GPU's SM groups, and on
+ * large calls the *free_sms SMs they leave run the two streaming passes over
+ * the rows past the first *cluster_rows of the call's row list at the same
+ * time. Other calls take the two passes alone: *cluster_rows, *cluster_size,
+ * *clusters and *free_sms are then 0. probs_dtype: a drs_probs_dtype value.
+ * All outputs are HOST pointers. Returns DRS_OK, or DRS_ERR_INVALID_ARG for a
+ * null pointer or sizes out of range.
+ */
+drs_status drs_row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds,
+                              int probs_dtype, int64_t *cluster_rows, int32_t *cluster_size,
+                              int32_t *clusters, int32_t *free_sms);
+
+/*
  * Measurement hook (not part of the sampler). enable != 0: from now on every
  * row-statistics call on the current device (drs_row_stats, its no-alloc and
  * top-k variants, drs_topk_logprobs for k <= 64) records a CUDA event on

@@ -38,7 +38,8 @@ EXPORTED = ("drs_row_stats", "drs_row_stats_workspace_bytes", "drs_row_stats_noa
             "drs_status_string", "drs_get_device_error", "drs_test_inject_fault",
             "drs_kernel_timing", "drs_kernel_times", "drs_row_stats_seeds",
             "drs_row_stats_seeds_workspace_bytes", "drs_stash_converged_logprobs",
-            "drs_stash_workspace_bytes", "drs_test_two_pass")
+            "drs_stash_workspace_bytes", "drs_test_two_pass",
+            "drs_row_split_plan")
 
 
 class DrsError(RuntimeError):
@@ -101,6 +102,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_test_inject_fault.restype = None
     lib.drs_test_two_pass.argtypes = [ctypes.c_int]
     lib.drs_test_two_pass.restype = None
+    lib.drs_row_split_plan.argtypes = [i64, i64, i32, i32, ctypes.c_int, vp, vp, vp, vp]
+    lib.drs_row_split_plan.restype = ctypes.c_int
     lib.drs_get_device_error.argtypes = [vp]
     lib.drs_get_device_error.restype = ctypes.c_int
     lib.drs_row_stats_seeds_workspace_bytes.argtypes = [i64, i64, i32]
@@ -300,6 +303,22 @@ def drs_test_two_pass(on: bool) -> None:
     over the logits instead of the one-read cluster kernel (see
     include/drs.h)."""
     load().drs_test_two_pass(1 if on else 0)
+
+
+def cluster_rows(rows: int, vocab: int, k: int, n_seeds: int = 1, probs_dtype: int = DRS_PROBS_BF16):
+    """How a row-statistics call of these sizes shares its rows on the
+    current device (drs_row_split_plan): None when it takes the two passes
+    alone, else a dict with the rows of the cluster kernel ("head"), of the
+    two passes beside it ("tail"), the cluster size, the clusters resident
+    at once and the SMs they leave free."""
+    head, size, ncl, free = ctypes.c_int64(0), ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load().drs_row_split_plan(rows, vocab, k, n_seeds, probs_dtype,
+                                     ctypes.byref(head), ctypes.byref(size), ctypes.byref(ncl),
+                                     ctypes.byref(free)), "drs_row_split_plan")
+    if size.value == 0:
+        return None
+    return {"head": int(head.value), "tail": int(rows - head.value), "cluster_size": int(size.value),
+            "clusters": int(ncl.value), "free_sms": int(free.value)}
 
 
 def drs_get_device_error(stream=None) -> int:

@@ -118,4 +118,12 @@ int32_t split_max_k();
 int32_t split_max_seeds();
 drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream);
 
+// How split_rows shares a call's rows on the current device: the first
+// *head rows of its list go to the cluster kernel (*clusters clusters of
+// *cluster_size CTAs resident at once), the others to the two passes on the
+// *free_sms SMs the clusters leave. False when the call takes the two passes
+// alone.
+bool split_plan_query(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16, int probs_dtype,
+                      int64_t* head, int32_t* cluster_size, int32_t* clusters, int32_t* free_sms);
+
 }  // namespace drs

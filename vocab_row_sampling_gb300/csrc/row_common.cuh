@@ -431,6 +431,18 @@ struct ClusterShape {
 // size.
 bool cluster_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16, ClusterShape* out,
                   int* cluster_size);
+// How a call's rows are shared (see split_plan_query in drs_internal.h): the
+// last `tail` rows of the list go to the two passes on the free SMs.
+struct RowSplitPlan {
+    ClusterShape shape;
+    int cluster_size;
+    int clusters;
+    int free_sms;
+    int64_t tail;
+};
+bool row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16, int probs_dtype,
+                    RowSplitPlan* out);
+
 // Clusters of the cluster kernel resident at once on the current device
 // (0 on failure).
 int cluster_active(int probs_dtype, int cluster_size);

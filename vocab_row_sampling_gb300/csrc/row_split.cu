@@ -1248,6 +1248,35 @@ int32_t split_max_seeds() { return kMaxSeeds; }
 
 int32_t split_max_k() { return kSplitMaxK; }
 
+bool rs::row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16,
+                        int probs_dtype, RowSplitPlan* out) {
+    RowSplitPlan pl{};
+    if (!cluster_plan(rows, vocab, k, n_seeds, aligned16, &pl.shape, &pl.cluster_size)) return false;
+    pl.clusters = cluster_active(probs_dtype, pl.cluster_size);
+    if (pl.clusters < 1) return false;
+    pl.free_sms = sm_count() - pl.clusters * pl.cluster_size;
+    // rows per SM and time: the two passes about 4/5 of the cluster
+    // kernel's (measured on the step workload), so the tail gets that share
+    // of the free SMs' weight
+    pl.tail = 0;
+    if (pl.free_sms >= 8 && rows >= 8 * static_cast<int64_t>(pl.clusters))
+        pl.tail = rows * (4 * pl.free_sms) / (4 * pl.free_sms + 5 * pl.clusters * pl.cluster_size);
+    *out = pl;
+    return true;
+}
+
+bool split_plan_query(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16, int probs_dtype,
+                      int64_t* head, int32_t* cluster_size, int32_t* clusters, int32_t* free_sms) {
+    RowSplitPlan pl{};
+    if (two_pass_forced() || !rs::row_split_plan(rows, vocab, k, n_seeds, aligned16, probs_dtype, &pl))
+        return false;
+    *head = rows - pl.tail;
+    *cluster_size = pl.cluster_size;
+    *clusters = pl.clusters;
+    *free_sms = pl.free_sms;
+    return true;
+}
+
 drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     if (c.rows <= 0) return DRS_OK;
     if (c.k > kSplitMaxK || c.vocab > DRS_MAX_VOCAB) return DRS_ERR_UNSUPPORTED;
@@ -1351,20 +1380,15 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     // tail of the row list at the same time, on a second stream (the two
     // parts fill one workspace, one finish kernel reduces both). Else the two
     // passes alone.
-    ClusterShape cshape{};
-    int csize = 0;
-    if (!two_pass_forced() && cluster_plan(c.rows, c.vocab, c.k, n_seeds, p.vec != 0, &cshape, &csize)) {
-        const int active = cluster_active(p.probs_dtype, csize);
-        if (active < 1) return DRS_ERR_CUDA;
-        const int free_sms = sm_count() - active * csize;
-        // rows per SM and time: the two passes about 4/5 of the cluster
-        // kernel's (the step workload), so the tail gets that share of the
-        // free SMs' weight
-        int64_t tail = 0;
+    RowSplitPlan plan{};
+    if (!two_pass_forced() && rs::row_split_plan(c.rows, c.vocab, c.k, n_seeds, p.vec != 0, p.probs_dtype, &plan)) {
+        const ClusterShape cshape = plan.shape;
+        const int csize = plan.cluster_size;
+        const int free_sms = plan.free_sms;
+        int64_t tail = plan.tail;
         cudaStream_t side = nullptr;
         cudaEvent_t fork = nullptr, join = nullptr;
-        if (free_sms >= 8 && c.rows >= 8 * static_cast<int64_t>(active) && side_stream(&side, &fork, &join))
-            tail = c.rows * (4 * free_sms) / (4 * free_sms + 5 * active * csize);
+        if (tail > 0 && !side_stream(&side, &fork, &join)) tail = 0;
         const int64_t head = c.rows - tail;
         p.tiles_per_row = G;
         if (!mark(2) || !mark(3) || !mark(4)) return DRS_ERR_CUDA;

@@ -78,6 +78,21 @@ bool drs::two_pass_forced() { return drs::g_two_pass.load() != 0; }
 
 extern "C" void drs_test_two_pass(int on) { drs::g_two_pass.store(on ? 1 : 0); }
 
+extern "C" drs_status drs_row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds,
+                                         int probs_dtype, int64_t* cluster_rows, int32_t* cluster_size,
+                                         int32_t* clusters, int32_t* free_sms) {
+    if (!cluster_rows || !cluster_size || !clusters || !free_sms) return DRS_ERR_INVALID_ARG;
+    if (rows < 0 || vocab < 1 || n_seeds < 1 || probs_dtype < 0 || probs_dtype > 2) return DRS_ERR_INVALID_ARG;
+    *cluster_rows = 0;
+    *cluster_size = 0;
+    *clusters = 0;
+    *free_sms = 0;
+    if (rows == 0) return DRS_OK;
+    drs::split_plan_query(rows, vocab, k, n_seeds, true, probs_dtype, cluster_rows, cluster_size, clusters,
+                          free_sms);
+    return DRS_OK;
+}
+
 extern "C" size_t drs_row_stats_workspace_bytes(int64_t rows, int64_t vocab) {
     if (rows < 0 || vocab < 1) return 0;
     return drs::split_workspace_bytes(rows, vocab, 0, 1);
