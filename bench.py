@@ -627,16 +627,22 @@ def _e2e(args, drs, w, rank, world, row0, temps_all, keep, k):
 
 
 def kernel_source_hash():
-    """sha256 over the sources of the row kernels: a traffic figure taken
-    from an ncu capture is used only while they are unchanged."""
+    """sha256 over the code of the row kernels' sources (comments and blank
+    lines dropped): a traffic figure taken from an ncu capture is used only
+    while that code is unchanged."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in ("vocab_row_sampling_gb300/csrc/row_split.cu",
                 "vocab_row_sampling_gb300/csrc/row_cluster.cu",
                 "vocab_row_sampling_gb300/csrc/row_common.cuh",
                 "vocab_row_sampling_gb300/csrc/drs_device.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            code = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        for line in code.splitlines():
+            line = line.split("//", 1)[0].rstrip()
+            if line.strip():
+                h.update(line.encode() + b"\n")
     return h.hexdigest()
 
 

@@ -7,23 +7,26 @@
 // each owning a contiguous chunk of at most 16384 columns (64 KiB) that stays
 // in its shared memory from the bulk copy (TMA) that brings it in until the
 // probabilities have been written from it. A CTA holds three rows at once in
-// a ring of three chunk buffers and runs two kinds of warps:
+// a ring of three chunk buffers and runs four kinds of warps:
 //   16 compute warps: for row t, phase A -- per warp, the raw max and its
 //            lowest column, S = sum e^(s - m) and W = sum e^(s - m)(s - m)
 //            (raw-domain exponentials while |m| < 256, exact quotients
 //            beyond) -- then, for row t - 1 whose merged statistics are
 //            ready, phase B -- the probabilities, the argmax ties, the
 //            pruned Gumbel race against B, the top-k candidates;
-//   1 control warp: combines the compute warps' phase-A results into the
-//            CTA's part (m, S, W, raw max and column, the best Gumbel-max
-//            score of the warps' argmax elements, the CTA's largest group
-//            maxima), pushes it into every CTA of the cluster (st.async into
-//            distributed shared memory, completing on each receiver's
-//            mbarrier), merges the C parts of the row once they have landed
-//            (the row's M, S, W, argmax column, B and top-k threshold), and
-//            after phase B writes the CTA's race winner, argmax tie and
-//            candidate count and starts the copy of row t + 3 into the freed
-//            buffer.
+//   the merge warp: combines the compute warps' phase-A results into the
+//            CTA's part (m, S, W, raw max and column, the CTA's largest group
+//            maxima, the best Gumbel-max score of its warps' argmax
+//            elements), pushes it into every CTA of the cluster (st.async
+//            into distributed shared memory, completing on each receiver's
+//            mbarrier) and merges the C parts of the row once they have
+//            landed (the row's M, S, W, argmax column and B);
+//   the noise warp: the Gumbel-max scores of the warps' argmax elements
+//            for the part, then the row's top-k threshold from the parts;
+//   the feed warp: the ring of row entries, the bulk copies into the
+//            buffers, and after phase B the CTA's race winner, argmax tie
+//            and candidate count, before it starts the copy of row t + 3
+//            into the freed buffer.
 // The compute warps never wait for the exchange of their current row: while
 // it runs they work on the previous one. The CTA's results go to the same
 // per-tile records the two-pass kernels write (a CTA is one tile of its row),
