@@ -227,31 +227,69 @@ __device__ __forceinline__ void read_tile(float4 (&v)[VEC], float4* stage, const
 
 // ================================================================ prep
 
+// The list of rows the passes work on, in row order, and each listed row's
+// RowTemp. The order is fixed so that a call divides its list between the
+// cluster kernel and the two passes the same way on every run (the two sum a
+// row's exponentials in different orders). With statistics, every row is
+// listed: the list is the identity. With a row map (the stash), the first
+// *map_count entries when k > 0. Otherwise (top-k-only calls) the rows of
+// kept slots: CTA 0 walks the rows 256 at a time and places each kept row
+// after the kept rows before it (a block-wide count); the other CTAs write
+// the RowTemps of their rows.
+__device__ __forceinline__ bool prep_row(const SplitParams& p, int64_t row) {
+    if (row >= p.rows) return false;
+    uint64_t slot = 0;
+    bool kept;
+    if (p.map_row) {
+        kept = row < *p.map_count;  // every listed entry is kept
+    } else {
+        slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
+        kept = p.keep == nullptr || p.keep[slot] != 0;
+    }
+    const bool work = (p.stats && !p.map_row) || (p.k > 0 && kept);
+    if (work) {
+        const float temp = p.map_row ? p.map_temp[row] : p.temps[slot];
+        const ScaledQuotient q = ScaledQuotient::of(fmaxf(temp, kTempFloor));
+        p.rt[row] = RowTemp{temp, q.t, q.y, q.mode};
+    }
+    return work;
+}
+
 __global__ void __launch_bounds__(256) split_prep(const __grid_constant__ SplitParams p) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int lane = threadIdx.x & 31;
-    bool work = false;
-    if (row < p.rows) {
-        uint64_t slot = 0;
-        bool kept;
-        if (p.map_row) {
-            kept = row < *p.map_count;  // every listed entry is kept
-        } else {
-            slot = slot_of(p, static_cast<uint64_t>(p.row0 + row));
-            kept = p.keep == nullptr || p.keep[slot] != 0;
-        }
-        work = (p.stats && !p.map_row) || (p.k > 0 && kept);
-        if (work) {
-            const float temp = p.map_row ? p.map_temp[row] : p.temps[slot];
-            const ScaledQuotient q = ScaledQuotient::of(fmaxf(temp, kTempFloor));
-            p.rt[row] = RowTemp{temp, q.t, q.y, q.mode};
-        }
+    if (p.stats || p.map_row) {
+        const int64_t n = p.map_row ? (p.k > 0 ? min(static_cast<int64_t>(*p.map_count), p.rows) : 0) : p.rows;
+        if (prep_row(p, row) && row < n) p.list1[row] = static_cast<int32_t>(row);
+        if (row == 0) p.hard[kCount1] = static_cast<int32_t>(n);
+        return;
     }
-    const uint32_t b = __ballot_sync(0xffffffffu, work);
+    if (blockIdx.x != 0) {
+        prep_row(p, row);
+        return;
+    }
+    __shared__ int wcount[8];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     int base = 0;
-    if (lane == 0 && b) base = atomicAdd(p.hard + kCount1, __popc(b));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (work) p.list1[base + __popc(b & lanemask_lt())] = static_cast<int32_t>(row);
+    for (int64_t r0 = 0; r0 < p.rows; r0 += 256) {
+        const int64_t r = r0 + threadIdx.x;
+        // rows of CTA 0's own block: their RowTemp too; later rows: the flag
+        const bool work = r < 256 ? prep_row(p, r)
+                                  : r < p.rows && p.k > 0 &&
+                                        (p.keep == nullptr || p.keep[slot_of(p, static_cast<uint64_t>(p.row0 + r))] != 0);
+        const uint32_t b = __ballot_sync(0xffffffffu, work);
+        if (lane == 0) wcount[warp] = __popc(b);
+        __syncthreads();
+        int before = base, total = 0;
+        for (int w = 0; w < 8; ++w) {
+            before += w < warp ? wcount[w] : 0;
+            total += wcount[w];
+        }
+        if (work) p.list1[before + __popc(b & lanemask_lt())] = static_cast<int32_t>(r);
+        base += total;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) p.hard[kCount1] = base;
 }
 
 // ============================================================== pass 1

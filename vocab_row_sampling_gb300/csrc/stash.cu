@@ -66,34 +66,53 @@ struct StashParams {
     const float* row_logs;
 };
 
-__global__ void __launch_bounds__(256) stash_list(const __grid_constant__ StashParams p) {
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+// The list of kept (request, position) pairs, in order: one CTA walks the
+// pairs 1024 at a time and places each kept pair after the kept pairs before
+// it (a block-wide count), so that the list, and how the row kernels divide
+// it among themselves, is the same on every run.
+constexpr int kListThreads = 1024;
+
+__global__ void __launch_bounds__(kListThreads) stash_list(const __grid_constant__ StashParams p) {
+    __shared__ int wcount[kListThreads / 32];
     const int lane = threadIdx.x & 31;
-    bool take = false;
-    int64_t j = 0, pos = 0, row = 0, out = 0;
-    if (idx < p.requests * p.canvas_len) {
-        j = idx / p.canvas_len;
-        pos = idx - j * p.canvas_len;
-        row = static_cast<int64_t>(p.src[j]) * p.canvas_len + pos;
-        out = static_cast<int64_t>(p.slots[j]) * p.canvas_len + pos;
-        // rows outside the logits or the stash are skipped, never touched
-        take = p.keep[j] != 0 && pos < p.valid[j] && p.src[j] >= 0 && row < p.logits_rows &&
-               p.slots[j] >= 0 && p.slots[j] < p.out_slots;
-    }
-    const uint32_t b = __ballot_sync(0xffffffffu, take);
+    const int warp = threadIdx.x >> 5;
+    const int64_t n = p.requests * p.canvas_len;
     int base = 0;
-    if (lane == 0 && b) base = atomicAdd(p.list, __popc(b));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (take) {
-        uint32_t lt;
-        asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
-        const int e = base + __popc(b & lt);
-        p.list[kListOffset + e] = e;
-        p.map_row[e] = static_cast<int32_t>(row);
-        p.map_temp[e] = p.temps[j];
-        p.map_out[e] = out;
-        p.map_req[e] = static_cast<int32_t>(j);
+    for (int64_t i0 = 0; i0 < n; i0 += kListThreads) {
+        const int64_t idx = i0 + threadIdx.x;
+        bool take = false;
+        int64_t j = 0, pos = 0, row = 0, out = 0;
+        if (idx < n) {
+            j = idx / p.canvas_len;
+            pos = idx - j * p.canvas_len;
+            row = static_cast<int64_t>(p.src[j]) * p.canvas_len + pos;
+            out = static_cast<int64_t>(p.slots[j]) * p.canvas_len + pos;
+            // rows outside the logits or the stash are skipped, never touched
+            take = p.keep[j] != 0 && pos < p.valid[j] && p.src[j] >= 0 && row < p.logits_rows &&
+                   p.slots[j] >= 0 && p.slots[j] < p.out_slots;
+        }
+        const uint32_t b = __ballot_sync(0xffffffffu, take);
+        if (lane == 0) wcount[warp] = __popc(b);
+        __syncthreads();
+        int before = base, total = 0;
+        for (int w = 0; w < kListThreads / 32; ++w) {
+            before += w < warp ? wcount[w] : 0;
+            total += wcount[w];
+        }
+        if (take) {
+            uint32_t lt;
+            asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+            const int e = before + __popc(b & lt);
+            p.list[kListOffset + e] = e;
+            p.map_row[e] = static_cast<int32_t>(row);
+            p.map_temp[e] = p.temps[j];
+            p.map_out[e] = out;
+            p.map_req[e] = static_cast<int32_t>(j);
+        }
+        base += total;
+        __syncthreads();
     }
+    if (threadIdx.x == 0) p.list[0] = base;
 }
 
 constexpr int kWriteWarps = 8;
@@ -255,8 +274,7 @@ extern "C" drs_status drs_stash_converged_logprobs(
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t R = requests * canvas_len;
-    if (cudaMemsetAsync(p.list, 0, 4, st) != cudaSuccess) return DRS_ERR_CUDA;
-    stash_list<<<static_cast<int>((R + 255) / 256), 256, 0, st>>>(p);
+    stash_list<<<1, kListThreads, 0, st>>>(p);  // writes the list's count too
     if (cudaGetLastError() != cudaSuccess) return DRS_ERR_CUDA;
     const ExactTopkMap map{p.map_row, p.map_temp, row_m, row_logs};
     const int32_t* exact_list = p.list;
