@@ -252,9 +252,17 @@ drs_status drs_topk_logprobs(const float *logits, int64_t rows, int64_t vocab,
 
 /*
  * The sampler's noise, materialised (the generator of drs_row_stats).
+ * Page "vllm.model_executor.models.diffusion_gemma_sampler",
+ * sample_row_stats_reference: the Gumbel noise -log(-log u) of a uniform u
+ * drawn like rand_like(...) and clamped below at 1e-20; the page's kernel
+ * takes a seed, and the uniform is drawn here by Philox4x32-10 (Salmon,
+ * Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+ * SC'11) keyed and laid out as the `seed` argument of drs_row_stats states.
  * For r in [0, rows), c in [0, vocab): out_bits[r * vocab + c] is the
  * Philox word of (row0 + r, c) and out_gumbel[r * vocab + c] the fp32
- * -log(-log u) of it. Either output may be NULL; rows == 0 is a no-op.
+ * -log(-log u) of it, u = max((word >> 8) * 2^-24, 1e-20f). Either output
+ * may be NULL; rows == 0 is a no-op. Outputs are caller-owned device
+ * memory; invalid sizes return DRS_ERR_INVALID_ARG before any launch.
  */
 drs_status drs_philox_gumbel(uint64_t seed, int64_t row0, int64_t rows,
                              int64_t vocab, uint32_t *out_bits,
