@@ -56,6 +56,11 @@ constexpr int kCChunkMax = 4 * kCChunkF4;           // 16384 columns per CTA
 constexpr int kCMaxCluster = 16;
 constexpr int kCBufs = 3;                           // rows held per CTA
 constexpr int kCGroups = kCompWarps;                // group maxima per CTA (a warp's 1024 columns)
+// Part slots, by row iteration t % kCPartSlots. Three make reuse safe by
+// causality: a CTA pushes row t + 3 only after all C parts of row t + 1 have
+// reached it, and a CTA pushes its part of row t + 1 only after it has
+// finished reading the parts of row t.
+constexpr int kCPartSlots = 3;
 
 // A CTA's phase-A part of a row (96 bytes), pushed to every CTA of the
 // cluster.
@@ -71,7 +76,11 @@ struct alignas(16) CPart {
     uint32_t gm[kCGroups];  // the CTA's largest group maxima (order keys), descending; 0 past ng
 };
 static_assert(sizeof(CPart) == 96, "CTA part");
-constexpr uint32_t kCPartWords = sizeof(CPart) / 16;
+// 16-byte words of a part that a row pushes: the statistics (32 bytes), and
+// for a top-k row the first top_m group maxima.
+__device__ __forceinline__ uint32_t part_words(bool topk, int top_m) {
+    return 2u + (topk ? static_cast<uint32_t>(top_m + 3) / 4u : 0u);
+}
 
 // The merged row as phase B uses it.
 struct alignas(16) CRow {
@@ -105,14 +114,14 @@ struct ClusterSmem {
     uint64_t adone[2];       // the compute warps' phase A of a row (by row parity)
     uint64_t recrdy[2];      // the merged row is ready for phase B
     uint64_t bdone[2];       // the compute warps' phase B of a row
-    uint64_t part_full[2];   // the C parts of a row landed
+    uint64_t part_full[kCPartSlots];  // the C parts of a row landed
     uint64_t cand_done[2];   // the noise warp scored the CTA's Gumbel candidates
     uint64_t thr_done[2];    // the noise warp set the row's top-k threshold
     int abort;
     int tile_nk[2];          // top-k candidates of the CTA, by row parity
     int issued[kCBufs];      // row iteration last copied into each buffer (-1: none)
     RowSlot ring[kCRing];    // row iteration t at t % kCRing
-    CPart part[2][kCMaxCluster];
+    CPart part[kCPartSlots][kCMaxCluster];
     CPart mine;
     WarpPart wparts[2][kCompWarps];
     WarpRes wres[2][kCompWarps];
@@ -202,8 +211,8 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const
 // The noise warp waits for the same phase of part_full as the merge warp (a
 // phase can be waited on by any number of threads; the merge warp re-arms
 // the barrier only after the noise warp has passed it for this row).
-__device__ __forceinline__ bool try_wait_parts(ClusterSmem& sh, int s, uint32_t par) {
-    return wait_phase<true>(&sh.part_full[s], par, &sh.abort);
+__device__ __forceinline__ bool try_wait_parts(ClusterSmem& sh, int ps, uint32_t ppar) {
+    return wait_phase<true>(&sh.part_full[ps], ppar, &sh.abort);
 }
 
 __device__ __forceinline__ void give_up(ClusterSmem& sh, int* err) {
@@ -394,17 +403,16 @@ __device__ __forceinline__ void make_part(const SplitParams& p, ClusterSmem& sh,
     }
 }
 
-// Push the CTA's part (sh.mine, its candidates filled in) into slot s of
-// every CTA of the cluster.
-__device__ __forceinline__ void push_part(ClusterSmem& sh, int s, uint32_t rank, uint32_t C, int lane) {
+// Push the first nw words of the CTA's part (sh.mine, its candidates filled
+// in) into part slot ps of every CTA of the cluster: lane d < C to CTA d.
+__device__ __forceinline__ void push_part(ClusterSmem& sh, int ps, uint32_t rank, uint32_t C, uint32_t nw, int lane) {
     __syncwarp();
-    const uint4* src = reinterpret_cast<const uint4*>(&sh.mine);
-    const uint32_t dst = smem_u32(&sh.part[s][rank]);
-    const uint32_t bar = smem_u32(&sh.part_full[s]);
-    for (uint32_t idx = lane; idx < kCPartWords * C; idx += 32) {
-        const uint32_t d = idx / kCPartWords;
-        const uint32_t q = idx - d * kCPartWords;
-        push16(map_to_rank(dst + 16u * q, d), src[q], map_to_rank(bar, d));
+    if (static_cast<uint32_t>(lane) < C) {
+        const uint4* src = reinterpret_cast<const uint4*>(&sh.mine);
+        const uint32_t dst = smem_u32(&sh.part[ps][rank]);
+        const uint32_t rbar = map_to_rank(smem_u32(&sh.part_full[ps]), static_cast<uint32_t>(lane));
+        for (uint32_t q = 0; q < nw; ++q)
+            push16(map_to_rank(dst + 16u * q, static_cast<uint32_t>(lane)), src[q], rbar);
     }
 }
 
@@ -412,15 +420,20 @@ __device__ __forceinline__ void push_part(ClusterSmem& sh, int s, uint32_t rank,
 // (lane w < 16: warp w's; its exact quotient is M_w), the best of them.
 __device__ __forceinline__ void score_candidates(const SplitParams& p, ClusterSmem& sh, const RowSlot& ro,
                                                  bool stats, int s, int lane) {
-    const ScaledQuotient sq{ro.qt, ro.qy, ro.qmode};
-    const WarpPart wp = lane < kCompWarps ? sh.wparts[s][lane] : WarpPart{0.0f, 0.0f, 0.0f, -INFINITY, INT_MAX};
-    const bool cand = stats && ro.temp > 0.0f && wp.arg != INT_MAX;
-    const int ccol = cand ? wp.arg : 0;
-    const uint4 nw = noise_group(p.rk[0], static_cast<uint64_t>(p.row0 + ro.row), static_cast<uint32_t>(ccol >> 2));
-    const float g = gumbel_of_bits(word_of(nw, ccol & 3));
-    float bs = cand ? sq.exact(wp.xmax) + g : -INFINITY;
-    int bc = cand ? wp.arg : INT_MAX;
-    warp_best(bs, bc);
+    float bs = -INFINITY;
+    int bc = INT_MAX;
+    if (stats && ro.temp > 0.0f) {  // rows that draw no noise need no B
+        const ScaledQuotient sq{ro.qt, ro.qy, ro.qmode};
+        const WarpPart wp = lane < kCompWarps ? sh.wparts[s][lane] : WarpPart{0.0f, 0.0f, 0.0f, -INFINITY, INT_MAX};
+        const bool cand = wp.arg != INT_MAX;
+        const int ccol = cand ? wp.arg : 0;
+        const uint4 nw =
+            noise_group(p.rk[0], static_cast<uint64_t>(p.row0 + ro.row), static_cast<uint32_t>(ccol >> 2));
+        const float g = gumbel_of_bits(word_of(nw, ccol & 3));
+        bs = cand ? sq.exact(wp.xmax) + g : -INFINITY;
+        bc = cand ? wp.arg : INT_MAX;
+        warp_best(bs, bc);
+    }
     if (lane == 0) {
         sh.cand_s[s] = bs;
         sh.cand_c[s] = bc;
@@ -498,8 +511,8 @@ __device__ __forceinline__ uint32_t kth_largest(const CPart* pr, int C, int top_
 // column). -inf when there is none (absent, or -inf): the exact kernel
 // takes the row.
 __device__ __forceinline__ void row_threshold(const SplitParams& p, ClusterSmem& sh, const RowSlot& ro, int top_m,
-                                              int s, uint32_t C, int lane) {
-    const uint32_t kth = kth_largest(sh.part[s], static_cast<int>(C), top_m, p.k, lane);
+                                              int s, int ps, uint32_t C, int lane) {
+    const uint32_t kth = kth_largest(sh.part[ps], static_cast<int>(C), top_m, p.k, lane);
     float thr = -INFINITY;
     if (kth > kOrdNegInf) {
         const float x = unord32(kth);
@@ -513,9 +526,9 @@ __device__ __forceinline__ void row_threshold(const SplitParams& p, ClusterSmem&
 // kernel, the entropy, the stash's max and log S, and rows without a
 // threshold on the hard list.
 __device__ __forceinline__ bool merge_parts(const SplitParams& p, ClusterSmem& sh, const RowSlot& ro, bool stats,
-                                            int s, int par, uint32_t rank, uint32_t C, int lane) {
+                                            int s, int par, int ps, uint32_t rank, uint32_t C, int lane) {
     const bool topk = ro.kept && p.k > 0;
-    const CPart* pr = sh.part[s];
+    const CPart* pr = sh.part[ps];
     float m = -INFINITY, sp = 0.0f, wq = 0.0f, xm = -INFINITY, bs = -INFINITY;
     int arg = INT_MAX, bc = INT_MAX;
     if (lane < static_cast<int>(C)) {
@@ -853,20 +866,17 @@ __global__ void __launch_bounds__(kCThreads, 1) split_cluster(const __grid_const
             mbar_init(&sh.full[b], 1);
             sh.issued[b] = -1;
         }
+        for (int s = 0; s < kCPartSlots; ++s) mbar_init(&sh.part_full[s], 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sh.adone[s], kCompWarps);
             mbar_init(&sh.bdone[s], kCompWarps);
             mbar_init(&sh.recrdy[s], 1);
-            mbar_init(&sh.part_full[s], 1);
             mbar_init(&sh.cand_done[s], 1);
             mbar_init(&sh.thr_done[s], 1);
             sh.tile_nk[s] = 0;
         }
         sh.abort = 0;
         fence_barrier_init();
-        // rows 0 and 1 of the cluster: C parts of 96 bytes each
-        mbar_arrive_expect_tx(&sh.part_full[0], kCPartWords * 16u * C);
-        mbar_arrive_expect_tx(&sh.part_full[1], kCPartWords * 16u * C);
     }
     __syncthreads();
     cluster_sync_all();  // every CTA's barriers are set before any push
@@ -931,6 +941,12 @@ __global__ void __launch_bounds__(kCThreads, 1) split_cluster(const __grid_const
                 break;
             }
             const RowSlot ro = sh.ring[t % kCRing];
+            const int ps = t % kCPartSlots;
+            const uint32_t ppar = static_cast<uint32_t>((t / kCPartSlots) & 1);
+            const uint32_t nw = part_words(ro.kept && p.k > 0, cs.top_m);
+            // the slot's phase for row t: C parts of nw words (parts that
+            // landed already count against it; the arrival completes it)
+            if (lane == 0) mbar_arrive_expect_tx(&sh.part_full[ps], nw * 16u * C);
             make_part(p, sh, ro, ncols, c0, cs.top_m, s, rank, C, lane);
             if (!__all_sync(0xffffffffu, wait_phase<false>(&sh.cand_done[s], par, &sh.abort))) {
                 if (lane == 0) give_up(sh, p.err);
@@ -940,18 +956,14 @@ __global__ void __launch_bounds__(kCThreads, 1) split_cluster(const __grid_const
                 sh.mine.bs = sh.cand_s[s];
                 sh.mine.bc = sh.cand_c[s];
             }
-            push_part(sh, s, rank, C, lane);
-            if (!__all_sync(0xffffffffu, wait_phase<true>(&sh.part_full[s], par, &sh.abort)) ||
-                !merge_parts(p, sh, ro, stats, s, static_cast<int>(par), rank, C, lane)) {
+            push_part(sh, ps, rank, C, nw, lane);
+            if (!__all_sync(0xffffffffu, wait_phase<true>(&sh.part_full[ps], ppar, &sh.abort)) ||
+                !merge_parts(p, sh, ro, stats, s, static_cast<int>(par), ps, rank, C, lane)) {
                 if (lane == 0) give_up(sh, p.err);
                 break;
             }
             __syncwarp();
-            if (lane == 0) {
-                // the slot takes the parts of row t + 2; row t is ready
-                mbar_arrive_expect_tx(&sh.part_full[s], kCPartWords * 16u * C);
-                mbar_arrive(&sh.recrdy[s]);
-            }
+            if (lane == 0) mbar_arrive(&sh.recrdy[s]);
         }
     } else if (warp == kNoiseWarp) {
         // ================================ the noise warp: each row's Gumbel
@@ -970,11 +982,13 @@ __global__ void __launch_bounds__(kCThreads, 1) split_cluster(const __grid_const
             // (every row takes one phase of thr_done, so that its parity
             // stays that of the row, whether the row wants a threshold or not)
             if (ro.kept && p.k > 0) {
-                if (!__all_sync(0xffffffffu, try_wait_parts(sh, s, par))) {
+                const int ps = t % kCPartSlots;
+                if (!__all_sync(0xffffffffu,
+                                try_wait_parts(sh, ps, static_cast<uint32_t>((t / kCPartSlots) & 1)))) {
                     if (lane == 0) give_up(sh, p.err);
                     break;
                 }
-                row_threshold(p, sh, ro, cs.top_m, s, C, lane);
+                row_threshold(p, sh, ro, cs.top_m, s, ps, C, lane);
                 __syncwarp();
             }
             if (lane == 0) mbar_arrive(&sh.thr_done[s]);
