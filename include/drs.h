@@ -309,15 +309,22 @@ void drs_test_two_pass(int on);
  * cluster (*cluster_size CTAs per row, *clusters clusters resident at once,
  * one CTA per SM); such clusters fit only some of the GPU's SM groups, and on
  * large calls the *free_sms SMs they leave run the two streaming passes over
- * the rows past the first *cluster_rows of the call's row list at the same
- * time. Other calls take the two passes alone: *cluster_rows, *cluster_size,
- * *clusters and *free_sms are then 0. probs_dtype: a drs_probs_dtype value.
+ * the tail of the call's row list at the same time. *cluster_rows is the
+ * head of a list of `rows` entries; a call whose list is shorter (a top-k
+ * call lists the rows of kept slots only) divides it in the same proportion
+ * on the device. Other calls take the two passes alone: *cluster_rows, *cluster_size,
+ * *clusters and *free_sms are then 0. probs_dtype: a drs_probs_dtype value;
+ * stats: nonzero for the calls that compute the row statistics
+ * (drs_row_stats, drs_row_stats_topk), 0 for the top-k calls
+ * (drs_topk_logprobs, the stash). Top-k calls take no cluster kernel: they
+ * read each row once in the first streaming pass and then only the columns
+ * of the row's warps whose max reaches its top-k threshold (all outputs 0).
  * All outputs are HOST pointers. Returns DRS_OK, or DRS_ERR_INVALID_ARG for a
  * null pointer or sizes out of range.
  */
 drs_status drs_row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds,
-                              int probs_dtype, int64_t *cluster_rows, int32_t *cluster_size,
-                              int32_t *clusters, int32_t *free_sms);
+                              int probs_dtype, int32_t stats, int64_t *cluster_rows,
+                              int32_t *cluster_size, int32_t *clusters, int32_t *free_sms);
 
 /*
  * Measurement hook (not part of the sampler). enable != 0: from now on every

@@ -163,3 +163,19 @@ def test_stash_workspace_sizes(lib):
     assert drs.drs_stash_workspace_bytes(8, 256, 262144, 20) >= 8 * 256 * 20 * 8
     assert drs.drs_stash_workspace_bytes(8, 256, 262144, 1025) == 0
     assert drs.drs_stash_workspace_bytes(-1, 256, 262144, 20) == 0
+
+
+def test_split_plan_argument_checks(lib):
+    out = [ctypes.c_int64(7), ctypes.c_int32(7), ctypes.c_int32(7), ctypes.c_int32(7)]
+    refs = [ctypes.byref(o) for o in out]
+    assert lib.drs_row_split_plan(2048, 262144, 20, 1, 1, 1, None, *refs[1:]) == INV
+    assert lib.drs_row_split_plan(-1, 262144, 20, 1, 1, 1, *refs) == INV
+    assert lib.drs_row_split_plan(2048, 0, 20, 1, 1, 1, *refs) == INV
+    assert lib.drs_row_split_plan(2048, 262144, 20, 0, 1, 1, *refs) == INV
+    assert lib.drs_row_split_plan(2048, 262144, 20, 1, 3, 1, *refs) == INV
+    # zero rows: nothing to divide
+    assert lib.drs_row_split_plan(0, 262144, 20, 1, 1, 0, *refs) == OK
+    assert [o.value for o in out] == [0, 0, 0, 0]
+    # several seeds always take the two passes alone
+    assert lib.drs_row_split_plan(2048, 262144, 0, 8, 0, 1, *refs) == OK
+    assert [o.value for o in out] == [0, 0, 0, 0]

@@ -102,7 +102,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.drs_test_inject_fault.restype = None
     lib.drs_test_two_pass.argtypes = [ctypes.c_int]
     lib.drs_test_two_pass.restype = None
-    lib.drs_row_split_plan.argtypes = [i64, i64, i32, i32, ctypes.c_int, vp, vp, vp, vp]
+    lib.drs_row_split_plan.argtypes = [i64, i64, i32, i32, ctypes.c_int, i32, vp, vp, vp, vp]
     lib.drs_row_split_plan.restype = ctypes.c_int
     lib.drs_get_device_error.argtypes = [vp]
     lib.drs_get_device_error.restype = ctypes.c_int
@@ -305,14 +305,15 @@ def drs_test_two_pass(on: bool) -> None:
     load().drs_test_two_pass(1 if on else 0)
 
 
-def cluster_rows(rows: int, vocab: int, k: int, n_seeds: int = 1, probs_dtype: int = DRS_PROBS_BF16):
+def cluster_rows(rows: int, vocab: int, k: int, n_seeds: int = 1, probs_dtype: int = DRS_PROBS_BF16,
+                 stats: bool = True):
     """How a row-statistics call of these sizes shares its rows on the
     current device (drs_row_split_plan): None when it takes the two passes
     alone, else a dict with the rows of the cluster kernel ("head"), of the
     two passes beside it ("tail"), the cluster size, the clusters resident
     at once and the SMs they leave free."""
     head, size, ncl, free = ctypes.c_int64(0), ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
-    _check(load().drs_row_split_plan(rows, vocab, k, n_seeds, probs_dtype,
+    _check(load().drs_row_split_plan(rows, vocab, k, n_seeds, probs_dtype, 1 if stats else 0,
                                      ctypes.byref(head), ctypes.byref(size), ctypes.byref(ncl),
                                      ctypes.byref(free)), "drs_row_split_plan")
     if size.value == 0:

@@ -124,6 +124,7 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream);
 // *free_sms SMs the clusters leave. False when the call takes the two passes
 // alone.
 bool split_plan_query(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16, int probs_dtype,
+                      bool stats,
                       int64_t* head, int32_t* cluster_size, int32_t* clusters, int32_t* free_sms);
 
 }  // namespace drs

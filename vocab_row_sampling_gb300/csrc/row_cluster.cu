@@ -834,7 +834,7 @@ __device__ __forceinline__ WarpRes phase_b(const SplitParams& p, ClusterSmem& sh
 // ------------------------------------------------------ the kernel
 
 // Grid: clusters of C CTAs (C = the cluster size of the launch), one CTA per
-// SM; cluster q takes list entries li_begin + q, + nclusters, ... Every CTA
+// SM; cluster q takes list entries list_begin + q, + nclusters, ... Every CTA
 // owns columns [rank * chunk_cols, min(V, (rank + 1) * chunk_cols)) of each
 // of its rows.
 template <int PD>
@@ -854,7 +854,7 @@ __global__ void __launch_bounds__(kCThreads, 1) split_cluster(const __grid_const
     const int ncols = min(max(p.vocab - c0, 0), cs.chunk_cols);
     const bool stats = p.stats != 0;
     const int lend = list_end(p);
-    const int li0 = p.li_begin + static_cast<int>(cluster_index());
+    const int li0 = list_begin(p) + static_cast<int>(cluster_index());
     const int T = li0 < lend ? (lend - li0 + ncl - 1) / ncl : 0;  // rows of this cluster
 
     // the buffers past this CTA's columns read as -inf (never copied into)

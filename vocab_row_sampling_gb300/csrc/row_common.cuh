@@ -161,8 +161,12 @@ struct SplitParams {
     const int32_t* map_count;
     float* out_m;
     float* out_logs;
-    int li_begin;     // the list entries of this launch: [li_begin, li_end),
-    int li_end;       // li_end < 0: to the end of the list
+    // The list entries of this launch: the whole list (li_part 0), or with
+    // the list of n entries divided at h = floor(n * li_num / li_den) (n is
+    // known on the device only), its head [0, h) (1) or its tail [h, n) (2).
+    int li_part;
+    int li_num;
+    int li_den;
     int* err;
     PhiloxRoundKeys rk[kMaxSeeds];
     int n_seeds;
@@ -328,10 +332,16 @@ __device__ __forceinline__ uint4 noise_folded(const PhiloxRoundKeys& rk, const R
     return make_uint4(c0, c1, c2, c3);
 }
 
-// The list entries of this launch: [li_begin, list_end).
+// The list entries of this launch: [list_begin, list_end).
+__device__ __forceinline__ int list_split(const SplitParams& p, int n) {
+    return static_cast<int>(static_cast<int64_t>(n) * p.li_num / p.li_den);
+}
+__device__ __forceinline__ int list_begin(const SplitParams& p) {
+    return p.li_part == 2 ? list_split(p, p.hard[kCount1]) : 0;
+}
 __device__ __forceinline__ int list_end(const SplitParams& p) {
     const int n = p.hard[kCount1];
-    return p.li_end < 0 || p.li_end > n ? n : p.li_end;
+    return p.li_part == 1 ? list_split(p, n) : n;
 }
 
 // A warp's part of a tile's statistics: the raw max and its lowest column,
@@ -438,15 +448,16 @@ struct RowSplitPlan {
     int cluster_size;
     int clusters;
     int free_sms;
-    int64_t tail;
+    int head_num, head_den;  // the head's share of the row list
+    int64_t tail;            // the tail of a list of `rows` entries
 };
 bool row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16, int probs_dtype,
-                    RowSplitPlan* out);
+                    bool stats, RowSplitPlan* out);
 
 // Clusters of the cluster kernel resident at once on the current device
 // (0 on failure).
 int cluster_active(int probs_dtype, int cluster_size);
-// Launch the cluster kernel on the list entries [li_begin, li_end) (after
+// Launch the cluster kernel on the list entries of p (after
 // split_prep, before split_finish; the CTA of rank r writes tile r of its
 // row's tiles_per_row records, tile r + cluster_size empty when it exists).
 drs_status cluster_launch(const SplitParams& p, const ClusterShape& cs, int cluster_size, int64_t rows,

@@ -140,7 +140,7 @@ __device__ __forceinline__ void issue_tile(const SplitParams& p, Pipe& pp, int n
 
 // The tiles of this launch: the list entries' tiles.
 __device__ __forceinline__ TileRange launch_tiles(const SplitParams& p, int G) {
-    return TileRange{static_cast<int64_t>(p.li_begin) * G, static_cast<int64_t>(list_end(p)) * G};
+    return TileRange{static_cast<int64_t>(list_begin(p)) * G, static_cast<int64_t>(list_end(p)) * G};
 }
 
 // Pipeline start: barriers, the first kMap tiles mapped, the first kStages
@@ -710,12 +710,12 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_merge(const __grid_const
     static_assert(W == 1 || W == kRowWarps, "a merge CTA holds kRowWarps rows or one row");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if constexpr (W == 1) {
-        const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+        const int64_t li = list_begin(p) + static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
         if (li >= list_end(p)) return;
         merge_row<NU, 1>(p, li, threadIdx.x & 31, nullptr);
     } else {
         __shared__ MergeShared<W> sh;
-        const int64_t li = p.li_begin + static_cast<int64_t>(blockIdx.x);
+        const int64_t li = list_begin(p) + static_cast<int64_t>(blockIdx.x);
         if (li >= list_end(p)) return;  // the whole CTA
         merge_row<NU, W>(p, li, threadIdx.x, &sh);
     }
@@ -1230,6 +1230,103 @@ __global__ void __launch_bounds__(kRowWarps * 32) split_finish(const __grid_cons
     }
 }
 
+// ============================================================== gather
+
+// Top-k calls read each row once. Pass 1 records every warp's raw max; the
+// merge takes the row's threshold from them (the k-th largest, lowered by
+// Te ulp). A logit at or above the threshold lies in a warp whose max
+// reaches it, so this kernel reads back only those warps' columns (the
+// "hot" warps: about k of a row's 344 on the step recipe, a few percent of
+// its bytes), keys the logits at or above the threshold by (exact value,
+// lower column), ranks them by counting and writes the row's top k. A row
+// with more hot warps or candidates than fit goes on the hard-row list.
+constexpr int kHotCap = 256;  // hot warps a row may have
+
+__global__ void __launch_bounds__(256) split_gather(const __grid_constant__ SplitParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ uint16_t hot[kHotCap];
+    __shared__ uint64_t keys[kRowKeys];
+    __shared__ int nhot, nkeys;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int64_t li = blockIdx.x;
+    if (li >= p.hard[kCount1]) return;
+    const int64_t row = p.list1[li];
+    const RowRecord rec = *reinterpret_cast<const RowRecord*>(p.rr + row * p.rec_bytes);
+    if (!(rec.flags & kFTopk)) return;  // no threshold: the exact kernel takes the row
+    const float thr = rec.thr;
+    const uint32_t thr_key = ord32(thr);
+    const int G1 = p.tiles1;
+    const TileStats* tr = p.ts + li * G1;
+    if (tid == 0) {
+        nhot = 0;
+        nkeys = 0;
+    }
+    __syncthreads();
+    for (int j = tid; j < G1 * kSWarps; j += 256) {
+        const uint32_t wm = tr[j / kSWarps].wmax[j % kSWarps];  // 0: a warp without columns
+        if (wm != 0u && wm >= thr_key) {
+            const int at = atomicAdd(&nhot, 1);
+            if (at < kHotCap) hot[at] = static_cast<uint16_t>(j);
+        }
+    }
+    __syncthreads();
+    const int nh = nhot;
+    if (nh <= kHotCap) {
+        const int64_t lrow = p.map_row ? p.map_row[row] : row;
+        const float* xr = p.logits + lrow * p.row_stride;
+        const ScaledQuotient sq{rec.qt, rec.qy, rec.qmode};
+        for (int h = warp; h < nh; h += kSWarps) {
+            const int j = hot[h];
+            const int w = j % kSWarps;
+            const int col0 = (j / kSWarps) * kP1Cols;
+#pragma unroll
+            for (int i = 0; i < kP1Vec4; ++i) {
+                // slot i of the warp's lane: float4 i * kSThreads + 32 w + lane of the tile
+                const int c = col0 + 4 * (i * kSThreads + 32 * w + lane);
+                if (c >= p.vocab) continue;
+                float4 x4;
+                if (p.vec && c + 4 <= p.vocab) {
+                    x4 = __ldcs(reinterpret_cast<const float4*>(xr + c));
+                } else {
+                    x4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                    for (int q = 0; q < 4 && c + q < p.vocab; ++q) set_comp(x4, q, __ldcs(xr + c + q));
+                }
+                if (max4f(x4) >= thr) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float x = comp(x4, q);
+                        if (x >= thr) {
+                            const int at = atomicAdd(&nkeys, 1);
+                            if (at < kRowKeys) keys[at] = topk_key(sq.exact(x), c + q);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int n = nkeys;
+    if (nh > kHotCap || n > kRowKeys || n < p.k) {
+        if (tid == 0) {
+            const int idx = atomicAdd(p.hard, 1);
+            p.hard[kHardOffset + idx] = static_cast<int32_t>(row);
+        }
+        return;
+    }
+    const int K = p.k;
+    for (int a = tid; a < n; a += 256) {
+        const uint64_t key = keys[a];
+        int rank = 0;
+        for (int o = 0; o < n; ++o) rank += keys[o] > key;
+        if (rank < K) {
+            p.out_ids[row * K + rank] = key_col(key);
+            p.out_lp[row * K + rank] = rec.M == -INFINITY ? NAN : (key_value(key) - rec.M) - rec.lns;
+        }
+    }
+}
+
 // ================================================================ host
 
 size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
@@ -1287,26 +1384,33 @@ int32_t split_max_seeds() { return kMaxSeeds; }
 int32_t split_max_k() { return kSplitMaxK; }
 
 bool rs::row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16,
-                        int probs_dtype, RowSplitPlan* out) {
+                        int probs_dtype, bool stats, RowSplitPlan* out) {
     RowSplitPlan pl{};
+    if (!stats) return false;  // top-k calls: pass 1 and the gather (one read)
     if (!cluster_plan(rows, vocab, k, n_seeds, aligned16, &pl.shape, &pl.cluster_size)) return false;
     pl.clusters = cluster_active(probs_dtype, pl.cluster_size);
     if (pl.clusters < 1) return false;
     pl.free_sms = sm_count() - pl.clusters * pl.cluster_size;
     // rows per SM and time: the two passes about 4/5 of the cluster
     // kernel's (measured on the step workload), so the tail gets that share
-    // of the free SMs' weight
+    // of the free SMs' weight; the head is the rest of the list, whatever
+    // its length on the device
+    pl.head_num = 1;
+    pl.head_den = 1;
     pl.tail = 0;
-    if (pl.free_sms >= 8 && rows >= 8 * static_cast<int64_t>(pl.clusters))
-        pl.tail = rows * (4 * pl.free_sms) / (4 * pl.free_sms + 5 * pl.clusters * pl.cluster_size);
+    if (pl.free_sms >= 8 && rows >= 8 * static_cast<int64_t>(pl.clusters)) {
+        pl.head_num = 5 * pl.clusters * pl.cluster_size;
+        pl.head_den = 4 * pl.free_sms + pl.head_num;
+        pl.tail = rows - rows * pl.head_num / pl.head_den;
+    }
     *out = pl;
     return true;
 }
 
 bool split_plan_query(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds, bool aligned16, int probs_dtype,
-                      int64_t* head, int32_t* cluster_size, int32_t* clusters, int32_t* free_sms) {
+                      bool stats, int64_t* head, int32_t* cluster_size, int32_t* clusters, int32_t* free_sms) {
     RowSplitPlan pl{};
-    if (two_pass_forced() || !rs::row_split_plan(rows, vocab, k, n_seeds, aligned16, probs_dtype, &pl))
+    if (two_pass_forced() || !rs::row_split_plan(rows, vocab, k, n_seeds, aligned16, probs_dtype, stats, &pl))
         return false;
     *head = rows - pl.tail;
     *cluster_size = pl.cluster_size;
@@ -1370,8 +1474,9 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
                 (c.canvas_len <= static_cast<int64_t>(UINT32_MAX));
     p.stats = c.stats ? 1 : 0;
     p.k = c.k;
-    p.li_begin = 0;
-    p.li_end = -1;
+    p.li_part = 0;
+    p.li_num = 1;
+    p.li_den = 1;
     p.fault = take_injected_fault();
     // the header of the hard-row list: its count and the two list lengths
     if (cudaMemsetAsync(ws + l.hard, 0, 16, stream) != cudaSuccess) return DRS_ERR_CUDA;
@@ -1418,8 +1523,23 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     // tail of the row list at the same time, on a second stream (the two
     // parts fill one workspace, one finish kernel reduces both). Else the two
     // passes alone.
+    if (!c.stats && c.k > 0) {
+        // top-k calls read each row once: pass 1, the merge's threshold,
+        // then only the columns of the warps whose max reaches it (the
+        // finish's event slot times the gather)
+        const bool short_m = G1 * kSWarps <= 32 * kOrdSmall;
+        if (!pdl(split_pass1, g1, kSThreads, smem1) || !mark(2)) return DRS_ERR_CUDA;
+        const bool ok = short_m ? pdl(split_merge<kOrdSmall, 1>, static_cast<int>(gr), kRowWarps * 32, 0)
+                                : pdl(split_merge<kOrdWide, kWideMergeWarps>, static_cast<int>(c.rows),
+                                      kRowWarps * 32, 0);
+        if (!ok || !mark(3) || !mark(4) || !mark(5)) return DRS_ERR_CUDA;
+        if (c.rows > INT_MAX || !pdl(split_gather, static_cast<int>(c.rows), 256, 0) || !mark(6))
+            return DRS_ERR_CUDA;
+        return DRS_OK;
+    }
     RowSplitPlan plan{};
-    if (!two_pass_forced() && rs::row_split_plan(c.rows, c.vocab, c.k, n_seeds, p.vec != 0, p.probs_dtype, &plan)) {
+    if (!two_pass_forced() &&
+        rs::row_split_plan(c.rows, c.vocab, c.k, n_seeds, p.vec != 0, p.probs_dtype, c.stats, &plan)) {
         const ClusterShape cshape = plan.shape;
         const int csize = plan.cluster_size;
         const int free_sms = plan.free_sms;
@@ -1431,13 +1551,14 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
         p.tiles_per_row = G;
         if (!mark(2) || !mark(3) || !mark(4)) return DRS_ERR_CUDA;
         if (tail > 0) {
-            // the two passes over list entries [head, end) beside the cluster
+            // the two passes over the tail of the list beside the cluster
             // kernel, their persistent grids sized for the free SMs
             if (cudaEventRecord(fork, stream) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
                 return DRS_ERR_CUDA;
             SplitParams q = p;
-            q.li_begin = static_cast<int>(head);
-            q.li_end = -1;
+            q.li_part = 2;
+            q.li_num = plan.head_num;
+            q.li_den = plan.head_den;
             q.tiles_per_row = G;
             auto pdl_side = [&](auto kernel, int grid, int block, size_t dsmem) {
                 cudaLaunchConfig_t cfg = {};
@@ -1464,8 +1585,11 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
                 return DRS_ERR_CUDA;
         }
         SplitParams pc = p;
-        pc.li_begin = 0;
-        pc.li_end = static_cast<int>(head);
+        if (tail > 0) {
+            pc.li_part = 1;
+            pc.li_num = plan.head_num;
+            pc.li_den = plan.head_den;
+        }
         if (cluster_launch(pc, cshape, csize, head, stream) != DRS_OK || !mark(5)) return DRS_ERR_CUDA;
         if (tail > 0 && cudaStreamWaitEvent(stream, join, 0) != cudaSuccess) return DRS_ERR_CUDA;
         auto finish = G <= 32 * kTilesSmall ? split_finish<kTilesSmall> : split_finish<kTilesLarge>;

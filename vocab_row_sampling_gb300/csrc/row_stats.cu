@@ -79,7 +79,8 @@ bool drs::two_pass_forced() { return drs::g_two_pass.load() != 0; }
 extern "C" void drs_test_two_pass(int on) { drs::g_two_pass.store(on ? 1 : 0); }
 
 extern "C" drs_status drs_row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds,
-                                         int probs_dtype, int64_t* cluster_rows, int32_t* cluster_size,
+                                         int probs_dtype, int32_t stats, int64_t* cluster_rows,
+                                         int32_t* cluster_size,
                                          int32_t* clusters, int32_t* free_sms) {
     if (!cluster_rows || !cluster_size || !clusters || !free_sms) return DRS_ERR_INVALID_ARG;
     if (rows < 0 || vocab < 1 || n_seeds < 1 || probs_dtype < 0 || probs_dtype > 2) return DRS_ERR_INVALID_ARG;
@@ -88,8 +89,8 @@ extern "C" drs_status drs_row_split_plan(int64_t rows, int64_t vocab, int32_t k,
     *clusters = 0;
     *free_sms = 0;
     if (rows == 0) return DRS_OK;
-    drs::split_plan_query(rows, vocab, k, n_seeds, true, probs_dtype, cluster_rows, cluster_size, clusters,
-                          free_sms);
+    drs::split_plan_query(rows, vocab, k, n_seeds, true, probs_dtype, stats != 0, cluster_rows, cluster_size,
+                          clusters, free_sms);
     return DRS_OK;
 }
 
