@@ -332,7 +332,8 @@ drs_status drs_row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_
  * top-k variants, drs_topk_logprobs for k <= 64) records a CUDA event on
  * its stream before each of six kernel slots (list of rows, pass 1, merge,
  * pass 2, cluster, finish) and after the last; the slots a call does not
- * launch (the two passes or the cluster kernel) measure about 0. The count
+ * launch (the two passes or the cluster kernel) measure about 0, and a
+ * top-k call's finish slot times its gather (split_gather). The count
  * of recorded calls restarts at 0. enable == 0 stops recording. The events
  * of the last 64 calls are kept. Returns DRS_OK or DRS_ERR_CUDA (event
  * creation failed).
