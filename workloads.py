@@ -18,7 +18,8 @@ the sampler runs on; "wide" exercises rows longer than the configurations'):
                k = 20, even slots kept.
   large        32 x 256 = 8192 rows, V = 262144, peaked rows: background
                N(0, 1) plus 64 random columns per row drawn from N(mu, 1),
-               mu ~ U[4, 12] (one mean per component), temps ~ U[0.1, 2.0]
+               mu ~ U[4, 12] (one mean per component; a column drawn twice
+               keeps the larger value), temps ~ U[0.1, 2.0]
                with 8 of the 32 slots exactly 0, fp16 probs, k = 20, all kept.
   strided      2048 rows (8 x 256) of V = 262144 inside a buffer with row
                stride 262208 whose pad columns hold NaN, x ~ N(0, 3^2),
@@ -134,7 +135,9 @@ def make_logits(name: str, device="cpu", data_seed: int = 0, rows: int | None = 
         mu = 4.0 + 8.0 * torch.rand(64, generator=g, device=device)
         cols = torch.randint(0, V, (R, 64), generator=g, device=device)
         vals = mu[None, :] + torch.randn(R, 64, generator=g, device=device)
-        buf.scatter_(1, cols, vals)
+        # columns drawn twice for a row keep the larger value (an order-free
+        # rule, so the batch is the same bytes on every run)
+        buf.scatter_reduce_(1, cols, vals, reduce="amax", include_self=False)
     elif name == "adversarial":
         buf = 3.0 * torch.randn(R, V, generator=g, device=device)
         masked = torch.rand(R, V, generator=g, device=device) < 0.3
