@@ -289,29 +289,47 @@ __device__ __forceinline__ void sums2(const float4 (&v)[kCSlots], float ls, floa
 }
 
 // The rare cases of phase A, out of line: a warp whose largest scaled value
-// may reach 256 (exact quotients first, t = (s - M_w) log2(e)), and a warp
-// holding -inf logits (the sums again with t clamped: 0 * -inf is NaN).
+// may reach 256 (exact quotients, t = (s - M_w) log2(e); logits whose
+// exponential is 0 anyway are not divided, and a slot none of the warp's
+// lanes needs is skipped), and a raw warp holding -inf logits (t clamped:
+// 0 * -inf is NaN). Slot by slot, with the accumulation order of sums2.
 __device__ __noinline__ void phase_a_rare(const float4* chunk, int ct, const ScaledQuotient& sq, float mxw,
                                           bool raw, float& sw, float& ww) {
-    float4 v[kCSlots];
-#pragma unroll
-    for (int i = 0; i < kCSlots; ++i) v[i] = chunk[i * kCompThreads + ct];
-    float lscale = kLog2e * sq.y, cref = mxw * lscale;
-    if (!raw) {
-        const float mw = sq.exact(mxw);
-#pragma unroll
-        for (int i = 0; i < kCSlots; ++i) {
-            v[i].x = sq.exact(v[i].x) - mw;
-            v[i].y = sq.exact(v[i].y) - mw;
-            v[i].z = sq.exact(v[i].z) - mw;
-            v[i].w = sq.exact(v[i].w) - mw;
+    const float yl = kLog2e * sq.y;
+    const float mw = raw ? 0.0f : sq.exact(mxw);
+    const FarBelow far(mxw, yl);
+    const float2 l2 = raw ? make_float2(yl, yl) : make_float2(kLog2e, kLog2e);
+    const float2 n2 = raw ? make_float2(-mxw * yl, -mxw * yl) : make_float2(-0.0f, -0.0f);
+    float2 sa = make_float2(0.0f, 0.0f), sb = sa, wa = sa, wb = sa;
+#pragma unroll 2
+    for (int i = 0; i < kCSlots; ++i) {
+        float4 v = chunk[i * kCompThreads + ct];
+        if (!raw) {
+            const bool f0 = far(v.x), f1 = far(v.y), f2 = far(v.z), f3 = far(v.w);
+            if (__any_sync(0xffffffffu, !(f0 && f1 && f2 && f3))) {
+                v.x = f0 ? kFarStandIn : sq.exact(v.x) - mw;
+                v.y = f1 ? kFarStandIn : sq.exact(v.y) - mw;
+                v.z = f2 ? kFarStandIn : sq.exact(v.z) - mw;
+                v.w = f3 ? kFarStandIn : sq.exact(v.w) - mw;
+            } else {
+                v = make_float4(kFarStandIn, kFarStandIn, kFarStandIn, kFarStandIn);
+            }
         }
-        lscale = kLog2e;
-        cref = 0.0f;
-        sums2<false>(v, lscale, cref, sw, ww);
-        if (!isnan(ww)) return;
+        float2 t01 = __ffma2_rn(make_float2(v.x, v.y), l2, n2);
+        float2 t23 = __ffma2_rn(make_float2(v.z, v.w), l2, n2);
+        if (raw) {
+            t01 = make_float2(fmaxf(t01.x, -FLT_MAX), fmaxf(t01.y, -FLT_MAX));
+            t23 = make_float2(fmaxf(t23.x, -FLT_MAX), fmaxf(t23.y, -FLT_MAX));
+        }
+        const float2 e01 = make_float2(ex2_ftz(t01.x), ex2_ftz(t01.y));
+        const float2 e23 = make_float2(ex2_ftz(t23.x), ex2_ftz(t23.y));
+        sa = __fadd2_rn(sa, e01);
+        sb = __fadd2_rn(sb, e23);
+        wa = __ffma2_rn(e01, t01, wa);
+        wb = __ffma2_rn(e23, t23, wb);
     }
-    sums2<true>(v, lscale, cref, sw, ww);
+    sw = warp_sum_f((sa.x + sa.y) + (sb.x + sb.y));
+    ww = warp_sum_f((wa.x + wa.y) + (wb.x + wb.y)) * kLn2;
 }
 
 // One compute warp's share of a chunk: the raw max M_w of its 1024 columns
@@ -634,6 +652,7 @@ __device__ __forceinline__ void probs_full(const float4 (&v)[kCSlots], const CRo
     const float cp = r.c2 - lift;
     const float2 n2 = make_float2(-cp, -cp);
     const float2 d2 = make_float2(BF16 ? 0x1p-64f : 1.0f, BF16 ? 0x1p-64f : 1.0f);
+    const FarBelow far(r.cthr, r.ls);  // exact rows only
 #pragma unroll
     for (int i = 0; i < kCSlots; ++i) {
         const int f = i * kCompThreads + ct;
@@ -642,9 +661,19 @@ __device__ __forceinline__ void probs_full(const float4 (&v)[kCSlots], const CRo
             t01 = __ffma2_rn(make_float2(v[i].x, v[i].y), l2, n2);
             t23 = __ffma2_rn(make_float2(v[i].z, v[i].w), l2, n2);
         } else {
+            // (cthr is at most the row's raw max: a lower reference only
+            // makes the far test more cautious)
             const float o = lift - r.log2s;
-            t01 = make_float2(fmaf(sq.exact(v[i].x) - r.M, kLog2e, o), fmaf(sq.exact(v[i].y) - r.M, kLog2e, o));
-            t23 = make_float2(fmaf(sq.exact(v[i].z) - r.M, kLog2e, o), fmaf(sq.exact(v[i].w) - r.M, kLog2e, o));
+            const bool f0 = far(v[i].x), f1 = far(v[i].y), f2 = far(v[i].z), f3 = far(v[i].w);
+            if (__any_sync(0xffffffffu, !(f0 && f1 && f2 && f3))) {
+                t01 = make_float2(f0 ? kFarStandIn : fmaf(sq.exact(v[i].x) - r.M, kLog2e, o),
+                                  f1 ? kFarStandIn : fmaf(sq.exact(v[i].y) - r.M, kLog2e, o));
+                t23 = make_float2(f2 ? kFarStandIn : fmaf(sq.exact(v[i].z) - r.M, kLog2e, o),
+                                  f3 ? kFarStandIn : fmaf(sq.exact(v[i].w) - r.M, kLog2e, o));
+            } else {
+                t01 = make_float2(kFarStandIn, kFarStandIn);
+                t23 = t01;
+            }
         }
         float2 e01 = make_float2(ex2_ftz(t01.x), ex2_ftz(t01.y));
         float2 e23 = make_float2(ex2_ftz(t23.x), ex2_ftz(t23.y));
@@ -670,7 +699,9 @@ __device__ __forceinline__ void probs_ragged(const float4 (&v)[kCSlots], const C
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float x = comp(v[i], q);
-            const float tq = RAW ? fmaf(x, r.ls, -r.c2) : fmaf(sq.exact(x) - r.M, kLog2e, -r.log2s);
+            const float tq = RAW                         ? fmaf(x, r.ls, -r.c2)
+                             : FarBelow(r.cthr, r.ls)(x) ? kFarStandIn
+                                                         : fmaf(sq.exact(x) - r.M, kLog2e, -r.log2s);
             pr[q] = ex2_approx(tq);
         }
         const uint32_t lo = pack2<BF16>(pr[0], pr[1]);

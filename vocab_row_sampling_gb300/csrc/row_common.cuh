@@ -332,6 +332,28 @@ __device__ __forceinline__ uint4 noise_folded(const PhiloxRoundKeys& rk, const R
     return make_uint4(c0, c1, c2, c3);
 }
 
+// Rows whose scaled values are too large for the raw domain take exact
+// quotients s = x / Te, with exponentials 2^((s - m) log2 e) against a
+// reference m = the exact quotient of a raw max xm. A logit far enough
+// below xm gives an exponential that is exactly 0 after flushing (for
+// bf16 probabilities too, whose exponent is lifted by 64), however the
+// quotients round, so its quotient need not be taken. The test is raw:
+// t = x yl - xm yl by one fused multiply-add, yl = RN(log2(e) RN(1/Te)),
+// against a limit that covers the roundings of 1/Te, of both quotients, of
+// their difference and of t itself (each within 2^-21 of |x yl| + |xm yl|):
+// t < -257 - 2^-19 |xm yl| implies (s - m) log2(e) < -256. A -inf logit
+// passes it (t = -inf). Used only for reading: a logit that passes is
+// given a large finite stand-in, never -inf, so that e t stays 0.
+struct FarBelow {
+    float yl, c, lim;
+    __device__ __forceinline__ FarBelow(float xm, float yl_) : yl(yl_) {
+        c = xm * yl_;
+        lim = -257.0f - fabsf(c) * 0x1p-19f;
+    }
+    __device__ __forceinline__ bool operator()(float x) const { return fmaf(x, yl, -c) < lim; }
+};
+constexpr float kFarStandIn = -1e30f;  // exponent far below any exponential's range
+
 // The list entries of this launch: [list_begin, list_end).
 __device__ __forceinline__ int list_split(const SplitParams& p, int n) {
     return static_cast<int>(static_cast<int64_t>(n) * p.li_num / p.li_den);

@@ -365,13 +365,21 @@ __device__ __forceinline__ WarpPart p1_warp(const SplitParams& p, float4* stage,
         lscale = kLog2e * sq.y;
         cref = mxw * lscale;
     } else {
+        // (logits whose exponential is 0 anyway are not divided; a slot
+        // none of the warp's lanes needs is skipped)
         const float mw = sq.exact(mxw);
+        const FarBelow far(mxw, kLog2e * sq.y);
 #pragma unroll
         for (int i = 0; i < kP1Vec4; ++i) {
-            v[i].x = sq.exact(v[i].x) - mw;
-            v[i].y = sq.exact(v[i].y) - mw;
-            v[i].z = sq.exact(v[i].z) - mw;
-            v[i].w = sq.exact(v[i].w) - mw;
+            const bool f0 = far(v[i].x), f1 = far(v[i].y), f2 = far(v[i].z), f3 = far(v[i].w);
+            if (__any_sync(0xffffffffu, !(f0 && f1 && f2 && f3))) {
+                v[i].x = f0 ? kFarStandIn : sq.exact(v[i].x) - mw;
+                v[i].y = f1 ? kFarStandIn : sq.exact(v[i].y) - mw;
+                v[i].z = f2 ? kFarStandIn : sq.exact(v[i].z) - mw;
+                v[i].w = f3 ? kFarStandIn : sq.exact(v[i].w) - mw;
+            } else {
+                v[i] = make_float4(kFarStandIn, kFarStandIn, kFarStandIn, kFarStandIn);
+            }
         }
         lscale = kLog2e;
         cref = 0.0f;
@@ -731,14 +739,20 @@ template <bool BF16, bool RAW, bool FTZ>
 __device__ __forceinline__ void store_tile_probs(const float4 (&v)[kSVec4], const RowRecord& rec,
                                                  const ScaledQuotient& sq, uint16_t* prow, int tid) {
     const float ls = rec.ls, c2 = rec.c2, big_m = rec.M, l2s = rec.log2s;
+    const FarBelow far(rec.cthr, ls);  // exact rows: cthr is at most the raw max
 #pragma unroll
     for (int i = 0; i < kSVec4; ++i) {
         const int f = i * kSThreads + tid;
         float pr[4];
+        // exact rows: a slot none of the warp's lanes needs is not divided
+        const bool skip = !RAW && !__any_sync(0xffffffffu, !(far(v[i].x) && far(v[i].y) && far(v[i].z) &&
+                                                             far(v[i].w)));
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float x = comp(v[i], q);
-            const float tq = RAW ? fmaf(x, ls, -c2) : fmaf(sq.exact(x) - big_m, kLog2e, -l2s);
+            const float tq = RAW              ? fmaf(x, ls, -c2)
+                             : skip || far(x) ? kFarStandIn
+                                              : fmaf(sq.exact(x) - big_m, kLog2e, -l2s);
             pr[q] = FTZ ? ex2_ftz(tq) : ex2_approx(tq);
         }
         __stcs(reinterpret_cast<uint2*>(prow + 4 * f),
@@ -781,7 +795,9 @@ __device__ __forceinline__ void write_probs(const float4 (&v)[kSVec4], const Row
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float x = comp(v[i], q);
-            const float tq = RAW ? fmaf(x, ls, -c2) : fmaf(sq.exact(x) - big_m, kLog2e, -l2s);
+            const float tq = RAW                              ? fmaf(x, ls, -c2)
+                             : FarBelow(rec.cthr, ls)(x) ? kFarStandIn
+                                                              : fmaf(sq.exact(x) - big_m, kLog2e, -l2s);
             pr[q] = ex2_approx(tq);
         }
         const uint32_t lo = pack2<BF16>(pr[0], pr[1]);
