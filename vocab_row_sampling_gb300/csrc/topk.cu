@@ -130,6 +130,33 @@ __device__ __forceinline__ int block_sum_int(int v, int* red) {
     return r;
 }
 
+__device__ __forceinline__ uint32_t block_min_u32(uint32_t v, int* red) {
+    asm("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(v) : "r"(v));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = static_cast<int>(v);
+    __syncthreads();
+    uint32_t r = (threadIdx.x & 31) < kWarps ? static_cast<uint32_t>(red[threadIdx.x & 31]) : 0xFFFFFFFFu;
+    asm("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(r));
+    __syncthreads();
+    return r;
+}
+
+// The sum of v over the threads before this one (thread order), every thread.
+__device__ __forceinline__ int block_excl_scan(int v, int* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += red[w];
+    __syncthreads();
+    return before + incl - v;
+}
+
 }  // namespace
 
 template <int VEC4>
@@ -308,37 +335,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ncand = sc.ncand;
 
         if (ncand > kFastCands) {
-            // Exact k-th largest 64-bit key over the CTA's valid elements:
-            // bitwise search on the order-preserving unsigned form.
-            uint64_t kth = 0;
+            // Tied values make the candidates too many. Exactly the CTA's
+            // top `want` keys instead: t2, the want-th largest value (key32),
+            // then all elements above it and the lowest columns among those
+            // equal to it (keys order equal values by lower column).
+            auto u32 = [&](float x) { return static_cast<uint32_t>(key32_of(x)) ^ 0x80000000u; };
             const int want = min(K, block_sum_int(nvalid, sc.wcnt));
-            for (int b = 63; b >= 0; --b) {
-                const uint64_t c = kth | (1ull << b);
-                int cnt = 0;
-#pragma unroll
-                for (int i = 0; i < VEC4; ++i)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (valid(i, q)) {
-                            const uint64_t u = static_cast<uint64_t>(make_key(comp(v[i], q), col_of(i, q))) ^
-                                               0x8000000000000000ull;
-                            cnt += u >= c;
-                        }
-                if (block_sum_int(cnt, sc.wcnt) >= want) kth = c;
-            }
-            if (tid == 0) sc.ncand = 0;
-            __syncthreads();
+            // the smallest candidate value is t2 when fewer than `want`
+            // elements exceed it (constant rows, rows of -inf ties);
+            // otherwise a bitwise search over the values
+            uint32_t mn = 0xFFFFFFFFu;
 #pragma unroll
             for (int i = 0; i < VEC4; ++i)
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
+                    if (valid(i, q) && u32(comp(v[i], q)) >= t) mn = min(mn, u32(comp(v[i], q)));
+            mn = block_min_u32(mn, sc.wcnt);
+            auto count_above = [&](uint32_t c) {  // elements with value > c, block-wide
+                int cnt = 0;
+#pragma unroll
+                for (int i = 0; i < VEC4; ++i)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) cnt += valid(i, q) && u32(comp(v[i], q)) > c;
+                return block_sum_int(cnt, sc.wcnt);
+            };
+            uint32_t t2 = mn;
+            int gt = count_above(mn);
+            if (gt >= want) {
+                // the largest c with #(value >= c) >= want
+                t2 = 0;
+                for (int b = 31; b >= 0; --b) {
+                    const uint32_t c = t2 | (1u << b);
+                    // #(value >= c) = #(value > c - 1)
+                    if (count_above(c - 1) >= want) t2 = c;
+                }
+                gt = count_above(t2);
+            }
+            const int r = want - gt;  // ties at t2 to take, lowest columns first
+            // the slot holding the r-th tie in column order (slot i of the
+            // block covers columns [4 i kThreads, 4 (i + 1) kThreads) of the
+            // chunk), then the ties before each thread within it
+            int ties[VEC4];
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i) {
+                ties[i] = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) ties[i] += valid(i, q) && u32(comp(v[i], q)) == t2;
+            }
+            int before = 0, istar = VEC4;
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i) {
+                const int tot = block_sum_int(ties[i], sc.wcnt);
+                if (istar == VEC4) {
+                    if (before + tot >= r) istar = i;
+                    else before += tot;
+                }
+            }
+            int mine = 0;
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i)
+                if (i == istar) mine = ties[i];
+            const int ex = block_excl_scan(mine, sc.wcnt);
+            const int need = r - before;  // ties to take inside slot istar
+            if (tid == 0) sc.ncand = 0;
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < VEC4; ++i) {
+                int seen = 0;  // this thread's earlier ties in slot i
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
                     if (valid(i, q)) {
-                        const int64_t key = make_key(comp(v[i], q), col_of(i, q));
-                        if ((static_cast<uint64_t>(key) ^ 0x8000000000000000ull) >= kth) {
+                        const float x = comp(v[i], q);
+                        const uint32_t u = u32(x);
+                        bool take = u > t2;
+                        if (u == t2) {
+                            take = i < istar || (i == istar && ex + seen < need);
+                            ++seen;
+                        }
+                        if (take) {
                             const int pos = atomicAdd(&sc.ncand, 1);
-                            if (pos < kCandCap) cand[pos] = key;
+                            if (pos < kCandCap) cand[pos] = make_key(x, col_of(i, q));
                         }
                     }
+            }
             __syncthreads();
             ncand = sc.ncand;
         }
