@@ -1407,16 +1407,16 @@ bool rs::row_split_plan(int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds,
     pl.clusters = cluster_active(probs_dtype, pl.cluster_size);
     if (pl.clusters < 1) return false;
     pl.free_sms = sm_count() - pl.clusters * pl.cluster_size;
-    // rows per SM and time: the two passes about 4/5 of the cluster
-    // kernel's (measured on the step workload), so the tail gets that share
-    // of the free SMs' weight; the head is the rest of the list, whatever
-    // its length on the device
+    // rows per SM and time: the two passes about 10/13 of the cluster
+    // kernel's (the best of a sweep of this weight on the step workload), so
+    // the tail gets that share of the free SMs' weight; the head is the rest
+    // of the list, whatever its length on the device
     pl.head_num = 1;
     pl.head_den = 1;
     pl.tail = 0;
     if (pl.free_sms >= 8 && rows >= 8 * static_cast<int64_t>(pl.clusters)) {
-        pl.head_num = 5 * pl.clusters * pl.cluster_size;
-        pl.head_den = 4 * pl.free_sms + pl.head_num;
+        pl.head_num = 13 * pl.clusters * pl.cluster_size;
+        pl.head_den = 10 * pl.free_sms + pl.head_num;
         pl.tail = rows - rows * pl.head_num / pl.head_den;
     }
     *out = pl;
