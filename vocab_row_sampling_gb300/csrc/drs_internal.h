@@ -92,6 +92,10 @@ struct RowCall {
     const int32_t* map_count;
     float* out_m;
     float* out_logs;
+    // The caller has already written the row list, its header and every
+    // listed entry's RowTemp (split_prep_targets): the call starts at pass 1
+    // (the stash writes them with its own list).
+    bool prepared;
 };
 
 // The fault-injection test hook (drs_test_inject_fault): the pending code,
@@ -117,6 +121,18 @@ size_t split_workspace_bytes(int64_t rows, int64_t vocab, int32_t k, int32_t n_s
 int32_t split_max_k();
 int32_t split_max_seeds();
 drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream);
+
+// Where a row call's workspace holds what its first kernel writes, for a
+// caller that writes it itself (RowCall::prepared): the list header (word 0
+// the hard-row count, 0 before pass 1; word 1 the list's length), the row
+// list, and one RowTemp per listed entry (16 bytes: T, the quotient's 1/Te,
+// y and mode).
+struct SplitPrepTargets {
+    int32_t* header;
+    int32_t* list;
+    void* row_temps;
+};
+SplitPrepTargets split_prep_targets(void* workspace, int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds);
 
 // How split_rows shares a call's rows on the current device: the first
 // *head rows of its list go to the cluster kernel (*clusters clusters of

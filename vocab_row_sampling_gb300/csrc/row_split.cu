@@ -1395,6 +1395,13 @@ size_t split_workspace_bytes(int64_t rows, int64_t vocab, int32_t k, int32_t n_s
     return split_layout(rows, vocab, k, n_seeds).total;
 }
 
+SplitPrepTargets split_prep_targets(void* workspace, int64_t rows, int64_t vocab, int32_t k, int32_t n_seeds) {
+    const SplitLayout l = split_layout(rows, vocab, k, n_seeds);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    return SplitPrepTargets{reinterpret_cast<int32_t*>(ws + l.hard), reinterpret_cast<int32_t*>(ws + l.list1),
+                            ws + l.rt};
+}
+
 int32_t split_max_seeds() { return kMaxSeeds; }
 
 int32_t split_max_k() { return kSplitMaxK; }
@@ -1494,8 +1501,9 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     p.li_num = 1;
     p.li_den = 1;
     p.fault = take_injected_fault();
-    // the header of the hard-row list: its count and the two list lengths
-    if (cudaMemsetAsync(ws + l.hard, 0, 16, stream) != cudaSuccess) return DRS_ERR_CUDA;
+    // the header of the hard-row list: its count and the list's length
+    // (unless the caller wrote the list)
+    if (!c.prepared && cudaMemsetAsync(ws + l.hard, 0, 16, stream) != cudaSuccess) return DRS_ERR_CUDA;
     const size_t smem = kStages * kStageBytes;                       // pass 2
     const size_t smem1 = static_cast<size_t>(kStages) * kP1Cols * 4;  // pass 1
     const int64_t gp = (c.rows + 255) / 256;
@@ -1516,7 +1524,7 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     const int g2 = resident_grid(pass2, kSThreads, smem);
     if (g1 < 1 || g2 < 1) return DRS_ERR_CUDA;
     if (!mark(0)) return DRS_ERR_CUDA;
-    split_prep<<<static_cast<int>(gp), 256, 0, stream>>>(p);
+    if (!c.prepared) split_prep<<<static_cast<int>(gp), 256, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess || !mark(1)) return DRS_ERR_CUDA;
     // pass 1, merge, pass 2 and finish may launch while their predecessor
     // drains (each waits for it before its first access)

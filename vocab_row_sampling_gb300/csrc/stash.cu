@@ -11,22 +11,26 @@
 // logit s in logits mode; out_ranks holds one rank per stash row (below).
 //
 // Kernels, in stream order:
-//   list   one thread per (request, position): the stash rows to write, each
-//          with its logits row, temperature, output row and request;
+//   list   one CTA over the (request, position) pairs: the stash rows to
+//          write, each with its logits row, temperature, output row and
+//          request; for the two passes also their row list, its header and
+//          each entry's RowTemp (their own list kernel is skipped);
 //   top-k  k = max(num_topk, 1) keys per entry (the first is the argmax:
 //          keys order by value, then by lower column), with each entry's max
 //          and log-sum: for k <= 64 the two streaming passes over the listed
 //          rows (row_split.cu, with the list as a row map), then the exact
 //          kernel on the rows they leave; for larger k the exact kernel on
 //          every entry;
-//   write  one warp per entry: the row's columns, values from one IEEE
-//          division each.
+//   write  one warp per entry: the row's columns; a value is the top-k's
+//          logprob where the column is one of the top-k (the same
+//          arithmetic), else from one IEEE division.
 // Rows of requests that are not kept are never read.
 #include <cfloat>
 #include <climits>
 
 #include "drs_device.cuh"
 #include "drs_internal.h"
+#include "row_common.cuh"
 
 namespace drs {
 namespace {
@@ -57,6 +61,12 @@ struct StashParams {
     float* out_vals;
     int32_t* out_ranks;
     int32_t* list;
+    // the two passes' row list, header and RowTemps (null: the exact kernel
+    // takes every entry)
+    int32_t* pass_list;
+    int32_t* pass_header;
+    rs::RowTemp* pass_rt;
+    const float* top_lp;
     int32_t* map_row;
     float* map_temp;
     int64_t* map_out;
@@ -67,52 +77,94 @@ struct StashParams {
 };
 
 // The list of kept (request, position) pairs, in order: one CTA walks the
-// pairs 1024 at a time and places each kept pair after the kept pairs before
-// it (a block-wide count), so that the list, and how the row kernels divide
-// it among themselves, is the same on every run.
+// pairs kListThreads * kListPer at a time, a thread kListPer consecutive
+// ones (their loads in flight together), and places its kept pairs after
+// the kept pairs before them (a block-wide scan of the counts), so that the
+// list, and how the row kernels divide it among themselves, is the same on
+// every run.
 constexpr int kListThreads = 1024;
+constexpr int kListPer = 2;
 
 __global__ void __launch_bounds__(kListThreads) stash_list(const __grid_constant__ StashParams p) {
-    __shared__ int wcount[kListThreads / 32];
+    __shared__ int wpre[kListThreads / 32];
+    __shared__ int wtot;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int64_t n = p.requests * p.canvas_len;
+    const int n = static_cast<int>(p.requests * p.canvas_len);  // below 2^31 (checked on the host)
+    const int cl = static_cast<int>(p.canvas_len);
     int base = 0;
-    for (int64_t i0 = 0; i0 < n; i0 += kListThreads) {
-        const int64_t idx = i0 + threadIdx.x;
-        bool take = false;
-        int64_t j = 0, pos = 0, row = 0, out = 0;
-        if (idx < n) {
-            j = idx / p.canvas_len;
-            pos = idx - j * p.canvas_len;
-            row = static_cast<int64_t>(p.src[j]) * p.canvas_len + pos;
-            out = static_cast<int64_t>(p.slots[j]) * p.canvas_len + pos;
-            // rows outside the logits or the stash are skipped, never touched
-            take = p.keep[j] != 0 && pos < p.valid[j] && p.src[j] >= 0 && row < p.logits_rows &&
-                   p.slots[j] >= 0 && p.slots[j] < p.out_slots;
+    for (int i0 = 0; i0 < n; i0 += kListThreads * kListPer) {
+        bool take[kListPer];
+        int req[kListPer];
+        int64_t row[kListPer], out[kListPer];
+        int cnt = 0;
+#pragma unroll
+        for (int q = 0; q < kListPer; ++q) {
+            const int idx = i0 + threadIdx.x * kListPer + q;
+            take[q] = false;
+            req[q] = 0;
+            row[q] = out[q] = 0;
+            if (idx < n) {
+                const int j = idx / cl;
+                const int pos = idx - j * cl;
+                req[q] = j;
+                row[q] = static_cast<int64_t>(p.src[j]) * cl + pos;
+                out[q] = static_cast<int64_t>(p.slots[j]) * cl + pos;
+                // rows outside the logits or the stash are skipped, never touched
+                take[q] = p.keep[j] != 0 && pos < p.valid[j] && p.src[j] >= 0 && row[q] < p.logits_rows &&
+                          p.slots[j] >= 0 && p.slots[j] < p.out_slots;
+            }
+            cnt += take[q] ? 1 : 0;
         }
-        const uint32_t b = __ballot_sync(0xffffffffu, take);
-        if (lane == 0) wcount[warp] = __popc(b);
+        // the block's exclusive scan of the counts: within the warp, then
+        // over the warps' totals
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) wpre[warp] = incl;
         __syncthreads();
-        int before = base, total = 0;
-        for (int w = 0; w < kListThreads / 32; ++w) {
-            before += w < warp ? wcount[w] : 0;
-            total += wcount[w];
+        if (warp == 0) {
+            const int wv = wpre[lane];
+            int wi = wv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += y;
+            }
+            wpre[lane] = wi - wv;
+            if (lane == 31) wtot = wi;
         }
-        if (take) {
-            uint32_t lt;
-            asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
-            const int e = before + __popc(b & lt);
+        __syncthreads();
+        int e = base + wpre[warp] + (incl - cnt);
+#pragma unroll
+        for (int q = 0; q < kListPer; ++q) {
+            if (!take[q]) continue;
+            const float temp = p.temps[req[q]];
             p.list[kListOffset + e] = e;
-            p.map_row[e] = static_cast<int32_t>(row);
-            p.map_temp[e] = p.temps[j];
-            p.map_out[e] = out;
-            p.map_req[e] = static_cast<int32_t>(j);
+            p.map_row[e] = static_cast<int32_t>(row[q]);
+            p.map_temp[e] = temp;
+            p.map_out[e] = out[q];
+            p.map_req[e] = req[q];
+            if (p.pass_rt) {
+                const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
+                p.pass_rt[e] = rs::RowTemp{temp, sq.t, sq.y, sq.mode};
+                p.pass_list[e] = e;
+            }
+            ++e;
         }
-        base += total;
+        base += wtot;
         __syncthreads();
     }
-    if (threadIdx.x == 0) p.list[0] = base;
+    if (threadIdx.x == 0) {
+        p.list[0] = base;
+        if (p.pass_header) {
+            p.pass_header[0] = 0;  // the hard-row count
+            p.pass_header[rs::kCount1] = base;
+        }
+    }
 }
 
 constexpr int kWriteWarps = 8;
@@ -120,14 +172,20 @@ constexpr int kWriteWarps = 8;
 __global__ void __launch_bounds__(kWriteWarps * 32) stash_write(const __grid_constant__ StashParams p) {
     const int lane = threadIdx.x & 31;
     const int64_t e = static_cast<int64_t>(blockIdx.x) * kWriteWarps + (threadIdx.x >> 5);
-    if (e >= p.list[0]) return;
+    if (e >= p.requests * p.canvas_len) return;
+    // the entry's fields load beside the list's length (an entry past it
+    // holds stale values, never used)
+    const int count = p.list[0];
     const int j = p.map_req[e];
     const int64_t out = p.map_out[e];
-    const float* xr = p.logits + static_cast<int64_t>(p.map_row[e]) * p.row_stride;
+    const int64_t lrow = p.map_row[e];
     const float te = fmaxf(p.map_temp[e], kTempFloor);
     const float big_m = p.row_m[e];
     const float logs = p.row_logs[e];
     const int32_t* keys = p.top_ids + e * p.kq;
+    const float* lps = p.top_lp + e * p.kq;
+    if (e >= count) return;
+    const float* xr = p.logits + lrow * p.row_stride;
     // a request's list holds ids_stride ids at most: a larger count reads no
     // further (the columns past the list are padding)
     const int n_ids = p.token_ids && p.num_token_ids
@@ -135,15 +193,20 @@ __global__ void __launch_bounds__(kWriteWarps * 32) stash_write(const __grid_con
                           : 0;
     for (int c = lane; c < p.width; c += 32) {
         int id = 0;
+        int kidx = -1;  // the column's place in the top-k, if it has one
         bool has = true;
         if (c == 0) {
             id = keys[0];
+            kidx = 0;
         } else if (n_ids > 0) {
             has = c - 1 < n_ids;
             if (has) id = p.token_ids[static_cast<int64_t>(j) * p.ids_stride + (c - 1)];
         } else {
             has = c - 1 < p.num_topk;
-            if (has) id = keys[c - 1];
+            if (has) {
+                id = keys[c - 1];
+                kidx = c - 1;
+            }
         }
         float v;
         if (!has) {
@@ -151,6 +214,8 @@ __global__ void __launch_bounds__(kWriteWarps * 32) stash_write(const __grid_con
             v = -INFINITY;
         } else if (id < 0 || id >= p.vocab) {
             v = NAN;  // a token id outside the vocabulary
+        } else if (kidx >= 0 && !p.logits_mode) {
+            v = lps[kidx];  // (s - max) - log S of the same exact quotient s
         } else {
             const float s = __fdiv_rn(xr[id], te) + 0.0f;
             v = p.logits_mode ? s : (big_m == -INFINITY ? NAN : (s - big_m) - logs);
@@ -269,8 +334,17 @@ extern "C" drs_status drs_stash_converged_logprobs(
     float* row_m = reinterpret_cast<float*>(ws + l.row_m);
     float* row_logs = reinterpret_cast<float*>(ws + l.row_logs);
     p.top_ids = top_ids;
+    p.top_lp = top_lp;
     p.row_m = row_m;
     p.row_logs = row_logs;
+    if (kq <= split_max_k()) {
+        // the two passes' list, header and RowTemps come from the list kernel
+        const SplitPrepTargets tg =
+            split_prep_targets(ws + l.split, requests * canvas_len, vocab, kq, 1);
+        p.pass_list = tg.list;
+        p.pass_header = tg.header;
+        p.pass_rt = static_cast<rs::RowTemp*>(tg.row_temps);
+    }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int64_t R = requests * canvas_len;
@@ -299,6 +373,7 @@ extern "C" drs_status drs_stash_converged_logprobs(
         c.map_count = p.list;
         c.out_m = row_m;
         c.out_logs = row_logs;
+        c.prepared = true;
         const drs_status s = split_rows(c, ws + l.split, st);
         if (s != DRS_OK) return s;
         exact_list = reinterpret_cast<const int32_t*>(ws + l.split);
