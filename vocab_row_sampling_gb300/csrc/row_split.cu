@@ -235,7 +235,8 @@ __device__ __forceinline__ void read_tile(float4 (&v)[VEC], float4* stage, const
 // *map_count entries when k > 0. Otherwise (top-k-only calls) the rows of
 // kept slots: CTA 0 walks the rows 256 at a time and places each kept row
 // after the kept rows before it (a block-wide count); the other CTAs write
-// the RowTemps of their rows.
+// the RowTemps of their rows. The list header too: its length, and the
+// hard-row count set to 0 (the kernels after it add to it).
 __device__ __forceinline__ bool prep_row(const SplitParams& p, int64_t row) {
     if (row >= p.rows) return false;
     uint64_t slot = 0;
@@ -260,7 +261,10 @@ __global__ void __launch_bounds__(256) split_prep(const __grid_constant__ SplitP
     if (p.stats || p.map_row) {
         const int64_t n = p.map_row ? (p.k > 0 ? min(static_cast<int64_t>(*p.map_count), p.rows) : 0) : p.rows;
         if (prep_row(p, row) && row < n) p.list1[row] = static_cast<int32_t>(row);
-        if (row == 0) p.hard[kCount1] = static_cast<int32_t>(n);
+        if (row == 0) {
+            p.hard[0] = 0;  // the hard-row count, before pass 1
+            p.hard[kCount1] = static_cast<int32_t>(n);
+        }
         return;
     }
     if (blockIdx.x != 0) {
@@ -289,7 +293,10 @@ __global__ void __launch_bounds__(256) split_prep(const __grid_constant__ SplitP
         base += total;
         __syncthreads();
     }
-    if (threadIdx.x == 0) p.hard[kCount1] = base;
+    if (threadIdx.x == 0) {
+        p.hard[0] = 0;  // the hard-row count, before pass 1
+        p.hard[kCount1] = base;
+    }
 }
 
 // ============================================================== pass 1
@@ -1501,9 +1508,6 @@ drs_status split_rows(const RowCall& c, void* workspace, cudaStream_t stream) {
     p.li_num = 1;
     p.li_den = 1;
     p.fault = take_injected_fault();
-    // the header of the hard-row list: its count and the list's length
-    // (unless the caller wrote the list)
-    if (!c.prepared && cudaMemsetAsync(ws + l.hard, 0, 16, stream) != cudaSuccess) return DRS_ERR_CUDA;
     const size_t smem = kStages * kStageBytes;                       // pass 2
     const size_t smem1 = static_cast<size_t>(kStages) * kP1Cols * 4;  // pass 1
     const int64_t gp = (c.rows + 255) / 256;
