@@ -13,17 +13,18 @@
 // Kernels, in stream order:
 //   list   one CTA over the (request, position) pairs: the stash rows to
 //          write, each with its logits row, temperature, output row and
-//          request; for the two passes also their row list, its header and
+//          request; for the row kernels also their row list, its header and
 //          each entry's RowTemp (their own list kernel is skipped);
 //   top-k  k = max(num_topk, 1) keys per entry (the first is the argmax:
 //          keys order by value, then by lower column), with each entry's max
-//          and log-sum: for k <= 64 the two streaming passes over the listed
-//          rows (row_split.cu, with the list as a row map), then the exact
-//          kernel on the rows they leave; for larger k the exact kernel on
+//          and log-sum: for k <= 64 the one-read top-k of row_split.cu over
+//          the listed rows (pass 1, the merge's threshold, the gather of the
+//          warps that reach it; the list as a row map), then the exact
+//          kernel on the rows it leaves; for larger k the exact kernel on
 //          every entry;
-//   write  one warp per entry: the row's columns; a value is the top-k's
-//          logprob where the column is one of the top-k (the same
-//          arithmetic), else from one IEEE division.
+//   write  one warp per entry: the row's columns; in logprobs mode a top-k
+//          column's value is the top-k's own logprob (the same arithmetic),
+//          any other value one IEEE division.
 // Rows of requests that are not kept are never read.
 #include <cfloat>
 #include <climits>
@@ -338,7 +339,7 @@ extern "C" drs_status drs_stash_converged_logprobs(
     p.row_m = row_m;
     p.row_logs = row_logs;
     if (kq <= split_max_k()) {
-        // the two passes' list, header and RowTemps come from the list kernel
+        // the row kernels' list, header and RowTemps come from the list kernel
         const SplitPrepTargets tg =
             split_prep_targets(ws + l.split, requests * canvas_len, vocab, kq, 1);
         p.pass_list = tg.list;
@@ -353,9 +354,9 @@ extern "C" drs_status drs_stash_converged_logprobs(
     const ExactTopkMap map{p.map_row, p.map_temp, row_m, row_logs};
     const int32_t* exact_list = p.list;
     if (kq <= split_max_k()) {
-        // the two passes over the listed rows; the rows they leave (no
+        // the one-read top-k over the listed rows; the rows it leaves (no
         // threshold, too many candidates) are on the hard-row list at the
-        // start of their workspace
+        // start of its workspace
         RowCall c{};
         c.logits = logits;
         c.rows = R;
