@@ -62,7 +62,7 @@ struct StashParams {
     float* out_vals;
     int32_t* out_ranks;
     int32_t* list;
-    // the two passes' row list, header and RowTemps (null: the exact kernel
+    // the row kernels' row list, header and RowTemps (null: the exact kernel
     // takes every entry)
     int32_t* pass_list;
     int32_t* pass_header;
