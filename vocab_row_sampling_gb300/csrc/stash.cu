@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kListThreads) stash_list(const __grid_constant
     for (int i0 = 0; i0 < n; i0 += kListThreads * kListPer) {
         bool take[kListPer];
         int req[kListPer];
+        float temp[kListPer];
         int64_t row[kListPer], out[kListPer];
         int cnt = 0;
 #pragma unroll
@@ -104,11 +105,13 @@ __global__ void __launch_bounds__(kListThreads) stash_list(const __grid_constant
             const int idx = i0 + threadIdx.x * kListPer + q;
             take[q] = false;
             req[q] = 0;
+            temp[q] = 0.0f;
             row[q] = out[q] = 0;
             if (idx < n) {
                 const int j = idx / cl;
                 const int pos = idx - j * cl;
                 req[q] = j;
+                temp[q] = p.temps[j];
                 row[q] = static_cast<int64_t>(p.src[j]) * cl + pos;
                 out[q] = static_cast<int64_t>(p.slots[j]) * cl + pos;
                 // rows outside the logits or the stash are skipped, never touched
@@ -143,15 +146,14 @@ __global__ void __launch_bounds__(kListThreads) stash_list(const __grid_constant
 #pragma unroll
         for (int q = 0; q < kListPer; ++q) {
             if (!take[q]) continue;
-            const float temp = p.temps[req[q]];
             p.list[kListOffset + e] = e;
             p.map_row[e] = static_cast<int32_t>(row[q]);
-            p.map_temp[e] = temp;
+            p.map_temp[e] = temp[q];
             p.map_out[e] = out[q];
             p.map_req[e] = req[q];
             if (p.pass_rt) {
-                const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp, kTempFloor));
-                p.pass_rt[e] = rs::RowTemp{temp, sq.t, sq.y, sq.mode};
+                const ScaledQuotient sq = ScaledQuotient::of(fmaxf(temp[q], kTempFloor));
+                p.pass_rt[e] = rs::RowTemp{temp[q], sq.t, sq.y, sq.mode};
                 p.pass_list[e] = e;
             }
             ++e;
@@ -175,12 +177,15 @@ __global__ void __launch_bounds__(kWriteWarps * 32) stash_write(const __grid_con
     const int64_t e = static_cast<int64_t>(blockIdx.x) * kWriteWarps + (threadIdx.x >> 5);
     if (e >= p.requests * p.canvas_len) return;
     // the entry's fields load beside the list's length (an entry past it
-    // holds stale values, never used)
+    // holds stale values, never used); the list kernel wrote them, so they
+    // load while the exact kernel before this one still runs (a
+    // programmatic dependent launch); its results only after it completes
     const int count = p.list[0];
     const int j = p.map_req[e];
     const int64_t out = p.map_out[e];
     const int64_t lrow = p.map_row[e];
     const float te = fmaxf(p.map_temp[e], kTempFloor);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float big_m = p.row_m[e];
     const float logs = p.row_logs[e];
     const int32_t* keys = p.top_ids + e * p.kq;
@@ -382,6 +387,14 @@ extern "C" drs_status drs_stash_converged_logprobs(
     const drs_status s = exact_topk(logits, R, vocab, row_stride, 0, nullptr, 1, nullptr, exact_list,
                                     kq, top_ids, top_lp, ws + l.exact, st, &map);
     if (s != DRS_OK) return s;
-    stash_write<<<static_cast<int>((R + kWriteWarps - 1) / kWriteWarps), kWriteWarps * 32, 0, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? DRS_OK : DRS_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((R + kWriteWarps - 1) / kWriteWarps));
+    cfg.blockDim = dim3(kWriteWarps * 32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, stash_write, p) == cudaSuccess ? DRS_OK : DRS_ERR_CUDA;
 }

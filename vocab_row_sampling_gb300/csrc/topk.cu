@@ -162,6 +162,9 @@ __device__ __forceinline__ int block_excl_scan(int v, int* red) {
 template <int VEC4>
 __global__ void __launch_bounds__(kThreads, 1)
     topk_kernel(const __grid_constant__ TopkParams p) {
+    // a programmatic dependent launched after this kernel (the stash's
+    // write) may start now: it waits for this grid before reading its results
+    asm volatile("griddepcontrol.launch_dependents;");
     extern __shared__ __align__(128) unsigned char smem[];
     TopkScratch& sc = *reinterpret_cast<TopkScratch*>(smem + p.nstage * p.stage_bytes);
     int64_t* cand = reinterpret_cast<int64_t*>(
