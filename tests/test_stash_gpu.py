@@ -157,3 +157,29 @@ def test_stash_skips_requests_outside_the_buffers():
     assert np.all(g_ids[~written] == SENT_ID) and np.all(g_ranks[~written] == SENT_R)
     assert np.array_equal(g_ranks[written], r_ranks[written])
     check_topk(g_ids[written], g_vals[written], r_ids[written], r_vals[written], "skipped requests")
+
+
+@pytest.mark.parametrize("vocab", [777, 70001])
+def test_topk_values_equal_the_division_path(vocab):
+    """In logprobs mode a top-k column takes the top-k's own logprob, a
+    token-id column one IEEE division and (s - max) - log S: with one
+    position per request and each request's top-k ids passed back as its
+    token ids, both paths must give the same bits (the argmax column too)."""
+    rng = np.random.default_rng(7)
+    m, k = 24, 8
+    x = (rng.standard_normal((m, vocab)) * 3).astype(np.float32)
+    x[2] = np.round(x[2])                      # ties
+    x[4][rng.random(vocab) < 0.999] = -np.inf  # fewer finite values than k
+    x[5] = -np.inf                             # all -inf
+    src = np.arange(m, dtype=np.int32)
+    slots = np.arange(m, dtype=np.int32)
+    keep = np.ones(m, np.uint8)
+    valid = np.ones(m, np.int32)
+    temps = np.array([0.7, 1.0, 1.3, 1e-3, 0.0, 2.0] * (m // 6), np.float32)
+    ids1, vals1, _ = _run(x, 1, src, slots, keep, valid, temps, k, None, None, m, k + 1, 0)
+    tok = np.ascontiguousarray(ids1[:, 0, 1:]).astype(np.int32)
+    nti = np.full(m, k, np.int32)
+    ids2, vals2, _ = _run(x, 1, src, slots, keep, valid, temps, k, nti, tok, m, k + 1, 0)
+    assert np.array_equal(ids1, ids2)
+    same = (vals1.view(np.uint32) == vals2.view(np.uint32)) | (np.isnan(vals1) & np.isnan(vals2))
+    assert same.all(), f"values differ at {np.argwhere(~same)[:4]}"
