@@ -298,9 +298,16 @@ def _run_ours(args, world, rank, local):
         # the steps back to back: events only around all of them (an event
         # between two calls holds the next one back)
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        _barrier(world)
-        torch.cuda.synchronize()
         with ClockSampler(torch.cuda.current_device()) as clk:
+            # the warm-up steps again once the sampler runs: its start-up
+            # pause leaves the GPU idle, and a GPU that has idled (even for
+            # the synchronize below) runs its next milliseconds of work about
+            # 20% slower, which the default 100 steps amortise
+            for _ in range(args.warmup):
+                step()
+            torch.cuda.synchronize()
+            _barrier(world)
+            torch.cuda.synchronize()
             start.record(stream)
             for _ in range(args.steps):
                 step()
@@ -427,7 +434,7 @@ def _launches_per_call(plan, k):
     return n + (1 if k > 0 else 0)
 
 
-def _separate_calls(drs, w, logits, temps, temps_all, keep, out, stream, row0, peak, n=10):
+def _separate_calls(drs, w, logits, temps, temps_all, keep, out, stream, row0, peak, n=30):
     """drs_row_stats, drs_topk_logprobs and the stash of the converged
     requests, each timed briefly (context for the fused call)."""
     rows, V, k, cl = w["rows"], w["vocab"], w["k"], w["canvas_len"]
@@ -781,7 +788,7 @@ def _run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
