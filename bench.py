@@ -379,7 +379,7 @@ def _run_ours(args, world, rank, local):
     # the same call with the two streaming passes alone (the previous design)
     drs.drs_test_two_pass(True)
     try:
-        tp_ms = _time_calls(call, stream, max(3, min(args.steps, 10)))
+        tp_ms = _time_calls(call, stream, max(3, min(args.steps, 30)))
     finally:
         drs.drs_test_two_pass(args.two_pass)
     kernels["two_passes_alone"] = {"avg_ms": round(tp_ms, 4),
@@ -470,7 +470,7 @@ def _separate_calls(drs, w, logits, temps, temps_all, keep, out, stream, row0, p
                                                  "read of each kept row"}}
 
 
-def _workload_case(drs, name, args, peak, sample_rows=6, steps=5):
+def _workload_case(drs, name, args, peak, sample_rows=6, steps=20):
     """One of the task's other workloads: its call timed, rows/s, GB/s and
     fraction of peak over one read and one write; the oracle's rows/s on a
     few of its rows on the host; those rows compared with the GPU's."""
