@@ -181,8 +181,8 @@ drs_status drs_row_stats_seeds(const float *logits, int64_t rows, int64_t vocab,
 size_t drs_row_stats_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k);
 
 /*
- * drs_row_stats and the top-k logprobs of the rows of converged slots in
- * the same passes over the logits (stash_converged_logprobs /
+ * drs_row_stats and the top-k logprobs of the rows of converged slots from
+ * the same read of the logits (stash_converged_logprobs /
  * _lp_topk_kernel on the page above, whose stash reads the kept rows again
  * in a kernel of its own). Every argument of drs_row_stats has its meaning
  * there; in addition:
@@ -200,9 +200,11 @@ size_t drs_row_stats_topk_workspace_bytes(int64_t rows, int64_t vocab, int32_t k
  *               of those columns (NaN for a row that is -inf everywhere).
  *   workspace   drs_row_stats_topk_workspace_bytes(rows, vocab, k) bytes.
  *
- * For k <= 64 the top-k candidates come out of the row statistics' own two
- * passes over the logits (the threshold from the first, the candidates in
- * the second); rows whose candidates overflow the fixed lists (many equal
+ * For k <= 64 the top-k candidates come out of the row statistics' own read
+ * of the logits: in the cluster kernel the threshold from the CTAs' parts
+ * (distributed shared memory) and the candidates from the row held in shared
+ * memory; in the two passes the threshold from the first and the candidates
+ * in the second. Rows whose candidates overflow the fixed lists (many equal
  * values) or that have no threshold are finished by the exact top-k kernel
  * on the same stream, which reads only those rows. For k > 64 the row
  * statistics and the exact top-k kernel run one after the other.
